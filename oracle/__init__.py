@@ -1,0 +1,120 @@
+"""Attention forward ORACLE -- test infrastructure only.
+
+A plain float64 CPU statement of the attention forward (``attention_oracle.c``,
+which carries the citations).  Only ``tests/``, ``__graft_entry__.smoke()`` and
+``bench.py``'s CPU-baseline / reference leg may import this package; the
+product library never does, and the two share no code.  Inputs come from the
+``seeded_inputs`` module as uint16 bit patterns.
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` against closed
+forms, invariants, library routines (numpy/scipy) and an mpmath brute force.
+"""
+from __future__ import annotations
+
+import ctypes
+import hashlib
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "attention_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_lock = threading.Lock()
+_libs: dict[str, ctypes.CDLL] = {}
+
+DTYPES = {"fp16": 0, "bf16": 1}
+
+
+def host_threads() -> int:
+    """Host cores this process may run on (sched_getaffinity)."""
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:  # pragma: no cover
+        return max(1, os.cpu_count() or 1)
+
+
+def build(source: str | None = None, tag: str = "") -> str:
+    """Compile the oracle (or a variant of its source text) with gcc -O2, no fast-math."""
+    text = open(SOURCE).read() if source is None else source
+    digest = hashlib.sha1(text.encode()).hexdigest()[:12]
+    out = os.path.join(_BUILD, f"liboracle{tag}-{digest}.so")
+    if not os.path.exists(out):
+        os.makedirs(_BUILD, exist_ok=True)
+        src_path = out[:-3] + f".{os.getpid()}.c"
+        with open(src_path, "w") as f:
+            f.write(text)
+        tmp = out + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", "-O2", "-std=c11", "-D_GNU_SOURCE", "-fPIC", "-shared", "-pthread",
+                        "-fno-fast-math", "-ffp-contract=off", "-o", tmp, src_path, "-lm"], check=True)
+        os.replace(tmp, out)
+        os.remove(src_path)
+    return out
+
+
+def load(source: str | None = None, tag: str = "") -> ctypes.CDLL:
+    path = build(source, tag)
+    with _lock:
+        lib = _libs.get(path)
+        if lib is None:
+            lib = ctypes.CDLL(path)
+            lib.oracle_attention_fwd.restype = ctypes.c_int
+            lib.oracle_attention_fwd.argtypes = [
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_double, ctypes.c_int, ctypes.c_void_p, ctypes.c_int64,
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+            lib.oracle_decode.restype = ctypes.c_double
+            lib.oracle_decode.argtypes = [ctypes.c_uint16, ctypes.c_int]
+            _libs[path] = lib
+        return lib
+
+
+def decode(bits: np.ndarray, dtype: str, lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """The oracle's own exact fp16/bf16 -> float64 decoding, element by element."""
+    lib = lib or load()
+    flat = np.asarray(bits, dtype=np.uint16).ravel()
+    code = DTYPES[dtype]
+    return np.fromiter((lib.oracle_decode(int(b), code) for b in flat), dtype=np.float64,
+                       count=flat.size).reshape(np.shape(bits))
+
+
+def attention_fwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, dtype: str, scale: float, causal: bool,
+                  rows: np.ndarray | None = None, nthreads: int | None = None,
+                  lib: ctypes.CDLL | None = None):
+    """Attention forward in float64.
+
+    q: (Z, Hq, Nq, D), k/v: (Z, Hkv, Nkv, D) uint16 bit arrays (fp16 or bf16).
+    rows: optional flat row ids ``(z*Hq + hq)*Nq + i``; by default every row.
+    Returns (o, lse): o is (Z, Hq, Nq, D) / lse (Z, Hq, Nq) for all rows, or
+    (R, D) / (R,) for the given rows, all float64.
+    """
+    lib = lib or load()
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    k = np.ascontiguousarray(k, dtype=np.uint16)
+    v = np.ascontiguousarray(v, dtype=np.uint16)
+    Z, Hq, Nq, D = q.shape
+    Zk, Hkv, Nkv, Dk = k.shape
+    if v.shape != k.shape or Zk != Z or Dk != D:
+        raise ValueError(f"shape mismatch q{q.shape} k{k.shape} v{v.shape}")
+    if rows is None:
+        nrows = Z * Hq * Nq
+        rows_arr = None
+    else:
+        rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
+        nrows = rows_arr.size
+    o = np.empty((nrows, D), dtype=np.float64)
+    lse = np.empty(nrows, dtype=np.float64)
+    rc = lib.oracle_attention_fwd(
+        q.ctypes.data, k.ctypes.data, v.ctypes.data, DTYPES[dtype], Z, Hq, Hkv, Nq, Nkv, D,
+        float(scale), int(bool(causal)), None if rows_arr is None else rows_arr.ctypes.data, nrows,
+        o.ctypes.data if nrows else None, lse.ctypes.data if nrows else None, nthreads or host_threads())
+    if rc == -1:
+        raise ValueError("oracle_attention_fwd: invalid arguments")
+    if rc != 0:
+        raise MemoryError("oracle_attention_fwd: out of memory")
+    if rows is None:
+        return o.reshape(Z, Hq, Nq, D), lse.reshape(Z, Hq, Nq)
+    return o, lse

@@ -1,0 +1,176 @@
+/*
+ * Attention forward ORACLE -- test infrastructure, not part of the product.
+ *
+ * A plain, slow, float64 CPU statement of what the fused attention forward
+ * computes.  Only the tests, the smoke check and the benchmark's CPU-baseline
+ * leg may load it.  It shares no code with the CUDA library.
+ *
+ * What it computes is the standard attention definition (page "把 FlashAttention
+ * 搬上昇腾：Triton-Ascend CV Pipeline 优化实战", section 一: S = Q Kᵀ · scale,
+ * P = softmax(S), O = P V), with the extensions that the page "Write Triton
+ * Attention Kernel" fixes:
+ *   - GQA/MQA: query head hq reads key/value head hq / (Hq / Hkv)
+ *     ("Required reasoning process", step 1);
+ *   - causal masking keeps key j for query i iff i >= j
+ *     (step 5c, the top-left convention for Nq != Nkv);
+ *   - the saved log-sum-exp is lse = m + log(l), i.e. the natural log of
+ *     sum_j exp(s_ij) over the kept keys (step 8).
+ * For each requested row (z, hq, i), in float64 on the exactly upcast
+ * fp16/bf16 inputs:
+ *   1. s_j   = scale * sum_d Q[z,hq,i,d] K[z,hk,j,d]  for every kept key j
+ *   2. M     = max_j s_j,   L = sum_j exp(s_j - M)
+ *   3. O[d]  = sum_j (exp(s_j - M) / L) V[z,hk,j,d]
+ *   4. lse   = M + ln L
+ * The whole row of S is materialised; nothing is tiled, fused or reordered.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---- exact decoding of the 16-bit storage formats -------------------------- */
+
+/* IEEE binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+static double decode_binary16(uint16_t h) {
+    int sign = (h >> 15) & 1, e = (h >> 10) & 0x1f, f = h & 0x3ff;
+    double mag;
+    if (e == 0) mag = ldexp((double)f, -24);                 /* zero / subnormal */
+    else if (e == 31) mag = f ? NAN : INFINITY;
+    else mag = ldexp((double)(1024 + f), e - 25);           /* 1.f * 2^(e-15) */
+    return sign ? -mag : mag;
+}
+
+/* bfloat16: 1 sign bit, 8 exponent bits (bias 127), 7 fraction bits. */
+static double decode_bfloat16(uint16_t h) {
+    int sign = (h >> 15) & 1, e = (h >> 7) & 0xff, f = h & 0x7f;
+    double mag;
+    if (e == 0) mag = ldexp((double)f, -133);                /* zero / subnormal */
+    else if (e == 255) mag = f ? NAN : INFINITY;
+    else mag = ldexp((double)(128 + f), e - 134);           /* 1.f * 2^(e-127) */
+    return sign ? -mag : mag;
+}
+
+/* Exposed so the tests can check the decoder bit pattern by bit pattern. */
+double oracle_decode(uint16_t bits, int dtype) {
+    return dtype == 0 ? decode_binary16(bits) : decode_bfloat16(bits);
+}
+
+/* ---- one row of the definition --------------------------------------------- */
+
+typedef struct {
+    const uint16_t* q;   /* (Z, Hq, Nq, D) bits, contiguous */
+    const double* k;     /* (Z, Hkv, Nkv, D) upcast, contiguous */
+    const double* v;
+    const double* table; /* 65536-entry decode table for q */
+    int Z, Hq, Hkv, Nq, Nkv, D;
+    double scale;
+    int causal;
+    const int64_t* rows; /* flat row ids (z*Hq + hq)*Nq + i, or NULL for all rows */
+    int64_t nrows;
+    double* o;           /* (nrows, D) */
+    double* lse;         /* (nrows) */
+    int64_t begin, end;  /* this worker's slice of [0, nrows) */
+    int status;
+} oracle_job;
+
+static void attention_row(const oracle_job* J, int64_t r, double* qrow, double* s, double* out, double* out_lse) {
+    const int D = J->D;
+    const int64_t i = r % J->Nq;
+    const int64_t zh = r / J->Nq;
+    const int hq = (int)(zh % J->Hq), z = (int)(zh / J->Hq);
+    const int hk = hq / (J->Hq / J->Hkv);
+    const double* kh = J->k + ((int64_t)z * J->Hkv + hk) * J->Nkv * D;
+    const double* vh = J->v + ((int64_t)z * J->Hkv + hk) * J->Nkv * D;
+    const uint16_t* qbits = J->q + r * D;
+    for (int d = 0; d < D; ++d) qrow[d] = J->table[qbits[d]];
+
+    /* kept keys: all of them, or j <= i under the causal mask */
+    int64_t nkept = J->Nkv;
+    if (J->causal && i + 1 < nkept) nkept = i + 1;
+
+    /* 1. scores */
+    for (int64_t j = 0; j < nkept; ++j) {
+        double acc = 0.0;
+        for (int d = 0; d < D; ++d) acc += qrow[d] * kh[j * D + d];
+        s[j] = J->scale * acc;
+    }
+    /* 2. row maximum and normaliser */
+    double M = -INFINITY;
+    for (int64_t j = 0; j < nkept; ++j) M = s[j] > M ? s[j] : M;
+    double L = 0.0;
+    for (int64_t j = 0; j < nkept; ++j) L += exp(s[j] - M);
+    /* 3. probabilities times values */
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    for (int64_t j = 0; j < nkept; ++j) {
+        const double p = exp(s[j] - M) / L;
+        for (int d = 0; d < D; ++d) out[d] += p * vh[j * D + d];
+    }
+    /* 4. log-sum-exp of the scaled scores */
+    *out_lse = M + log(L);
+}
+
+static void* oracle_worker(void* arg) {
+    oracle_job* J = (oracle_job*)arg;
+    double* qrow = (double*)malloc(sizeof(double) * (size_t)J->D);
+    double* s = (double*)malloc(sizeof(double) * (size_t)J->Nkv);
+    if (!qrow || !s) { J->status = -2; free(qrow); free(s); return NULL; }
+    for (int64_t t = J->begin; t < J->end; ++t) {
+        const int64_t r = J->rows ? J->rows[t] : t;
+        attention_row(J, r, qrow, s, J->o + t * J->D, J->lse + t);
+    }
+    free(qrow);
+    free(s);
+    return NULL;
+}
+
+/*
+ * Attention forward for the rows `rows[0..nrows)` (flat ids (z*Hq + hq)*Nq + i),
+ * or for every row in (z, hq, i) order when rows == NULL (then nrows must be
+ * Z*Hq*Nq).  q/k/v are contiguous BNSD bit arrays of dtype 0 (fp16) or 1 (bf16).
+ * Writes o[nrows*D] and lse[nrows] in float64.
+ * Returns 0, -1 for invalid arguments, -2 when memory runs out.
+ */
+int oracle_attention_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, int dtype,
+                         int Z, int Hq, int Hkv, int Nq, int Nkv, int D, double scale, int causal,
+                         const int64_t* rows, int64_t nrows, double* o, double* lse, int nthreads) {
+    if (dtype < 0 || dtype > 1 || Z < 0 || Hq < 1 || Hkv < 1 || Nq < 0 || Nkv < 1 || D < 1) return -1;
+    if (Hq % Hkv != 0 || !isfinite(scale) || nrows < 0) return -1;
+    const int64_t total = (int64_t)Z * Hq * Nq;
+    if (!rows && nrows != total) return -1;
+    for (int64_t t = 0; rows && t < nrows; ++t)
+        if (rows[t] < 0 || rows[t] >= total) return -1;
+    if (nrows == 0) return 0;
+
+    double* table = (double*)malloc(sizeof(double) * 65536);
+    const int64_t nk = (int64_t)Z * Hkv * Nkv * D;
+    double* kd = (double*)malloc(sizeof(double) * (size_t)nk);
+    double* vd = (double*)malloc(sizeof(double) * (size_t)nk);
+    if (!table || !kd || !vd) { free(table); free(kd); free(vd); return -2; }
+    for (int b = 0; b < 65536; ++b) table[b] = oracle_decode((uint16_t)b, dtype);
+    for (int64_t x = 0; x < nk; ++x) { kd[x] = table[k[x]]; vd[x] = table[v[x]]; }
+
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 512) nthreads = 512;
+    if (nthreads > nrows) nthreads = (int)nrows;
+    oracle_job* jobs = (oracle_job*)calloc((size_t)nthreads, sizeof(oracle_job));
+    pthread_t* tid = (pthread_t*)calloc((size_t)nthreads, sizeof(pthread_t));
+    int* created = (int*)calloc((size_t)nthreads, sizeof(int));
+    if (!jobs || !tid || !created) { free(jobs); free(tid); free(created); free(table); free(kd); free(vd); return -2; }
+    const int64_t chunk = (nrows + nthreads - 1) / nthreads;
+    for (int t = 0; t < nthreads; ++t) {
+        oracle_job* J = &jobs[t];
+        *J = (oracle_job){q, kd, vd, table, Z, Hq, Hkv, Nq, Nkv, D, scale, causal, rows, nrows, o, lse,
+                          (int64_t)t * chunk, (int64_t)t * chunk + chunk < nrows ? (int64_t)t * chunk + chunk : nrows, 0};
+        if (J->begin >= J->end) continue;
+        if (nthreads > 1 && pthread_create(&tid[t], NULL, oracle_worker, J) == 0) created[t] = 1;
+        else oracle_worker(J);
+    }
+    int status = 0;
+    for (int t = 0; t < nthreads; ++t) {
+        if (created[t]) pthread_join(tid[t], NULL);
+        if (jobs[t].status) status = jobs[t].status;
+    }
+    free(jobs); free(tid); free(created); free(table); free(kd); free(vd);
+    return status;
+}

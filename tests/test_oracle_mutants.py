@@ -1,0 +1,65 @@
+"""The oracle's pins must catch plausible mistakes in the oracle itself.
+
+Each mutant is a copy of the oracle's C source with one planted mistake (a
+dropped term, a wrong sign or index, a transposed operand), compiled on the
+CPU.  The test swaps it in for the real oracle and runs the pins of
+test_oracle_pins.py; at least one pin must fail for every mutant.
+"""
+import pytest
+
+import oracle
+import test_oracle_pins as pins
+
+MUTANTS = {
+    "dropped scale": ("s[j] = J->scale * acc;", "s[j] = acc;"),
+    "causal off by one": ("if (J->causal && i + 1 < nkept) nkept = i + 1;",
+                          "if (J->causal && i + 2 < nkept) nkept = i + 2;"),
+    "gqa head modulo": ("const int hk = hq / (J->Hq / J->Hkv);", "const int hk = hq % J->Hkv;"),
+    "K transposed": ("acc += qrow[d] * kh[j * D + d];", "acc += qrow[d] * kh[(int64_t)d * J->Nkv + j];"),
+    "lse drops max": ("*out_lse = M + log(L);", "*out_lse = log(L);"),
+    "lse base 2": ("*out_lse = M + log(L);", "*out_lse = M + log2(L);"),
+    "no normalisation": ("const double p = exp(s[j] - M) / L;", "const double p = exp(s[j] - M);"),
+    "unshifted normaliser": ("L += exp(s[j] - M);", "L += exp(s[j]);"),
+    "no max shift": ("M = s[j] > M ? s[j] : M;", "M = 0.0;"),
+    "value row shifted": ("out[d] += p * vh[j * D + d];", "out[d] += p * vh[((j + 1) % J->Nkv) * D + d];"),
+    "query ignores head": ("const uint16_t* qbits = J->q + r * D;", "const uint16_t* qbits = J->q + i * D;"),
+    "fp16 exponent bias": ("mag = ldexp((double)(1024 + f), e - 25);", "mag = ldexp((double)(1024 + f), e - 24);"),
+    "bf16 fraction width": ("mag = ldexp((double)(128 + f), e - 134);", "mag = ldexp((double)(128 + f), e - 133);"),
+    "sign of score": ("s[j] = J->scale * acc;", "s[j] = -J->scale * acc;"),
+}
+
+PIN_CALLS = [
+    ("decode fp16", lambda: pins.test_decode_every_bit_pattern("fp16")),
+    ("decode bf16", lambda: pins.test_decode_every_bit_pattern("bf16")),
+    ("single key", lambda: pins.test_single_key_gives_v0("fp16", False)),
+    ("identical keys", lambda: pins.test_identical_keys_give_mean_v("bf16")),
+    ("causal row 0", lambda: pins.test_causal_row0_is_v0("fp16")),
+    ("probabilities", lambda: pins.test_identity_values_expose_probabilities(True)),
+    ("mpmath", lambda: pins.test_mpmath_bruteforce("fp16", 0.25, False)),
+    ("mpmath large", lambda: pins.test_mpmath_bruteforce("fp16", 200.0, False)),
+    ("mpmath causal", lambda: pins.test_mpmath_bruteforce("bf16", 0.25, True)),
+    ("scipy", lambda: pins.test_matches_scipy("fp16", True, (2, 4, 2, 37, 53, 32))),
+    ("gqa", pins.test_gqa_equals_mha_on_repeated_kv),
+    ("prefix", pins.test_causal_row_is_prefix_attention),
+]
+
+
+def test_every_mutation_is_applicable():
+    src = open(oracle.SOURCE).read()
+    for name, (old, _new) in MUTANTS.items():
+        assert src.count(old) == 1, name
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, monkeypatch):
+    old, new = MUTANTS[name]
+    src = open(oracle.SOURCE).read().replace(old, new)
+    lib = oracle.load(src, tag="-mutant")
+    monkeypatch.setattr(oracle, "load", lambda *a, **k: lib)
+    caught = []
+    for pin_name, call in PIN_CALLS:
+        try:
+            call()
+        except (AssertionError, ValueError, FloatingPointError):
+            caught.append(pin_name)
+    assert caught, f"no pin caught the mutant {name!r}"

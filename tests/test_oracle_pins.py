@@ -1,0 +1,243 @@
+"""Pins for the CPU oracle: closed forms, invariants, library routines and a brute force.
+
+None of these re-types the oracle's own formula: each compares it with something
+the pages or the mathematics fix independently of it.
+  - decoding: every fp16/bf16 bit pattern against numpy / the fp32 bit layout;
+  - one key: O = V[0], lse = s_00 (closed form);
+  - identical keys or scale = 0: O = mean(V), lse = s + ln(Nkv) (closed form);
+  - causal row 0: O = V[0]; causal row i = non-causal attention over keys 0..i;
+  - V = identity exposes P itself: rows sum to 1, P >= 0, P_ij = 0 above the
+    diagonal under the causal mask;
+  - an mpmath brute force at 60 digits (no max shift, exact scores);
+  - numpy matmul + scipy.special.softmax/logsumexp on small shapes;
+  - GQA equals MHA on K/V repeated per group; key permutation invariance.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import seeded_inputs as si
+
+mpmath = pytest.importorskip("mpmath")
+
+
+def _bits(values, dtype):
+    return si.round_bits(np.asarray(values, dtype=np.float64), dtype)
+
+
+def _np_decode(bits, dtype):
+    """Reference decoding through numpy's binary16 and the fp32 bit layout of bf16."""
+    bits = np.asarray(bits, dtype=np.uint16)
+    if dtype == "fp16":
+        return bits.view(np.float16).astype(np.float64)
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+# ---------------------------------------------------------------- decoding ----
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_decode_every_bit_pattern(dtype):
+    allbits = np.arange(65536, dtype=np.uint16)
+    got = oracle.decode(allbits, dtype)
+    want = _np_decode(allbits, dtype)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))
+
+
+# ------------------------------------------------------------ closed forms ----
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_single_key_gives_v0(dtype, causal):
+    q, k, v = si.qkv(11, 2, 4, 2, 9, 1, 32, dtype)
+    scale = 0.3
+    o, lse = oracle.attention_fwd(q, k, v, dtype, scale, causal)
+    K, V, Q = _np_decode(k, dtype), _np_decode(v, dtype), _np_decode(q, dtype)
+    for z in range(2):
+        for h in range(4):
+            hk = h // 2
+            assert np.array_equal(o[z, h], np.broadcast_to(V[z, hk, 0], o[z, h].shape))
+            s00 = scale * np.array([math.fsum(Q[z, h, i] * K[z, hk, 0]) for i in range(9)])
+            np.testing.assert_allclose(lse[z, h], s00, rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_identical_keys_give_mean_v(dtype):
+    Nkv, D = 37, 64
+    q, k, v = si.qkv(5, 1, 2, 1, 6, Nkv, D, dtype)
+    k[:] = k[:, :, :1, :]                 # every key equals key 0
+    scale = 1 / 8
+    o, lse = oracle.attention_fwd(q, k, v, dtype, scale, False)
+    Q, K, V = _np_decode(q, dtype), _np_decode(k, dtype), _np_decode(v, dtype)
+    mean_v = np.array([math.fsum(V[0, 0, :, d]) / Nkv for d in range(D)])
+    for h in range(2):
+        np.testing.assert_allclose(o[0, h], np.broadcast_to(mean_v, (6, D)), rtol=0, atol=1e-14)
+        s = scale * np.array([math.fsum(Q[0, h, i] * K[0, 0, 0]) for i in range(6)])
+        np.testing.assert_allclose(lse[0, h], s + math.log(Nkv), rtol=0, atol=1e-13)
+
+
+def test_zero_scale_gives_uniform_attention():
+    q, k, v = si.qkv(6, 1, 1, 1, 5, 19, 16, "fp16")
+    o, lse = oracle.attention_fwd(q, k, v, "fp16", 0.0, False)
+    V = _np_decode(v, "fp16")[0, 0]
+    np.testing.assert_allclose(o[0, 0], np.broadcast_to(V.mean(0), (5, 16)), rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse[0, 0], math.log(19), rtol=0, atol=1e-15)
+    # causal: row i averages keys 0..i, lse = ln(i + 1)
+    o, lse = oracle.attention_fwd(q, k, v, "fp16", 0.0, True)
+    for i in range(5):
+        np.testing.assert_allclose(o[0, 0, i], V[: i + 1].mean(0), rtol=0, atol=1e-14)
+        assert abs(lse[0, 0, i] - math.log(i + 1)) < 1e-15
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_causal_row0_is_v0(dtype):
+    q, k, v = si.qkv(3, 2, 4, 4, 20, 20, 16, dtype)
+    scale = 0.25
+    o, lse = oracle.attention_fwd(q, k, v, dtype, scale, True)
+    Q, K, V = _np_decode(q, dtype), _np_decode(k, dtype), _np_decode(v, dtype)
+    assert np.array_equal(o[:, :, 0], V[:, :, 0])
+    s00 = scale * np.array([[math.fsum(Q[z, h, 0] * K[z, h, 0]) for h in range(4)] for z in range(2)])
+    np.testing.assert_allclose(lse[:, :, 0], s00, rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_identity_values_expose_probabilities(causal):
+    # With V = I (Nkv = D) row i of O is row i of P = softmax(S).
+    D = 16
+    q, k, _ = si.qkv(9, 1, 1, 1, D, D, D, "fp16")
+    v = _bits(np.eye(D)[None, None], "fp16")
+    P, lse = oracle.attention_fwd(q, k, v, "fp16", 0.5, causal)
+    P = P[0, 0]
+    assert np.all(P >= 0)
+    np.testing.assert_allclose(P.sum(1), 1.0, rtol=0, atol=1e-14)
+    if causal:
+        assert np.all(np.triu(P, 1) == 0)
+        assert np.all(np.diag(P) > 0)
+    else:
+        assert np.all(P > 0)
+
+
+# --------------------------------------------------- brute force (mpmath) ----
+
+@pytest.mark.parametrize("dtype,scale,causal", [("fp16", 0.25, False), ("bf16", 0.25, True),
+                                                ("fp16", 200.0, False), ("bf16", 500.0, True)])
+def test_mpmath_bruteforce(dtype, scale, causal):
+    """Exact scores, exp without a max shift, 60 significant digits.
+
+    The large scales give scores in the thousands, beyond the float64 range of
+    exp (about 709), so an oracle without the max shift returns inf/nan there."""
+    Nq, Nkv, D = 4, 6, 16
+    q, k, v = si.qkv(21, 1, 1, 1, Nq, Nkv, D, dtype)
+    o, lse = oracle.attention_fwd(q, k, v, dtype, scale, causal)
+    Q, K, V = _np_decode(q, dtype)[0, 0], _np_decode(k, dtype)[0, 0], _np_decode(v, dtype)[0, 0]
+    if scale > 100:
+        assert np.max(np.abs(scale * Q @ K.T)) > 1000.0
+    with mpmath.workdps(60):
+        sc = mpmath.mpf(scale)
+        for i in range(Nq):
+            keys = range(i + 1) if causal else range(Nkv)
+            s = [sc * mpmath.fsum(mpmath.mpf(Q[i, d]) * mpmath.mpf(K[j, d]) for d in range(D)) for j in keys]
+            e = [mpmath.exp(x) for x in s]
+            tot = mpmath.fsum(e)
+            assert abs(lse[0, 0, i] - float(mpmath.log(tot))) <= 1e-13 * max(1.0, abs(float(mpmath.log(tot))))
+            for d in range(D):
+                ref = mpmath.fsum(e[t] * mpmath.mpf(V[j, d]) for t, j in enumerate(keys)) / tot
+                assert abs(o[0, 0, i, d] - float(ref)) <= 2e-14
+
+
+# -------------------------------------------------- library routines (scipy) ----
+
+def _scipy_attention(q, k, v, dtype, scale, causal):
+    from scipy.special import logsumexp, softmax
+
+    Q, K, V = _np_decode(q, dtype), _np_decode(k, dtype), _np_decode(v, dtype)
+    g = Q.shape[1] // K.shape[1]
+    K = np.repeat(K, g, axis=1)
+    V = np.repeat(V, g, axis=1)
+    S = scale * np.matmul(Q, np.swapaxes(K, -1, -2))
+    if causal:
+        Nq, Nkv = S.shape[-2:]
+        S = np.where(np.arange(Nkv)[None, :] <= np.arange(Nq)[:, None], S, -np.inf)
+    return np.matmul(softmax(S, axis=-1), V), logsumexp(S, axis=-1)
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", [(2, 4, 2, 37, 53, 32), (1, 8, 1, 70, 41, 16), (1, 2, 2, 129, 129, 64)])
+def test_matches_scipy(dtype, causal, shape):
+    Z, Hq, Hkv, Nq, Nkv, D = shape
+    q, k, v = si.qkv(4, Z, Hq, Hkv, Nq, Nkv, D, dtype)
+    scale = 1 / math.sqrt(D)
+    o, lse = oracle.attention_fwd(q, k, v, dtype, scale, causal)
+    o_ref, lse_ref = _scipy_attention(q, k, v, dtype, scale, causal)
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse, lse_ref, rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------------------- invariants ----
+
+def test_gqa_equals_mha_on_repeated_kv():
+    q, k, v = si.qkv(8, 2, 8, 2, 33, 45, 32, "bf16")
+    for causal in (False, True):
+        o, lse = oracle.attention_fwd(q, k, v, "bf16", 0.2, causal)
+        o2, lse2 = oracle.attention_fwd(q, np.repeat(k, 4, axis=1), np.repeat(v, 4, axis=1), "bf16", 0.2, causal)
+        assert np.array_equal(o, o2) and np.array_equal(lse, lse2)
+    # and a different grouping of the same K/V heads is a different answer
+    o3, _ = oracle.attention_fwd(q, np.tile(k, (1, 4, 1, 1)), np.tile(v, (1, 4, 1, 1)), "bf16", 0.2, False)
+    assert not np.allclose(o, o3)
+
+
+def test_key_permutation_invariance():
+    q, k, v = si.qkv(12, 1, 2, 1, 17, 64, 32, "fp16")
+    perm = np.random.default_rng(0).permutation(64)
+    o, lse = oracle.attention_fwd(q, k, v, "fp16", 0.17, False)
+    o2, lse2 = oracle.attention_fwd(q, k[:, :, perm], v[:, :, perm], "fp16", 0.17, False)
+    np.testing.assert_allclose(o, o2, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse, lse2, rtol=0, atol=1e-13)
+
+
+def test_causal_row_is_prefix_attention():
+    q, k, v = si.qkv(13, 1, 2, 2, 40, 40, 16, "fp16")
+    o, lse = oracle.attention_fwd(q, k, v, "fp16", 0.3, True)
+    for i in (0, 1, 7, 31, 39):
+        op, lp = oracle.attention_fwd(q[:, :, i:i + 1], k[:, :, : i + 1], v[:, :, : i + 1], "fp16", 0.3, False)
+        assert np.array_equal(o[:, :, i], op[:, :, 0]) and np.array_equal(lse[:, :, i], lp[:, :, 0])
+
+
+def test_causal_top_left_when_nq_exceeds_nkv():
+    # row i keeps keys j <= i: rows i >= Nkv - 1 see every key
+    q, k, v = si.qkv(14, 1, 1, 1, 30, 12, 16, "bf16")
+    oc, lc = oracle.attention_fwd(q, k, v, "bf16", 0.3, True)
+    on, ln = oracle.attention_fwd(q, k, v, "bf16", 0.3, False)
+    assert np.array_equal(oc[0, 0, 11:], on[0, 0, 11:]) and np.array_equal(lc[0, 0, 11:], ln[0, 0, 11:])
+    assert not np.allclose(oc[0, 0, :11], on[0, 0, :11])
+
+
+def test_row_subset_equals_full():
+    q, k, v = si.qkv(15, 2, 4, 2, 50, 60, 32, "fp16")
+    o, lse = oracle.attention_fwd(q, k, v, "fp16", 0.2, True)
+    rows = np.array([0, 49, 50, 199, 201, 399, 123])
+    os_, ls_ = oracle.attention_fwd(q, k, v, "fp16", 0.2, True, rows=rows)
+    assert np.array_equal(os_, o.reshape(-1, 32)[rows]) and np.array_equal(ls_, lse.reshape(-1)[rows])
+
+
+def test_threads_do_not_change_results():
+    q, k, v = si.qkv(16, 1, 4, 4, 64, 64, 32, "bf16")
+    a = oracle.attention_fwd(q, k, v, "bf16", 0.2, False, nthreads=1)
+    b = oracle.attention_fwd(q, k, v, "bf16", 0.2, False, nthreads=5)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_rejects_invalid_arguments():
+    q, k, v = si.qkv(0, 1, 3, 2, 4, 4, 16, "fp16")
+    with pytest.raises(ValueError):
+        oracle.attention_fwd(q, k, v, "fp16", 0.1, False)          # Hq % Hkv != 0
+    q, k, v = si.qkv(0, 1, 2, 1, 4, 4, 16, "fp16")
+    with pytest.raises(ValueError):
+        oracle.attention_fwd(q, k, v, "fp16", float("nan"), False)
+    with pytest.raises(ValueError):
+        oracle.attention_fwd(q, k, v, "fp16", 0.1, False, rows=np.array([8]))
