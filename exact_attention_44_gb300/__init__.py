@@ -1,0 +1,19 @@
+"""GB300-native fused attention forward (libfa, sm_103a).
+
+    from exact_attention_44_gb300 import fa_fwd
+    o, lse = fa_fwd(q, k, v, causal=True)     # q,k,v: CUDA (Z,H,N,D) fp16/bf16
+
+The computation runs in libfa.so's CUDA kernels (TMA + tcgen05 + TMEM); this
+package only marshals arguments.  Build the library with
+``python -m exact_attention_44_gb300.build``.
+"""
+from ._binding import (FA_DTYPE_BF16, FA_DTYPE_F16, FA_ERR_ALIGNMENT, FA_ERR_CUDA, FA_ERR_DEVICE_TIMEOUT,
+                       FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_OK, FaError, fa_debug_inject_stall,
+                       fa_debug_set_wait_limit_ms, fa_device_status, fa_fwd, fa_fwd_plan, fa_fwd_raw, fa_status_string,
+                       fa_strides, library_path, load)
+from .build import build
+
+__all__ = ["fa_fwd", "fa_fwd_raw", "fa_fwd_plan", "fa_device_status", "fa_status_string", "fa_debug_inject_stall",
+           "fa_debug_set_wait_limit_ms", "fa_strides", "FaError", "build", "load", "library_path", "FA_OK",
+           "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_ALIGNMENT", "FA_ERR_CUDA", "FA_ERR_DEVICE_TIMEOUT",
+           "FA_DTYPE_F16", "FA_DTYPE_BF16"]

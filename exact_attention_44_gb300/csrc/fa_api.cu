@@ -1,0 +1,268 @@
+// C ABI of libfa: argument validation, TMA tensor maps, specialisation
+// dispatch, launch, and the per-device status word.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_fwd_kernel.cuh"
+#include "fa_launch.h"
+
+namespace {
+
+__device__ uint32_t g_fa_status;  // first device-side error of any launch on this device
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    std::once_flag once;
+    cudaError_t err = cudaSuccess;
+    int sms = 0;
+    uint32_t* status = nullptr;
+};
+DeviceInfo g_devices[kMaxDevices];
+
+cudaError_t device_info(int dev, DeviceInfo** out) {
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    DeviceInfo& d = g_devices[dev];
+    std::call_once(d.once, [&] {
+        d.err = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (d.err == cudaSuccess) d.err = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_fa_status);
+    });
+    *out = &d;
+    return d.err;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+std::atomic<uint64_t> g_wait_limit_ns{0};
+std::atomic<int> g_inject_stall{0};
+
+uint64_t wait_limit_ns() {
+    uint64_t v = g_wait_limit_ns.load();
+    if (v) return v;
+    double ms = 2000.0;  // every wait in a healthy kernel takes microseconds
+    if (const char* e = std::getenv("FA_WAIT_LIMIT_MS")) {
+        double x = std::atof(e);
+        if (x >= 1.0 && x <= 600000.0) ms = x;
+    }
+    v = (uint64_t)(ms * 1e6);
+    g_wait_limit_ns.store(v);
+    return v;
+}
+
+bool supported_head_dim(int D) { return D == 16 || D == 32 || D == 64 || D == 128 || D == 256; }
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+fa_status check_shape(int Z, int Hq, int Hkv, int Nq, int Nkv, int D, int causal) {
+    if (Z < 0 || Hq < 0 || Hkv < 1 || Nq < 0 || Nkv < 0) return FA_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;  // GQA group size Hq / Hkv must be whole
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (!supported_head_dim(D)) return FA_ERR_UNSUPPORTED;
+    const int64_t rows = (int64_t)Z * Hq * Nq;
+    if (rows > 0 && Nkv == 0) return FA_ERR_INVALID_ARG;  // softmax over no keys is undefined
+    if ((int64_t)Z * Hq * cdiv(Nq, fa::BM) > INT32_MAX) return FA_ERR_UNSUPPORTED;
+    return FA_OK;
+}
+
+// d-stride 1, 16-byte aligned base, non-negative strides that are multiples of
+// 8 elements in every dimension of extent > 1 (TMA and 16-byte stores).
+fa_status check_tensor(const void* ptr, const fa_strides* s, int64_t nb, int64_t nh, int64_t nn) {
+    if (ptr == nullptr || s == nullptr) return FA_ERR_INVALID_ARG;
+    if (s->d != 1) return FA_ERR_ALIGNMENT;
+    if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return FA_ERR_ALIGNMENT;
+    const int64_t st[3] = {s->b, s->h, s->n};
+    const int64_t ext[3] = {nb, nh, nn};
+    for (int i = 0; i < 3; ++i) {
+        if (ext[i] <= 1) continue;
+        if (st[i] < 0 || st[i] % 8 != 0 || st[i] >= (int64_t(1) << 38)) return FA_ERR_ALIGNMENT;
+    }
+    return FA_OK;
+}
+
+// 4-D tensor map (d, n, h, b) with a box of `box_rows` rows x one swizzle chunk.
+CUresult make_map(CUtensorMap* map, const void* ptr, fa_dtype dt, int D, int N, int H, int B, const fa_strides* s,
+                  int box_rows) {
+    const int swe = fa::swizzle_elems_for(D);
+    const CUtensorMapSwizzle sw = swe == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : swe == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                              : CU_TENSOR_MAP_SWIZZLE_32B;
+    // a dimension of extent 1 is never stepped along; give it a harmless stride
+    const uint64_t filler = (uint64_t)D * 2 * (uint64_t)(N > 0 ? N : 1);
+    auto bytes = [&](int64_t stride, int64_t extent) -> cuuint64_t {
+        return extent > 1 ? (cuuint64_t)(stride * 2) : (cuuint64_t)filler;
+    };
+    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)H, (cuuint64_t)B};
+    cuuint64_t strides[3] = {bytes(s->n, N), bytes(s->h, H), bytes(s->b, B)};
+    cuuint32_t box[4] = {(cuuint32_t)swe, (cuuint32_t)box_rows, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    auto fn = encode_fn();
+    if (fn == nullptr) return CUDA_ERROR_NOT_SUPPORTED;
+    return fn(map, dt == FA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+              const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+}  // namespace
+
+namespace fa {
+template <int D>
+static void facts(int* bn, int* smem, int* swe) {
+    *bn = Traits<D>::BN;
+    *smem = Traits<D>::SMEM_BYTES;
+    *swe = Traits<D>::SWE;
+}
+static void facts_for(int D, int* bn, int* smem, int* swe) {
+    switch (D) {
+        case 16: facts<16>(bn, smem, swe); break;
+        case 32: facts<32>(bn, smem, swe); break;
+        case 64: facts<64>(bn, smem, swe); break;
+        case 128: facts<128>(bn, smem, swe); break;
+        default: facts<256>(bn, smem, swe); break;
+    }
+}
+int block_n_for(int D) { int a, b, c; facts_for(D, &a, &b, &c); return a; }
+int smem_bytes_for(int D) { int a, b, c; facts_for(D, &a, &b, &c); return b; }
+int swizzle_elems_for(int D) { int a, b, c; facts_for(D, &a, &b, &c); return c; }
+}  // namespace fa
+
+extern "C" {
+
+const char* fa_status_string(fa_status s) {
+    switch (s) {
+        case FA_OK: return "FA_OK";
+        case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+        case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+        case FA_ERR_ALIGNMENT: return "FA_ERR_ALIGNMENT";
+        case FA_ERR_CUDA: return "FA_ERR_CUDA";
+        case FA_ERR_DEVICE_TIMEOUT: return "FA_ERR_DEVICE_TIMEOUT";
+    }
+    return "FA_ERR_UNKNOWN";
+}
+
+fa_status fa_fwd_plan(int Z, int Hq, int Hkv, int Nq, int Nkv, int D, int causal, int num_sms, int64_t* tiles,
+                      int64_t* kv_blocks, int* block_n, int* grid, int* smem_bytes) {
+    const fa_status st = check_shape(Z, Hq, Hkv, Nq, Nkv, D, causal);
+    if (st != FA_OK) return st;
+    const int bn = fa::block_n_for(D);
+    const int64_t tq = cdiv(Nq, fa::BM), tk = cdiv(Nkv, bn);
+    const int64_t nt = (int64_t)Z * Hq * tq;
+    int64_t pairs = 0;
+    if (causal) {
+        for (int64_t mb = 0; mb < tq; ++mb) {  // same bound as the kernel's tile_info
+            const int64_t last_row = std::min<int64_t>(mb * fa::BM + fa::BM, Nq) - 1;
+            pairs += std::min<int64_t>(tk, last_row / bn + 1);
+        }
+        pairs *= (int64_t)Z * Hq;
+    } else {
+        pairs = nt * tk;
+    }
+    if (tiles) *tiles = nt;
+    if (kv_blocks) *kv_blocks = pairs;
+    if (block_n) *block_n = bn;
+    if (grid) *grid = (int)(num_sms > 0 ? std::min<int64_t>(nt, num_sms) : nt);
+    if (smem_bytes) *smem_bytes = fa::smem_bytes_for(D);
+    return FA_OK;
+}
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int Z, int Hq, int Hkv, int Nq,
+                 int Nkv, int D, const fa_strides* sq, const fa_strides* sk, const fa_strides* sv,
+                 const fa_strides* so, float scale, int causal, fa_dtype dtype, cudaStream_t stream) {
+    fa_status st = check_shape(Z, Hq, Hkv, Nq, Nkv, D, causal);
+    if (st != FA_OK) return st;
+    if (dtype != FA_DTYPE_F16 && dtype != FA_DTYPE_BF16) return FA_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;  // a softmax temperature is positive
+    if ((int64_t)Z * Hq * Nq == 0) return FA_OK;
+    if ((st = check_tensor(q, sq, Z, Hq, Nq)) != FA_OK) return st;
+    if ((st = check_tensor(k, sk, Z, Hkv, Nkv)) != FA_OK) return st;
+    if ((st = check_tensor(v, sv, Z, Hkv, Nkv)) != FA_OK) return st;
+    if ((st = check_tensor(o, so, Z, Hq, Nq)) != FA_OK) return st;
+    if (lse != nullptr && reinterpret_cast<uintptr_t>(lse) % 4 != 0) return FA_ERR_ALIGNMENT;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+    DeviceInfo* info = nullptr;
+    if (device_info(dev, &info) != cudaSuccess) return FA_ERR_CUDA;
+
+    const int bn = fa::block_n_for(D);
+    CUtensorMap mq, mk, mv;
+    if (make_map(&mq, q, dtype, D, Nq, Hq, Z, sq, fa::BM) != CUDA_SUCCESS) return FA_ERR_CUDA;
+    if (make_map(&mk, k, dtype, D, Nkv, Hkv, Z, sk, bn) != CUDA_SUCCESS) return FA_ERR_CUDA;
+    if (make_map(&mv, v, dtype, D, Nkv, Hkv, Z, sv, bn) != CUDA_SUCCESS) return FA_ERR_CUDA;
+
+    fa::LaunchArgs a;
+    a.tmQ = &mq;
+    a.tmK = &mk;
+    a.tmV = &mv;
+    fa::FwdParams& p = a.params;
+    p.o = o;
+    p.lse = lse;
+    p.so_z = so->b;
+    p.so_h = so->h;
+    p.so_n = so->n;
+    p.Z = Z;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.Nq = Nq;
+    p.Nkv = Nkv;
+    p.group = Hq / Hkv;
+    p.Tq = (int)cdiv(Nq, fa::BM);
+    p.Tk = (int)cdiv(Nkv, bn);
+    p.ntiles = (int)((int64_t)Z * Hq * p.Tq);
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634);  // exp(x) = 2^(x log2 e)
+    p.status = info->status;
+    p.wait_limit_ns = wait_limit_ns();
+    p.inject_stall = g_inject_stall.load();
+    a.grid = std::min(p.ntiles, info->sms);
+    a.stream = stream;
+
+    cudaError_t err;
+    switch (D) {
+        case 16: err = fa::launch_d16(a, causal != 0, dtype == FA_DTYPE_BF16); break;
+        case 32: err = fa::launch_d32(a, causal != 0, dtype == FA_DTYPE_BF16); break;
+        case 64: err = fa::launch_d64(a, causal != 0, dtype == FA_DTYPE_BF16); break;
+        case 128: err = fa::launch_d128(a, causal != 0, dtype == FA_DTYPE_BF16); break;
+        default: err = fa::launch_d256(a, causal != 0, dtype == FA_DTYPE_BF16); break;
+    }
+    return err == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_device_status(cudaStream_t stream, uint32_t* detail) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;
+    uint32_t word = 0;
+    if (cudaMemcpyFromSymbol(&word, g_fa_status, sizeof(word)) != cudaSuccess) return FA_ERR_CUDA;
+    if (word != 0) {
+        const uint32_t zero = 0;
+        if (cudaMemcpyToSymbol(g_fa_status, &zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
+    }
+    if (detail) *detail = word;
+    return word == 0 ? FA_OK : (fa_status)(word & 0xFFu);
+}
+
+// Test hooks (declared in fa.h): the bound on every device-side wait, and a
+// switch that makes CTA 0 withhold one K tile so that its waits run out.
+void fa_debug_set_wait_limit_ms(double ms) {
+    g_wait_limit_ns.store(ms > 0 ? (uint64_t)(ms * 1e6) : 0);
+}
+void fa_debug_inject_stall(int enable) { g_inject_stall.store(enable ? 1 : 0); }
+
+}  // extern "C"

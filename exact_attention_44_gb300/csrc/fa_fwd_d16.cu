@@ -1,0 +1,34 @@
+// Specialisations of the attention forward kernel for head dim 16.
+#include <atomic>
+#include <cstdint>
+
+#include "fa_fwd_kernel.cuh"
+#include "fa_launch.h"
+
+namespace fa {
+
+template <bool CAUSAL, bool BF16>
+static cudaError_t launch_one(const LaunchArgs& a) {
+    auto kernel = fa_fwd_kernel<16, CAUSAL, BF16>;
+    constexpr int smem = Traits<16>::SMEM_BYTES;
+    // the opt-in shared memory size is set once per device
+    static std::atomic<uint64_t> configured{0};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(configured.load() & bit)) {
+        err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (err != cudaSuccess) return err;
+        configured.fetch_or(bit);
+    }
+    kernel<<<a.grid, NUM_THREADS, smem, a.stream>>>(*a.tmQ, *a.tmK, *a.tmV, a.params);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_d16(const LaunchArgs& a, bool causal, bool bf16) {
+    if (causal) return bf16 ? launch_one<true, true>(a) : launch_one<true, false>(a);
+    return bf16 ? launch_one<false, true>(a) : launch_one<false, false>(a);
+}
+
+}  // namespace fa

@@ -1,0 +1,498 @@
+// Fused attention forward, O = softmax(Q Kᵀ · scale) V with the per-row
+// log-sum-exp, for sm_103a: TMA tile loads through mbarrier rings, tcgen05
+// MMAs accumulating in tensor memory, online softmax in registers.
+//
+// The method is the tiled online-softmax forward of the pages
+//   "Build Triton-Ascend Fused Attention" (Workflow, Implementation Pattern),
+//   "Write Triton Attention Kernel" (Required reasoning process, steps 1-9;
+//     Kernel design rules; Correctness requirements),
+//   "把 FlashAttention 搬上昇腾：Triton-Ascend CV Pipeline 优化实战" (section 一:
+//     exp2 with scale·log2(e), fp32 state, P cast to the input type;
+//     section 八: causal loop bound at the diagonal).
+// Its GB300 form:
+//   * one persistent CTA per SM walks a static list of 128-row query tiles;
+//   * warp 0 (one lane) streams Q once per tile and K_j, V_j per key block by
+//     TMA into swizzled shared-memory rings guarded by full/empty mbarriers;
+//   * warp 1 (one lane) issues S_j = Q K_jᵀ into a double-buffered S in TMEM
+//     and O += P_j V_j with P_j read from TMEM, committing to mbarriers;
+//   * warps 2-5 (128 threads, thread = query row = TMEM lane) run the online
+//     softmax: mask (diagonal/tail blocks only), row max, exp2, row sum,
+//     P -> fp16/bf16 into TMEM, rescale O when the max moved, and the epilogue
+//     O / l -> global and lse = (m + log2 l)·ln 2.
+// Every mbarrier wait is bounded; on expiry the CTA records the site in the
+// status word, stops every role, lets its copies and MMAs land and frees TMEM.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "fa_params.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+
+template <int D_>
+struct Traits {
+    static constexpr int D = D_;
+    static constexpr int BN = D == 256 ? 64 : 128;            // keys per block
+    static constexpr int SW = D * 2 >= 128 ? 128 : D * 2;      // bytes per swizzled row chunk
+    static constexpr int SWE = SW / 2;                         // elements per row chunk
+    static constexpr int NCHUNK = D / SWE;                     // row chunks per tile row
+    static constexpr uint32_t SWIZZLE_CODE = SW == 128 ? 2u : SW == 64 ? 4u : 6u;  // UMMA descriptor code
+    static constexpr int Q_BYTES = BM * D * 2;
+    static constexpr int KV_BYTES = BN * D * 2;
+    static constexpr int Q_STAGES = D == 256 ? 1 : 2;
+    static constexpr int K_STAGES = D <= 32 ? 4 : D == 64 ? 3 : 2;
+    static constexpr int V_STAGES = K_STAGES;
+    // tensor memory columns (lane = query row)
+    static constexpr uint32_t TM_S = 0;                        // S[b] at TM_S + b * BN (fp32)
+    static constexpr uint32_t TM_P = 2 * BN;                   // P[b] at TM_P + b * BN/2 (2 x 16 bit per column)
+    static constexpr uint32_t TM_O = 3 * BN;                   // O, D fp32 columns
+    static constexpr uint32_t TMEM_COLS = 512;
+    static_assert(TM_O + D <= TMEM_COLS, "tensor memory budget");
+    // shared memory (offsets from a 1024-byte aligned base)
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = OFF_Q + Q_STAGES * Q_BYTES;
+    static constexpr int OFF_V = OFF_K + K_STAGES * KV_BYTES;
+    static constexpr int OFF_BAR = OFF_V + V_STAGES * KV_BYTES;
+    // barrier indices
+    static constexpr int B_QFULL = 0;
+    static constexpr int B_QEMPTY = B_QFULL + Q_STAGES;
+    static constexpr int B_KFULL = B_QEMPTY + Q_STAGES;
+    static constexpr int B_KEMPTY = B_KFULL + K_STAGES;
+    static constexpr int B_VFULL = B_KEMPTY + K_STAGES;
+    static constexpr int B_VEMPTY = B_VFULL + V_STAGES;
+    static constexpr int B_SFULL = B_VEMPTY + V_STAGES;        // 2
+    static constexpr int B_PFULL = B_SFULL + 2;                // 2
+    static constexpr int B_PVDONE = B_PFULL + 2;               // 1
+    static constexpr int B_DRAIN = B_PVDONE + 1;               // 1
+    static constexpr int NUM_BARS = B_DRAIN + 1;
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;    // tmem base, abort flag
+    static constexpr int SMEM_USED = OFF_MISC + 16;
+    // >= 120 KB keeps one CTA per SM, so no CTA ever waits on another's TMEM
+    static constexpr int SMEM_BYTES = (SMEM_USED + 1024) > 120 * 1024 ? SMEM_USED + 1024 : 120 * 1024;
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+};
+
+struct Ctl {
+    volatile int* abort_flag;
+    uint32_t* status;
+    uint64_t limit_ns;
+};
+
+__device__ __forceinline__ void record_timeout(const Ctl& c, uint32_t site) {
+    *c.abort_flag = 1;
+    atomicCAS(c.status, 0u, 5u /* FA_ERR_DEVICE_TIMEOUT */ | (site << 8) | ((blockIdx.x & 0xFFFFu) << 16));
+}
+
+// Wait for the phase of `bar` with parity `parity`.  Gives up (false) when
+// another role has aborted or after limit_ns, recording the site.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Ctl& c, uint32_t site) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (;;) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (*c.abort_flag) return false;
+        if (ptx::globaltimer_ns() - t0 > c.limit_ns) {
+            record_timeout(c, site);
+            return false;
+        }
+    }
+}
+
+// The same wait taken by a whole warp: every lane leaves with the same answer,
+// so no lane can run ahead into a warp-collective tcgen05 access alone.
+__device__ __forceinline__ bool warp_wait_phase(uint32_t bar, uint32_t parity, const Ctl& c, uint32_t site) {
+    return __all_sync(0xffffffffu, wait_phase(bar, parity, c, site));
+}
+
+// Teardown wait after an abort: ignores the abort flag, bounded by limit_ns.
+__device__ __forceinline__ bool drain_phase(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (!ptx::mbar_try_wait(bar, parity))
+        if (ptx::globaltimer_ns() - t0 > limit_ns) return false;
+    return true;
+}
+
+struct TileInfo {
+    int z, hq, hk, q_start, nkv;
+};
+
+// Tile t of the static schedule.  Non-causal: head-major, so the CTAs running
+// at the same time share a head's K/V in L2.  Causal: query blocks from the
+// last (most key blocks) to the first, heads innermost, so the heavy tiles go
+// first and the light ones fill the tail.  A causal tile stops at the key
+// block holding its last row ("Write Triton Attention Kernel", step 9).
+template <bool CAUSAL, int BN>
+__device__ __forceinline__ TileInfo tile_info(int t, const FwdParams& p) {
+    TileInfo ti;
+    const int heads = p.Z * p.Hq;
+    int head, mb;
+    if (CAUSAL) {
+        mb = p.Tq - 1 - t / heads;
+        head = t % heads;
+    } else {
+        head = t / p.Tq;
+        mb = t % p.Tq;
+    }
+    ti.z = head / p.Hq;
+    ti.hq = head % p.Hq;
+    ti.hk = ti.hq / p.group;  // GQA: kv head = q head // (Hq / Hkv)
+    ti.q_start = mb * BM;
+    if (CAUSAL) {
+        const int last_row = min(ti.q_start + BM, p.Nq) - 1;
+        ti.nkv = min(p.Tk, last_row / BN + 1);
+    } else {
+        ti.nkv = p.Tk;
+    }
+    return ti;
+}
+
+// ------------------------------------------------------------ TMA producer --
+template <int D, bool CAUSAL>
+__device__ void run_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
+                             const FwdParams& p, uint32_t sbase, uint32_t bar0, const Ctl& ctl) {
+    using T = Traits<D>;
+    auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+    const uint64_t pol_q = ptx::policy_evict_first();
+    const uint64_t pol_kv = ptx::policy_evict_last();
+    uint32_t qi = 0, ki = 0, vi = 0;  // loads issued into each ring
+    bool ok = true;
+    bool withheld = false;
+    for (int t = blockIdx.x; ok && t < p.ntiles; t += gridDim.x) {
+        const TileInfo ti = tile_info<CAUSAL, T::BN>(t, p);
+        {
+            const uint32_t s = qi % T::Q_STAGES, ph = (qi / T::Q_STAGES) & 1u;
+            if (!wait_phase(bar(T::B_QEMPTY + s), ph ^ 1u, ctl, SITE_Q_EMPTY)) { ok = false; break; }
+            ptx::mbar_arrive_expect_tx(bar(T::B_QFULL + s), T::Q_BYTES);
+            const uint32_t dst = sbase + T::OFF_Q + s * T::Q_BYTES;
+            for (int c = 0; c < T::NCHUNK; ++c)
+                ptx::tma_load_4d(dst + c * (BM * T::SW), tmQ, bar(T::B_QFULL + s), c * T::SWE, ti.q_start, ti.hq,
+                                 ti.z, pol_q);
+            ++qi;
+        }
+        for (int j = 0; j < ti.nkv; ++j) {
+            {
+                const uint32_t s = ki % T::K_STAGES, ph = (ki / T::K_STAGES) & 1u;
+                if (!wait_phase(bar(T::B_KEMPTY + s), ph ^ 1u, ctl, SITE_K_EMPTY)) { ok = false; break; }
+                if (p.inject_stall && blockIdx.x == 0 && !withheld) {
+                    withheld = true;  // never issued: the MMA warp's wait for this tile must time out
+                } else {
+                    ptx::mbar_arrive_expect_tx(bar(T::B_KFULL + s), T::KV_BYTES);
+                    const uint32_t dst = sbase + T::OFF_K + s * T::KV_BYTES;
+                    for (int c = 0; c < T::NCHUNK; ++c)
+                        ptx::tma_load_4d(dst + c * (T::BN * T::SW), tmK, bar(T::B_KFULL + s), c * T::SWE, j * T::BN,
+                                         ti.hk, ti.z, pol_kv);
+                }
+                ++ki;
+            }
+            {
+                const uint32_t s = vi % T::V_STAGES, ph = (vi / T::V_STAGES) & 1u;
+                if (!wait_phase(bar(T::B_VEMPTY + s), ph ^ 1u, ctl, SITE_V_EMPTY)) { ok = false; break; }
+                ptx::mbar_arrive_expect_tx(bar(T::B_VFULL + s), T::KV_BYTES);
+                const uint32_t dst = sbase + T::OFF_V + s * T::KV_BYTES;
+                for (int c = 0; c < T::NCHUNK; ++c)
+                    ptx::tma_load_4d(dst + c * (T::BN * T::SW), tmV, bar(T::B_VFULL + s), c * T::SWE, j * T::BN,
+                                     ti.hk, ti.z, pol_kv);
+                ++vi;
+            }
+        }
+    }
+    if (!ok) {
+        // Let every copy still in flight land before shared memory is released.
+        // The withheld load never completes; its wait simply runs out.
+        const uint64_t lim = ctl.limit_ns;
+        for (uint32_t i = qi > (uint32_t)T::Q_STAGES ? qi - T::Q_STAGES : 0; i < qi; ++i)
+            drain_phase(bar(T::B_QFULL + i % T::Q_STAGES), (i / T::Q_STAGES) & 1u, lim);
+        for (uint32_t i = ki > (uint32_t)T::K_STAGES ? ki - T::K_STAGES : 0; i < ki; ++i)
+            drain_phase(bar(T::B_KFULL + i % T::K_STAGES), (i / T::K_STAGES) & 1u, withheld ? lim / 64 : lim);
+        for (uint32_t i = vi > (uint32_t)T::V_STAGES ? vi - T::V_STAGES : 0; i < vi; ++i)
+            drain_phase(bar(T::B_VFULL + i % T::V_STAGES), (i / T::V_STAGES) & 1u, lim);
+    }
+}
+
+// ------------------------------------------------------------ MMA issuer ----
+template <int D, bool CAUSAL, bool BF16>
+__device__ void run_mma(const FwdParams& p, uint32_t sbase, uint32_t bar0, uint32_t tmem, const Ctl& ctl) {
+    using T = Traits<D>;
+    auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+    constexpr uint32_t IDESC_QK = ptx::idesc_f16(BM, T::BN, BF16, false, false);  // Q, K both K-major
+    constexpr uint32_t IDESC_PV = ptx::idesc_f16(BM, D, BF16, false, true);       // V is MN-major (D contiguous)
+    constexpr uint32_t KMAJ_SBO = 8 * T::SW;                  // 8-row swizzle atom
+    constexpr uint32_t V_LBO = T::BN * T::SW;                 // next 64/32/16-column chunk of V
+    uint32_t qi = 0, ki = 0, vi = 0, qk_step = 0, pv_step = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < p.ntiles; t += gridDim.x) {
+        const TileInfo ti = tile_info<CAUSAL, T::BN>(t, p);
+        const uint32_t qs = qi % T::Q_STAGES;
+        if (!wait_phase(bar(T::B_QFULL + qs), (qi / T::Q_STAGES) & 1u, ctl, SITE_Q_FULL)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const uint32_t q_base = sbase + T::OFF_Q + qs * T::Q_BYTES;
+
+        // S_j = Q K_jᵀ into S[qk_step & 1]  ("Write Triton Attention Kernel", step 5b)
+        auto issue_qk = [&](int j) -> bool {
+            const uint32_t ks = ki % T::K_STAGES;
+            if (!wait_phase(bar(T::B_KFULL + ks), (ki / T::K_STAGES) & 1u, ctl, SITE_K_FULL)) return false;
+            ptx::tc_fence_after();
+            const uint32_t k_base = sbase + T::OFF_K + ks * T::KV_BYTES;
+            const uint32_t d_tmem = tmem + T::TM_S + (qk_step & 1u) * T::BN;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const int chunk = (kk * 16) / T::SWE, within = (kk * 16) % T::SWE;
+                const uint64_t a = ptx::smem_desc(q_base + chunk * (BM * T::SW) + within * 2, 16, KMAJ_SBO,
+                                                  T::SWIZZLE_CODE);
+                const uint64_t b = ptx::smem_desc(k_base + chunk * (T::BN * T::SW) + within * 2, 16, KMAJ_SBO,
+                                                  T::SWIZZLE_CODE);
+                ptx::mma_ss(d_tmem, a, b, IDESC_QK, kk > 0 ? 1u : 0u);
+            }
+            ptx::tc_commit(bar(T::B_SFULL + (qk_step & 1u)));
+            ptx::tc_commit(bar(T::B_KEMPTY + ks));
+            if (j == ti.nkv - 1) {
+                ptx::tc_commit(bar(T::B_QEMPTY + qs));  // last use of this Q tile
+                ++qi;
+            }
+            ++ki;
+            ++qk_step;
+            return true;
+        };
+
+        if (!issue_qk(0)) { ok = false; break; }
+        for (int j = 0; j < ti.nkv; ++j) {
+            // the next score block runs on the tensor cores while softmax works on this one
+            if (j + 1 < ti.nkv && !issue_qk(j + 1)) { ok = false; break; }
+            // O += P_j V_j  (step 5h), accumulating into O from the second block on
+            const uint32_t b = pv_step & 1u;
+            if (!wait_phase(bar(T::B_PFULL + b), (pv_step >> 1) & 1u, ctl, SITE_P_FULL)) { ok = false; break; }
+            const uint32_t vs = vi % T::V_STAGES;
+            if (!wait_phase(bar(T::B_VFULL + vs), (vi / T::V_STAGES) & 1u, ctl, SITE_V_FULL)) { ok = false; break; }
+            ptx::tc_fence_after();
+            const uint32_t v_base = sbase + T::OFF_V + vs * T::KV_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < T::BN / 16; ++kk) {
+                const uint64_t bdesc = ptx::smem_desc(v_base + kk * 16 * T::SW, V_LBO, KMAJ_SBO, T::SWIZZLE_CODE);
+                ptx::mma_ts(tmem + T::TM_O, tmem + T::TM_P + b * (T::BN / 2) + kk * 8, bdesc, IDESC_PV,
+                            (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            ptx::tc_commit(bar(T::B_VEMPTY + vs));
+            ptx::tc_commit(bar(T::B_PVDONE));
+            ++vi;
+            ++pv_step;
+        }
+    }
+    if (!ok) {
+        // every MMA issued so far must finish before TMEM and shared memory go away
+        ptx::tc_commit(bar(T::B_DRAIN));
+        drain_phase(bar(T::B_DRAIN), 0u, ctl.limit_ns);
+    }
+}
+
+// ------------------------------------------------------------ softmax -------
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    if constexpr (BF16) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&h);
+    } else {
+        __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+}
+
+template <int D, bool CAUSAL, bool BF16>
+__device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, const Ctl& ctl) {
+    using T = Traits<D>;
+    constexpr int BN = T::BN;
+    auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+    const int quad = (threadIdx.x / 32) % 4;  // TMEM lane quadrant this warp may access
+    const int row = quad * 32 + threadIdx.x % 32;
+    const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
+    const float c = p.scale_log2;
+    uint32_t step = 0, pv_waits = 0;
+
+    for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
+        const TileInfo ti = tile_info<CAUSAL, BN>(t, p);
+        const int q_row = ti.q_start + row;
+        // running max (log2 units of the scaled score) and denominator, fp32
+        // ("Write Triton Attention Kernel", step 4; the initial l is 0)
+        float m = -INFINITY, l = 0.f;
+        for (int j = 0; j < ti.nkv; ++j) {
+            const uint32_t b = step & 1u;
+            if (!warp_wait_phase(bar(T::B_SFULL + b), (step >> 1) & 1u, ctl, SITE_S_FULL)) return;
+            ptx::tc_fence_after();
+            float s[BN];
+#pragma unroll
+            for (int i = 0; i < BN / 32; ++i) {
+                uint32_t r[32];
+                ptx::tmem_ld32(tmem + lane_addr + T::TM_S + b * BN + 32 * i, r);
+#pragma unroll
+                for (int x = 0; x < 32; ++x) s[32 * i + x] = __uint_as_float(r[x]);
+            }
+            // the mask goes on the scores before the row max (Correctness
+            // requirements); only the diagonal block and the key tail need it
+            const int k0 = j * BN;
+            const bool need_mask = (CAUSAL && k0 + BN - 1 > ti.q_start) || (k0 + BN > p.Nkv);
+            if (need_mask) {
+                const int kmax = CAUSAL ? min(p.Nkv - 1, q_row) : p.Nkv - 1;  // last kept key for this row
+#pragma unroll
+                for (int x = 0; x < BN; ++x)
+                    if (k0 + x > kmax) s[x] = -INFINITY;
+            }
+            float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+            for (int x = 4; x < BN; x += 4) {
+                mx0 = fmaxf(mx0, s[x]);
+                mx1 = fmaxf(mx1, s[x + 1]);
+                mx2 = fmaxf(mx2, s[x + 2]);
+                mx3 = fmaxf(mx3, s[x + 3]);
+            }
+            const float m_new = fmaxf(m, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c);
+            const float alpha = ptx::ex2(m - m_new);  // 0 on the first block (m = -inf)
+            const float neg = -m_new;
+            // p = 2^(s·scale·log2e − m); l sums the fp32 p, P V uses p cast to the input type
+            uint32_t pk[BN / 2];
+            float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+            for (int x = 0; x < BN / 2; ++x) {
+                const float p0 = ptx::ex2(fmaf(s[2 * x], c, neg));
+                const float p1 = ptx::ex2(fmaf(s[2 * x + 1], c, neg));
+                sum0 += p0;
+                sum1 += p1;
+                pk[x] = pack2<BF16>(p0, p1);
+            }
+            if (j > 0) {
+                // PV of the previous block is complete: O is stable, and P[b]
+                // (read two blocks ago) is free.  Rescale O by alpha before the
+                // next block is added to it (Kernel design rules).
+                if (!warp_wait_phase(bar(T::B_PVDONE), pv_waits & 1u, ctl, SITE_PV_DONE)) return;
+                ++pv_waits;
+                ptx::tc_fence_after();
+                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+                    if constexpr (D >= 32) {
+#pragma unroll
+                        for (int i = 0; i < D / 32; ++i) {
+                            uint32_t r[32];
+                            const uint32_t a = tmem + lane_addr + T::TM_O + 32 * i;
+                            ptx::tmem_ld32(a, r);
+#pragma unroll
+                            for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * alpha);
+                            ptx::tmem_st32(a, r);
+                        }
+                    } else {
+                        uint32_t r[16];
+                        const uint32_t a = tmem + lane_addr + T::TM_O;
+                        ptx::tmem_ld16(a, r);
+#pragma unroll
+                        for (int x = 0; x < 16; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * alpha);
+                        ptx::tmem_st16(a, r);
+                    }
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < BN / 64; ++i) {
+                uint32_t r[32];
+#pragma unroll
+                for (int x = 0; x < 32; ++x) r[x] = pk[32 * i + x];
+                ptx::tmem_st32(tmem + lane_addr + T::TM_P + b * (BN / 2) + 32 * i, r);
+            }
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(T::B_PFULL + b));
+            l = l * alpha + (sum0 + sum1);
+            m = m_new;
+            ++step;
+        }
+        // epilogue: O = acc / l in the input type, lse = m + log(l) in natural-log units
+        if (!warp_wait_phase(bar(T::B_PVDONE), pv_waits & 1u, ctl, SITE_PV_DONE)) return;
+        ++pv_waits;
+        ptx::tc_fence_after();
+        const float inv_l = 1.f / l;
+        const bool store = q_row < p.Nq;
+        uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
+                        2 * ((int64_t)ti.z * p.so_z + (int64_t)ti.hq * p.so_h + (int64_t)q_row * p.so_n);
+        if constexpr (D >= 32) {
+#pragma unroll
+            for (int i = 0; i < D / 32; ++i) {
+                uint32_t r[32];
+                ptx::tmem_ld32(tmem + lane_addr + T::TM_O + 32 * i, r);
+                uint32_t o16[16];
+#pragma unroll
+                for (int x = 0; x < 16; ++x)
+                    o16[x] = pack2<BF16>(__uint_as_float(r[2 * x]) * inv_l, __uint_as_float(r[2 * x + 1]) * inv_l);
+                if (store) {
+                    uint4* dst = reinterpret_cast<uint4*>(orow + 64 * i);
+#pragma unroll
+                    for (int x = 0; x < 4; ++x)
+                        dst[x] = make_uint4(o16[4 * x], o16[4 * x + 1], o16[4 * x + 2], o16[4 * x + 3]);
+                }
+            }
+        } else {
+            uint32_t r[16];
+            ptx::tmem_ld16(tmem + lane_addr + T::TM_O, r);
+            uint32_t o8[8];
+#pragma unroll
+            for (int x = 0; x < 8; ++x)
+                o8[x] = pack2<BF16>(__uint_as_float(r[2 * x]) * inv_l, __uint_as_float(r[2 * x + 1]) * inv_l);
+            if (store) {
+                uint4* dst = reinterpret_cast<uint4*>(orow);
+                dst[0] = make_uint4(o8[0], o8[1], o8[2], o8[3]);
+                dst[1] = make_uint4(o8[4], o8[5], o8[6], o8[7]);
+            }
+        }
+        if (store && p.lse != nullptr)
+            p.lse[((int64_t)ti.z * p.Hq + ti.hq) * p.Nq + q_row] = (m + log2f(l)) * 0.6931471805599453f;
+    }
+}
+
+// ------------------------------------------------------------ kernel --------
+template <int D, bool CAUSAL, bool BF16>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+    using T = Traits<D>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = ptx::smem_addr(smem);
+    const uint32_t bar0 = sbase + T::OFF_BAR;
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + T::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + T::OFF_MISC + 4);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < T::NUM_BARS; ++i) {
+            uint32_t count = 1;
+            if (i >= T::B_PFULL && i < T::B_PFULL + 2) count = 128;  // every softmax thread arrives
+            ptx::mbar_init(bar0 + 8u * i, count);
+        }
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+        ptx::prefetch_tmap(&tmQ);
+        ptx::prefetch_tmap(&tmK);
+        ptx::prefetch_tmap(&tmV);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_addr(const_cast<uint32_t*>(tmem_slot)), T::TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const Ctl ctl{abort_flag, p.status, p.wait_limit_ns};
+
+    if (warp == 0) {
+        if (lane == 0) run_producer<D, CAUSAL>(&tmQ, &tmK, &tmV, p, sbase, bar0, ctl);
+    } else if (warp == 1) {
+        if (lane == 0) run_mma<D, CAUSAL, BF16>(p, sbase, bar0, tmem, ctl);
+    } else {
+        run_softmax<D, CAUSAL, BF16>(p, bar0, tmem, ctl);
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, T::TMEM_COLS);
+    }
+}
+
+}  // namespace fa

@@ -1,0 +1,32 @@
+// Per-head-dim launchers, one translation unit each (compiled in parallel).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime_api.h>
+
+#include "fa_params.h"
+
+namespace fa {
+
+struct LaunchArgs {
+    const CUtensorMap* tmQ;
+    const CUtensorMap* tmK;
+    const CUtensorMap* tmV;
+    FwdParams params;
+    int grid;
+    cudaStream_t stream;
+};
+
+// Launch fa_fwd_kernel<D, causal, bf16>; returns the launch's error code.
+cudaError_t launch_d16(const LaunchArgs& a, bool causal, bool bf16);
+cudaError_t launch_d32(const LaunchArgs& a, bool causal, bool bf16);
+cudaError_t launch_d64(const LaunchArgs& a, bool causal, bool bf16);
+cudaError_t launch_d128(const LaunchArgs& a, bool causal, bool bf16);
+cudaError_t launch_d256(const LaunchArgs& a, bool causal, bool bf16);
+
+// Host-side shape facts of each specialisation.
+int block_n_for(int D);      // keys per block
+int smem_bytes_for(int D);   // dynamic shared memory per CTA
+int swizzle_elems_for(int D);  // elements per swizzled row chunk (TMA box inner extent)
+
+}  // namespace fa

@@ -1,0 +1,38 @@
+// Kernel parameter block for the attention forward kernels (host and device).
+#pragma once
+
+#include <cstdint>
+
+namespace fa {
+
+constexpr int BM = 128;            // query rows per tile (one TMEM lane per row)
+constexpr int NUM_THREADS = 192;   // warp 0: TMA producer, warp 1: MMA issuer, warps 2-5: softmax
+
+// Where a bounded wait gave up; recorded in bits 8-15 of the device status word.
+enum WaitSite : uint32_t {
+    SITE_Q_FULL = 1,
+    SITE_K_FULL = 2,
+    SITE_V_FULL = 3,
+    SITE_Q_EMPTY = 4,
+    SITE_K_EMPTY = 5,
+    SITE_V_EMPTY = 6,
+    SITE_S_FULL = 7,
+    SITE_P_FULL = 8,
+    SITE_PV_DONE = 9,
+};
+
+struct FwdParams {
+    void* o;                 // output, dtype of the inputs, d-stride 1
+    float* lse;              // (Z, Hq, Nq) fp32 contiguous, or nullptr
+    int64_t so_z, so_h, so_n;  // O strides in elements
+    int Z, Hq, Hkv, Nq, Nkv;
+    int group;               // Hq / Hkv
+    int Tq, Tk;              // ceil(Nq / BM), ceil(Nkv / BN)
+    int ntiles;              // Z * Hq * Tq
+    float scale_log2;        // scale * log2(e)
+    uint32_t* status;        // device status word (first error wins)
+    uint64_t wait_limit_ns;  // bound on every mbarrier wait
+    int inject_stall;        // test hook: 1 = withhold the first K tile of CTA 0 (waits must time out)
+};
+
+}  // namespace fa

@@ -1,0 +1,138 @@
+/*
+ * libfa -- fused scaled-dot-product attention forward for GB300 (sm_103a).
+ *
+ * C ABI.  Plain pointers and sizes only; every tensor pointer is a DEVICE
+ * pointer owned by the caller.  Link against libfa.so.
+ *
+ * The operation (pages "把 FlashAttention 搬上昇腾：Triton-Ascend CV Pipeline
+ * 优化实战", section 一, and "Write Triton Attention Kernel", Required reasoning
+ * process steps 1-9): for every batch z < Z, query head hq < Hq with key/value
+ * head hk = hq / (Hq / Hkv), query row i < Nq,
+ *
+ *     s_ij       = scale * sum_d Q[z,hq,i,d] * K[z,hk,j,d]     for kept keys j
+ *     O[z,hq,i,:] = sum_j softmax_j(s_i.) * V[z,hk,j,:]
+ *     lse[z,hq,i] = log(sum_j exp(s_ij))                       (natural log)
+ *
+ * where the kept keys are j < Nkv, and with causal != 0 only j <= i (the
+ * top-left convention: query row i sees keys 0..i, also when Nq != Nkv).
+ * The N x N score matrix never reaches global memory: the kernel tiles over
+ * keys with the online softmax ("Build Triton-Ascend Fused Attention",
+ * Implementation Pattern), keeping the running max, denominator and output
+ * accumulator in fp32 and casting the probabilities to the input type before
+ * the P·V product.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes.  Host-side errors are returned before anything is enqueued. */
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,     /* null pointer, negative size, Hq % Hkv != 0, Nkv == 0 with work, bad scale */
+    FA_ERR_UNSUPPORTED = 2,     /* D not in {16, 32, 64, 128, 256}, dtype not fp16/bf16 */
+    FA_ERR_ALIGNMENT = 3,       /* d-stride != 1, a base or stride not 16-byte aligned, negative stride */
+    FA_ERR_CUDA = 4,            /* a CUDA runtime/driver call failed (launch, tensor map, device query) */
+    FA_ERR_DEVICE_TIMEOUT = 5   /* a bounded device-side wait ran out (see fa_device_status) */
+} fa_status;
+
+typedef enum { FA_DTYPE_F16 = 0, FA_DTYPE_BF16 = 1 } fa_dtype;
+
+/* Element strides of a BNSD tensor: batch, head, sequence, head-dim.  Every
+ * tensor carries its own strides ("Build Triton-Ascend Fused Attention",
+ * Ascend Guardrails; "Write Triton Attention Kernel", Kernel design rules), so
+ * BNSD, BSND ("BNHD") and other permuted or padded layouts are all accepted as
+ * long as d == 1 and the other strides are multiples of 8 elements. */
+typedef struct {
+    int64_t b, h, n, d;
+} fa_strides;
+
+/*
+ * fa_fwd -- enqueue the attention forward on `stream` (asynchronous).
+ *
+ *   q    (Z, Hq,  Nq,  D)  dtype, strides *sq
+ *   k    (Z, Hkv, Nkv, D)  dtype, strides *sk
+ *   v    (Z, Hkv, Nkv, D)  dtype, strides *sv
+ *   o    (Z, Hq,  Nq,  D)  dtype, strides *so   (written)
+ *   lse  (Z, Hq,  Nq)      fp32, contiguous      (written; may be NULL to skip)
+ *   scale   softmax scale, finite and > 0 (commonly 1/sqrt(D))
+ *   causal  0 or 1
+ *   dtype   FA_DTYPE_F16 or FA_DTYPE_BF16 for Q, K, V and O
+ *   stream  CUDA stream (0 = legacy default stream)
+ *
+ * Requirements: D in {16, 32, 64, 128, 256}; Hq % Hkv == 0 (GQA/MQA when
+ * Hkv < Hq); Nkv >= 1 whenever Z*Hq*Nq > 0; q, k, v, o 16-byte aligned with
+ * d-stride 1 and the other strides multiples of 8 elements (16 bytes);
+ * lse 4-byte aligned.  Any Nq, Nkv (ragged tails are masked).  Z*Hq*Nq == 0
+ * is a no-op that returns FA_OK.
+ *
+ * Ownership: the caller owns every buffer and must keep them alive until the
+ * stream reaches this work.  The library allocates no device memory per call;
+ * it keeps one 4-byte status word per device for device-side errors.
+ *
+ * Errors: argument errors return FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED /
+ * FA_ERR_ALIGNMENT synchronously and enqueue nothing; a failed launch returns
+ * FA_ERR_CUDA.  A device-side wait that runs out is reported later through
+ * fa_device_status().  No CPU fallback exists.
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int Z, int Hq, int Hkv, int Nq,
+                 int Nkv, int D, const fa_strides* sq, const fa_strides* sk, const fa_strides* sv,
+                 const fa_strides* so, float scale, int causal, fa_dtype dtype, cudaStream_t stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* fa_status_string(fa_status status);
+
+/*
+ * fa_device_status -- synchronise `stream`, then read and clear the current
+ * device's status word.  Returns FA_OK, FA_ERR_DEVICE_TIMEOUT (a bounded
+ * mbarrier wait inside a kernel gave up and the kernel exited cleanly), or
+ * FA_ERR_CUDA if the synchronisation itself failed.  When `detail` is not
+ * NULL it receives the raw word: bits 0-7 the code, 8-15 the wait site,
+ * 16-31 the CTA index that gave up first.
+ */
+fa_status fa_device_status(cudaStream_t stream, uint32_t* detail);
+
+/*
+ * fa_fwd_plan -- host-only description of the work fa_fwd would launch; no
+ * CUDA call is made.  Pass num_sms > 0 to size the persistent grid for that
+ * many SMs (0 leaves *grid at the tile count).  Outputs (each may be NULL):
+ *   tiles      query tiles of 128 rows, Z * Hq * ceil(Nq / 128)
+ *   kv_blocks  (query tile, key block) pairs the kernel visits; with causal
+ *              set the loop stops at the diagonal block (page "把 FlashAttention
+ *              搬上昇腾...", section 八: 8 x 8 tiles -> 36 visited)
+ *   block_n    keys per block for this D (128, or 64 at D = 256)
+ *   grid       CTAs launched: min(tiles, num_sms)
+ *   smem_bytes dynamic shared memory per CTA
+ * Returns the same argument errors as fa_fwd for bad shapes.
+ */
+fa_status fa_fwd_plan(int Z, int Hq, int Hkv, int Nq, int Nkv, int D, int causal, int num_sms, int64_t* tiles,
+                      int64_t* kv_blocks, int* block_n, int* grid, int* smem_bytes);
+
+/*
+ * Test hooks for the failure-detection path; not for production use.
+ *
+ * fa_debug_set_wait_limit_ms -- bound, in milliseconds, on every mbarrier wait
+ *   inside later launches (default 2000, or FA_WAIT_LIMIT_MS from the
+ *   environment; ms <= 0 restores that default).  A healthy kernel waits
+ *   microseconds; the bound only matters when something is wrong.
+ * fa_debug_inject_stall -- when enabled, CTA 0 of later launches never issues
+ *   the copy of its first K tile, so the wait for it runs out: the kernel
+ *   records FA_ERR_DEVICE_TIMEOUT (read with fa_device_status), every role of
+ *   that CTA stops, in-flight copies and MMAs land, TMEM is freed and the
+ *   kernel returns.  The other CTAs finish their tiles.  Outputs of such a
+ *   launch are incomplete.  No GPU fault, trap or hang is involved.
+ */
+void fa_debug_set_wait_limit_ms(double ms);
+void fa_debug_inject_stall(int enable);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -1,0 +1,122 @@
+"""Shared helpers for the GPU-vs-oracle parity tests.
+
+Inputs come from seeded_inputs (the same bits go to the GPU and the oracle);
+the CUDA side is called only through the libfa binding; expected values come
+only from the oracle.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+import oracle
+import seeded_inputs as si
+
+# max |ΔO| for N(0,1) inputs per dtype and max |Δlse|: the tolerances the
+# specification of this path fixes.  They absorb the kernel's fp16/bf16
+# rounding of P before P·V and of O at the store (half an ulp of |O| <= 4 is
+# 2e-3 in fp16 and 1.6e-2 in bf16) plus fp32 accumulation.
+TOL_O = {"fp16": 5e-3, "bf16": 2e-2}
+TOL_LSE = 1e-3
+
+
+def torch_dtype(dtype):
+    import torch
+    return torch.float16 if dtype == "fp16" else torch.bfloat16
+
+
+def to_device(bits: np.ndarray, dtype: str, device="cuda"):
+    return si.as_torch(bits, dtype).to(device)
+
+
+def run_gpu(q, k, v, dtype, scale, causal, layout="bnsd", o_layout="bnsd"):
+    """Run libfa on seeded bits; returns (O as float64 numpy (Z,Hq,Nq,D), lse float64 (Z,Hq,Nq))."""
+    import torch
+    from exact_attention_44_gb300 import fa_fwd
+
+    qt, kt, vt = (relayout(to_device(x, dtype), layout) for x in (q, k, v))
+    o = relayout(torch.empty(qt.shape, dtype=qt.dtype, device="cuda"), o_layout)
+    o, lse = fa_fwd(qt, kt, vt, o=o, scale=scale, causal=causal)
+    torch.cuda.synchronize()
+    return o.double().cpu().numpy(), lse.double().cpu().numpy()
+
+
+def relayout(t, layout):
+    """Same values, another memory layout: 'bnsd' (contiguous), 'bsnd' (heads
+    inside rows, i.e. (Z, N, H, D) storage), or 'padded' (row pitch D + 8)."""
+    import torch
+    if layout == "bnsd":
+        return t.contiguous()
+    Z, H, N, D = t.shape
+    if layout == "bsnd":
+        store = torch.empty((Z, N, H, D), dtype=t.dtype, device=t.device)
+        view = store.permute(0, 2, 1, 3)
+    elif layout == "padded":
+        store = torch.empty((Z, H, N, D + 8), dtype=t.dtype, device=t.device)
+        view = store[..., :D]
+    else:
+        raise ValueError(layout)
+    view.copy_(t)
+    return view
+
+
+def compare(o_gpu, lse_gpu, o_ref, lse_ref, dtype, what=""):
+    do = float(np.max(np.abs(o_gpu - o_ref))) if o_ref.size else 0.0
+    dl = float(np.max(np.abs(lse_gpu - lse_ref))) if lse_ref.size else 0.0
+    assert np.all(np.isfinite(o_gpu)) and np.all(np.isfinite(lse_gpu)), f"{what}: non-finite GPU output"
+    assert do <= TOL_O[dtype], f"{what}: max|dO| = {do:.3e} > {TOL_O[dtype]}"
+    assert dl <= TOL_LSE, f"{what}: max|dlse| = {dl:.3e} > {TOL_LSE}"
+    return do, dl
+
+
+def check_full(seed, Z, Hq, Hkv, Nq, Nkv, D, dtype, causal, scale=None, layout="bnsd", o_layout="bnsd",
+               transform=None):
+    """Every output row against the oracle."""
+    scale = 1 / math.sqrt(D) if scale is None else scale
+    q, k, v = si.qkv(seed, Z, Hq, Hkv, Nq, Nkv, D, dtype)
+    if transform is not None:
+        q, k, v = transform(q, k, v)
+    o_gpu, lse_gpu = run_gpu(q, k, v, dtype, scale, causal, layout, o_layout)
+    o_ref, lse_ref = oracle.attention_fwd(q, k, v, dtype, scale, causal)
+    return compare(o_gpu, lse_gpu, o_ref, lse_ref, dtype, f"{(Z, Hq, Hkv, Nq, Nkv, D, dtype, causal)}")
+
+
+def sample_rows(Nq, n_random, rng):
+    """Row indices of one head: tile edges (0, 127, 128, ...), the last row, and random rows."""
+    rows = {0, Nq - 1}
+    for t in range(0, Nq, 128):
+        rows.update(r for r in (t, t + 127) if r < Nq)
+    rows.update(rng.integers(0, Nq, size=n_random).tolist())
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+def check_sampled(seed, Z, Hq, Hkv, Nq, Nkv, D, dtype, causal, n_groups=2, rows_per_head=48, scale=None):
+    """Full-size run on the GPU; the oracle checks sampled rows of a few GQA groups.
+
+    For each sampled (z, kv head) the oracle gets just that group's query heads
+    and its K/V, and computes the sampled rows one by one."""
+    scale = 1 / math.sqrt(D) if scale is None else scale
+    q, k, v = si.qkv(seed, Z, Hq, Hkv, Nq, Nkv, D, dtype)
+    o_gpu, lse_gpu = run_gpu(q, k, v, dtype, scale, causal)
+    g = Hq // Hkv
+    rng = np.random.default_rng(seed + 1)
+    groups = {(0, 0), (Z - 1, Hkv - 1)}
+    while len(groups) < min(n_groups, Z * Hkv):
+        groups.add((int(rng.integers(Z)), int(rng.integers(Hkv))))
+    worst = (0.0, 0.0)
+    for z, hk in sorted(groups):
+        qs = q[z:z + 1, hk * g:(hk + 1) * g]
+        ks, vs = k[z:z + 1, hk:hk + 1], v[z:z + 1, hk:hk + 1]
+        heads = sorted({0, g - 1} | {int(rng.integers(g))})
+        rows, flat = [], []
+        for h in heads:
+            r = sample_rows(Nq, rows_per_head, rng)
+            rows.append((h, r))
+            flat.append(h * Nq + r)
+        o_ref, lse_ref = oracle.attention_fwd(qs, ks, vs, dtype, scale, causal, rows=np.concatenate(flat))
+        og = np.concatenate([o_gpu[z, hk * g + h, r] for h, r in rows])
+        lg = np.concatenate([lse_gpu[z, hk * g + h, r] for h, r in rows])
+        d = compare(og, lg, o_ref, lse_ref, dtype, f"z={z} hk={hk} {(Z, Hq, Hkv, Nq, Nkv, D, dtype, causal)}")
+        worst = (max(worst[0], d[0]), max(worst[1], d[1]))
+    return worst

@@ -1,0 +1,148 @@
+"""GPU parity: libfa against the fp64 oracle, element by element, on small and
+ragged shapes that span several tiles, every head dim and dtype, both masks,
+GQA groupings, strided layouts, and the failure modes the pages list
+("Write Triton Attention Kernel", Common failure modes)."""
+import math
+
+import numpy as np
+import pytest
+
+import seeded_inputs as si
+from parity_util import check_full, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+DIMS = [16, 32, 64, 128, 256]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import exact_attention_44_gb300 as fa
+    fa.build()
+    fa.load()
+
+
+@pytest.mark.parametrize("D", DIMS)
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_head_dims(D, dtype, causal):
+    check_full(1, 1, 2, 2, 300, 300, D, dtype, causal)
+
+
+@pytest.mark.parametrize("Nq,Nkv", [(1, 1), (1, 300), (127, 127), (129, 129), (128, 1), (200, 77), (77, 200),
+                                    (1000, 1000), (256, 1024), (1024, 256)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_ragged_lengths(Nq, Nkv, causal):
+    # tails on either side; causal with Nq != Nkv keeps the top-left convention
+    check_full(2, 1, 2, 1, Nq, Nkv, 64, "fp16", causal)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(1, 1), (2, 1), (4, 1), (8, 2), (8, 8), (32, 1), (32, 8)])
+def test_gqa_groupings(Hq, Hkv):
+    # distinct K/V per kv head: a wrong head stride reads another head's keys
+    check_full(3, 2, Hq, Hkv, 130, 260, 32, "bf16", True)
+
+
+@pytest.mark.parametrize("layout,o_layout", [("bsnd", "bnsd"), ("bnsd", "bsnd"), ("padded", "padded"),
+                                             ("bsnd", "bsnd")])
+@pytest.mark.parametrize("D", [64, 128])
+def test_strided_layouts(layout, o_layout, D):
+    check_full(4, 2, 4, 2, 200, 300, D, "fp16", False, layout=layout, o_layout=o_layout)
+    check_full(4, 2, 4, 2, 200, 300, D, "bf16", True, layout=layout, o_layout=o_layout)
+
+
+def test_growing_block_maxima_need_rescaling():
+    # later key blocks score higher, so the running max moves at every block:
+    # a missing alpha rescale of O or l is caught here
+    def grow(q, k, v):
+        kd = (k.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        ramp = np.linspace(0.2, 3.0, k.shape[2])[None, None, :, None]
+        return q, si.round_bits(kd * ramp, "bf16"), v
+    check_full(5, 1, 2, 2, 256, 1024, 64, "bf16", False, transform=grow)
+
+
+def test_future_keys_score_high_under_causal():
+    # keys after the query score far above the past ones: masking after the
+    # row max (instead of before) would shift the softmax
+    def future_heavy(q, k, v):
+        kd = q[:, :, : k.shape[2]].view(np.float16).astype(np.float64) * 0.5
+        kd = kd * np.linspace(0.1, 4.0, k.shape[2])[None, None, :, None]
+        return q, si.round_bits(kd, "fp16"), v
+    check_full(6, 1, 2, 2, 384, 384, 64, "fp16", True, transform=future_heavy)
+
+
+def test_unscaled_scores_of_magnitude_d():
+    # scale 1: scores of size ~D stay exact in the fp32 state
+    check_full(7, 1, 2, 1, 256, 512, 128, "bf16", False, scale=1.0)
+    check_full(7, 1, 2, 1, 256, 512, 128, "fp16", True, scale=0.5)
+
+
+def test_tiny_scale_gives_mean_of_values():
+    check_full(8, 1, 1, 1, 130, 390, 64, "fp16", False, scale=1e-6)
+
+
+def test_identical_rows_in_both_dtypes_and_lse_optional():
+    import torch
+    from exact_attention_44_gb300 import fa_fwd
+    q, k, v = si.qkv(9, 1, 4, 4, 256, 256, 64, "bf16")
+    qt, kt, vt = (si.as_torch(x, "bf16").cuda() for x in (q, k, v))
+    o1, lse1 = fa_fwd(qt, kt, vt, causal=True)
+    o2, lse2 = fa_fwd(qt, kt, vt, causal=True, want_lse=False)
+    torch.cuda.synchronize()
+    assert lse2 is None
+    assert torch.equal(o1, o2)
+
+
+def test_deterministic_bitwise():
+    import torch
+    from exact_attention_44_gb300 import fa_fwd
+    q, k, v = si.qkv(10, 2, 8, 2, 1000, 1000, 128, "bf16")
+    qt, kt, vt = (si.as_torch(x, "bf16").cuda() for x in (q, k, v))
+    outs = [fa_fwd(qt, kt, vt, causal=c) for c in (True, True, False, False)]
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    assert torch.equal(outs[2][0], outs[3][0]) and torch.equal(outs[2][1], outs[3][1])
+
+
+def test_empty_problems_are_noops():
+    import torch
+    from exact_attention_44_gb300 import fa_fwd
+    q = torch.empty(0, 2, 64, 64, dtype=torch.float16, device="cuda")
+    o, lse = fa_fwd(q, q[:, :1], q[:, :1])
+    assert o.shape == q.shape and lse.shape == (0, 2, 64)
+    q = torch.empty(1, 2, 0, 64, dtype=torch.float16, device="cuda")
+    k = torch.randn(1, 2, 5, 64, dtype=torch.float16, device="cuda")
+    fa_fwd(q, k, k)
+    torch.cuda.synchronize()
+
+
+def test_device_status_is_clean_after_normal_runs():
+    from exact_attention_44_gb300 import fa_device_status, fa_fwd
+    q, k, v = si.qkv(11, 1, 2, 1, 300, 300, 64, "fp16")
+    fa_fwd(*(si.as_torch(x, "fp16").cuda() for x in (q, k, v)), causal=True)
+    code, word = fa_device_status()
+    assert code == 0 and word == 0
+
+
+def test_misaligned_views_are_rejected_not_computed():
+    import torch
+    from exact_attention_44_gb300 import FA_ERR_ALIGNMENT, FaError, fa_fwd
+    base = torch.zeros(1, 1, 64, 72, dtype=torch.float16, device="cuda")
+    q = base[..., 4:68]  # 8-byte offset: not 16-byte aligned
+    with pytest.raises(FaError) as e:
+        fa_fwd(q, q, q)
+    assert e.value.code == FA_ERR_ALIGNMENT
+
+
+def test_output_matches_torch_sdpa_as_a_second_opinion():
+    # not the oracle: PyTorch's own attention in fp32 on the same inputs, as a
+    # sanity cross-check of the harness (tolerance of the oracle comparison)
+    import torch
+    q, k, v = si.qkv(12, 2, 4, 4, 333, 333, 64, "fp16")
+    o, lse = run_gpu(q, k, v, "fp16", 0.125, True)
+    qt, kt, vt = (si.as_torch(x, "fp16").float() for x in (q, k, v))
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, is_causal=True, scale=0.125)
+    assert np.max(np.abs(o - ref.double().numpy())) < 5e-3
+    s = (qt @ kt.transpose(-1, -2)) * 0.125
+    s = s.masked_fill(torch.ones(333, 333, dtype=torch.bool).triu(1), float("-inf"))
+    assert np.max(np.abs(lse - torch.logsumexp(s, -1).double().numpy())) < 1e-3
