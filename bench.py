@@ -1,0 +1,492 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused attention forward (libfa) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+
+One step = one pass of the whole path over one batch of the workload
+"Z=4 Hq=Hkv=16 Nq=Nkv=1024 D=128 bf16, non-causal and causal": two fa_fwd
+launches on the same inputs.  Metric: attention forward TFLOP/s, counting
+4*Nq*Nkv*D per head and half of it for causal.  Inputs are seeded synthetic
+N(0,1) (seeded_inputs); several input sets rotate so that consecutive steps
+never find their operands in L2.  Rank 0 prints one JSON line.
+
+--impl reference times the fp64 CPU oracle on the host cores instead, on a
+bounded sample of the same workload (rows computed one by one).
+N > 1 runs one independent replica per GPU ("replicas only": the path needs
+no exchange between GPUs); value = all ranks' FLOPs / max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOPS (causal-halved) and % of GB300 dense bf16/fp16 peak"
+L2_BYTES = 129 * 2 ** 20
+
+WORKLOADS = {
+    # name: (Z, Hq, Hkv, Nq, Nkv, D, dtype, [causal flags per step])
+    "z4_h16_n1024_d128_bf16": (4, 16, 16, 1024, 1024, 128, "bf16", [False, True]),
+    "z1_hq32_hkv8_nq1024_nkv8192_d128_bf16_cross": (1, 32, 8, 1024, 8192, 128, "bf16", [False]),
+    "z1_hq32_hkv8_n8192_d128_bf16_noncausal": (1, 32, 8, 8192, 8192, 128, "bf16", [False]),
+    "z1_hq32_hkv8_n32768_d128_bf16_causal": (1, 32, 8, 32768, 32768, 128, "bf16", [True]),
+    "z128_h8_n1024_d128_fp16": (128, 8, 8, 1024, 1024, 128, "fp16", [False, True]),
+    "z128_h8_n1024_d64_fp16": (128, 8, 8, 1024, 1024, 64, "fp16", [False, True]),
+    "z8_h16_n2048_d16_fp16": (8, 16, 16, 2048, 2048, 16, "fp16", [False, True]),
+    "z8_h16_n2048_d32_fp16": (8, 16, 16, 2048, 2048, 32, "fp16", [False, True]),
+    "z8_h16_n2048_d64_fp16": (8, 16, 16, 2048, 2048, 64, "fp16", [False, True]),
+    "z8_h16_n2048_d128_bf16": (8, 16, 16, 2048, 2048, 128, "bf16", [False, True]),
+    "z8_h16_n2048_d256_bf16": (8, 16, 16, 2048, 2048, 256, "bf16", [False, True]),
+    "z1_h2_n128_d64_fp16_tiny": (1, 2, 2, 128, 128, 64, "fp16", [False]),
+}
+MAIN = "z4_h16_n1024_d128_bf16"
+# the shapes the throughput target is stated on (D = 128, N >= 4096, non-causal)
+TARGET_SHAPES = ["z1_hq32_hkv8_n8192_d128_bf16_noncausal", "z1_hq32_hkv8_nq1024_nkv8192_d128_bf16_cross"]
+
+
+def flops_of(Z, Hq, Nq, Nkv, D, causal) -> float:
+    f = 4.0 * Z * Hq * Nq * Nkv * D
+    return f / 2 if causal else f
+
+
+def step_flops(wl) -> float:
+    Z, Hq, Hkv, Nq, Nkv, D, dtype, flags = wl
+    return sum(flops_of(Z, Hq, Nq, Nkv, D, c) for c in flags)
+
+
+def io_bytes(wl):
+    Z, Hq, Hkv, Nq, Nkv, D, dtype, flags = wl
+    qkv = 2 * (Z * Hq * Nq * D + 2 * Z * Hkv * Nkv * D)
+    out = len(flags) * (2 * Z * Hq * Nq * D + 4 * Z * Hq * Nq)
+    return qkv, out
+
+
+def algorithmic_bytes(wl) -> int:
+    """Read Q, K, V once and write O and lse once (per launch)."""
+    Z, Hq, Hkv, Nq, Nkv, D, dtype, flags = wl
+    return 2 * (2 * Z * Hq * Nq * D + 2 * Z * Hkv * Nkv * D) + 4 * Z * Hq * Nq
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"bf16_tflops": d["bf16_tflops"], "bf16_tflops_sustained": d.get("bf16_tflops_sustained"),
+                "hbm_gbs": d["hbm_gbs"], "source": "measured"}
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for d in (os.path.join(ROOT, "exact_attention_44_gb300", "csrc"), os.path.join(ROOT, "include")):
+        for name in sorted(os.listdir(d)):
+            if name.endswith((".cu", ".cuh", ".h")):
+                h.update(name.encode() + b"\0" + open(os.path.join(d, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        rec = json.load(open(p)).get(kernel)
+    except Exception:
+        return None
+    if not rec or rec.get("source_hash") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks --
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu_index = gpu_index
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power)}
+
+
+# ------------------------------------------------------------------ native --
+
+def make_inputs(wl, seed, device):
+    import torch
+
+    import seeded_inputs as si
+    Z, Hq, Hkv, Nq, Nkv, D, dtype, flags = wl
+    q, k, v = si.qkv(seed, Z, Hq, Hkv, Nq, Nkv, D, dtype)
+    host = [si.as_torch(x, dtype).pin_memory() for x in (q, k, v)]
+    return host, [h.to(device) for h in host]
+
+
+def run_native(args, rank, world, device):
+    import torch
+
+    import exact_attention_44_gb300 as fa
+
+    fa.build()
+    fa.load()
+    peaks = load_peaks()
+    wl = WORKLOADS[args.workload]
+    Z, Hq, Hkv, Nq, Nkv, D, dtype, flags = wl
+    scale = 1.0 / math.sqrt(D)
+    tdt = torch.float16 if dtype == "fp16" else torch.bfloat16
+    stream = torch.cuda.current_stream(device)
+
+    # rotating input sets: their total is > 3x L2, so a step never reuses the previous step's operands in L2
+    per_set = sum(io_bytes(wl))
+    nsets = max(2, min(8, math.ceil(3 * L2_BYTES / per_set)))
+    host, dev0 = make_inputs(wl, 0, device)
+    sets = [dev0] + [[x.clone() for x in dev0] for _ in range(nsets - 1)]
+    outs = [[(torch.empty((Z, Hq, Nq, D), dtype=tdt, device=device),
+              torch.empty((Z, Hq, Nq), dtype=torch.float32, device=device)) for _ in flags] for _ in range(nsets)]
+
+    def step(i, evs=None):
+        q, k, v = sets[i % nsets]
+        for f, causal in enumerate(flags):
+            if evs is not None:
+                evs[f].record(stream)
+            o, lse = outs[i % nsets][f]
+            fa.fa_fwd(q, k, v, o=o, lse=lse, scale=scale, causal=causal, stream=stream)
+        if evs is not None:
+            evs[len(flags)].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(device)
+    code, word = fa.fa_device_status(stream)
+    if code != fa.FA_OK:
+        raise RuntimeError(f"device status after warm-up: {word:#x}")
+    barrier(world)
+    clocks = ClockSampler(device.index if device.index is not None else 0) if rank == 0 else None
+    time.sleep(0.25 if clocks else 0)
+    torch.cuda.synchronize(device)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(flags) + 1)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        step(i, ev[i])
+    torch.cuda.synchronize(device)
+    clock = clocks.stop() if clocks else None
+    barrier(world)
+    total_ms = ev[0][0].elapsed_time(ev[-1][-1])
+    per_kernel_ms = [[e[f].elapsed_time(e[f + 1]) for e in ev] for f in range(len(flags))]
+    code, word = fa.fa_device_status(stream)
+    if code != fa.FA_OK:
+        raise RuntimeError(f"device status after timing: {word:#x}")
+    max_ms = all_reduce_max(total_ms, world, device)
+
+    flops = step_flops(wl)
+    value = world * flops * args.steps / (max_ms * 1e-3) / 1e12
+
+    # dominant kernel: the launch kind with the largest share of the step
+    shares = [sum(x) for x in per_kernel_ms]
+    dom = max(range(len(flags)), key=lambda f: shares[f])
+    dom_ms = statistics.fmean(per_kernel_ms[dom])
+    dom_flops = flops_of(Z, Hq, Nq, Nkv, D, flags[dom])
+    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
+    kname = f"fa_fwd_kernel<{D},{str(flags[dom]).lower()},{'bf16' if dtype == 'bf16' else 'fp16'}>"
+    roofline = {"bound": "tensor", "kernel": kname, "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                "peak_source": f"{peaks['source']} bf16 burst (cuBLAS)",
+                "frac_of_sustained": (round(achieved / peaks["bf16_tflops_sustained"], 4)
+                                      if peaks.get("bf16_tflops_sustained") else None),
+                "traffic": recorded_traffic(kname),
+                "algorithmic_bytes": algorithmic_bytes(wl), "ms_per_launch": round(dom_ms, 5)}
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": "synthetic (seeded N(0,1))",
+        "config": {"workload": args.workload, "Z": Z, "Hq": Hq, "Hkv": Hkv, "Nq": Nq, "Nkv": Nkv, "D": D,
+                   "causal_per_step": flags, "scale": scale, "layout": "BNSD contiguous",
+                   "l2": f"{nsets} rotating input sets ({nsets * per_set / 2**20:.0f} MiB > 3x L2)",
+                   "parallelism": "replicas only" if world > 1 else "single GPU"},
+        "frac_of_peak": round(value / world / peaks["bf16_tflops"], 4),
+        "per_launch_ms": {f"causal={c}": round(statistics.fmean(per_kernel_ms[f]), 5) for f, c in enumerate(flags)},
+        "roofline": roofline,
+        "gpu_launches": len(flags) * args.steps,
+        "clocks": clock,
+    }
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(args, wl, host, flags, scale, device, stream, world)
+    if args.shapes and rank == 0:
+        result["target_shapes"] = [measure_shape(name, device, stream, peaks) for name in TARGET_SHAPES]
+    return result
+
+
+def run_e2e(args, wl, host, flags, scale, device, stream, world):
+    """Same metric through the public API with host buffers: H2D of Q/K/V from pinned memory,
+    both launches, D2H of O and lse, every step, all inside the timed region."""
+    import torch
+
+    import exact_attention_44_gb300 as fa
+    Z, Hq, Hkv, Nq, Nkv, D, dtype, _ = wl
+    tdt = host[0].dtype
+    dq, dk, dv = (torch.empty_like(h, device=device) for h in host)
+    outs = [(torch.empty((Z, Hq, Nq, D), dtype=tdt, device=device),
+             torch.empty((Z, Hq, Nq), dtype=torch.float32, device=device)) for _ in flags]
+    host_out = [(torch.empty((Z, Hq, Nq, D), dtype=tdt).pin_memory(),
+                 torch.empty((Z, Hq, Nq), dtype=torch.float32).pin_memory()) for _ in flags]
+    steps = max(3, min(args.steps, 50))
+
+    def step():
+        for d, h in zip((dq, dk, dv), host):
+            d.copy_(h, non_blocking=True)
+        for (o, lse), causal in zip(outs, flags):
+            fa.fa_fwd(dq, dk, dv, o=o, lse=lse, scale=scale, causal=causal, stream=stream)
+        for (o, lse), (ho, hl) in zip(outs, host_out):
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(device)
+    barrier(world)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(device)
+    ms = all_reduce_max(a.elapsed_time(b), world, device)
+    h2d, d2h = io_bytes(wl)
+    return {"value": round(world * step_flops(wl) * steps / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "ms_per_step": round(ms / steps, 4)}
+
+
+def measure_shape(name, device, stream, peaks, steps=10):
+    """TFLOP/s of one extra workload (same timing method, 10 steps, inputs > L2 or rotated)."""
+    import torch
+
+    import exact_attention_44_gb300 as fa
+    wl = WORKLOADS[name]
+    Z, Hq, Hkv, Nq, Nkv, D, dtype, flags = wl
+    scale = 1.0 / math.sqrt(D)
+    per_set = sum(io_bytes(wl))
+    nsets = max(1, min(6, math.ceil(3 * L2_BYTES / per_set)))
+    _, dev0 = make_inputs(wl, 0, device)
+    sets = [dev0] + [[x.clone() for x in dev0] for _ in range(nsets - 1)]
+    o = torch.empty((Z, Hq, Nq, D), dtype=dev0[0].dtype, device=device)
+    lse = torch.empty((Z, Hq, Nq), dtype=torch.float32, device=device)
+    for i in range(3):
+        for c in flags:
+            fa.fa_fwd(*sets[i % nsets], o=o, lse=lse, scale=scale, causal=c, stream=stream)
+    torch.cuda.synchronize(device)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(steps):
+        for c in flags:
+            fa.fa_fwd(*sets[i % nsets], o=o, lse=lse, scale=scale, causal=c, stream=stream)
+    b.record(stream)
+    torch.cuda.synchronize(device)
+    ms = a.elapsed_time(b) / steps
+    tf = step_flops(wl) / (ms * 1e-3) / 1e12
+    del sets, dev0
+    torch.cuda.empty_cache()
+    return {"workload": name, "tflops": round(tf, 2), "frac_of_peak": round(tf / peaks["bf16_tflops"], 4),
+            "ms_per_step": round(ms, 4), "steps": steps}
+
+
+# ------------------------------------------------------------------ oracle --
+
+def run_oracle_sample(wl, budget_s: float):
+    """Time the fp64 CPU oracle on rows of the workload, growing the sample until ~budget_s."""
+    import numpy as np
+
+    import oracle
+    import seeded_inputs as si
+    Z, Hq, Hkv, Nq, Nkv, D, dtype, flags = wl
+    scale = 1.0 / math.sqrt(D)
+    # one GQA group of (z = 0, kv head 0): its query heads and K/V
+    g = Hq // Hkv
+    nq = g * Nq * D
+    q = si.normals(0, 0, nq, dtype).reshape(1, g, Nq, D)  # BNSD: the first g heads of z = 0
+    k = si.normals(0, Z * Hq * Nq * D, Nkv * D, dtype).reshape(1, 1, Nkv, D)
+    v = si.normals(0, Z * Hq * Nq * D + Z * Hkv * Nkv * D, Nkv * D, dtype).reshape(1, 1, Nkv, D)
+    threads = oracle.host_threads()
+    rng = np.random.default_rng(0)
+    rows_n, elapsed, done_flops = 16, 0.0, 0.0
+    total_rows = 0
+    while True:
+        rows = np.sort(rng.integers(0, g * Nq, size=rows_n)).astype(np.int64)
+        f = 0.0
+        for c in flags:
+            kept = (rows % Nq + 1).clip(max=Nkv) if c else np.full(rows.shape, Nkv)
+            f += float(np.sum(4.0 * kept * D))
+        t0 = time.perf_counter()
+        for c in flags:
+            oracle.attention_fwd(q, k, v, dtype, scale, c, rows=rows, nthreads=threads)
+        dt = time.perf_counter() - t0
+        elapsed += dt
+        done_flops += f
+        total_rows += rows_n
+        if elapsed >= budget_s or dt > budget_s / 3:
+            break
+        rows_n *= 2
+    return {"value": done_flops / elapsed / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{total_rows} query rows of (z=0, kv head 0) of {WORKLOADS_NAME(wl)}, each for "
+                      f"{'+'.join('causal' if c else 'non-causal' for c in flags)}, fp64, {elapsed:.1f} s"}
+
+
+def WORKLOADS_NAME(wl):
+    for k, v in WORKLOADS.items():
+        if v == wl:
+            return k
+    return "workload"
+
+
+def run_reference(args, rank, world):
+    wl = WORKLOADS[args.workload]
+    Z, Hq, Hkv, Nq, Nkv, D, dtype, flags = wl
+    times, values = [], []
+    budget = max(0.05, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    for i in range(args.warmup):
+        run_oracle_sample(wl, budget / 4)
+    info = None
+    for i in range(args.steps):
+        info = run_oracle_sample(wl, budget)
+        values.append(info["value"])
+    value = statistics.fmean(values)
+    ms_per_step = step_flops(wl) / (value * 1e12) * 1e3  # time the oracle would take for one whole step
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1))",
+            "config": {"workload": args.workload, "Z": Z, "Hq": Hq, "Hkv": Hkv, "Nq": Nq, "Nkv": Nkv, "D": D,
+                       "causal_per_step": flags, "parallelism": "host cores"},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": info["cores"], "kind": "oracle",
+                             "sample": info["sample"]},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+# ------------------------------------------------------------------ dist ----
+
+def init_dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if _cuda_ok() else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def _cuda_ok():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def all_reduce_max(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=MAIN)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--shapes", dest="shapes", action="store_true", default=True,
+                    help="also time the D=128, N>=4096 non-causal target shapes (default)")
+    ap.add_argument("--no-shapes", dest="shapes", action="store_false")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "native":
+        ap.error("--warmup must be >= 3")
+    rank, world, local = init_dist()
+    if args.gpus != world and world > 1:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return 0
+
+    import torch
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the native path has no CPU fallback)")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    result = run_native(args, rank, world, device)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            result["cpu_baseline"] = run_oracle_sample(WORKLOADS[args.workload], args.cpu_budget)
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
