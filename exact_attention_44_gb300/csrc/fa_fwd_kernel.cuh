@@ -14,10 +14,16 @@
 //   * warp 0 (one lane) streams Q once per tile and K_j, V_j per key block by
 //     TMA into swizzled shared-memory rings guarded by full/empty mbarriers;
 //   * warp 1 (one lane) issues S_j = Q K_jᵀ into a double-buffered S in TMEM
-//     and O += P_j V_j with P_j read from TMEM, committing to mbarriers;
+//     and O += P_j V_j with P_j read from TMEM (double-buffered), committing
+//     each to mbarriers; S_{j+1} runs on the tensor cores while the softmax
+//     works on S_j;
 //   * warps 2-5 (128 threads, thread = query row = TMEM lane) run the online
-//     softmax: mask (diagonal/tail blocks only), row max, exp2, row sum,
-//     P -> fp16/bf16 into TMEM, rescale O when the max moved, and the epilogue
+//     softmax: mask (diagonal and tail blocks only), row max, exp2, row sum,
+//     P -> fp16/bf16 into TMEM; O is rescaled in TMEM only when a row maximum
+//     grows by more than 2^RESCALE_LOG2 (below that the stale maximum keeps
+//     every p <= 2^RESCALE_LOG2, and O / l and lse are unchanged);
+//   * warps 6-9 run the epilogue of the previous tile while the softmax warps
+//     start the next one: read O out of TMEM, release it to the MMA warp, then
 //     O / l -> global and lse = (m + log2 l)·ln 2.
 // Every mbarrier wait is bounded; on expiry the CTA records the site in the
 // status word, stops every role, lets its copies and MMAs land and frees TMEM.
@@ -30,6 +36,11 @@
 #include "fa_ptx.cuh"
 
 namespace fa {
+
+// A row maximum (in log2 units of the scaled score) may run ahead of the one
+// the probabilities are referenced to by at most this much before O and l
+// are rescaled: probabilities stay <= 2^8 = 256, exact in fp16/bf16 range.
+constexpr float RESCALE_LOG2 = 8.0f;
 
 template <int D_>
 struct Traits {
@@ -54,7 +65,8 @@ struct Traits {
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + Q_STAGES * Q_BYTES;
     static constexpr int OFF_V = OFF_K + K_STAGES * KV_BYTES;
-    static constexpr int OFF_BAR = OFF_V + V_STAGES * KV_BYTES;
+    static constexpr int OFF_HAND = OFF_V + V_STAGES * KV_BYTES;  // softmax -> epilogue: m, l per row, 2 slots
+    static constexpr int OFF_BAR = OFF_HAND + 2 * 2 * BM * 4;
     // barrier indices
     static constexpr int B_QFULL = 0;
     static constexpr int B_QEMPTY = B_QFULL + Q_STAGES;
@@ -62,16 +74,25 @@ struct Traits {
     static constexpr int B_KEMPTY = B_KFULL + K_STAGES;
     static constexpr int B_VFULL = B_KEMPTY + K_STAGES;
     static constexpr int B_VEMPTY = B_VFULL + V_STAGES;
-    static constexpr int B_SFULL = B_VEMPTY + V_STAGES;        // 2
-    static constexpr int B_PFULL = B_SFULL + 2;                // 2
-    static constexpr int B_PVDONE = B_PFULL + 2;               // 1
-    static constexpr int B_DRAIN = B_PVDONE + 1;               // 1
+    static constexpr int B_SFULL = B_VEMPTY + V_STAGES;        // [2] S_g ready (commit)
+    static constexpr int B_PFULL = B_SFULL + 2;                // [2] P_g written (128 softmax threads)
+    static constexpr int B_PVDONE = B_PFULL + 2;               // [2] O += P_g V_g complete (commit)
+    static constexpr int B_EPIFULL = B_PVDONE + 2;             // [2] m, l of a tile handed over (128)
+    static constexpr int B_EPIEMPTY = B_EPIFULL + 2;           // [2] hand-over slot read (128)
+    static constexpr int B_OFREE = B_EPIEMPTY + 2;             // O read out of TMEM (128)
+    static constexpr int B_DRAIN = B_OFREE + 1;                // MMA teardown
     static constexpr int NUM_BARS = B_DRAIN + 1;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;    // tmem base, abort flag
     static constexpr int SMEM_USED = OFF_MISC + 16;
     // >= 120 KB keeps one CTA per SM, so no CTA ever waits on another's TMEM
     static constexpr int SMEM_BYTES = (SMEM_USED + 1024) > 120 * 1024 ? SMEM_USED + 1024 : 120 * 1024;
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+
+    static __device__ __forceinline__ uint32_t bar_count(int i) {
+        if (i >= B_PFULL && i < B_PFULL + 2) return 128;
+        if (i >= B_EPIFULL && i < B_OFREE + 1) return 128;
+        return 1;
+    }
 };
 
 struct Ctl {
@@ -220,9 +241,9 @@ __device__ void run_mma(const FwdParams& p, uint32_t sbase, uint32_t bar0, uint3
     constexpr uint32_t IDESC_PV = ptx::idesc_f16(BM, D, BF16, false, true);       // V is MN-major (D contiguous)
     constexpr uint32_t KMAJ_SBO = 8 * T::SW;                  // 8-row swizzle atom
     constexpr uint32_t V_LBO = T::BN * T::SW;                 // next 64/32/16-column chunk of V
-    uint32_t qi = 0, ki = 0, vi = 0, qk_step = 0, pv_step = 0;
+    uint32_t qi = 0, ki = 0, vi = 0, qk_step = 0, pv_step = 0, ntile = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < p.ntiles; t += gridDim.x) {
+    for (int t = blockIdx.x; ok && t < p.ntiles; t += gridDim.x, ++ntile) {
         const TileInfo ti = tile_info<CAUSAL, T::BN>(t, p);
         const uint32_t qs = qi % T::Q_STAGES;
         if (!wait_phase(bar(T::B_QFULL + qs), (qi / T::Q_STAGES) & 1u, ctl, SITE_Q_FULL)) { ok = false; break; }
@@ -260,7 +281,10 @@ __device__ void run_mma(const FwdParams& p, uint32_t sbase, uint32_t bar0, uint3
         for (int j = 0; j < ti.nkv; ++j) {
             // the next score block runs on the tensor cores while softmax works on this one
             if (j + 1 < ti.nkv && !issue_qk(j + 1)) { ok = false; break; }
-            // O += P_j V_j  (step 5h), accumulating into O from the second block on
+            // O += P_j V_j  (step 5h); the first block of a tile overwrites O,
+            // once the epilogue has read the previous tile's O out of TMEM
+            if (j == 0 && ntile > 0 &&
+                !wait_phase(bar(T::B_OFREE), (ntile - 1) & 1u, ctl, SITE_O_FREE)) { ok = false; break; }
             const uint32_t b = pv_step & 1u;
             if (!wait_phase(bar(T::B_PFULL + b), (pv_step >> 1) & 1u, ctl, SITE_P_FULL)) { ok = false; break; }
             const uint32_t vs = vi % T::V_STAGES;
@@ -274,7 +298,7 @@ __device__ void run_mma(const FwdParams& p, uint32_t sbase, uint32_t bar0, uint3
                             (j > 0 || kk > 0) ? 1u : 0u);
             }
             ptx::tc_commit(bar(T::B_VEMPTY + vs));
-            ptx::tc_commit(bar(T::B_PVDONE));
+            ptx::tc_commit(bar(T::B_PVDONE + b));
             ++vi;
             ++pv_step;
         }
@@ -298,8 +322,37 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     }
 }
 
+// O[row, :] *= alpha for the rows of this warp's lane quadrant
+template <int D>
+__device__ __forceinline__ void rescale_o(uint32_t taddr, float alpha) {
+    const uint64_t a2 = ptx::pack_f32x2(alpha, alpha);
+    if constexpr (D >= 32) {
+#pragma unroll
+        for (int i = 0; i < D / 32; ++i) {
+            uint32_t r[32];
+            ptx::tmem_ld32(taddr + 32 * i, r);
+#pragma unroll
+            for (int x = 0; x < 16; ++x) {
+                float lo, hi;
+                ptx::unpack_f32x2(ptx::fmul2(ptx::pack_f32x2(__uint_as_float(r[2 * x]), __uint_as_float(r[2 * x + 1])),
+                                             a2),
+                                  lo, hi);
+                r[2 * x] = __float_as_uint(lo);
+                r[2 * x + 1] = __float_as_uint(hi);
+            }
+            ptx::tmem_st32(taddr + 32 * i, r);
+        }
+    } else {
+        uint32_t r[16];
+        ptx::tmem_ld16(taddr, r);
+#pragma unroll
+        for (int x = 0; x < 16; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * alpha);
+        ptx::tmem_st16(taddr, r);
+    }
+}
+
 template <int D, bool CAUSAL, bool BF16>
-__device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, const Ctl& ctl) {
+__device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, float* hand, const Ctl& ctl) {
     using T = Traits<D>;
     constexpr int BN = T::BN;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
@@ -307,9 +360,10 @@ __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, co
     const int row = quad * 32 + threadIdx.x % 32;
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
     const float c = p.scale_log2;
-    uint32_t step = 0, pv_waits = 0;
+    const uint64_t c2 = ptx::pack_f32x2(c, c);
+    uint32_t step = 0, ntile = 0;
 
-    for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
+    for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++ntile) {
         const TileInfo ti = tile_info<CAUSAL, BN>(t, p);
         const int q_row = ti.q_start + row;
         // running max (log2 units of the scaled score) and denominator, fp32
@@ -337,105 +391,124 @@ __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, co
                 for (int x = 0; x < BN; ++x)
                     if (k0 + x > kmax) s[x] = -INFINITY;
             }
-            float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+            float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]);
 #pragma unroll
-            for (int x = 4; x < BN; x += 4) {
-                mx0 = fmaxf(mx0, s[x]);
-                mx1 = fmaxf(mx1, s[x + 1]);
-                mx2 = fmaxf(mx2, s[x + 2]);
-                mx3 = fmaxf(mx3, s[x + 3]);
+            for (int x = 4; x < BN; x += 4) {  // BN is a multiple of 4
+                mx0 = ptx::fmax3(mx0, s[x], s[x + 1]);
+                mx1 = ptx::fmax3(mx1, s[x + 2], s[x + 3]);
             }
-            const float m_new = fmaxf(m, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c);
-            const float alpha = ptx::ex2(m - m_new);  // 0 on the first block (m = -inf)
-            const float neg = -m_new;
-            // p = 2^(s·scale·log2e − m); l sums the fp32 p, P V uses p cast to the input type
-            uint32_t pk[BN / 2];
-            float sum0 = 0.f, sum1 = 0.f;
-#pragma unroll
-            for (int x = 0; x < BN / 2; ++x) {
-                const float p0 = ptx::ex2(fmaf(s[2 * x], c, neg));
-                const float p1 = ptx::ex2(fmaf(s[2 * x + 1], c, neg));
-                sum0 += p0;
-                sum1 += p1;
-                pk[x] = pack2<BF16>(p0, p1);
+            const float m_tile = fmaxf(mx0, mx1) * c;  // scale > 0: max commutes with the scaling
+            float alpha = 1.f;
+            bool rescale = false;
+            if (j == 0) {
+                m = m_tile;
+            } else if (__any_sync(0xffffffffu, m_tile > m + RESCALE_LOG2)) {
+                const float m_new = fmaxf(m, m_tile);
+                alpha = ptx::ex2(m - m_new);
+                m = m_new;
+                rescale = true;
             }
-            if (j > 0) {
-                // PV of the previous block is complete: O is stable, and P[b]
-                // (read two blocks ago) is free.  Rescale O by alpha before the
-                // next block is added to it (Kernel design rules).
-                if (!warp_wait_phase(bar(T::B_PVDONE), pv_waits & 1u, ctl, SITE_PV_DONE)) return;
-                ++pv_waits;
-                ptx::tc_fence_after();
-                if (__any_sync(0xffffffffu, alpha != 1.f)) {
-                    if constexpr (D >= 32) {
-#pragma unroll
-                        for (int i = 0; i < D / 32; ++i) {
-                            uint32_t r[32];
-                            const uint32_t a = tmem + lane_addr + T::TM_O + 32 * i;
-                            ptx::tmem_ld32(a, r);
-#pragma unroll
-                            for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * alpha);
-                            ptx::tmem_st32(a, r);
-                        }
-                    } else {
-                        uint32_t r[16];
-                        const uint32_t a = tmem + lane_addr + T::TM_O;
-                        ptx::tmem_ld16(a, r);
-#pragma unroll
-                        for (int x = 0; x < 16; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * alpha);
-                        ptx::tmem_st16(a, r);
-                    }
-                }
-            }
+            // p = 2^(s·scale·log2e − m); l sums the fp32 p, P V uses p cast to
+            // the input type.  P[b] was last read by the P·V of two blocks ago,
+            // which completed before S_j did (committed in issue order), so it
+            // is free; it is written 64 columns at a time as they are produced.
+            const uint64_t negm2 = ptx::pack_f32x2(-m, -m);
+            uint64_t sum2 = ptx::pack_f32x2(0.f, 0.f);
 #pragma unroll
             for (int i = 0; i < BN / 64; ++i) {
-                uint32_t r[32];
+                uint32_t pk[32];
 #pragma unroll
-                for (int x = 0; x < 32; ++x) r[x] = pk[32 * i + x];
-                ptx::tmem_st32(tmem + lane_addr + T::TM_P + b * (BN / 2) + 32 * i, r);
+                for (int x = 0; x < 32; ++x) {
+                    float a0, a1;
+                    ptx::unpack_f32x2(ptx::ffma2(ptx::pack_f32x2(s[64 * i + 2 * x], s[64 * i + 2 * x + 1]), c2, negm2),
+                                      a0, a1);
+                    const float p0 = ptx::ex2(a0), p1 = ptx::ex2(a1);
+                    sum2 = ptx::fadd2(sum2, ptx::pack_f32x2(p0, p1));
+                    pk[x] = pack2<BF16>(p0, p1);
+                }
+                ptx::tmem_st32(tmem + lane_addr + T::TM_P + b * (BN / 2) + 32 * i, pk);
+            }
+            if (rescale) {
+                // O and l are rescaled by alpha before this block is added to
+                // them (Kernel design rules): wait until O += P_{j-1} V_{j-1}
+                // has landed, then scale O in place.
+                const uint32_t g = step - 1;
+                if (!warp_wait_phase(bar(T::B_PVDONE + (g & 1u)), (g >> 1) & 1u, ctl, SITE_PV_DONE)) return;
+                ptx::tc_fence_after();
+                rescale_o<D>(tmem + lane_addr + T::TM_O, alpha);
             }
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(T::B_PFULL + b));
-            l = l * alpha + (sum0 + sum1);
-            m = m_new;
+            float sl, sh;
+            ptx::unpack_f32x2(sum2, sl, sh);
+            l = l * alpha + (sl + sh);
             ++step;
         }
-        // epilogue: O = acc / l in the input type, lse = m + log(l) in natural-log units
-        if (!warp_wait_phase(bar(T::B_PVDONE), pv_waits & 1u, ctl, SITE_PV_DONE)) return;
-        ++pv_waits;
+        // hand m and l of this tile to the epilogue warps
+        const uint32_t slot = ntile & 1u;
+        if (!warp_wait_phase(bar(T::B_EPIEMPTY + slot), ((ntile >> 1) & 1u) ^ 1u, ctl, SITE_EPI_EMPTY)) return;
+        hand[slot * 2 * BM + row] = m;
+        hand[slot * 2 * BM + BM + row] = l;
+        ptx::mbar_arrive(bar(T::B_EPIFULL + slot));
+    }
+}
+
+// ------------------------------------------------------------ epilogue ------
+// O = acc / l in the input type, lse = m + log(l) in natural-log units
+// ("Write Triton Attention Kernel", steps 6-8).
+template <int D, bool CAUSAL, bool BF16>
+__device__ void run_epilogue(const FwdParams& p, uint32_t bar0, uint32_t tmem, const float* hand, const Ctl& ctl) {
+    using T = Traits<D>;
+    auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+    const int quad = (threadIdx.x / 32) % 4;
+    const int row = quad * 32 + threadIdx.x % 32;
+    const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
+    uint32_t step = 0, ntile = 0;
+    constexpr int CH = D >= 32 ? 32 : 16;             // columns per TMEM load
+    constexpr int HELD = D <= 128 ? D / CH : 64 / CH;  // chunks held in registers at once
+    for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++ntile) {
+        const TileInfo ti = tile_info<CAUSAL, T::BN>(t, p);
+        step += ti.nkv;
+        const uint32_t slot = ntile & 1u;
+        if (!warp_wait_phase(bar(T::B_EPIFULL + slot), (ntile >> 1) & 1u, ctl, SITE_EPI_FULL)) return;
+        const float m = hand[slot * 2 * BM + row];
+        const float l = hand[slot * 2 * BM + BM + row];
+        ptx::mbar_arrive(bar(T::B_EPIEMPTY + slot));
+        const uint32_t g = step - 1;  // the tile's last P·V
+        if (!warp_wait_phase(bar(T::B_PVDONE + (g & 1u)), (g >> 1) & 1u, ctl, SITE_PV_DONE)) return;
         ptx::tc_fence_after();
-        const float inv_l = 1.f / l;
+
+        const int q_row = ti.q_start + row;
         const bool store = q_row < p.Nq;
+        const float inv_l = 1.f / l;
         uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
                         2 * ((int64_t)ti.z * p.so_z + (int64_t)ti.hq * p.so_h + (int64_t)q_row * p.so_n);
-        if constexpr (D >= 32) {
 #pragma unroll
-            for (int i = 0; i < D / 32; ++i) {
-                uint32_t r[32];
-                ptx::tmem_ld32(tmem + lane_addr + T::TM_O + 32 * i, r);
-                uint32_t o16[16];
+        for (int base = 0; base < D / CH; base += HELD) {
+            uint32_t r[HELD][CH];
 #pragma unroll
-                for (int x = 0; x < 16; ++x)
-                    o16[x] = pack2<BF16>(__uint_as_float(r[2 * x]) * inv_l, __uint_as_float(r[2 * x + 1]) * inv_l);
-                if (store) {
-                    uint4* dst = reinterpret_cast<uint4*>(orow + 64 * i);
-#pragma unroll
-                    for (int x = 0; x < 4; ++x)
-                        dst[x] = make_uint4(o16[4 * x], o16[4 * x + 1], o16[4 * x + 2], o16[4 * x + 3]);
-                }
+            for (int i = 0; i < HELD; ++i) {
+                if constexpr (CH == 32) ptx::tmem_ld32(tmem + lane_addr + T::TM_O + (base + i) * CH, r[i]);
+                else ptx::tmem_ld16(tmem + lane_addr + T::TM_O + (base + i) * CH, r[i]);
             }
-        } else {
-            uint32_t r[16];
-            ptx::tmem_ld16(tmem + lane_addr + T::TM_O, r);
-            uint32_t o8[8];
+            if (base + HELD == D / CH) {
+                // all of O is in registers: the MMA warp may overwrite it with the next tile
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(bar(T::B_OFREE));
+            }
 #pragma unroll
-            for (int x = 0; x < 8; ++x)
-                o8[x] = pack2<BF16>(__uint_as_float(r[2 * x]) * inv_l, __uint_as_float(r[2 * x + 1]) * inv_l);
-            if (store) {
-                uint4* dst = reinterpret_cast<uint4*>(orow);
-                dst[0] = make_uint4(o8[0], o8[1], o8[2], o8[3]);
-                dst[1] = make_uint4(o8[4], o8[5], o8[6], o8[7]);
+            for (int i = 0; i < HELD; ++i) {
+                uint32_t o2[CH / 2];
+#pragma unroll
+                for (int x = 0; x < CH / 2; ++x)
+                    o2[x] = pack2<BF16>(__uint_as_float(r[i][2 * x]) * inv_l, __uint_as_float(r[i][2 * x + 1]) * inv_l);
+                if (store) {
+                    uint4* dst = reinterpret_cast<uint4*>(orow + 2 * (base + i) * CH);
+#pragma unroll
+                    for (int x = 0; x < CH / 8; ++x)
+                        dst[x] = make_uint4(o2[4 * x], o2[4 * x + 1], o2[4 * x + 2], o2[4 * x + 3]);
+                }
             }
         }
         if (store && p.lse != nullptr)
@@ -453,16 +526,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = ptx::smem_addr(smem);
     const uint32_t bar0 = sbase + T::OFF_BAR;
+    float* hand = reinterpret_cast<float*>(smem + T::OFF_HAND);
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + T::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + T::OFF_MISC + 4);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < T::NUM_BARS; ++i) {
-            uint32_t count = 1;
-            if (i >= T::B_PFULL && i < T::B_PFULL + 2) count = 128;  // every softmax thread arrives
-            ptx::mbar_init(bar0 + 8u * i, count);
-        }
+        for (int i = 0; i < T::NUM_BARS; ++i) ptx::mbar_init(bar0 + 8u * i, T::bar_count(i));
         *abort_flag = 0;
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&tmQ);
@@ -483,8 +553,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) run_producer<D, CAUSAL>(&tmQ, &tmK, &tmV, p, sbase, bar0, ctl);
     } else if (warp == 1) {
         if (lane == 0) run_mma<D, CAUSAL, BF16>(p, sbase, bar0, tmem, ctl);
+    } else if (warp < 6) {
+        run_softmax<D, CAUSAL, BF16>(p, bar0, tmem, hand, ctl);
     } else {
-        run_softmax<D, CAUSAL, BF16>(p, bar0, tmem, ctl);
+        run_epilogue<D, CAUSAL, BF16>(p, bar0, tmem, hand, ctl);
     }
 
     ptx::tc_fence_before();

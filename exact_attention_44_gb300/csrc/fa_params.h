@@ -6,7 +6,7 @@
 namespace fa {
 
 constexpr int BM = 128;            // query rows per tile (one TMEM lane per row)
-constexpr int NUM_THREADS = 192;   // warp 0: TMA producer, warp 1: MMA issuer, warps 2-5: softmax
+constexpr int NUM_THREADS = 320;   // warp 0: TMA, warp 1: MMA, warps 2-5: softmax, warps 6-9: epilogue
 
 // Where a bounded wait gave up; recorded in bits 8-15 of the device status word.
 enum WaitSite : uint32_t {
@@ -19,6 +19,9 @@ enum WaitSite : uint32_t {
     SITE_S_FULL = 7,
     SITE_P_FULL = 8,
     SITE_PV_DONE = 9,
+    SITE_EPI_FULL = 10,
+    SITE_EPI_EMPTY = 11,
+    SITE_O_FREE = 12,
 };
 
 struct FwdParams {
