@@ -53,8 +53,10 @@ struct Traits {
     static constexpr int Q_BYTES = BM * D * 2;
     static constexpr int KV_BYTES = BN * D * 2;
     static constexpr int Q_STAGES = D == 256 ? 1 : 2;
-    static constexpr int K_STAGES = D <= 32 ? 4 : D == 64 ? 3 : 2;
-    static constexpr int V_STAGES = K_STAGES;
+    // K and V rings are two deep, like S and P: K slot s is free once S of
+    // that block is complete, V slot s once its P·V is; those two commits
+    // release the slots, so no separate "empty" barriers exist.
+    static constexpr int KV_STAGES = 2;
     // tensor memory columns (lane = query row)
     static constexpr uint32_t TM_S = 0;                        // S[b] at TM_S + b * BN (fp32)
     static constexpr uint32_t TM_P = 2 * BN;                   // P[b] at TM_P + b * BN/2 (2 x 16 bit per column)
@@ -64,19 +66,17 @@ struct Traits {
     // shared memory (offsets from a 1024-byte aligned base)
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + Q_STAGES * Q_BYTES;
-    static constexpr int OFF_V = OFF_K + K_STAGES * KV_BYTES;
-    static constexpr int OFF_HAND = OFF_V + V_STAGES * KV_BYTES;  // softmax -> epilogue: m, l per row, 2 slots
+    static constexpr int OFF_V = OFF_K + KV_STAGES * KV_BYTES;
+    static constexpr int OFF_HAND = OFF_V + KV_STAGES * KV_BYTES;  // softmax -> epilogue: m, l per row, 2 slots
     static constexpr int OFF_BAR = OFF_HAND + 2 * 2 * BM * 4;
     // barrier indices
     static constexpr int B_QFULL = 0;
     static constexpr int B_QEMPTY = B_QFULL + Q_STAGES;
-    static constexpr int B_KFULL = B_QEMPTY + Q_STAGES;
-    static constexpr int B_KEMPTY = B_KFULL + K_STAGES;
-    static constexpr int B_VFULL = B_KEMPTY + K_STAGES;
-    static constexpr int B_VEMPTY = B_VFULL + V_STAGES;
-    static constexpr int B_SFULL = B_VEMPTY + V_STAGES;        // [2] S_g ready (commit)
+    static constexpr int B_KFULL = B_QEMPTY + Q_STAGES;        // [2] K tile landed (TMA)
+    static constexpr int B_VFULL = B_KFULL + KV_STAGES;        // [2] V tile landed (TMA)
+    static constexpr int B_SFULL = B_VFULL + KV_STAGES;        // [2] S_g ready; K slot g&1 free (commit)
     static constexpr int B_PFULL = B_SFULL + 2;                // [2] P_g written (128 softmax threads)
-    static constexpr int B_PVDONE = B_PFULL + 2;               // [2] O += P_g V_g complete (commit)
+    static constexpr int B_PVDONE = B_PFULL + 2;               // [2] O += P_g V_g complete; V slot g&1 free (commit)
     static constexpr int B_EPIFULL = B_PVDONE + 2;             // [2] m, l of a tile handed over (128)
     static constexpr int B_EPIEMPTY = B_EPIFULL + 2;           // [2] hand-over slot read (128)
     static constexpr int B_OFREE = B_EPIEMPTY + 2;             // O read out of TMEM (128)
@@ -194,8 +194,9 @@ __device__ void run_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, con
         }
         for (int j = 0; j < ti.nkv; ++j) {
             {
-                const uint32_t s = ki % T::K_STAGES, ph = (ki / T::K_STAGES) & 1u;
-                if (!wait_phase(bar(T::B_KEMPTY + s), ph ^ 1u, ctl, SITE_K_EMPTY)) { ok = false; break; }
+                // slot ki & 1 held block ki - 2, whose S is complete once that phase of s_full is
+                const uint32_t s = ki & 1u, ph = (ki >> 1) & 1u;
+                if (!wait_phase(bar(T::B_SFULL + s), ph ^ 1u, ctl, SITE_K_EMPTY)) { ok = false; break; }
                 if (p.inject_stall && blockIdx.x == 0 && !withheld) {
                     withheld = true;  // never issued: the MMA warp's wait for this tile must time out
                 } else {
@@ -208,8 +209,9 @@ __device__ void run_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, con
                 ++ki;
             }
             {
-                const uint32_t s = vi % T::V_STAGES, ph = (vi / T::V_STAGES) & 1u;
-                if (!wait_phase(bar(T::B_VEMPTY + s), ph ^ 1u, ctl, SITE_V_EMPTY)) { ok = false; break; }
+                // slot vi & 1 held block vi - 2, free once its P·V is complete
+                const uint32_t s = vi & 1u, ph = (vi >> 1) & 1u;
+                if (!wait_phase(bar(T::B_PVDONE + s), ph ^ 1u, ctl, SITE_V_EMPTY)) { ok = false; break; }
                 ptx::mbar_arrive_expect_tx(bar(T::B_VFULL + s), T::KV_BYTES);
                 const uint32_t dst = sbase + T::OFF_V + s * T::KV_BYTES;
                 for (int c = 0; c < T::NCHUNK; ++c)
@@ -225,82 +227,77 @@ __device__ void run_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, con
         const uint64_t lim = ctl.limit_ns;
         for (uint32_t i = qi > (uint32_t)T::Q_STAGES ? qi - T::Q_STAGES : 0; i < qi; ++i)
             drain_phase(bar(T::B_QFULL + i % T::Q_STAGES), (i / T::Q_STAGES) & 1u, lim);
-        for (uint32_t i = ki > (uint32_t)T::K_STAGES ? ki - T::K_STAGES : 0; i < ki; ++i)
-            drain_phase(bar(T::B_KFULL + i % T::K_STAGES), (i / T::K_STAGES) & 1u, withheld ? lim / 64 : lim);
-        for (uint32_t i = vi > (uint32_t)T::V_STAGES ? vi - T::V_STAGES : 0; i < vi; ++i)
-            drain_phase(bar(T::B_VFULL + i % T::V_STAGES), (i / T::V_STAGES) & 1u, lim);
+        for (uint32_t i = ki > 2u ? ki - 2u : 0u; i < ki; ++i)
+            drain_phase(bar(T::B_KFULL + (i & 1u)), (i >> 1) & 1u, withheld ? lim / 64 : lim);
+        for (uint32_t i = vi > 2u ? vi - 2u : 0u; i < vi; ++i)
+            drain_phase(bar(T::B_VFULL + (i & 1u)), (i >> 1) & 1u, lim);
     }
 }
 
 // ------------------------------------------------------------ MMA issuer ----
+// One thread issues every MMA.  Issuing a tcgen05.mma costs the thread tens of
+// cycles, close to the 64 the tensor core spends on an N = 128 instruction, so
+// the loop is kept lean: descriptors are a per-stage base word plus a
+// compile-time offset, and each block commits twice (S ready, P·V done).
 template <int D, bool CAUSAL, bool BF16>
 __device__ void run_mma(const FwdParams& p, uint32_t sbase, uint32_t bar0, uint32_t tmem, const Ctl& ctl) {
     using T = Traits<D>;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     constexpr uint32_t IDESC_QK = ptx::idesc_f16(BM, T::BN, BF16, false, false);  // Q, K both K-major
     constexpr uint32_t IDESC_PV = ptx::idesc_f16(BM, D, BF16, false, true);       // V is MN-major (D contiguous)
-    constexpr uint32_t KMAJ_SBO = 8 * T::SW;                  // 8-row swizzle atom
-    constexpr uint32_t V_LBO = T::BN * T::SW;                 // next 64/32/16-column chunk of V
-    uint32_t qi = 0, ki = 0, vi = 0, qk_step = 0, pv_step = 0, ntile = 0;
+    constexpr uint32_t HI = ptx::smem_desc_hi(8 * T::SW, T::SWIZZLE_CODE);          // 8-row swizzle atoms
+    // low descriptor words of stage 0; a stage / K step moves the start address
+    const uint32_t q_lo0 = ptx::smem_desc_lo(sbase + T::OFF_Q, 16);
+    const uint32_t k_lo0 = ptx::smem_desc_lo(sbase + T::OFF_K, 16);
+    const uint32_t v_lo0 = ptx::smem_desc_lo(sbase + T::OFF_V, T::BN * T::SW);  // LBO: next column chunk of V
+    uint32_t qi = 0, qk = 0, pv = 0, ntile = 0;  // Q tiles, S blocks and P·V blocks issued
     bool ok = true;
     for (int t = blockIdx.x; ok && t < p.ntiles; t += gridDim.x, ++ntile) {
         const TileInfo ti = tile_info<CAUSAL, T::BN>(t, p);
         const uint32_t qs = qi % T::Q_STAGES;
         if (!wait_phase(bar(T::B_QFULL + qs), (qi / T::Q_STAGES) & 1u, ctl, SITE_Q_FULL)) { ok = false; break; }
-        ptx::tc_fence_after();
-        const uint32_t q_base = sbase + T::OFF_Q + qs * T::Q_BYTES;
-
-        // S_j = Q K_jᵀ into S[qk_step & 1]  ("Write Triton Attention Kernel", step 5b)
-        auto issue_qk = [&](int j) -> bool {
-            const uint32_t ks = ki % T::K_STAGES;
-            if (!wait_phase(bar(T::B_KFULL + ks), (ki / T::K_STAGES) & 1u, ctl, SITE_K_FULL)) return false;
-            ptx::tc_fence_after();
-            const uint32_t k_base = sbase + T::OFF_K + ks * T::KV_BYTES;
-            const uint32_t d_tmem = tmem + T::TM_S + (qk_step & 1u) * T::BN;
+        const uint32_t q_lo = q_lo0 + qs * (T::Q_BYTES >> 4);
+        for (int j = -1; j < ti.nkv; ++j) {
+            // S_{j+1} = Q K_{j+1}ᵀ ("Write Triton Attention Kernel", step 5b) runs on
+            // the tensor cores while the softmax works on S_j
+            if (j + 1 < ti.nkv) {
+                const uint32_t b = qk & 1u;
+                if (!wait_phase(bar(T::B_KFULL + b), (qk >> 1) & 1u, ctl, SITE_K_FULL)) { ok = false; break; }
+                ptx::tc_fence_after();
+                const uint32_t k_lo = k_lo0 + b * (T::KV_BYTES >> 4);
+                const uint32_t d_tmem = tmem + T::TM_S + b * T::BN;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const int chunk = (kk * 16) / T::SWE, within = (kk * 16) % T::SWE;
-                const uint64_t a = ptx::smem_desc(q_base + chunk * (BM * T::SW) + within * 2, 16, KMAJ_SBO,
-                                                  T::SWIZZLE_CODE);
-                const uint64_t b = ptx::smem_desc(k_base + chunk * (T::BN * T::SW) + within * 2, 16, KMAJ_SBO,
-                                                  T::SWIZZLE_CODE);
-                ptx::mma_ss(d_tmem, a, b, IDESC_QK, kk > 0 ? 1u : 0u);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t a_off = (((kk * 16) / T::SWE) * (BM * T::SW) + ((kk * 16) % T::SWE) * 2) >> 4;
+                    const uint32_t b_off = (((kk * 16) / T::SWE) * (T::BN * T::SW) + ((kk * 16) % T::SWE) * 2) >> 4;
+                    ptx::mma_ss(d_tmem, ptx::desc64(q_lo + a_off, HI), ptx::desc64(k_lo + b_off, HI), IDESC_QK,
+                                kk > 0 ? 1u : 0u);
+                }
+                ptx::tc_commit(bar(T::B_SFULL + b));           // S ready, K slot b free
+                if (j + 2 == ti.nkv) {
+                    ptx::tc_commit(bar(T::B_QEMPTY + qs));     // last use of this Q tile
+                    ++qi;
+                }
+                ++qk;
             }
-            ptx::tc_commit(bar(T::B_SFULL + (qk_step & 1u)));
-            ptx::tc_commit(bar(T::B_KEMPTY + ks));
-            if (j == ti.nkv - 1) {
-                ptx::tc_commit(bar(T::B_QEMPTY + qs));  // last use of this Q tile
-                ++qi;
-            }
-            ++ki;
-            ++qk_step;
-            return true;
-        };
-
-        if (!issue_qk(0)) { ok = false; break; }
-        for (int j = 0; j < ti.nkv; ++j) {
-            // the next score block runs on the tensor cores while softmax works on this one
-            if (j + 1 < ti.nkv && !issue_qk(j + 1)) { ok = false; break; }
-            // O += P_j V_j  (step 5h); the first block of a tile overwrites O,
+            if (j < 0) continue;
+            // O += P_j V_j (step 5h); the first block of a tile overwrites O,
             // once the epilogue has read the previous tile's O out of TMEM
             if (j == 0 && ntile > 0 &&
                 !wait_phase(bar(T::B_OFREE), (ntile - 1) & 1u, ctl, SITE_O_FREE)) { ok = false; break; }
-            const uint32_t b = pv_step & 1u;
-            if (!wait_phase(bar(T::B_PFULL + b), (pv_step >> 1) & 1u, ctl, SITE_P_FULL)) { ok = false; break; }
-            const uint32_t vs = vi % T::V_STAGES;
-            if (!wait_phase(bar(T::B_VFULL + vs), (vi / T::V_STAGES) & 1u, ctl, SITE_V_FULL)) { ok = false; break; }
+            const uint32_t b = pv & 1u;
+            if (!wait_phase(bar(T::B_PFULL + b), (pv >> 1) & 1u, ctl, SITE_P_FULL)) { ok = false; break; }
+            if (!wait_phase(bar(T::B_VFULL + b), (pv >> 1) & 1u, ctl, SITE_V_FULL)) { ok = false; break; }
             ptx::tc_fence_after();
-            const uint32_t v_base = sbase + T::OFF_V + vs * T::KV_BYTES;
+            const uint32_t v_lo = v_lo0 + b * (T::KV_BYTES >> 4);
+            const uint32_t a_tmem = tmem + T::TM_P + b * (T::BN / 2);
+            const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
-            for (int kk = 0; kk < T::BN / 16; ++kk) {
-                const uint64_t bdesc = ptx::smem_desc(v_base + kk * 16 * T::SW, V_LBO, KMAJ_SBO, T::SWIZZLE_CODE);
-                ptx::mma_ts(tmem + T::TM_O, tmem + T::TM_P + b * (T::BN / 2) + kk * 8, bdesc, IDESC_PV,
-                            (j > 0 || kk > 0) ? 1u : 0u);
-            }
-            ptx::tc_commit(bar(T::B_VEMPTY + vs));
-            ptx::tc_commit(bar(T::B_PVDONE + b));
-            ++vi;
-            ++pv_step;
+            for (int kk = 0; kk < T::BN / 16; ++kk)
+                ptx::mma_ts(tmem + T::TM_O, a_tmem + kk * 8, ptx::desc64(v_lo + ((kk * 16 * T::SW) >> 4), HI), IDESC_PV,
+                            kk > 0 ? 1u : acc0);
+            ptx::tc_commit(bar(T::B_PVDONE + b));              // O updated, V slot b free
+            ++pv;
         }
     }
     if (!ok) {

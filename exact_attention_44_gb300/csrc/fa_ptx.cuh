@@ -153,6 +153,21 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | ((uint64_t)(swizzle_code & 7u) << 61);
 }
 
+// The same descriptor split into its two 32-bit words, so that stepping the
+// start address is one 32-bit add: the 14-bit start field never carries,
+// since shared-memory addresses stay below 2^18 bytes.
+__device__ __forceinline__ uint32_t smem_desc_lo(uint32_t saddr, uint32_t lbo) {
+    return ((saddr >> 4) & 0x3FFFu) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+__host__ __device__ constexpr uint32_t smem_desc_hi(uint32_t sbo, uint32_t swizzle_code) {
+    return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | ((swizzle_code & 7u) << 29);
+}
+__device__ __forceinline__ uint64_t desc64(uint32_t lo, uint32_t hi) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+    return d;
+}
+
 // TMEM -> registers, 32 lanes x 32 bit, 32 consecutive columns, waiting for
 // completion inside the same asm so no consumer can be scheduled early.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
