@@ -67,21 +67,25 @@ struct Traits {
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + Q_STAGES * Q_BYTES;
     static constexpr int OFF_V = OFF_K + KV_STAGES * KV_BYTES;
-    static constexpr int OFF_HAND = OFF_V + KV_STAGES * KV_BYTES;  // softmax -> epilogue: m, l per row, 2 slots
-    static constexpr int OFF_BAR = OFF_HAND + 2 * 2 * BM * 4;
+    // softmax -> epilogue hand-over, 2 slots of {m, l of half 0, l of half 1} per row
+    static constexpr int OFF_HAND = OFF_V + KV_STAGES * KV_BYTES;
+    // partial row maxima of the two column halves, 2 slots (by block parity)
+    static constexpr int OFF_RED = OFF_HAND + 2 * 3 * BM * 4;
+    static constexpr int OFF_BAR = OFF_RED + 2 * 2 * BM * 4;
     // barrier indices
     static constexpr int B_QFULL = 0;
     static constexpr int B_QEMPTY = B_QFULL + Q_STAGES;
     static constexpr int B_KFULL = B_QEMPTY + Q_STAGES;        // [2] K tile landed (TMA)
     static constexpr int B_VFULL = B_KFULL + KV_STAGES;        // [2] V tile landed (TMA)
     static constexpr int B_SFULL = B_VFULL + KV_STAGES;        // [2] S_g ready; K slot g&1 free (commit)
-    static constexpr int B_PFULL = B_SFULL + 2;                // [2] P_g written (128 softmax threads)
+    static constexpr int B_PFULL = B_SFULL + 2;                // [2] P_g written (256 softmax threads)
     static constexpr int B_PVDONE = B_PFULL + 2;               // [2] O += P_g V_g complete; V slot g&1 free (commit)
-    static constexpr int B_EPIFULL = B_PVDONE + 2;             // [2] m, l of a tile handed over (128)
+    static constexpr int B_EPIFULL = B_PVDONE + 2;             // [2] m, l of a tile handed over (256)
     static constexpr int B_EPIEMPTY = B_EPIFULL + 2;           // [2] hand-over slot read (128)
     static constexpr int B_OFREE = B_EPIEMPTY + 2;             // O read out of TMEM (128)
-    static constexpr int B_DRAIN = B_OFREE + 1;                // MMA teardown
-    static constexpr int NUM_BARS = B_DRAIN + 1;
+    static constexpr int B_RED = B_OFREE + 1;                  // [2] both halves' partial maxima written (256)
+    static constexpr int B_DRAIN = B_RED + 2;                  // [2] teardown of the two MMA issuers
+    static constexpr int NUM_BARS = B_DRAIN + 2;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;    // tmem base, abort flag
     static constexpr int SMEM_USED = OFF_MISC + 16;
     // >= 120 KB keeps one CTA per SM, so no CTA ever waits on another's TMEM
@@ -89,8 +93,10 @@ struct Traits {
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
     static __device__ __forceinline__ uint32_t bar_count(int i) {
-        if (i >= B_PFULL && i < B_PFULL + 2) return 128;
-        if (i >= B_EPIFULL && i < B_OFREE + 1) return 128;
+        if (i >= B_PFULL && i < B_PFULL + 2) return 256;
+        if (i >= B_EPIFULL && i < B_EPIFULL + 2) return 256;
+        if (i >= B_EPIEMPTY && i < B_OFREE + 1) return 128;
+        if (i >= B_RED && i < B_RED + 2) return 256;
         return 1;
     }
 };
@@ -234,76 +240,93 @@ __device__ void run_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, con
     }
 }
 
-// ------------------------------------------------------------ MMA issuer ----
-// One thread issues every MMA.  Issuing a tcgen05.mma costs the thread tens of
-// cycles, close to the 64 the tensor core spends on an N = 128 instruction, so
-// the loop is kept lean: descriptors are a per-stage base word plus a
-// compile-time offset, and each block commits twice (S ready, P·V done).
+// ------------------------------------------------------------ MMA issuers ---
+// Issuing a tcgen05.mma stalls the issuing thread until the tensor core takes
+// it, and the tensor core queues little, so a single issuer leaves it idle
+// whenever that thread waits on a barrier.  Two threads issue instead: one
+// the S = Q Kᵀ stream, one the O += P V stream; each waits while the other
+// feeds the tensor core.  The streams touch disjoint TMEM (S vs P and O) and
+// shared memory (Q, K vs V) and are ordered only through mbarriers.
+// Descriptors are a per-stage base word plus a compile-time offset.
+
+// S_g = Q K_gᵀ ("Write Triton Attention Kernel", step 5b) into S[g & 1]
 template <int D, bool CAUSAL, bool BF16>
-__device__ void run_mma(const FwdParams& p, uint32_t sbase, uint32_t bar0, uint32_t tmem, const Ctl& ctl) {
+__device__ void run_mma_qk(const FwdParams& p, uint32_t sbase, uint32_t bar0, uint32_t tmem, const Ctl& ctl) {
     using T = Traits<D>;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
-    constexpr uint32_t IDESC_QK = ptx::idesc_f16(BM, T::BN, BF16, false, false);  // Q, K both K-major
-    constexpr uint32_t IDESC_PV = ptx::idesc_f16(BM, D, BF16, false, true);       // V is MN-major (D contiguous)
-    constexpr uint32_t HI = ptx::smem_desc_hi(8 * T::SW, T::SWIZZLE_CODE);          // 8-row swizzle atoms
-    // low descriptor words of stage 0; a stage / K step moves the start address
+    constexpr uint32_t IDESC = ptx::idesc_f16(BM, T::BN, BF16, false, false);  // Q, K both K-major
+    constexpr uint32_t HI = ptx::smem_desc_hi(8 * T::SW, T::SWIZZLE_CODE);     // 8-row swizzle atoms
     const uint32_t q_lo0 = ptx::smem_desc_lo(sbase + T::OFF_Q, 16);
     const uint32_t k_lo0 = ptx::smem_desc_lo(sbase + T::OFF_K, 16);
-    const uint32_t v_lo0 = ptx::smem_desc_lo(sbase + T::OFF_V, T::BN * T::SW);  // LBO: next column chunk of V
-    uint32_t qi = 0, qk = 0, pv = 0, ntile = 0;  // Q tiles, S blocks and P·V blocks issued
+    uint32_t qi = 0, g = 0;  // Q tiles and S blocks issued
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < p.ntiles; t += gridDim.x, ++ntile) {
+    for (int t = blockIdx.x; ok && t < p.ntiles; t += gridDim.x) {
         const TileInfo ti = tile_info<CAUSAL, T::BN>(t, p);
         const uint32_t qs = qi % T::Q_STAGES;
         if (!wait_phase(bar(T::B_QFULL + qs), (qi / T::Q_STAGES) & 1u, ctl, SITE_Q_FULL)) { ok = false; break; }
         const uint32_t q_lo = q_lo0 + qs * (T::Q_BYTES >> 4);
-        for (int j = -1; j < ti.nkv; ++j) {
-            // S_{j+1} = Q K_{j+1}ᵀ ("Write Triton Attention Kernel", step 5b) runs on
-            // the tensor cores while the softmax works on S_j
-            if (j + 1 < ti.nkv) {
-                const uint32_t b = qk & 1u;
-                if (!wait_phase(bar(T::B_KFULL + b), (qk >> 1) & 1u, ctl, SITE_K_FULL)) { ok = false; break; }
-                ptx::tc_fence_after();
-                const uint32_t k_lo = k_lo0 + b * (T::KV_BYTES >> 4);
-                const uint32_t d_tmem = tmem + T::TM_S + b * T::BN;
+        for (int j = 0; j < ti.nkv; ++j, ++g) {
+            const uint32_t b = g & 1u, ph = (g >> 1) & 1u;
+            if (!wait_phase(bar(T::B_KFULL + b), ph, ctl, SITE_K_FULL)) { ok = false; break; }
+            // S[b] still holds S_{g-2} until the softmax has read it (P_{g-2} written)
+            if (!wait_phase(bar(T::B_PFULL + b), ph ^ 1u, ctl, SITE_S_FREE)) { ok = false; break; }
+            ptx::tc_fence_after();
+            const uint32_t k_lo = k_lo0 + b * (T::KV_BYTES >> 4);
+            const uint32_t d_tmem = tmem + T::TM_S + b * T::BN;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t a_off = (((kk * 16) / T::SWE) * (BM * T::SW) + ((kk * 16) % T::SWE) * 2) >> 4;
-                    const uint32_t b_off = (((kk * 16) / T::SWE) * (T::BN * T::SW) + ((kk * 16) % T::SWE) * 2) >> 4;
-                    ptx::mma_ss(d_tmem, ptx::desc64(q_lo + a_off, HI), ptx::desc64(k_lo + b_off, HI), IDESC_QK,
-                                kk > 0 ? 1u : 0u);
-                }
-                ptx::tc_commit(bar(T::B_SFULL + b));           // S ready, K slot b free
-                if (j + 2 == ti.nkv) {
-                    ptx::tc_commit(bar(T::B_QEMPTY + qs));     // last use of this Q tile
-                    ++qi;
-                }
-                ++qk;
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t a_off = (((kk * 16) / T::SWE) * (BM * T::SW) + ((kk * 16) % T::SWE) * 2) >> 4;
+                const uint32_t b_off = (((kk * 16) / T::SWE) * (T::BN * T::SW) + ((kk * 16) % T::SWE) * 2) >> 4;
+                ptx::mma_ss(d_tmem, ptx::desc64(q_lo + a_off, HI), ptx::desc64(k_lo + b_off, HI), IDESC,
+                            kk > 0 ? 1u : 0u);
             }
-            if (j < 0) continue;
-            // O += P_j V_j (step 5h); the first block of a tile overwrites O,
-            // once the epilogue has read the previous tile's O out of TMEM
+            ptx::tc_commit(bar(T::B_SFULL + b));  // S ready, K slot b free
+            if (j == ti.nkv - 1) {
+                ptx::tc_commit(bar(T::B_QEMPTY + qs));  // last use of this Q tile
+                ++qi;
+            }
+        }
+    }
+    if (!ok) {
+        // every MMA this thread issued must finish before TMEM and shared memory go away
+        ptx::tc_commit(bar(T::B_DRAIN));
+        drain_phase(bar(T::B_DRAIN), 0u, ctl.limit_ns);
+    }
+}
+
+// O += P_g V_g (step 5h); the first block of a tile overwrites O, once the
+// epilogue has read the previous tile's O out of TMEM
+template <int D, bool CAUSAL, bool BF16>
+__device__ void run_mma_pv(const FwdParams& p, uint32_t sbase, uint32_t bar0, uint32_t tmem, const Ctl& ctl) {
+    using T = Traits<D>;
+    auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+    constexpr uint32_t IDESC = ptx::idesc_f16(BM, D, BF16, false, true);      // V is MN-major (D contiguous)
+    constexpr uint32_t HI = ptx::smem_desc_hi(8 * T::SW, T::SWIZZLE_CODE);
+    const uint32_t v_lo0 = ptx::smem_desc_lo(sbase + T::OFF_V, T::BN * T::SW);  // LBO: next column chunk of V
+    uint32_t g = 0, ntile = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < p.ntiles; t += gridDim.x, ++ntile) {
+        const TileInfo ti = tile_info<CAUSAL, T::BN>(t, p);
+        for (int j = 0; j < ti.nkv; ++j, ++g) {
+            const uint32_t b = g & 1u, ph = (g >> 1) & 1u;
             if (j == 0 && ntile > 0 &&
                 !wait_phase(bar(T::B_OFREE), (ntile - 1) & 1u, ctl, SITE_O_FREE)) { ok = false; break; }
-            const uint32_t b = pv & 1u;
-            if (!wait_phase(bar(T::B_PFULL + b), (pv >> 1) & 1u, ctl, SITE_P_FULL)) { ok = false; break; }
-            if (!wait_phase(bar(T::B_VFULL + b), (pv >> 1) & 1u, ctl, SITE_V_FULL)) { ok = false; break; }
+            if (!wait_phase(bar(T::B_PFULL + b), ph, ctl, SITE_P_FULL)) { ok = false; break; }
+            if (!wait_phase(bar(T::B_VFULL + b), ph, ctl, SITE_V_FULL)) { ok = false; break; }
             ptx::tc_fence_after();
             const uint32_t v_lo = v_lo0 + b * (T::KV_BYTES >> 4);
             const uint32_t a_tmem = tmem + T::TM_P + b * (T::BN / 2);
             const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
             for (int kk = 0; kk < T::BN / 16; ++kk)
-                ptx::mma_ts(tmem + T::TM_O, a_tmem + kk * 8, ptx::desc64(v_lo + ((kk * 16 * T::SW) >> 4), HI), IDESC_PV,
+                ptx::mma_ts(tmem + T::TM_O, a_tmem + kk * 8, ptx::desc64(v_lo + ((kk * 16 * T::SW) >> 4), HI), IDESC,
                             kk > 0 ? 1u : acc0);
-            ptx::tc_commit(bar(T::B_PVDONE + b));              // O updated, V slot b free
-            ++pv;
+            ptx::tc_commit(bar(T::B_PVDONE + b));  // O updated, P[b] and V slot b free
         }
     }
     if (!ok) {
-        // every MMA issued so far must finish before TMEM and shared memory go away
-        ptx::tc_commit(bar(T::B_DRAIN));
-        drain_phase(bar(T::B_DRAIN), 0u, ctl.limit_ns);
+        ptx::tc_commit(bar(T::B_DRAIN + 1));
+        drain_phase(bar(T::B_DRAIN + 1), 0u, ctl.limit_ns);
     }
 }
 
@@ -319,13 +342,13 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     }
 }
 
-// O[row, :] *= alpha for the rows of this warp's lane quadrant
-template <int D>
+// O[row, c0 : c0 + NCOL] *= alpha for the rows of this warp's lane quadrant
+template <int NCOL>
 __device__ __forceinline__ void rescale_o(uint32_t taddr, float alpha) {
-    const uint64_t a2 = ptx::pack_f32x2(alpha, alpha);
-    if constexpr (D >= 32) {
+    if constexpr (NCOL >= 32) {
+        const uint64_t a2 = ptx::pack_f32x2(alpha, alpha);
 #pragma unroll
-        for (int i = 0; i < D / 32; ++i) {
+        for (int i = 0; i < NCOL / 32; ++i) {
             uint32_t r[32];
             ptx::tmem_ld32(taddr + 32 * i, r);
 #pragma unroll
@@ -339,19 +362,31 @@ __device__ __forceinline__ void rescale_o(uint32_t taddr, float alpha) {
             }
             ptx::tmem_st32(taddr + 32 * i, r);
         }
-    } else {
+    } else if constexpr (NCOL == 16) {
         uint32_t r[16];
         ptx::tmem_ld16(taddr, r);
 #pragma unroll
         for (int x = 0; x < 16; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * alpha);
         ptx::tmem_st16(taddr, r);
+    } else {
+        uint32_t r[8];
+        ptx::tmem_ld8(taddr, r);
+#pragma unroll
+        for (int x = 0; x < 8; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * alpha);
+        ptx::tmem_st8(taddr, r);
     }
 }
 
+// Online softmax for one column half of every key block: 128 threads, thread
+// = query row = TMEM lane; the two halves swap partial row maxima through
+// shared memory, so both reference the same maximum m, and each keeps its
+// own partial denominator (the epilogue adds them).
 template <int D, bool CAUSAL, bool BF16>
-__device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, float* hand, const Ctl& ctl) {
+__device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, float* hand, float* red, int h,
+                            const Ctl& ctl) {
     using T = Traits<D>;
     constexpr int BN = T::BN;
+    constexpr int HC = BN / 2;                 // score columns per thread
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     const int quad = (threadIdx.x / 32) % 4;  // TMEM lane quadrant this warp may access
     const int row = quad * 32 + threadIdx.x % 32;
@@ -367,55 +402,64 @@ __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, fl
         // ("Write Triton Attention Kernel", step 4; the initial l is 0)
         float m = -INFINITY, l = 0.f;
         for (int j = 0; j < ti.nkv; ++j) {
-            const uint32_t b = step & 1u;
-            if (!warp_wait_phase(bar(T::B_SFULL + b), (step >> 1) & 1u, ctl, SITE_S_FULL)) return;
+            const uint32_t b = step & 1u, ph = (step >> 1) & 1u;
+            if (!warp_wait_phase(bar(T::B_SFULL + b), ph, ctl, SITE_S_FULL)) return;
             ptx::tc_fence_after();
-            float s[BN];
+            float s[HC];
 #pragma unroll
-            for (int i = 0; i < BN / 32; ++i) {
+            for (int i = 0; i < HC / 32; ++i) {
                 uint32_t r[32];
-                ptx::tmem_ld32(tmem + lane_addr + T::TM_S + b * BN + 32 * i, r);
+                ptx::tmem_ld32(tmem + lane_addr + T::TM_S + b * BN + h * HC + 32 * i, r);
 #pragma unroll
                 for (int x = 0; x < 32; ++x) s[32 * i + x] = __uint_as_float(r[x]);
             }
             // the mask goes on the scores before the row max (Correctness
             // requirements); only the diagonal block and the key tail need it
-            const int k0 = j * BN;
-            const bool need_mask = (CAUSAL && k0 + BN - 1 > ti.q_start) || (k0 + BN > p.Nkv);
+            const int k0 = j * BN + h * HC;
+            const bool need_mask = (CAUSAL && j * BN + BN - 1 > ti.q_start) || (j * BN + BN > p.Nkv);
             if (need_mask) {
                 const int kmax = CAUSAL ? min(p.Nkv - 1, q_row) : p.Nkv - 1;  // last kept key for this row
 #pragma unroll
-                for (int x = 0; x < BN; ++x)
+                for (int x = 0; x < HC; ++x)
                     if (k0 + x > kmax) s[x] = -INFINITY;
             }
             float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]);
 #pragma unroll
-            for (int x = 4; x < BN; x += 4) {  // BN is a multiple of 4
+            for (int x = 4; x < HC; x += 4) {  // HC is a multiple of 4
                 mx0 = ptx::fmax3(mx0, s[x], s[x + 1]);
                 mx1 = ptx::fmax3(mx1, s[x + 2], s[x + 3]);
             }
-            const float m_tile = fmaxf(mx0, mx1) * c;  // scale > 0: max commutes with the scaling
+            // swap partial maxima with the other half (slot b is free: every
+            // thread read it two blocks ago before arriving on it last block)
+            red[(b * 2 + h) * BM + row] = fmaxf(mx0, mx1);
+            ptx::mbar_arrive(bar(T::B_RED + b));
+            if (!warp_wait_phase(bar(T::B_RED + b), ph, ctl, SITE_MAX_XCHG)) return;
+            const float m_tile = fmaxf(fmaxf(mx0, mx1), red[(b * 2 + (h ^ 1)) * BM + row]) * c;  // scale > 0
             float alpha = 1.f;
             bool rescale = false;
             if (j == 0) {
                 m = m_tile;
             } else if (__any_sync(0xffffffffu, m_tile > m + RESCALE_LOG2)) {
+                // both halves take this branch for the same rows (same m, m_tile)
                 const float m_new = fmaxf(m, m_tile);
                 alpha = ptx::ex2(m - m_new);
                 m = m_new;
                 rescale = true;
             }
+            // P[b] was last read by the P·V of two blocks ago: wait for it
+            // (it has long finished; S and P·V are issued by different threads)
+            if (!warp_wait_phase(bar(T::B_PVDONE + b), ph ^ 1u, ctl, SITE_P_FREE)) return;
             // p = 2^(s·scale·log2e − m); l sums the fp32 p, P V uses p cast to
-            // the input type.  P[b] was last read by the P·V of two blocks ago,
-            // which completed before S_j did (committed in issue order), so it
-            // is free; it is written 64 columns at a time as they are produced.
+            // the input type
             const uint64_t negm2 = ptx::pack_f32x2(-m, -m);
             uint64_t sum2 = ptx::pack_f32x2(0.f, 0.f);
+            const uint32_t p_addr = tmem + lane_addr + T::TM_P + b * (BN / 2) + h * (HC / 2);
 #pragma unroll
-            for (int i = 0; i < BN / 64; ++i) {
-                uint32_t pk[32];
+            for (int i = 0; i < (HC + 63) / 64; ++i) {
+                constexpr int NP = HC >= 64 ? 32 : HC / 2;  // packed columns per store
+                uint32_t pk[NP];
 #pragma unroll
-                for (int x = 0; x < 32; ++x) {
+                for (int x = 0; x < NP; ++x) {
                     float a0, a1;
                     ptx::unpack_f32x2(ptx::ffma2(ptx::pack_f32x2(s[64 * i + 2 * x], s[64 * i + 2 * x + 1]), c2, negm2),
                                       a0, a1);
@@ -423,16 +467,17 @@ __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, fl
                     sum2 = ptx::fadd2(sum2, ptx::pack_f32x2(p0, p1));
                     pk[x] = pack2<BF16>(p0, p1);
                 }
-                ptx::tmem_st32(tmem + lane_addr + T::TM_P + b * (BN / 2) + 32 * i, pk);
+                if constexpr (NP == 32) ptx::tmem_st32(p_addr + 32 * i, pk);
+                else ptx::tmem_st16(p_addr + 16 * i, pk);
             }
             if (rescale) {
                 // O and l are rescaled by alpha before this block is added to
                 // them (Kernel design rules): wait until O += P_{j-1} V_{j-1}
-                // has landed, then scale O in place.
+                // has landed, then scale this half's columns of O in place.
                 const uint32_t g = step - 1;
                 if (!warp_wait_phase(bar(T::B_PVDONE + (g & 1u)), (g >> 1) & 1u, ctl, SITE_PV_DONE)) return;
                 ptx::tc_fence_after();
-                rescale_o<D>(tmem + lane_addr + T::TM_O, alpha);
+                rescale_o<D / 2>(tmem + lane_addr + T::TM_O + h * (D / 2), alpha);
             }
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
@@ -442,18 +487,19 @@ __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, fl
             l = l * alpha + (sl + sh);
             ++step;
         }
-        // hand m and l of this tile to the epilogue warps
+        // hand m and this half's l to the epilogue warps
         const uint32_t slot = ntile & 1u;
         if (!warp_wait_phase(bar(T::B_EPIEMPTY + slot), ((ntile >> 1) & 1u) ^ 1u, ctl, SITE_EPI_EMPTY)) return;
-        hand[slot * 2 * BM + row] = m;
-        hand[slot * 2 * BM + BM + row] = l;
+        if (h == 0) hand[slot * 3 * BM + row] = m;
+        hand[slot * 3 * BM + (1 + h) * BM + row] = l;
         ptx::mbar_arrive(bar(T::B_EPIFULL + slot));
     }
 }
 
 // ------------------------------------------------------------ epilogue ------
 // O = acc / l in the input type, lse = m + log(l) in natural-log units
-// ("Write Triton Attention Kernel", steps 6-8).
+// ("Write Triton Attention Kernel", steps 6-8).  O is read out of TMEM and
+// converted first, TMEM is handed back to the MMA warp, then rows are stored.
 template <int D, bool CAUSAL, bool BF16>
 __device__ void run_epilogue(const FwdParams& p, uint32_t bar0, uint32_t tmem, const float* hand, const Ctl& ctl) {
     using T = Traits<D>;
@@ -462,15 +508,15 @@ __device__ void run_epilogue(const FwdParams& p, uint32_t bar0, uint32_t tmem, c
     const int row = quad * 32 + threadIdx.x % 32;
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
     uint32_t step = 0, ntile = 0;
-    constexpr int CH = D >= 32 ? 32 : 16;             // columns per TMEM load
-    constexpr int HELD = D <= 128 ? D / CH : 64 / CH;  // chunks held in registers at once
+    constexpr int CH = D >= 32 ? 32 : 16;               // columns per TMEM load
+    constexpr int HELD = D <= 64 ? D / CH : 64 / CH;     // chunks converted before their stores
     for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++ntile) {
         const TileInfo ti = tile_info<CAUSAL, T::BN>(t, p);
         step += ti.nkv;
         const uint32_t slot = ntile & 1u;
         if (!warp_wait_phase(bar(T::B_EPIFULL + slot), (ntile >> 1) & 1u, ctl, SITE_EPI_FULL)) return;
-        const float m = hand[slot * 2 * BM + row];
-        const float l = hand[slot * 2 * BM + BM + row];
+        const float m = hand[slot * 3 * BM + row];
+        const float l = hand[slot * 3 * BM + BM + row] + hand[slot * 3 * BM + 2 * BM + row];
         ptx::mbar_arrive(bar(T::B_EPIEMPTY + slot));
         const uint32_t g = step - 1;  // the tile's last P·V
         if (!warp_wait_phase(bar(T::B_PVDONE + (g & 1u)), (g >> 1) & 1u, ctl, SITE_PV_DONE)) return;
@@ -483,28 +529,28 @@ __device__ void run_epilogue(const FwdParams& p, uint32_t bar0, uint32_t tmem, c
                         2 * ((int64_t)ti.z * p.so_z + (int64_t)ti.hq * p.so_h + (int64_t)q_row * p.so_n);
 #pragma unroll
         for (int base = 0; base < D / CH; base += HELD) {
-            uint32_t r[HELD][CH];
+            uint32_t o2[HELD][CH / 2];
 #pragma unroll
             for (int i = 0; i < HELD; ++i) {
-                if constexpr (CH == 32) ptx::tmem_ld32(tmem + lane_addr + T::TM_O + (base + i) * CH, r[i]);
-                else ptx::tmem_ld16(tmem + lane_addr + T::TM_O + (base + i) * CH, r[i]);
+                uint32_t r[CH];
+                if constexpr (CH == 32) ptx::tmem_ld32(tmem + lane_addr + T::TM_O + (base + i) * CH, r);
+                else ptx::tmem_ld16(tmem + lane_addr + T::TM_O + (base + i) * CH, r);
+#pragma unroll
+                for (int x = 0; x < CH / 2; ++x)
+                    o2[i][x] = pack2<BF16>(__uint_as_float(r[2 * x]) * inv_l, __uint_as_float(r[2 * x + 1]) * inv_l);
             }
             if (base + HELD == D / CH) {
-                // all of O is in registers: the MMA warp may overwrite it with the next tile
+                // all of O has been read: the MMA warp may overwrite it with the next tile
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(bar(T::B_OFREE));
             }
+            if (store) {
 #pragma unroll
-            for (int i = 0; i < HELD; ++i) {
-                uint32_t o2[CH / 2];
-#pragma unroll
-                for (int x = 0; x < CH / 2; ++x)
-                    o2[x] = pack2<BF16>(__uint_as_float(r[i][2 * x]) * inv_l, __uint_as_float(r[i][2 * x + 1]) * inv_l);
-                if (store) {
+                for (int i = 0; i < HELD; ++i) {
                     uint4* dst = reinterpret_cast<uint4*>(orow + 2 * (base + i) * CH);
 #pragma unroll
                     for (int x = 0; x < CH / 8; ++x)
-                        dst[x] = make_uint4(o2[4 * x], o2[4 * x + 1], o2[4 * x + 2], o2[4 * x + 3]);
+                        dst[x] = make_uint4(o2[i][4 * x], o2[i][4 * x + 1], o2[i][4 * x + 2], o2[i][4 * x + 3]);
                 }
             }
         }
@@ -524,6 +570,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t sbase = ptx::smem_addr(smem);
     const uint32_t bar0 = sbase + T::OFF_BAR;
     float* hand = reinterpret_cast<float*>(smem + T::OFF_HAND);
+    float* red = reinterpret_cast<float*>(smem + T::OFF_RED);
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + T::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + T::OFF_MISC + 4);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -549,9 +596,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 0) {
         if (lane == 0) run_producer<D, CAUSAL>(&tmQ, &tmK, &tmV, p, sbase, bar0, ctl);
     } else if (warp == 1) {
-        if (lane == 0) run_mma<D, CAUSAL, BF16>(p, sbase, bar0, tmem, ctl);
-    } else if (warp < 6) {
-        run_softmax<D, CAUSAL, BF16>(p, bar0, tmem, hand, ctl);
+        if (lane == 0) run_mma_qk<D, CAUSAL, BF16>(p, sbase, bar0, tmem, ctl);
+    } else if (warp == 2) {
+        if (lane == 0) run_mma_pv<D, CAUSAL, BF16>(p, sbase, bar0, tmem, ctl);
+    } else if (warp < 11) {
+        run_softmax<D, CAUSAL, BF16>(p, bar0, tmem, hand, red, (warp - 3) / 4, ctl);
     } else {
         run_epilogue<D, CAUSAL, BF16>(p, bar0, tmem, hand, ctl);
     }

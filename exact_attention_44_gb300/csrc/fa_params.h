@@ -6,7 +6,9 @@
 namespace fa {
 
 constexpr int BM = 128;            // query rows per tile (one TMEM lane per row)
-constexpr int NUM_THREADS = 320;   // warp 0: TMA, warp 1: MMA, warps 2-5: softmax, warps 6-9: epilogue
+// warp 0: TMA, warp 1: S = Q Kᵀ issuer, warp 2: O += P V issuer, warps 3-6 and
+// 7-10: softmax of the two column halves of each key block, warps 11-14: epilogue
+constexpr int NUM_THREADS = 480;
 
 // Where a bounded wait gave up; recorded in bits 8-15 of the device status word.
 enum WaitSite : uint32_t {
@@ -22,6 +24,9 @@ enum WaitSite : uint32_t {
     SITE_EPI_FULL = 10,
     SITE_EPI_EMPTY = 11,
     SITE_O_FREE = 12,
+    SITE_MAX_XCHG = 13,
+    SITE_P_FREE = 14,
+    SITE_S_FREE = 15,
 };
 
 struct FwdParams {
