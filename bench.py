@@ -388,7 +388,7 @@ def run_reference(args, rank, world):
     wl = WORKLOADS[args.workload]
     Z, Hq, Hkv, Nq, Nkv, D, dtype, flags = wl
     times, values = [], []
-    budget = max(0.05, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    budget = max(0.05, min(args.cpu_budget, 150.0 / max(1, args.steps + args.warmup)))
     for i in range(args.warmup):
         run_oracle_sample(wl, budget / 4)
     info = None
@@ -449,8 +449,8 @@ def all_reduce_max(x: float, world: int, device) -> float:
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=12000)
+    ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=MAIN)
     ap.add_argument("--no-e2e", action="store_true")
@@ -458,7 +458,10 @@ def main(argv=None):
     ap.add_argument("--shapes", dest="shapes", action="store_true", default=True,
                     help="also time the D=128, N>=4096 non-causal target shapes (default)")
     ap.add_argument("--no-shapes", dest="shapes", action="store_false")
-    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle work for cpu_baseline (and the cap per step of --impl reference)")
+    ap.add_argument("--all", action="store_true",
+                    help="instead of the bench line, time every workload (one JSON line each) for the results table")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "native":
         ap.error("--warmup must be >= 3")
@@ -477,6 +480,20 @@ def main(argv=None):
         raise SystemExit("bench.py: no CUDA device (the native path has no CPU fallback)")
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
+    if args.all:
+        import exact_attention_44_gb300 as fa
+        fa.build()
+        fa.load()
+        peaks = load_peaks()
+        for name, wl in list(WORKLOADS.items()):
+            for causal in wl[7]:
+                single = wl[:7] + ([causal],)
+                WORKLOADS[name + ("_causal" if causal else "_noncausal")] = single
+                r = measure_shape(name + ("_causal" if causal else "_noncausal"), device,
+                                  torch.cuda.current_stream(device), peaks, steps=20)
+                r.update(dtype=wl[6], causal=causal)
+                print(json.dumps(r), flush=True)
+        return 0
     result = run_native(args, rank, world, device)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:

@@ -1,0 +1,37 @@
+"""Failure detection on the GPU without a fault: every device-side wait is
+bounded.  A test hook makes CTA 0 withhold one K copy; its waits run out after
+a short limit, the kernel records FA_ERR_DEVICE_TIMEOUT and exits cleanly, and
+the context stays usable for the next launch."""
+import pytest
+
+import seeded_inputs as si
+from parity_util import check_full
+
+pytestmark = pytest.mark.gpu
+
+
+def test_withheld_copy_times_out_and_the_context_recovers():
+    import torch
+
+    import exact_attention_44_gb300 as fa
+    fa.build()
+    q, k, v = si.qkv(21, 1, 4, 2, 1024, 1024, 64, "bf16")
+    qt, kt, vt = (si.as_torch(x, "bf16").cuda() for x in (q, k, v))
+    assert fa.fa_device_status()[0] == fa.FA_OK
+    fa.fa_debug_set_wait_limit_ms(100)
+    fa.fa_debug_inject_stall(True)
+    try:
+        fa.fa_fwd(qt, kt, vt, causal=False)
+        code, word = fa.fa_device_status()
+    finally:
+        fa.fa_debug_inject_stall(False)
+        fa.fa_debug_set_wait_limit_ms(0)
+    assert code == fa.FA_ERR_DEVICE_TIMEOUT, hex(word)
+    assert word & 0xFF == fa.FA_ERR_DEVICE_TIMEOUT
+    assert (word >> 16) == 0          # CTA 0 gave up first
+    assert 1 <= (word >> 8) & 0xFF <= 15  # a known wait site
+    # the status word was cleared, and the next launch is correct
+    assert fa.fa_device_status() == (fa.FA_OK, 0)
+    check_full(22, 1, 4, 2, 300, 300, 64, "bf16", True)
+    assert fa.fa_device_status() == (fa.FA_OK, 0)
+    torch.cuda.synchronize()
