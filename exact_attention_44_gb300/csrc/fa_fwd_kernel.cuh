@@ -175,55 +175,59 @@ __device__ __forceinline__ TileInfo tile_info(int t, const FwdParams& p) {
     return ti;
 }
 
-// ------------------------------------------------------------ TMA producer --
+// ------------------------------------------------------------ TMA producers -
+// Two threads load: one Q and K (the S stream's operands), one V (the P·V
+// stream's), so a K load never queues behind a V slot that is still in use.
+// With two Q slots the next tile's Q is requested right after the current
+// tile's first K: its slot held the tile before, whose last S is complete by
+// the time the second K's slot frees anyway.
+
 template <int D, bool CAUSAL>
-__device__ void run_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
-                             const FwdParams& p, uint32_t sbase, uint32_t bar0, const Ctl& ctl) {
+__device__ void run_producer_qk(const CUtensorMap* tmQ, const CUtensorMap* tmK, const FwdParams& p, uint32_t sbase,
+                                uint32_t bar0, const Ctl& ctl) {
     using T = Traits<D>;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     const uint64_t pol_q = ptx::policy_evict_first();
     const uint64_t pol_kv = ptx::policy_evict_last();
-    uint32_t qi = 0, ki = 0, vi = 0;  // loads issued into each ring
+    uint32_t qi = 0, ki = 0;  // loads issued into each ring
     bool ok = true;
     bool withheld = false;
-    for (int t = blockIdx.x; ok && t < p.ntiles; t += gridDim.x) {
+    auto load_q = [&](const TileInfo& ti) -> bool {
+        const uint32_t s = qi % T::Q_STAGES, ph = (qi / T::Q_STAGES) & 1u;
+        if (!wait_phase(bar(T::B_QEMPTY + s), ph ^ 1u, ctl, SITE_Q_EMPTY)) return false;
+        ptx::mbar_arrive_expect_tx(bar(T::B_QFULL + s), T::Q_BYTES);
+        const uint32_t dst = sbase + T::OFF_Q + s * T::Q_BYTES;
+        for (int c = 0; c < T::NCHUNK; ++c)
+            ptx::tma_load_4d(dst + c * (BM * T::SW), tmQ, bar(T::B_QFULL + s), c * T::SWE, ti.q_start, ti.hq, ti.z,
+                             pol_q);
+        ++qi;
+        return true;
+    };
+    int t = blockIdx.x;
+    if (t < p.ntiles) ok = load_q(tile_info<CAUSAL, T::BN>(t, p));
+    for (; ok && t < p.ntiles; t += gridDim.x) {
         const TileInfo ti = tile_info<CAUSAL, T::BN>(t, p);
-        {
-            const uint32_t s = qi % T::Q_STAGES, ph = (qi / T::Q_STAGES) & 1u;
-            if (!wait_phase(bar(T::B_QEMPTY + s), ph ^ 1u, ctl, SITE_Q_EMPTY)) { ok = false; break; }
-            ptx::mbar_arrive_expect_tx(bar(T::B_QFULL + s), T::Q_BYTES);
-            const uint32_t dst = sbase + T::OFF_Q + s * T::Q_BYTES;
-            for (int c = 0; c < T::NCHUNK; ++c)
-                ptx::tma_load_4d(dst + c * (BM * T::SW), tmQ, bar(T::B_QFULL + s), c * T::SWE, ti.q_start, ti.hq,
-                                 ti.z, pol_q);
-            ++qi;
-        }
         for (int j = 0; j < ti.nkv; ++j) {
-            {
-                // slot ki & 1 held block ki - 2, whose S is complete once that phase of s_full is
-                const uint32_t s = ki & 1u, ph = (ki >> 1) & 1u;
-                if (!wait_phase(bar(T::B_SFULL + s), ph ^ 1u, ctl, SITE_K_EMPTY)) { ok = false; break; }
-                if (p.inject_stall && blockIdx.x == 0 && !withheld) {
-                    withheld = true;  // never issued: the MMA warp's wait for this tile must time out
-                } else {
-                    ptx::mbar_arrive_expect_tx(bar(T::B_KFULL + s), T::KV_BYTES);
-                    const uint32_t dst = sbase + T::OFF_K + s * T::KV_BYTES;
-                    for (int c = 0; c < T::NCHUNK; ++c)
-                        ptx::tma_load_4d(dst + c * (T::BN * T::SW), tmK, bar(T::B_KFULL + s), c * T::SWE, j * T::BN,
-                                         ti.hk, ti.z, pol_kv);
-                }
-                ++ki;
-            }
-            {
-                // slot vi & 1 held block vi - 2, free once its P·V is complete
-                const uint32_t s = vi & 1u, ph = (vi >> 1) & 1u;
-                if (!wait_phase(bar(T::B_PVDONE + s), ph ^ 1u, ctl, SITE_V_EMPTY)) { ok = false; break; }
-                ptx::mbar_arrive_expect_tx(bar(T::B_VFULL + s), T::KV_BYTES);
-                const uint32_t dst = sbase + T::OFF_V + s * T::KV_BYTES;
+            // slot ki & 1 held block ki - 2, whose S is complete once that phase of s_full is
+            const uint32_t s = ki & 1u, ph = (ki >> 1) & 1u;
+            if (!wait_phase(bar(T::B_SFULL + s), ph ^ 1u, ctl, SITE_K_EMPTY)) { ok = false; break; }
+            if (p.inject_stall && blockIdx.x == 0 && !withheld) {
+                withheld = true;  // never issued: the S issuer's wait for this block must time out
+            } else {
+                ptx::mbar_arrive_expect_tx(bar(T::B_KFULL + s), T::KV_BYTES);
+                const uint32_t dst = sbase + T::OFF_K + s * T::KV_BYTES;
                 for (int c = 0; c < T::NCHUNK; ++c)
-                    ptx::tma_load_4d(dst + c * (T::BN * T::SW), tmV, bar(T::B_VFULL + s), c * T::SWE, j * T::BN,
+                    ptx::tma_load_4d(dst + c * (T::BN * T::SW), tmK, bar(T::B_KFULL + s), c * T::SWE, j * T::BN,
                                      ti.hk, ti.z, pol_kv);
-                ++vi;
+            }
+            ++ki;
+            // with two Q slots the next tile's Q can go right after the first
+            // K; with one, only after the last K (its slot frees at this
+            // tile's last S, which needs that K)
+            const int q_at = T::Q_STAGES >= 2 ? 0 : ti.nkv - 1;
+            if (j == q_at && t + (int)gridDim.x < p.ntiles && !load_q(tile_info<CAUSAL, T::BN>(t + gridDim.x, p))) {
+                ok = false;
+                break;
             }
         }
     }
@@ -235,9 +239,34 @@ __device__ void run_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, con
             drain_phase(bar(T::B_QFULL + i % T::Q_STAGES), (i / T::Q_STAGES) & 1u, lim);
         for (uint32_t i = ki > 2u ? ki - 2u : 0u; i < ki; ++i)
             drain_phase(bar(T::B_KFULL + (i & 1u)), (i >> 1) & 1u, withheld ? lim / 64 : lim);
-        for (uint32_t i = vi > 2u ? vi - 2u : 0u; i < vi; ++i)
-            drain_phase(bar(T::B_VFULL + (i & 1u)), (i >> 1) & 1u, lim);
     }
+}
+
+template <int D, bool CAUSAL>
+__device__ void run_producer_v(const CUtensorMap* tmV, const FwdParams& p, uint32_t sbase, uint32_t bar0,
+                               const Ctl& ctl) {
+    using T = Traits<D>;
+    auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+    const uint64_t pol_kv = ptx::policy_evict_last();
+    uint32_t vi = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < p.ntiles; t += gridDim.x) {
+        const TileInfo ti = tile_info<CAUSAL, T::BN>(t, p);
+        for (int j = 0; j < ti.nkv; ++j) {
+            // slot vi & 1 held block vi - 2, free once its P·V is complete
+            const uint32_t s = vi & 1u, ph = (vi >> 1) & 1u;
+            if (!wait_phase(bar(T::B_PVDONE + s), ph ^ 1u, ctl, SITE_V_EMPTY)) { ok = false; break; }
+            ptx::mbar_arrive_expect_tx(bar(T::B_VFULL + s), T::KV_BYTES);
+            const uint32_t dst = sbase + T::OFF_V + s * T::KV_BYTES;
+            for (int c = 0; c < T::NCHUNK; ++c)
+                ptx::tma_load_4d(dst + c * (T::BN * T::SW), tmV, bar(T::B_VFULL + s), c * T::SWE, j * T::BN, ti.hk,
+                                 ti.z, pol_kv);
+            ++vi;
+        }
+    }
+    if (!ok)
+        for (uint32_t i = vi > 2u ? vi - 2u : 0u; i < vi; ++i)
+            drain_phase(bar(T::B_VFULL + (i & 1u)), (i >> 1) & 1u, ctl.limit_ns);
 }
 
 // ------------------------------------------------------------ MMA issuers ---
@@ -509,7 +538,7 @@ __device__ void run_epilogue(const FwdParams& p, uint32_t bar0, uint32_t tmem, c
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
     uint32_t step = 0, ntile = 0;
     constexpr int CH = D >= 32 ? 32 : 16;               // columns per TMEM load
-    constexpr int HELD = D <= 64 ? D / CH : 64 / CH;     // chunks converted before their stores
+    constexpr int HELD = D <= 128 ? D / CH : 64 / CH;    // chunks converted before their stores
     for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++ntile) {
         const TileInfo ti = tile_info<CAUSAL, T::BN>(t, p);
         step += ti.nkv;
@@ -594,14 +623,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const Ctl ctl{abort_flag, p.status, p.wait_limit_ns};
 
     if (warp == 0) {
-        if (lane == 0) run_producer<D, CAUSAL>(&tmQ, &tmK, &tmV, p, sbase, bar0, ctl);
+        if (lane == 0) run_producer_qk<D, CAUSAL>(&tmQ, &tmK, p, sbase, bar0, ctl);
+    } else if (warp == 15) {
+        if (lane == 0) run_producer_v<D, CAUSAL>(&tmV, p, sbase, bar0, ctl);
     } else if (warp == 1) {
         if (lane == 0) run_mma_qk<D, CAUSAL, BF16>(p, sbase, bar0, tmem, ctl);
     } else if (warp == 2) {
         if (lane == 0) run_mma_pv<D, CAUSAL, BF16>(p, sbase, bar0, tmem, ctl);
     } else if (warp < 11) {
         run_softmax<D, CAUSAL, BF16>(p, bar0, tmem, hand, red, (warp - 3) / 4, ctl);
-    } else {
+    } else if (warp < 15) {
         run_epilogue<D, CAUSAL, BF16>(p, bar0, tmem, hand, ctl);
     }
 

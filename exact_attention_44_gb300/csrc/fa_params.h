@@ -6,9 +6,10 @@
 namespace fa {
 
 constexpr int BM = 128;            // query rows per tile (one TMEM lane per row)
-// warp 0: TMA, warp 1: S = Q Kᵀ issuer, warp 2: O += P V issuer, warps 3-6 and
-// 7-10: softmax of the two column halves of each key block, warps 11-14: epilogue
-constexpr int NUM_THREADS = 480;
+// warp 0: Q/K loads, warp 1: S = Q Kᵀ issuer, warp 2: O += P V issuer, warps
+// 3-6 and 7-10: softmax of the two column halves of each key block, warps
+// 11-14: epilogue, warp 15: V loads
+constexpr int NUM_THREADS = 512;
 
 // Where a bounded wait gave up; recorded in bits 8-15 of the device status word.
 enum WaitSite : uint32_t {

@@ -33,12 +33,13 @@ def to_device(bits: np.ndarray, dtype: str, device="cuda"):
 def run_gpu(q, k, v, dtype, scale, causal, layout="bnsd", o_layout="bnsd"):
     """Run libfa on seeded bits; returns (O as float64 numpy (Z,Hq,Nq,D), lse float64 (Z,Hq,Nq))."""
     import torch
-    from exact_attention_44_gb300 import fa_fwd
+    from exact_attention_44_gb300 import fa_device_status, fa_fwd
 
     qt, kt, vt = (relayout(to_device(x, dtype), layout) for x in (q, k, v))
     o = relayout(torch.empty(qt.shape, dtype=qt.dtype, device="cuda"), o_layout)
     o, lse = fa_fwd(qt, kt, vt, o=o, scale=scale, causal=causal)
-    torch.cuda.synchronize()
+    code, word = fa_device_status()
+    assert code == 0, f"device status {word:#x}: a bounded wait ran out"
     return o.double().cpu().numpy(), lse.double().cpu().numpy()
 
 
