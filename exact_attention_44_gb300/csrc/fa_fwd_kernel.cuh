@@ -57,10 +57,12 @@ struct Traits {
     // that block is complete, V slot s once its P·V is; those two commits
     // release the slots, so no separate "empty" barriers exist.
     static constexpr int KV_STAGES = 2;
-    // tensor memory columns (lane = query row)
-    static constexpr uint32_t TM_S = 0;                        // S[b] at TM_S + b * BN (fp32)
-    static constexpr uint32_t TM_P = 2 * BN;                   // P[b] at TM_P + b * BN/2 (2 x 16 bit per column)
-    static constexpr uint32_t TM_O = 3 * BN;                   // O, D fp32 columns
+    // tensor memory columns (lane = query row): a ring of SR score blocks,
+    // each holding S_g (BN fp32 columns) and then, in its first BN/2
+    // columns, P_g (two 16-bit values per column); then O (D fp32 columns)
+    static constexpr int SR = 3;
+    static constexpr uint32_t TM_S = 0;                        // S/P ring slot r at TM_S + r * BN
+    static constexpr uint32_t TM_O = SR * BN;                  // O
     static constexpr uint32_t TMEM_COLS = 512;
     static_assert(TM_O + D <= TMEM_COLS, "tensor memory budget");
     // shared memory (offsets from a 1024-byte aligned base)
@@ -77,10 +79,10 @@ struct Traits {
     static constexpr int B_QEMPTY = B_QFULL + Q_STAGES;
     static constexpr int B_KFULL = B_QEMPTY + Q_STAGES;        // [2] K tile landed (TMA)
     static constexpr int B_VFULL = B_KFULL + KV_STAGES;        // [2] V tile landed (TMA)
-    static constexpr int B_SFULL = B_VFULL + KV_STAGES;        // [2] S_g ready; K slot g&1 free (commit)
-    static constexpr int B_PFULL = B_SFULL + 2;                // [2] P_g written (256 softmax threads)
-    static constexpr int B_PVDONE = B_PFULL + 2;               // [2] O += P_g V_g complete; V slot g&1 free (commit)
-    static constexpr int B_EPIFULL = B_PVDONE + 2;             // [2] m, l of a tile handed over (256)
+    static constexpr int B_SFULL = B_VFULL + KV_STAGES;        // [SR] S_g ready; K slot free (commit)
+    static constexpr int B_PFULL = B_SFULL + SR;               // [SR] P_g written (256 softmax threads)
+    static constexpr int B_PVDONE = B_PFULL + SR;              // [SR] O += P_g V_g complete; slot and V slot free (commit)
+    static constexpr int B_EPIFULL = B_PVDONE + SR;            // [2] m, l of a tile handed over (256)
     static constexpr int B_EPIEMPTY = B_EPIFULL + 2;           // [2] hand-over slot read (128)
     static constexpr int B_OFREE = B_EPIEMPTY + 2;             // O read out of TMEM (128)
     static constexpr int B_RED = B_OFREE + 1;                  // [2] both halves' partial maxima written (256)
@@ -93,7 +95,7 @@ struct Traits {
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
     static __device__ __forceinline__ uint32_t bar_count(int i) {
-        if (i >= B_PFULL && i < B_PFULL + 2) return 256;
+        if (i >= B_PFULL && i < B_PFULL + SR) return 256;
         if (i >= B_EPIFULL && i < B_EPIFULL + 2) return 256;
         if (i >= B_EPIEMPTY && i < B_OFREE + 1) return 128;
         if (i >= B_RED && i < B_RED + 2) return 256;
@@ -144,6 +146,12 @@ __device__ __forceinline__ bool drain_phase(uint32_t bar, uint32_t parity, uint6
 struct TileInfo {
     int z, hq, hk, q_start, nkv;
 };
+
+// Barrier slot and phase parity of key block g (global count) in a ring of R.
+template <int R>
+__device__ __forceinline__ uint32_t rslot(uint32_t g) { return g % R; }
+template <int R>
+__device__ __forceinline__ uint32_t rphase(uint32_t g) { return (g / R) & 1u; }
 
 // Tile t of the static schedule.  Non-causal: head-major, so the CTAs running
 // at the same time share a head's K/V in L2.  Causal: query blocks from the
@@ -208,9 +216,10 @@ __device__ void run_producer_qk(const CUtensorMap* tmQ, const CUtensorMap* tmK, 
     for (; ok && t < p.ntiles; t += gridDim.x) {
         const TileInfo ti = tile_info<CAUSAL, T::BN>(t, p);
         for (int j = 0; j < ti.nkv; ++j) {
-            // slot ki & 1 held block ki - 2, whose S is complete once that phase of s_full is
-            const uint32_t s = ki & 1u, ph = (ki >> 1) & 1u;
-            if (!wait_phase(bar(T::B_SFULL + s), ph ^ 1u, ctl, SITE_K_EMPTY)) { ok = false; break; }
+            // slot ki & 1 held block ki - 2, free once S of that block is complete
+            const uint32_t s = ki & 1u;
+            if (ki >= 2 && !wait_phase(bar(T::B_SFULL + rslot<T::SR>(ki - 2)), rphase<T::SR>(ki - 2), ctl,
+                                       SITE_K_EMPTY)) { ok = false; break; }
             if (p.inject_stall && blockIdx.x == 0 && !withheld) {
                 withheld = true;  // never issued: the S issuer's wait for this block must time out
             } else {
@@ -254,8 +263,9 @@ __device__ void run_producer_v(const CUtensorMap* tmV, const FwdParams& p, uint3
         const TileInfo ti = tile_info<CAUSAL, T::BN>(t, p);
         for (int j = 0; j < ti.nkv; ++j) {
             // slot vi & 1 held block vi - 2, free once its P·V is complete
-            const uint32_t s = vi & 1u, ph = (vi >> 1) & 1u;
-            if (!wait_phase(bar(T::B_PVDONE + s), ph ^ 1u, ctl, SITE_V_EMPTY)) { ok = false; break; }
+            const uint32_t s = vi & 1u;
+            if (vi >= 2 && !wait_phase(bar(T::B_PVDONE + rslot<T::SR>(vi - 2)), rphase<T::SR>(vi - 2), ctl,
+                                       SITE_V_EMPTY)) { ok = false; break; }
             ptx::mbar_arrive_expect_tx(bar(T::B_VFULL + s), T::KV_BYTES);
             const uint32_t dst = sbase + T::OFF_V + s * T::KV_BYTES;
             for (int c = 0; c < T::NCHUNK; ++c)
@@ -295,13 +305,17 @@ __device__ void run_mma_qk(const FwdParams& p, uint32_t sbase, uint32_t bar0, ui
         if (!wait_phase(bar(T::B_QFULL + qs), (qi / T::Q_STAGES) & 1u, ctl, SITE_Q_FULL)) { ok = false; break; }
         const uint32_t q_lo = q_lo0 + qs * (T::Q_BYTES >> 4);
         for (int j = 0; j < ti.nkv; ++j, ++g) {
-            const uint32_t b = g & 1u, ph = (g >> 1) & 1u;
-            if (!wait_phase(bar(T::B_KFULL + b), ph, ctl, SITE_K_FULL)) { ok = false; break; }
-            // S[b] still holds S_{g-2} until the softmax has read it (P_{g-2} written)
-            if (!wait_phase(bar(T::B_PFULL + b), ph ^ 1u, ctl, SITE_S_FREE)) { ok = false; break; }
+            const uint32_t kb = g & 1u, r = rslot<T::SR>(g);
+            if (!wait_phase(bar(T::B_KFULL + kb), (g >> 1) & 1u, ctl, SITE_K_FULL)) { ok = false; break; }
+            // ring slot r held block g - SR (S, then P) until O += P V of that
+            // block completed; the softmax, seeing S_g, may then overwrite it
+            if (g >= (uint32_t)T::SR && !wait_phase(bar(T::B_PVDONE + r), rphase<T::SR>(g - T::SR), ctl, SITE_S_FREE)) {
+                ok = false;
+                break;
+            }
             ptx::tc_fence_after();
-            const uint32_t k_lo = k_lo0 + b * (T::KV_BYTES >> 4);
-            const uint32_t d_tmem = tmem + T::TM_S + b * T::BN;
+            const uint32_t k_lo = k_lo0 + kb * (T::KV_BYTES >> 4);
+            const uint32_t d_tmem = tmem + T::TM_S + r * T::BN;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t a_off = (((kk * 16) / T::SWE) * (BM * T::SW) + ((kk * 16) % T::SWE) * 2) >> 4;
@@ -309,7 +323,7 @@ __device__ void run_mma_qk(const FwdParams& p, uint32_t sbase, uint32_t bar0, ui
                 ptx::mma_ss(d_tmem, ptx::desc64(q_lo + a_off, HI), ptx::desc64(k_lo + b_off, HI), IDESC,
                             kk > 0 ? 1u : 0u);
             }
-            ptx::tc_commit(bar(T::B_SFULL + b));  // S ready, K slot b free
+            ptx::tc_commit(bar(T::B_SFULL + r));  // S ready, K slot kb free
             if (j == ti.nkv - 1) {
                 ptx::tc_commit(bar(T::B_QEMPTY + qs));  // last use of this Q tile
                 ++qi;
@@ -337,20 +351,20 @@ __device__ void run_mma_pv(const FwdParams& p, uint32_t sbase, uint32_t bar0, ui
     for (int t = blockIdx.x; ok && t < p.ntiles; t += gridDim.x, ++ntile) {
         const TileInfo ti = tile_info<CAUSAL, T::BN>(t, p);
         for (int j = 0; j < ti.nkv; ++j, ++g) {
-            const uint32_t b = g & 1u, ph = (g >> 1) & 1u;
+            const uint32_t vb = g & 1u, r = rslot<T::SR>(g);
             if (j == 0 && ntile > 0 &&
                 !wait_phase(bar(T::B_OFREE), (ntile - 1) & 1u, ctl, SITE_O_FREE)) { ok = false; break; }
-            if (!wait_phase(bar(T::B_PFULL + b), ph, ctl, SITE_P_FULL)) { ok = false; break; }
-            if (!wait_phase(bar(T::B_VFULL + b), ph, ctl, SITE_V_FULL)) { ok = false; break; }
+            if (!wait_phase(bar(T::B_PFULL + r), rphase<T::SR>(g), ctl, SITE_P_FULL)) { ok = false; break; }
+            if (!wait_phase(bar(T::B_VFULL + vb), (g >> 1) & 1u, ctl, SITE_V_FULL)) { ok = false; break; }
             ptx::tc_fence_after();
-            const uint32_t v_lo = v_lo0 + b * (T::KV_BYTES >> 4);
-            const uint32_t a_tmem = tmem + T::TM_P + b * (T::BN / 2);
+            const uint32_t v_lo = v_lo0 + vb * (T::KV_BYTES >> 4);
+            const uint32_t a_tmem = tmem + T::TM_S + r * T::BN;  // P_g over the first BN/2 columns of the slot
             const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
             for (int kk = 0; kk < T::BN / 16; ++kk)
                 ptx::mma_ts(tmem + T::TM_O, a_tmem + kk * 8, ptx::desc64(v_lo + ((kk * 16 * T::SW) >> 4), HI), IDESC,
                             kk > 0 ? 1u : acc0);
-            ptx::tc_commit(bar(T::B_PVDONE + b));  // O updated, P[b] and V slot b free
+            ptx::tc_commit(bar(T::B_PVDONE + r));  // O updated, ring slot r and V slot vb free
         }
     }
     if (!ok) {
@@ -431,16 +445,18 @@ __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, fl
         // ("Write Triton Attention Kernel", step 4; the initial l is 0)
         float m = -INFINITY, l = 0.f;
         for (int j = 0; j < ti.nkv; ++j) {
-            const uint32_t b = step & 1u, ph = (step >> 1) & 1u;
-            if (!warp_wait_phase(bar(T::B_SFULL + b), ph, ctl, SITE_S_FULL)) return;
+            const uint32_t r = rslot<T::SR>(step);      // ring slot of S_j / P_j
+            const uint32_t b = step & 1u, ph = (step >> 1) & 1u;  // max-exchange slot
+            if (!warp_wait_phase(bar(T::B_SFULL + r), rphase<T::SR>(step), ctl, SITE_S_FULL)) return;
             ptx::tc_fence_after();
+            const uint32_t s_addr = tmem + lane_addr + T::TM_S + r * BN;
             float s[HC];
 #pragma unroll
             for (int i = 0; i < HC / 32; ++i) {
-                uint32_t r[32];
-                ptx::tmem_ld32(tmem + lane_addr + T::TM_S + b * BN + h * HC + 32 * i, r);
+                uint32_t rr[32];
+                ptx::tmem_ld32(s_addr + h * HC + 32 * i, rr);
 #pragma unroll
-                for (int x = 0; x < 32; ++x) s[32 * i + x] = __uint_as_float(r[x]);
+                for (int x = 0; x < 32; ++x) s[32 * i + x] = __uint_as_float(rr[x]);
             }
             // the mask goes on the scores before the row max (Correctness
             // requirements); only the diagonal block and the key tail need it
@@ -458,59 +474,63 @@ __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, fl
                 mx0 = ptx::fmax3(mx0, s[x], s[x + 1]);
                 mx1 = ptx::fmax3(mx1, s[x + 2], s[x + 3]);
             }
-            // swap partial maxima with the other half (slot b is free: every
-            // thread read it two blocks ago before arriving on it last block)
-            red[(b * 2 + h) * BM + row] = fmaxf(mx0, mx1);
+            // Swap partial maxima with the other half.  Arriving also says this
+            // thread's S is in registers: P is written over the slot's first
+            // columns only once both halves have arrived.  (Exchange slot b is
+            // free: every thread read it two blocks ago before arriving last block.)
+            const float pmax = fmaxf(mx0, mx1);
+            red[(b * 2 + h) * BM + row] = pmax;
             ptx::mbar_arrive(bar(T::B_RED + b));
-            if (!warp_wait_phase(bar(T::B_RED + b), ph, ctl, SITE_MAX_XCHG)) return;
-            const float m_tile = fmaxf(fmaxf(mx0, mx1), red[(b * 2 + (h ^ 1)) * BM + row]) * c;  // scale > 0
-            float alpha = 1.f;
-            bool rescale = false;
             if (j == 0) {
-                m = m_tile;
-            } else if (__any_sync(0xffffffffu, m_tile > m + RESCALE_LOG2)) {
-                // both halves take this branch for the same rows (same m, m_tile)
-                const float m_new = fmaxf(m, m_tile);
-                alpha = ptx::ex2(m - m_new);
-                m = m_new;
-                rescale = true;
+                // the first block sets the reference maximum m
+                if (!warp_wait_phase(bar(T::B_RED + b), ph, ctl, SITE_MAX_XCHG)) return;
+                m = fmaxf(pmax, red[(b * 2 + (h ^ 1)) * BM + row]) * c;  // scale > 0
             }
-            // P[b] was last read by the P·V of two blocks ago: wait for it
-            // (it has long finished; S and P·V are issued by different threads)
-            if (!warp_wait_phase(bar(T::B_PVDONE + b), ph ^ 1u, ctl, SITE_P_FREE)) return;
-            // p = 2^(s·scale·log2e − m); l sums the fp32 p, P V uses p cast to
-            // the input type
-            const uint64_t negm2 = ptx::pack_f32x2(-m, -m);
-            uint64_t sum2 = ptx::pack_f32x2(0.f, 0.f);
-            const uint32_t p_addr = tmem + lane_addr + T::TM_P + b * (BN / 2) + h * (HC / 2);
-#pragma unroll
-            for (int i = 0; i < (HC + 63) / 64; ++i) {
-                constexpr int NP = HC >= 64 ? 32 : HC / 2;  // packed columns per store
-                uint32_t pk[NP];
+            // p = 2^(s·scale·log2e − m) against the current reference m; l sums
+            // the fp32 p, P V uses p cast to the input type
+            constexpr int NP = HC / 2;  // packed P columns of this half
+            uint32_t pk[NP];
+            auto exps = [&](float ref) -> uint64_t {
+                const uint64_t negm2 = ptx::pack_f32x2(-ref, -ref);
+                uint64_t sum2 = ptx::pack_f32x2(0.f, 0.f);
 #pragma unroll
                 for (int x = 0; x < NP; ++x) {
                     float a0, a1;
-                    ptx::unpack_f32x2(ptx::ffma2(ptx::pack_f32x2(s[64 * i + 2 * x], s[64 * i + 2 * x + 1]), c2, negm2),
-                                      a0, a1);
+                    ptx::unpack_f32x2(ptx::ffma2(ptx::pack_f32x2(s[2 * x], s[2 * x + 1]), c2, negm2), a0, a1);
                     const float p0 = ptx::ex2(a0), p1 = ptx::ex2(a1);
                     sum2 = ptx::fadd2(sum2, ptx::pack_f32x2(p0, p1));
                     pk[x] = pack2<BF16>(p0, p1);
                 }
-                if constexpr (NP == 32) ptx::tmem_st32(p_addr + 32 * i, pk);
-                else ptx::tmem_st16(p_addr + 16 * i, pk);
+                return sum2;
+            };
+            uint64_t sum2 = exps(m);
+            float alpha = 1.f;
+            if (j > 0) {
+                // the block maximum arrives while the exponentials run; only
+                // when it exceeds m by more than 2^RESCALE_LOG2 are P redone
+                // against the new maximum, and O and l rescaled by alpha before
+                // this block is added to them (Kernel design rules).  Both
+                // halves see the same values, so both take the same branch.
+                if (!warp_wait_phase(bar(T::B_RED + b), ph, ctl, SITE_MAX_XCHG)) return;
+                const float m_tile = fmaxf(pmax, red[(b * 2 + (h ^ 1)) * BM + row]) * c;
+                if (__any_sync(0xffffffffu, m_tile > m + RESCALE_LOG2)) {
+                    const float m_new = fmaxf(m, m_tile);
+                    alpha = ptx::ex2(m - m_new);
+                    m = m_new;
+                    sum2 = exps(m);
+                    const uint32_t g = step - 1;
+                    if (!warp_wait_phase(bar(T::B_PVDONE + rslot<T::SR>(g)), rphase<T::SR>(g), ctl, SITE_PV_DONE))
+                        return;
+                    ptx::tc_fence_after();
+                    rescale_o<D / 2>(tmem + lane_addr + T::TM_O + h * (D / 2), alpha);
+                }
             }
-            if (rescale) {
-                // O and l are rescaled by alpha before this block is added to
-                // them (Kernel design rules): wait until O += P_{j-1} V_{j-1}
-                // has landed, then scale this half's columns of O in place.
-                const uint32_t g = step - 1;
-                if (!warp_wait_phase(bar(T::B_PVDONE + (g & 1u)), (g >> 1) & 1u, ctl, SITE_PV_DONE)) return;
-                ptx::tc_fence_after();
-                rescale_o<D / 2>(tmem + lane_addr + T::TM_O + h * (D / 2), alpha);
-            }
+            // P_j over the first BN/2 columns of its slot: keys h*HC.. at packed column h*HC/2
+            if constexpr (NP == 32) ptx::tmem_st32(s_addr + h * NP, pk);
+            else ptx::tmem_st16(s_addr + h * NP, pk);
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(bar(T::B_PFULL + b));
+            ptx::mbar_arrive(bar(T::B_PFULL + r));
             float sl, sh;
             ptx::unpack_f32x2(sum2, sl, sh);
             l = l * alpha + (sl + sh);
@@ -548,7 +568,7 @@ __device__ void run_epilogue(const FwdParams& p, uint32_t bar0, uint32_t tmem, c
         const float l = hand[slot * 3 * BM + BM + row] + hand[slot * 3 * BM + 2 * BM + row];
         ptx::mbar_arrive(bar(T::B_EPIEMPTY + slot));
         const uint32_t g = step - 1;  // the tile's last P·V
-        if (!warp_wait_phase(bar(T::B_PVDONE + (g & 1u)), (g >> 1) & 1u, ctl, SITE_PV_DONE)) return;
+        if (!warp_wait_phase(bar(T::B_PVDONE + rslot<T::SR>(g)), rphase<T::SR>(g), ctl, SITE_PV_DONE)) return;
         ptx::tc_fence_after();
 
         const int q_row = ti.q_start + row;
