@@ -7,7 +7,9 @@ product library never does, and the two share no code.  Inputs come from the
 ``seeded_inputs`` module as uint16 bit patterns.
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` against closed
-forms, invariants, library routines (numpy/scipy) and an mpmath brute force.
+forms, invariants, library routines (numpy/scipy) and an mpmath brute force;
+the merge of results over disjoint key sets is pinned against the attention
+forward over their union.
 """
 from __future__ import annotations
 
@@ -66,6 +68,9 @@ def load(source: str | None = None, tag: str = "") -> ctypes.CDLL:
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_double, ctypes.c_int, ctypes.c_void_p, ctypes.c_int64,
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+            lib.oracle_lse_merge.restype = ctypes.c_int
+            lib.oracle_lse_merge.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                             ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
             lib.oracle_decode.restype = ctypes.c_double
             lib.oracle_decode.argtypes = [ctypes.c_uint16, ctypes.c_int]
             _libs[path] = lib
@@ -118,3 +123,27 @@ def attention_fwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, dtype: str, scale
     if rows is None:
         return o.reshape(Z, Hq, Nq, D), lse.reshape(Z, Hq, Nq)
     return o, lse
+
+
+def lse_merge(o_parts, lse_parts, lib: ctypes.CDLL | None = None):
+    """Combine results over disjoint key sets in float64 (``oracle_lse_merge``).
+
+    o_parts: sequence of float64 arrays of one shape (..., D); lse_parts:
+    matching arrays of shape (...) in natural-log units.  Returns (o, lse)
+    for the union of the key sets.
+    """
+    lib = lib or load()
+    n = len(o_parts)
+    if n < 1 or n != len(lse_parts):
+        raise ValueError("need at least one part and one lse per part")
+    shape = np.shape(o_parts[0])
+    D = shape[-1]
+    rows = int(np.prod(shape[:-1], dtype=np.int64))
+    op = np.ascontiguousarray(np.stack([np.asarray(x, dtype=np.float64).reshape(rows, D) for x in o_parts]))
+    lp = np.ascontiguousarray(np.stack([np.asarray(x, dtype=np.float64).reshape(rows) for x in lse_parts]))
+    o = np.empty((rows, D), dtype=np.float64)
+    lse = np.empty(rows, dtype=np.float64)
+    rc = lib.oracle_lse_merge(n, op.ctypes.data, lp.ctypes.data, rows, D, o.ctypes.data, lse.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle_lse_merge: invalid arguments")
+    return o.reshape(shape), lse.reshape(shape[:-1])

@@ -22,6 +22,13 @@
  *   3. O[d]  = sum_j (exp(s_j - M) / L) V[z,hk,j,d]
  *   4. lse   = M + ln L
  * The whole row of S is materialised; nothing is tiled, fused or reordered.
+ *
+ * It also states the combination of results computed over disjoint key sets
+ * (oracle_lse_merge below): the sum over a union of key sets is the sum of
+ * the per-set sums, so with each set's lse_s = log sum_j exp(s_j) and its
+ * normalised O_s, lse = log sum_s exp(lse_s) and O = sum_s exp(lse_s - lse) O_s
+ * -- the max-shifted rescaling of the page "Write Triton Attention Kernel"
+ * (Kernel design rules) applied to whole sets instead of key blocks.
  */
 #include <math.h>
 #include <pthread.h>
@@ -173,4 +180,39 @@ int oracle_attention_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v
     }
     free(jobs); free(tid); free(created); free(table); free(kd); free(vd);
     return status;
+}
+
+/*
+ * Combination of nparts results over disjoint key sets, row by row, in
+ * float64: o_parts is (nparts, rows, D), lse_parts (nparts, rows), natural
+ * log.  For each row: M = max_s lse_s; if M = -inf (no key in any set) the
+ * row gets O = 0 and lse = -inf; otherwise
+ *   w_s = exp(lse_s - M),  L = sum_s w_s,  O = sum_s w_s O_s / L,  lse = M + ln L.
+ * Returns 0, or -1 for invalid arguments.
+ */
+int oracle_lse_merge(int nparts, const double* o_parts, const double* lse_parts, int64_t rows, int D, double* o,
+                     double* lse) {
+    if (nparts < 1 || rows < 0 || D < 1) return -1;
+    for (int64_t r = 0; r < rows; ++r) {
+        double M = -INFINITY;
+        for (int s = 0; s < nparts; ++s) {
+            const double x = lse_parts[(int64_t)s * rows + r];
+            M = x > M ? x : M;
+        }
+        double* out = o + r * D;
+        for (int d = 0; d < D; ++d) out[d] = 0.0;
+        if (M == -INFINITY) {
+            lse[r] = -INFINITY;
+            continue;
+        }
+        double L = 0.0;
+        for (int s = 0; s < nparts; ++s) L += exp(lse_parts[(int64_t)s * rows + r] - M);
+        for (int s = 0; s < nparts; ++s) {
+            const double w = exp(lse_parts[(int64_t)s * rows + r] - M) / L;
+            const double* os = o_parts + ((int64_t)s * rows + r) * D;
+            for (int d = 0; d < D; ++d) out[d] += w * os[d];
+        }
+        lse[r] = M + log(L);
+    }
+    return 0;
 }

@@ -26,6 +26,15 @@ MUTANTS = {
     "fp16 exponent bias": ("mag = ldexp((double)(1024 + f), e - 25);", "mag = ldexp((double)(1024 + f), e - 24);"),
     "bf16 fraction width": ("mag = ldexp((double)(128 + f), e - 134);", "mag = ldexp((double)(128 + f), e - 133);"),
     "sign of score": ("s[j] = J->scale * acc;", "s[j] = -J->scale * acc;"),
+    "merge drops max": ("lse[r] = M + log(L);", "lse[r] = log(L);"),
+    "merge unnormalised": ("const double w = exp(lse_parts[(int64_t)s * rows + r] - M) / L;",
+                           "const double w = exp(lse_parts[(int64_t)s * rows + r] - M);"),
+    "merge weight sign": ("const double w = exp(lse_parts[(int64_t)s * rows + r] - M) / L;",
+                          "const double w = exp(M - lse_parts[(int64_t)s * rows + r]) / L;"),
+    "merge part index": ("const double* os = o_parts + ((int64_t)s * rows + r) * D;",
+                         "const double* os = o_parts + ((int64_t)0 * rows + r) * D;"),
+    "merge unshifted normaliser": ("L += exp(lse_parts[(int64_t)s * rows + r] - M);",
+                                   "L += exp(lse_parts[(int64_t)s * rows + r]);"),
 }
 
 PIN_CALLS = [
@@ -41,6 +50,9 @@ PIN_CALLS = [
     ("scipy", lambda: pins.test_matches_scipy("fp16", True, (2, 4, 2, 37, 53, 32))),
     ("gqa", pins.test_gqa_equals_mha_on_repeated_kv),
     ("prefix", pins.test_causal_row_is_prefix_attention),
+    ("merge shards", lambda: pins.test_merge_of_key_shards_is_attention_over_their_union((0, 40, 97))),
+    ("merge closed form", pins.test_merge_two_parts_closed_form),
+    ("merge equal lse", pins.test_merge_equal_lse_gives_mean_and_log_count),
 ]
 
 

@@ -241,3 +241,58 @@ def test_rejects_invalid_arguments():
         oracle.attention_fwd(q, k, v, "fp16", float("nan"), False)
     with pytest.raises(ValueError):
         oracle.attention_fwd(q, k, v, "fp16", 0.1, False, rows=np.array([8]))
+
+
+# ------------------------------------------------- merge over disjoint key sets ----
+# The sum over a union of key sets is the sum of the per-set sums: merging the
+# oracle's results over key shards must reproduce its result over all keys.
+
+@pytest.mark.parametrize("cuts", [(0, 40, 97), (0, 1, 96, 97), (0, 13, 50, 51, 97)])
+def test_merge_of_key_shards_is_attention_over_their_union(cuts):
+    dtype = "fp16"
+    q, k, v = si.qkv(21, 2, 4, 2, 19, 97, 32, dtype)
+    scale = 0.7  # score spread of a few units, so the shards' lse differ widely
+    o_full, lse_full = oracle.attention_fwd(q, k, v, dtype, scale, False)
+    parts = [oracle.attention_fwd(q, k[:, :, a:b], v[:, :, a:b], dtype, scale, False) for a, b in zip(cuts, cuts[1:])]
+    assert max(np.ptp(np.stack([p[1] for p in parts]), axis=0).ravel()) > 2.0
+    o, lse = oracle.lse_merge([p[0] for p in parts], [p[1] for p in parts])
+    np.testing.assert_allclose(o, o_full, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_full, rtol=0, atol=1e-12)
+
+
+def test_merge_single_part_is_identity():
+    rng = np.random.default_rng(3)
+    o = rng.standard_normal((3, 5, 16))
+    lse = rng.standard_normal((3, 5)) * 10
+    mo, ml = oracle.lse_merge([o], [lse])
+    assert np.array_equal(mo, o) and np.array_equal(ml, lse)
+
+
+def test_merge_two_parts_closed_form():
+    # lse = log 1 and log 3: weights 1/4 and 3/4, merged lse = log 4
+    rng = np.random.default_rng(4)
+    o1, o2 = rng.standard_normal((2, 7, 8))
+    mo, ml = oracle.lse_merge([o1, o2], [np.full(7, 0.0), np.full(7, math.log(3.0))])
+    np.testing.assert_allclose(mo, (o1 + 3 * o2) / 4, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(ml, math.log(4.0), rtol=0, atol=1e-14)
+
+
+def test_merge_equal_lse_gives_mean_and_log_count():
+    rng = np.random.default_rng(5)
+    parts = [rng.standard_normal((4, 8)) for _ in range(5)]
+    c = 123.25  # far from 0: the shift by the maximum matters
+    mo, ml = oracle.lse_merge(parts, [np.full(4, c)] * 5)
+    np.testing.assert_allclose(mo, np.mean(parts, axis=0), rtol=0, atol=1e-14)
+    np.testing.assert_allclose(ml, c + math.log(5.0), rtol=0, atol=1e-12)
+
+
+def test_merge_ignores_empty_parts():
+    rng = np.random.default_rng(6)
+    a, b = rng.standard_normal((2, 6, 16))
+    la, lb = rng.standard_normal((2, 6))
+    junk = np.full((6, 16), 1e30)
+    mo, ml = oracle.lse_merge([a, junk, b], [la, np.full(6, -np.inf), lb])
+    ro, rl = oracle.lse_merge([a, b], [la, lb])
+    assert np.array_equal(mo, ro) and np.array_equal(ml, rl)
+    eo, el = oracle.lse_merge([a, b], [np.full(6, -np.inf)] * 2)
+    assert np.all(eo == 0) and np.all(el == -np.inf)
