@@ -47,10 +47,16 @@ WORKLOADS = {
     "z8_h16_n2048_d128_bf16": (8, 16, 16, 2048, 2048, 128, "bf16", [False, True]),
     "z8_h16_n2048_d256_bf16": (8, 16, 16, 2048, 2048, 256, "bf16", [False, True]),
     "z1_h2_n128_d64_fp16_tiny": (1, 2, 2, 128, 128, 64, "fp16", [False]),
+    # few query tiles against many keys: the shapes fa_fwd_splitkv is for
+    "z1_hq32_hkv8_nq1_nkv32768_d128_bf16_decode": (1, 32, 8, 1, 32768, 128, "bf16", [False]),
+    "z1_h8_nq128_nkv65536_d128_bf16": (1, 8, 8, 128, 65536, 128, "bf16", [False]),
 }
 MAIN = "z4_h16_n1024_d128_bf16"
 # the shapes the throughput target is stated on (D = 128, N >= 4096, non-causal)
 TARGET_SHAPES = ["z1_hq32_hkv8_n8192_d128_bf16_noncausal", "z1_hq32_hkv8_nq1024_nkv8192_d128_bf16_cross"]
+# timed through both entry points: whole tiles (fa_fwd) and cut key ranges where that pays (fa_fwd_splitkv)
+SPLIT_SHAPES = TARGET_SHAPES + ["z1_hq32_hkv8_n32768_d128_bf16_causal", "z1_hq32_hkv8_nq1_nkv32768_d128_bf16_decode",
+                                "z1_h8_nq128_nkv65536_d128_bf16"]
 
 
 def flops_of(Z, Hq, Nq, Nkv, D, causal) -> float:
@@ -259,6 +265,8 @@ def run_native(args, rank, world, device):
         result["e2e"] = run_e2e(args, wl, host, flags, scale, device, stream, world)
     if args.shapes and rank == 0:
         result["target_shapes"] = [measure_shape(name, device, stream, peaks) for name in TARGET_SHAPES]
+        result["split_kv_shapes"] = [measure_shape(name, device, stream, peaks, impl=impl)
+                                     for name in SPLIT_SHAPES for impl in ("fwd", "splitkv")]
     return result
 
 
@@ -303,8 +311,11 @@ def run_e2e(args, wl, host, flags, scale, device, stream, world):
             "ms_per_step": round(ms / steps, 4)}
 
 
-def measure_shape(name, device, stream, peaks, steps=10):
-    """TFLOP/s of one extra workload (same timing method, 10 steps, inputs > L2 or rotated)."""
+def measure_shape(name, device, stream, peaks, steps=10, impl="fwd"):
+    """TFLOP/s of one extra workload (same timing method, 10 steps, inputs > L2 or rotated).
+
+    impl "fwd" calls fa_fwd; "splitkv" calls fa_fwd_splitkv, which cuts the key
+    ranges across SMs when that beats whole tiles."""
     import torch
 
     import exact_attention_44_gb300 as fa
@@ -317,22 +328,33 @@ def measure_shape(name, device, stream, peaks, steps=10):
     sets = [dev0] + [[x.clone() for x in dev0] for _ in range(nsets - 1)]
     o = torch.empty((Z, Hq, Nq, D), dtype=dev0[0].dtype, device=device)
     lse = torch.empty((Z, Hq, Nq), dtype=torch.float32, device=device)
+    ws = fa.workspace_for(D, device) if impl == "splitkv" else None
+
+    def call(i, c):
+        if impl == "splitkv":
+            fa.fa_fwd_splitkv(*sets[i % nsets], o=o, lse=lse, scale=scale, causal=c, workspace=ws, stream=stream)
+        else:
+            fa.fa_fwd(*sets[i % nsets], o=o, lse=lse, scale=scale, causal=c, stream=stream)
+
     for i in range(3):
         for c in flags:
-            fa.fa_fwd(*sets[i % nsets], o=o, lse=lse, scale=scale, causal=c, stream=stream)
+            call(i, c)
     torch.cuda.synchronize(device)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
     for i in range(steps):
         for c in flags:
-            fa.fa_fwd(*sets[i % nsets], o=o, lse=lse, scale=scale, causal=c, stream=stream)
+            call(i, c)
     b.record(stream)
     torch.cuda.synchronize(device)
     ms = a.elapsed_time(b) / steps
     tf = step_flops(wl) / (ms * 1e-3) / 1e12
-    del sets, dev0
+    code, word = fa.fa_device_status(stream)
+    if code != fa.FA_OK:
+        raise RuntimeError(f"device status after {name}: {word:#x}")
+    del sets, dev0, ws
     torch.cuda.empty_cache()
-    return {"workload": name, "tflops": round(tf, 2), "frac_of_peak": round(tf / peaks["bf16_tflops"], 4),
+    return {"workload": name, "impl": impl, "tflops": round(tf, 2), "frac_of_peak": round(tf / peaks["bf16_tflops"], 4),
             "ms_per_step": round(ms, 4), "steps": steps}
 
 
@@ -489,10 +511,11 @@ def main(argv=None):
             for causal in wl[7]:
                 single = wl[:7] + ([causal],)
                 WORKLOADS[name + ("_causal" if causal else "_noncausal")] = single
-                r = measure_shape(name + ("_causal" if causal else "_noncausal"), device,
-                                  torch.cuda.current_stream(device), peaks, steps=20)
-                r.update(dtype=wl[6], causal=causal)
-                print(json.dumps(r), flush=True)
+                for impl in ("fwd", "splitkv"):
+                    r = measure_shape(name + ("_causal" if causal else "_noncausal"), device,
+                                      torch.cuda.current_stream(device), peaks, steps=20, impl=impl)
+                    r.update(dtype=wl[6], causal=causal)
+                    print(json.dumps(r), flush=True)
         return 0
     result = run_native(args, rank, world, device)
     if rank == 0:

@@ -20,6 +20,8 @@ FA_ERR_UNSUPPORTED = 2
 FA_ERR_ALIGNMENT = 3
 FA_ERR_CUDA = 4
 FA_ERR_DEVICE_TIMEOUT = 5
+FA_ERR_WORKSPACE = 6
+FA_MERGE_MAX_PARTS = 16
 FA_DTYPE_F16 = 0
 FA_DTYPE_BF16 = 1
 
@@ -27,12 +29,19 @@ FA_DTYPE_BF16 = 1
 _SIGNATURES = {
     "fa_fwd": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_void_p] + [ctypes.c_int] * 6 +
                [ctypes.c_void_p] * 4 + [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
+    "fa_fwd_splitkv": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_void_p] + [ctypes.c_int] * 6 +
+                       [ctypes.c_void_p] * 4 + [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                                 ctypes.c_size_t, ctypes.c_void_p]),
+    "fa_fwd_splitkv_workspace_size": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]),
+    "fa_lse_merge": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_void_p)] +
+                     [ctypes.c_int] * 4 + [ctypes.c_void_p] * 4 + [ctypes.c_int, ctypes.c_void_p]),
     "fa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "fa_device_status": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)]),
     "fa_fwd_plan": (ctypes.c_int, [ctypes.c_int] * 8 + [ctypes.POINTER(ctypes.c_int64)] * 2 +
                     [ctypes.POINTER(ctypes.c_int)] * 3),
     "fa_debug_set_wait_limit_ms": (None, [ctypes.c_double]),
     "fa_debug_inject_stall": (None, [ctypes.c_int]),
+    "fa_debug_force_split": (None, [ctypes.c_int]),
 }
 
 _lock = threading.Lock()
@@ -95,16 +104,7 @@ def _strides(t) -> fa_strides:
     return fa_strides(b, h, n, d)
 
 
-def fa_fwd(q, k, v, o=None, lse=None, *, scale: float | None = None, causal: bool = False, stream=None,
-           want_lse: bool = True):
-    """Attention forward through libfa.
-
-    q: (Z, Hq, Nq, D); k, v: (Z, Hkv, Nkv, D) CUDA tensors of one dtype (fp16
-    or bf16), any strides with d-stride 1.  o (optional) receives the output
-    in the same dtype; lse (optional) is a contiguous (Z, Hq, Nq) fp32 tensor.
-    scale defaults to 1/sqrt(D).  Launches on `stream` (a torch.cuda.Stream)
-    or the current stream and returns (o, lse) without synchronising.
-    """
+def _prepare(q, k, v, o, lse, scale, want_lse, stream):
     import torch
 
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
@@ -128,14 +128,110 @@ def fa_fwd(q, k, v, o=None, lse=None, *, scale: float | None = None, causal: boo
         scale = 1.0 / math.sqrt(D)
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
-    sq, sk, sv, so = _strides(q), _strides(k), _strides(v), _strides(o)
+    args = [q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr() if lse is not None else None,
+            Z, Hq, Hkv, Nq, Nkv, D]
+    strides = [_strides(q), _strides(k), _strides(v), _strides(o)]
+    return o, lse, dt, float(scale), stream, args, strides
+
+
+def fa_fwd(q, k, v, o=None, lse=None, *, scale: float | None = None, causal: bool = False, stream=None,
+           want_lse: bool = True):
+    """Attention forward through libfa.
+
+    q: (Z, Hq, Nq, D); k, v: (Z, Hkv, Nkv, D) CUDA tensors of one dtype (fp16
+    or bf16), any strides with d-stride 1.  o (optional) receives the output
+    in the same dtype; lse (optional) is a contiguous (Z, Hq, Nq) fp32 tensor.
+    scale defaults to 1/sqrt(D).  Launches on `stream` (a torch.cuda.Stream)
+    or the current stream and returns (o, lse) without synchronising.
+    """
+    import torch
+
+    o, lse, dt, scale, stream, args, st = _prepare(q, k, v, o, lse, scale, want_lse, stream)
     with torch.cuda.device(q.device):
-        rc = load().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                           lse.data_ptr() if lse is not None else None, Z, Hq, Hkv, Nq, Nkv, D,
-                           ctypes.byref(sq), ctypes.byref(sk), ctypes.byref(sv), ctypes.byref(so),
-                           float(scale), int(bool(causal)), dt, ctypes.c_void_p(stream.cuda_stream))
+        rc = load().fa_fwd(*args, *[ctypes.byref(x) for x in st], scale, int(bool(causal)), dt,
+                           ctypes.c_void_p(stream.cuda_stream))
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd")
+    return o, lse
+
+
+def fa_fwd_splitkv_workspace_size(D: int, device=None) -> int:
+    """Workspace bytes fa_fwd_splitkv needs for head dim D on `device` (default: current)."""
+    import torch
+
+    n = ctypes.c_size_t(0)
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        rc = load().fa_fwd_splitkv_workspace_size(int(D), ctypes.byref(n))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_splitkv_workspace_size")
+    return n.value
+
+
+def workspace_for(D: int, device=None):
+    """A uint8 CUDA tensor big enough to serve as fa_fwd_splitkv's workspace for head dim D."""
+    import torch
+
+    device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    return torch.empty(fa_fwd_splitkv_workspace_size(D, device), dtype=torch.uint8, device=device)
+
+
+def fa_fwd_splitkv(q, k, v, o=None, lse=None, *, scale: float | None = None, causal: bool = False,
+                   workspace=None, stream=None, want_lse: bool = True):
+    """fa_fwd with the key blocks of all query tiles cut into one equal range per SM.
+
+    Same arguments and results as fa_fwd, plus `workspace`: a CUDA uint8
+    tensor of at least fa_fwd_splitkv_workspace_size(D) bytes (256-byte
+    aligned, as torch allocations are); one is allocated when omitted.
+    """
+    import torch
+
+    o, lse, dt, scale, stream, args, st = _prepare(q, k, v, o, lse, scale, want_lse, stream)
+    if workspace is None:
+        workspace = workspace_for(q.shape[3], q.device)
+    with torch.cuda.device(q.device):
+        rc = load().fa_fwd_splitkv(*args, *[ctypes.byref(x) for x in st], scale, int(bool(causal)), dt,
+                                   workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                   ctypes.c_void_p(stream.cuda_stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_splitkv")
+    return o, lse
+
+
+def fa_lse_merge(o_parts, lse_parts, o=None, lse=None, *, stream=None, want_lse: bool = True):
+    """Combine results over disjoint key sets by their log-sum-exps (libfa's fa_lse_merge).
+
+    o_parts: sequence of (Z, H, N, D) fp16/bf16 CUDA tensors sharing one
+    layout; lse_parts: matching contiguous (Z, H, N) fp32 tensors.  Returns
+    (o, lse) for the union of the key sets, without synchronising.
+    """
+    import torch
+
+    n = len(o_parts)
+    if n != len(lse_parts) or not 1 <= n <= FA_MERGE_MAX_PARTS:
+        raise ValueError(f"need 1..{FA_MERGE_MAX_PARTS} matching O and lse parts")
+    o0 = o_parts[0]
+    Z, H, N, D = o0.shape
+    dt = _dtype_code(o0)
+    for x, l in zip(o_parts, lse_parts):
+        if tuple(x.shape) != (Z, H, N, D) or x.dtype != o0.dtype or x.stride() != o0.stride():
+            raise ValueError("O parts must share shape, dtype and strides")
+        if l.dtype != torch.float32 or tuple(l.shape) != (Z, H, N) or not l.is_contiguous():
+            raise ValueError("lse parts must be contiguous float32 (Z, H, N) tensors")
+    if o is None:
+        o = torch.empty((Z, H, N, D), dtype=o0.dtype, device=o0.device)
+    if lse is None and want_lse:
+        lse = torch.empty((Z, H, N), dtype=torch.float32, device=o0.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(o0.device)
+    optr = (ctypes.c_void_p * n)(*[x.data_ptr() for x in o_parts])
+    lptr = (ctypes.c_void_p * n)(*[l.data_ptr() for l in lse_parts])
+    sp, so = _strides(o0), _strides(o)
+    with torch.cuda.device(o0.device):
+        rc = load().fa_lse_merge(n, optr, lptr, Z, H, N, D, ctypes.byref(sp), o.data_ptr(),
+                                 lse.data_ptr() if lse is not None else None, ctypes.byref(so), dt,
+                                 ctypes.c_void_p(stream.cuda_stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_lse_merge")
     return o, lse
 
 
@@ -147,6 +243,16 @@ def fa_fwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int | No
     refs = [ctypes.byref(s) if s is not None else None for s in st]
     return load().fa_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, Z, Hq, Hkv, Nq, Nkv, D, *refs, float(scale),
                          int(causal), int(dtype), ctypes.c_void_p(stream_handle))
+
+
+def fa_fwd_splitkv_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int | None, Z: int, Hq: int,
+                       Hkv: int, Nq: int, Nkv: int, D: int, sq, sk, sv, so, scale: float, causal: bool, dtype: int,
+                       ws_ptr: int | None, ws_bytes: int, stream_handle: int = 0) -> int:
+    """fa_fwd_splitkv with raw pointers and (b, h, n, d) stride tuples; returns the status code."""
+    st = [fa_strides(*s) if s is not None else None for s in (sq, sk, sv, so)]
+    refs = [ctypes.byref(s) if s is not None else None for s in st]
+    return load().fa_fwd_splitkv(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, Z, Hq, Hkv, Nq, Nkv, D, *refs, float(scale),
+                                 int(causal), int(dtype), ws_ptr, int(ws_bytes), ctypes.c_void_p(stream_handle))
 
 
 def fa_device_status(stream=None) -> tuple[int, int]:
@@ -178,3 +284,8 @@ def fa_debug_set_wait_limit_ms(ms: float) -> None:
 
 def fa_debug_inject_stall(enable: bool) -> None:
     load().fa_debug_inject_stall(int(bool(enable)))
+
+
+def fa_debug_force_split(mode: int) -> None:
+    """fa_fwd_splitkv's choice: 0 by shape (default), 1 always cut key ranges, 2 never."""
+    load().fa_debug_force_split(int(mode))

@@ -55,6 +55,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 std::atomic<uint64_t> g_wait_limit_ns{0};
 std::atomic<int> g_inject_stall{0};
+std::atomic<int> g_force_split{0};  // 0: decide by shape, 1: always cut key ranges, 2: never
 
 uint64_t wait_limit_ns() {
     uint64_t v = g_wait_limit_ns.load();
@@ -145,6 +146,139 @@ int smem_bytes_for(int D) { int a, b, c; facts_for(D, &a, &b, &c); return b; }
 int swizzle_elems_for(int D) { int a, b, c; facts_for(D, &a, &b, &c); return c; }
 }  // namespace fa
 
+namespace {
+
+// Floats per partial-result slot of the split schedule: O / l of BM rows
+// (BM x D) and their base-2 log-sum-exps (BM), padded to 256 bytes.
+int64_t split_slot_floats(int D) { return ((int64_t)fa::BM * D + fa::BM + 63) / 64 * 64; }
+size_t split_workspace_bytes(int D, int grid) { return (size_t)2 * grid * split_slot_floats(D) * sizeof(float); }
+
+// (tile, key block) pairs of one (z, hq) head under the kernel's schedule
+template <bool CAUSAL, int BN>
+int64_t head_blocks_t(const fa::FwdParams& p) {
+    using S = fa::Sched<CAUSAL, BN>;
+    return S::head_prefix(p.Tq - 1, p) + S::tile_nkv(p.Tq - 1, p);
+}
+int64_t head_blocks(const fa::FwdParams& p, bool causal, int bn) {
+    if (bn == 64) return causal ? head_blocks_t<true, 64>(p) : head_blocks_t<false, 64>(p);
+    return causal ? head_blocks_t<true, 128>(p) : head_blocks_t<false, 128>(p);
+}
+
+// Key blocks of the busiest CTA when whole tiles are dealt round-robin to
+// `grid` CTAs in the kernel's tile order (causal: last query block first).
+template <bool CAUSAL, int BN>
+int64_t tile_mode_max_blocks_t(const fa::FwdParams& p, int grid) {
+    using S = fa::Sched<CAUSAL, BN>;
+    if (!CAUSAL) return cdiv(p.ntiles, grid) * p.Tk;
+    const int64_t heads = (int64_t)p.Z * p.Hq;
+    int64_t worst = 0;
+    for (int c = 0; c < grid; ++c) {
+        int64_t sum = 0;
+        for (int64_t t = c; t < p.ntiles; t += grid) sum += S::tile_nkv(p.Tq - 1 - (int)(t / heads), p);
+        worst = std::max(worst, sum);
+    }
+    return worst;
+}
+int64_t tile_mode_max_blocks(const fa::FwdParams& p, bool causal, int bn, int grid) {
+    if (bn == 64) return causal ? tile_mode_max_blocks_t<true, 64>(p, grid) : tile_mode_max_blocks_t<false, 64>(p, grid);
+    return causal ? tile_mode_max_blocks_t<true, 128>(p, grid) : tile_mode_max_blocks_t<false, 128>(p, grid);
+}
+
+// Cutting key ranges costs a partial write per cut tile, a merge launch and
+// shorter pipelines, measured on GB300 at about the time of 2048 keys of one
+// tile; it pays when whole tiles would leave the busiest CTA that much more
+// work than an even cut.  Many tiles per CTA are balanced already.
+constexpr int64_t kSplitGainKeys = 2048;
+bool split_pays(const fa::FwdParams& p, bool causal, int bn, int sms) {
+    if ((int64_t)p.ntiles >= 16 * (int64_t)sms) return false;
+    const int tile_grid = std::min(p.ntiles, sms);
+    const int64_t tile_max = tile_mode_max_blocks(p, causal, bn, tile_grid);
+    const int64_t split_max = cdiv(p.total_blocks, std::min<int64_t>(p.total_blocks, sms));
+    return (tile_max - split_max) * bn > kSplitGainKeys;
+}
+
+fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int Z, int Hq, int Hkv, int Nq,
+                   int Nkv, int D, const fa_strides* sq, const fa_strides* sk, const fa_strides* sv,
+                   const fa_strides* so, float scale, int causal, fa_dtype dtype, cudaStream_t stream, bool split,
+                   void* workspace, size_t workspace_bytes) {
+    fa_status st = check_shape(Z, Hq, Hkv, Nq, Nkv, D, causal);
+    if (st != FA_OK) return st;
+    if (dtype != FA_DTYPE_F16 && dtype != FA_DTYPE_BF16) return FA_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;  // a softmax temperature is positive
+    if ((int64_t)Z * Hq * Nq == 0) return FA_OK;
+    if ((st = check_tensor(q, sq, Z, Hq, Nq)) != FA_OK) return st;
+    if ((st = check_tensor(k, sk, Z, Hkv, Nkv)) != FA_OK) return st;
+    if ((st = check_tensor(v, sv, Z, Hkv, Nkv)) != FA_OK) return st;
+    if ((st = check_tensor(o, so, Z, Hq, Nq)) != FA_OK) return st;
+    if (lse != nullptr && reinterpret_cast<uintptr_t>(lse) % 4 != 0) return FA_ERR_ALIGNMENT;
+    if (split && (workspace == nullptr || reinterpret_cast<uintptr_t>(workspace) % 256 != 0))
+        return FA_ERR_WORKSPACE;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+    DeviceInfo* info = nullptr;
+    if (device_info(dev, &info) != cudaSuccess) return FA_ERR_CUDA;
+
+    const int bn = fa::block_n_for(D);
+    fa::LaunchArgs a;
+    fa::FwdParams& p = a.params;
+    p = fa::FwdParams{};
+    p.o = o;
+    p.lse = lse;
+    p.so_z = so->b;
+    p.so_h = so->h;
+    p.so_n = so->n;
+    p.Z = Z;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.Nq = Nq;
+    p.Nkv = Nkv;
+    p.group = Hq / Hkv;
+    p.Tq = (int)cdiv(Nq, fa::BM);
+    p.Tk = (int)cdiv(Nkv, bn);
+    p.ntiles = (int)((int64_t)Z * Hq * p.Tq);
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634);  // exp(x) = 2^(x log2 e)
+    p.status = info->status;
+    p.wait_limit_ns = wait_limit_ns();
+    p.inject_stall = g_inject_stall.load();
+    a.grid = std::min(p.ntiles, info->sms);
+    if (split) {
+        // one equal range of (tile, key block) pairs per SM (every range
+        // non-empty), when that beats whole tiles for this shape
+        if (workspace_bytes < split_workspace_bytes(D, info->sms)) return FA_ERR_WORKSPACE;
+        p.head_blocks = head_blocks(p, causal != 0, bn);
+        p.total_blocks = (int64_t)Z * Hq * p.head_blocks;
+        const int force = g_force_split.load();
+        if (force == 1 || (force == 0 && split_pays(p, causal != 0, bn, info->sms))) {
+            p.split = 1;
+            a.grid = (int)std::min<int64_t>(p.total_blocks, info->sms);
+            p.slot_floats = split_slot_floats(D);
+            p.scratch = static_cast<float*>(workspace);
+        }
+    }
+
+    CUtensorMap mq, mk, mv;
+    if (make_map(&mq, q, dtype, D, Nq, Hq, Z, sq, fa::BM) != CUDA_SUCCESS) return FA_ERR_CUDA;
+    if (make_map(&mk, k, dtype, D, Nkv, Hkv, Z, sk, bn) != CUDA_SUCCESS) return FA_ERR_CUDA;
+    if (make_map(&mv, v, dtype, D, Nkv, Hkv, Z, sv, bn) != CUDA_SUCCESS) return FA_ERR_CUDA;
+    a.tmQ = &mq;
+    a.tmK = &mk;
+    a.tmV = &mv;
+    a.stream = stream;
+
+    cudaError_t err;
+    switch (D) {
+        case 16: err = fa::launch_d16(a, causal != 0, dtype == FA_DTYPE_BF16); break;
+        case 32: err = fa::launch_d32(a, causal != 0, dtype == FA_DTYPE_BF16); break;
+        case 64: err = fa::launch_d64(a, causal != 0, dtype == FA_DTYPE_BF16); break;
+        case 128: err = fa::launch_d128(a, causal != 0, dtype == FA_DTYPE_BF16); break;
+        default: err = fa::launch_d256(a, causal != 0, dtype == FA_DTYPE_BF16); break;
+    }
+    return err == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* fa_status_string(fa_status s) {
@@ -155,6 +289,7 @@ const char* fa_status_string(fa_status s) {
         case FA_ERR_ALIGNMENT: return "FA_ERR_ALIGNMENT";
         case FA_ERR_CUDA: return "FA_ERR_CUDA";
         case FA_ERR_DEVICE_TIMEOUT: return "FA_ERR_DEVICE_TIMEOUT";
+        case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE";
     }
     return "FA_ERR_UNKNOWN";
 }
@@ -187,63 +322,69 @@ fa_status fa_fwd_plan(int Z, int Hq, int Hkv, int Nq, int Nkv, int D, int causal
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int Z, int Hq, int Hkv, int Nq,
                  int Nkv, int D, const fa_strides* sq, const fa_strides* sk, const fa_strides* sv,
                  const fa_strides* so, float scale, int causal, fa_dtype dtype, cudaStream_t stream) {
-    fa_status st = check_shape(Z, Hq, Hkv, Nq, Nkv, D, causal);
-    if (st != FA_OK) return st;
-    if (dtype != FA_DTYPE_F16 && dtype != FA_DTYPE_BF16) return FA_ERR_UNSUPPORTED;
-    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;  // a softmax temperature is positive
-    if ((int64_t)Z * Hq * Nq == 0) return FA_OK;
-    if ((st = check_tensor(q, sq, Z, Hq, Nq)) != FA_OK) return st;
-    if ((st = check_tensor(k, sk, Z, Hkv, Nkv)) != FA_OK) return st;
-    if ((st = check_tensor(v, sv, Z, Hkv, Nkv)) != FA_OK) return st;
-    if ((st = check_tensor(o, so, Z, Hq, Nq)) != FA_OK) return st;
-    if (lse != nullptr && reinterpret_cast<uintptr_t>(lse) % 4 != 0) return FA_ERR_ALIGNMENT;
+    return fwd_impl(q, k, v, o, lse, Z, Hq, Hkv, Nq, Nkv, D, sq, sk, sv, so, scale, causal, dtype, stream, false,
+                    nullptr, 0);
+}
 
+fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int Z, int Hq, int Hkv,
+                         int Nq, int Nkv, int D, const fa_strides* sq, const fa_strides* sk, const fa_strides* sv,
+                         const fa_strides* so, float scale, int causal, fa_dtype dtype, void* workspace,
+                         size_t workspace_bytes, cudaStream_t stream) {
+    return fwd_impl(q, k, v, o, lse, Z, Hq, Hkv, Nq, Nkv, D, sq, sk, sv, so, scale, causal, dtype, stream, true,
+                    workspace, workspace_bytes);
+}
+
+fa_status fa_fwd_splitkv_workspace_size(int D, size_t* bytes) {
+    if (bytes == nullptr) return FA_ERR_INVALID_ARG;
+    if (!supported_head_dim(D)) return FA_ERR_UNSUPPORTED;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
     DeviceInfo* info = nullptr;
     if (device_info(dev, &info) != cudaSuccess) return FA_ERR_CUDA;
+    *bytes = split_workspace_bytes(D, info->sms);
+    return FA_OK;
+}
 
-    const int bn = fa::block_n_for(D);
-    CUtensorMap mq, mk, mv;
-    if (make_map(&mq, q, dtype, D, Nq, Hq, Z, sq, fa::BM) != CUDA_SUCCESS) return FA_ERR_CUDA;
-    if (make_map(&mk, k, dtype, D, Nkv, Hkv, Z, sk, bn) != CUDA_SUCCESS) return FA_ERR_CUDA;
-    if (make_map(&mv, v, dtype, D, Nkv, Hkv, Z, sv, bn) != CUDA_SUCCESS) return FA_ERR_CUDA;
-
-    fa::LaunchArgs a;
-    a.tmQ = &mq;
-    a.tmK = &mk;
-    a.tmV = &mv;
-    fa::FwdParams& p = a.params;
-    p.o = o;
-    p.lse = lse;
-    p.so_z = so->b;
-    p.so_h = so->h;
-    p.so_n = so->n;
-    p.Z = Z;
-    p.Hq = Hq;
-    p.Hkv = Hkv;
-    p.Nq = Nq;
-    p.Nkv = Nkv;
-    p.group = Hq / Hkv;
-    p.Tq = (int)cdiv(Nq, fa::BM);
-    p.Tk = (int)cdiv(Nkv, bn);
-    p.ntiles = (int)((int64_t)Z * Hq * p.Tq);
-    p.scale_log2 = (float)((double)scale * 1.4426950408889634);  // exp(x) = 2^(x log2 e)
-    p.status = info->status;
-    p.wait_limit_ns = wait_limit_ns();
-    p.inject_stall = g_inject_stall.load();
-    a.grid = std::min(p.ntiles, info->sms);
-    a.stream = stream;
-
-    cudaError_t err;
-    switch (D) {
-        case 16: err = fa::launch_d16(a, causal != 0, dtype == FA_DTYPE_BF16); break;
-        case 32: err = fa::launch_d32(a, causal != 0, dtype == FA_DTYPE_BF16); break;
-        case 64: err = fa::launch_d64(a, causal != 0, dtype == FA_DTYPE_BF16); break;
-        case 128: err = fa::launch_d128(a, causal != 0, dtype == FA_DTYPE_BF16); break;
-        default: err = fa::launch_d256(a, causal != 0, dtype == FA_DTYPE_BF16); break;
+fa_status fa_lse_merge(int nparts, const void* const* o_parts, const float* const* lse_parts, int Z, int H, int N,
+                       int D, const fa_strides* sp, void* o, float* lse, const fa_strides* so, fa_dtype dtype,
+                       cudaStream_t stream) {
+    if (nparts < 1 || nparts > FA_MERGE_MAX_PARTS || o_parts == nullptr || lse_parts == nullptr)
+        return FA_ERR_INVALID_ARG;
+    if (Z < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
+    if (!supported_head_dim(D) || (dtype != FA_DTYPE_F16 && dtype != FA_DTYPE_BF16)) return FA_ERR_UNSUPPORTED;
+    const int64_t rows = (int64_t)Z * H * N;
+    if (rows == 0) return FA_OK;
+    fa_status st;
+    fa::MergeArgs a{};
+    for (int s = 0; s < nparts; ++s) {
+        if ((st = check_tensor(o_parts[s], sp, Z, H, N)) != FA_OK) return st;
+        if (lse_parts[s] == nullptr) return FA_ERR_INVALID_ARG;
+        if (reinterpret_cast<uintptr_t>(lse_parts[s]) % 4 != 0) return FA_ERR_ALIGNMENT;
+        a.o[s] = o_parts[s];
+        a.lse[s] = lse_parts[s];
     }
-    return err == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    if ((st = check_tensor(o, so, Z, H, N)) != FA_OK) return st;
+    if (lse != nullptr && reinterpret_cast<uintptr_t>(lse) % 4 != 0) return FA_ERR_ALIGNMENT;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+    DeviceInfo* info = nullptr;
+    if (device_info(dev, &info) != cudaSuccess) return FA_ERR_CUDA;
+    a.nparts = nparts;
+    a.H = H;
+    a.N = N;
+    a.D = D;
+    a.rows = rows;
+    a.sp_b = sp->b;
+    a.sp_h = sp->h;
+    a.sp_n = sp->n;
+    a.so_b = so->b;
+    a.so_h = so->h;
+    a.so_n = so->n;
+    a.out = o;
+    a.out_lse = lse;
+    const int64_t items = rows * (D / 8);
+    const int grid = (int)std::min<int64_t>(cdiv(items, 256), (int64_t)info->sms * 8);
+    return fa::launch_lse_merge(a, dtype == FA_DTYPE_BF16, grid, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 fa_status fa_device_status(cudaStream_t stream, uint32_t* detail) {
@@ -264,5 +405,6 @@ void fa_debug_set_wait_limit_ms(double ms) {
     g_wait_limit_ns.store(ms > 0 ? (uint64_t)(ms * 1e6) : 0);
 }
 void fa_debug_inject_stall(int enable) { g_inject_stall.store(enable ? 1 : 0); }
+void fa_debug_force_split(int mode) { g_force_split.store(mode == 1 || mode == 2 ? mode : 0); }
 
 }  // extern "C"

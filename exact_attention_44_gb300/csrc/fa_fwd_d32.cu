@@ -23,7 +23,13 @@ static cudaError_t launch_one(const LaunchArgs& a) {
         configured.fetch_or(bit);
     }
     kernel<<<a.grid, NUM_THREADS, smem, a.stream>>>(*a.tmQ, *a.tmK, *a.tmV, a.params);
-    return cudaGetLastError();
+    err = cudaGetLastError();
+    // split schedule: one merge block per cut between CTA ranges, same stream
+    if (err == cudaSuccess && a.params.split && a.grid > 1) {
+        fa_split_merge_kernel<32, CAUSAL, BF16><<<a.grid - 1, MERGE_THREADS, 0, a.stream>>>(a.params, a.grid);
+        err = cudaGetLastError();
+    }
+    return err;
 }
 
 cudaError_t launch_d32(const LaunchArgs& a, bool causal, bool bf16) {

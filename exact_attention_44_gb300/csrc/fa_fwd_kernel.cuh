@@ -10,21 +10,25 @@
 //     exp2 with scale·log2(e), fp32 state, P cast to the input type;
 //     section 八: causal loop bound at the diagonal).
 // Its GB300 form:
-//   * one persistent CTA per SM walks a static list of 128-row query tiles;
-//   * warp 0 (one lane) streams Q once per tile and K_j, V_j per key block by
-//     TMA into swizzled shared-memory rings guarded by full/empty mbarriers;
-//   * warp 1 (one lane) issues S_j = Q K_jᵀ into a double-buffered S in TMEM
-//     and O += P_j V_j with P_j read from TMEM (double-buffered), committing
-//     each to mbarriers; S_{j+1} runs on the tensor cores while the softmax
-//     works on S_j;
-//   * warps 2-5 (128 threads, thread = query row = TMEM lane) run the online
-//     softmax: mask (diagonal and tail blocks only), row max, exp2, row sum,
-//     P -> fp16/bf16 into TMEM; O is rescaled in TMEM only when a row maximum
-//     grows by more than 2^RESCALE_LOG2 (below that the stale maximum keeps
-//     every p <= 2^RESCALE_LOG2, and O / l and lse are unchanged);
-//   * warps 6-9 run the epilogue of the previous tile while the softmax warps
-//     start the next one: read O out of TMEM, release it to the MMA warp, then
-//     O / l -> global and lse = (m + log2 l)·ln 2.
+//   * one persistent CTA per SM walks a static schedule (Sched): whole
+//     128-row query tiles, or, in split mode, one equal range of
+//     (tile, key block) pairs per CTA whose cut tiles a second kernel merges;
+//   * warp 0 (one lane) streams Q once per segment and K_j per key block, warp
+//     15 (one lane) V_j, by TMA into swizzled shared-memory rings guarded by
+//     mbarriers;
+//   * warp 1 (one lane) issues S_g = Q K_gᵀ into a three-slot ring in TMEM,
+//     warp 2 (one lane) O += P_g V_g with P_g read from the same slot; each
+//     commits to mbarriers, so S of later blocks runs while the softmax works;
+//   * warps 3-10 (two column halves x 128 threads, thread = query row = TMEM
+//     lane) run the online softmax: mask (diagonal and tail blocks only), row
+//     max swapped between the halves, exp2, row sum, P -> fp16/bf16 into TMEM;
+//     O is rescaled in TMEM only when a row maximum grows by more than
+//     2^RESCALE_LOG2 (below that the stale maximum keeps every
+//     p <= 2^RESCALE_LOG2, and O / l and lse are unchanged);
+//   * warps 11-14 run the epilogue of the previous segment while the softmax
+//     warps start the next: read O out of TMEM, release it to the P·V issuer,
+//     then O / l -> global and lse = (m + log2 l)·ln 2 (or the part's O / l
+//     and base-2 lse -> workspace).
 // Every mbarrier wait is bounded; on expiry the CTA records the site in the
 // status word, stops every role, lets its copies and MMAs land and frees TMEM.
 #pragma once
@@ -143,8 +147,13 @@ __device__ __forceinline__ bool drain_phase(uint32_t bar, uint32_t parity, uint6
     return true;
 }
 
-struct TileInfo {
-    int z, hq, hk, q_start, nkv;
+// One unit of a CTA's work: key blocks [jb, je) of the query tile
+// (z, hq, q_start), whose whole key range is [0, nkv).
+struct Seg {
+    int z, hq, hk, q_start;
+    int nkv;     // key blocks the whole tile visits
+    int jb, je;  // the key blocks of this segment
+    int slot;    // -1: the whole tile, finished into O and lse; else the partial-result slot
 };
 
 // Barrier slot and phase parity of key block g (global count) in a ring of R.
@@ -153,35 +162,113 @@ __device__ __forceinline__ uint32_t rslot(uint32_t g) { return g % R; }
 template <int R>
 __device__ __forceinline__ uint32_t rphase(uint32_t g) { return (g / R) & 1u; }
 
-// Tile t of the static schedule.  Non-causal: head-major, so the CTAs running
-// at the same time share a head's K/V in L2.  Causal: query blocks from the
-// last (most key blocks) to the first, heads innermost, so the heavy tiles go
-// first and the light ones fill the tail.  A causal tile stops at the key
-// block holding its last row ("Write Triton Attention Kernel", step 9).
+// The static schedule, in one of two modes.
+//
+// Tile mode (split == 0): CTA c takes whole tiles c, c + grid, ...
+// Non-causal tiles go head-major, so the CTAs running at the same time share
+// a head's K/V in L2; causal ones go from the last query block (most key
+// blocks) to the first with heads innermost, so the heavy tiles go first and
+// the light ones fill the tail.
+//
+// Split mode (split != 0): the (tile, key block) pairs of all tiles, tiles
+// head-major and query blocks ascending, are laid end to end and cut into
+// `grid` equal ranges, one per CTA.  A tile that a cut crosses leaves a
+// partial result (O / l in fp32 and the base-2 log-sum-exp of the part) in a
+// slot of the workspace: slot 2c holds the part CTA c starts with, slot 2c + 1
+// the part it ends with; a second kernel merges the parts of each cut tile.
+//
+// A causal tile stops at the key block holding its last row ("Write Triton
+// Attention Kernel", step 9).  Positions are tiles in tile mode and
+// (tile, key block) pairs in split mode.
 template <bool CAUSAL, int BN>
-__device__ __forceinline__ TileInfo tile_info(int t, const FwdParams& p) {
-    TileInfo ti;
-    const int heads = p.Z * p.Hq;
-    int head, mb;
-    if (CAUSAL) {
-        mb = p.Tq - 1 - t / heads;
-        head = t % heads;
-    } else {
-        head = t / p.Tq;
-        mb = t % p.Tq;
+struct Sched {
+    int64_t hi;  // split mode: end of this CTA's range
+
+    static __host__ __device__ __forceinline__ int tile_nkv(int mb, const FwdParams& p) {
+        if (!CAUSAL) return p.Tk;
+        const int end = mb * BM + BM < p.Nq ? mb * BM + BM : p.Nq;
+        const int n = (end - 1) / BN + 1;
+        return n < p.Tk ? n : p.Tk;
     }
-    ti.z = head / p.Hq;
-    ti.hq = head % p.Hq;
-    ti.hk = ti.hq / p.group;  // GQA: kv head = q head // (Hq / Hkv)
-    ti.q_start = mb * BM;
-    if (CAUSAL) {
-        const int last_row = min(ti.q_start + BM, p.Nq) - 1;
-        ti.nkv = min(p.Tk, last_row / BN + 1);
-    } else {
-        ti.nkv = p.Tk;
+    // key blocks visited by query blocks 0 .. mb-1 of one head: for a causal
+    // block m below the last, tile_nkv(m) = min(Tk, r (m + 1)) with r = BM / BN
+    static __host__ __device__ __forceinline__ int64_t head_prefix(int mb, const FwdParams& p) {
+        if (!CAUSAL) return (int64_t)mb * p.Tk;
+        constexpr int64_t r = BM / BN;
+        const int64_t full = p.Tk / r;  // blocks m with r (m + 1) <= Tk
+        const int64_t m = mb < full ? mb : full;
+        return r * m * (m + 1) / 2 + (mb - m) * (int64_t)p.Tk;
     }
-    return ti;
-}
+    // split mode: first position of tile (head, mb), and the tile holding position x
+    static __host__ __device__ __forceinline__ int64_t tile_pos(int64_t head, int mb, const FwdParams& p) {
+        return head * p.head_blocks + head_prefix(mb, p);
+    }
+    static __host__ __device__ __forceinline__ void tile_of(int64_t x, const FwdParams& p, int64_t& head, int& mb) {
+        head = x / p.head_blocks;
+        const int64_t rem = x - head * p.head_blocks;
+        if (!CAUSAL) {
+            mb = (int)(rem / p.Tk);
+        } else {  // largest mb with head_prefix(mb) <= rem
+            int lo = 0, up = p.Tq - 1;
+            while (lo < up) {
+                const int mid = (lo + up + 1) / 2;
+                if (head_prefix(mid, p) <= rem) lo = mid;
+                else up = mid - 1;
+            }
+            mb = lo;
+        }
+    }
+    // split mode: range of CTA c is [range_lo(c), range_lo(c + 1)); cta_of(x)
+    // is the CTA whose range holds x (every range is non-empty: grid <= total)
+    static __host__ __device__ __forceinline__ int64_t range_lo(int64_t c, int64_t grid, const FwdParams& p) {
+        return p.total_blocks * c / grid;
+    }
+    static __host__ __device__ __forceinline__ int64_t cta_of(int64_t x, int64_t grid, const FwdParams& p) {
+        return ((x + 1) * grid + p.total_blocks - 1) / p.total_blocks - 1;
+    }
+
+    __device__ explicit Sched(const FwdParams& p) : hi(p.split ? range_lo(blockIdx.x + 1, gridDim.x, p) : 0) {}
+    __device__ __forceinline__ int64_t first(const FwdParams& p) const {
+        return p.split ? range_lo(blockIdx.x, gridDim.x, p) : (int64_t)blockIdx.x;
+    }
+    __device__ __forceinline__ bool valid(int64_t pos, const FwdParams& p) const {
+        return p.split ? pos < hi : pos < p.ntiles;
+    }
+    __device__ __forceinline__ int64_t next(int64_t pos, const Seg& sg, const FwdParams& p) const {
+        return p.split ? pos + (sg.je - sg.jb) : pos + gridDim.x;
+    }
+    __device__ __forceinline__ Seg seg(int64_t pos, const FwdParams& p) const {
+        Seg s;
+        int64_t head;
+        int mb;
+        if (p.split) {
+            tile_of(pos, p, head, mb);
+        } else if (CAUSAL) {
+            const int heads = p.Z * p.Hq;
+            mb = p.Tq - 1 - (int)(pos / heads);
+            head = pos % heads;
+        } else {
+            head = pos / p.Tq;
+            mb = (int)(pos % p.Tq);
+        }
+        s.z = (int)(head / p.Hq);
+        s.hq = (int)(head % p.Hq);
+        s.hk = s.hq / p.group;  // GQA: kv head = q head // (Hq / Hkv)
+        s.q_start = mb * BM;
+        s.nkv = tile_nkv(mb, p);
+        if (p.split) {
+            const int64_t t0 = tile_pos(head, mb, p);
+            s.jb = (int)(pos - t0);
+            s.je = hi - t0 < s.nkv ? (int)(hi - t0) : s.nkv;
+            s.slot = (s.jb == 0 && s.je == s.nkv) ? -1 : 2 * (int)blockIdx.x + (s.jb > 0 ? 0 : 1);
+        } else {
+            s.jb = 0;
+            s.je = s.nkv;
+            s.slot = -1;
+        }
+        return s;
+    }
+};
 
 // ------------------------------------------------------------ TMA producers -
 // Two threads load: one Q and K (the S stream's operands), one V (the P·V
@@ -200,22 +287,24 @@ __device__ void run_producer_qk(const CUtensorMap* tmQ, const CUtensorMap* tmK, 
     uint32_t qi = 0, ki = 0;  // loads issued into each ring
     bool ok = true;
     bool withheld = false;
-    auto load_q = [&](const TileInfo& ti) -> bool {
+    auto load_q = [&](const Seg& sg) -> bool {
         const uint32_t s = qi % T::Q_STAGES, ph = (qi / T::Q_STAGES) & 1u;
         if (!wait_phase(bar(T::B_QEMPTY + s), ph ^ 1u, ctl, SITE_Q_EMPTY)) return false;
         ptx::mbar_arrive_expect_tx(bar(T::B_QFULL + s), T::Q_BYTES);
         const uint32_t dst = sbase + T::OFF_Q + s * T::Q_BYTES;
         for (int c = 0; c < T::NCHUNK; ++c)
-            ptx::tma_load_4d(dst + c * (BM * T::SW), tmQ, bar(T::B_QFULL + s), c * T::SWE, ti.q_start, ti.hq, ti.z,
+            ptx::tma_load_4d(dst + c * (BM * T::SW), tmQ, bar(T::B_QFULL + s), c * T::SWE, sg.q_start, sg.hq, sg.z,
                              pol_q);
         ++qi;
         return true;
     };
-    int t = blockIdx.x;
-    if (t < p.ntiles) ok = load_q(tile_info<CAUSAL, T::BN>(t, p));
-    for (; ok && t < p.ntiles; t += gridDim.x) {
-        const TileInfo ti = tile_info<CAUSAL, T::BN>(t, p);
-        for (int j = 0; j < ti.nkv; ++j) {
+    const Sched<CAUSAL, T::BN> sc(p);
+    int64_t pos = sc.first(p);
+    if (sc.valid(pos, p)) ok = load_q(sc.seg(pos, p));
+    while (ok && sc.valid(pos, p)) {
+        const Seg sg = sc.seg(pos, p);
+        const int64_t nxt = sc.next(pos, sg, p);
+        for (int j = sg.jb; j < sg.je; ++j) {
             // slot ki & 1 held block ki - 2, free once S of that block is complete
             const uint32_t s = ki & 1u;
             if (ki >= 2 && !wait_phase(bar(T::B_SFULL + rslot<T::SR>(ki - 2)), rphase<T::SR>(ki - 2), ctl,
@@ -227,18 +316,19 @@ __device__ void run_producer_qk(const CUtensorMap* tmQ, const CUtensorMap* tmK, 
                 const uint32_t dst = sbase + T::OFF_K + s * T::KV_BYTES;
                 for (int c = 0; c < T::NCHUNK; ++c)
                     ptx::tma_load_4d(dst + c * (T::BN * T::SW), tmK, bar(T::B_KFULL + s), c * T::SWE, j * T::BN,
-                                     ti.hk, ti.z, pol_kv);
+                                     sg.hk, sg.z, pol_kv);
             }
             ++ki;
-            // with two Q slots the next tile's Q can go right after the first
-            // K; with one, only after the last K (its slot frees at this
-            // tile's last S, which needs that K)
-            const int q_at = T::Q_STAGES >= 2 ? 0 : ti.nkv - 1;
-            if (j == q_at && t + (int)gridDim.x < p.ntiles && !load_q(tile_info<CAUSAL, T::BN>(t + gridDim.x, p))) {
+            // with two Q slots the next segment's Q can go right after the
+            // first K; with one, only after the last K (its slot frees at this
+            // segment's last S, which needs that K)
+            const int q_at = T::Q_STAGES >= 2 ? sg.jb : sg.je - 1;
+            if (j == q_at && sc.valid(nxt, p) && !load_q(sc.seg(nxt, p))) {
                 ok = false;
                 break;
             }
         }
+        pos = nxt;
     }
     if (!ok) {
         // Let every copy still in flight land before shared memory is released.
@@ -259,9 +349,10 @@ __device__ void run_producer_v(const CUtensorMap* tmV, const FwdParams& p, uint3
     const uint64_t pol_kv = ptx::policy_evict_last();
     uint32_t vi = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < p.ntiles; t += gridDim.x) {
-        const TileInfo ti = tile_info<CAUSAL, T::BN>(t, p);
-        for (int j = 0; j < ti.nkv; ++j) {
+    const Sched<CAUSAL, T::BN> sc(p);
+    for (int64_t pos = sc.first(p); ok && sc.valid(pos, p);) {
+        const Seg sg = sc.seg(pos, p);
+        for (int j = sg.jb; j < sg.je; ++j) {
             // slot vi & 1 held block vi - 2, free once its P·V is complete
             const uint32_t s = vi & 1u;
             if (vi >= 2 && !wait_phase(bar(T::B_PVDONE + rslot<T::SR>(vi - 2)), rphase<T::SR>(vi - 2), ctl,
@@ -269,10 +360,11 @@ __device__ void run_producer_v(const CUtensorMap* tmV, const FwdParams& p, uint3
             ptx::mbar_arrive_expect_tx(bar(T::B_VFULL + s), T::KV_BYTES);
             const uint32_t dst = sbase + T::OFF_V + s * T::KV_BYTES;
             for (int c = 0; c < T::NCHUNK; ++c)
-                ptx::tma_load_4d(dst + c * (T::BN * T::SW), tmV, bar(T::B_VFULL + s), c * T::SWE, j * T::BN, ti.hk,
-                                 ti.z, pol_kv);
+                ptx::tma_load_4d(dst + c * (T::BN * T::SW), tmV, bar(T::B_VFULL + s), c * T::SWE, j * T::BN, sg.hk,
+                                 sg.z, pol_kv);
             ++vi;
         }
+        pos = sc.next(pos, sg, p);
     }
     if (!ok)
         for (uint32_t i = vi > 2u ? vi - 2u : 0u; i < vi; ++i)
@@ -299,12 +391,14 @@ __device__ void run_mma_qk(const FwdParams& p, uint32_t sbase, uint32_t bar0, ui
     const uint32_t k_lo0 = ptx::smem_desc_lo(sbase + T::OFF_K, 16);
     uint32_t qi = 0, g = 0;  // Q tiles and S blocks issued
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < p.ntiles; t += gridDim.x) {
-        const TileInfo ti = tile_info<CAUSAL, T::BN>(t, p);
+    const Sched<CAUSAL, T::BN> sc(p);
+    for (int64_t pos = sc.first(p); ok && sc.valid(pos, p);) {
+        const Seg sg = sc.seg(pos, p);
+        pos = sc.next(pos, sg, p);
         const uint32_t qs = qi % T::Q_STAGES;
         if (!wait_phase(bar(T::B_QFULL + qs), (qi / T::Q_STAGES) & 1u, ctl, SITE_Q_FULL)) { ok = false; break; }
         const uint32_t q_lo = q_lo0 + qs * (T::Q_BYTES >> 4);
-        for (int j = 0; j < ti.nkv; ++j, ++g) {
+        for (int j = sg.jb; j < sg.je; ++j, ++g) {
             const uint32_t kb = g & 1u, r = rslot<T::SR>(g);
             if (!wait_phase(bar(T::B_KFULL + kb), (g >> 1) & 1u, ctl, SITE_K_FULL)) { ok = false; break; }
             // ring slot r held block g - SR (S, then P) until O += P V of that
@@ -324,7 +418,7 @@ __device__ void run_mma_qk(const FwdParams& p, uint32_t sbase, uint32_t bar0, ui
                             kk > 0 ? 1u : 0u);
             }
             ptx::tc_commit(bar(T::B_SFULL + r));  // S ready, K slot kb free
-            if (j == ti.nkv - 1) {
+            if (j == sg.je - 1) {
                 ptx::tc_commit(bar(T::B_QEMPTY + qs));  // last use of this Q tile
                 ++qi;
             }
@@ -337,8 +431,8 @@ __device__ void run_mma_qk(const FwdParams& p, uint32_t sbase, uint32_t bar0, ui
     }
 }
 
-// O += P_g V_g (step 5h); the first block of a tile overwrites O, once the
-// epilogue has read the previous tile's O out of TMEM
+// O += P_g V_g (step 5h); the first block of a segment overwrites O, once
+// the epilogue has read the previous segment's O out of TMEM
 template <int D, bool CAUSAL, bool BF16>
 __device__ void run_mma_pv(const FwdParams& p, uint32_t sbase, uint32_t bar0, uint32_t tmem, const Ctl& ctl) {
     using T = Traits<D>;
@@ -348,18 +442,20 @@ __device__ void run_mma_pv(const FwdParams& p, uint32_t sbase, uint32_t bar0, ui
     const uint32_t v_lo0 = ptx::smem_desc_lo(sbase + T::OFF_V, T::BN * T::SW);  // LBO: next column chunk of V
     uint32_t g = 0, ntile = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < p.ntiles; t += gridDim.x, ++ntile) {
-        const TileInfo ti = tile_info<CAUSAL, T::BN>(t, p);
-        for (int j = 0; j < ti.nkv; ++j, ++g) {
+    const Sched<CAUSAL, T::BN> sc(p);
+    for (int64_t pos = sc.first(p); ok && sc.valid(pos, p); ++ntile) {
+        const Seg sg = sc.seg(pos, p);
+        pos = sc.next(pos, sg, p);
+        for (int j = sg.jb; j < sg.je; ++j, ++g) {
             const uint32_t vb = g & 1u, r = rslot<T::SR>(g);
-            if (j == 0 && ntile > 0 &&
+            if (j == sg.jb && ntile > 0 &&
                 !wait_phase(bar(T::B_OFREE), (ntile - 1) & 1u, ctl, SITE_O_FREE)) { ok = false; break; }
             if (!wait_phase(bar(T::B_PFULL + r), rphase<T::SR>(g), ctl, SITE_P_FULL)) { ok = false; break; }
             if (!wait_phase(bar(T::B_VFULL + vb), (g >> 1) & 1u, ctl, SITE_V_FULL)) { ok = false; break; }
             ptx::tc_fence_after();
             const uint32_t v_lo = v_lo0 + vb * (T::KV_BYTES >> 4);
             const uint32_t a_tmem = tmem + T::TM_S + r * T::BN;  // P_g over the first BN/2 columns of the slot
-            const uint32_t acc0 = j > 0 ? 1u : 0u;
+            const uint32_t acc0 = j > sg.jb ? 1u : 0u;
 #pragma unroll
             for (int kk = 0; kk < T::BN / 16; ++kk)
                 ptx::mma_ts(tmem + T::TM_O, a_tmem + kk * 8, ptx::desc64(v_lo + ((kk * 16 * T::SW) >> 4), HI), IDESC,
@@ -438,13 +534,15 @@ __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, fl
     const uint64_t c2 = ptx::pack_f32x2(c, c);
     uint32_t step = 0, ntile = 0;
 
-    for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++ntile) {
-        const TileInfo ti = tile_info<CAUSAL, BN>(t, p);
+    const Sched<CAUSAL, BN> sc(p);
+    for (int64_t pos = sc.first(p); sc.valid(pos, p); ++ntile) {
+        const Seg ti = sc.seg(pos, p);
+        pos = sc.next(pos, ti, p);
         const int q_row = ti.q_start + row;
         // running max (log2 units of the scaled score) and denominator, fp32
         // ("Write Triton Attention Kernel", step 4; the initial l is 0)
         float m = -INFINITY, l = 0.f;
-        for (int j = 0; j < ti.nkv; ++j) {
+        for (int j = ti.jb; j < ti.je; ++j) {
             const uint32_t r = rslot<T::SR>(step);      // ring slot of S_j / P_j
             const uint32_t b = step & 1u, ph = (step >> 1) & 1u;  // max-exchange slot
             if (!warp_wait_phase(bar(T::B_SFULL + r), rphase<T::SR>(step), ctl, SITE_S_FULL)) return;
@@ -481,7 +579,7 @@ __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, fl
             const float pmax = fmaxf(mx0, mx1);
             red[(b * 2 + h) * BM + row] = pmax;
             ptx::mbar_arrive(bar(T::B_RED + b));
-            if (j == 0) {
+            if (j == ti.jb) {
                 // the first block sets the reference maximum m
                 if (!warp_wait_phase(bar(T::B_RED + b), ph, ctl, SITE_MAX_XCHG)) return;
                 m = fmaxf(pmax, red[(b * 2 + (h ^ 1)) * BM + row]) * c;  // scale > 0
@@ -491,6 +589,9 @@ __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, fl
             constexpr int NP = HC / 2;  // packed P columns of this half
             uint32_t pk[NP];
             auto exps = [&](float ref) -> uint64_t {
+                // a row with no kept key so far (only in a segment that starts
+                // past the diagonal of a causal tile) has p = 0, not 2^(-inf + inf)
+                ref = ref == -INFINITY ? 0.f : ref;
                 const uint64_t negm2 = ptx::pack_f32x2(-ref, -ref);
                 uint64_t sum2 = ptx::pack_f32x2(0.f, 0.f);
 #pragma unroll
@@ -505,7 +606,7 @@ __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, fl
             };
             uint64_t sum2 = exps(m);
             float alpha = 1.f;
-            if (j > 0) {
+            if (j > ti.jb) {
                 // the block maximum arrives while the exponentials run; only
                 // when it exceeds m by more than 2^RESCALE_LOG2 are P redone
                 // against the new maximum, and O and l rescaled by alpha before
@@ -559,9 +660,11 @@ __device__ void run_epilogue(const FwdParams& p, uint32_t bar0, uint32_t tmem, c
     uint32_t step = 0, ntile = 0;
     constexpr int CH = D >= 32 ? 32 : 16;               // columns per TMEM load
     constexpr int HELD = D <= 128 ? D / CH : 64 / CH;    // chunks converted before their stores
-    for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++ntile) {
-        const TileInfo ti = tile_info<CAUSAL, T::BN>(t, p);
-        step += ti.nkv;
+    const Sched<CAUSAL, T::BN> sc(p);
+    for (int64_t pos = sc.first(p); sc.valid(pos, p); ++ntile) {
+        const Seg ti = sc.seg(pos, p);
+        pos = sc.next(pos, ti, p);
+        step += ti.je - ti.jb;
         const uint32_t slot = ntile & 1u;
         if (!warp_wait_phase(bar(T::B_EPIFULL + slot), (ntile >> 1) & 1u, ctl, SITE_EPI_FULL)) return;
         const float m = hand[slot * 3 * BM + row];
@@ -571,6 +674,35 @@ __device__ void run_epilogue(const FwdParams& p, uint32_t bar0, uint32_t tmem, c
         if (!warp_wait_phase(bar(T::B_PVDONE + rslot<T::SR>(g)), rphase<T::SR>(g), ctl, SITE_PV_DONE)) return;
         ptx::tc_fence_after();
 
+        if (ti.slot >= 0) {
+            // part of a tile cut by the split schedule: O / l in fp32 and the
+            // base-2 log-sum-exp of this part, for the merge kernel.  Slot
+            // layout: float4 column group c4 of row r at [c4][r], then the
+            // BM log-sum-exps, so a warp's 32 rows store 512 contiguous
+            // bytes.  Rows past Nq are not stored (the merge skips them too).
+            // A row with no kept key in the part (l = 0) gets O = 0 and -inf.
+            const bool keep = ti.q_start + row < p.Nq;
+            float* part = p.scratch + (int64_t)ti.slot * p.slot_floats;
+            float4* pcol = reinterpret_cast<float4*>(part) + row;
+            const float inv_l = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+            for (int i = 0; i < D / CH; ++i) {
+                uint32_t r[CH];
+                if constexpr (CH == 32) ptx::tmem_ld32(tmem + lane_addr + T::TM_O + i * CH, r);
+                else ptx::tmem_ld16(tmem + lane_addr + T::TM_O + i * CH, r);
+                if (keep) {
+#pragma unroll
+                    for (int x = 0; x < CH / 4; ++x)
+                        pcol[(i * (CH / 4) + x) * BM] =
+                            make_float4(__uint_as_float(r[4 * x]) * inv_l, __uint_as_float(r[4 * x + 1]) * inv_l,
+                                        __uint_as_float(r[4 * x + 2]) * inv_l, __uint_as_float(r[4 * x + 3]) * inv_l);
+                }
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(T::B_OFREE));
+            if (keep) part[(int64_t)BM * D + row] = l > 0.f ? m + log2f(l) : -INFINITY;
+            continue;
+        }
         const int q_row = ti.q_start + row;
         const bool store = q_row < p.Nq;
         const float inv_l = 1.f / l;
@@ -661,6 +793,90 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, T::TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------ split merge ---
+// Finishes every tile that the split schedule cut.  Block b - 1 looks at the
+// cut between the ranges of CTAs b - 1 and b; the first cut inside a tile
+// merges that tile, from the part CTA b - 1 ends with (slot 2(b-1) + 1) and
+// the parts CTAs b .. c1 start with (slots 2c).  With λ_s the base-2
+// log-sum-exp of part s (over its keys) and O_s = its O / l,
+//     λ = log2 Σ_s 2^λ_s,      O = Σ_s 2^(λ_s − λ) O_s,
+// the same rescaling by the change of maximum that the online softmax applies
+// between key blocks ("Write Triton Attention Kernel", Kernel design rules).
+// Four threads per row, each a quarter of the columns; every part's columns
+// of a thread are loaded together so their latencies overlap.
+constexpr int MERGE_THREADS = 4 * BM;
+
+template <int D, bool CAUSAL, bool BF16>
+__global__ void __launch_bounds__(MERGE_THREADS) fa_split_merge_kernel(const FwdParams p, int grid) {
+    using S = Sched<CAUSAL, Traits<D>::BN>;
+    const int64_t b = (int64_t)blockIdx.x + 1;
+    const int64_t xb = S::range_lo(b, grid, p);
+    int64_t head;
+    int mb;
+    S::tile_of(xb, p, head, mb);
+    const int64_t t0 = S::tile_pos(head, mb, p);
+    if (xb == t0) return;                                     // the cut falls between tiles
+    if (b >= 2 && S::range_lo(b - 1, grid, p) > t0) return;  // an earlier cut merges this tile
+    const int r = threadIdx.x % BM, quarter = threadIdx.x / BM;
+    const int q_row = mb * BM + r;
+    if (q_row >= p.Nq) return;                                // no part stored this row
+    const int64_t c0 = b - 1;
+    const int64_t c1 = S::cta_of(t0 + S::tile_nkv(mb, p) - 1, grid, p);
+    auto part = [&](int64_t c) -> const float* {
+        return p.scratch + (c == c0 ? 2 * c + 1 : 2 * c) * p.slot_floats;
+    };
+    // the parts' log-sum-exps of this row, PB at a time so their loads overlap
+    constexpr int PB = 8;
+    float mx = -INFINITY;
+    for (int64_t c = c0; c <= c1; c += PB) {
+        float x[PB];
+#pragma unroll
+        for (int i = 0; i < PB; ++i) x[i] = c + i <= c1 ? __ldg(part(c + i) + BM * D + r) : -INFINITY;
+#pragma unroll
+        for (int i = 0; i < PB; ++i) mx = fmaxf(mx, x[i]);
+    }
+    float den = 0.f;
+#pragma unroll 4
+    for (int64_t c = c0; c <= c1; ++c) den += exp2f(__ldg(part(c) + BM * D + r) - mx);
+    const float inv = 1.f / den;
+    const int z = (int)(head / p.Hq), hq = (int)(head % p.Hq);
+    if (quarter == 0 && p.lse != nullptr) p.lse[head * p.Nq + q_row] = (mx + log2f(den)) * 0.6931471805599453f;
+
+    constexpr int G4 = D / 16;                // float4 column groups per thread
+    constexpr int CHUNK = G4 < 8 ? G4 : 8;    // groups loaded together
+    uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
+                    2 * ((int64_t)z * p.so_z + (int64_t)hq * p.so_h + (int64_t)q_row * p.so_n);
+#pragma unroll
+    for (int g0 = 0; g0 < G4; g0 += CHUNK) {
+        float4 acc[CHUNK];
+#pragma unroll
+        for (int i = 0; i < CHUNK; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 2
+        for (int64_t c = c0; c <= c1; ++c) {
+            const float* pc = part(c);
+            const float w = exp2f(__ldg(pc + BM * D + r) - mx);
+            const float4* col = reinterpret_cast<const float4*>(pc) + r;
+            float4 v[CHUNK];
+#pragma unroll
+            for (int i = 0; i < CHUNK; ++i) v[i] = __ldg(col + (quarter * G4 + g0 + i) * BM);
+#pragma unroll
+            for (int i = 0; i < CHUNK; ++i) {
+                acc[i].x += w * v[i].x;
+                acc[i].y += w * v[i].y;
+                acc[i].z += w * v[i].z;
+                acc[i].w += w * v[i].w;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < CHUNK; ++i) {
+            uint2 out;
+            out.x = pack2<BF16>(acc[i].x * inv, acc[i].y * inv);
+            out.y = pack2<BF16>(acc[i].z * inv, acc[i].w * inv);
+            reinterpret_cast<uint2*>(orow)[quarter * G4 + g0 + i] = out;
+        }
     }
 }
 

@@ -4,6 +4,8 @@
 #include <cuda.h>
 #include <cuda_runtime_api.h>
 
+#include <cstdint>
+
 #include "fa_params.h"
 
 namespace fa {
@@ -23,6 +25,20 @@ cudaError_t launch_d32(const LaunchArgs& a, bool causal, bool bf16);
 cudaError_t launch_d64(const LaunchArgs& a, bool causal, bool bf16);
 cudaError_t launch_d128(const LaunchArgs& a, bool causal, bool bf16);
 cudaError_t launch_d256(const LaunchArgs& a, bool causal, bool bf16);
+
+// fa_lse_merge: parts share one layout; rows = Z * H * N
+constexpr int MERGE_MAX_PARTS = 16;
+struct MergeArgs {
+    const void* o[MERGE_MAX_PARTS];
+    const float* lse[MERGE_MAX_PARTS];
+    int nparts, H, N, D;
+    int64_t rows;
+    int64_t sp_b, sp_h, sp_n;  // part strides (elements)
+    int64_t so_b, so_h, so_n;  // output strides (elements)
+    void* out;
+    float* out_lse;
+};
+cudaError_t launch_lse_merge(const MergeArgs& a, bool bf16, int grid, cudaStream_t stream);
 
 // Host-side shape facts of each specialisation.
 int block_n_for(int D);      // keys per block

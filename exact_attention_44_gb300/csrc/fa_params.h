@@ -42,6 +42,12 @@ struct FwdParams {
     uint32_t* status;        // device status word (first error wins)
     uint64_t wait_limit_ns;  // bound on every mbarrier wait
     int inject_stall;        // test hook: 1 = withhold the first K tile of CTA 0 (waits must time out)
+    // split-KV schedule (split != 0): (tile, key block) pairs cut into one range per CTA
+    int split;
+    int64_t head_blocks;     // key blocks visited by all query tiles of one (z, hq) head
+    int64_t total_blocks;    // Z * Hq * head_blocks
+    float* scratch;          // partial-result slots, 2 per CTA, each slot_floats floats
+    int64_t slot_floats;     // BM * D floats of O / l, then BM floats of base-2 lse, padded
 };
 
 }  // namespace fa

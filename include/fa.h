@@ -24,6 +24,7 @@
 #ifndef FA_H_
 #define FA_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #include <cuda_runtime_api.h>
@@ -39,7 +40,8 @@ typedef enum {
     FA_ERR_UNSUPPORTED = 2,     /* D not in {16, 32, 64, 128, 256}, dtype not fp16/bf16 */
     FA_ERR_ALIGNMENT = 3,       /* d-stride != 1, a base or stride not 16-byte aligned, negative stride */
     FA_ERR_CUDA = 4,            /* a CUDA runtime/driver call failed (launch, tensor map, device query) */
-    FA_ERR_DEVICE_TIMEOUT = 5   /* a bounded device-side wait ran out (see fa_device_status) */
+    FA_ERR_DEVICE_TIMEOUT = 5,  /* a bounded device-side wait ran out (see fa_device_status) */
+    FA_ERR_WORKSPACE = 6        /* workspace missing, not 256-byte aligned, or smaller than required */
 } fa_status;
 
 typedef enum { FA_DTYPE_F16 = 0, FA_DTYPE_BF16 = 1 } fa_dtype;
@@ -85,6 +87,84 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  int Nkv, int D, const fa_strides* sq, const fa_strides* sk, const fa_strides* sv,
                  const fa_strides* so, float scale, int causal, fa_dtype dtype, cudaStream_t stream);
 
+/*
+ * fa_fwd_splitkv -- the same attention forward as fa_fwd (same arguments,
+ * same results up to rounding), scheduled for problems with few query tiles
+ * and many keys: decode-like and cross-attention shapes, long causal heads.
+ *
+ * fa_fwd hands whole 128-row query tiles to the SMs, so with fewer tiles than
+ * SMs (or a tile count just above a multiple of it) SMs idle.  When that
+ * idle share is large (the busiest SM would get at least 2048 keys' worth of
+ * key blocks more than an even cut gives it), the (query tile, key block)
+ * pairs of all tiles are laid end to end and cut into one equal range per
+ * SM; otherwise the call runs exactly as fa_fwd does.  A tile that a cut
+ * crosses is computed in parts,
+ * each over a contiguous range of key blocks; every part leaves its O / l in
+ * fp32 and its log-sum-exp in `workspace`, and a second kernel on the same
+ * stream combines the parts of each such tile by their log-sum-exps:
+ *     lse = log(sum_s exp(lse_s)),   O = sum_s exp(lse_s - lse) * O_s,
+ * the rescaling the online softmax applies between key blocks ("Write
+ * Triton Attention Kernel", Kernel design rules), with the per-part lse of
+ * step 8.  No CTA waits for another.
+ *
+ *   workspace        device memory, 256-byte aligned, at least the size
+ *                    fa_fwd_splitkv_workspace_size() returns for D on this
+ *                    device; its contents need no initialisation and are
+ *                    overwritten.  Two calls that may run at the same time
+ *                    (different streams) must not share one workspace.
+ *   workspace_bytes  its size in bytes
+ *
+ * Errors: those of fa_fwd, plus FA_ERR_WORKSPACE for a missing, misaligned or
+ * too small workspace.  Results are bitwise reproducible for a given shape
+ * and device (the cut points depend only on the shape and the SM count).
+ */
+fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int Z, int Hq, int Hkv,
+                         int Nq, int Nkv, int D, const fa_strides* sq, const fa_strides* sk, const fa_strides* sv,
+                         const fa_strides* so, float scale, int causal, fa_dtype dtype, void* workspace,
+                         size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * fa_fwd_splitkv_workspace_size -- bytes of workspace fa_fwd_splitkv needs
+ * for head dim D on the current device, for any problem size: two partial
+ * slots per SM, each 128 x D fp32 values plus 128 fp32 log-sum-exps (about
+ * 20 MB for D = 128 and 40 MB for D = 256 on 152 SMs).  Returns
+ * FA_ERR_UNSUPPORTED for an unsupported D, FA_ERR_CUDA without a device.
+ */
+fa_status fa_fwd_splitkv_workspace_size(int D, size_t* bytes);
+
+/* Most partial results fa_lse_merge combines in one call. */
+#define FA_MERGE_MAX_PARTS 16
+
+/*
+ * fa_lse_merge -- combine attention results computed over disjoint key sets
+ * (for instance a sequence split into shards, each run through fa_fwd
+ * against its own keys, on one GPU or several) into the result over their
+ * union:
+ *     lse[r] = log(sum_s exp(lse_s[r])),
+ *     o[r,:] = sum_s exp(lse_s[r] - lse[r]) * o_s[r,:]
+ * for every row r = (z, h, n).  The parts are what fa_fwd writes: O
+ * normalised by its own denominator, in dtype, and the natural-log lse
+ * ("Write Triton Attention Kernel", step 8).  Arithmetic is fp32; O is
+ * rounded once to dtype.  A row whose parts all have lse = -inf (no kept
+ * key anywhere) gets o = 0 and lse = -inf.
+ *
+ *   nparts     1 .. FA_MERGE_MAX_PARTS
+ *   o_parts    host array of nparts device pointers, each (Z, H, N, D) dtype
+ *              with the element strides *sp (shared by all parts)
+ *   lse_parts  host array of nparts device pointers, each (Z, H, N) fp32
+ *              contiguous
+ *   o          (Z, H, N, D) dtype, strides *so (written; may alias no part)
+ *   lse        (Z, H, N) fp32 contiguous (written), or NULL to skip
+ *
+ * Requirements: D in {16, 32, 64, 128, 256}; every O pointer 16-byte aligned
+ * with d-stride 1 and other strides multiples of 8 elements; lse pointers
+ * 4-byte aligned.  Z*H*N == 0 is a no-op.  Asynchronous on `stream`;
+ * argument errors return before anything is enqueued.
+ */
+fa_status fa_lse_merge(int nparts, const void* const* o_parts, const float* const* lse_parts, int Z, int H, int N,
+                       int D, const fa_strides* sp, void* o, float* lse, const fa_strides* so, fa_dtype dtype,
+                       cudaStream_t stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* fa_status_string(fa_status status);
 
@@ -121,6 +201,8 @@ fa_status fa_fwd_plan(int Z, int Hq, int Hkv, int Nq, int Nkv, int D, int causal
  *   inside later launches (default 2000, or FA_WAIT_LIMIT_MS from the
  *   environment; ms <= 0 restores that default).  A healthy kernel waits
  *   microseconds; the bound only matters when something is wrong.
+ * fa_debug_force_split -- how fa_fwd_splitkv chooses between cutting key
+ *   ranges and whole tiles: 0 by the shape (default), 1 always cut, 2 never.
  * fa_debug_inject_stall -- when enabled, CTA 0 of later launches never issues
  *   the copy of its first K tile, so the wait for it runs out: the kernel
  *   records FA_ERR_DEVICE_TIMEOUT (read with fa_device_status), every role of
@@ -130,6 +212,7 @@ fa_status fa_fwd_plan(int Z, int Hq, int Hkv, int Nq, int Nkv, int D, int causal
  */
 void fa_debug_set_wait_limit_ms(double ms);
 void fa_debug_inject_stall(int enable);
+void fa_debug_force_split(int mode);
 
 #ifdef __cplusplus
 }

@@ -30,14 +30,20 @@ def to_device(bits: np.ndarray, dtype: str, device="cuda"):
     return si.as_torch(bits, dtype).to(device)
 
 
-def run_gpu(q, k, v, dtype, scale, causal, layout="bnsd", o_layout="bnsd"):
-    """Run libfa on seeded bits; returns (O as float64 numpy (Z,Hq,Nq,D), lse float64 (Z,Hq,Nq))."""
+def run_gpu(q, k, v, dtype, scale, causal, layout="bnsd", o_layout="bnsd", impl="fwd"):
+    """Run libfa on seeded bits; returns (O as float64 numpy (Z,Hq,Nq,D), lse float64 (Z,Hq,Nq)).
+
+    impl: "fwd" (fa_fwd, whole query tiles per CTA) or "splitkv" (fa_fwd_splitkv,
+    key blocks cut into one range per SM, parts merged by their lse)."""
     import torch
-    from exact_attention_44_gb300 import fa_device_status, fa_fwd
+    from exact_attention_44_gb300 import fa_device_status, fa_fwd, fa_fwd_splitkv
 
     qt, kt, vt = (relayout(to_device(x, dtype), layout) for x in (q, k, v))
     o = relayout(torch.empty(qt.shape, dtype=qt.dtype, device="cuda"), o_layout)
-    o, lse = fa_fwd(qt, kt, vt, o=o, scale=scale, causal=causal)
+    if impl == "splitkv":
+        o, lse = fa_fwd_splitkv(qt, kt, vt, o=o, scale=scale, causal=causal)
+    else:
+        o, lse = fa_fwd(qt, kt, vt, o=o, scale=scale, causal=causal)
     code, word = fa_device_status()
     assert code == 0, f"device status {word:#x}: a bounded wait ran out"
     return o.double().cpu().numpy(), lse.double().cpu().numpy()
@@ -72,13 +78,13 @@ def compare(o_gpu, lse_gpu, o_ref, lse_ref, dtype, what=""):
 
 
 def check_full(seed, Z, Hq, Hkv, Nq, Nkv, D, dtype, causal, scale=None, layout="bnsd", o_layout="bnsd",
-               transform=None):
+               transform=None, impl="fwd"):
     """Every output row against the oracle."""
     scale = 1 / math.sqrt(D) if scale is None else scale
     q, k, v = si.qkv(seed, Z, Hq, Hkv, Nq, Nkv, D, dtype)
     if transform is not None:
         q, k, v = transform(q, k, v)
-    o_gpu, lse_gpu = run_gpu(q, k, v, dtype, scale, causal, layout, o_layout)
+    o_gpu, lse_gpu = run_gpu(q, k, v, dtype, scale, causal, layout, o_layout, impl)
     o_ref, lse_ref = oracle.attention_fwd(q, k, v, dtype, scale, causal)
     return compare(o_gpu, lse_gpu, o_ref, lse_ref, dtype, f"{(Z, Hq, Hkv, Nq, Nkv, D, dtype, causal)}")
 
@@ -92,14 +98,15 @@ def sample_rows(Nq, n_random, rng):
     return np.array(sorted(rows), dtype=np.int64)
 
 
-def check_sampled(seed, Z, Hq, Hkv, Nq, Nkv, D, dtype, causal, n_groups=2, rows_per_head=48, scale=None):
+def check_sampled(seed, Z, Hq, Hkv, Nq, Nkv, D, dtype, causal, n_groups=2, rows_per_head=48, scale=None,
+                  impl="fwd"):
     """Full-size run on the GPU; the oracle checks sampled rows of a few GQA groups.
 
     For each sampled (z, kv head) the oracle gets just that group's query heads
     and its K/V, and computes the sampled rows one by one."""
     scale = 1 / math.sqrt(D) if scale is None else scale
     q, k, v = si.qkv(seed, Z, Hq, Hkv, Nq, Nkv, D, dtype)
-    o_gpu, lse_gpu = run_gpu(q, k, v, dtype, scale, causal)
+    o_gpu, lse_gpu = run_gpu(q, k, v, dtype, scale, causal, impl=impl)
     g = Hq // Hkv
     rng = np.random.default_rng(seed + 1)
     groups = {(0, 0), (Z - 1, Hkv - 1)}

@@ -147,3 +147,45 @@ def test_binding_never_imports_the_oracle():
             "bad = [k for k in sys.modules if k == 'oracle' or k.startswith('oracle.')]; "
             "assert not bad, bad")
     subprocess.run([sys.executable, "-c", code], check=True, cwd=ROOT)
+
+
+# ------------------------------------------------ split-KV and merge (host) ---
+
+def test_splitkv_rejects_missing_or_misaligned_workspace(lib):
+    s = (2 * 64 * 64, 64 * 64, 64, 1)
+    kv = (64 * 64, 64 * 64, 64, 1)
+    args = (0x10000, 0x10000, 0x10000, 0x10000, None, 1, 2, 1, 64, 64, 64, s, kv, kv, s, 0.125, 0, 0)
+    assert fa.fa_fwd_splitkv_raw(*args, None, 1 << 30) == fa.FA_ERR_WORKSPACE
+    assert fa.fa_fwd_splitkv_raw(*args, 0x10010, 1 << 30) == fa.FA_ERR_WORKSPACE
+    # argument errors come first, as in fa_fwd
+    bad = list(args)
+    bad[10] = 48
+    assert fa.fa_fwd_splitkv_raw(*bad, None, 0) == fa.FA_ERR_UNSUPPORTED
+    # nothing to compute: no workspace needed
+    empty = list(args)
+    empty[8] = 0
+    assert fa.fa_fwd_splitkv_raw(*empty, None, 0) == fa.FA_OK
+
+
+def _merge_raw(lib, nparts=2, Z=1, H=2, N=64, D=64, optr=0x10000, lptr=0x20000, out=0x30000, dtype=0):
+    s = fa.fa_strides(H * N * D, N * D, D, 1)
+    o_arr = (ctypes.c_void_p * max(nparts, 1))(*([optr] * max(nparts, 1)))
+    l_arr = (ctypes.c_void_p * max(nparts, 1))(*([lptr] * max(nparts, 1)))
+    return lib.fa_lse_merge(nparts, o_arr, l_arr, Z, H, N, D, ctypes.byref(s), out, None, ctypes.byref(s), dtype,
+                            None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(nparts=0), fa.FA_ERR_INVALID_ARG),
+    (dict(nparts=17), fa.FA_ERR_INVALID_ARG),
+    (dict(N=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(D=48), fa.FA_ERR_UNSUPPORTED),
+    (dict(dtype=2), fa.FA_ERR_UNSUPPORTED),
+    (dict(optr=0x10008), fa.FA_ERR_ALIGNMENT),
+    (dict(lptr=0x20002), fa.FA_ERR_ALIGNMENT),
+    (dict(lptr=0), fa.FA_ERR_INVALID_ARG),
+    (dict(out=0), fa.FA_ERR_INVALID_ARG),
+    (dict(N=0), fa.FA_OK),
+])
+def test_merge_argument_errors(lib, kw, code):
+    assert _merge_raw(lib, **kw) == code
