@@ -33,6 +33,8 @@ _SIGNATURES = {
                        [ctypes.c_void_p] * 4 + [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                                  ctypes.c_size_t, ctypes.c_void_p]),
     "fa_fwd_splitkv_workspace_size": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]),
+    "fa_fwd_splitkv_noalloc": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_void_p] + [ctypes.c_int] * 6 +
+                               [ctypes.c_void_p] * 4 + [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
     "fa_lse_merge": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_void_p)] +
                      [ctypes.c_int] * 4 + [ctypes.c_void_p] * 4 + [ctypes.c_int, ctypes.c_void_p]),
     "fa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -194,6 +196,27 @@ def fa_fwd_splitkv(q, k, v, o=None, lse=None, *, scale: float | None = None, cau
                                    ctypes.c_void_p(stream.cuda_stream))
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd_splitkv")
+    return o, lse
+
+
+def fa_fwd_splitkv_noalloc(q, k, v, o, lse=None, *, scale: float | None = None, causal: bool = False,
+                           stream=None):
+    """fa_fwd_splitkv working in the library's fixed device array instead of a workspace.
+
+    The C entry point allocates nothing; so that this wrapper does not either,
+    the caller passes the output `o` (and optionally `lse`).  Calls whose work
+    may overlap on the GPU share the array and must be ordered (one stream).
+    """
+    import torch
+
+    if o is None:
+        raise ValueError("fa_fwd_splitkv_noalloc needs a preallocated output o")
+    o, lse, dt, scale, stream, args, st = _prepare(q, k, v, o, lse, scale, False, stream)
+    with torch.cuda.device(q.device):
+        rc = load().fa_fwd_splitkv_noalloc(*args, *[ctypes.byref(x) for x in st], scale, int(bool(causal)), dt,
+                                           ctypes.c_void_p(stream.cuda_stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_splitkv_noalloc")
     return o, lse
 
 

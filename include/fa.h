@@ -132,6 +132,39 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
  */
 fa_status fa_fwd_splitkv_workspace_size(int D, size_t* bytes);
 
+/* Size in bytes of the device array fa_fwd_splitkv_noalloc works in (40 MiB). */
+#define FA_NOALLOC_SCRATCH_BYTES (40u * 1024u * 1024u)
+
+/*
+ * fa_fwd_splitkv_noalloc -- fa_fwd_splitkv without a caller workspace and
+ * without allocating anything: the partial results live in a fixed array of
+ * FA_NOALLOC_SCRATCH_BYTES inside this library's device image.  (The pages
+ * have no counterpart of this entry point.)
+ *
+ * For callers that cannot allocate device memory while they run: a
+ * cudaMalloc synchronises the whole device and can take milliseconds, which
+ * a latency-bound serving loop cannot afford; a plugin interface may hand
+ * over only input and output buffers; another allocator may own all of the
+ * device's memory.  Arguments, results and the other errors are those of
+ * fa_fwd_splitkv; this call makes no cudaMalloc or cudaFree.
+ *
+ * The array: every GPU on which this entry point runs holds it from that
+ * first call until the process exits.  The first call on each device also
+ * looks up the array's device address (once per device, with that device
+ * current); make that first call before any stream capture.  40 MiB covers
+ * two partial slots per SM at D = 256 on GPUs of up to 159 SMs; a device that
+ * needs more is rejected with FA_ERR_WORKSPACE before anything is enqueued.
+ * Nothing in the array has to start at zero: each call writes every slot it
+ * later reads.  All calls on a device share the one array, so two calls whose
+ * work may overlap on the GPU (different streams without ordering between
+ * them, or other host threads) corrupt each other's results; order them on
+ * one stream or synchronise between them.
+ */
+fa_status fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int Z, int Hq,
+                                 int Hkv, int Nq, int Nkv, int D, const fa_strides* sq, const fa_strides* sk,
+                                 const fa_strides* sv, const fa_strides* so, float scale, int causal, fa_dtype dtype,
+                                 cudaStream_t stream);
+
 /* Most partial results fa_lse_merge combines in one call. */
 #define FA_MERGE_MAX_PARTS 16
 
