@@ -68,6 +68,12 @@ def load(source: str | None = None, tag: str = "") -> ctypes.CDLL:
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_double, ctypes.c_int, ctypes.c_void_p, ctypes.c_int64,
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+            lib.oracle_attention_fwd_ex.restype = ctypes.c_int
+            lib.oracle_attention_fwd_ex.argtypes = [
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_double, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
             lib.oracle_lse_merge.restype = ctypes.c_int
             lib.oracle_lse_merge.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
                                              ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
@@ -147,3 +153,57 @@ def lse_merge(o_parts, lse_parts, lib: ctypes.CDLL | None = None):
     if rc != 0:
         raise ValueError("oracle_lse_merge: invalid arguments")
     return o.reshape(shape), lse.reshape(shape[:-1])
+
+
+def attention_fwd_ex(q: np.ndarray, k: np.ndarray, v: np.ndarray, dtype: str, scale: float, causal: bool,
+                     window=(-1, -1), alibi=None, cu_q=None, cu_k=None, rows=None, nthreads: int | None = None,
+                     lib: ctypes.CDLL | None = None):
+    """Attention forward with the variants (``oracle_attention_fwd_ex``), float64.
+
+    window: (left, right), -1 for an open side; alibi: Hq slopes or None.
+    Without cu_q/cu_k: q (Z, Hq, Nq, D), k/v (Z, Hkv, Nkv, D) bits as for
+    attention_fwd.  With them (int arrays of Z + 1 offsets): q (1, Hq, total_q, D),
+    k/v (1, Hkv, total_k, D); rows are flat ids hq * total_q + packed row, and
+    rows outside every sequence come back NaN.
+    Returns (o, lse) shaped like q without D (all rows) or (R, D) / (R,).
+    """
+    lib = lib or load()
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    k = np.ascontiguousarray(k, dtype=np.uint16)
+    v = np.ascontiguousarray(v, dtype=np.uint16)
+    Zq, Hq, Nq, D = q.shape
+    Zk, Hkv, Nkv, Dk = k.shape
+    if v.shape != k.shape or Zk != Zq or Dk != D:
+        raise ValueError(f"shape mismatch q{q.shape} k{k.shape} v{v.shape}")
+    varlen = cu_q is not None
+    if varlen:
+        cq = np.ascontiguousarray(cu_q, dtype=np.int32)
+        ck = np.ascontiguousarray(cu_k, dtype=np.int32)
+        if Zq != 1 or cq.shape != ck.shape:
+            raise ValueError("varlen takes (1, H, total, D) tensors and matching offset arrays")
+        Z = cq.size - 1
+    else:
+        cq = ck = None
+        Z = Zq
+    sl = None if alibi is None else np.ascontiguousarray(alibi, dtype=np.float64)
+    total = Hq * Nq * (1 if varlen else Z)
+    if rows is None:
+        nrows, rows_arr = total, None
+    else:
+        rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
+        nrows = rows_arr.size
+    o = np.empty((nrows, D), dtype=np.float64)
+    lse = np.empty(nrows, dtype=np.float64)
+    rc = lib.oracle_attention_fwd_ex(
+        q.ctypes.data, k.ctypes.data, v.ctypes.data, DTYPES[dtype], Z, Hq, Hkv, Nq, Nkv, D, float(scale),
+        int(bool(causal)), int(window[0]), int(window[1]), None if sl is None else sl.ctypes.data,
+        None if cq is None else cq.ctypes.data, None if ck is None else ck.ctypes.data,
+        None if rows_arr is None else rows_arr.ctypes.data, nrows, o.ctypes.data if nrows else None,
+        lse.ctypes.data if nrows else None, nthreads or host_threads())
+    if rc == -1:
+        raise ValueError("oracle_attention_fwd_ex: invalid arguments")
+    if rc != 0:
+        raise MemoryError("oracle_attention_fwd_ex: out of memory")
+    if rows is None:
+        return o.reshape(q.shape), lse.reshape(q.shape[:3])
+    return o, lse

@@ -216,3 +216,180 @@ int oracle_lse_merge(int nparts, const double* o_parts, const double* lse_parts,
     }
     return 0;
 }
+
+/* ---- variants: sliding window, ALiBi, variable-length batches --------------
+ *
+ * The page "Write Triton Attention Kernel" names windowed attention and ALiBi
+ * among the variants such a kernel serves ("Use this when"; "Inputs", item 3)
+ * and requires, for variable-length (CSR-style) batches, that each sequence's
+ * key loop end at its own length and padding never contribute ("Inputs",
+ * item 6; "Correctness requirements").  It gives no formulas; the readings
+ * taken, for query row i and key j of one sequence (positions from 0, the
+ * top-left convention of the causal mask):
+ *   - window: key j is kept iff j >= i - window_left (window_left >= 0) and
+ *     j <= i + window_right (window_right >= 0); -1 leaves that side open;
+ *     with causal, also j <= i;
+ *   - ALiBi: the scaled score gets the linear bias -slope[hq] * |i - j|;
+ *   - variable length: sequence z holds query rows cu_q[z] .. cu_q[z+1]-1 and
+ *     key rows cu_k[z] .. cu_k[z+1]-1 of packed tensors; its rows attend only
+ *     to its own keys.
+ * A row with no kept key gets O = 0 and lse = -inf.
+ */
+typedef struct {
+    const uint16_t* q;   /* (Z, Hq, Nq, D) bits, or (1, Hq, total_q, D) when varlen */
+    const double* k;     /* (Z, Hkv, Nkv, D) upcast, or (1, Hkv, total_k, D) */
+    const double* v;
+    const double* table;
+    int Z, Hq, Hkv, Nq, Nkv, D;
+    double scale;
+    int causal, window_left, window_right;
+    const double* alibi;                 /* (Hq) slopes or NULL */
+    const int32_t* cu_q;                 /* (Z + 1) or NULL */
+    const int32_t* cu_k;
+    const int64_t* rows;
+    int64_t nrows;
+    double* o;
+    double* lse;
+    int64_t begin, end;
+    int status;
+} oracle_ex_job;
+
+static void attention_row_ex(const oracle_ex_job* J, int64_t r, double* qrow, double* s, double* out,
+                             double* out_lse) {
+    const int D = J->D;
+    const int group = J->Hq / J->Hkv;  /* GQA: query heads per key/value head */
+    int64_t i, n_keys;
+    int hq, z;
+    const double *kh, *vh;
+    if (J->cu_q) {
+        const int64_t g = r % J->Nq;  /* packed query row */
+        hq = (int)(r / J->Nq);
+        for (z = 0; z < J->Z && !(g >= J->cu_q[z] && g < J->cu_q[z + 1]); ++z) {}
+        if (z == J->Z) {  /* a row of no sequence: not part of the result */
+            for (int d = 0; d < D; ++d) out[d] = NAN;
+            *out_lse = NAN;
+            return;
+        }
+        i = g - J->cu_q[z];
+        n_keys = J->cu_k[z + 1] - J->cu_k[z];
+        const int kv_head = hq / group;
+        kh = J->k + ((int64_t)kv_head * J->Nkv + J->cu_k[z]) * D;
+        vh = J->v + ((int64_t)kv_head * J->Nkv + J->cu_k[z]) * D;
+    } else {
+        i = r % J->Nq;
+        const int64_t zh = r / J->Nq;
+        hq = (int)(zh % J->Hq);
+        z = (int)(zh / J->Hq);
+        n_keys = J->Nkv;
+        const int kv_head = hq / group;
+        kh = J->k + ((int64_t)z * J->Hkv + kv_head) * J->Nkv * D;
+        vh = J->v + ((int64_t)z * J->Hkv + kv_head) * J->Nkv * D;
+    }
+    const uint16_t* qsrc = J->q + r * D;  /* flat row r of the query tensor */
+    for (int d = 0; d < D; ++d) qrow[d] = J->table[qsrc[d]];
+
+    /* kept keys: [lo, hi) */
+    int64_t lo = 0, hi = n_keys;
+    if (J->causal && i + 1 < hi) hi = i + 1;
+    if (J->window_right >= 0 && i + J->window_right + 1 < hi) hi = i + J->window_right + 1;
+    if (J->window_left >= 0 && i - J->window_left > lo) lo = i - J->window_left;
+    if (lo >= hi) {
+        for (int d = 0; d < D; ++d) out[d] = 0.0;
+        *out_lse = -INFINITY;
+        return;
+    }
+    const double slope = J->alibi ? J->alibi[hq] : 0.0;
+    for (int64_t j = lo; j < hi; ++j) {
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += qrow[d] * kh[j * D + d];
+        const double dist = (double)(i > j ? i - j : j - i);
+        s[j - lo] = J->scale * dot - slope * dist;
+    }
+    const int64_t n = hi - lo;
+    double M = -INFINITY;
+    for (int64_t t = 0; t < n; ++t) M = s[t] > M ? s[t] : M;
+    double L = 0.0;
+    for (int64_t t = 0; t < n; ++t) L += exp(s[t] - M);
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    for (int64_t t = 0; t < n; ++t) {
+        const double p = exp(s[t] - M) / L;
+        for (int d = 0; d < D; ++d) out[d] += p * vh[(lo + t) * D + d];
+    }
+    *out_lse = log(L) + M;
+}
+
+static void* oracle_ex_worker(void* arg) {
+    oracle_ex_job* J = (oracle_ex_job*)arg;
+    double* qrow = (double*)malloc(sizeof(double) * (size_t)J->D);
+    double* s = (double*)malloc(sizeof(double) * (size_t)(J->Nkv > 0 ? J->Nkv : 1));
+    if (!qrow || !s) { J->status = -2; free(qrow); free(s); return NULL; }
+    for (int64_t t = J->begin; t < J->end; ++t) {
+        const int64_t r = J->rows ? J->rows[t] : t;
+        attention_row_ex(J, r, qrow, s, J->o + t * J->D, J->lse + t);
+    }
+    free(qrow);
+    free(s);
+    return NULL;
+}
+
+/*
+ * The attention forward with the variants above.  Without cu_q/cu_k the
+ * tensors are (Z, H, N, D) as for oracle_attention_fwd and rows are flat ids
+ * (z*Hq + hq)*Nq + i; with them, Z is the number of sequences, the tensors
+ * are (1, H, total, D) with Nq = total_q and Nkv = total_k, and rows are flat
+ * ids hq*total_q + packed row (a row outside every sequence comes back NaN).
+ * alibi (Hq slopes) may be NULL; window_left/right are -1 for an open side.
+ * Returns 0, -1 for invalid arguments, -2 when memory runs out.
+ */
+int oracle_attention_fwd_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v, int dtype, int Z, int Hq,
+                            int Hkv, int Nq, int Nkv, int D, double scale, int causal, int window_left,
+                            int window_right, const double* alibi, const int32_t* cu_q, const int32_t* cu_k,
+                            const int64_t* rows, int64_t nrows, double* o, double* lse, int nthreads) {
+    if (dtype < 0 || dtype > 1 || Z < 0 || Hq < 1 || Hkv < 1 || Nq < 0 || Nkv < 0 || D < 1) return -1;
+    if (Hq % Hkv != 0 || !isfinite(scale) || nrows < 0 || window_left < -1 || window_right < -1) return -1;
+    if ((cu_q == NULL) != (cu_k == NULL)) return -1;
+    if (cu_q) {
+        if (cu_q[0] != 0 || cu_k[0] != 0) return -1;
+        for (int z = 0; z < Z; ++z)
+            if (cu_q[z + 1] < cu_q[z] || cu_k[z + 1] < cu_k[z]) return -1;
+        if (cu_q[Z] > Nq || cu_k[Z] > Nkv) return -1;
+    }
+    const int64_t total = cu_q ? (int64_t)Hq * Nq : (int64_t)Z * Hq * Nq;
+    if (!rows && nrows != total) return -1;
+    for (int64_t t = 0; rows && t < nrows; ++t)
+        if (rows[t] < 0 || rows[t] >= total) return -1;
+    if (nrows == 0) return 0;
+
+    double* table = (double*)malloc(sizeof(double) * 65536);
+    const int64_t nk = (cu_q ? (int64_t)Hkv * Nkv : (int64_t)Z * Hkv * Nkv) * D;
+    double* kd = (double*)malloc(sizeof(double) * (size_t)(nk > 0 ? nk : 1));
+    double* vd = (double*)malloc(sizeof(double) * (size_t)(nk > 0 ? nk : 1));
+    if (!table || !kd || !vd) { free(table); free(kd); free(vd); return -2; }
+    for (int b = 0; b < 65536; ++b) table[b] = oracle_decode((uint16_t)b, dtype);
+    for (int64_t x = 0; x < nk; ++x) { kd[x] = table[k[x]]; vd[x] = table[v[x]]; }
+
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 512) nthreads = 512;
+    if (nthreads > nrows) nthreads = (int)nrows;
+    oracle_ex_job* jobs = (oracle_ex_job*)calloc((size_t)nthreads, sizeof(oracle_ex_job));
+    pthread_t* tid = (pthread_t*)calloc((size_t)nthreads, sizeof(pthread_t));
+    int* created = (int*)calloc((size_t)nthreads, sizeof(int));
+    if (!jobs || !tid || !created) { free(jobs); free(tid); free(created); free(table); free(kd); free(vd); return -2; }
+    const int64_t chunk = (nrows + nthreads - 1) / nthreads;
+    for (int t = 0; t < nthreads; ++t) {
+        oracle_ex_job* J = &jobs[t];
+        *J = (oracle_ex_job){q, kd, vd, table, Z, Hq, Hkv, Nq, Nkv, D, scale, causal, window_left, window_right,
+                             alibi, cu_q, cu_k, rows, nrows, o, lse, (int64_t)t * chunk,
+                             (int64_t)t * chunk + chunk < nrows ? (int64_t)t * chunk + chunk : nrows, 0};
+        if (J->begin >= J->end) continue;
+        if (nthreads > 1 && pthread_create(&tid[t], NULL, oracle_ex_worker, J) == 0) created[t] = 1;
+        else oracle_ex_worker(J);
+    }
+    int status = 0;
+    for (int t = 0; t < nthreads; ++t) {
+        if (created[t]) pthread_join(tid[t], NULL);
+        if (jobs[t].status) status = jobs[t].status;
+    }
+    free(jobs); free(tid); free(created); free(table); free(kd); free(vd);
+    return status;
+}

@@ -35,6 +35,21 @@ MUTANTS = {
                          "const double* os = o_parts + ((int64_t)0 * rows + r) * D;"),
     "merge unshifted normaliser": ("L += exp(lse_parts[(int64_t)s * rows + r] - M);",
                                    "L += exp(lse_parts[(int64_t)s * rows + r]);"),
+    "alibi sign": ("s[j - lo] = J->scale * dot - slope * dist;", "s[j - lo] = J->scale * dot + slope * dist;"),
+    "variant K transposed": ("dot += qrow[d] * kh[j * D + d];", "dot += qrow[d] * kh[(int64_t)d * n_keys + j];"),
+    "variant lse drops max": ("*out_lse = log(L) + M;", "*out_lse = log(L);"),
+    "variant query row": ("const uint16_t* qsrc = J->q + r * D;", "const uint16_t* qsrc = J->q + (r % J->Nq) * D;"),
+    "alibi distance sign": ("const double dist = (double)(i > j ? i - j : j - i);",
+                            "const double dist = (double)(j - i);"),
+    "window left off by one": ("if (J->window_left >= 0 && i - J->window_left > lo) lo = i - J->window_left;",
+                               "if (J->window_left >= 0 && i - J->window_left + 1 > lo) lo = i - J->window_left + 1;"),
+    "window right off by one": ("if (J->window_right >= 0 && i + J->window_right + 1 < hi) hi = i + J->window_right + 1;",
+                                "if (J->window_right >= 0 && i + J->window_right < hi) hi = i + J->window_right;"),
+    "varlen key offset": ("kh = J->k + ((int64_t)kv_head * J->Nkv + J->cu_k[z]) * D;",
+                          "kh = J->k + ((int64_t)kv_head * J->Nkv + J->cu_q[z]) * D;"),
+    "variant gqa head modulo": ("const int group = J->Hq / J->Hkv;", "const int group = 1;"),
+    "varlen key count": ("n_keys = J->cu_k[z + 1] - J->cu_k[z];", "n_keys = J->cu_q[z + 1] - J->cu_q[z];"),
+    "variant causal dropped": ("if (J->causal && i + 1 < hi) hi = i + 1;", "if (0 && i + 1 < hi) hi = i + 1;"),
 }
 
 PIN_CALLS = [
@@ -53,6 +68,12 @@ PIN_CALLS = [
     ("merge shards", lambda: pins.test_merge_of_key_shards_is_attention_over_their_union((0, 40, 97))),
     ("merge closed form", pins.test_merge_two_parts_closed_form),
     ("merge equal lse", pins.test_merge_equal_lse_gives_mean_and_log_count),
+    ("ex base", lambda: pins.test_ex_with_no_variant_is_the_base_forward(True)),
+    ("window", lambda: pins.test_window_is_attention_over_the_window((5, 3), False)),
+    ("window causal", lambda: pins.test_window_is_attention_over_the_window((7, 2), True)),
+    ("alibi extra dim", lambda: pins.test_alibi_is_an_extra_dimension_where_the_distance_has_one_sign(False)),
+    ("alibi weights", pins.test_alibi_weights_decay_geometrically_and_symmetrically),
+    ("varlen", lambda: pins.test_varlen_is_attention_per_sequence(True)),
 ]
 
 

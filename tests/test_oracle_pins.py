@@ -296,3 +296,126 @@ def test_merge_ignores_empty_parts():
     assert np.array_equal(mo, ro) and np.array_equal(ml, rl)
     eo, el = oracle.lse_merge([a, b], [np.full(6, -np.inf)] * 2)
     assert np.all(eo == 0) and np.all(el == -np.inf)
+
+
+# ---------------------------------------------- variants: window, ALiBi, varlen ----
+# Each variant is pinned by reducing it to the (pinned) base definition on
+# sliced or extended inputs, or by closed-form properties of its weights.
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_ex_with_no_variant_is_the_base_forward(causal):
+    q, k, v = si.qkv(81, 2, 4, 2, 45, 70, 16, "bf16")
+    a = oracle.attention_fwd(q, k, v, "bf16", 0.3, causal)
+    b = oracle.attention_fwd_ex(q, k, v, "bf16", 0.3, causal)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def _row_on_slice(q, k, v, dtype, scale, z, hq, i, lo, hi, g):
+    """The base forward for one query row against keys lo..hi-1 only."""
+    qs = np.ascontiguousarray(q[z:z + 1, hq:hq + 1, i:i + 1])
+    ks = np.ascontiguousarray(k[z:z + 1, hq // g:hq // g + 1, lo:hi])
+    vs = np.ascontiguousarray(v[z:z + 1, hq // g:hq // g + 1, lo:hi])
+    o, lse = oracle.attention_fwd(qs, ks, vs, dtype, scale, False)
+    return o[0, 0, 0], lse[0, 0, 0]
+
+
+@pytest.mark.parametrize("window,causal", [((5, 3), False), ((0, 0), False), ((10, -1), True), ((-1, 4), False),
+                                           ((7, 2), True), ((3, -1), False)])
+def test_window_is_attention_over_the_window(window, causal):
+    dtype, scale = "fp16", 0.4
+    Z, Hq, Hkv, Nq, Nkv, D = 1, 2, 1, 37, 44, 16
+    q, k, v = si.qkv(82, Z, Hq, Hkv, Nq, Nkv, D, dtype)
+    o, lse = oracle.attention_fwd_ex(q, k, v, dtype, scale, causal, window=window)
+    wl, wr = window
+    for hq in range(Hq):
+        for i in range(Nq):
+            lo = 0 if wl < 0 else max(0, i - wl)
+            hi = Nkv if wr < 0 else min(Nkv, i + wr + 1)
+            if causal:
+                hi = min(hi, i + 1)
+            if lo >= hi:
+                assert np.all(o[0, hq, i] == 0) and lse[0, hq, i] == -np.inf
+                continue
+            ro, rl = _row_on_slice(q, k, v, dtype, scale, 0, hq, i, lo, hi, Hq // Hkv)
+            np.testing.assert_allclose(o[0, hq, i], ro, rtol=0, atol=1e-12)
+            assert abs(lse[0, hq, i] - rl) <= 1e-12
+
+
+def test_window_with_no_key_gives_zero_and_neg_inf():
+    q, k, v = si.qkv(83, 1, 1, 1, 30, 10, 16, "fp16")
+    o, lse = oracle.attention_fwd_ex(q, k, v, "fp16", 0.5, False, window=(0, 0))
+    # row i keeps only key i: rows 10.. have none
+    assert np.all(o[0, 0, 10:] == 0) and np.all(lse[0, 0, 10:] == -np.inf)
+    V = si.as_torch(v, "fp16").double().numpy()
+    np.testing.assert_array_equal(o[0, 0, :10], V[0, 0, :10])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_alibi_is_an_extra_dimension_where_the_distance_has_one_sign(causal):
+    # For keys j <= i the bias -s (i - j) = s j - s i: the same softmax as one
+    # extra dimension with q = 1 and k_j = s j / scale (exact in fp16 here),
+    # with lse shifted by -s i.  Keys j >= i (row 0) take k_j = -s j / scale.
+    dtype, scale = "fp16", 0.25
+    Z, Hq, Hkv, N, D = 1, 2, 1, 60, 16
+    slopes = np.array([1 / 64, 1 / 32])
+    q, k, v = si.qkv(84, Z, Hq, Hkv, N, N, D, dtype)
+    o, lse = oracle.attention_fwd_ex(q, k, v, dtype, scale, causal, alibi=slopes)
+    one = si.round_bits(np.ones((Z, 1, N, 1)), dtype)
+    for hq in range(Hq):
+        s = slopes[hq]
+        for sign, rows in ((+1, range(N) if causal else [N - 1]), (-1, [0])):
+            col = si.round_bits((sign * s / scale) * np.arange(N, dtype=np.float64).reshape(1, 1, N, 1), dtype)
+            assert np.array_equal(si.as_torch(col, dtype).double().numpy().ravel(),
+                                  (sign * s / scale) * np.arange(N))  # exact
+            qx = np.concatenate([q[:, hq:hq + 1], one], axis=3)
+            kx = np.concatenate([k, col], axis=3)
+            vx = v
+            bo, bl = oracle.attention_fwd(qx, kx, np.concatenate([vx, si.round_bits(np.zeros((1, 1, N, 1)), dtype)],
+                                                                 axis=3), dtype, scale, causal)
+            for i in rows:
+                np.testing.assert_allclose(o[0, hq, i], bo[0, 0, i, :D], rtol=0, atol=1e-12)
+                assert abs(lse[0, hq, i] - (bl[0, 0, i] - sign * s * i)) <= 1e-11
+
+
+def test_alibi_weights_decay_geometrically_and_symmetrically():
+    # Q = 0 leaves only the bias: with V = I the output row is the weight row
+    # P_ij proportional to exp(-s |i - j|)
+    dtype, N, s = "fp16", 16, 0.3
+    q = si.round_bits(np.zeros((1, 1, N, N)), dtype)
+    k = si.round_bits(np.ones((1, 1, N, N)), dtype)
+    v = si.round_bits(np.eye(N).reshape(1, 1, N, N), dtype)
+    P, lse = oracle.attention_fwd_ex(q, k, v, dtype, 0.7, False, alibi=[s])
+    P = P[0, 0]
+    np.testing.assert_allclose(P.sum(axis=1), 1.0, rtol=0, atol=1e-14)
+    for i in range(N):
+        for j in range(i, N - 1):
+            assert abs(P[i, j] / P[i, j + 1] - math.exp(s)) < 1e-12
+        for d in range(1, min(i, N - 1 - i) + 1):
+            assert abs(P[i, i - d] - P[i, i + d]) < 1e-15
+    # lse = log sum_j exp(-s |i - j|), a finite geometric sum
+    i = 5
+    want = math.log(sum(math.exp(-s * abs(i - j)) for j in range(N)))
+    assert abs(lse[0, 0, i] - want) < 1e-12
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_is_attention_per_sequence(causal):
+    dtype, scale, D, Hq, Hkv = "bf16", 0.3, 32, 4, 2
+    cu_q = np.array([0, 5, 5, 140, 200], dtype=np.int32)
+    cu_k = np.array([0, 7, 30, 30, 330], dtype=np.int32)
+    tq, tk = 210, 340  # packed extents; rows 200.. belong to no sequence
+    q = si.normals(85, 0, Hq * tq * D, dtype).reshape(1, Hq, tq, D)
+    k = si.normals(85, q.size, Hkv * tk * D, dtype).reshape(1, Hkv, tk, D)
+    v = si.normals(85, q.size + k.size, Hkv * tk * D, dtype).reshape(1, Hkv, tk, D)
+    o, lse = oracle.attention_fwd_ex(q, k, v, dtype, scale, causal, cu_q=cu_q, cu_k=cu_k)
+    for z in range(4):
+        a, b, c, d = cu_q[z], cu_q[z + 1], cu_k[z], cu_k[z + 1]
+        if b == a:
+            continue
+        if d == c:  # no keys: every row of the sequence is empty
+            assert np.all(o[0, :, a:b] == 0) and np.all(lse[0, :, a:b] == -np.inf)
+            continue
+        ro, rl = oracle.attention_fwd(q[:, :, a:b], k[:, :, c:d], v[:, :, c:d], dtype, scale, causal)
+        np.testing.assert_allclose(o[:, :, a:b], ro, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse[:, :, a:b], rl, rtol=0, atol=1e-12)
+    assert np.all(np.isnan(o[0, :, 200:])) and np.all(np.isnan(lse[0, :, 200:]))
