@@ -33,6 +33,9 @@ _SIGNATURES = {
                        [ctypes.c_void_p] * 4 + [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                                  ctypes.c_size_t, ctypes.c_void_p]),
     "fa_fwd_splitkv_workspace_size": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]),
+    "fa_fwd_ex": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_void_p] + [ctypes.c_int] * 6 +
+                  [ctypes.c_void_p] * 4 + [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                            ctypes.c_void_p]),
     "fa_fwd_splitkv_noalloc": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_void_p] + [ctypes.c_int] * 6 +
                                [ctypes.c_void_p] * 4 + [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
     "fa_lse_merge": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_void_p)] +
@@ -58,6 +61,11 @@ class FaError(RuntimeError):
 
 class fa_strides(ctypes.Structure):
     _fields_ = [("b", ctypes.c_int64), ("h", ctypes.c_int64), ("n", ctypes.c_int64), ("d", ctypes.c_int64)]
+
+
+class fa_fwd_options(ctypes.Structure):
+    _fields_ = [("window_left", ctypes.c_int), ("window_right", ctypes.c_int), ("alibi_slopes", ctypes.c_void_p),
+                ("cu_seqlens_q", ctypes.c_void_p), ("cu_seqlens_k", ctypes.c_void_p), ("max_seqlen_q", ctypes.c_int)]
 
 
 def library_path() -> str:
@@ -155,6 +163,66 @@ def fa_fwd(q, k, v, o=None, lse=None, *, scale: float | None = None, causal: boo
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd")
     return o, lse
+
+
+def _packed(t):
+    """(total, H, D) packed rows -> the (1, H, total, D) view the C ABI takes; 4-D passes through."""
+    return t.unsqueeze(0).permute(0, 2, 1, 3) if t.dim() == 3 else t
+
+
+def fa_fwd_ex(q, k, v, o=None, lse=None, *, scale: float | None = None, causal: bool = False, window=(-1, -1),
+              alibi_slopes=None, cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q: int | None = None,
+              stream=None, want_lse: bool = True):
+    """fa_fwd with a sliding window, ALiBi slopes and/or packed variable-length sequences (libfa's fa_fwd_ex).
+
+    window: (left, right), -1 for an open side.  alibi_slopes: CUDA fp32 (Hq,).
+    With cu_seqlens_q / cu_seqlens_k (CUDA int32, Z + 1 offsets), q, k, v
+    (and o) hold packed rows, either (total, H, D) or (1, H, total, D), and o
+    comes back in q's form; lse is then (Hq, total_q); max_seqlen_q defaults
+    to the longest query sequence (read back from the device once).
+    """
+    import torch
+
+    varlen = cu_seqlens_q is not None or cu_seqlens_k is not None
+    o_user = o
+    if varlen:
+        if cu_seqlens_q is None or cu_seqlens_k is None:
+            raise ValueError("pass both cu_seqlens_q and cu_seqlens_k")
+        if o is None and q.dim() == 3:
+            o_user = torch.empty_like(q, memory_format=torch.contiguous_format)
+        q, k, v = _packed(q), _packed(k), _packed(v)
+        if o_user is not None:
+            o = _packed(o_user)
+        if max_seqlen_q is None:
+            cq = cu_seqlens_q.cpu()
+            max_seqlen_q = int((cq[1:] - cq[:-1]).max().item()) if cq.numel() > 1 else 0
+    if o is None:
+        o = torch.empty_like(q, memory_format=torch.contiguous_format)
+    _, Hq, Nq, D = q.shape
+    if varlen and lse is None and want_lse:
+        lse = torch.empty((Hq, Nq), dtype=torch.float32, device=q.device)
+    lse_arg = lse
+    if varlen and lse is not None:
+        if lse.dtype != torch.float32 or tuple(lse.shape) != (Hq, Nq) or not lse.is_contiguous():
+            raise ValueError("lse must be a contiguous float32 (Hq, total_q) tensor")
+        lse_arg = lse.view(1, Hq, Nq)
+    o, lse_arg, dt, scale, stream, args, st = _prepare(q, k, v, o, lse_arg, scale, want_lse and not varlen, stream)
+    if varlen:
+        args[5] = cu_seqlens_q.numel() - 1  # Z: number of sequences
+        if cu_seqlens_q.dtype != torch.int32 or cu_seqlens_k.dtype != torch.int32:
+            raise TypeError("cu_seqlens must be int32")
+    if alibi_slopes is not None and (alibi_slopes.dtype != torch.float32 or alibi_slopes.numel() != Hq):
+        raise ValueError("alibi_slopes must be float32 with Hq entries")
+    opt = fa_fwd_options(int(window[0]), int(window[1]),
+                         alibi_slopes.data_ptr() if alibi_slopes is not None else None,
+                         cu_seqlens_q.data_ptr() if varlen else None, cu_seqlens_k.data_ptr() if varlen else None,
+                         int(max_seqlen_q or 0))
+    with torch.cuda.device(q.device):
+        rc = load().fa_fwd_ex(*args, *[ctypes.byref(x) for x in st], scale, int(bool(causal)), dt, ctypes.byref(opt),
+                              ctypes.c_void_p(stream.cuda_stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_ex")
+    return (o_user if o_user is not None else o), (lse if varlen else lse_arg)
 
 
 def fa_fwd_splitkv_workspace_size(D: int, device=None) -> int:

@@ -197,6 +197,16 @@ bool split_pays(const fa::FwdParams& p, bool causal, int bn, int sms) {
     return (tile_max - split_max) * bn > kSplitGainKeys;
 }
 
+cudaError_t launch_for(int D, const fa::LaunchArgs& a, bool causal, bool bf16, bool variant) {
+    switch (D) {
+        case 16: return fa::launch_d16(a, causal, bf16, variant);
+        case 32: return fa::launch_d32(a, causal, bf16, variant);
+        case 64: return fa::launch_d64(a, causal, bf16, variant);
+        case 128: return fa::launch_d128(a, causal, bf16, variant);
+        default: return fa::launch_d256(a, causal, bf16, variant);
+    }
+}
+
 fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int Z, int Hq, int Hkv, int Nq,
                    int Nkv, int D, const fa_strides* sq, const fa_strides* sk, const fa_strides* sv,
                    const fa_strides* so, float scale, int causal, fa_dtype dtype, cudaStream_t stream, bool split,
@@ -266,15 +276,85 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* 
     a.tmV = &mv;
     a.stream = stream;
 
-    cudaError_t err;
-    switch (D) {
-        case 16: err = fa::launch_d16(a, causal != 0, dtype == FA_DTYPE_BF16); break;
-        case 32: err = fa::launch_d32(a, causal != 0, dtype == FA_DTYPE_BF16); break;
-        case 64: err = fa::launch_d64(a, causal != 0, dtype == FA_DTYPE_BF16); break;
-        case 128: err = fa::launch_d128(a, causal != 0, dtype == FA_DTYPE_BF16); break;
-        default: err = fa::launch_d256(a, causal != 0, dtype == FA_DTYPE_BF16); break;
-    }
-    return err == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    return launch_for(D, a, causal != 0, dtype == FA_DTYPE_BF16, false) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+// The variant forward (fa_fwd_ex): window, ALiBi and packed variable-length
+// batches, whole tiles only.
+fa_status fwd_ex_impl(const void* q, const void* k, const void* v, void* o, float* lse, int Z, int Hq, int Hkv,
+                      int Nq, int Nkv, int D, const fa_strides* sq, const fa_strides* sk, const fa_strides* sv,
+                      const fa_strides* so, float scale, int causal, fa_dtype dtype, const fa_fwd_options* opt,
+                      cudaStream_t stream) {
+    fa_status st = check_shape(Z, Hq, Hkv, Nq, Nkv, D, causal);
+    if (st != FA_OK) return st;
+    if (dtype != FA_DTYPE_F16 && dtype != FA_DTYPE_BF16) return FA_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+    if (opt->window_left < -1 || opt->window_right < -1) return FA_ERR_INVALID_ARG;
+    const bool varlen = opt->cu_seqlens_q != nullptr || opt->cu_seqlens_k != nullptr;
+    if (varlen && (opt->cu_seqlens_q == nullptr || opt->cu_seqlens_k == nullptr || opt->max_seqlen_q < 0))
+        return FA_ERR_INVALID_ARG;
+    if (varlen && (reinterpret_cast<uintptr_t>(opt->cu_seqlens_q) % 4 != 0 ||
+                   reinterpret_cast<uintptr_t>(opt->cu_seqlens_k) % 4 != 0))
+        return FA_ERR_ALIGNMENT;
+    if (opt->alibi_slopes != nullptr && reinterpret_cast<uintptr_t>(opt->alibi_slopes) % 4 != 0)
+        return FA_ERR_ALIGNMENT;
+    const int tq = (int)cdiv(varlen ? opt->max_seqlen_q : Nq, fa::BM);
+    if ((int64_t)Z * Hq * tq > INT32_MAX) return FA_ERR_UNSUPPORTED;
+    if ((varlen ? (int64_t)Nq : (int64_t)Z * Hq * Nq) == 0 || (int64_t)Z * Hq * tq == 0) return FA_OK;
+    // packed tensors of a variable-length batch have one batch entry
+    const int nb = varlen ? 1 : Z;
+    if ((st = check_tensor(q, sq, nb, Hq, Nq)) != FA_OK) return st;
+    if ((st = check_tensor(k, sk, nb, Hkv, Nkv)) != FA_OK) return st;
+    if ((st = check_tensor(v, sv, nb, Hkv, Nkv)) != FA_OK) return st;
+    if ((st = check_tensor(o, so, nb, Hq, Nq)) != FA_OK) return st;
+    if (lse != nullptr && reinterpret_cast<uintptr_t>(lse) % 4 != 0) return FA_ERR_ALIGNMENT;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+    DeviceInfo* info = nullptr;
+    if (device_info(dev, &info) != cudaSuccess) return FA_ERR_CUDA;
+
+    const int bn = fa::block_n_for(D);
+    fa::LaunchArgs a;
+    fa::FwdParams& p = a.params;
+    p = fa::FwdParams{};
+    p.o = o;
+    p.lse = lse;
+    p.so_z = so->b;
+    p.so_h = so->h;
+    p.so_n = so->n;
+    p.Z = Z;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.Nq = Nq;
+    p.Nkv = Nkv;
+    p.group = Hq / Hkv;
+    p.Tq = tq;
+    p.Tk = (int)cdiv(Nkv, bn);
+    p.ntiles = (int)((int64_t)Z * Hq * tq);
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    p.status = info->status;
+    p.wait_limit_ns = wait_limit_ns();
+    p.inject_stall = g_inject_stall.load();
+    // a side longer than every distance between a query and a key is open
+    // (and i +- window can then not overflow on the device)
+    const int64_t reach = (int64_t)Nq + Nkv;
+    p.win_left = opt->window_left > reach ? -1 : opt->window_left;
+    p.win_right = opt->window_right > reach ? -1 : opt->window_right;
+    p.alibi = opt->alibi_slopes;
+    p.cu_q = varlen ? opt->cu_seqlens_q : nullptr;
+    p.cu_k = varlen ? opt->cu_seqlens_k : nullptr;
+    a.grid = std::min(p.ntiles, info->sms);
+
+    CUtensorMap mq, mk, mv;
+    if (make_map(&mq, q, dtype, D, Nq, Hq, nb, sq, fa::BM) != CUDA_SUCCESS) return FA_ERR_CUDA;
+    if (make_map(&mk, k, dtype, D, Nkv, Hkv, nb, sk, bn) != CUDA_SUCCESS) return FA_ERR_CUDA;
+    if (make_map(&mv, v, dtype, D, Nkv, Hkv, nb, sv, bn) != CUDA_SUCCESS) return FA_ERR_CUDA;
+    a.tmQ = &mq;
+    a.tmK = &mk;
+    a.tmV = &mv;
+    a.stream = stream;
+    return launch_for(D, a, causal != 0, dtype == FA_DTYPE_BF16, true) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 }  // namespace
@@ -332,6 +412,15 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
                          size_t workspace_bytes, cudaStream_t stream) {
     return fwd_impl(q, k, v, o, lse, Z, Hq, Hkv, Nq, Nkv, D, sq, sk, sv, so, scale, causal, dtype, stream, true,
                     workspace, workspace_bytes);
+}
+
+fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int Z, int Hq, int Hkv, int Nq,
+                    int Nkv, int D, const fa_strides* sq, const fa_strides* sk, const fa_strides* sv,
+                    const fa_strides* so, float scale, int causal, fa_dtype dtype, const fa_fwd_options* options,
+                    cudaStream_t stream) {
+    static const fa_fwd_options none = {-1, -1, nullptr, nullptr, nullptr, 0};
+    return fwd_ex_impl(q, k, v, o, lse, Z, Hq, Hkv, Nq, Nkv, D, sq, sk, sv, so, scale, causal, dtype,
+                       options ? options : &none, stream);
 }
 
 fa_status fa_fwd_splitkv_workspace_size(int D, size_t* bytes) {

@@ -7,9 +7,9 @@
 
 namespace fa {
 
-template <bool CAUSAL, bool BF16>
+template <bool CAUSAL, bool BF16, bool VAR>
 static cudaError_t launch_one(const LaunchArgs& a) {
-    auto kernel = fa_fwd_kernel<32, CAUSAL, BF16>;
+    auto kernel = fa_fwd_kernel<32, CAUSAL, BF16, VAR>;
     constexpr int smem = Traits<32>::SMEM_BYTES;
     // the opt-in shared memory size is set once per device
     static std::atomic<uint64_t> configured{0};
@@ -25,16 +25,22 @@ static cudaError_t launch_one(const LaunchArgs& a) {
     kernel<<<a.grid, NUM_THREADS, smem, a.stream>>>(*a.tmQ, *a.tmK, *a.tmV, a.params);
     err = cudaGetLastError();
     // split schedule: one merge block per cut between CTA ranges, same stream
-    if (err == cudaSuccess && a.params.split && a.grid > 1) {
-        fa_split_merge_kernel<32, CAUSAL, BF16><<<a.grid - 1, MERGE_THREADS, 0, a.stream>>>(a.params, a.grid);
-        err = cudaGetLastError();
+    if constexpr (!VAR) {
+        if (err == cudaSuccess && a.params.split && a.grid > 1) {
+            fa_split_merge_kernel<32, CAUSAL, BF16><<<a.grid - 1, MERGE_THREADS, 0, a.stream>>>(a.params, a.grid);
+            err = cudaGetLastError();
+        }
     }
     return err;
 }
 
-cudaError_t launch_d32(const LaunchArgs& a, bool causal, bool bf16) {
-    if (causal) return bf16 ? launch_one<true, true>(a) : launch_one<true, false>(a);
-    return bf16 ? launch_one<false, true>(a) : launch_one<false, false>(a);
+cudaError_t launch_d32(const LaunchArgs& a, bool causal, bool bf16, bool variant) {
+    if (variant) {
+        if (causal) return bf16 ? launch_one<true, true, true>(a) : launch_one<true, false, true>(a);
+        return bf16 ? launch_one<false, true, true>(a) : launch_one<false, false, true>(a);
+    }
+    if (causal) return bf16 ? launch_one<true, true, false>(a) : launch_one<true, false, false>(a);
+    return bf16 ? launch_one<false, true, false>(a) : launch_one<false, false, false>(a);
 }
 
 }  // namespace fa

@@ -33,6 +33,8 @@
 // status word, stops every role, lets its copies and MMAs land and frees TMEM.
 #pragma once
 
+#include <climits>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -154,6 +156,10 @@ struct Seg {
     int nkv;     // key blocks the whole tile visits
     int jb, je;  // the key blocks of this segment
     int slot;    // -1: the whole tile, finished into O and lse; else the partial-result slot
+    // the tile's sequence: query and key lengths, first packed rows, the
+    // batch coordinate of the tensor maps, and where its lse rows start
+    int nq, nk, qrow0, krow0, zc;
+    int64_t lse0;
 };
 
 // Barrier slot and phase parity of key block g (global count) in a ring of R.
@@ -180,7 +186,7 @@ __device__ __forceinline__ uint32_t rphase(uint32_t g) { return (g / R) & 1u; }
 // A causal tile stops at the key block holding its last row ("Write Triton
 // Attention Kernel", step 9).  Positions are tiles in tile mode and
 // (tile, key block) pairs in split mode.
-template <bool CAUSAL, int BN>
+template <bool CAUSAL, int BN, bool VAR = false>
 struct Sched {
     int64_t hi;  // split mode: end of this CTA's range
 
@@ -228,16 +234,30 @@ struct Sched {
     }
 
     __device__ explicit Sched(const FwdParams& p) : hi(p.split ? range_lo(blockIdx.x + 1, gridDim.x, p) : 0) {}
+    // the variant schedule skips tiles past the end of their sequence
+    __device__ __forceinline__ int64_t skip_empty(int64_t pos, const FwdParams& p) const {
+        if constexpr (VAR) {
+            for (; pos < p.ntiles; pos += gridDim.x) {
+                const Seg t = var_seg(pos, p);
+                if (t.q_start < t.nq) break;
+            }
+        }
+        return pos;
+    }
     __device__ __forceinline__ int64_t first(const FwdParams& p) const {
+        if constexpr (VAR) return skip_empty(blockIdx.x, p);
         return p.split ? range_lo(blockIdx.x, gridDim.x, p) : (int64_t)blockIdx.x;
     }
     __device__ __forceinline__ bool valid(int64_t pos, const FwdParams& p) const {
+        if constexpr (VAR) return pos < p.ntiles;
         return p.split ? pos < hi : pos < p.ntiles;
     }
     __device__ __forceinline__ int64_t next(int64_t pos, const Seg& sg, const FwdParams& p) const {
+        if constexpr (VAR) return skip_empty(pos + gridDim.x, p);
         return p.split ? pos + (sg.je - sg.jb) : pos + gridDim.x;
     }
     __device__ __forceinline__ Seg seg(int64_t pos, const FwdParams& p) const {
+        if constexpr (VAR) return var_seg(pos, p);
         Seg s;
         int64_t head;
         int mb;
@@ -256,6 +276,12 @@ struct Sched {
         s.hk = s.hq / p.group;  // GQA: kv head = q head // (Hq / Hkv)
         s.q_start = mb * BM;
         s.nkv = tile_nkv(mb, p);
+        s.nq = p.Nq;
+        s.nk = p.Nkv;
+        s.qrow0 = 0;
+        s.krow0 = 0;
+        s.zc = s.z;
+        s.lse0 = head * p.Nq;
         if (p.split) {
             const int64_t t0 = tile_pos(head, mb, p);
             s.jb = (int)(pos - t0);
@@ -268,6 +294,60 @@ struct Sched {
         }
         return s;
     }
+
+    // Variant tiles (whole tiles only): the sequence's lengths and packed
+    // offsets, and the key blocks that hold a kept key for some row of the
+    // tile -- at least one block, so that a tile whose rows keep no key at
+    // all still finishes them (as O = 0, lse = -inf).
+    __device__ __forceinline__ Seg var_seg(int64_t pos, const FwdParams& p) const {
+        Seg s;
+        const int heads = p.Z * p.Hq;
+        int head, mb;
+        if (CAUSAL) {
+            mb = p.Tq - 1 - (int)(pos / heads);
+            head = (int)(pos % heads);
+        } else {
+            head = (int)(pos / p.Tq);
+            mb = (int)(pos % p.Tq);
+        }
+        s.z = head / p.Hq;
+        s.hq = head % p.Hq;
+        s.hk = s.hq / p.group;
+        s.q_start = mb * BM;
+        if (p.cu_q != nullptr) {
+            const int q0 = __ldg(p.cu_q + s.z), q1 = __ldg(p.cu_q + s.z + 1);
+            const int k0 = __ldg(p.cu_k + s.z), k1 = __ldg(p.cu_k + s.z + 1);
+            // clamp to the packed extents so that no store leaves the tensors
+            s.qrow0 = q0 < 0 ? 0 : (q0 > p.Nq ? p.Nq : q0);
+            s.krow0 = k0 < 0 ? 0 : (k0 > p.Nkv ? p.Nkv : k0);
+            const int nq = q1 - s.qrow0, nk = k1 - s.krow0;
+            s.nq = nq < 0 ? 0 : (nq > p.Nq - s.qrow0 ? p.Nq - s.qrow0 : nq);
+            s.nk = nk < 0 ? 0 : (nk > p.Nkv - s.krow0 ? p.Nkv - s.krow0 : nk);
+            s.zc = 0;
+            s.lse0 = (int64_t)s.hq * p.Nq + s.qrow0;
+        } else {
+            s.nq = p.Nq;
+            s.nk = p.Nkv;
+            s.qrow0 = 0;
+            s.krow0 = 0;
+            s.zc = s.z;
+            s.lse0 = (int64_t)head * p.Nq;
+        }
+        const int q_last = (s.q_start + BM < s.nq ? s.q_start + BM : s.nq) - 1;
+        int hi_key = s.nk - 1;
+        if (CAUSAL && q_last < hi_key) hi_key = q_last;
+        if (p.win_right >= 0 && q_last + p.win_right < hi_key) hi_key = q_last + p.win_right;
+        const int lo_key = (p.win_left >= 0 && s.q_start - p.win_left > 0) ? s.q_start - p.win_left : 0;
+        const int tk = (s.nk + BN - 1) / BN;
+        int jb = lo_key / BN;
+        if (jb > tk - 1) jb = tk > 0 ? tk - 1 : 0;
+        const int je = hi_key >= lo_key ? hi_key / BN + 1 : jb + 1;
+        s.jb = jb;
+        s.je = je > jb ? je : jb + 1;
+        s.nkv = s.je;
+        s.slot = -1;
+        return s;
+    }
 };
 
 // ------------------------------------------------------------ TMA producers -
@@ -277,7 +357,7 @@ struct Sched {
 // tile's first K: its slot held the tile before, whose last S is complete by
 // the time the second K's slot frees anyway.
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VAR>
 __device__ void run_producer_qk(const CUtensorMap* tmQ, const CUtensorMap* tmK, const FwdParams& p, uint32_t sbase,
                                 uint32_t bar0, const Ctl& ctl) {
     using T = Traits<D>;
@@ -293,12 +373,12 @@ __device__ void run_producer_qk(const CUtensorMap* tmQ, const CUtensorMap* tmK, 
         ptx::mbar_arrive_expect_tx(bar(T::B_QFULL + s), T::Q_BYTES);
         const uint32_t dst = sbase + T::OFF_Q + s * T::Q_BYTES;
         for (int c = 0; c < T::NCHUNK; ++c)
-            ptx::tma_load_4d(dst + c * (BM * T::SW), tmQ, bar(T::B_QFULL + s), c * T::SWE, sg.q_start, sg.hq, sg.z,
-                             pol_q);
+            ptx::tma_load_4d(dst + c * (BM * T::SW), tmQ, bar(T::B_QFULL + s), c * T::SWE, sg.qrow0 + sg.q_start,
+                             sg.hq, sg.zc, pol_q);
         ++qi;
         return true;
     };
-    const Sched<CAUSAL, T::BN> sc(p);
+    const Sched<CAUSAL, T::BN, VAR> sc(p);
     int64_t pos = sc.first(p);
     if (sc.valid(pos, p)) ok = load_q(sc.seg(pos, p));
     while (ok && sc.valid(pos, p)) {
@@ -315,8 +395,8 @@ __device__ void run_producer_qk(const CUtensorMap* tmQ, const CUtensorMap* tmK, 
                 ptx::mbar_arrive_expect_tx(bar(T::B_KFULL + s), T::KV_BYTES);
                 const uint32_t dst = sbase + T::OFF_K + s * T::KV_BYTES;
                 for (int c = 0; c < T::NCHUNK; ++c)
-                    ptx::tma_load_4d(dst + c * (T::BN * T::SW), tmK, bar(T::B_KFULL + s), c * T::SWE, j * T::BN,
-                                     sg.hk, sg.z, pol_kv);
+                    ptx::tma_load_4d(dst + c * (T::BN * T::SW), tmK, bar(T::B_KFULL + s), c * T::SWE,
+                                     sg.krow0 + j * T::BN, sg.hk, sg.zc, pol_kv);
             }
             ++ki;
             // with two Q slots the next segment's Q can go right after the
@@ -341,7 +421,7 @@ __device__ void run_producer_qk(const CUtensorMap* tmQ, const CUtensorMap* tmK, 
     }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VAR>
 __device__ void run_producer_v(const CUtensorMap* tmV, const FwdParams& p, uint32_t sbase, uint32_t bar0,
                                const Ctl& ctl) {
     using T = Traits<D>;
@@ -349,7 +429,7 @@ __device__ void run_producer_v(const CUtensorMap* tmV, const FwdParams& p, uint3
     const uint64_t pol_kv = ptx::policy_evict_last();
     uint32_t vi = 0;
     bool ok = true;
-    const Sched<CAUSAL, T::BN> sc(p);
+    const Sched<CAUSAL, T::BN, VAR> sc(p);
     for (int64_t pos = sc.first(p); ok && sc.valid(pos, p);) {
         const Seg sg = sc.seg(pos, p);
         for (int j = sg.jb; j < sg.je; ++j) {
@@ -360,8 +440,8 @@ __device__ void run_producer_v(const CUtensorMap* tmV, const FwdParams& p, uint3
             ptx::mbar_arrive_expect_tx(bar(T::B_VFULL + s), T::KV_BYTES);
             const uint32_t dst = sbase + T::OFF_V + s * T::KV_BYTES;
             for (int c = 0; c < T::NCHUNK; ++c)
-                ptx::tma_load_4d(dst + c * (T::BN * T::SW), tmV, bar(T::B_VFULL + s), c * T::SWE, j * T::BN, sg.hk,
-                                 sg.z, pol_kv);
+                ptx::tma_load_4d(dst + c * (T::BN * T::SW), tmV, bar(T::B_VFULL + s), c * T::SWE,
+                                 sg.krow0 + j * T::BN, sg.hk, sg.zc, pol_kv);
             ++vi;
         }
         pos = sc.next(pos, sg, p);
@@ -381,7 +461,7 @@ __device__ void run_producer_v(const CUtensorMap* tmV, const FwdParams& p, uint3
 // Descriptors are a per-stage base word plus a compile-time offset.
 
 // S_g = Q K_gᵀ ("Write Triton Attention Kernel", step 5b) into S[g & 1]
-template <int D, bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16, bool VAR>
 __device__ void run_mma_qk(const FwdParams& p, uint32_t sbase, uint32_t bar0, uint32_t tmem, const Ctl& ctl) {
     using T = Traits<D>;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
@@ -391,7 +471,7 @@ __device__ void run_mma_qk(const FwdParams& p, uint32_t sbase, uint32_t bar0, ui
     const uint32_t k_lo0 = ptx::smem_desc_lo(sbase + T::OFF_K, 16);
     uint32_t qi = 0, g = 0;  // Q tiles and S blocks issued
     bool ok = true;
-    const Sched<CAUSAL, T::BN> sc(p);
+    const Sched<CAUSAL, T::BN, VAR> sc(p);
     for (int64_t pos = sc.first(p); ok && sc.valid(pos, p);) {
         const Seg sg = sc.seg(pos, p);
         pos = sc.next(pos, sg, p);
@@ -433,7 +513,7 @@ __device__ void run_mma_qk(const FwdParams& p, uint32_t sbase, uint32_t bar0, ui
 
 // O += P_g V_g (step 5h); the first block of a segment overwrites O, once
 // the epilogue has read the previous segment's O out of TMEM
-template <int D, bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16, bool VAR>
 __device__ void run_mma_pv(const FwdParams& p, uint32_t sbase, uint32_t bar0, uint32_t tmem, const Ctl& ctl) {
     using T = Traits<D>;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
@@ -442,7 +522,7 @@ __device__ void run_mma_pv(const FwdParams& p, uint32_t sbase, uint32_t bar0, ui
     const uint32_t v_lo0 = ptx::smem_desc_lo(sbase + T::OFF_V, T::BN * T::SW);  // LBO: next column chunk of V
     uint32_t g = 0, ntile = 0;
     bool ok = true;
-    const Sched<CAUSAL, T::BN> sc(p);
+    const Sched<CAUSAL, T::BN, VAR> sc(p);
     for (int64_t pos = sc.first(p); ok && sc.valid(pos, p); ++ntile) {
         const Seg sg = sc.seg(pos, p);
         pos = sc.next(pos, sg, p);
@@ -520,7 +600,7 @@ __device__ __forceinline__ void rescale_o(uint32_t taddr, float alpha) {
 // = query row = TMEM lane; the two halves swap partial row maxima through
 // shared memory, so both reference the same maximum m, and each keeps its
 // own partial denominator (the epilogue adds them).
-template <int D, bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16, bool VAR>
 __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, float* hand, float* red, int h,
                             const Ctl& ctl) {
     using T = Traits<D>;
@@ -531,14 +611,19 @@ __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, fl
     const int row = quad * 32 + threadIdx.x % 32;
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
     const float c = p.scale_log2;
-    const uint64_t c2 = ptx::pack_f32x2(c, c);
+    // with an ALiBi bias the scores are scaled and biased in place (units of
+    // log2), so the maximum and the exponentials take them as they are
+    const bool bias = VAR && p.alibi != nullptr;
+    const float cm = bias ? 1.f : c;
+    const uint64_t c2 = ptx::pack_f32x2(cm, cm);
     uint32_t step = 0, ntile = 0;
 
-    const Sched<CAUSAL, BN> sc(p);
+    const Sched<CAUSAL, BN, VAR> sc(p);
     for (int64_t pos = sc.first(p); sc.valid(pos, p); ++ntile) {
         const Seg ti = sc.seg(pos, p);
         pos = sc.next(pos, ti, p);
         const int q_row = ti.q_start + row;
+        const float slope2 = bias ? -__ldg(p.alibi + ti.hq) * 1.4426950408889634f : 0.f;
         // running max (log2 units of the scaled score) and denominator, fp32
         // ("Write Triton Attention Kernel", step 4; the initial l is 0)
         float m = -INFINITY, l = 0.f;
@@ -559,12 +644,38 @@ __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, fl
             // the mask goes on the scores before the row max (Correctness
             // requirements); only the diagonal block and the key tail need it
             const int k0 = j * BN + h * HC;
-            const bool need_mask = (CAUSAL && j * BN + BN - 1 > ti.q_start) || (j * BN + BN > p.Nkv);
-            if (need_mask) {
-                const int kmax = CAUSAL ? min(p.Nkv - 1, q_row) : p.Nkv - 1;  // last kept key for this row
+            if constexpr (!VAR) {
+                const bool need_mask = (CAUSAL && j * BN + BN - 1 > ti.q_start) || (j * BN + BN > p.Nkv);
+                if (need_mask) {
+                    const int kmax = CAUSAL ? min(p.Nkv - 1, q_row) : p.Nkv - 1;  // last kept key for this row
 #pragma unroll
-                for (int x = 0; x < HC; ++x)
-                    if (k0 + x > kmax) s[x] = -INFINITY;
+                    for (int x = 0; x < HC; ++x)
+                        if (k0 + x > kmax) s[x] = -INFINITY;
+                }
+            } else {
+                // kept keys of this row: kmin .. kmax (sequence end, causal
+                // diagonal, window sides); the mask is applied only when some
+                // row of the tile loses a key of this block
+                const int blast = j * BN + BN - 1;
+                bool full = blast < ti.nk;
+                if (CAUSAL) full = full && blast <= ti.q_start;
+                if (p.win_right >= 0) full = full && blast <= ti.q_start + p.win_right;
+                if (p.win_left >= 0) full = full && j * BN >= ti.q_start + BM - 1 - p.win_left;
+                if (!full) {
+                    int kmax = ti.nk - 1;
+                    if (CAUSAL) kmax = min(kmax, q_row);
+                    if (p.win_right >= 0) kmax = min(kmax, q_row + p.win_right);
+                    const int kmin = p.win_left >= 0 ? q_row - p.win_left : INT_MIN;
+#pragma unroll
+                    for (int x = 0; x < HC; ++x)
+                        if (k0 + x > kmax || k0 + x < kmin) s[x] = -INFINITY;
+                }
+                if (bias) {
+                    // scaled score plus -slope |i - j|, in log2 units
+#pragma unroll
+                    for (int x = 0; x < HC; ++x)
+                        s[x] = fmaf(s[x], c, slope2 * fabsf((float)(q_row - (k0 + x))));
+                }
             }
             float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]);
 #pragma unroll
@@ -582,7 +693,7 @@ __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, fl
             if (j == ti.jb) {
                 // the first block sets the reference maximum m
                 if (!warp_wait_phase(bar(T::B_RED + b), ph, ctl, SITE_MAX_XCHG)) return;
-                m = fmaxf(pmax, red[(b * 2 + (h ^ 1)) * BM + row]) * c;  // scale > 0
+                m = fmaxf(pmax, red[(b * 2 + (h ^ 1)) * BM + row]) * cm;  // scale > 0
             }
             // p = 2^(s·scale·log2e − m) against the current reference m; l sums
             // the fp32 p, P V uses p cast to the input type
@@ -613,10 +724,12 @@ __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, fl
                 // this block is added to them (Kernel design rules).  Both
                 // halves see the same values, so both take the same branch.
                 if (!warp_wait_phase(bar(T::B_RED + b), ph, ctl, SITE_MAX_XCHG)) return;
-                const float m_tile = fmaxf(pmax, red[(b * 2 + (h ^ 1)) * BM + row]) * c;
+                const float m_tile = fmaxf(pmax, red[(b * 2 + (h ^ 1)) * BM + row]) * cm;
                 if (__any_sync(0xffffffffu, m_tile > m + RESCALE_LOG2)) {
                     const float m_new = fmaxf(m, m_tile);
-                    alpha = ptx::ex2(m - m_new);
+                    // a row that has kept no key yet (m = -inf) has l = 0 and
+                    // O = 0: alpha 0, not 2^(-inf + inf)
+                    alpha = m == -INFINITY ? 0.f : ptx::ex2(m - m_new);
                     m = m_new;
                     sum2 = exps(m);
                     const uint32_t g = step - 1;
@@ -650,7 +763,7 @@ __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, fl
 // O = acc / l in the input type, lse = m + log(l) in natural-log units
 // ("Write Triton Attention Kernel", steps 6-8).  O is read out of TMEM and
 // converted first, TMEM is handed back to the MMA warp, then rows are stored.
-template <int D, bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16, bool VAR>
 __device__ void run_epilogue(const FwdParams& p, uint32_t bar0, uint32_t tmem, const float* hand, const Ctl& ctl) {
     using T = Traits<D>;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
@@ -660,7 +773,7 @@ __device__ void run_epilogue(const FwdParams& p, uint32_t bar0, uint32_t tmem, c
     uint32_t step = 0, ntile = 0;
     constexpr int CH = D >= 32 ? 32 : 16;               // columns per TMEM load
     constexpr int HELD = D <= 128 ? D / CH : 64 / CH;    // chunks converted before their stores
-    const Sched<CAUSAL, T::BN> sc(p);
+    const Sched<CAUSAL, T::BN, VAR> sc(p);
     for (int64_t pos = sc.first(p); sc.valid(pos, p); ++ntile) {
         const Seg ti = sc.seg(pos, p);
         pos = sc.next(pos, ti, p);
@@ -704,10 +817,11 @@ __device__ void run_epilogue(const FwdParams& p, uint32_t bar0, uint32_t tmem, c
             continue;
         }
         const int q_row = ti.q_start + row;
-        const bool store = q_row < p.Nq;
-        const float inv_l = 1.f / l;
+        const bool store = q_row < ti.nq;
+        // a variant row with no kept key (l = 0) is finished as O = 0, lse = -inf
+        const float inv_l = (VAR && !(l > 0.f)) ? 0.f : 1.f / l;
         uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
-                        2 * ((int64_t)ti.z * p.so_z + (int64_t)ti.hq * p.so_h + (int64_t)q_row * p.so_n);
+                        2 * ((int64_t)ti.zc * p.so_z + (int64_t)ti.hq * p.so_h + (int64_t)(ti.qrow0 + q_row) * p.so_n);
 #pragma unroll
         for (int base = 0; base < D / CH; base += HELD) {
             uint32_t o2[HELD][CH / 2];
@@ -736,12 +850,12 @@ __device__ void run_epilogue(const FwdParams& p, uint32_t bar0, uint32_t tmem, c
             }
         }
         if (store && p.lse != nullptr)
-            p.lse[((int64_t)ti.z * p.Hq + ti.hq) * p.Nq + q_row] = (m + log2f(l)) * 0.6931471805599453f;
+            p.lse[ti.lse0 + q_row] = (VAR && !(l > 0.f)) ? -INFINITY : (m + log2f(l)) * 0.6931471805599453f;
     }
 }
 
 // ------------------------------------------------------------ kernel --------
-template <int D, bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16, bool VAR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -775,17 +889,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const Ctl ctl{abort_flag, p.status, p.wait_limit_ns};
 
     if (warp == 0) {
-        if (lane == 0) run_producer_qk<D, CAUSAL>(&tmQ, &tmK, p, sbase, bar0, ctl);
+        if (lane == 0) run_producer_qk<D, CAUSAL, VAR>(&tmQ, &tmK, p, sbase, bar0, ctl);
     } else if (warp == 15) {
-        if (lane == 0) run_producer_v<D, CAUSAL>(&tmV, p, sbase, bar0, ctl);
+        if (lane == 0) run_producer_v<D, CAUSAL, VAR>(&tmV, p, sbase, bar0, ctl);
     } else if (warp == 1) {
-        if (lane == 0) run_mma_qk<D, CAUSAL, BF16>(p, sbase, bar0, tmem, ctl);
+        if (lane == 0) run_mma_qk<D, CAUSAL, BF16, VAR>(p, sbase, bar0, tmem, ctl);
     } else if (warp == 2) {
-        if (lane == 0) run_mma_pv<D, CAUSAL, BF16>(p, sbase, bar0, tmem, ctl);
+        if (lane == 0) run_mma_pv<D, CAUSAL, BF16, VAR>(p, sbase, bar0, tmem, ctl);
     } else if (warp < 11) {
-        run_softmax<D, CAUSAL, BF16>(p, bar0, tmem, hand, red, (warp - 3) / 4, ctl);
+        run_softmax<D, CAUSAL, BF16, VAR>(p, bar0, tmem, hand, red, (warp - 3) / 4, ctl);
     } else if (warp < 15) {
-        run_epilogue<D, CAUSAL, BF16>(p, bar0, tmem, hand, ctl);
+        run_epilogue<D, CAUSAL, BF16, VAR>(p, bar0, tmem, hand, ctl);
     }
 
     ptx::tc_fence_before();

@@ -48,6 +48,14 @@ struct FwdParams {
     int64_t total_blocks;    // Z * Hq * head_blocks
     float* scratch;          // partial-result slots, 2 per CTA, each slot_floats floats
     int64_t slot_floats;     // BM * D floats of O / l, then BM floats of base-2 lse, padded
+    // variants (the kernel instantiated with VAR): key j is kept for query i
+    // iff i - win_left <= j <= i + win_right (-1: open side); ALiBi adds
+    // -alibi[hq] * |i - j| to the scaled score; with cu_q / cu_k, Z counts
+    // sequences of packed rows and Tq covers the longest query sequence
+    int win_left, win_right;
+    const float* alibi;      // (Hq) slopes, or nullptr
+    const int* cu_q;         // (Z + 1) offsets into the packed query rows, or nullptr
+    const int* cu_k;         // (Z + 1) offsets into the packed key rows
 };
 
 }  // namespace fa

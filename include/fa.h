@@ -88,6 +88,60 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  const fa_strides* so, float scale, int causal, fa_dtype dtype, cudaStream_t stream);
 
 /*
+ * Options of fa_fwd_ex: the variants the page "Write Triton Attention Kernel"
+ * names for such a kernel ("Use this when": windowed attention, ALiBi;
+ * "Inputs", items 3 and 6, and "Correctness requirements": CSR-style
+ * variable-length batches whose key loop ends at each sequence's length).
+ * The pages give no formulas; with i the query row and j the key within one
+ * sequence (both from 0, the top-left convention of the causal mask):
+ *
+ *   window_left, window_right   key j is kept iff j >= i - window_left and
+ *                               j <= i + window_right; -1 leaves a side open
+ *                               (and with causal, also j <= i)
+ *   alibi_slopes                NULL, or a device array of Hq fp32 slopes:
+ *                               the scaled score of (i, j) in head hq gets
+ *                               -alibi_slopes[hq] * |i - j|
+ *   cu_seqlens_q, cu_seqlens_k  NULL (padded batches), or device arrays of
+ *                               Z + 1 int32 offsets: sequence z owns query
+ *                               rows cu_seqlens_q[z] .. cu_seqlens_q[z+1]-1
+ *                               and key rows cu_seqlens_k[z] .. [z+1]-1 of
+ *                               packed tensors, and attends only to its own
+ *                               keys; both start at 0 and never decrease
+ *   max_seqlen_q                with cu_seqlens: at least the longest query
+ *                               sequence (rows past it are not computed)
+ *
+ * A query row with no kept key gets O = 0 and lse = -inf.
+ */
+typedef struct {
+    int window_left;
+    int window_right;
+    const float* alibi_slopes;
+    const int32_t* cu_seqlens_q;
+    const int32_t* cu_seqlens_k;
+    int max_seqlen_q;
+} fa_fwd_options;
+
+/*
+ * fa_fwd_ex -- fa_fwd with the options above (NULL options: exactly fa_fwd's
+ * result, through the variant kernel).  Arguments are those of fa_fwd, except
+ * with cu_seqlens set: Z is the number of sequences, the tensors are packed
+ * with a batch extent of one -- q and o (1, Hq, Nq, D), k and v (1, Hkv, Nkv,
+ * D), any strides as for fa_fwd (the batch stride is ignored), Nq and Nkv the
+ * packed row counts (total rows, Nkv >= 1) -- and lse is (Hq, Nq) fp32
+ * contiguous.  Whole query tiles only (no split-KV schedule).
+ *
+ * Errors: those of fa_fwd, plus FA_ERR_INVALID_ARG for a window side below
+ * -1, only one of the cu_seqlens arrays, or max_seqlen_q < 0, and
+ * FA_ERR_ALIGNMENT for an option array not 4-byte aligned.  The contents of
+ * the device arrays are not validated on the host; offsets outside the packed
+ * extents are clamped to them on the device.
+ */
+fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int Z, int Hq, int Hkv, int Nq,
+                    int Nkv, int D, const fa_strides* sq, const fa_strides* sk, const fa_strides* sv,
+                    const fa_strides* so, float scale, int causal, fa_dtype dtype, const fa_fwd_options* options,
+                    cudaStream_t stream);
+
+/*
  * fa_fwd_splitkv -- the same attention forward as fa_fwd (same arguments,
  * same results up to rounding), scheduled for problems with few query tiles
  * and many keys: decode-like and cross-attention shapes, long causal heads.

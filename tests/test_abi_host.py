@@ -189,3 +189,20 @@ def _merge_raw(lib, nparts=2, Z=1, H=2, N=64, D=64, optr=0x10000, lptr=0x20000, 
 ])
 def test_merge_argument_errors(lib, kw, code):
     assert _merge_raw(lib, **kw) == code
+
+
+def test_fwd_ex_option_errors_on_the_host(lib):
+    s = fa.fa_strides(2 * 64 * 64, 64 * 64, 64, 1)
+    kv = fa.fa_strides(64 * 64, 64 * 64, 64, 1)
+
+    def call(**kw):
+        opt = fa.fa_fwd_options(kw.get("wl", -1), kw.get("wr", -1), kw.get("alibi"), kw.get("cq"), kw.get("ck"),
+                                kw.get("maxq", 0))
+        return lib.fa_fwd_ex(0x10000, 0x10000, 0x10000, 0x10000, None, 1, 2, 1, 64, 64, 64, ctypes.byref(s),
+                             ctypes.byref(kv), ctypes.byref(kv), ctypes.byref(s), 0.125, 0, 0, ctypes.byref(opt), None)
+    assert call(wl=-2) == fa.FA_ERR_INVALID_ARG
+    assert call(wr=-5) == fa.FA_ERR_INVALID_ARG
+    assert call(cq=0x1000) == fa.FA_ERR_INVALID_ARG          # only one offset array
+    assert call(cq=0x1000, ck=0x2000, maxq=-1) == fa.FA_ERR_INVALID_ARG
+    assert call(cq=0x1002, ck=0x2000, maxq=8) == fa.FA_ERR_ALIGNMENT
+    assert call(alibi=0x1001) == fa.FA_ERR_ALIGNMENT
