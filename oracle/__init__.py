@@ -74,6 +74,11 @@ def load(source: str | None = None, tag: str = "") -> ctypes.CDLL:
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_double, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+            lib.oracle_attention_bwd.restype = ctypes.c_int
+            lib.oracle_attention_bwd.argtypes = [
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_double, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
             lib.oracle_lse_merge.restype = ctypes.c_int
             lib.oracle_lse_merge.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
                                              ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
@@ -207,3 +212,28 @@ def attention_fwd_ex(q: np.ndarray, k: np.ndarray, v: np.ndarray, dtype: str, sc
     if rows is None:
         return o.reshape(q.shape), lse.reshape(q.shape[:3])
     return o, lse
+
+
+def attention_bwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, do: np.ndarray, dtype: str, scale: float, causal: bool,
+                  nthreads: int | None = None, lib: ctypes.CDLL | None = None):
+    """Gradients (dq, dk, dv) of the attention forward for upstream gradient do, float64.
+
+    q, do: (Z, Hq, Nq, D); k, v: (Z, Hkv, Nkv, D) uint16 bit arrays of dtype.
+    """
+    lib = lib or load()
+    q, k, v, do = (np.ascontiguousarray(x, dtype=np.uint16) for x in (q, k, v, do))
+    Z, Hq, Nq, D = q.shape
+    Zk, Hkv, Nkv, Dk = k.shape
+    if v.shape != k.shape or do.shape != q.shape or Zk != Z or Dk != D:
+        raise ValueError("shape mismatch")
+    dq = np.zeros(q.shape, dtype=np.float64)
+    dk = np.zeros(k.shape, dtype=np.float64)
+    dv = np.zeros(k.shape, dtype=np.float64)
+    rc = lib.oracle_attention_bwd(q.ctypes.data, k.ctypes.data, v.ctypes.data, do.ctypes.data, DTYPES[dtype], Z, Hq,
+                                  Hkv, Nq, Nkv, D, float(scale), int(bool(causal)), dq.ctypes.data, dk.ctypes.data,
+                                  dv.ctypes.data, nthreads or host_threads())
+    if rc == -1:
+        raise ValueError("oracle_attention_bwd: invalid arguments")
+    if rc != 0:
+        raise MemoryError("oracle_attention_bwd: out of memory")
+    return dq, dk, dv

@@ -393,3 +393,133 @@ int oracle_attention_fwd_ex(const uint16_t* q, const uint16_t* k, const uint16_t
     free(jobs); free(tid); free(created); free(table); free(kd); free(vd);
     return status;
 }
+
+/* ---- backward ---------------------------------------------------------------
+ *
+ * Gradients of the forward above (GQA and causal as there) for an upstream
+ * gradient dO, the pass the blog "把 FlashAttention 搬上昇腾：Triton-Ascend CV
+ * Pipeline 优化实战" describes in section 二 and that the saved lse serves
+ * ("Write Triton Attention Kernel", step 8).  Stated from the definition of
+ * the softmax, row by row, in float64 on the exactly decoded inputs:
+ *   P_ij  = exp(s_ij - M_i) / L_i        (s_ij = scale q_i . k_j, kept keys)
+ *   dV_j += P_ij dO_i
+ *   dP_ij = dO_i . v_j
+ *   dS_ij = P_ij (dP_ij - sum_k P_ik dP_ik)     (the softmax Jacobian)
+ *   dQ_i  = scale sum_j dS_ij k_j
+ *   dK_j += scale dS_ij q_i
+ * with dK and dV of a key/value head summed over the query heads of its group.
+ */
+typedef struct {
+    const double *q, *k, *v, *dO;    /* decoded (Z,Hq,Nq,D), (Z,Hkv,Nkv,D) x2, (Z,Hq,Nq,D) */
+    int Z, Hq, Hkv, Nq, Nkv, D;
+    double scale;
+    int causal;
+    double *dq, *dk, *dv;            /* outputs, float64 */
+    int64_t begin, end;              /* this worker's (z, kv head) groups */
+    int status;
+} oracle_bwd_job;
+
+static void* oracle_bwd_worker(void* arg) {
+    oracle_bwd_job* J = (oracle_bwd_job*)arg;
+    const int D = J->D, g = J->Hq / J->Hkv;
+    double* sc = (double*)malloc(sizeof(double) * (size_t)J->Nkv);
+    double* dp = (double*)malloc(sizeof(double) * (size_t)J->Nkv);
+    if (!sc || !dp) { J->status = -2; free(sc); free(dp); return NULL; }
+    for (int64_t grp = J->begin; grp < J->end; ++grp) {
+        const int z = (int)(grp / J->Hkv), hk = (int)(grp % J->Hkv);
+        const int64_t kvoff = ((int64_t)z * J->Hkv + hk) * J->Nkv * D;
+        const double* kh = J->k + kvoff;
+        const double* vh = J->v + kvoff;
+        double* dkh = J->dk + kvoff;
+        double* dvh = J->dv + kvoff;
+        for (int64_t x = 0; x < (int64_t)J->Nkv * D; ++x) { dkh[x] = 0.0; dvh[x] = 0.0; }
+        for (int hq = hk * g; hq < hk * g + g; ++hq) {
+            const int64_t qoff = ((int64_t)z * J->Hq + hq) * J->Nq * D;
+            for (int64_t i = 0; i < J->Nq; ++i) {
+                const double* qi = J->q + qoff + i * D;
+                const double* gi = J->dO + qoff + i * D;
+                double* dqi = J->dq + qoff + i * D;
+                int64_t n = J->Nkv;
+                if (J->causal && i + 1 < n) n = i + 1;
+                double Mx = -INFINITY;  /* row maximum and normaliser of the scaled scores */
+                for (int64_t j = 0; j < n; ++j) {
+                    double qk = 0.0;
+                    for (int d = 0; d < D; ++d) qk += qi[d] * kh[j * D + d];
+                    sc[j] = J->scale * qk;
+                    Mx = sc[j] > Mx ? sc[j] : Mx;
+                }
+                double Ls = 0.0;
+                for (int64_t j = 0; j < n; ++j) Ls += exp(sc[j] - Mx);
+                double rowdot = 0.0;  /* sum_k P_ik dP_ik */
+                for (int64_t j = 0; j < n; ++j) {
+                    const double pj = exp(sc[j] - Mx) / Ls;
+                    double acc = 0.0;
+                    for (int d = 0; d < D; ++d) acc += gi[d] * vh[j * D + d];
+                    dp[j] = acc;
+                    rowdot += pj * acc;
+                    for (int d = 0; d < D; ++d) dvh[j * D + d] += pj * gi[d];
+                }
+                for (int d = 0; d < D; ++d) dqi[d] = 0.0;
+                for (int64_t j = 0; j < n; ++j) {
+                    const double pj = exp(sc[j] - Mx) / Ls;
+                    const double dsj = pj * (dp[j] - rowdot);
+                    for (int d = 0; d < D; ++d) {
+                        dqi[d] += J->scale * dsj * kh[j * D + d];
+                        dkh[j * D + d] += J->scale * dsj * qi[d];
+                    }
+                }
+            }
+        }
+    }
+    free(sc);
+    free(dp);
+    return NULL;
+}
+
+/*
+ * Backward of the attention forward: q, dO (Z, Hq, Nq, D) and k, v
+ * (Z, Hkv, Nkv, D) contiguous bits of dtype 0 (fp16) or 1 (bf16); writes
+ * dq (Z, Hq, Nq, D) and dk, dv (Z, Hkv, Nkv, D) in float64.
+ * Returns 0, -1 for invalid arguments, -2 when memory runs out.
+ */
+int oracle_attention_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* dO, int dtype,
+                         int Z, int Hq, int Hkv, int Nq, int Nkv, int D, double scale, int causal, double* dq,
+                         double* dk, double* dv, int nthreads) {
+    if (dtype < 0 || dtype > 1 || Z < 0 || Hq < 1 || Hkv < 1 || Nq < 0 || Nkv < 1 || D < 1) return -1;
+    if (Hq % Hkv != 0 || !isfinite(scale)) return -1;
+    const int64_t nq = (int64_t)Z * Hq * Nq * D, nk = (int64_t)Z * Hkv * Nkv * D;
+    if (nk == 0) return 0;
+    double* table = (double*)malloc(sizeof(double) * 65536);
+    double* buf = (double*)malloc(sizeof(double) * (size_t)(2 * nq + 2 * nk + 1));
+    if (!table || !buf) { free(table); free(buf); return -2; }
+    for (int b = 0; b < 65536; ++b) table[b] = oracle_decode((uint16_t)b, dtype);
+    double *qd = buf, *gd = buf + nq, *kd = buf + 2 * nq, *vd = buf + 2 * nq + nk;
+    for (int64_t x = 0; x < nq; ++x) { qd[x] = table[q[x]]; gd[x] = table[dO[x]]; }
+    for (int64_t x = 0; x < nk; ++x) { kd[x] = table[k[x]]; vd[x] = table[v[x]]; }
+
+    const int64_t groups = (int64_t)Z * Hkv;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 512) nthreads = 512;
+    if (nthreads > groups) nthreads = (int)groups;
+    oracle_bwd_job* jobs = (oracle_bwd_job*)calloc((size_t)nthreads, sizeof(oracle_bwd_job));
+    pthread_t* tid = (pthread_t*)calloc((size_t)nthreads, sizeof(pthread_t));
+    int* created = (int*)calloc((size_t)nthreads, sizeof(int));
+    if (!jobs || !tid || !created) { free(jobs); free(tid); free(created); free(table); free(buf); return -2; }
+    const int64_t chunk = (groups + nthreads - 1) / nthreads;
+    for (int t = 0; t < nthreads; ++t) {
+        oracle_bwd_job* J = &jobs[t];
+        *J = (oracle_bwd_job){qd, kd, vd, gd, Z, Hq, Hkv, Nq, Nkv, D, scale, causal, dq, dk, dv,
+                              (int64_t)t * chunk, (int64_t)t * chunk + chunk < groups ? (int64_t)t * chunk + chunk : groups,
+                              0};
+        if (J->begin >= J->end) continue;
+        if (nthreads > 1 && pthread_create(&tid[t], NULL, oracle_bwd_worker, J) == 0) created[t] = 1;
+        else oracle_bwd_worker(J);
+    }
+    int status = 0;
+    for (int t = 0; t < nthreads; ++t) {
+        if (created[t]) pthread_join(tid[t], NULL);
+        if (jobs[t].status) status = jobs[t].status;
+    }
+    free(jobs); free(tid); free(created); free(table); free(buf);
+    return status;
+}

@@ -49,6 +49,16 @@ MUTANTS = {
                           "kh = J->k + ((int64_t)kv_head * J->Nkv + J->cu_q[z]) * D;"),
     "variant gqa head modulo": ("const int group = J->Hq / J->Hkv;", "const int group = 1;"),
     "varlen key count": ("n_keys = J->cu_k[z + 1] - J->cu_k[z];", "n_keys = J->cu_q[z + 1] - J->cu_q[z];"),
+    "bwd dq scale dropped": ("dqi[d] += J->scale * dsj * kh[j * D + d];", "dqi[d] += dsj * kh[j * D + d];"),
+    "bwd softmax jacobian": ("const double dsj = pj * (dp[j] - rowdot);", "const double dsj = pj * dp[j];"),
+    "bwd dv uses dp": ("dvh[j * D + d] += pj * gi[d];", "dvh[j * D + d] += dp[j] * gi[d];"),
+    "bwd dk uses k": ("dkh[j * D + d] += J->scale * dsj * qi[d];", "dkh[j * D + d] += J->scale * dsj * kh[j * D + d];"),
+    "bwd causal dropped": ("if (J->causal && i + 1 < n) n = i + 1;", "if (0 && i + 1 < n) n = i + 1;"),
+    "bwd rowdot unweighted": ("rowdot += pj * acc;", "rowdot += acc;"),
+    "bwd unshifted normaliser": ("Ls += exp(sc[j] - Mx);", "Ls += exp(sc[j]);"),
+    "bwd score scale dropped": ("sc[j] = J->scale * qk;", "sc[j] = qk;"),
+    "bwd dp uses q": ("for (int d = 0; d < D; ++d) acc += gi[d] * vh[j * D + d];",
+                      "for (int d = 0; d < D; ++d) acc += qi[d] * vh[j * D + d];"),
     "variant causal dropped": ("if (J->causal && i + 1 < hi) hi = i + 1;", "if (0 && i + 1 < hi) hi = i + 1;"),
 }
 
@@ -74,6 +84,9 @@ PIN_CALLS = [
     ("alibi extra dim", lambda: pins.test_alibi_is_an_extra_dimension_where_the_distance_has_one_sign(False)),
     ("alibi weights", pins.test_alibi_weights_decay_geometrically_and_symmetrically),
     ("varlen", lambda: pins.test_varlen_is_attention_per_sequence(True)),
+    ("bwd fd", lambda: pins.test_bwd_matches_finite_differences("bf16", True, (2, 4, 2, 9, 6, 4))),
+    ("bwd single key", pins.test_bwd_single_key_closed_form),
+    ("bwd scale zero", pins.test_bwd_scale_zero_closed_form),
 ]
 
 

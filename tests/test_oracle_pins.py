@@ -419,3 +419,93 @@ def test_varlen_is_attention_per_sequence(causal):
         np.testing.assert_allclose(o[:, :, a:b], ro, rtol=0, atol=1e-12)
         np.testing.assert_allclose(lse[:, :, a:b], rl, rtol=0, atol=1e-12)
     assert np.all(np.isnan(o[0, :, 200:])) and np.all(np.isnan(lse[0, :, 200:]))
+
+
+# ---------------------------------------------------------------- backward ----
+# The gradients are pinned by central finite differences of an independent
+# float64 forward (numpy matmul + scipy softmax), by closed forms, and by the
+# GQA reduction.
+
+def _np_forward(Q, K, V, scale, causal):
+    """float64 attention forward from library routines, for finite differences."""
+    from scipy.special import softmax
+    Z, Hq, Nq, D = Q.shape
+    g = Hq // K.shape[1]
+    O = np.empty_like(Q)
+    for z in range(Z):
+        for h in range(Hq):
+            S = scale * Q[z, h] @ K[z, h // g].T
+            if causal:
+                S = np.where(np.arange(K.shape[2])[None, :] > np.arange(Nq)[:, None], -np.inf, S)
+            O[z, h] = softmax(S, axis=1) @ V[z, h // g]
+    return O
+
+
+@pytest.mark.parametrize("dtype,causal,shape", [("fp16", False, (1, 2, 1, 7, 9, 8)), ("bf16", True, (2, 4, 2, 9, 6, 4)),
+                                                ("fp16", True, (1, 2, 2, 5, 5, 16))])
+def test_bwd_matches_finite_differences(dtype, causal, shape):
+    Z, Hq, Hkv, Nq, Nkv, D = shape
+    scale = 0.6
+    q, k, v = si.qkv(111, Z, Hq, Hkv, Nq, Nkv, D, dtype)
+    do = si.normals(112, 0, q.size, dtype).reshape(q.shape)
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, dtype, scale, causal)
+    Q, K, V, G = (_np_decode(x, dtype) for x in (q, k, v, do))
+
+    def loss(Qx, Kx, Vx):
+        return float(np.sum(G * _np_forward(Qx, Kx, Vx, scale, causal)))
+
+    rng = np.random.default_rng(7)
+    h = 1e-5
+    for name, X, grad in (("q", Q, dq), ("k", K, dk), ("v", V, dv)):
+        for _ in range(12):
+            idx = tuple(int(rng.integers(n)) for n in X.shape)
+            Xp, Xm = X.copy(), X.copy()
+            Xp[idx] += h
+            Xm[idx] -= h
+            args_p = {"q": (Xp, K, V), "k": (Q, Xp, V), "v": (Q, K, Xp)}[name]
+            args_m = {"q": (Xm, K, V), "k": (Q, Xm, V), "v": (Q, K, Xm)}[name]
+            fd = (loss(*args_p) - loss(*args_m)) / (2 * h)
+            assert abs(fd - grad[idx]) <= 1e-7 * max(1.0, abs(fd)), (name, idx, fd, grad[idx])
+
+
+def test_bwd_single_key_closed_form():
+    # one key: P = 1, so dS = 0 (dQ = dK = 0) and dV_0 is the sum of dO over the group's rows
+    q, k, v = si.qkv(113, 2, 4, 2, 6, 1, 8, "fp16")
+    do = si.normals(114, 0, q.size, "fp16").reshape(q.shape)
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, "fp16", 0.9, False)
+    G = _np_decode(do, "fp16")
+    assert np.all(dq == 0) and np.all(dk == 0)
+    for z in range(2):
+        for hk in range(2):
+            np.testing.assert_allclose(dv[z, hk, 0], G[z, 2 * hk:2 * hk + 2].sum(axis=(0, 1)), rtol=0, atol=1e-12)
+
+
+def test_bwd_scale_zero_closed_form():
+    # scale 0: uniform P over the kept keys, dQ = dK = 0, dV_j = sum over rows keeping j of dO_i / n_i
+    Nq = Nkv = 7
+    q, k, v = si.qkv(115, 1, 1, 1, Nq, Nkv, 8, "bf16")
+    do = si.normals(116, 0, q.size, "bf16").reshape(q.shape)
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, "bf16", 0.0, True)
+    G = _np_decode(do, "bf16")[0, 0]
+    assert np.all(dq == 0) and np.all(dk == 0)
+    for j in range(Nkv):
+        want = sum(G[i] / (i + 1) for i in range(j, Nq))
+        np.testing.assert_allclose(dv[0, 0, j], want, rtol=0, atol=1e-12)
+
+
+def test_bwd_gqa_is_mha_summed_over_the_group():
+    q, k, v = si.qkv(117, 1, 4, 1, 10, 12, 8, "fp16")
+    do = si.normals(118, 0, q.size, "fp16").reshape(q.shape)
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, "fp16", 0.4, True)
+    kr, vr = np.repeat(k, 4, axis=1), np.repeat(v, 4, axis=1)
+    mq, mk, mv = oracle.attention_bwd(q, kr, vr, do, "fp16", 0.4, True)
+    np.testing.assert_allclose(dq, mq, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dk[:, 0], mk.sum(axis=1), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dv[:, 0], mv.sum(axis=1), rtol=0, atol=1e-12)
+
+
+def test_bwd_causal_first_row_has_no_query_gradient():
+    q, k, v = si.qkv(119, 1, 2, 2, 8, 8, 8, "fp16")
+    do = si.normals(120, 0, q.size, "fp16").reshape(q.shape)
+    dq, _, _ = oracle.attention_bwd(q, k, v, do, "fp16", 0.7, True)
+    assert np.all(dq[:, :, 0] == 0) and np.any(dq[:, :, 1] != 0)
