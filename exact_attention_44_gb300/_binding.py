@@ -33,6 +33,9 @@ _SIGNATURES = {
                        [ctypes.c_void_p] * 4 + [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                                  ctypes.c_size_t, ctypes.c_void_p]),
     "fa_fwd_splitkv_workspace_size": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]),
+    "fa_bwd": (ctypes.c_int, [ctypes.c_void_p] * 9 + [ctypes.c_int] * 6 + [ctypes.c_void_p] * 8 +
+               [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "fa_bwd_workspace_size": (ctypes.c_int, [ctypes.c_int] * 4 + [ctypes.POINTER(ctypes.c_size_t)]),
     "fa_fwd_ex": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_void_p] + [ctypes.c_int] * 6 +
                   [ctypes.c_void_p] * 4 + [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                             ctypes.c_void_p]),
@@ -223,6 +226,55 @@ def fa_fwd_ex(q, k, v, o=None, lse=None, *, scale: float | None = None, causal: 
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd_ex")
     return (o_user if o_user is not None else o), (lse if varlen else lse_arg)
+
+
+def fa_bwd_workspace_size(Z: int, Hq: int, Nq: int, D: int) -> int:
+    """Workspace bytes fa_bwd needs (host only)."""
+    n = ctypes.c_size_t(0)
+    rc = load().fa_bwd_workspace_size(int(Z), int(Hq), int(Nq), int(D), ctypes.byref(n))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_bwd_workspace_size")
+    return n.value
+
+
+def fa_bwd(q, k, v, o, lse, do, dq=None, dk=None, dv=None, *, scale: float | None = None, causal: bool = False,
+           workspace=None, stream=None):
+    """Gradients (dq, dk, dv) of the attention forward through libfa's fa_bwd.
+
+    q, k, v, o, lse: the forward's inputs, output and lse (fa_fwd's layouts);
+    do: upstream gradient shaped like o.  Outputs are allocated when omitted;
+    workspace (CUDA uint8, >= fa_bwd_workspace_size bytes) likewise.
+    """
+    import torch
+
+    Z, Hq, Nq, D = q.shape
+    _, Hkv, Nkv, _ = k.shape
+    dt = _dtype_code(q)
+    for name, t in (("k", k), ("v", v), ("o", o), ("do", do)):
+        if t.dtype != q.dtype:
+            raise TypeError(f"{name} must have q's dtype")
+    if tuple(o.shape) != tuple(q.shape) or tuple(do.shape) != tuple(q.shape) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("shape mismatch")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (Z, Hq, Nq) or not lse.is_contiguous():
+        raise ValueError("lse must be the forward's contiguous float32 (Z, Hq, Nq) tensor")
+    dq = torch.empty_like(q, memory_format=torch.contiguous_format) if dq is None else dq
+    dk = torch.empty_like(k, memory_format=torch.contiguous_format) if dk is None else dk
+    dv = torch.empty_like(v, memory_format=torch.contiguous_format) if dv is None else dv
+    if workspace is None:
+        workspace = torch.empty(fa_bwd_workspace_size(Z, Hq, Nq, D), dtype=torch.uint8, device=q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    st = [_strides(x) for x in (q, k, v, o, do, dq, dk, dv)]
+    with torch.cuda.device(q.device):
+        rc = load().fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+                           dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), Z, Hq, Hkv, Nq, Nkv, D,
+                           *[ctypes.byref(x) for x in st], float(scale), int(bool(causal)), dt, workspace.data_ptr(),
+                           workspace.numel() * workspace.element_size(), ctypes.c_void_p(stream.cuda_stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_bwd")
+    return dq, dk, dv
 
 
 def fa_fwd_splitkv_workspace_size(D: int, device=None) -> int:

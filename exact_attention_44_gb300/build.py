@@ -23,7 +23,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libfa.so")
 
-SOURCES = ["fa_api.cu", "fa_lse_merge.cu", "fa_noalloc.cu"] + [f"fa_fwd_d{d}.cu" for d in (16, 32, 64, 128, 256)]
+SOURCES = (["fa_api.cu", "fa_lse_merge.cu", "fa_noalloc.cu"] + [f"fa_fwd_d{d}.cu" for d in (16, 32, 64, 128, 256)] +
+           [f"fa_bwd_d{d}.cu" for d in (16, 32, 64, 128)])
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
                 "--expt-relaxed-constexpr", f"-I{INCLUDE}", f"-I{CSRC}"]

@@ -7,10 +7,12 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <cstdio>
 #include <cstdlib>
 #include <mutex>
 
 #include "fa.h"
+#include "fa_bwd_kernel.cuh"
 #include "fa_fwd_kernel.cuh"
 #include "fa_launch.h"
 
@@ -69,6 +71,16 @@ uint64_t wait_limit_ns() {
     g_wait_limit_ns.store(v);
     return v;
 }
+
+// With FA_DEBUG set in the environment, a failed CUDA call is described on
+// stderr before FA_ERR_CUDA is returned.
+fa_status cuda_fail(const char* what, int code, const char* text) {
+    static const bool verbose = std::getenv("FA_DEBUG") != nullptr;
+    if (verbose) std::fprintf(stderr, "libfa: %s failed: %d %s\n", what, code, text ? text : "");
+    return FA_ERR_CUDA;
+}
+fa_status cuda_fail(const char* what, cudaError_t e) { return cuda_fail(what, (int)e, cudaGetErrorString(e)); }
+fa_status cuda_fail(const char* what, CUresult r) { return cuda_fail(what, (int)r, "driver error"); }
 
 bool supported_head_dim(int D) { return D == 16 || D == 32 || D == 64 || D == 128 || D == 256; }
 
@@ -147,6 +159,15 @@ int swizzle_elems_for(int D) { int a, b, c; facts_for(D, &a, &b, &c); return c; 
 }  // namespace fa
 
 namespace {
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Backward workspace: the fp32 dQ accumulator, then lse2 and Δ per query
+// row padded to whole 128-row blocks.
+size_t bwd_workspace_bytes(int Z, int Hq, int Nq, int D) {
+    const size_t tq = (size_t)cdiv(Nq, 128);
+    return align256((size_t)Z * Hq * Nq * D * 4) + 2 * align256((size_t)Z * Hq * tq * 128 * 4);
+}
 
 // Floats per partial-result slot of the split schedule: O / l of BM rows
 // (BM x D) and their base-2 log-sum-exps (BM), padded to 256 bytes.
@@ -276,7 +297,8 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* 
     a.tmV = &mv;
     a.stream = stream;
 
-    return launch_for(D, a, causal != 0, dtype == FA_DTYPE_BF16, false) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    const cudaError_t err = launch_for(D, a, causal != 0, dtype == FA_DTYPE_BF16, false);
+    return err == cudaSuccess ? FA_OK : cuda_fail("forward launch", err);
 }
 
 // The variant forward (fa_fwd_ex): window, ALiBi and packed variable-length
@@ -421,6 +443,108 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float*
     static const fa_fwd_options none = {-1, -1, nullptr, nullptr, nullptr, 0};
     return fwd_ex_impl(q, k, v, o, lse, Z, Hq, Hkv, Nq, Nkv, D, sq, sk, sv, so, scale, causal, dtype,
                        options ? options : &none, stream);
+}
+
+fa_status fa_bwd_workspace_size(int Z, int Hq, int Nq, int D, size_t* bytes) {
+    if (bytes == nullptr || Z < 0 || Hq < 0 || Nq < 0) return FA_ERR_INVALID_ARG;
+    if (!(D == 16 || D == 32 || D == 64 || D == 128)) return FA_ERR_UNSUPPORTED;
+    *bytes = bwd_workspace_bytes(Z, Hq, Nq, D);
+    return FA_OK;
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                 void* dq, void* dk, void* dv, int Z, int Hq, int Hkv, int Nq, int Nkv, int D, const fa_strides* sq,
+                 const fa_strides* sk, const fa_strides* sv, const fa_strides* so, const fa_strides* sdo,
+                 const fa_strides* sdq, const fa_strides* sdk, const fa_strides* sdv, float scale, int causal,
+                 fa_dtype dtype, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    fa_status st = check_shape(Z, Hq, Hkv, Nq, Nkv, D, causal);
+    if (st != FA_OK) return st;
+    if (!(D == 16 || D == 32 || D == 64 || D == 128)) return FA_ERR_UNSUPPORTED;
+    if (dtype != FA_DTYPE_F16 && dtype != FA_DTYPE_BF16) return FA_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+    if ((int64_t)Z * Hkv * Nkv == 0) return FA_OK;
+    if (Nq == 0) return FA_ERR_INVALID_ARG;  // gradients of an empty query set: nothing to differentiate
+    if ((st = check_tensor(q, sq, Z, Hq, Nq)) != FA_OK) return st;
+    if ((st = check_tensor(k, sk, Z, Hkv, Nkv)) != FA_OK) return st;
+    if ((st = check_tensor(v, sv, Z, Hkv, Nkv)) != FA_OK) return st;
+    if ((st = check_tensor(o, so, Z, Hq, Nq)) != FA_OK) return st;
+    if ((st = check_tensor(dO, sdo, Z, Hq, Nq)) != FA_OK) return st;
+    if ((st = check_tensor(dq, sdq, Z, Hq, Nq)) != FA_OK) return st;
+    if ((st = check_tensor(dk, sdk, Z, Hkv, Nkv)) != FA_OK) return st;
+    if ((st = check_tensor(dv, sdv, Z, Hkv, Nkv)) != FA_OK) return st;
+    if (lse == nullptr) return FA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(lse) % 4 != 0) return FA_ERR_ALIGNMENT;
+    if (workspace == nullptr || reinterpret_cast<uintptr_t>(workspace) % 256 != 0 ||
+        workspace_bytes < bwd_workspace_bytes(Z, Hq, Nq, D))
+        return FA_ERR_WORKSPACE;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+    DeviceInfo* info = nullptr;
+    if (device_info(dev, &info) != cudaSuccess) return FA_ERR_CUDA;
+
+    fa::BwdLaunchArgs a;
+    fa::BwdParams& p = a.params;
+    p = fa::BwdParams{};
+    p.o = o;
+    p.lse = lse;
+    p.dO = dO;
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    p.so_z = so->b; p.so_h = so->h; p.so_n = so->n;
+    p.sdo_z = sdo->b; p.sdo_h = sdo->h; p.sdo_n = sdo->n;
+    p.sdq_z = sdq->b; p.sdq_h = sdq->h; p.sdq_n = sdq->n;
+    p.sdk_z = sdk->b; p.sdk_h = sdk->h; p.sdk_n = sdk->n;
+    p.sdv_z = sdv->b; p.sdv_h = sdv->h; p.sdv_n = sdv->n;
+    p.Z = Z;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.Nq = Nq;
+    p.Nkv = Nkv;
+    p.group = Hq / Hkv;
+    p.Tq = (int)cdiv(Nq, 128);
+    p.Tk = (int)cdiv(Nkv, 128);
+    const int64_t units = (int64_t)Z * Hkv * p.Tk;
+    if (units > INT32_MAX) return FA_ERR_UNSUPPORTED;
+    p.nunits = (int)units;
+    p.scale = scale;
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const size_t acc_bytes = align256((size_t)Z * Hq * Nq * D * 4);
+    const size_t row_bytes = align256((size_t)Z * Hq * p.Tq * 128 * 4);
+    p.dq_acc = reinterpret_cast<float*>(ws);
+    p.lse2 = reinterpret_cast<float*>(ws + acc_bytes);
+    p.delta = reinterpret_cast<float*>(ws + acc_bytes + row_bytes);
+    p.status = info->status;
+    p.wait_limit_ns = wait_limit_ns();
+
+    CUtensorMap mk, mv, mq, mdo;
+    CUresult cr;
+    if ((cr = make_map(&mk, k, dtype, D, Nkv, Hkv, Z, sk, 128)) != CUDA_SUCCESS) return cuda_fail("K tensor map", cr);
+    if ((cr = make_map(&mv, v, dtype, D, Nkv, Hkv, Z, sv, 128)) != CUDA_SUCCESS) return cuda_fail("V tensor map", cr);
+    if ((cr = make_map(&mq, q, dtype, D, Nq, Hq, Z, sq, 128)) != CUDA_SUCCESS) return cuda_fail("Q tensor map", cr);
+    if ((cr = make_map(&mdo, dO, dtype, D, Nq, Hq, Z, sdo, 128)) != CUDA_SUCCESS)
+        return cuda_fail("dO tensor map", cr);
+    a.tmK = &mk;
+    a.tmV = &mv;
+    a.tmQ = &mq;
+    a.tmDO = &mdo;
+    a.grid = (int)std::min<int64_t>(units, info->sms);
+    const int64_t pre_rows = (int64_t)Z * Hq * p.Tq * 128;
+    a.pre_grid = (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(pre_rows, 256), (int64_t)info->sms * 8));
+    const int64_t post_items = (int64_t)Z * Hq * Nq * (D / 8);
+    a.post_grid = (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(post_items, 256), (int64_t)info->sms * 8));
+    a.stream = stream;
+    const bool bf16 = dtype == FA_DTYPE_BF16;
+    cudaError_t err;
+    switch (D) {
+        case 16: err = fa::launch_bwd_d16(a, causal != 0, bf16); break;
+        case 32: err = fa::launch_bwd_d32(a, causal != 0, bf16); break;
+        case 64: err = fa::launch_bwd_d64(a, causal != 0, bf16); break;
+        default: err = fa::launch_bwd_d128(a, causal != 0, bf16); break;
+    }
+    return err == cudaSuccess ? FA_OK : cuda_fail("backward launch", err);
 }
 
 fa_status fa_fwd_splitkv_workspace_size(int D, size_t* bytes) {

@@ -41,6 +41,21 @@ struct MergeArgs {
 };
 cudaError_t launch_lse_merge(const MergeArgs& a, bool bf16, int grid, cudaStream_t stream);
 
+// Backward: pre kernel, gradient kernel, dQ conversion on one stream
+struct BwdLaunchArgs {
+    const CUtensorMap* tmK;
+    const CUtensorMap* tmV;
+    const CUtensorMap* tmQ;
+    const CUtensorMap* tmDO;
+    BwdParams params;
+    int grid, pre_grid, post_grid;
+    cudaStream_t stream;
+};
+cudaError_t launch_bwd_d16(const BwdLaunchArgs& a, bool causal, bool bf16);
+cudaError_t launch_bwd_d32(const BwdLaunchArgs& a, bool causal, bool bf16);
+cudaError_t launch_bwd_d64(const BwdLaunchArgs& a, bool causal, bool bf16);
+cudaError_t launch_bwd_d128(const BwdLaunchArgs& a, bool causal, bool bf16);
+
 // Host-side shape facts of each specialisation.
 int block_n_for(int D);      // keys per block
 int smem_bytes_for(int D);   // dynamic shared memory per CTA

@@ -28,6 +28,20 @@ enum WaitSite : uint32_t {
     SITE_MAX_XCHG = 13,
     SITE_P_FREE = 14,
     SITE_S_FREE = 15,
+    // backward
+    SITE_B_KV_FULL = 20,
+    SITE_B_KV_EMPTY = 21,
+    SITE_B_QD_FULL = 22,
+    SITE_B_QD_EMPTY = 23,
+    SITE_B_S_FULL = 24,
+    SITE_B_DP_FULL = 25,
+    SITE_B_P_FULL = 26,
+    SITE_B_DS_FULL = 27,
+    SITE_B_DS_FREE = 28,
+    SITE_B_DQ_FULL = 29,
+    SITE_B_DQ_FREE = 30,
+    SITE_B_ACC_FULL = 31,
+    SITE_B_ACC_FREE = 32,
 };
 
 struct FwdParams {
@@ -56,6 +70,34 @@ struct FwdParams {
     const float* alibi;      // (Hq) slopes, or nullptr
     const int* cu_q;         // (Z + 1) offsets into the packed query rows, or nullptr
     const int* cu_k;         // (Z + 1) offsets into the packed key rows
+};
+
+// Backward kernel parameters (fa_bwd).  Tensor strides are in elements; the
+// workspace holds the fp32 dQ accumulator and, per query row padded to whole
+// 128-row blocks, the base-2 lse (+inf past Nq) and Delta = rowsum(dO * O).
+struct BwdParams {
+    const void* o;           // forward output, dtype
+    const float* lse;        // forward lse (Z, Hq, Nq), natural log
+    const void* dO;          // upstream gradient, dtype
+    void* dq;                // outputs, dtype
+    void* dk;
+    void* dv;
+    int64_t so_z, so_h, so_n;
+    int64_t sdo_z, sdo_h, sdo_n;
+    int64_t sdq_z, sdq_h, sdq_n;
+    int64_t sdk_z, sdk_h, sdk_n;
+    int64_t sdv_z, sdv_h, sdv_n;
+    int Z, Hq, Hkv, Nq, Nkv;
+    int group;               // Hq / Hkv
+    int Tq, Tk;              // query blocks of 128 rows, key blocks of 128 keys
+    int nunits;              // Z * Hkv * Tk: one unit = one key block of one kv head
+    float scale;             // softmax scale (dQ and dK carry it)
+    float scale_log2;        // scale * log2(e)
+    float* dq_acc;           // (Z, Hq, Nq, D) fp32
+    float* lse2;             // (Z, Hq, Tq * 128) fp32
+    float* delta;            // (Z, Hq, Tq * 128) fp32
+    uint32_t* status;
+    uint64_t wait_limit_ns;
 };
 
 }  // namespace fa

@@ -252,6 +252,47 @@ fa_status fa_lse_merge(int nparts, const void* const* o_parts, const float* cons
                        int D, const fa_strides* sp, void* o, float* lse, const fa_strides* so, fa_dtype dtype,
                        cudaStream_t stream);
 
+/*
+ * fa_bwd -- gradients of the attention forward (blog "把 FlashAttention 搬上昇腾：
+ * Triton-Ascend CV Pipeline 优化实战", section 二; "Write Triton Attention
+ * Kernel", step 8: the backward rebuilds the probabilities from the saved
+ * lse).  For a loss with upstream gradient dO = dLoss/dO:
+ *
+ *     P_ij  = exp(s_ij - lse_i)           s_ij = scale q_i . k_j (kept keys)
+ *     dV_j  = sum_i P_ij dO_i             dP_ij = dO_i . v_j
+ *     dS_ij = P_ij (dP_ij - Delta_i)      Delta_i = dO_i . O_i
+ *     dQ_i  = scale sum_j dS_ij k_j       dK_j = scale sum_i dS_ij q_i
+ *
+ * with dK, dV of a key/value head summed over the query heads of its GQA
+ * group, and the causal rule of fa_fwd.
+ *
+ *   q, k, v, o   the forward's inputs and output, layouts as for fa_fwd
+ *   lse          the forward's lse (Z, Hq, Nq) fp32 contiguous (required)
+ *   dO           (Z, Hq, Nq, D) dtype, strides *sdo
+ *   dq           (Z, Hq, Nq, D) dtype, strides *sdq     (written)
+ *   dk, dv       (Z, Hkv, Nkv, D) dtype, strides *sdk, *sdv (written)
+ *   workspace    device memory, 256-byte aligned, at least
+ *                fa_bwd_workspace_size(Z, Hq, Nq, D) bytes (fp32 dQ
+ *                accumulator and per-row Delta / lse); no initialisation
+ *                needed, overwritten; not shared by calls that may overlap
+ *
+ * Requirements: those of fa_fwd, with D in {16, 32, 64, 128} (D = 256 returns
+ * FA_ERR_UNSUPPORTED: dK and dV of a 128-key block live in tensor memory)
+ * and Nq >= 1 whenever Z*Hkv*Nkv > 0.  Three kernels on `stream`: Delta and
+ * lse per row, the gradients (dQ accumulated with fp32 atomic adds, so dQ
+ * may differ in the last bits between runs), and the dQ conversion.
+ * Errors: those of fa_fwd, plus FA_ERR_WORKSPACE for a missing, misaligned
+ * or small workspace.
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                 void* dq, void* dk, void* dv, int Z, int Hq, int Hkv, int Nq, int Nkv, int D, const fa_strides* sq,
+                 const fa_strides* sk, const fa_strides* sv, const fa_strides* so, const fa_strides* sdo,
+                 const fa_strides* sdq, const fa_strides* sdk, const fa_strides* sdv, float scale, int causal,
+                 fa_dtype dtype, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Bytes of workspace fa_bwd needs (host only; FA_ERR_UNSUPPORTED for D = 256). */
+fa_status fa_bwd_workspace_size(int Z, int Hq, int Nq, int D, size_t* bytes);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* fa_status_string(fa_status status);
 

@@ -1,0 +1,122 @@
+"""GPU parity of fa_bwd (dQ, dK, dV) against the fp64 oracle's backward.
+
+The GPU backward takes the GPU forward's O and lse (its own chain); the
+oracle takes only Q, K, V and dO and differentiates the definition.  The
+tolerance is relative to the largest reference gradient of each tensor:
+the kernel rounds P and dS to the input type before the tensor-core
+products (relative 2^-11 in fp16, 2^-8 in bf16 each), takes Delta from the
+rounded O, and accumulates in fp32.  Measured worst cases over these tests
+are 6e-4 (fp16) and 5.2e-3 (bf16) of the largest gradient; the bounds below
+keep about four times that.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import seeded_inputs as si
+from parity_util import relayout, to_device
+
+pytestmark = pytest.mark.gpu
+
+TOL_GRAD = {"fp16": 3e-3, "bf16": 2e-2}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import exact_attention_44_gb300 as fa
+    fa.build()
+    fa.load()
+
+
+def check_bwd(seed, Z, Hq, Hkv, Nq, Nkv, D, dtype, causal, scale=None, layout="bnsd"):
+    import torch
+    import exact_attention_44_gb300 as fa
+    scale = 1 / math.sqrt(D) if scale is None else scale
+    q, k, v = si.qkv(seed, Z, Hq, Hkv, Nq, Nkv, D, dtype)
+    do = si.normals(seed + 1000, 0, q.size, dtype).reshape(q.shape)
+    qt, kt, vt, dot = (relayout(to_device(x, dtype), layout) for x in (q, k, v, do))
+    o, lse = fa.fa_fwd(qt, kt, vt, scale=scale, causal=causal)
+    dq, dk, dv = fa.fa_bwd(qt, kt, vt, o, lse, dot, scale=scale, causal=causal)
+    torch.cuda.synchronize()
+    code, word = fa.fa_device_status()
+    assert code == 0, f"device status {word:#x}"
+    ref = oracle.attention_bwd(q, k, v, do, dtype, scale, causal)
+    worst = {}
+    for name, got, want in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        g = got.double().cpu().numpy()
+        assert np.all(np.isfinite(g)), f"{name}: non-finite"
+        err = float(np.max(np.abs(g - want)))
+        mag = float(np.max(np.abs(want)))
+        worst[name] = (err, mag)
+        assert err <= TOL_GRAD[dtype] * max(mag, 1e-3), f"{name}: max|d| = {err:.3e}, max|ref| = {mag:.3e}"
+    return worst
+
+
+@pytest.mark.parametrize("D", [16, 32, 64, 128])
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_head_dims(D, dtype, causal):
+    print(check_bwd(201, 1, 2, 2, 300, 300, D, dtype, causal))
+
+
+@pytest.mark.parametrize("Nq,Nkv", [(1, 1), (1, 200), (129, 129), (200, 77), (77, 200), (256, 640), (640, 256)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_ragged(Nq, Nkv, causal):
+    print(check_bwd(202, 2, 2, 1, Nq, Nkv, 64, "fp16", causal))
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 1), (8, 2), (8, 8)])
+def test_gqa(Hq, Hkv):
+    print(check_bwd(203, 1, Hq, Hkv, 260, 260, 128, "bf16", True))
+
+
+def test_layouts():
+    print(check_bwd(204, 2, 4, 2, 200, 300, 64, "bf16", False, layout="bsnd"))
+
+
+def test_large_scores():
+    print(check_bwd(205, 1, 2, 1, 256, 256, 64, "fp16", False, scale=1.0))
+
+
+def test_workspace_and_argument_errors():
+    import torch
+    import exact_attention_44_gb300 as fa
+    q = torch.zeros(1, 1, 64, 64, dtype=torch.float16, device="cuda")
+    lse = torch.zeros(1, 1, 64, device="cuda")
+    with pytest.raises(fa.FaError) as e:
+        fa.fa_bwd(q, q, q, q, lse, q, workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
+    assert e.value.code == fa.FA_ERR_WORKSPACE
+    q256 = torch.zeros(1, 1, 64, 256, dtype=torch.float16, device="cuda")
+    with pytest.raises(fa.FaError) as e:
+        fa.fa_bwd(q256, q256, q256, q256, lse, q256, workspace=torch.empty(1 << 20, dtype=torch.uint8, device="cuda"))
+    assert e.value.code == fa.FA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_full_size_every_element(causal):
+    # Z=4 H=16 N=1024 D=128 bf16: the forward's main workload, every gradient element
+    print(check_bwd(206, 4, 16, 16, 1024, 1024, 128, "bf16", causal))
+
+
+def test_long_gqa_causal_sampled_heads():
+    # GQA group of 4 at N=4096: the oracle differentiates one (z, kv head) group
+    import torch
+    import exact_attention_44_gb300 as fa
+    Z, Hq, Hkv, N, D, dtype = 1, 8, 2, 4096, 128, "bf16"
+    scale = 1 / math.sqrt(D)
+    q, k, v = si.qkv(207, Z, Hq, Hkv, N, N, D, dtype)
+    do = si.normals(1207, 0, q.size, dtype).reshape(q.shape)
+    qt, kt, vt, dot = (to_device(x, dtype) for x in (q, k, v, do))
+    o, lse = fa.fa_fwd(qt, kt, vt, causal=True)
+    dq, dk, dv = fa.fa_bwd(qt, kt, vt, o, lse, dot, causal=True)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status()[0] == 0
+    hk = 1
+    sl = slice(hk * 4, hk * 4 + 4)
+    ref = oracle.attention_bwd(q[:, sl], k[:, hk:hk + 1], v[:, hk:hk + 1], do[:, sl], dtype, scale, True)
+    for name, got, want in zip(("dq", "dk", "dv"), (dq[:, sl], dk[:, hk:hk + 1], dv[:, hk:hk + 1]), ref):
+        g = got.double().cpu().numpy()
+        err, mag = float(np.max(np.abs(g - want))), float(np.max(np.abs(want)))
+        assert err <= TOL_GRAD[dtype] * mag, f"{name}: {err:.3e} vs {mag:.3e}"
