@@ -186,7 +186,10 @@ def run_native(args, rank, world, device):
     Z, Hq, Hkv, Nq, Nkv, D, dtype, flags = wl
     scale = 1.0 / math.sqrt(D)
     tdt = torch.float16 if dtype == "fp16" else torch.bfloat16
-    stream = torch.cuda.current_stream(device)
+    # a stream of its own (CUDA graphs are not captured on the default stream),
+    # made current so that every copy and launch below is ordered on it
+    stream = torch.cuda.Stream(device)
+    torch.cuda.set_stream(stream)
 
     # rotating input sets: their total is > 3x L2, so a step never reuses the previous step's operands in L2
     per_set = sum(io_bytes(wl))
@@ -196,34 +199,62 @@ def run_native(args, rank, world, device):
     outs = [[(torch.empty((Z, Hq, Nq, D), dtype=tdt, device=device),
               torch.empty((Z, Hq, Nq), dtype=torch.float32, device=device)) for _ in flags] for _ in range(nsets)]
 
-    def step(i, evs=None):
+    def launch(i, f):
         q, k, v = sets[i % nsets]
-        for f, causal in enumerate(flags):
-            if evs is not None:
-                evs[f].record(stream)
-            o, lse = outs[i % nsets][f]
-            fa.fa_fwd(q, k, v, o=o, lse=lse, scale=scale, causal=causal, stream=stream)
-        if evs is not None:
-            evs[len(flags)].record(stream)
+        o, lse = outs[i % nsets][f]
+        fa.fa_fwd(q, k, v, o=o, lse=lse, scale=scale, causal=flags[f], stream=stream)
 
     for i in range(args.warmup):
-        step(i)
+        for f in range(len(flags)):
+            launch(i, f)
     torch.cuda.synchronize(device)
     code, word = fa.fa_device_status(stream)
     if code != fa.FA_OK:
         raise RuntimeError(f"device status after warm-up: {word:#x}")
+    # The timed loop replays CUDA graphs: per causal flag, one graph holding that
+    # flag's launch on each of the nsets input sets in turn (nsets steps' worth
+    # of that flag's work).  A replay of every flag's graph is nsets whole steps.
+    graphs = []
+    if not args.eager:
+        with torch.cuda.stream(stream):
+            for f in range(len(flags)):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for i in range(nsets):
+                        launch(i, f)
+                graphs.append(g)
+        for g in graphs:
+            g.replay()
+        torch.cuda.synchronize(device)
+    # exactly K steps: K // nsets replays of every flag's graph, then the
+    # remaining K % nsets steps as eager launches, all inside the timed region
+    reps = args.steps // nsets if graphs else 0
+    tail = args.steps - reps * nsets
     barrier(world)
     clocks = ClockSampler(device.index if device.index is not None else 0) if rank == 0 else None
     time.sleep(0.25 if clocks else 0)
     torch.cuda.synchronize(device)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(flags) + 1)] for _ in range(args.steps)]
-    for i in range(args.steps):
-        step(i, ev[i])
+    nrec = reps + tail
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(flags) + 1)] for _ in range(nrec)]
+    for r in range(reps):
+        for f in range(len(flags)):
+            ev[r][f].record(stream)
+            graphs[f].replay()
+        ev[r][len(flags)].record(stream)
+    for x in range(tail):
+        e = ev[reps + x]
+        for f in range(len(flags)):
+            e[f].record(stream)
+            launch(reps * nsets + x, f)
+        e[len(flags)].record(stream)
     torch.cuda.synchronize(device)
     clock = clocks.stop() if clocks else None
     barrier(world)
     total_ms = ev[0][0].elapsed_time(ev[-1][-1])
-    per_kernel_ms = [[e[f].elapsed_time(e[f + 1]) for e in ev] for f in range(len(flags))]
+    # per-launch durations: a graph replay holds nsets launches of its flag
+    per_kernel_ms = [[ev[r][f].elapsed_time(ev[r][f + 1]) / nsets for r in range(reps) for _ in range(nsets)] +
+                     [ev[reps + x][f].elapsed_time(ev[reps + x][f + 1]) for x in range(tail)]
+                     for f in range(len(flags))]
     code, word = fa.fa_device_status(stream)
     if code != fa.FA_OK:
         raise RuntimeError(f"device status after timing: {word:#x}")
@@ -254,6 +285,8 @@ def run_native(args, rank, world, device):
         "config": {"workload": args.workload, "Z": Z, "Hq": Hq, "Hkv": Hkv, "Nq": Nq, "Nkv": Nkv, "D": D,
                    "causal_per_step": flags, "scale": scale, "layout": "BNSD contiguous",
                    "l2": f"{nsets} rotating input sets ({nsets * per_set / 2**20:.0f} MiB > 3x L2)",
+                   "launch": ("eager fa_fwd calls" if not graphs else
+                              f"CUDA graph per causal flag, {nsets} fa_fwd launches (one per input set) per replay"),
                    "parallelism": "replicas only" if world > 1 else "single GPU"},
         "frac_of_peak": round(value / world / peaks["bf16_tflops"], 4),
         "per_launch_ms": {f"causal={c}": round(statistics.fmean(per_kernel_ms[f]), 5) for f, c in enumerate(flags)},
@@ -267,6 +300,8 @@ def run_native(args, rank, world, device):
         result["target_shapes"] = [measure_shape(name, device, stream, peaks) for name in TARGET_SHAPES]
         result["split_kv_shapes"] = [measure_shape(name, device, stream, peaks, impl=impl)
                                      for name in SPLIT_SHAPES for impl in ("fwd", "splitkv")]
+        result["variant_shapes"] = [measure_variant(name, device, stream, peaks) for name in VARIANT_SHAPES]
+        result["bwd_shapes"] = [r for name in BWD_SHAPES for r in measure_bwd(name, device, stream, peaks)]
     return result
 
 
@@ -356,6 +391,130 @@ def measure_shape(name, device, stream, peaks, steps=10, impl="fwd"):
     torch.cuda.empty_cache()
     return {"workload": name, "impl": impl, "tflops": round(tf, 2), "frac_of_peak": round(tf / peaks["bf16_tflops"], 4),
             "ms_per_step": round(ms, 4), "steps": steps}
+
+
+# fa_fwd_ex workloads: name -> (Z, Hq, Hkv, N, D, dtype, causal, window, alibi, varlen lengths or None)
+VARIANT_SHAPES = {
+    "z4_h16_n4096_d128_bf16_causal_window512": (4, 16, 16, 4096, 128, "bf16", True, (512, 0), False, None),
+    "z4_h16_n2048_d128_bf16_causal_alibi": (4, 16, 16, 2048, 128, "bf16", True, (-1, -1), True, None),
+    "varlen_16seq_256to4096_h16_d128_bf16_causal": (16, 16, 16, 0, 128, "bf16", True, (-1, -1), False, "seeded"),
+}
+
+
+def variant_lengths(Z, seed=0):
+    """Seeded sequence lengths, uniform on [256, 4096]."""
+    import numpy as np
+    return np.random.default_rng(seed).integers(256, 4097, size=Z)
+
+
+def variant_flops(Z, Hq, N, D, causal, window, lens):
+    """4 D per kept (query, key) pair; causal without a window counts half of N^2, as the metric does."""
+    if lens is not None:
+        return sum(4.0 * Hq * L * L * D / (2 if causal else 1) for L in lens)
+    wl, wr = window
+    if wl < 0 and wr < 0:
+        return flops_of(Z, Hq, N, N, D, causal)
+    pairs = 0
+    for i in range(N):
+        lo = 0 if wl < 0 else max(0, i - wl)
+        hi = N - 1 if wr < 0 else min(N - 1, i + wr)
+        if causal:
+            hi = min(hi, i)
+        pairs += max(0, hi - lo + 1)
+    return 4.0 * Z * Hq * pairs * D
+
+
+def measure_variant(name, device, stream, peaks, steps=10):
+    """TFLOP/s of fa_fwd_ex on a window / ALiBi / variable-length workload (kept pairs only)."""
+    import numpy as np
+    import torch
+
+    import exact_attention_44_gb300 as fa
+    import seeded_inputs as si
+    Z, Hq, Hkv, N, D, dtype, causal, window, alibi, varlen = VARIANT_SHAPES[name]
+    tdt = torch.float16 if dtype == "fp16" else torch.bfloat16
+    lens = variant_lengths(Z) if varlen else None
+    kw = {}
+    if lens is not None:
+        cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+        total = int(cu[-1])
+        shape_q, shape_k = (1, Hq, total, D), (1, Hkv, total, D)
+        cu_t = torch.from_numpy(cu).to(device)
+        kw.update(cu_seqlens_q=cu_t, cu_seqlens_k=cu_t, max_seqlen_q=int(lens.max()))
+    else:
+        shape_q, shape_k = (Z, Hq, N, D), (Z, Hkv, N, D)
+    nq, nk = int(np.prod(shape_q)), int(np.prod(shape_k))
+    q = si.as_torch(si.normals(0, 0, nq, dtype).reshape(shape_q), dtype).to(device)
+    k = si.as_torch(si.normals(0, nq, nk, dtype).reshape(shape_k), dtype).to(device)
+    v = si.as_torch(si.normals(0, nq + nk, nk, dtype).reshape(shape_k), dtype).to(device)
+    if alibi:
+        kw["alibi_slopes"] = torch.tensor([2.0 ** (-8.0 * (h + 1) / Hq) for h in range(Hq)], dtype=torch.float32,
+                                          device=device)
+    o = torch.empty_like(q)
+
+    def call():
+        fa.fa_fwd_ex(q, k, v, o=o, causal=causal, window=window, stream=stream, **kw)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize(device)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        call()
+    b.record(stream)
+    torch.cuda.synchronize(device)
+    ms = a.elapsed_time(b) / steps
+    code, word = fa.fa_device_status(stream)
+    if code != fa.FA_OK:
+        raise RuntimeError(f"device status after {name}: {word:#x}")
+    tf = variant_flops(Z, Hq, N, D, causal, window, lens) / (ms * 1e-3) / 1e12
+    return {"workload": name, "impl": "fwd_ex", "tflops": round(tf, 2), "frac_of_peak": round(tf / peaks["bf16_tflops"], 4),
+            "ms_per_step": round(ms, 4), "steps": steps, "flops": "kept (query, key) pairs x 4 D"}
+
+
+# fa_bwd workloads (gradients of the forward; 5 products of 2 N^2 D per head, half for causal)
+BWD_SHAPES = ["z4_h16_n1024_d128_bf16", "z1_hq32_hkv8_n8192_d128_bf16_noncausal", "z8_h16_n2048_d64_fp16"]
+
+
+def measure_bwd(name, device, stream, peaks, steps=10):
+    """TFLOP/s of fa_bwd (all three of its kernels) per causal flag of a workload."""
+    import torch
+
+    import exact_attention_44_gb300 as fa
+    Z, Hq, Hkv, Nq, Nkv, D, dtype, flags = WORKLOADS[name]
+    _, dev0 = make_inputs(WORKLOADS[name], 0, device)
+    q, k, v = dev0
+    do = torch.randn_like(q)
+    ws = torch.empty(fa.fa_bwd_workspace_size(Z, Hq, Nq, D), dtype=torch.uint8, device=device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    out = []
+    for causal in flags:
+        o, lse = fa.fa_fwd(q, k, v, causal=causal, stream=stream)
+
+        def call():
+            fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, causal=causal, workspace=ws, stream=stream)
+
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize(device)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            call()
+        b.record(stream)
+        torch.cuda.synchronize(device)
+        ms = a.elapsed_time(b) / steps
+        code, word = fa.fa_device_status(stream)
+        if code != fa.FA_OK:
+            raise RuntimeError(f"device status after the backward of {name}: {word:#x}")
+        tf = 2.5 * flops_of(Z, Hq, Nq, Nkv, D, causal) / (ms * 1e-3) / 1e12
+        out.append({"workload": name, "causal": causal, "impl": "bwd", "tflops": round(tf, 2),
+                    "frac_of_peak": round(tf / peaks["bf16_tflops"], 4), "ms_per_step": round(ms, 4), "steps": steps,
+                    "flops": "10 N^2 D per head (5 products), half for causal"})
+    del dev0, q, k, v, do, ws, dq, dk, dv
+    torch.cuda.empty_cache()
+    return out
 
 
 # ------------------------------------------------------------------ oracle --
@@ -476,12 +635,15 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=MAIN)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="time eager fa_fwd calls instead of CUDA-graph replays")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--shapes", dest="shapes", action="store_true", default=True,
                     help="also time the D=128, N>=4096 non-causal target shapes (default)")
     ap.add_argument("--no-shapes", dest="shapes", action="store_false")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for cpu_baseline (and the cap per step of --impl reference)")
+    ap.add_argument("--bwd-only", action="store_true",
+                    help="time only fa_bwd on --workload (one JSON line per causal flag; for profiling)")
     ap.add_argument("--all", action="store_true",
                     help="instead of the bench line, time every workload (one JSON line each) for the results table")
     args = ap.parse_args(argv)
@@ -502,6 +664,13 @@ def main(argv=None):
         raise SystemExit("bench.py: no CUDA device (the native path has no CPU fallback)")
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
+    if args.bwd_only:
+        import exact_attention_44_gb300 as fa
+        fa.build()
+        fa.load()
+        for r in measure_bwd(args.workload, device, torch.cuda.current_stream(device), load_peaks(), steps=args.steps):
+            print(json.dumps(r), flush=True)
+        return 0
     if args.all:
         import exact_attention_44_gb300 as fa
         fa.build()

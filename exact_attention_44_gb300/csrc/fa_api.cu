@@ -531,8 +531,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     a.tmQ = &mq;
     a.tmDO = &mdo;
     a.grid = (int)std::min<int64_t>(units, info->sms);
-    const int64_t pre_rows = (int64_t)Z * Hq * p.Tq * 128;
-    a.pre_grid = (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(pre_rows, 256), (int64_t)info->sms * 8));
+    const int64_t pre_threads = (int64_t)Z * Hq * p.Tq * 128 * (D / 8);
+    a.pre_grid = (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(pre_threads, 256), (int64_t)info->sms * 16));
     const int64_t post_items = (int64_t)Z * Hq * Nq * (D / 8);
     a.post_grid = (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(post_items, 256), (int64_t)info->sms * 8));
     a.stream = stream;

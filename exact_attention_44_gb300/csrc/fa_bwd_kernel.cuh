@@ -198,26 +198,35 @@ __device__ void bwd_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0, ui
     auto kmaj = [&](int kk, int swe, int sw) -> uint32_t {
         return (uint32_t)((((kk * 16) / swe) * (128 * sw) + ((kk * 16) % swe) * 2) >> 4);
     };
+    // Sᵀ of step t into TMEM; its operands are stage t & 1
+    auto issue_s = [&](uint32_t t) -> bool {
+        const uint32_t st = t & 1u;
+        if (!wait_phase(bar(T::B_QD_FULL + st), (t >> 1) & 1u, ctl, SITE_B_QD_FULL)) return false;
+        ptx::tc_fence_after();
+        const uint32_t q_lo = ptx::smem_desc_lo(sbase + T::OFF_Q + st * T::TILE, 16);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+            ptx::mma_ss(tmem + T::TM_S, ptx::desc64(k_lo + kmaj(kk, T::SWE, T::SW), HI),
+                        ptx::desc64(q_lo + kmaj(kk, T::SWE, T::SW), HI), ID_SQ, kk > 0 ? 1u : 0u);
+        ptx::tc_commit(bar(T::B_S_FULL));
+        return true;
+    };
+    // Order per step t: dPᵀ_t, dV_t, then Sᵀ_{t+1} (its columns were last read
+    // by dV_t, issued before it; the softmax warps keep Pᵀ_t in registers), then
+    // dK_t and dQ_t -- so the softmax warps build Pᵀ_{t+1} while the tensor core
+    // runs dK_t and dQ_t.
     uint32_t uc = 0, t = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < p.nunits; u += gridDim.x) {
         const BwdUnit w = bwd_unit<CAUSAL>(u, p);
         if (w.nsteps == 0) continue;
         if (!wait_phase(bar(T::B_KV_FULL), uc & 1u, ctl, SITE_B_KV_FULL)) { ok = false; break; }
+        if (!issue_s(t)) { ok = false; break; }
         for (int s = 0; s < w.nsteps; ++s, ++t) {
             const uint32_t st = t & 1u;
-            if (!wait_phase(bar(T::B_QD_FULL + st), (t >> 1) & 1u, ctl, SITE_B_QD_FULL)) { ok = false; break; }
-            ptx::tc_fence_after();
-            const uint32_t q_lo = ptx::smem_desc_lo(sbase + T::OFF_Q + st * T::TILE, 16);
             const uint32_t qmn_lo = ptx::smem_desc_lo(sbase + T::OFF_Q + st * T::TILE, 128 * T::SW);
             const uint32_t do_lo = ptx::smem_desc_lo(sbase + T::OFF_DO + st * T::TILE, 16);
             const uint32_t domn_lo = ptx::smem_desc_lo(sbase + T::OFF_DO + st * T::TILE, 128 * T::SW);
-            // Sᵀ = K Qᵢᵀ
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-                ptx::mma_ss(tmem + T::TM_S, ptx::desc64(k_lo + kmaj(kk, T::SWE, T::SW), HI),
-                            ptx::desc64(q_lo + kmaj(kk, T::SWE, T::SW), HI), ID_SQ, kk > 0 ? 1u : 0u);
-            ptx::tc_commit(bar(T::B_S_FULL));
             // dPᵀ = V dOᵢᵀ, once the previous dQ partial (same columns) is read out
             if (t > 0 && !wait_phase(bar(T::B_DQ_FREE), (t - 1) & 1u, ctl, SITE_B_DQ_FREE)) { ok = false; break; }
             ptx::tc_fence_after();
@@ -238,6 +247,7 @@ __device__ void bwd_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0, ui
             for (int kk = 0; kk < 128 / 16; ++kk)
                 ptx::mma_ts(tmem + T::TM_DV, tmem + T::TM_S + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
                             ptx::desc64(domn_lo + ((kk * 16 * T::SW) >> 4), HI), ID_ND, (s > 0 || kk > 0) ? 1u : 0u);
+            if (s + 1 < w.nsteps && !issue_s(t + 1)) { ok = false; break; }
             // dK += dSᵀ Qᵢ and dQᵢ = dS K, once dSᵀ is in shared memory
             if (!wait_phase(bar(T::B_DS_FULL), t & 1u, ctl, SITE_B_DS_FULL)) { ok = false; break; }
             ptx::tc_fence_after();
@@ -493,43 +503,38 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 // columns get P = 0), and a zeroed row of the dQ accumulator.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
+    constexpr int TPR = D / 8;  // threads per row, 16 bytes of O and of dO each
     const int64_t rows = (int64_t)p.Z * p.Hq * p.Tq * 128;
-    for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < rows; r += (int64_t)gridDim.x * blockDim.x) {
+    const int sub = threadIdx.x % TPR;
+    for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / TPR; r < rows;
+         r += (int64_t)gridDim.x * blockDim.x / TPR) {
         const int64_t head = r / ((int64_t)p.Tq * 128);
         const int i = (int)(r - head * p.Tq * 128);
         const int z = (int)(head / p.Hq), hq = (int)(head % p.Hq);
-        float delta = 0.f, l2 = INFINITY;
+        float delta = 0.f;
         if (i < p.Nq) {
-            const uint4* orow = reinterpret_cast<const uint4*>(
-                static_cast<const uint16_t*>(p.o) + (int64_t)z * p.so_z + (int64_t)hq * p.so_h + (int64_t)i * p.so_n);
-            const uint4* grow = reinterpret_cast<const uint4*>(
-                static_cast<const uint16_t*>(p.dO) + (int64_t)z * p.sdo_z + (int64_t)hq * p.sdo_h +
-                (int64_t)i * p.sdo_n);
+            const uint4 a = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.o) + (int64_t)z * p.so_z +
+                                                           (int64_t)hq * p.so_h + (int64_t)i * p.so_n)[sub];
+            const uint4 b = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.dO) + (int64_t)z * p.sdo_z +
+                                                           (int64_t)hq * p.sdo_h + (int64_t)i * p.sdo_n)[sub];
+            const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-            for (int x = 0; x < D / 8; ++x) {
-                const uint4 a = orow[x], b = grow[x];
-                const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-                for (int y = 0; y < 4; ++y) {
-                    float2 fa, fb;
-                    if constexpr (BF16) {
-                        fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&aw[y]));
-                        fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bw[y]));
-                    } else {
-                        fa = __half22float2(*reinterpret_cast<const __half2*>(&aw[y]));
-                        fb = __half22float2(*reinterpret_cast<const __half2*>(&bw[y]));
-                    }
-                    delta = fmaf(fa.x, fb.x, delta);
-                    delta = fmaf(fa.y, fb.y, delta);
-                }
+            for (int y = 0; y < 4; ++y) {
+                const float2 fa = unpack2<BF16>(aw[y]), fb = unpack2<BF16>(bw[y]);
+                delta = fmaf(fa.x, fb.x, delta);
+                delta = fmaf(fa.y, fb.y, delta);
             }
-            l2 = p.lse[head * p.Nq + i] * 1.4426950408889634f;
-            float4* acc = reinterpret_cast<float4*>(p.dq_acc + (head * p.Nq + i) * D);
-#pragma unroll
-            for (int x = 0; x < D / 4; ++x) acc[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+            float4* acc = reinterpret_cast<float4*>(p.dq_acc + (head * p.Nq + i) * D) + 2 * sub;
+            acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+            acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        p.delta[r] = delta;
-        p.lse2[r] = l2;
+        // the row's TPR lanes are consecutive lanes of one warp
+#pragma unroll
+        for (int m = TPR / 2; m > 0; m /= 2) delta += __shfl_xor_sync(0xffffffffu, delta, m);
+        if (sub == 0) {
+            p.delta[r] = delta;
+            p.lse2[r] = i < p.Nq ? p.lse[head * p.Nq + i] * 1.4426950408889634f : INFINITY;
+        }
     }
 }
 
