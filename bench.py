@@ -91,16 +91,20 @@ def load_peaks():
     return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
 
 
-def kernel_source_hash() -> str:
+# the sources the forward kernel of head dim D is compiled from
+FWD_SOURCES = ["fa_fwd_kernel.cuh", "fa_ptx.cuh", "fa_params.h", "fa_launch.h", "fa_fwd_d{D}.cu"]
+
+
+def kernel_source_hash(D: int = 128) -> str:
+    """Hash of the forward kernel's own sources (a change anywhere else leaves its counters valid)."""
     h = hashlib.sha256()
-    for d in (os.path.join(ROOT, "exact_attention_44_gb300", "csrc"), os.path.join(ROOT, "include")):
-        for name in sorted(os.listdir(d)):
-            if name.endswith((".cu", ".cuh", ".h")):
-                h.update(name.encode() + b"\0" + open(os.path.join(d, name), "rb").read())
+    for name in FWD_SOURCES:
+        name = name.format(D=D)
+        h.update(name.encode() + b"\0" + open(os.path.join(ROOT, "exact_attention_44_gb300", "csrc", name), "rb").read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str):
+def recorded_traffic(kernel: str, D: int = 128):
     """DRAM bytes per launch from the committed ncu summary, if taken on the current kernel source."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
@@ -109,7 +113,7 @@ def recorded_traffic(kernel: str):
         rec = json.load(open(p)).get(kernel)
     except Exception:
         return None
-    if not rec or rec.get("source_hash") != kernel_source_hash():
+    if not rec or rec.get("source_hash") != kernel_source_hash(D):
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -275,7 +279,7 @@ def run_native(args, rank, world, device):
                 "peak_source": f"{peaks['source']} bf16 burst (cuBLAS)",
                 "frac_of_sustained": (round(achieved / peaks["bf16_tflops_sustained"], 4)
                                       if peaks.get("bf16_tflops_sustained") else None),
-                "traffic": recorded_traffic(kname),
+                "traffic": recorded_traffic(kname, D),
                 "algorithmic_bytes": algorithmic_bytes(wl), "ms_per_launch": round(dom_ms, 5)}
 
     result = {

@@ -162,11 +162,11 @@ namespace {
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
-// Backward workspace: the fp32 dQ accumulator, then lse2 and Δ per query
-// row padded to whole 128-row blocks.
+// Backward workspace: lse2 and Δ per query row padded to whole 128-row blocks.
 size_t bwd_workspace_bytes(int Z, int Hq, int Nq, int D) {
+    (void)D;
     const size_t tq = (size_t)cdiv(Nq, 128);
-    return align256((size_t)Z * Hq * Nq * D * 4) + 2 * align256((size_t)Z * Hq * tq * 128 * 4);
+    return 2 * align256((size_t)Z * Hq * tq * 128 * 4);
 }
 
 // Floats per partial-result slot of the split schedule: O / l of BM rows
@@ -505,17 +505,16 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     p.group = Hq / Hkv;
     p.Tq = (int)cdiv(Nq, 128);
     p.Tk = (int)cdiv(Nkv, 128);
-    const int64_t units = (int64_t)Z * Hkv * p.Tk;
-    if (units > INT32_MAX) return FA_ERR_UNSUPPORTED;
+    const int64_t units = (int64_t)Z * Hkv * p.Tk, units_q = (int64_t)Z * Hq * p.Tq;
+    if (units > INT32_MAX || units_q > INT32_MAX) return FA_ERR_UNSUPPORTED;
     p.nunits = (int)units;
+    p.nunits_q = (int)units_q;
     p.scale = scale;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    const size_t acc_bytes = align256((size_t)Z * Hq * Nq * D * 4);
     const size_t row_bytes = align256((size_t)Z * Hq * p.Tq * 128 * 4);
-    p.dq_acc = reinterpret_cast<float*>(ws);
-    p.lse2 = reinterpret_cast<float*>(ws + acc_bytes);
-    p.delta = reinterpret_cast<float*>(ws + acc_bytes + row_bytes);
+    p.lse2 = reinterpret_cast<float*>(ws);
+    p.delta = reinterpret_cast<float*>(ws + row_bytes);
     p.status = info->status;
     p.wait_limit_ns = wait_limit_ns();
 
@@ -531,10 +530,9 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     a.tmQ = &mq;
     a.tmDO = &mdo;
     a.grid = (int)std::min<int64_t>(units, info->sms);
+    a.grid_q = (int)std::min<int64_t>(units_q, info->sms);
     const int64_t pre_threads = (int64_t)Z * Hq * p.Tq * 128 * (D / 8);
     a.pre_grid = (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(pre_threads, 256), (int64_t)info->sms * 16));
-    const int64_t post_items = (int64_t)Z * Hq * Nq * (D / 8);
-    a.post_grid = (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(post_items, 256), (int64_t)info->sms * 8));
     a.stream = stream;
     const bool bf16 = dtype == FA_DTYPE_BF16;
     cudaError_t err;

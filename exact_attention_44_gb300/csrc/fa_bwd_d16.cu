@@ -7,11 +7,8 @@
 
 namespace fa {
 
-template <bool CAUSAL, bool BF16>
-static cudaError_t launch_one(const BwdLaunchArgs& a) {
-    auto kernel = fa_bwd_kernel<16, CAUSAL, BF16>;
-    constexpr int smem = BwdTraits<16>::SMEM_BYTES;
-    static std::atomic<uint64_t> configured{0};
+template <typename K>
+static cudaError_t set_smem_once(K kernel, int smem, std::atomic<uint64_t>& configured) {
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
@@ -21,12 +18,24 @@ static cudaError_t launch_one(const BwdLaunchArgs& a) {
         if (err != cudaSuccess) return err;
         configured.fetch_or(bit);
     }
-    // Δ and lse2 per query row, zeroed dQ accumulator; then the gradients; then dQ
+    return cudaSuccess;
+}
+
+template <bool CAUSAL, bool BF16>
+static cudaError_t launch_one(const BwdLaunchArgs& a) {
+    using T = BwdTraits<16>;
+    auto kv = fa_bwd_kv_kernel<16, CAUSAL, BF16>;
+    auto dq = fa_bwd_dq_kernel<16, CAUSAL, BF16>;
+    static std::atomic<uint64_t> kv_configured{0}, dq_configured{0};
+    cudaError_t err;
+    if ((err = set_smem_once(kv, T::KV_SMEM_BYTES, kv_configured)) != cudaSuccess) return err;
+    if ((err = set_smem_once(dq, T::Q_SMEM_BYTES, dq_configured)) != cudaSuccess) return err;
+    // Δ and lse2 per query row; then dK, dV; then dQ
     fa_bwd_pre_kernel<16, BF16><<<a.pre_grid, 256, 0, a.stream>>>(a.params);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    kernel<<<a.grid, BWD_THREADS, smem, a.stream>>>(*a.tmK, *a.tmV, *a.tmQ, *a.tmDO, a.params);
+    kv<<<a.grid, BWD_THREADS, T::KV_SMEM_BYTES, a.stream>>>(*a.tmK, *a.tmV, *a.tmQ, *a.tmDO, a.params);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    fa_bwd_dq_kernel<16, BF16><<<a.post_grid, 256, 0, a.stream>>>(a.params);
+    dq<<<a.grid_q, BWD_THREADS, T::Q_SMEM_BYTES, a.stream>>>(*a.tmK, *a.tmV, *a.tmQ, *a.tmDO, a.params);
     return cudaGetLastError();
 }
 

@@ -5,27 +5,29 @@
 // Triton Attention Kernel", step 8 and Correctness requirements: the backward
 // needs lse = m + log l).
 //
-// One unit of work is one block of 128 keys of one key/value head; a
-// persistent CTA walks units, and for each loops over every query block of
-// every query head of the GQA group (from the diagonal block on, when
-// causal).  Per step (query block i of head hq), with keys as TMEM lanes:
-//     Sᵀ  = K Qᵢᵀ                       (tcgen05, both from shared memory)
-//     Pᵀ  = 2^(Sᵀ·scale·log2e − lse2ᵢ)   (softmax warps; -> TMEM as fp16/bf16)
-//     dPᵀ = V dOᵢᵀ
-//     dV += Pᵀ dOᵢ                       (A = Pᵀ from TMEM)
-//     dSᵀ = Pᵀ ∘ (dPᵀ − Δᵢ)               (softmax warps; -> shared memory)
-//     dK += dSᵀ Qᵢ                       (A = dSᵀ, K-major)
-//     dQᵢ = dS K                         (A = dSᵀ read MN-major; -> fp32 adds
-//                                         into the dQ accumulator in global)
-// dK and dV stay in TMEM for the whole unit and are written once (dK times
-// scale); dQ = scale · accumulator is converted by a last kernel.  Δ =
-// rowsum(dO ∘ O) and the base-2 lse come from a first kernel.
+// Three kernels on one stream:
+//   fa_bwd_pre_kernel  per query row: Δ = rowsum(dO ∘ O) and the base-2 lse;
+//   fa_bwd_kv_kernel   one unit per (128-key block, kv head): loops over every
+//                      query block of every query head of the GQA group (from
+//                      the diagonal on when causal), keys as TMEM lanes:
+//                          Sᵀ  = K Qᵢᵀ,  Pᵀ = 2^(Sᵀ·scale·log2e − lse2ᵢ)
+//                          dPᵀ = V dOᵢᵀ, dSᵀ = Pᵀ ∘ (dPᵀ − Δᵢ)
+//                          dV += Pᵀ dOᵢ,  dK += dSᵀ Qᵢ   (Pᵀ, dSᵀ from TMEM)
+//                      dK (times scale) and dV stay in TMEM and are stored once;
+//   fa_bwd_dq_kernel   one unit per (128-row query block, query head): loops
+//                      over the key blocks it sees, queries as TMEM lanes:
+//                          S = Qᵢ Kⱼᵀ, dP = dOᵢ Vⱼᵀ, dS = P ∘ (dP − Δ),
+//                          dQ += dS Kⱼ   (dS from TMEM)
+//                      dQ (times scale) stays in TMEM and is stored once.
+// dQ is summed over key blocks inside one CTA, so no atomics are needed and
+// the result is bitwise reproducible; the price is recomputing S and dP in
+// the dQ kernel (7 tensor-core products per block pair instead of 5).
 //
-// Warps: 0-3 and 4-7 the two column halves of each 128x128 block (thread =
-// key = TMEM lane), 8-11 the epilogue (dQ adds, dK and dV stores; thread =
-// TMEM lane), 12 the TMA producer, 13 the MMA issuer.  Every wait is bounded
-// as in the forward kernel.  Head dims 16 to 128 (TMEM holds Sᵀ/Pᵀ, dPᵀ/dQ,
-// dV and dK: 256 + 2D columns).
+// Warps (both gradient kernels): 0-3 and 4-7 the two column halves of each
+// 128x128 block (thread = TMEM lane), 8-11 the epilogue, 12 the TMA producer,
+// 13 the MMA issuer.  Every wait is bounded as in the forward kernel.  Head
+// dims 16 to 128 (the kv kernel's TMEM holds Sᵀ/Pᵀ, dPᵀ/dSᵀ, dV and dK:
+// 256 + 2D columns).
 #pragma once
 
 #include "fa_fwd_kernel.cuh"
@@ -45,60 +47,97 @@ template <int D_>
 struct BwdTraits {
     static constexpr int D = D_;
     static_assert(D <= 128, "the backward keeps dK and dV in TMEM: D <= 128");
-    static constexpr int BN = 128;                            // keys per unit
     static constexpr int SW = D * 2 >= 128 ? 128 : D * 2;      // bytes per swizzled row chunk of Q, K, V, dO
     static constexpr int SWE = SW / 2;
     static constexpr int NCHUNK = D / SWE;
     static constexpr uint32_t SWIZZLE_CODE = SW == 128 ? 2u : SW == 64 ? 4u : 6u;
     static constexpr int TILE = 128 * D * 2;                  // one 128-row tile of Q, K, V or dO
-    static constexpr int DS_BYTES = 128 * 128 * 2;            // dSᵀ: 128 keys x 128 queries, 128-B swizzle
-    // shared memory
-    static constexpr int OFF_K = 0;
-    static constexpr int OFF_V = OFF_K + TILE;
-    static constexpr int OFF_Q = OFF_V + TILE;                // [2]
-    static constexpr int OFF_DO = OFF_Q + 2 * TILE;           // [2]
-    static constexpr int OFF_DS = OFF_DO + 2 * TILE;
-    static constexpr int OFF_LSE = OFF_DS + DS_BYTES;         // [2] x 128 floats
-    static constexpr int OFF_DELTA = OFF_LSE + 2 * 512;       // [2] x 128 floats
-    static constexpr int OFF_BAR = OFF_DELTA + 2 * 512;
-    // barriers
-    static constexpr int B_KV_FULL = 0;       // K, V of a unit landed (TMA)
-    static constexpr int B_KV_EMPTY = 1;      // the unit's MMAs are done (commit)
-    static constexpr int B_QD_FULL = 2;       // [2] Q, dO, lse2, Δ of a step landed (TMA)
-    static constexpr int B_QD_EMPTY = 4;      // [2] that step's MMAs are done (commit)
-    static constexpr int B_S_FULL = 6;        // Sᵀ in TMEM (commit)
-    static constexpr int B_DP_FULL = 7;       // dPᵀ in TMEM (commit)
-    static constexpr int B_P_FULL = 8;        // Pᵀ written to TMEM (256)
-    static constexpr int B_DS_FULL = 9;       // dSᵀ written to shared memory (256)
-    static constexpr int B_DQ_FULL = 10;      // dQ partial in TMEM; dSᵀ buffer free (commit)
-    static constexpr int B_DQ_FREE = 11;      // dQ partial read out of TMEM (128)
-    static constexpr int B_ACC_FULL = 12;     // dK, dV of a unit complete (commit)
-    static constexpr int B_ACC_FREE = 13;     // dK, dV read out of TMEM (128)
-    static constexpr int B_DRAIN = 14;        // issuer teardown
-    static constexpr int NUM_BARS = 15;
-    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-    static constexpr int SMEM_USED = OFF_MISC + 16;
-    // + slack to align the base to 1024 bytes where it fits (D = 128 fills
-    // the 227 KB; there the base must already be aligned, which the kernel checks)
-    static constexpr int SMEM_BYTES = SMEM_USED + 1024 <= 227 * 1024 ? SMEM_USED + 1024 : SMEM_USED;
-    static_assert(SMEM_USED <= 227 * 1024, "shared memory budget");
-    // TMEM columns
-    static constexpr uint32_t TM_S = 0;                       // Sᵀ (fp32); Pᵀ over columns 0-31 and 64-95
-    static constexpr uint32_t TM_DP = 128;                    // dPᵀ (fp32), then the dQ partial (D columns)
+
+    // ---- dK / dV kernel ----
+    // shared memory: K, V of the unit; Q, dO, lse2, Δ of two steps
+    static constexpr int KV_OFF_K = 0;
+    static constexpr int KV_OFF_V = KV_OFF_K + TILE;
+    static constexpr int KV_OFF_Q = KV_OFF_V + TILE;          // [2]
+    static constexpr int KV_OFF_DO = KV_OFF_Q + 2 * TILE;     // [2]
+    static constexpr int KV_OFF_LSE = KV_OFF_DO + 2 * TILE;   // [2] x 128 floats
+    static constexpr int KV_OFF_DELTA = KV_OFF_LSE + 2 * 512; // [2] x 128 floats
+    static constexpr int KV_OFF_BAR = KV_OFF_DELTA + 2 * 512;
+    static constexpr int KB_KV_FULL = 0;      // K, V of a unit landed (TMA)
+    static constexpr int KB_KV_EMPTY = 1;     // the unit's products are done (commit)
+    static constexpr int KB_QD_FULL = 2;      // [2] Q, dO, lse2, Δ of a step landed (TMA)
+    static constexpr int KB_QD_EMPTY = 4;     // [2] that step's products are done (commit)
+    static constexpr int KB_S_FULL = 6;       // Sᵀ in TMEM (commit)
+    static constexpr int KB_DP_FULL = 7;      // dPᵀ in TMEM (commit)
+    static constexpr int KB_P_FULL = 8;       // Pᵀ written over Sᵀ (256)
+    static constexpr int KB_DS_FULL = 9;      // dSᵀ written over dPᵀ (256)
+    static constexpr int KB_ACC_FULL = 10;    // dK, dV of a unit complete (commit)
+    static constexpr int KB_ACC_FREE = 11;    // dK, dV read out of TMEM (128)
+    static constexpr int KB_DRAIN = 12;
+    static constexpr int KV_NUM_BARS = 13;
+    static constexpr int KV_OFF_MISC = KV_OFF_BAR + KV_NUM_BARS * 8;
+    static constexpr int KV_SMEM_USED = KV_OFF_MISC + 16;
+    static constexpr int KV_SMEM_BYTES = KV_SMEM_USED + 1024;  // + slack to align the base to 1024 bytes
+    static_assert(KV_SMEM_BYTES <= 227 * 1024, "shared memory budget");
+    static constexpr uint32_t TM_S = 0;       // Sᵀ (fp32); Pᵀ packed over columns 0-31 and 64-95
+    static constexpr uint32_t TM_DP = 128;    // dPᵀ (fp32); dSᵀ packed over columns 128-159 and 192-223
     static constexpr uint32_t TM_DV = 256;
     static constexpr uint32_t TM_DK = 256 + D;
-    static constexpr uint32_t TMEM_COLS = 512;
 
-    static __device__ __forceinline__ uint32_t bar_count(int i) {
-        if (i == B_P_FULL || i == B_DS_FULL) return 256;
-        if (i == B_DQ_FREE || i == B_ACC_FREE) return 128;
+    // ---- dQ kernel ----
+    // shared memory: Q, dO of the unit; K, V of two key blocks
+    static constexpr int Q_OFF_Q = 0;
+    static constexpr int Q_OFF_DO = Q_OFF_Q + TILE;
+    static constexpr int Q_OFF_K = Q_OFF_DO + TILE;           // [2]
+    static constexpr int Q_OFF_V = Q_OFF_K + 2 * TILE;        // [2]
+    static constexpr int Q_OFF_BAR = Q_OFF_V + 2 * TILE;
+    static constexpr int QB_QD_FULL = 0;      // Q, dO of a unit landed (TMA)
+    static constexpr int QB_QD_EMPTY = 1;     // the unit's products are done (commit)
+    static constexpr int QB_KV_FULL = 2;      // [2] K, V of a key block landed (TMA)
+    static constexpr int QB_KV_EMPTY = 4;     // [2] that block's products are done (commit)
+    static constexpr int QB_S_FULL = 6;       // [2] S in its TMEM slot (commit)
+    static constexpr int QB_DP_FULL = 8;      // dP in TMEM (commit)
+    static constexpr int QB_DS_FULL = 9;      // [2] dS written over S in its slot (256)
+    static constexpr int QB_DQ_FULL = 11;     // dQ of a unit complete (commit)
+    static constexpr int QB_DQ_FREE = 12;     // dQ read out of TMEM (128)
+    static constexpr int QB_DRAIN = 13;
+    static constexpr int Q_NUM_BARS = 14;
+    static constexpr int Q_OFF_MISC = Q_OFF_BAR + Q_NUM_BARS * 8;
+    static constexpr int Q_SMEM_USED = Q_OFF_MISC + 16;
+    static constexpr int Q_SMEM_BYTES = Q_SMEM_USED + 1024;
+    static_assert(Q_SMEM_BYTES <= 227 * 1024, "shared memory budget");
+    static constexpr uint32_t TM_QS = 0;      // [2] S (fp32); dS packed over columns s*128 + 0-31 and 64-95
+    static constexpr uint32_t TM_QDP = 256;   // dP (fp32)
+    static constexpr uint32_t TM_DQ = 384;
+
+    static constexpr uint32_t TMEM_COLS = 512;
+    static_assert(256 + 2 * D <= 512 && 384 + D <= 512, "tensor memory budget");
+
+    static __device__ __forceinline__ uint32_t kv_bar_count(int i) {
+        if (i == KB_P_FULL || i == KB_DS_FULL) return 256;
+        if (i == KB_ACC_FREE) return 128;
+        return 1;
+    }
+    static __device__ __forceinline__ uint32_t q_bar_count(int i) {
+        if (i == QB_DS_FULL || i == QB_DS_FULL + 1) return 256;
+        if (i == QB_DQ_FREE) return 128;
         return 1;
     }
 };
 
-// Unit u: key block j (ascending: with a causal mask the first key blocks
-// have the most query blocks), then z, kv head.  Its steps run over the
-// group's query heads and, per head, the query blocks from i0 on.
+// K-major operand of 128 rows in swizzled chunks of swe elements: descriptor
+// start offset (16-byte units) of the 16-element K step kk
+__host__ __device__ constexpr uint32_t kmaj_off(int kk, int swe, int sw) {
+    return (uint32_t)((((kk * 16) / swe) * (128 * sw) + ((kk * 16) % swe) * 2) >> 4);
+}
+
+// Packed 16-bit columns of a 128-wide block written by two halves over their
+// own fp32 columns: K step kk (16 elements) of the block
+__device__ __forceinline__ uint32_t packed_col(int kk) { return kk < 4 ? kk * 8 : 64 + (kk - 4) * 8; }
+
+// ---------------------------------------------------------------- schedules --
+// dK/dV unit u: key block j (ascending: with a causal mask the first key
+// blocks have the most query blocks), then z, kv head.  Its steps run over
+// the group's query heads and, per head, the query blocks from i0 on.
 struct BwdUnit {
     int z, hk, j, i0, per_head, nsteps;
 };
@@ -118,17 +157,42 @@ __device__ __forceinline__ BwdUnit bwd_unit(int u, const BwdParams& p) {
     return w;
 }
 
-// step s of a unit: query head and query block
 __device__ __forceinline__ void bwd_step(const BwdUnit& w, int s, const BwdParams& p, int& hq, int& i) {
     hq = w.hk * p.group + s / w.per_head;
     i = w.i0 + s % w.per_head;
 }
 
-// ------------------------------------------------------------ producer ------
+// dQ unit u: query block i of head (z, hq); causal: last query block first
+// (most key blocks), heads innermost.  It sees key blocks 0 .. nkv - 1.
+struct DqUnit {
+    int z, hq, hk, i, nkv;
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ DqUnit dq_unit(int u, const BwdParams& p) {
+    DqUnit w;
+    const int heads = p.Z * p.Hq;
+    int head;
+    if (CAUSAL) {
+        w.i = p.Tq - 1 - u / heads;
+        head = u % heads;
+    } else {
+        head = u / p.Tq;
+        w.i = u % p.Tq;
+    }
+    w.z = head / p.Hq;
+    w.hq = head % p.Hq;
+    w.hk = w.hq / p.group;
+    w.nkv = CAUSAL ? (w.i + 1 < p.Tk ? w.i + 1 : p.Tk) : p.Tk;
+    return w;
+}
+
+// ================================================================ dK / dV ===
+
 template <int D, bool CAUSAL>
-__device__ void bwd_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const CUtensorMap* tmQ,
-                             const CUtensorMap* tmDO, const BwdParams& p, uint32_t sbase, uint32_t bar0,
-                             const Ctl& ctl) {
+__device__ void kv_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const CUtensorMap* tmQ,
+                            const CUtensorMap* tmDO, const BwdParams& p, uint32_t sbase, uint32_t bar0,
+                            const Ctl& ctl) {
     using T = BwdTraits<D>;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     const uint64_t pol_kv = ptx::policy_evict_first();  // read once per unit
@@ -138,148 +202,124 @@ __device__ void bwd_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, con
     for (int u = blockIdx.x; ok && u < p.nunits; u += gridDim.x) {
         const BwdUnit w = bwd_unit<CAUSAL>(u, p);
         if (w.nsteps == 0) continue;
-        if (uc > 0 && !wait_phase(bar(T::B_KV_EMPTY), (uc - 1) & 1u, ctl, SITE_B_KV_EMPTY)) { ok = false; break; }
-        ptx::mbar_arrive_expect_tx(bar(T::B_KV_FULL), 2 * T::TILE);
+        if (uc > 0 && !wait_phase(bar(T::KB_KV_EMPTY), (uc - 1) & 1u, ctl, SITE_B_KV_EMPTY)) { ok = false; break; }
+        ptx::mbar_arrive_expect_tx(bar(T::KB_KV_FULL), 2 * T::TILE);
         for (int c = 0; c < T::NCHUNK; ++c) {
-            ptx::tma_load_4d(sbase + T::OFF_K + c * (128 * T::SW), tmK, bar(T::B_KV_FULL), c * T::SWE, w.j * 128,
+            ptx::tma_load_4d(sbase + T::KV_OFF_K + c * (128 * T::SW), tmK, bar(T::KB_KV_FULL), c * T::SWE, w.j * 128,
                              w.hk, w.z, pol_kv);
-            ptx::tma_load_4d(sbase + T::OFF_V + c * (128 * T::SW), tmV, bar(T::B_KV_FULL), c * T::SWE, w.j * 128,
+            ptx::tma_load_4d(sbase + T::KV_OFF_V + c * (128 * T::SW), tmV, bar(T::KB_KV_FULL), c * T::SWE, w.j * 128,
                              w.hk, w.z, pol_kv);
         }
         ++uc;
         for (int s = 0; s < w.nsteps; ++s, ++t) {
             const uint32_t st = t & 1u;
-            if (t >= 2 && !wait_phase(bar(T::B_QD_EMPTY + st), ((t - 2) >> 1) & 1u, ctl, SITE_B_QD_EMPTY)) {
+            if (t >= 2 && !wait_phase(bar(T::KB_QD_EMPTY + st), ((t - 2) >> 1) & 1u, ctl, SITE_B_QD_EMPTY)) {
                 ok = false;
                 break;
             }
             int hq, i;
             bwd_step(w, s, p, hq, i);
-            const uint32_t full = bar(T::B_QD_FULL + st);
+            const uint32_t full = bar(T::KB_QD_FULL + st);
             ptx::mbar_arrive_expect_tx(full, 2 * T::TILE + 1024);
             for (int c = 0; c < T::NCHUNK; ++c) {
-                ptx::tma_load_4d(sbase + T::OFF_Q + st * T::TILE + c * (128 * T::SW), tmQ, full, c * T::SWE, i * 128,
-                                 hq, w.z, pol_q);
-                ptx::tma_load_4d(sbase + T::OFF_DO + st * T::TILE + c * (128 * T::SW), tmDO, full, c * T::SWE,
+                ptx::tma_load_4d(sbase + T::KV_OFF_Q + st * T::TILE + c * (128 * T::SW), tmQ, full, c * T::SWE,
+                                 i * 128, hq, w.z, pol_q);
+                ptx::tma_load_4d(sbase + T::KV_OFF_DO + st * T::TILE + c * (128 * T::SW), tmDO, full, c * T::SWE,
                                  i * 128, hq, w.z, pol_q);
             }
             const int64_t row0 = ((int64_t)w.z * p.Hq + hq) * p.Tq * 128 + (int64_t)i * 128;
-            ptx::bulk_load(sbase + T::OFF_LSE + st * 512, p.lse2 + row0, 512, full);
-            ptx::bulk_load(sbase + T::OFF_DELTA + st * 512, p.delta + row0, 512, full);
+            ptx::bulk_load(sbase + T::KV_OFF_LSE + st * 512, p.lse2 + row0, 512, full);
+            ptx::bulk_load(sbase + T::KV_OFF_DELTA + st * 512, p.delta + row0, 512, full);
         }
     }
     if (!ok) {
         // let the copies in flight land before shared memory goes away
-        if (uc > 0) drain_phase(bar(T::B_KV_FULL), (uc - 1) & 1u, ctl.limit_ns);
+        if (uc > 0) drain_phase(bar(T::KB_KV_FULL), (uc - 1) & 1u, ctl.limit_ns);
         for (uint32_t x = t > 2u ? t - 2u : 0u; x < t; ++x)
-            drain_phase(bar(T::B_QD_FULL + (x & 1u)), (x >> 1) & 1u, ctl.limit_ns);
+            drain_phase(bar(T::KB_QD_FULL + (x & 1u)), (x >> 1) & 1u, ctl.limit_ns);
     }
 }
 
-// ------------------------------------------------------------ MMA issuer ----
+// Per step t: dPᵀ_t, dV_t, then Sᵀ_{t+1} (its columns were last read by dV_t,
+// issued before it), then dK_t -- so the softmax warps build Pᵀ_{t+1} while
+// the tensor core runs dK_t and dPᵀ_{t+1}.  Products issued by one thread
+// run in order, so a product never overwrites TMEM an earlier one still reads.
 template <int D, bool CAUSAL, bool BF16>
-__device__ void bwd_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0, uint32_t tmem, const Ctl& ctl) {
+__device__ void kv_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0, uint32_t tmem, const Ctl& ctl) {
     using T = BwdTraits<D>;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
-    // Sᵀ = K Qᵀ and dPᵀ = V dOᵀ: A and B K-major (rows of 128 keys / queries, D contiguous)
-    constexpr uint32_t ID_SQ = ptx::idesc_f16(128, 128, BF16, false, false);
-    // dV += Pᵀ dO and dK += dSᵀ Q: N = D, B MN-major (D contiguous along N)
-    constexpr uint32_t ID_ND = ptx::idesc_f16(128, D, BF16, false, true);
-    // dQ = dS K: A = dSᵀ read MN-major (queries contiguous), B = K MN-major
-    constexpr uint32_t ID_DQ = ptx::idesc_f16(128, D, BF16, true, true);
-    constexpr uint32_t HI = ptx::smem_desc_hi(8 * T::SW, T::SWIZZLE_CODE);  // Q, K, V, dO tiles
-    constexpr uint32_t HI_DS = ptx::smem_desc_hi(8 * 128, 2u);              // dSᵀ: 128-B swizzle
-    const uint32_t k_lo = ptx::smem_desc_lo(sbase + T::OFF_K, 16);
-    const uint32_t v_lo = ptx::smem_desc_lo(sbase + T::OFF_V, 16);
-    const uint32_t kmn_lo = ptx::smem_desc_lo(sbase + T::OFF_K, 128 * T::SW);     // K as MN-major B
-    const uint32_t ds_lo = ptx::smem_desc_lo(sbase + T::OFF_DS, 16);             // dSᵀ as K-major A
-    const uint32_t dsmn_lo = ptx::smem_desc_lo(sbase + T::OFF_DS, 128 * 128);    // dSᵀ as MN-major A
-    // K-major operand of 128 rows: 16-element step kk inside swizzled chunks
-    auto kmaj = [&](int kk, int swe, int sw) -> uint32_t {
-        return (uint32_t)((((kk * 16) / swe) * (128 * sw) + ((kk * 16) % swe) * 2) >> 4);
-    };
-    // Sᵀ of step t into TMEM; its operands are stage t & 1
+    constexpr uint32_t ID_SQ = ptx::idesc_f16(128, 128, BF16, false, false);  // Sᵀ = K Qᵀ, dPᵀ = V dOᵀ
+    constexpr uint32_t ID_ND = ptx::idesc_f16(128, D, BF16, false, true);     // dV, dK: B MN-major (N = D)
+    constexpr uint32_t HI = ptx::smem_desc_hi(8 * T::SW, T::SWIZZLE_CODE);
+    const uint32_t k_lo = ptx::smem_desc_lo(sbase + T::KV_OFF_K, 16);
+    const uint32_t v_lo = ptx::smem_desc_lo(sbase + T::KV_OFF_V, 16);
     auto issue_s = [&](uint32_t t) -> bool {
         const uint32_t st = t & 1u;
-        if (!wait_phase(bar(T::B_QD_FULL + st), (t >> 1) & 1u, ctl, SITE_B_QD_FULL)) return false;
+        if (!wait_phase(bar(T::KB_QD_FULL + st), (t >> 1) & 1u, ctl, SITE_B_QD_FULL)) return false;
         ptx::tc_fence_after();
-        const uint32_t q_lo = ptx::smem_desc_lo(sbase + T::OFF_Q + st * T::TILE, 16);
+        const uint32_t q_lo = ptx::smem_desc_lo(sbase + T::KV_OFF_Q + st * T::TILE, 16);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-            ptx::mma_ss(tmem + T::TM_S, ptx::desc64(k_lo + kmaj(kk, T::SWE, T::SW), HI),
-                        ptx::desc64(q_lo + kmaj(kk, T::SWE, T::SW), HI), ID_SQ, kk > 0 ? 1u : 0u);
-        ptx::tc_commit(bar(T::B_S_FULL));
+            ptx::mma_ss(tmem + T::TM_S, ptx::desc64(k_lo + kmaj_off(kk, T::SWE, T::SW), HI),
+                        ptx::desc64(q_lo + kmaj_off(kk, T::SWE, T::SW), HI), ID_SQ, kk > 0 ? 1u : 0u);
+        ptx::tc_commit(bar(T::KB_S_FULL));
         return true;
     };
-    // Order per step t: dPᵀ_t, dV_t, then Sᵀ_{t+1} (its columns were last read
-    // by dV_t, issued before it; the softmax warps keep Pᵀ_t in registers), then
-    // dK_t and dQ_t -- so the softmax warps build Pᵀ_{t+1} while the tensor core
-    // runs dK_t and dQ_t.
     uint32_t uc = 0, t = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < p.nunits; u += gridDim.x) {
         const BwdUnit w = bwd_unit<CAUSAL>(u, p);
         if (w.nsteps == 0) continue;
-        if (!wait_phase(bar(T::B_KV_FULL), uc & 1u, ctl, SITE_B_KV_FULL)) { ok = false; break; }
+        if (!wait_phase(bar(T::KB_KV_FULL), uc & 1u, ctl, SITE_B_KV_FULL)) { ok = false; break; }
         if (!issue_s(t)) { ok = false; break; }
         for (int s = 0; s < w.nsteps; ++s, ++t) {
             const uint32_t st = t & 1u;
-            const uint32_t qmn_lo = ptx::smem_desc_lo(sbase + T::OFF_Q + st * T::TILE, 128 * T::SW);
-            const uint32_t do_lo = ptx::smem_desc_lo(sbase + T::OFF_DO + st * T::TILE, 16);
-            const uint32_t domn_lo = ptx::smem_desc_lo(sbase + T::OFF_DO + st * T::TILE, 128 * T::SW);
-            // dPᵀ = V dOᵢᵀ, once the previous dQ partial (same columns) is read out
-            if (t > 0 && !wait_phase(bar(T::B_DQ_FREE), (t - 1) & 1u, ctl, SITE_B_DQ_FREE)) { ok = false; break; }
-            ptx::tc_fence_after();
+            const uint32_t do_lo = ptx::smem_desc_lo(sbase + T::KV_OFF_DO + st * T::TILE, 16);
+            const uint32_t domn_lo = ptx::smem_desc_lo(sbase + T::KV_OFF_DO + st * T::TILE, 128 * T::SW);
+            const uint32_t qmn_lo = ptx::smem_desc_lo(sbase + T::KV_OFF_Q + st * T::TILE, 128 * T::SW);
+            // dPᵀ = V dOᵢᵀ
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
-                ptx::mma_ss(tmem + T::TM_DP, ptx::desc64(v_lo + kmaj(kk, T::SWE, T::SW), HI),
-                            ptx::desc64(do_lo + kmaj(kk, T::SWE, T::SW), HI), ID_SQ, kk > 0 ? 1u : 0u);
-            ptx::tc_commit(bar(T::B_DP_FULL));
-            // dV += Pᵀ dOᵢ; the first step of a unit waits for the last unit's dK, dV to be read
-            if (!wait_phase(bar(T::B_P_FULL), t & 1u, ctl, SITE_B_P_FULL)) { ok = false; break; }
-            if (s == 0 && uc > 0 && !wait_phase(bar(T::B_ACC_FREE), (uc - 1) & 1u, ctl, SITE_B_ACC_FREE)) {
+                ptx::mma_ss(tmem + T::TM_DP, ptx::desc64(v_lo + kmaj_off(kk, T::SWE, T::SW), HI),
+                            ptx::desc64(do_lo + kmaj_off(kk, T::SWE, T::SW), HI), ID_SQ, kk > 0 ? 1u : 0u);
+            ptx::tc_commit(bar(T::KB_DP_FULL));
+            // dV += Pᵀ dOᵢ; a unit's first step waits for the last unit's dK, dV to be read
+            if (!wait_phase(bar(T::KB_P_FULL), t & 1u, ctl, SITE_B_P_FULL)) { ok = false; break; }
+            if (s == 0 && uc > 0 && !wait_phase(bar(T::KB_ACC_FREE), (uc - 1) & 1u, ctl, SITE_B_ACC_FREE)) {
                 ok = false;
                 break;
             }
             ptx::tc_fence_after();
-            // Pᵀ of queries 0-63 sits in packed columns 0-31, of queries 64-127 in 64-95
 #pragma unroll
             for (int kk = 0; kk < 128 / 16; ++kk)
-                ptx::mma_ts(tmem + T::TM_DV, tmem + T::TM_S + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
+                ptx::mma_ts(tmem + T::TM_DV, tmem + T::TM_S + packed_col(kk),
                             ptx::desc64(domn_lo + ((kk * 16 * T::SW) >> 4), HI), ID_ND, (s > 0 || kk > 0) ? 1u : 0u);
             if (s + 1 < w.nsteps && !issue_s(t + 1)) { ok = false; break; }
-            // dK += dSᵀ Qᵢ and dQᵢ = dS K, once dSᵀ is in shared memory
-            if (!wait_phase(bar(T::B_DS_FULL), t & 1u, ctl, SITE_B_DS_FULL)) { ok = false; break; }
+            // dK += dSᵀ Qᵢ
+            if (!wait_phase(bar(T::KB_DS_FULL), t & 1u, ctl, SITE_B_DS_FULL)) { ok = false; break; }
             ptx::tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 128 / 16; ++kk)
-                ptx::mma_ss(tmem + T::TM_DK, ptx::desc64(ds_lo + kmaj(kk, 64, 128), HI_DS),
+                ptx::mma_ts(tmem + T::TM_DK, tmem + T::TM_DP + packed_col(kk),
                             ptx::desc64(qmn_lo + ((kk * 16 * T::SW) >> 4), HI), ID_ND, (s > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-            for (int kk = 0; kk < 128 / 16; ++kk)
-                ptx::mma_ss(tmem + T::TM_DP, ptx::desc64(dsmn_lo + ((kk * 16 * 128) >> 4), HI_DS),
-                            ptx::desc64(kmn_lo + ((kk * 16 * T::SW) >> 4), HI), ID_DQ, kk > 0 ? 1u : 0u);
-            ptx::tc_commit(bar(T::B_DQ_FULL));       // dQ partial ready, dSᵀ buffer free
-            ptx::tc_commit(bar(T::B_QD_EMPTY + st));  // Qᵢ, dOᵢ slot free
+            ptx::tc_commit(bar(T::KB_QD_EMPTY + st));  // Qᵢ, dOᵢ slot free
         }
         if (!ok) break;
-        ptx::tc_commit(bar(T::B_ACC_FULL));  // dK, dV of the unit complete
-        ptx::tc_commit(bar(T::B_KV_EMPTY));  // K, V free
+        ptx::tc_commit(bar(T::KB_ACC_FULL));  // dK, dV of the unit complete
+        ptx::tc_commit(bar(T::KB_KV_EMPTY));  // K, V free
         ++uc;
     }
     if (!ok) {
-        ptx::tc_commit(bar(T::B_DRAIN));
-        drain_phase(bar(T::B_DRAIN), 0u, ctl.limit_ns);
+        ptx::tc_commit(bar(T::KB_DRAIN));
+        drain_phase(bar(T::KB_DRAIN), 0u, ctl.limit_ns);
     }
 }
 
-// ------------------------------------------------------------ Pᵀ and dSᵀ ----
-// Thread = key (TMEM lane); half h takes queries h*64 .. h*64 + 63.  Each
-// half writes its Pᵀ over its own Sᵀ columns (packed columns h*64 ..), so no
-// half overwrites scores the other has not read.
+// Thread = key (TMEM lane); half h takes queries h*64 .. h*64 + 63 and writes
+// its Pᵀ and dSᵀ (input type, two per column) over its own fp32 columns, so
+// no half overwrites values the other has not read.
 template <int D, bool CAUSAL, bool BF16>
-__device__ void bwd_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar0, uint32_t tmem, int h,
-                            const Ctl& ctl) {
+__device__ void kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar0, uint32_t tmem, int h, const Ctl& ctl) {
     using T = BwdTraits<D>;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     const int quad = (threadIdx.x / 32) % 4;
@@ -294,16 +334,14 @@ __device__ void bwd_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar0, u
             int hq, i;
             bwd_step(w, s, p, hq, i);
             // lse2 and Δ of the step's queries arrive with Qᵢ (TMA)
-            if (!warp_wait_phase(bar(T::B_QD_FULL + st), (t >> 1) & 1u, ctl, SITE_B_QD_FULL)) return;
-            const uint32_t lse_a = sbase + T::OFF_LSE + st * 512 + h * 256;
-            const uint32_t del_a = sbase + T::OFF_DELTA + st * 512 + h * 256;
-            if (!warp_wait_phase(bar(T::B_S_FULL), t & 1u, ctl, SITE_B_S_FULL)) return;
+            if (!warp_wait_phase(bar(T::KB_QD_FULL + st), (t >> 1) & 1u, ctl, SITE_B_QD_FULL)) return;
+            const uint32_t lse_a = sbase + T::KV_OFF_LSE + st * 512 + h * 256;
+            const uint32_t del_a = sbase + T::KV_OFF_DELTA + st * 512 + h * 256;
+            if (!warp_wait_phase(bar(T::KB_S_FULL), t & 1u, ctl, SITE_B_S_FULL)) return;
             ptx::tc_fence_after();
             // causal: only the diagonal block has keys after queries (key > query -> 0)
             const bool diag = CAUSAL && i == w.j;
-            // Pᵀ in the input type (it is the tensor-core operand of dV, and
-            // dS below uses the same rounded values)
-            uint32_t pk[32];
+            uint32_t pk[32];  // Pᵀ in the input type: the dV operand, and what dS uses
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 uint32_t r[32];
@@ -323,13 +361,10 @@ __device__ void bwd_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar0, u
             ptx::tmem_st32(tmem + lane_addr + T::TM_S + h * 64, pk);
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(bar(T::B_P_FULL));
+            ptx::mbar_arrive(bar(T::KB_P_FULL));
 
-            if (!warp_wait_phase(bar(T::B_DP_FULL), t & 1u, ctl, SITE_B_DP_FULL)) return;
-            // the dSᵀ buffer is free once the previous step's dK and dQ MMAs completed
-            if (t > 0 && !warp_wait_phase(bar(T::B_DQ_FULL), (t - 1) & 1u, ctl, SITE_B_DS_FREE)) return;
+            if (!warp_wait_phase(bar(T::KB_DP_FULL), t & 1u, ctl, SITE_B_DP_FULL)) return;
             ptx::tc_fence_after();
-            const uint32_t ds_row = sbase + T::OFF_DS + h * (128 * 128) + row * 128;
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 uint32_t r[32];
@@ -342,32 +377,27 @@ __device__ void bwd_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar0, u
                     const float2 pp = unpack2<BF16>(pk[16 * cc + x]);
                     ds[x] = pack2<BF16>(pp.x * (__uint_as_float(r[2 * x]) - d0), pp.y * (__uint_as_float(r[2 * x + 1]) - d1));
                 }
-                // 16-byte units 4cc .. 4cc + 3 of this row of the chunk, 128-B swizzle
-#pragma unroll
-                for (int uu = 0; uu < 4; ++uu) {
-                    const uint32_t unit = (uint32_t)(4 * cc + uu) ^ (uint32_t)(row & 7);
-                    ptx::st_shared_v4(ds_row + unit * 16, ds[4 * uu], ds[4 * uu + 1], ds[4 * uu + 2], ds[4 * uu + 3]);
-                }
+                // packed columns h*64 + 16cc .. : fp32 columns this thread has already read
+                ptx::tmem_st16(tmem + lane_addr + T::TM_DP + h * 64 + 16 * cc, ds);
             }
-            ptx::fence_proxy_async_smem();
-            ptx::mbar_arrive(bar(T::B_DS_FULL));
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(T::KB_DS_FULL));
         }
     }
 }
 
-// ------------------------------------------------------------ epilogue ------
-// Thread = TMEM lane.  Per step: the dQ partial (lane = query) is read out,
-// released, and added into the fp32 accumulator.  Per unit: dK (times scale)
-// and dV (lane = key) are read out, released and stored in the input type.
+// Thread = TMEM lane = key: per unit, dK (times scale) and dV are read out,
+// released and stored in the input type; a unit no query sees gets zeros.
 template <int D, bool CAUSAL, bool BF16>
-__device__ void bwd_epilogue(const BwdParams& p, uint32_t bar0, uint32_t tmem, const Ctl& ctl) {
+__device__ void kv_epilogue(const BwdParams& p, uint32_t bar0, uint32_t tmem, const Ctl& ctl) {
     using T = BwdTraits<D>;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     const int quad = (threadIdx.x / 32) % 4;
     const int row = quad * 32 + threadIdx.x % 32;
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
     constexpr int CH = D >= 32 ? 32 : 16;
-    uint32_t t = 0, uc = 0;
+    uint32_t uc = 0;
     for (int u = blockIdx.x; u < p.nunits; u += gridDim.x) {
         const BwdUnit w = bwd_unit<CAUSAL>(u, p);
         const int key = w.j * 128 + row;
@@ -376,7 +406,6 @@ __device__ void bwd_epilogue(const BwdParams& p, uint32_t bar0, uint32_t tmem, c
         uint8_t* dv_row = reinterpret_cast<uint8_t*>(p.dv) +
                           2 * ((int64_t)w.z * p.sdv_z + (int64_t)w.hk * p.sdv_h + (int64_t)key * p.sdv_n);
         if (w.nsteps == 0) {
-            // no query sees these keys: zero gradients
             if (key < p.Nkv) {
 #pragma unroll
                 for (int x = 0; x < D / 8; ++x) {
@@ -386,31 +415,7 @@ __device__ void bwd_epilogue(const BwdParams& p, uint32_t bar0, uint32_t tmem, c
             }
             continue;
         }
-        for (int s = 0; s < w.nsteps; ++s, ++t) {
-            int hq, i;
-            bwd_step(w, s, p, hq, i);
-            if (!warp_wait_phase(bar(T::B_DQ_FULL), t & 1u, ctl, SITE_B_DQ_FULL)) return;
-            ptx::tc_fence_after();
-            const int q = i * 128 + row;
-            float* acc = p.dq_acc + (((int64_t)w.z * p.Hq + hq) * p.Nq + q) * D;
-#pragma unroll
-            for (int cc = 0; cc < D / CH; ++cc) {
-                uint32_t r[CH];
-                if constexpr (CH == 32) ptx::tmem_ld32(tmem + lane_addr + T::TM_DP + cc * CH, r);
-                else ptx::tmem_ld16(tmem + lane_addr + T::TM_DP + cc * CH, r);
-                if (cc == D / CH - 1) {
-                    ptx::tc_fence_before();
-                    ptx::mbar_arrive(bar(T::B_DQ_FREE));
-                }
-                if (q < p.Nq) {
-#pragma unroll
-                    for (int x = 0; x < CH / 4; ++x)
-                        ptx::red_add_v4(acc + cc * CH + 4 * x, __uint_as_float(r[4 * x]), __uint_as_float(r[4 * x + 1]),
-                                        __uint_as_float(r[4 * x + 2]), __uint_as_float(r[4 * x + 3]));
-                }
-            }
-        }
-        if (!warp_wait_phase(bar(T::B_ACC_FULL), uc & 1u, ctl, SITE_B_ACC_FULL)) return;
+        if (!warp_wait_phase(bar(T::KB_ACC_FULL), uc & 1u, ctl, SITE_B_ACC_FULL)) return;
         ptx::tc_fence_after();
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
@@ -424,7 +429,7 @@ __device__ void bwd_epilogue(const BwdParams& p, uint32_t bar0, uint32_t tmem, c
                 else ptx::tmem_ld16(tmem + lane_addr + col0 + cc * CH, r);
                 if (which == 1 && cc == D / CH - 1) {
                     ptx::tc_fence_before();
-                    ptx::mbar_arrive(bar(T::B_ACC_FREE));
+                    ptx::mbar_arrive(bar(T::KB_ACC_FREE));
                 }
                 if (key < p.Nkv) {
 #pragma unroll
@@ -441,29 +446,35 @@ __device__ void bwd_epilogue(const BwdParams& p, uint32_t bar0, uint32_t tmem, c
     }
 }
 
-// ------------------------------------------------------------ kernel --------
+// Aligned dynamic shared memory base (the swizzled tiles need 1024 bytes);
+// false (and an error in the status word) when the launch left no room.
+__device__ __forceinline__ bool bwd_smem_base(uint8_t* raw, int used, int bytes, const BwdParams& p, uint8_t*& smem) {
+    const uint32_t a = ptx::smem_addr(raw);
+    const uint32_t pad = (1024u - (a & 1023u)) & 1023u;
+    if (pad + (uint32_t)used > (uint32_t)bytes) {
+        if (threadIdx.x == 0) atomicCAS(p.status, 0u, 4u /* FA_ERR_CUDA */ | (0xFFu << 8) | ((blockIdx.x & 0xFFFFu) << 16));
+        return false;
+    }
+    smem = raw + pad;
+    return true;
+}
+
 template <int D, bool CAUSAL, bool BF16>
 __global__ void __launch_bounds__(BWD_THREADS, 1)
-    fa_bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                  const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
-                  const BwdParams p) {
+    fa_bwd_kv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
+                     const BwdParams p) {
     using T = BwdTraits<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    const uint32_t raw = ptx::smem_addr(smem_raw);
-    const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
-    if (pad + T::SMEM_USED > T::SMEM_BYTES) {
-        // no room to align the swizzled tiles: report and leave (uniform for the CTA)
-        if (threadIdx.x == 0) atomicCAS(p.status, 0u, 4u /* FA_ERR_CUDA */ | (0xFFu << 8) | ((blockIdx.x & 0xFFFFu) << 16));
-        return;
-    }
-    uint8_t* smem = smem_raw + pad;
-    const uint32_t sbase = raw + pad;
-    const uint32_t bar0 = sbase + T::OFF_BAR;
-    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + T::OFF_MISC);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + T::OFF_MISC + 4);
+    uint8_t* smem = nullptr;
+    if (!bwd_smem_base(smem_raw, T::KV_SMEM_USED, T::KV_SMEM_BYTES, p, smem)) return;
+    const uint32_t sbase = ptx::smem_addr(smem);
+    const uint32_t bar0 = sbase + T::KV_OFF_BAR;
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + T::KV_OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + T::KV_OFF_MISC + 4);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (threadIdx.x == 0) {
-        for (int i = 0; i < T::NUM_BARS; ++i) ptx::mbar_init(bar0 + 8u * i, T::bar_count(i));
+        for (int i = 0; i < T::KV_NUM_BARS; ++i) ptx::mbar_init(bar0 + 8u * i, T::kv_bar_count(i));
         *abort_flag = 0;
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&tmK);
@@ -481,13 +492,13 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const uint32_t tmem = *tmem_slot;
     const Ctl ctl{abort_flag, p.status, p.wait_limit_ns};
     if (warp < 8) {
-        bwd_softmax<D, CAUSAL, BF16>(p, sbase, bar0, tmem, warp / 4, ctl);
+        kv_softmax<D, CAUSAL, BF16>(p, sbase, bar0, tmem, warp / 4, ctl);
     } else if (warp < 12) {
-        bwd_epilogue<D, CAUSAL, BF16>(p, bar0, tmem, ctl);
+        kv_epilogue<D, CAUSAL, BF16>(p, bar0, tmem, ctl);
     } else if (warp == 12) {
-        if (lane == 0) bwd_producer<D, CAUSAL>(&tmK, &tmV, &tmQ, &tmDO, p, sbase, bar0, ctl);
+        if (lane == 0) kv_producer<D, CAUSAL>(&tmK, &tmV, &tmQ, &tmDO, p, sbase, bar0, ctl);
     } else {
-        if (lane == 0) bwd_issuer<D, CAUSAL, BF16>(p, sbase, bar0, tmem, ctl);
+        if (lane == 0) kv_issuer<D, CAUSAL, BF16>(p, sbase, bar0, tmem, ctl);
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -497,15 +508,275 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     }
 }
 
-// ------------------------------------------------------------ pre / post ----
+// ===================================================================== dQ ===
+
+template <int D, bool CAUSAL>
+__device__ void q_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const CUtensorMap* tmQ,
+                           const CUtensorMap* tmDO, const BwdParams& p, uint32_t sbase, uint32_t bar0, const Ctl& ctl) {
+    using T = BwdTraits<D>;
+    auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+    const uint64_t pol_q = ptx::policy_evict_first();  // read once per unit
+    const uint64_t pol_kv = ptx::policy_evict_last();  // read by every query block of the group
+    uint32_t uc = 0, g = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < p.nunits_q; u += gridDim.x) {
+        const DqUnit w = dq_unit<CAUSAL>(u, p);
+        if (uc > 0 && !wait_phase(bar(T::QB_QD_EMPTY), (uc - 1) & 1u, ctl, SITE_B_QD_EMPTY)) { ok = false; break; }
+        ptx::mbar_arrive_expect_tx(bar(T::QB_QD_FULL), 2 * T::TILE);
+        for (int c = 0; c < T::NCHUNK; ++c) {
+            ptx::tma_load_4d(sbase + T::Q_OFF_Q + c * (128 * T::SW), tmQ, bar(T::QB_QD_FULL), c * T::SWE, w.i * 128,
+                             w.hq, w.z, pol_q);
+            ptx::tma_load_4d(sbase + T::Q_OFF_DO + c * (128 * T::SW), tmDO, bar(T::QB_QD_FULL), c * T::SWE,
+                             w.i * 128, w.hq, w.z, pol_q);
+        }
+        ++uc;
+        for (int j = 0; j < w.nkv; ++j, ++g) {
+            const uint32_t st = g & 1u;
+            if (g >= 2 && !wait_phase(bar(T::QB_KV_EMPTY + st), ((g - 2) >> 1) & 1u, ctl, SITE_B_KV_EMPTY)) {
+                ok = false;
+                break;
+            }
+            const uint32_t full = bar(T::QB_KV_FULL + st);
+            ptx::mbar_arrive_expect_tx(full, 2 * T::TILE);
+            for (int c = 0; c < T::NCHUNK; ++c) {
+                ptx::tma_load_4d(sbase + T::Q_OFF_K + st * T::TILE + c * (128 * T::SW), tmK, full, c * T::SWE,
+                                 j * 128, w.hk, w.z, pol_kv);
+                ptx::tma_load_4d(sbase + T::Q_OFF_V + st * T::TILE + c * (128 * T::SW), tmV, full, c * T::SWE,
+                                 j * 128, w.hk, w.z, pol_kv);
+            }
+        }
+    }
+    if (!ok) {
+        if (uc > 0) drain_phase(bar(T::QB_QD_FULL), (uc - 1) & 1u, ctl.limit_ns);
+        for (uint32_t x = g > 2u ? g - 2u : 0u; x < g; ++x)
+            drain_phase(bar(T::QB_KV_FULL + (x & 1u)), (x >> 1) & 1u, ctl.limit_ns);
+    }
+}
+
+// Per key block g: S_{g+1} goes to the other TMEM slot while the softmax
+// warps turn S_g and dP_g into dS_g; then dQ += dS_g K_g and dP_{g+1}.
+template <int D, bool CAUSAL, bool BF16>
+__device__ void q_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0, uint32_t tmem, const Ctl& ctl) {
+    using T = BwdTraits<D>;
+    auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+    constexpr uint32_t ID_SQ = ptx::idesc_f16(128, 128, BF16, false, false);  // S = Q Kᵀ, dP = dO Vᵀ
+    constexpr uint32_t ID_DQ = ptx::idesc_f16(128, D, BF16, false, true);     // dQ += dS K (K MN-major)
+    constexpr uint32_t HI = ptx::smem_desc_hi(8 * T::SW, T::SWIZZLE_CODE);
+    const uint32_t q_lo = ptx::smem_desc_lo(sbase + T::Q_OFF_Q, 16);
+    const uint32_t do_lo = ptx::smem_desc_lo(sbase + T::Q_OFF_DO, 16);
+    auto issue_s = [&](uint32_t g) -> bool {
+        const uint32_t st = g & 1u;
+        if (!wait_phase(bar(T::QB_KV_FULL + st), (g >> 1) & 1u, ctl, SITE_B_KV_FULL)) return false;
+        ptx::tc_fence_after();
+        const uint32_t k_lo = ptx::smem_desc_lo(sbase + T::Q_OFF_K + st * T::TILE, 16);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+            ptx::mma_ss(tmem + T::TM_QS + st * 128, ptx::desc64(q_lo + kmaj_off(kk, T::SWE, T::SW), HI),
+                        ptx::desc64(k_lo + kmaj_off(kk, T::SWE, T::SW), HI), ID_SQ, kk > 0 ? 1u : 0u);
+        ptx::tc_commit(bar(T::QB_S_FULL + st));
+        return true;
+    };
+    auto issue_dp = [&](uint32_t g) {
+        const uint32_t v_lo = ptx::smem_desc_lo(sbase + T::Q_OFF_V + (g & 1u) * T::TILE, 16);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+            ptx::mma_ss(tmem + T::TM_QDP, ptx::desc64(do_lo + kmaj_off(kk, T::SWE, T::SW), HI),
+                        ptx::desc64(v_lo + kmaj_off(kk, T::SWE, T::SW), HI), ID_SQ, kk > 0 ? 1u : 0u);
+        ptx::tc_commit(bar(T::QB_DP_FULL));
+    };
+    uint32_t uc = 0, g = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < p.nunits_q; u += gridDim.x) {
+        const DqUnit w = dq_unit<CAUSAL>(u, p);
+        if (!wait_phase(bar(T::QB_QD_FULL), uc & 1u, ctl, SITE_B_QD_FULL)) { ok = false; break; }
+        if (!issue_s(g)) { ok = false; break; }
+        issue_dp(g);
+        for (int j = 0; j < w.nkv; ++j, ++g) {
+            const uint32_t st = g & 1u;
+            if (j + 1 < w.nkv && !issue_s(g + 1)) { ok = false; break; }
+            if (!wait_phase(bar(T::QB_DS_FULL + st), (g >> 1) & 1u, ctl, SITE_B_DS_FULL)) { ok = false; break; }
+            if (j == 0 && uc > 0 && !wait_phase(bar(T::QB_DQ_FREE), (uc - 1) & 1u, ctl, SITE_B_DQ_FREE)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t kmn_lo = ptx::smem_desc_lo(sbase + T::Q_OFF_K + st * T::TILE, 128 * T::SW);
+#pragma unroll
+            for (int kk = 0; kk < 128 / 16; ++kk)
+                ptx::mma_ts(tmem + T::TM_DQ, tmem + T::TM_QS + st * 128 + packed_col(kk),
+                            ptx::desc64(kmn_lo + ((kk * 16 * T::SW) >> 4), HI), ID_DQ, (j > 0 || kk > 0) ? 1u : 0u);
+            ptx::tc_commit(bar(T::QB_KV_EMPTY + st));  // K_g, V_g free
+            if (j + 1 < w.nkv) issue_dp(g + 1);
+        }
+        if (!ok) break;
+        ptx::tc_commit(bar(T::QB_DQ_FULL));   // dQ of the unit complete
+        ptx::tc_commit(bar(T::QB_QD_EMPTY));  // Q, dO free
+        ++uc;
+    }
+    if (!ok) {
+        ptx::tc_commit(bar(T::QB_DRAIN));
+        drain_phase(bar(T::QB_DRAIN), 0u, ctl.limit_ns);
+    }
+}
+
+// Thread = query (TMEM lane); half h takes keys h*64 .. h*64 + 63 of each
+// block.  lse2 and Δ are per row, so they stay in registers for the unit.
+template <int D, bool CAUSAL, bool BF16>
+__device__ void q_softmax(const BwdParams& p, uint32_t bar0, uint32_t tmem, int h, const Ctl& ctl) {
+    using T = BwdTraits<D>;
+    auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+    const int quad = (threadIdx.x / 32) % 4;
+    const int row = quad * 32 + threadIdx.x % 32;  // query within the block
+    const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
+    const float c = p.scale_log2;
+    uint32_t g = 0;
+    for (int u = blockIdx.x; u < p.nunits_q; u += gridDim.x) {
+        const DqUnit w = dq_unit<CAUSAL>(u, p);
+        const int64_t r = ((int64_t)w.z * p.Hq + w.hq) * p.Tq * 128 + (int64_t)w.i * 128 + row;
+        const float l2 = __ldg(p.lse2 + r), dl = __ldg(p.delta + r);
+        for (int j = 0; j < w.nkv; ++j, ++g) {
+            const uint32_t st = g & 1u;
+            const uint32_t slot = tmem + lane_addr + T::TM_QS + st * 128;
+            if (!warp_wait_phase(bar(T::QB_S_FULL + st), (g >> 1) & 1u, ctl, SITE_B_S_FULL)) return;
+            ptx::tc_fence_after();
+            const bool diag = CAUSAL && j == w.i;  // key > query only on the diagonal block
+            uint32_t pk[32];
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                uint32_t rr[32];
+                ptx::tmem_ld32(slot + h * 64 + 32 * cc, rr);
+#pragma unroll
+                for (int x = 0; x < 16; ++x) {
+                    const int col = h * 64 + 32 * cc + 2 * x;
+                    float e0 = fmaf(__uint_as_float(rr[2 * x]), c, -l2);
+                    float e1 = fmaf(__uint_as_float(rr[2 * x + 1]), c, -l2);
+                    if (diag && col > row) e0 = -INFINITY;
+                    if (diag && col + 1 > row) e1 = -INFINITY;
+                    pk[16 * cc + x] = pack2<BF16>(ptx::ex2(e0), ptx::ex2(e1));
+                }
+            }
+            if (!warp_wait_phase(bar(T::QB_DP_FULL), g & 1u, ctl, SITE_B_DP_FULL)) return;
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                uint32_t rr[32];
+                ptx::tmem_ld32(tmem + lane_addr + T::TM_QDP + h * 64 + 32 * cc, rr);
+                uint32_t ds[16];
+#pragma unroll
+                for (int x = 0; x < 16; ++x) {
+                    const float2 pp = unpack2<BF16>(pk[16 * cc + x]);
+                    ds[x] = pack2<BF16>(pp.x * (__uint_as_float(rr[2 * x]) - dl), pp.y * (__uint_as_float(rr[2 * x + 1]) - dl));
+                }
+                // dS over the slot's packed columns h*64 + 16cc .. (S already read)
+                ptx::tmem_st16(slot + h * 64 + 16 * cc, ds);
+            }
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(T::QB_DS_FULL + st));
+        }
+    }
+}
+
+// Thread = TMEM lane = query: dQ (times scale) read out, released, stored.
+template <int D, bool CAUSAL, bool BF16>
+__device__ void q_epilogue(const BwdParams& p, uint32_t bar0, uint32_t tmem, const Ctl& ctl) {
+    using T = BwdTraits<D>;
+    auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+    const int quad = (threadIdx.x / 32) % 4;
+    const int row = quad * 32 + threadIdx.x % 32;
+    const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
+    constexpr int CH = D >= 32 ? 32 : 16;
+    uint32_t uc = 0;
+    for (int u = blockIdx.x; u < p.nunits_q; u += gridDim.x, ++uc) {
+        const DqUnit w = dq_unit<CAUSAL>(u, p);
+        const int q = w.i * 128 + row;
+        uint8_t* dst = reinterpret_cast<uint8_t*>(p.dq) +
+                       2 * ((int64_t)w.z * p.sdq_z + (int64_t)w.hq * p.sdq_h + (int64_t)q * p.sdq_n);
+        if (!warp_wait_phase(bar(T::QB_DQ_FULL), uc & 1u, ctl, SITE_B_DQ_FULL)) return;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int cc = 0; cc < D / CH; ++cc) {
+            uint32_t r[CH];
+            if constexpr (CH == 32) ptx::tmem_ld32(tmem + lane_addr + T::TM_DQ + cc * CH, r);
+            else ptx::tmem_ld16(tmem + lane_addr + T::TM_DQ + cc * CH, r);
+            if (cc == D / CH - 1) {
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(bar(T::QB_DQ_FREE));
+            }
+            if (q < p.Nq) {
+                const float m = p.scale;
+#pragma unroll
+                for (int x = 0; x < CH / 8; ++x)
+                    reinterpret_cast<uint4*>(dst + 2 * cc * CH)[x] =
+                        make_uint4(pack2<BF16>(__uint_as_float(r[8 * x]) * m, __uint_as_float(r[8 * x + 1]) * m),
+                                   pack2<BF16>(__uint_as_float(r[8 * x + 2]) * m, __uint_as_float(r[8 * x + 3]) * m),
+                                   pack2<BF16>(__uint_as_float(r[8 * x + 4]) * m, __uint_as_float(r[8 * x + 5]) * m),
+                                   pack2<BF16>(__uint_as_float(r[8 * x + 6]) * m, __uint_as_float(r[8 * x + 7]) * m));
+            }
+        }
+    }
+}
+
+template <int D, bool CAUSAL, bool BF16>
+__global__ void __launch_bounds__(BWD_THREADS, 1)
+    fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
+                     const BwdParams p) {
+    using T = BwdTraits<D>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = nullptr;
+    if (!bwd_smem_base(smem_raw, T::Q_SMEM_USED, T::Q_SMEM_BYTES, p, smem)) return;
+    const uint32_t sbase = ptx::smem_addr(smem);
+    const uint32_t bar0 = sbase + T::Q_OFF_BAR;
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + T::Q_OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + T::Q_OFF_MISC + 4);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < T::Q_NUM_BARS; ++i) ptx::mbar_init(bar0 + 8u * i, T::q_bar_count(i));
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+        ptx::prefetch_tmap(&tmK);
+        ptx::prefetch_tmap(&tmV);
+        ptx::prefetch_tmap(&tmQ);
+        ptx::prefetch_tmap(&tmDO);
+    }
+    if (warp == 13) {
+        ptx::tmem_alloc(ptx::smem_addr(const_cast<uint32_t*>(tmem_slot)), T::TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const Ctl ctl{abort_flag, p.status, p.wait_limit_ns};
+    if (warp < 8) {
+        q_softmax<D, CAUSAL, BF16>(p, bar0, tmem, warp / 4, ctl);
+    } else if (warp < 12) {
+        q_epilogue<D, CAUSAL, BF16>(p, bar0, tmem, ctl);
+    } else if (warp == 12) {
+        if (lane == 0) q_producer<D, CAUSAL>(&tmK, &tmV, &tmQ, &tmDO, p, sbase, bar0, ctl);
+    } else {
+        if (lane == 0) q_issuer<D, CAUSAL, BF16>(p, sbase, bar0, tmem, ctl);
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 13) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, T::TMEM_COLS);
+    }
+}
+
+// ================================================================ pre pass ==
 // Per query row, padded to whole 128-row blocks: Δ = rowsum(dO ∘ O) in fp32
-// from the input-type values, the lse in base 2 (+inf past Nq, so those
-// columns get P = 0), and a zeroed row of the dQ accumulator.
+// from the input-type values, and the lse in base 2 (+inf past Nq, so those
+// rows and columns get P = 0).  D/8 threads per row, 16 bytes of O and dO each.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
-    constexpr int TPR = D / 8;  // threads per row, 16 bytes of O and of dO each
+    constexpr int TPR = D / 8;
     const int64_t rows = (int64_t)p.Z * p.Hq * p.Tq * 128;
     const int sub = threadIdx.x % TPR;
+    // the trip count is the same for the TPR lanes of a row (rows and the
+    // stride are multiples of 32 / TPR), so the shuffles below see them all
     for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / TPR; r < rows;
          r += (int64_t)gridDim.x * blockDim.x / TPR) {
         const int64_t head = r / ((int64_t)p.Tq * 128);
@@ -524,38 +795,13 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
                 delta = fmaf(fa.x, fb.x, delta);
                 delta = fmaf(fa.y, fb.y, delta);
             }
-            float4* acc = reinterpret_cast<float4*>(p.dq_acc + (head * p.Nq + i) * D) + 2 * sub;
-            acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-            acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        // the row's TPR lanes are consecutive lanes of one warp
 #pragma unroll
         for (int m = TPR / 2; m > 0; m /= 2) delta += __shfl_xor_sync(0xffffffffu, delta, m);
         if (sub == 0) {
             p.delta[r] = delta;
             p.lse2[r] = i < p.Nq ? p.lse[head * p.Nq + i] * 1.4426950408889634f : INFINITY;
         }
-    }
-}
-
-// dQ = scale · accumulator, in the input type; one thread per 8 columns
-template <int D, bool BF16>
-__global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const BwdParams p) {
-    constexpr int C = D / 8;
-    const int64_t items = (int64_t)p.Z * p.Hq * p.Nq * C;
-    for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < items; x += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t r = x / C;
-        const int c = (int)(x - r * C);
-        const int64_t head = r / p.Nq;
-        const int i = (int)(r - head * p.Nq);
-        const int z = (int)(head / p.Hq), hq = (int)(head % p.Hq);
-        const float4* a = reinterpret_cast<const float4*>(p.dq_acc + r * D + 8 * c);
-        const float4 a0 = a[0], a1 = a[1];
-        const float m = p.scale;
-        uint4 out = make_uint4(pack2<BF16>(a0.x * m, a0.y * m), pack2<BF16>(a0.z * m, a0.w * m),
-                               pack2<BF16>(a1.x * m, a1.y * m), pack2<BF16>(a1.z * m, a1.w * m));
-        *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dq) + (int64_t)z * p.sdq_z + (int64_t)hq * p.sdq_h +
-                                  (int64_t)i * p.sdq_n + 8 * c) = out;
     }
 }
 

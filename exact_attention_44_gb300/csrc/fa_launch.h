@@ -41,14 +41,14 @@ struct MergeArgs {
 };
 cudaError_t launch_lse_merge(const MergeArgs& a, bool bf16, int grid, cudaStream_t stream);
 
-// Backward: pre kernel, gradient kernel, dQ conversion on one stream
+// Backward: pre kernel, dK/dV kernel, dQ kernel on one stream
 struct BwdLaunchArgs {
     const CUtensorMap* tmK;
     const CUtensorMap* tmV;
     const CUtensorMap* tmQ;
     const CUtensorMap* tmDO;
     BwdParams params;
-    int grid, pre_grid, post_grid;
+    int grid, grid_q, pre_grid;  // dK/dV kernel, dQ kernel, pre kernel
     cudaStream_t stream;
 };
 cudaError_t launch_bwd_d16(const BwdLaunchArgs& a, bool causal, bool bf16);

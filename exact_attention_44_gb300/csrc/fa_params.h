@@ -73,8 +73,8 @@ struct FwdParams {
 };
 
 // Backward kernel parameters (fa_bwd).  Tensor strides are in elements; the
-// workspace holds the fp32 dQ accumulator and, per query row padded to whole
-// 128-row blocks, the base-2 lse (+inf past Nq) and Delta = rowsum(dO * O).
+// workspace holds, per query row padded to whole 128-row blocks, the base-2
+// lse (+inf past Nq) and Delta = rowsum(dO * O).
 struct BwdParams {
     const void* o;           // forward output, dtype
     const float* lse;        // forward lse (Z, Hq, Nq), natural log
@@ -90,10 +90,10 @@ struct BwdParams {
     int Z, Hq, Hkv, Nq, Nkv;
     int group;               // Hq / Hkv
     int Tq, Tk;              // query blocks of 128 rows, key blocks of 128 keys
-    int nunits;              // Z * Hkv * Tk: one unit = one key block of one kv head
+    int nunits;              // dK/dV units: Z * Hkv * Tk (one key block of one kv head)
+    int nunits_q;            // dQ units: Z * Hq * Tq (one query block of one query head)
     float scale;             // softmax scale (dQ and dK carry it)
     float scale_log2;        // scale * log2(e)
-    float* dq_acc;           // (Z, Hq, Nq, D) fp32
     float* lse2;             // (Z, Hq, Tq * 128) fp32
     float* delta;            // (Z, Hq, Tq * 128) fp32
     uint32_t* status;

@@ -272,15 +272,16 @@ fa_status fa_lse_merge(int nparts, const void* const* o_parts, const float* cons
  *   dq           (Z, Hq, Nq, D) dtype, strides *sdq     (written)
  *   dk, dv       (Z, Hkv, Nkv, D) dtype, strides *sdk, *sdv (written)
  *   workspace    device memory, 256-byte aligned, at least
- *                fa_bwd_workspace_size(Z, Hq, Nq, D) bytes (fp32 dQ
- *                accumulator and per-row Delta / lse); no initialisation
- *                needed, overwritten; not shared by calls that may overlap
+ *                fa_bwd_workspace_size(Z, Hq, Nq, D) bytes (per-row Delta
+ *                and lse); no initialisation needed, overwritten; not shared
+ *                by calls that may overlap
  *
  * Requirements: those of fa_fwd, with D in {16, 32, 64, 128} (D = 256 returns
  * FA_ERR_UNSUPPORTED: dK and dV of a 128-key block live in tensor memory)
  * and Nq >= 1 whenever Z*Hkv*Nkv > 0.  Three kernels on `stream`: Delta and
- * lse per row, the gradients (dQ accumulated with fp32 atomic adds, so dQ
- * may differ in the last bits between runs), and the dQ conversion.
+ * lse per row; dK and dV (one CTA per key block and kv head, over every
+ * query of the group); dQ (one CTA per query block and head, over its keys,
+ * recomputing the scores).  No atomics: results are bitwise reproducible.
  * Errors: those of fa_fwd, plus FA_ERR_WORKSPACE for a missing, misaligned
  * or small workspace.
  */

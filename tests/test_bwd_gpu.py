@@ -120,3 +120,17 @@ def test_long_gqa_causal_sampled_heads():
         g = got.double().cpu().numpy()
         err, mag = float(np.max(np.abs(g - want))), float(np.max(np.abs(want)))
         assert err <= TOL_GRAD[dtype] * mag, f"{name}: {err:.3e} vs {mag:.3e}"
+
+
+def test_bitwise_repeatable():
+    # no atomics: two runs give identical bits for dQ, dK and dV
+    import torch
+    import exact_attention_44_gb300 as fa
+    q, k, v = (to_device(x, "bf16") for x in si.qkv(208, 2, 8, 2, 700, 900, 128, "bf16"))
+    do = to_device(si.normals(1208, 0, 2 * 8 * 700 * 128, "bf16").reshape(2, 8, 700, 128), "bf16")
+    for causal in (False, True):
+        o, lse = fa.fa_fwd(q, k, v, causal=causal)
+        a = fa.fa_bwd(q, k, v, o, lse, do, causal=causal)
+        b = fa.fa_bwd(q, k, v, o, lse, do, causal=causal)
+        torch.cuda.synchronize()
+        assert all(torch.equal(x, y) for x, y in zip(a, b))
