@@ -671,10 +671,19 @@ __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, fl
                         if (k0 + x > kmax || k0 + x < kmin) s[x] = -INFINITY;
                 }
                 if (bias) {
-                    // scaled score plus -slope |i - j|, in log2 units
+                    // scaled score plus -slope |i - j|, in log2 units.  When the
+                    // whole block lies on one side of every row of the tile,
+                    // |i - j| is linear in the key: two FMAs per score.
+                    const float d0 = (float)(q_row - k0);  // i - j at x = 0
+                    if (blast <= ti.q_start || j * BN >= ti.q_start + BM - 1) {
+                        const float sgn = blast <= ti.q_start ? 1.f : -1.f;
+                        const float b0 = slope2 * sgn * d0, step = -slope2 * sgn;
 #pragma unroll
-                    for (int x = 0; x < HC; ++x)
-                        s[x] = fmaf(s[x], c, slope2 * fabsf((float)(q_row - (k0 + x))));
+                        for (int x = 0; x < HC; ++x) s[x] = fmaf(s[x], c, fmaf((float)x, step, b0));
+                    } else {
+#pragma unroll
+                        for (int x = 0; x < HC; ++x) s[x] = fmaf(s[x], c, slope2 * fabsf(d0 - (float)x));
+                    }
                 }
             }
             float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]);
