@@ -218,7 +218,7 @@ bool split_pays(const fa::FwdParams& p, bool causal, int bn, int sms) {
     return (tile_max - split_max) * bn > kSplitGainKeys;
 }
 
-cudaError_t launch_for(int D, const fa::LaunchArgs& a, bool causal, bool bf16, bool variant) {
+cudaError_t launch_for(int D, const fa::LaunchArgs& a, bool causal, bool bf16, int variant) {
     switch (D) {
         case 16: return fa::launch_d16(a, causal, bf16, variant);
         case 32: return fa::launch_d32(a, causal, bf16, variant);
@@ -297,7 +297,7 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* 
     a.tmV = &mv;
     a.stream = stream;
 
-    const cudaError_t err = launch_for(D, a, causal != 0, dtype == FA_DTYPE_BF16, false);
+    const cudaError_t err = launch_for(D, a, causal != 0, dtype == FA_DTYPE_BF16, 0);
     return err == cudaSuccess ? FA_OK : cuda_fail("forward launch", err);
 }
 
@@ -376,7 +376,8 @@ fa_status fwd_ex_impl(const void* q, const void* k, const void* v, void* o, floa
     a.tmK = &mk;
     a.tmV = &mv;
     a.stream = stream;
-    return launch_for(D, a, causal != 0, dtype == FA_DTYPE_BF16, true) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    const cudaError_t err = launch_for(D, a, causal != 0, dtype == FA_DTYPE_BF16, p.alibi != nullptr ? 2 : 1);
+    return err == cudaSuccess ? FA_OK : cuda_fail("variant forward launch", err);
 }
 
 }  // namespace

@@ -7,7 +7,7 @@
 
 namespace fa {
 
-template <bool CAUSAL, bool BF16, bool VAR>
+template <bool CAUSAL, bool BF16, int VAR>
 static cudaError_t launch_one(const LaunchArgs& a) {
     auto kernel = fa_fwd_kernel<64, CAUSAL, BF16, VAR>;
     constexpr int smem = Traits<64>::SMEM_BYTES;
@@ -25,7 +25,7 @@ static cudaError_t launch_one(const LaunchArgs& a) {
     kernel<<<a.grid, NUM_THREADS, smem, a.stream>>>(*a.tmQ, *a.tmK, *a.tmV, a.params);
     err = cudaGetLastError();
     // split schedule: one merge block per cut between CTA ranges, same stream
-    if constexpr (!VAR) {
+    if constexpr (VAR == 0) {
         if (err == cudaSuccess && a.params.split && a.grid > 1) {
             fa_split_merge_kernel<64, CAUSAL, BF16><<<a.grid - 1, MERGE_THREADS, 0, a.stream>>>(a.params, a.grid);
             err = cudaGetLastError();
@@ -34,13 +34,18 @@ static cudaError_t launch_one(const LaunchArgs& a) {
     return err;
 }
 
-cudaError_t launch_d64(const LaunchArgs& a, bool causal, bool bf16, bool variant) {
-    if (variant) {
-        if (causal) return bf16 ? launch_one<true, true, true>(a) : launch_one<true, false, true>(a);
-        return bf16 ? launch_one<false, true, true>(a) : launch_one<false, false, true>(a);
+// variant 0: fa_fwd; 1: window / variable length; 2: the same with ALiBi
+cudaError_t launch_d64(const LaunchArgs& a, bool causal, bool bf16, int variant) {
+    if (variant == 2) {
+        if (causal) return bf16 ? launch_one<true, true, 2>(a) : launch_one<true, false, 2>(a);
+        return bf16 ? launch_one<false, true, 2>(a) : launch_one<false, false, 2>(a);
     }
-    if (causal) return bf16 ? launch_one<true, true, false>(a) : launch_one<true, false, false>(a);
-    return bf16 ? launch_one<false, true, false>(a) : launch_one<false, false, false>(a);
+    if (variant == 1) {
+        if (causal) return bf16 ? launch_one<true, true, 1>(a) : launch_one<true, false, 1>(a);
+        return bf16 ? launch_one<false, true, 1>(a) : launch_one<false, false, 1>(a);
+    }
+    if (causal) return bf16 ? launch_one<true, true, 0>(a) : launch_one<true, false, 0>(a);
+    return bf16 ? launch_one<false, true, 0>(a) : launch_one<false, false, 0>(a);
 }
 
 }  // namespace fa

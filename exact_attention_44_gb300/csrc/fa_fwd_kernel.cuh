@@ -357,7 +357,7 @@ struct Sched {
 // tile's first K: its slot held the tile before, whose last S is complete by
 // the time the second K's slot frees anyway.
 
-template <int D, bool CAUSAL, bool VAR>
+template <int D, bool CAUSAL, int VAR>
 __device__ void run_producer_qk(const CUtensorMap* tmQ, const CUtensorMap* tmK, const FwdParams& p, uint32_t sbase,
                                 uint32_t bar0, const Ctl& ctl) {
     using T = Traits<D>;
@@ -378,7 +378,7 @@ __device__ void run_producer_qk(const CUtensorMap* tmQ, const CUtensorMap* tmK, 
         ++qi;
         return true;
     };
-    const Sched<CAUSAL, T::BN, VAR> sc(p);
+    const Sched<CAUSAL, T::BN, (VAR != 0)> sc(p);
     int64_t pos = sc.first(p);
     if (sc.valid(pos, p)) ok = load_q(sc.seg(pos, p));
     while (ok && sc.valid(pos, p)) {
@@ -421,7 +421,7 @@ __device__ void run_producer_qk(const CUtensorMap* tmQ, const CUtensorMap* tmK, 
     }
 }
 
-template <int D, bool CAUSAL, bool VAR>
+template <int D, bool CAUSAL, int VAR>
 __device__ void run_producer_v(const CUtensorMap* tmV, const FwdParams& p, uint32_t sbase, uint32_t bar0,
                                const Ctl& ctl) {
     using T = Traits<D>;
@@ -429,7 +429,7 @@ __device__ void run_producer_v(const CUtensorMap* tmV, const FwdParams& p, uint3
     const uint64_t pol_kv = ptx::policy_evict_last();
     uint32_t vi = 0;
     bool ok = true;
-    const Sched<CAUSAL, T::BN, VAR> sc(p);
+    const Sched<CAUSAL, T::BN, (VAR != 0)> sc(p);
     for (int64_t pos = sc.first(p); ok && sc.valid(pos, p);) {
         const Seg sg = sc.seg(pos, p);
         for (int j = sg.jb; j < sg.je; ++j) {
@@ -461,7 +461,7 @@ __device__ void run_producer_v(const CUtensorMap* tmV, const FwdParams& p, uint3
 // Descriptors are a per-stage base word plus a compile-time offset.
 
 // S_g = Q K_gᵀ ("Write Triton Attention Kernel", step 5b) into S[g & 1]
-template <int D, bool CAUSAL, bool BF16, bool VAR>
+template <int D, bool CAUSAL, bool BF16, int VAR>
 __device__ void run_mma_qk(const FwdParams& p, uint32_t sbase, uint32_t bar0, uint32_t tmem, const Ctl& ctl) {
     using T = Traits<D>;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
@@ -471,7 +471,7 @@ __device__ void run_mma_qk(const FwdParams& p, uint32_t sbase, uint32_t bar0, ui
     const uint32_t k_lo0 = ptx::smem_desc_lo(sbase + T::OFF_K, 16);
     uint32_t qi = 0, g = 0;  // Q tiles and S blocks issued
     bool ok = true;
-    const Sched<CAUSAL, T::BN, VAR> sc(p);
+    const Sched<CAUSAL, T::BN, (VAR != 0)> sc(p);
     for (int64_t pos = sc.first(p); ok && sc.valid(pos, p);) {
         const Seg sg = sc.seg(pos, p);
         pos = sc.next(pos, sg, p);
@@ -513,7 +513,7 @@ __device__ void run_mma_qk(const FwdParams& p, uint32_t sbase, uint32_t bar0, ui
 
 // O += P_g V_g (step 5h); the first block of a segment overwrites O, once
 // the epilogue has read the previous segment's O out of TMEM
-template <int D, bool CAUSAL, bool BF16, bool VAR>
+template <int D, bool CAUSAL, bool BF16, int VAR>
 __device__ void run_mma_pv(const FwdParams& p, uint32_t sbase, uint32_t bar0, uint32_t tmem, const Ctl& ctl) {
     using T = Traits<D>;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
@@ -522,7 +522,7 @@ __device__ void run_mma_pv(const FwdParams& p, uint32_t sbase, uint32_t bar0, ui
     const uint32_t v_lo0 = ptx::smem_desc_lo(sbase + T::OFF_V, T::BN * T::SW);  // LBO: next column chunk of V
     uint32_t g = 0, ntile = 0;
     bool ok = true;
-    const Sched<CAUSAL, T::BN, VAR> sc(p);
+    const Sched<CAUSAL, T::BN, (VAR != 0)> sc(p);
     for (int64_t pos = sc.first(p); ok && sc.valid(pos, p); ++ntile) {
         const Seg sg = sc.seg(pos, p);
         pos = sc.next(pos, sg, p);
@@ -600,7 +600,7 @@ __device__ __forceinline__ void rescale_o(uint32_t taddr, float alpha) {
 // = query row = TMEM lane; the two halves swap partial row maxima through
 // shared memory, so both reference the same maximum m, and each keeps its
 // own partial denominator (the epilogue adds them).
-template <int D, bool CAUSAL, bool BF16, bool VAR>
+template <int D, bool CAUSAL, bool BF16, int VAR>
 __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, float* hand, float* red, int h,
                             const Ctl& ctl) {
     using T = Traits<D>;
@@ -611,19 +611,21 @@ __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, fl
     const int row = quad * 32 + threadIdx.x % 32;
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
     const float c = p.scale_log2;
-    // with an ALiBi bias the scores are scaled and biased in place (units of
-    // log2), so the maximum and the exponentials take them as they are
-    const bool bias = VAR && p.alibi != nullptr;
+    // with an ALiBi bias (the VAR == 2 instantiation) the scores are scaled
+    // and biased in place (units of log2), so the maximum and the
+    // exponentials take them as they are
+    constexpr bool bias = VAR == 2;
     const float cm = bias ? 1.f : c;
     const uint64_t c2 = ptx::pack_f32x2(cm, cm);
     uint32_t step = 0, ntile = 0;
 
-    const Sched<CAUSAL, BN, VAR> sc(p);
+    const Sched<CAUSAL, BN, (VAR != 0)> sc(p);
     for (int64_t pos = sc.first(p); sc.valid(pos, p); ++ntile) {
         const Seg ti = sc.seg(pos, p);
         pos = sc.next(pos, ti, p);
         const int q_row = ti.q_start + row;
-        const float slope2 = bias ? -__ldg(p.alibi + ti.hq) * 1.4426950408889634f : 0.f;
+        float slope2 = 0.f;
+        if constexpr (bias) slope2 = -__ldg(p.alibi + ti.hq) * 1.4426950408889634f;
         // running max (log2 units of the scaled score) and denominator, fp32
         // ("Write Triton Attention Kernel", step 4; the initial l is 0)
         float m = -INFINITY, l = 0.f;
@@ -670,7 +672,7 @@ __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, fl
                     for (int x = 0; x < HC; ++x)
                         if (k0 + x > kmax || k0 + x < kmin) s[x] = -INFINITY;
                 }
-                if (bias) {
+                if constexpr (bias) {
                     // scaled score plus -slope |i - j|, in log2 units.  When the
                     // whole block lies on one side of every row of the tile,
                     // |i - j| is linear in the key: two FMAs per score.
@@ -772,7 +774,7 @@ __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, fl
 // O = acc / l in the input type, lse = m + log(l) in natural-log units
 // ("Write Triton Attention Kernel", steps 6-8).  O is read out of TMEM and
 // converted first, TMEM is handed back to the MMA warp, then rows are stored.
-template <int D, bool CAUSAL, bool BF16, bool VAR>
+template <int D, bool CAUSAL, bool BF16, int VAR>
 __device__ void run_epilogue(const FwdParams& p, uint32_t bar0, uint32_t tmem, const float* hand, const Ctl& ctl) {
     using T = Traits<D>;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
@@ -782,7 +784,7 @@ __device__ void run_epilogue(const FwdParams& p, uint32_t bar0, uint32_t tmem, c
     uint32_t step = 0, ntile = 0;
     constexpr int CH = D >= 32 ? 32 : 16;               // columns per TMEM load
     constexpr int HELD = D <= 128 ? D / CH : 64 / CH;    // chunks converted before their stores
-    const Sched<CAUSAL, T::BN, VAR> sc(p);
+    const Sched<CAUSAL, T::BN, (VAR != 0)> sc(p);
     for (int64_t pos = sc.first(p); sc.valid(pos, p); ++ntile) {
         const Seg ti = sc.seg(pos, p);
         pos = sc.next(pos, ti, p);
@@ -864,7 +866,7 @@ __device__ void run_epilogue(const FwdParams& p, uint32_t bar0, uint32_t tmem, c
 }
 
 // ------------------------------------------------------------ kernel --------
-template <int D, bool CAUSAL, bool BF16, bool VAR>
+template <int D, bool CAUSAL, bool BF16, int VAR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {

@@ -19,13 +19,14 @@ struct LaunchArgs {
     cudaStream_t stream;
 };
 
-// Launch fa_fwd_kernel<D, causal, bf16, variant> (and the split merge when the
+// Launch fa_fwd_kernel<D, causal, bf16, variant> (variant 0: fa_fwd, 1:
+// window / variable length, 2: with ALiBi; and the split merge when the
 // parameters ask for the split schedule); returns the launches' error code.
-cudaError_t launch_d16(const LaunchArgs& a, bool causal, bool bf16, bool variant);
-cudaError_t launch_d32(const LaunchArgs& a, bool causal, bool bf16, bool variant);
-cudaError_t launch_d64(const LaunchArgs& a, bool causal, bool bf16, bool variant);
-cudaError_t launch_d128(const LaunchArgs& a, bool causal, bool bf16, bool variant);
-cudaError_t launch_d256(const LaunchArgs& a, bool causal, bool bf16, bool variant);
+cudaError_t launch_d16(const LaunchArgs& a, bool causal, bool bf16, int variant);
+cudaError_t launch_d32(const LaunchArgs& a, bool causal, bool bf16, int variant);
+cudaError_t launch_d64(const LaunchArgs& a, bool causal, bool bf16, int variant);
+cudaError_t launch_d128(const LaunchArgs& a, bool causal, bool bf16, int variant);
+cudaError_t launch_d256(const LaunchArgs& a, bool causal, bool bf16, int variant);
 
 // fa_lse_merge: parts share one layout; rows = Z * H * N
 constexpr int MERGE_MAX_PARTS = 16;
