@@ -22,13 +22,30 @@ static cudaError_t launch_one(const LaunchArgs& a) {
         if (err != cudaSuccess) return err;
         configured.fetch_or(bit);
     }
-    kernel<<<a.grid, NUM_THREADS, smem, a.stream>>>(*a.tmQ, *a.tmK, *a.tmV, a.params);
-    err = cudaGetLastError();
+    // programmatic dependent launch: the kernel's set-up may overlap the tail
+    // of the previous kernel on the stream (it waits for it before any
+    // global memory access)
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.grid);
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = a.stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    err = cudaLaunchKernelEx(&cfg, kernel, *a.tmQ, *a.tmK, *a.tmV, a.params);
     // split schedule: one merge block per cut between CTA ranges, same stream
     if constexpr (VAR == 0) {
         if (err == cudaSuccess && a.params.split && a.grid > 1) {
-            fa_split_merge_kernel<256, CAUSAL, BF16><<<a.grid - 1, MERGE_THREADS, 0, a.stream>>>(a.params, a.grid);
-            err = cudaGetLastError();
+            cudaLaunchConfig_t mcfg = {};
+            mcfg.gridDim = dim3(a.grid - 1);
+            mcfg.blockDim = dim3(MERGE_THREADS);
+            mcfg.stream = a.stream;
+            mcfg.attrs = attr;
+            mcfg.numAttrs = 1;
+            err = cudaLaunchKernelEx(&mcfg, fa_split_merge_kernel<256, CAUSAL, BF16>, a.params, a.grid);
         }
     }
     return err;

@@ -898,6 +898,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const Ctl ctl{abort_flag, p.status, p.wait_limit_ns};
+    // launched as a programmatic dependent of the previous kernel on the
+    // stream: the set-up above overlaps its tail, nothing below touches
+    // global memory before it has completed
+    ptx::grid_dependency_wait();
+    ptx::grid_launch_dependents();
 
     if (warp == 0) {
         if (lane == 0) run_producer_qk<D, CAUSAL, VAR>(&tmQ, &tmK, p, sbase, bar0, ctl);
@@ -937,6 +942,7 @@ constexpr int MERGE_THREADS = 4 * BM;
 template <int D, bool CAUSAL, bool BF16>
 __global__ void __launch_bounds__(MERGE_THREADS) fa_split_merge_kernel(const FwdParams p, int grid) {
     using S = Sched<CAUSAL, Traits<D>::BN>;
+    ptx::grid_dependency_wait();  // the parts are written by the launch before
     const int64_t b = (int64_t)blockIdx.x + 1;
     const int64_t xb = S::range_lo(b, grid, p);
     int64_t head;
