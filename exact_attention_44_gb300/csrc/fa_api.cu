@@ -228,12 +228,46 @@ cudaError_t launch_for(int D, const fa::LaunchArgs& a, bool causal, bool bf16, i
     }
 }
 
+// GQA packing.  Without a causal mask a query row's result does not depend on
+// its position, so the g query heads that share a key/value head can be run
+// as one head of g * Nq rows against that K/V: each key block is then loaded
+// and multiplied once per group instead of once per query head.  Done when
+// the rows of a group are short (Nq < 128: decode-like and few-query shapes)
+// and the layout allows the view: a query head's rows follow the previous
+// head's (h-stride = Nq * n-stride), batches follow whole head sets, and K/V
+// heads are evenly strided within a batch.  The lse layout (Z, Hq, Nq)
+// contiguous is the same memory as (Z * Hkv, 1, g * Nq).
+bool gqa_pack_view(int Z, int Hq, int Hkv, int Nq, int causal, const fa_strides* sq, const fa_strides* sk,
+                   const fa_strides* sv, const fa_strides* so, fa_strides* pq, fa_strides* pk, fa_strides* pv,
+                   fa_strides* po) {
+    const int g = Hkv > 0 ? Hq / Hkv : 0;
+    if (causal || g < 2 || Nq >= fa::BM || Nq < 1) return false;
+    if (!sq || !sk || !sv || !so) return false;
+    auto rows_follow = [&](const fa_strides* s) {
+        return s->d == 1 && s->h == (int64_t)Nq * s->n && (Z <= 1 || s->b == (int64_t)Hq * s->h);
+    };
+    auto kv_even = [&](const fa_strides* s) { return s->d == 1 && (Z <= 1 || s->b == (int64_t)Hkv * s->h); };
+    if (!rows_follow(sq) || !rows_follow(so) || !kv_even(sk) || !kv_even(sv)) return false;
+    // batch index z * Hkv + hk; one head; rows gi * Nq + n
+    *pq = fa_strides{(int64_t)g * sq->h, 0, sq->n, 1};
+    *po = fa_strides{(int64_t)g * so->h, 0, so->n, 1};
+    *pk = fa_strides{sk->h, 0, sk->n, 1};
+    *pv = fa_strides{sv->h, 0, sv->n, 1};
+    return true;
+}
+
 fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int Z, int Hq, int Hkv, int Nq,
                    int Nkv, int D, const fa_strides* sq, const fa_strides* sk, const fa_strides* sv,
                    const fa_strides* so, float scale, int causal, fa_dtype dtype, cudaStream_t stream, bool split,
                    void* workspace, size_t workspace_bytes) {
     fa_status st = check_shape(Z, Hq, Hkv, Nq, Nkv, D, causal);
     if (st != FA_OK) return st;
+    fa_strides pq, pk, pv, po;
+    if ((int64_t)Z * Hq * Nq > 0 && gqa_pack_view(Z, Hq, Hkv, Nq, causal, sq, sk, sv, so, &pq, &pk, &pv, &po)) {
+        // the same problem seen as Z * Hkv heads of g * Nq query rows (validated as such)
+        return fwd_impl(q, k, v, o, lse, Z * Hkv, 1, 1, Nq * (Hq / Hkv), Nkv, D, &pq, &pk, &pv, &po, scale, causal,
+                        dtype, stream, split, workspace, workspace_bytes);
+    }
     if (dtype != FA_DTYPE_F16 && dtype != FA_DTYPE_BF16) return FA_ERR_UNSUPPORTED;
     if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;  // a softmax temperature is positive
     if ((int64_t)Z * Hq * Nq == 0) return FA_OK;

@@ -134,3 +134,17 @@ def test_automatic_choice(shape, causal):
         check_full(41, *shape, causal, impl="splitkv")
     finally:
         fa.fa_debug_force_split(1)
+
+
+@pytest.mark.parametrize("Z,Hq,Hkv,Nq,Nkv", [(1, 8, 2, 1, 3000), (2, 8, 2, 5, 1000), (3, 16, 2, 16, 700),
+                                             (1, 32, 4, 31, 2049), (2, 4, 2, 100, 513), (1, 8, 8, 1, 900)])
+@pytest.mark.parametrize("impl", ["fwd", "splitkv"])
+def test_gqa_packed_short_queries(Z, Hq, Hkv, Nq, Nkv, impl):
+    # non-causal, Nq < 128, contiguous: the g query heads of a group run as one
+    # head of g * Nq rows (the last case, g = 1, is not packed)
+    check_full(42, Z, Hq, Hkv, Nq, Nkv, 128, "bf16", False, impl=impl)
+
+
+def test_gqa_pack_skipped_for_other_layouts_and_causal():
+    check_full(43, 2, 8, 2, 7, 800, 64, "fp16", False, layout="bsnd", impl="splitkv")
+    check_full(44, 2, 8, 2, 7, 800, 64, "fp16", True, impl="splitkv")
