@@ -30,7 +30,7 @@ static cudaError_t launch_one(const LaunchArgs& a) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.grid);
-    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.blockDim = dim3(Traits<128>::THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = a.stream;
     cfg.attrs = attr;

@@ -14,18 +14,19 @@
 //     128-row query tiles, or, in split mode, one equal range of
 //     (tile, key block) pairs per CTA whose cut tiles a second kernel merges;
 //   * warp 0 (one lane) streams Q once per segment and K_j per key block, warp
-//     15 (one lane) V_j, by TMA into swizzled shared-memory rings guarded by
+//     3 (one lane) V_j, by TMA into swizzled shared-memory rings guarded by
 //     mbarriers;
 //   * warp 1 (one lane) issues S_g = Q K_gᵀ into a three-slot ring in TMEM,
 //     warp 2 (one lane) O += P_g V_g with P_g read from the same slot; each
 //     commits to mbarriers, so S of later blocks runs while the softmax works;
-//   * warps 3-10 (two column halves x 128 threads, thread = query row = TMEM
-//     lane) run the online softmax: mask (diagonal and tail blocks only), row
-//     max swapped between the halves, exp2, row sum, P -> fp16/bf16 into TMEM;
+//   * warps 4 .. 4 + 4 NG - 1 (NG column groups x 128 threads, thread = query
+//     row = TMEM lane) run the online softmax: mask (diagonal and tail blocks
+//     only), row max swapped between the groups, exp2, row sum, P -> fp16/bf16
+//     into TMEM;
 //     O is rescaled in TMEM only when a row maximum grows by more than
 //     2^RESCALE_LOG2 (below that the stale maximum keeps every
 //     p <= 2^RESCALE_LOG2, and O / l and lse are unchanged);
-//   * warps 11-14 run the epilogue of the previous segment while the softmax
+//   * the last 4 warps run the epilogue of the previous segment while the softmax
 //     warps start the next: read O out of TMEM, release it to the P·V issuer,
 //     then O / l -> global and lse = (m + log2 l)·ln 2 (or the part's O / l
 //     and base-2 lse -> workspace).
@@ -75,23 +76,29 @@ struct Traits {
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + Q_STAGES * Q_BYTES;
     static constexpr int OFF_V = OFF_K + KV_STAGES * KV_BYTES;
-    // softmax -> epilogue hand-over, 2 slots of {m, l of half 0, l of half 1} per row
+    // softmax -> epilogue hand-over, 2 slots of {m, l of each column group} per row
+    // softmax column groups: four keep each thread's chain per key block
+    // short; at D = 256 two (the 64-key blocks are narrow, and four groups
+    // of 768 threads leave too few registers for the 256-column epilogue)
+    static constexpr int NG = D == 256 ? 2 : 4;
+    static constexpr int THREADS = fwd_threads(NG);
+    static constexpr int HAND_ROWS = 1 + NG;
     static constexpr int OFF_HAND = OFF_V + KV_STAGES * KV_BYTES;
-    // partial row maxima of the two column halves, 2 slots (by block parity)
-    static constexpr int OFF_RED = OFF_HAND + 2 * 3 * BM * 4;
-    static constexpr int OFF_BAR = OFF_RED + 2 * 2 * BM * 4;
+    // partial row maxima of the column groups, 2 slots (by block parity)
+    static constexpr int OFF_RED = OFF_HAND + 2 * HAND_ROWS * BM * 4;
+    static constexpr int OFF_BAR = OFF_RED + 2 * NG * BM * 4;
     // barrier indices
     static constexpr int B_QFULL = 0;
     static constexpr int B_QEMPTY = B_QFULL + Q_STAGES;
     static constexpr int B_KFULL = B_QEMPTY + Q_STAGES;        // [2] K tile landed (TMA)
     static constexpr int B_VFULL = B_KFULL + KV_STAGES;        // [2] V tile landed (TMA)
     static constexpr int B_SFULL = B_VFULL + KV_STAGES;        // [SR] S_g ready; K slot free (commit)
-    static constexpr int B_PFULL = B_SFULL + SR;               // [SR] P_g written (256 softmax threads)
+    static constexpr int B_PFULL = B_SFULL + SR;               // [SR] P_g written (all softmax threads)
     static constexpr int B_PVDONE = B_PFULL + SR;              // [SR] O += P_g V_g complete; slot and V slot free (commit)
-    static constexpr int B_EPIFULL = B_PVDONE + SR;            // [2] m, l of a tile handed over (256)
+    static constexpr int B_EPIFULL = B_PVDONE + SR;            // [2] m, l of a tile handed over (softmax threads)
     static constexpr int B_EPIEMPTY = B_EPIFULL + 2;           // [2] hand-over slot read (128)
     static constexpr int B_OFREE = B_EPIEMPTY + 2;             // O read out of TMEM (128)
-    static constexpr int B_RED = B_OFREE + 1;                  // [2] both halves' partial maxima written (256)
+    static constexpr int B_RED = B_OFREE + 1;                  // [2] every group's partial maxima written
     static constexpr int B_DRAIN = B_RED + 2;                  // [2] teardown of the two MMA issuers
     static constexpr int NUM_BARS = B_DRAIN + 2;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;    // tmem base, abort flag
@@ -101,10 +108,10 @@ struct Traits {
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
     static __device__ __forceinline__ uint32_t bar_count(int i) {
-        if (i >= B_PFULL && i < B_PFULL + SR) return 256;
-        if (i >= B_EPIFULL && i < B_EPIFULL + 2) return 256;
+        if (i >= B_PFULL && i < B_PFULL + SR) return 128 * NG;
+        if (i >= B_EPIFULL && i < B_EPIFULL + 2) return 128 * NG;
         if (i >= B_EPIEMPTY && i < B_OFREE + 1) return 128;
-        if (i >= B_RED && i < B_RED + 2) return 256;
+        if (i >= B_RED && i < B_RED + 2) return 128 * NG;
         return 1;
     }
 };
@@ -587,25 +594,33 @@ __device__ __forceinline__ void rescale_o(uint32_t taddr, float alpha) {
 #pragma unroll
         for (int x = 0; x < 16; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * alpha);
         ptx::tmem_st16(taddr, r);
-    } else {
+    } else if constexpr (NCOL == 8) {
         uint32_t r[8];
         ptx::tmem_ld8(taddr, r);
 #pragma unroll
         for (int x = 0; x < 8; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * alpha);
         ptx::tmem_st8(taddr, r);
+    } else {
+        uint32_t r[4];
+        ptx::tmem_ld4(taddr, r);
+#pragma unroll
+        for (int x = 0; x < 4; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * alpha);
+        ptx::tmem_st4(taddr, r);
     }
 }
 
-// Online softmax for one column half of every key block: 128 threads, thread
-// = query row = TMEM lane; the two halves swap partial row maxima through
-// shared memory, so both reference the same maximum m, and each keeps its
-// own partial denominator (the epilogue adds them).
+// Online softmax for one column group of every key block: 128 threads, thread
+// = query row = TMEM lane; the groups swap partial row maxima through shared
+// memory, so all reference the same maximum m, and each keeps its own
+// partial denominator (the epilogue adds them).
 template <int D, bool CAUSAL, bool BF16, int VAR>
 __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, float* hand, float* red, int h,
                             const Ctl& ctl) {
     using T = Traits<D>;
     constexpr int BN = T::BN;
-    constexpr int HC = BN / 2;                 // score columns per thread
+    constexpr int NG = T::NG;                  // column groups; h is this thread's
+    constexpr int HC = BN / NG;                // score columns per thread
+    static_assert(HC == 16 || HC == 32, "column group width");
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     const int quad = (threadIdx.x / 32) % 4;  // TMEM lane quadrant this warp may access
     const int row = quad * 32 + threadIdx.x % 32;
@@ -636,12 +651,12 @@ __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, fl
             ptx::tc_fence_after();
             const uint32_t s_addr = tmem + lane_addr + T::TM_S + r * BN;
             float s[HC];
+            {
+                uint32_t rr[HC];
+                if constexpr (HC == 32) ptx::tmem_ld32(s_addr + h * HC, rr);
+                else ptx::tmem_ld16(s_addr + h * HC, rr);
 #pragma unroll
-            for (int i = 0; i < HC / 32; ++i) {
-                uint32_t rr[32];
-                ptx::tmem_ld32(s_addr + h * HC + 32 * i, rr);
-#pragma unroll
-                for (int x = 0; x < 32; ++x) s[32 * i + x] = __uint_as_float(rr[x]);
+                for (int x = 0; x < HC; ++x) s[x] = __uint_as_float(rr[x]);
             }
             // the mask goes on the scores before the row max (Correctness
             // requirements); only the diagonal block and the key tail need it
@@ -694,21 +709,28 @@ __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, fl
                 mx0 = ptx::fmax3(mx0, s[x], s[x + 1]);
                 mx1 = ptx::fmax3(mx1, s[x + 2], s[x + 3]);
             }
-            // Swap partial maxima with the other half.  Arriving also says this
-            // thread's S is in registers: P is written over the slot's first
-            // columns only once both halves have arrived.  (Exchange slot b is
-            // free: every thread read it two blocks ago before arriving last block.)
+            // Swap partial maxima with the other groups.  Arriving also says
+            // this thread's S is in registers: P is written over the slot's
+            // first columns only once every group has arrived.  (Exchange slot
+            // b is free: every thread read it two blocks ago before arriving
+            // last block.)
             const float pmax = fmaxf(mx0, mx1);
-            red[(b * 2 + h) * BM + row] = pmax;
+            red[(b * NG + h) * BM + row] = pmax;
             ptx::mbar_arrive(bar(T::B_RED + b));
+            auto block_max = [&]() {
+                float mm = pmax;
+#pragma unroll
+                for (int g2 = 0; g2 < NG; ++g2) mm = fmaxf(mm, red[(b * NG + g2) * BM + row]);
+                return mm * cm;  // scale > 0
+            };
             if (j == ti.jb) {
                 // the first block sets the reference maximum m
                 if (!warp_wait_phase(bar(T::B_RED + b), ph, ctl, SITE_MAX_XCHG)) return;
-                m = fmaxf(pmax, red[(b * 2 + (h ^ 1)) * BM + row]) * cm;  // scale > 0
+                m = block_max();
             }
             // p = 2^(s·scale·log2e − m) against the current reference m; l sums
             // the fp32 p, P V uses p cast to the input type
-            constexpr int NP = HC / 2;  // packed P columns of this half
+            constexpr int NP = HC / 2;  // packed P columns of this group
             uint32_t pk[NP];
             auto exps = [&](float ref) -> uint64_t {
                 // a row with no kept key so far (only in a segment that starts
@@ -735,7 +757,7 @@ __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, fl
                 // this block is added to them (Kernel design rules).  Both
                 // halves see the same values, so both take the same branch.
                 if (!warp_wait_phase(bar(T::B_RED + b), ph, ctl, SITE_MAX_XCHG)) return;
-                const float m_tile = fmaxf(pmax, red[(b * 2 + (h ^ 1)) * BM + row]) * cm;
+                const float m_tile = block_max();
                 if (__any_sync(0xffffffffu, m_tile > m + RESCALE_LOG2)) {
                     const float m_new = fmaxf(m, m_tile);
                     // a row that has kept no key yet (m = -inf) has l = 0 and
@@ -747,12 +769,12 @@ __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, fl
                     if (!warp_wait_phase(bar(T::B_PVDONE + rslot<T::SR>(g)), rphase<T::SR>(g), ctl, SITE_PV_DONE))
                         return;
                     ptx::tc_fence_after();
-                    rescale_o<D / 2>(tmem + lane_addr + T::TM_O + h * (D / 2), alpha);
+                    rescale_o<D / NG>(tmem + lane_addr + T::TM_O + h * (D / NG), alpha);
                 }
             }
             // P_j over the first BN/2 columns of its slot: keys h*HC.. at packed column h*HC/2
-            if constexpr (NP == 32) ptx::tmem_st32(s_addr + h * NP, pk);
-            else ptx::tmem_st16(s_addr + h * NP, pk);
+            if constexpr (NP == 16) ptx::tmem_st16(s_addr + h * NP, pk);
+            else ptx::tmem_st8(s_addr + h * NP, pk);
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(T::B_PFULL + r));
@@ -764,8 +786,8 @@ __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, fl
         // hand m and this half's l to the epilogue warps
         const uint32_t slot = ntile & 1u;
         if (!warp_wait_phase(bar(T::B_EPIEMPTY + slot), ((ntile >> 1) & 1u) ^ 1u, ctl, SITE_EPI_EMPTY)) return;
-        if (h == 0) hand[slot * 3 * BM + row] = m;
-        hand[slot * 3 * BM + (1 + h) * BM + row] = l;
+        if (h == 0) hand[slot * T::HAND_ROWS * BM + row] = m;
+        hand[slot * T::HAND_ROWS * BM + (1 + h) * BM + row] = l;
         ptx::mbar_arrive(bar(T::B_EPIFULL + slot));
     }
 }
@@ -783,7 +805,7 @@ __device__ void run_epilogue(const FwdParams& p, uint32_t bar0, uint32_t tmem, c
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
     uint32_t step = 0, ntile = 0;
     constexpr int CH = D >= 32 ? 32 : 16;               // columns per TMEM load
-    constexpr int HELD = D <= 128 ? D / CH : 64 / CH;    // chunks converted before their stores
+    constexpr int HELD = D / CH < 2 ? D / CH : 2;        // chunks converted before their stores
     const Sched<CAUSAL, T::BN, (VAR != 0)> sc(p);
     for (int64_t pos = sc.first(p); sc.valid(pos, p); ++ntile) {
         const Seg ti = sc.seg(pos, p);
@@ -791,8 +813,10 @@ __device__ void run_epilogue(const FwdParams& p, uint32_t bar0, uint32_t tmem, c
         step += ti.je - ti.jb;
         const uint32_t slot = ntile & 1u;
         if (!warp_wait_phase(bar(T::B_EPIFULL + slot), (ntile >> 1) & 1u, ctl, SITE_EPI_FULL)) return;
-        const float m = hand[slot * 3 * BM + row];
-        const float l = hand[slot * 3 * BM + BM + row] + hand[slot * 3 * BM + 2 * BM + row];
+        const float m = hand[slot * T::HAND_ROWS * BM + row];
+        float l = 0.f;
+#pragma unroll
+        for (int g2 = 0; g2 < T::NG; ++g2) l += hand[slot * T::HAND_ROWS * BM + (1 + g2) * BM + row];
         ptx::mbar_arrive(bar(T::B_EPIEMPTY + slot));
         const uint32_t g = step - 1;  // the tile's last P·V
         if (!warp_wait_phase(bar(T::B_PVDONE + rslot<T::SR>(g)), rphase<T::SR>(g), ctl, SITE_PV_DONE)) return;
@@ -867,7 +891,7 @@ __device__ void run_epilogue(const FwdParams& p, uint32_t bar0, uint32_t tmem, c
 
 // ------------------------------------------------------------ kernel --------
 template <int D, bool CAUSAL, bool BF16, int VAR>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(Traits<D>::THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
     using T = Traits<D>;
@@ -904,17 +928,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::grid_dependency_wait();
     ptx::grid_launch_dependents();
 
+    constexpr int SOFTMAX_END = 4 + 4 * T::NG;  // warps 4 .. SOFTMAX_END - 1: softmax; then 4 epilogue warps
     if (warp == 0) {
         if (lane == 0) run_producer_qk<D, CAUSAL, VAR>(&tmQ, &tmK, p, sbase, bar0, ctl);
-    } else if (warp == 15) {
+    } else if (warp == 3) {
         if (lane == 0) run_producer_v<D, CAUSAL, VAR>(&tmV, p, sbase, bar0, ctl);
     } else if (warp == 1) {
         if (lane == 0) run_mma_qk<D, CAUSAL, BF16, VAR>(p, sbase, bar0, tmem, ctl);
     } else if (warp == 2) {
         if (lane == 0) run_mma_pv<D, CAUSAL, BF16, VAR>(p, sbase, bar0, tmem, ctl);
-    } else if (warp < 11) {
-        run_softmax<D, CAUSAL, BF16, VAR>(p, bar0, tmem, hand, red, (warp - 3) / 4, ctl);
-    } else if (warp < 15) {
+    } else if (warp < SOFTMAX_END) {
+        run_softmax<D, CAUSAL, BF16, VAR>(p, bar0, tmem, hand, red, (warp - 4) / 4, ctl);
+    } else {
         run_epilogue<D, CAUSAL, BF16, VAR>(p, bar0, tmem, hand, ctl);
     }
 

@@ -6,10 +6,11 @@
 namespace fa {
 
 constexpr int BM = 128;            // query rows per tile (one TMEM lane per row)
-// warp 0: Q/K loads, warp 1: S = Q Kᵀ issuer, warp 2: O += P V issuer, warps
-// 3-6 and 7-10: softmax of the two column halves of each key block, warps
-// 11-14: epilogue, warp 15: V loads
-constexpr int NUM_THREADS = 512;
+// Warp roles of the forward kernel: warp 0: Q/K loads, warp 1: S = Q Kᵀ
+// issuer, warp 2: O += P V issuer, warp 3: V loads, then 4 warps per softmax
+// column group (thread = query row = TMEM lane), then 4 epilogue warps.  The
+// number of column groups depends on the head dim (Traits<D>::NG).
+constexpr int fwd_threads(int groups) { return 32 * (4 + 4 * groups + 4); }
 
 // Where a bounded wait gave up; recorded in bits 8-15 of the device status word.
 enum WaitSite : uint32_t {
