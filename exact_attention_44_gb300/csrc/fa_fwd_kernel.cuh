@@ -783,7 +783,7 @@ __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, fl
             l = l * alpha + (sl + sh);
             ++step;
         }
-        // hand m and this half's l to the epilogue warps
+        // hand m and this column group's l to the epilogue warps
         const uint32_t slot = ntile & 1u;
         if (!warp_wait_phase(bar(T::B_EPIEMPTY + slot), ((ntile >> 1) & 1u) ^ 1u, ctl, SITE_EPI_EMPTY)) return;
         if (h == 0) hand[slot * T::HAND_ROWS * BM + row] = m;
