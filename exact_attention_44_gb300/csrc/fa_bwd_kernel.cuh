@@ -135,6 +135,17 @@ __host__ __device__ constexpr uint32_t kmaj_off(int kk, int swe, int sw) {
 __device__ __forceinline__ uint32_t packed_col(int kk) { return kk < 4 ? kk * 8 : 64 + (kk - 4) * 8; }
 
 // ---------------------------------------------------------------- schedules --
+// CTA c takes one unit per round of `grid` units.  Causal units are ordered
+// heaviest first; the rounds alternate direction (unit c of round 0, unit
+// grid - 1 - c of round 1, ...), so a CTA that drew a heavier unit in one
+// round draws a lighter one in the next.
+template <bool CAUSAL>
+__device__ __forceinline__ int unit_at(int pos) {
+    if (!CAUSAL) return pos;
+    const int grid = (int)gridDim.x, round = pos / grid;
+    return (round & 1) ? 2 * round * grid + grid - 1 - pos : pos;
+}
+
 // dK/dV unit u: key block j (ascending: with a causal mask the first key
 // blocks have the most query blocks), then z, kv head.  Its steps run over
 // the group's query heads and, per head, the query blocks from i0 on.
@@ -199,8 +210,8 @@ __device__ void kv_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, cons
     const uint64_t pol_q = ptx::policy_evict_last();    // read by every key block
     uint32_t uc = 0, t = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.nunits; u += gridDim.x) {
-        const BwdUnit w = bwd_unit<CAUSAL>(u, p);
+    for (int pos = blockIdx.x; ok && unit_at<CAUSAL>(pos) < p.nunits; pos += gridDim.x) {
+        const BwdUnit w = bwd_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
         if (w.nsteps == 0) continue;
         if (uc > 0 && !wait_phase(bar(T::KB_KV_EMPTY), (uc - 1) & 1u, ctl, SITE_B_KV_EMPTY)) { ok = false; break; }
         ptx::mbar_arrive_expect_tx(bar(T::KB_KV_FULL), 2 * T::TILE);
@@ -267,8 +278,8 @@ __device__ void kv_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0, uin
     };
     uint32_t uc = 0, t = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.nunits; u += gridDim.x) {
-        const BwdUnit w = bwd_unit<CAUSAL>(u, p);
+    for (int pos = blockIdx.x; ok && unit_at<CAUSAL>(pos) < p.nunits; pos += gridDim.x) {
+        const BwdUnit w = bwd_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
         if (w.nsteps == 0) continue;
         if (!wait_phase(bar(T::KB_KV_FULL), uc & 1u, ctl, SITE_B_KV_FULL)) { ok = false; break; }
         if (!issue_s(t)) { ok = false; break; }
@@ -327,8 +338,8 @@ __device__ void kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar0, ui
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
     const float c = p.scale_log2;
     uint32_t t = 0;
-    for (int u = blockIdx.x; u < p.nunits; u += gridDim.x) {
-        const BwdUnit w = bwd_unit<CAUSAL>(u, p);
+    for (int pos = blockIdx.x; unit_at<CAUSAL>(pos) < p.nunits; pos += gridDim.x) {
+        const BwdUnit w = bwd_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
         for (int s = 0; s < w.nsteps; ++s, ++t) {
             const uint32_t st = t & 1u;
             int hq, i;
@@ -398,8 +409,8 @@ __device__ void kv_epilogue(const BwdParams& p, uint32_t bar0, uint32_t tmem, co
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
     constexpr int CH = D >= 32 ? 32 : 16;
     uint32_t uc = 0;
-    for (int u = blockIdx.x; u < p.nunits; u += gridDim.x) {
-        const BwdUnit w = bwd_unit<CAUSAL>(u, p);
+    for (int pos = blockIdx.x; unit_at<CAUSAL>(pos) < p.nunits; pos += gridDim.x) {
+        const BwdUnit w = bwd_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
         const int key = w.j * 128 + row;
         uint8_t* dk_row = reinterpret_cast<uint8_t*>(p.dk) +
                           2 * ((int64_t)w.z * p.sdk_z + (int64_t)w.hk * p.sdk_h + (int64_t)key * p.sdk_n);
@@ -519,8 +530,8 @@ __device__ void q_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const
     const uint64_t pol_kv = ptx::policy_evict_last();  // read by every query block of the group
     uint32_t uc = 0, g = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.nunits_q; u += gridDim.x) {
-        const DqUnit w = dq_unit<CAUSAL>(u, p);
+    for (int pos = blockIdx.x; ok && unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x) {
+        const DqUnit w = dq_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
         if (uc > 0 && !wait_phase(bar(T::QB_QD_EMPTY), (uc - 1) & 1u, ctl, SITE_B_QD_EMPTY)) { ok = false; break; }
         ptx::mbar_arrive_expect_tx(bar(T::QB_QD_FULL), 2 * T::TILE);
         for (int c = 0; c < T::NCHUNK; ++c) {
@@ -586,8 +597,8 @@ __device__ void q_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0, uint
     };
     uint32_t uc = 0, g = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.nunits_q; u += gridDim.x) {
-        const DqUnit w = dq_unit<CAUSAL>(u, p);
+    for (int pos = blockIdx.x; ok && unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x) {
+        const DqUnit w = dq_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
         if (!wait_phase(bar(T::QB_QD_FULL), uc & 1u, ctl, SITE_B_QD_FULL)) { ok = false; break; }
         if (!issue_s(g)) { ok = false; break; }
         issue_dp(g);
@@ -630,8 +641,8 @@ __device__ void q_softmax(const BwdParams& p, uint32_t bar0, uint32_t tmem, int 
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
     const float c = p.scale_log2;
     uint32_t g = 0;
-    for (int u = blockIdx.x; u < p.nunits_q; u += gridDim.x) {
-        const DqUnit w = dq_unit<CAUSAL>(u, p);
+    for (int pos = blockIdx.x; unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x) {
+        const DqUnit w = dq_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
         const int64_t r = ((int64_t)w.z * p.Hq + w.hq) * p.Tq * 128 + (int64_t)w.i * 128 + row;
         const float l2 = __ldg(p.lse2 + r), dl = __ldg(p.delta + r);
         for (int j = 0; j < w.nkv; ++j, ++g) {
@@ -687,8 +698,8 @@ __device__ void q_epilogue(const BwdParams& p, uint32_t bar0, uint32_t tmem, con
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
     constexpr int CH = D >= 32 ? 32 : 16;
     uint32_t uc = 0;
-    for (int u = blockIdx.x; u < p.nunits_q; u += gridDim.x, ++uc) {
-        const DqUnit w = dq_unit<CAUSAL>(u, p);
+    for (int pos = blockIdx.x; unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x, ++uc) {
+        const DqUnit w = dq_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
         const int q = w.i * 128 + row;
         uint8_t* dst = reinterpret_cast<uint8_t*>(p.dq) +
                        2 * ((int64_t)w.z * p.sdq_z + (int64_t)w.hq * p.sdq_h + (int64_t)q * p.sdq_n);
