@@ -322,13 +322,15 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* 
         }
     }
 
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     if (make_map(&mq, q, dtype, D, Nq, Hq, Z, sq, fa::BM) != CUDA_SUCCESS) return FA_ERR_CUDA;
     if (make_map(&mk, k, dtype, D, Nkv, Hkv, Z, sk, bn) != CUDA_SUCCESS) return FA_ERR_CUDA;
     if (make_map(&mv, v, dtype, D, Nkv, Hkv, Z, sv, bn) != CUDA_SUCCESS) return FA_ERR_CUDA;
+    if (make_map(&mo, o, dtype, D, Nq, Hq, Z, so, 32) != CUDA_SUCCESS) return FA_ERR_CUDA;
     a.tmQ = &mq;
     a.tmK = &mk;
     a.tmV = &mv;
+    a.tmO = &mo;
     a.stream = stream;
 
     const cudaError_t err = launch_for(D, a, causal != 0, dtype == FA_DTYPE_BF16, 0);
@@ -402,13 +404,15 @@ fa_status fwd_ex_impl(const void* q, const void* k, const void* v, void* o, floa
     p.cu_k = varlen ? opt->cu_seqlens_k : nullptr;
     a.grid = std::min(p.ntiles, info->sms);
 
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     if (make_map(&mq, q, dtype, D, Nq, Hq, nb, sq, fa::BM) != CUDA_SUCCESS) return FA_ERR_CUDA;
     if (make_map(&mk, k, dtype, D, Nkv, Hkv, nb, sk, bn) != CUDA_SUCCESS) return FA_ERR_CUDA;
     if (make_map(&mv, v, dtype, D, Nkv, Hkv, nb, sv, bn) != CUDA_SUCCESS) return FA_ERR_CUDA;
+    if (make_map(&mo, o, dtype, D, Nq, Hq, nb, so, 32) != CUDA_SUCCESS) return FA_ERR_CUDA;
     a.tmQ = &mq;
     a.tmK = &mk;
     a.tmV = &mv;
+    a.tmO = &mo;
     a.stream = stream;
     const cudaError_t err = launch_for(D, a, causal != 0, dtype == FA_DTYPE_BF16, p.alibi != nullptr ? 2 : 1);
     return err == cudaSuccess ? FA_OK : cuda_fail("variant forward launch", err);

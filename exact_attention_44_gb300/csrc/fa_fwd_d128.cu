@@ -35,7 +35,7 @@ static cudaError_t launch_one(const LaunchArgs& a) {
     cfg.stream = a.stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    err = cudaLaunchKernelEx(&cfg, kernel, *a.tmQ, *a.tmK, *a.tmV, a.params);
+    err = cudaLaunchKernelEx(&cfg, kernel, *a.tmQ, *a.tmK, *a.tmV, *a.tmO, a.params);
     // split schedule: one merge block per cut between CTA ranges, same stream
     if constexpr (VAR == 0) {
         if (err == cudaSuccess && a.params.split && a.grid > 1) {

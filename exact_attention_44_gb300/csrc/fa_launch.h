@@ -14,6 +14,7 @@ struct LaunchArgs {
     const CUtensorMap* tmQ;
     const CUtensorMap* tmK;
     const CUtensorMap* tmV;
+    const CUtensorMap* tmO;  // O in 32-row boxes, for the epilogue's tensor stores
     FwdParams params;
     int grid;
     cudaStream_t stream;
