@@ -564,10 +564,17 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     if ((cr = make_map(&mq, q, dtype, D, Nq, Hq, Z, sq, 128)) != CUDA_SUCCESS) return cuda_fail("Q tensor map", cr);
     if ((cr = make_map(&mdo, dO, dtype, D, Nq, Hq, Z, sdo, 128)) != CUDA_SUCCESS)
         return cuda_fail("dO tensor map", cr);
+    CUtensorMap mdq, mdk, mdv;
+    if ((cr = make_map(&mdq, dq, dtype, D, Nq, Hq, Z, sdq, 32)) != CUDA_SUCCESS) return cuda_fail("dQ tensor map", cr);
+    if ((cr = make_map(&mdk, dk, dtype, D, Nkv, Hkv, Z, sdk, 32)) != CUDA_SUCCESS) return cuda_fail("dK tensor map", cr);
+    if ((cr = make_map(&mdv, dv, dtype, D, Nkv, Hkv, Z, sdv, 32)) != CUDA_SUCCESS) return cuda_fail("dV tensor map", cr);
     a.tmK = &mk;
     a.tmV = &mv;
     a.tmQ = &mq;
     a.tmDO = &mdo;
+    a.tmDQ = &mdq;
+    a.tmDK = &mdk;
+    a.tmDV = &mdv;
     a.grid = (int)std::min<int64_t>(units, info->sms);
     a.grid_q = (int)std::min<int64_t>(units_q, info->sms);
     const int64_t pre_threads = (int64_t)Z * Hq * p.Tq * 128 * (D / 8);

@@ -33,9 +33,10 @@ static cudaError_t launch_one(const BwdLaunchArgs& a) {
     // Δ and lse2 per query row; then dK, dV; then dQ
     fa_bwd_pre_kernel<32, BF16><<<a.pre_grid, 256, 0, a.stream>>>(a.params);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    kv<<<a.grid, BWD_THREADS, T::KV_SMEM_BYTES, a.stream>>>(*a.tmK, *a.tmV, *a.tmQ, *a.tmDO, a.params);
+    kv<<<a.grid, BWD_THREADS, T::KV_SMEM_BYTES, a.stream>>>(*a.tmK, *a.tmV, *a.tmQ, *a.tmDO, *a.tmDK, *a.tmDV,
+                                                            a.params);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    dq<<<a.grid_q, BWD_THREADS, T::Q_SMEM_BYTES, a.stream>>>(*a.tmK, *a.tmV, *a.tmQ, *a.tmDO, a.params);
+    dq<<<a.grid_q, BWD_THREADS, T::Q_SMEM_BYTES, a.stream>>>(*a.tmK, *a.tmV, *a.tmQ, *a.tmDO, *a.tmDQ, a.params);
     return cudaGetLastError();
 }
 

@@ -61,7 +61,10 @@ struct BwdTraits {
     static constexpr int KV_OFF_DO = KV_OFF_Q + 2 * TILE;     // [2]
     static constexpr int KV_OFF_LSE = KV_OFF_DO + 2 * TILE;   // [2] x 128 floats
     static constexpr int KV_OFF_DELTA = KV_OFF_LSE + 2 * 512; // [2] x 128 floats
-    static constexpr int KV_OFF_BAR = KV_OFF_DELTA + 2 * 512;
+    // dK / dV staging for the tensor stores: 32 rows x one swizzle chunk per
+    // epilogue warp, aligned to the swizzle pattern's 1024-byte period
+    static constexpr int KV_OFF_OST = (KV_OFF_DELTA + 2 * 512 + 1023) / 1024 * 1024;
+    static constexpr int KV_OFF_BAR = KV_OFF_OST + 128 * SW;
     static constexpr int KB_KV_FULL = 0;      // K, V of a unit landed (TMA)
     static constexpr int KB_KV_EMPTY = 1;     // the unit's products are done (commit)
     static constexpr int KB_QD_FULL = 2;      // [2] Q, dO, lse2, Δ of a step landed (TMA)
@@ -89,7 +92,8 @@ struct BwdTraits {
     static constexpr int Q_OFF_DO = Q_OFF_Q + TILE;
     static constexpr int Q_OFF_K = Q_OFF_DO + TILE;           // [2]
     static constexpr int Q_OFF_V = Q_OFF_K + 2 * TILE;        // [2]
-    static constexpr int Q_OFF_BAR = Q_OFF_V + 2 * TILE;
+    static constexpr int Q_OFF_OST = Q_OFF_V + 2 * TILE;       // dQ staging (as KV_OFF_OST)
+    static constexpr int Q_OFF_BAR = Q_OFF_OST + 128 * SW;
     static constexpr int QB_QD_FULL = 0;      // Q, dO of a unit landed (TMA)
     static constexpr int QB_QD_EMPTY = 1;     // the unit's products are done (commit)
     static constexpr int QB_KV_FULL = 2;      // [2] K, V of a key block landed (TMA)
@@ -401,13 +405,18 @@ __device__ void kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar0, ui
 // Thread = TMEM lane = key: per unit, dK (times scale) and dV are read out,
 // released and stored in the input type; a unit no query sees gets zeros.
 template <int D, bool CAUSAL, bool BF16>
-__device__ void kv_epilogue(const BwdParams& p, uint32_t bar0, uint32_t tmem, const Ctl& ctl) {
+__device__ void kv_epilogue(const CUtensorMap* tmDK, const CUtensorMap* tmDV, const BwdParams& p, uint32_t sbase,
+                            uint32_t bar0, uint32_t tmem, const Ctl& ctl) {
     using T = BwdTraits<D>;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     const int quad = (threadIdx.x / 32) % 4;
     const int row = quad * 32 + threadIdx.x % 32;
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
-    constexpr int CH = D >= 32 ? 32 : 16;
+    const uint32_t stage = sbase + T::KV_OFF_OST + (uint32_t)quad * 32u * T::SW;  // this warp's staging rows
+    // lane 0's stores must have read shared memory before the CTA exits
+    auto drain = [&]() {
+        if (threadIdx.x % 32 == 0) ptx::bulk_wait_all();
+    };
     uint32_t uc = 0;
     for (int pos = blockIdx.x; unit_at<CAUSAL>(pos) < p.nunits; pos += gridDim.x) {
         const BwdUnit w = bwd_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
@@ -426,35 +435,25 @@ __device__ void kv_epilogue(const BwdParams& p, uint32_t bar0, uint32_t tmem, co
             }
             continue;
         }
-        if (!warp_wait_phase(bar(T::KB_ACC_FULL), uc & 1u, ctl, SITE_B_ACC_FULL)) return;
-        ptx::tc_fence_after();
-#pragma unroll
-        for (int which = 0; which < 2; ++which) {
-            const uint32_t col0 = which == 0 ? T::TM_DV : T::TM_DK;
-            const float mul = which == 0 ? 1.f : p.scale;
-            uint8_t* dst = which == 0 ? dv_row : dk_row;
-#pragma unroll
-            for (int cc = 0; cc < D / CH; ++cc) {
-                uint32_t r[CH];
-                if constexpr (CH == 32) ptx::tmem_ld32(tmem + lane_addr + col0 + cc * CH, r);
-                else ptx::tmem_ld16(tmem + lane_addr + col0 + cc * CH, r);
-                if (which == 1 && cc == D / CH - 1) {
-                    ptx::tc_fence_before();
-                    ptx::mbar_arrive(bar(T::KB_ACC_FREE));
-                }
-                if (key < p.Nkv) {
-#pragma unroll
-                    for (int x = 0; x < CH / 8; ++x)
-                        reinterpret_cast<uint4*>(dst + 2 * cc * CH)[x] = make_uint4(
-                            pack2<BF16>(__uint_as_float(r[8 * x]) * mul, __uint_as_float(r[8 * x + 1]) * mul),
-                            pack2<BF16>(__uint_as_float(r[8 * x + 2]) * mul, __uint_as_float(r[8 * x + 3]) * mul),
-                            pack2<BF16>(__uint_as_float(r[8 * x + 4]) * mul, __uint_as_float(r[8 * x + 5]) * mul),
-                            pack2<BF16>(__uint_as_float(r[8 * x + 6]) * mul, __uint_as_float(r[8 * x + 7]) * mul));
-                }
-            }
+        if (!warp_wait_phase(bar(T::KB_ACC_FULL), uc & 1u, ctl, SITE_B_ACC_FULL)) {
+            drain();
+            return;
         }
+        ptx::tc_fence_after();
+        // dV, then dK (x scale), as 32-row boxes of this warp's keys; a box
+        // that starts past the last key has nothing to store
+        const int key0 = w.j * 128 + 32 * quad;
+        tma_store_rows<D, T::SW, BF16>(tmem + lane_addr + T::TM_DV, 1.f, stage, tmDV, key0, w.hk, w.z, key0 < p.Nkv,
+                                       []() {});
+        tma_store_rows<D, T::SW, BF16>(tmem + lane_addr + T::TM_DK, p.scale, stage, tmDK, key0, w.hk, w.z,
+                                       key0 < p.Nkv, [&]() {
+                                           // dK and dV read: the next unit may accumulate into them
+                                           ptx::tc_fence_before();
+                                           ptx::mbar_arrive(bar(T::KB_ACC_FREE));
+                                       });
         ++uc;
     }
+    drain();
 }
 
 // Aligned dynamic shared memory base (the swizzled tiles need 1024 bytes);
@@ -474,6 +473,7 @@ template <int D, bool CAUSAL, bool BF16>
 __global__ void __launch_bounds__(BWD_THREADS, 1)
     fa_bwd_kv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
+                     const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV,
                      const BwdParams p) {
     using T = BwdTraits<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -492,6 +492,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         ptx::prefetch_tmap(&tmV);
         ptx::prefetch_tmap(&tmQ);
         ptx::prefetch_tmap(&tmDO);
+        ptx::prefetch_tmap(&tmDK);
+        ptx::prefetch_tmap(&tmDV);
     }
     if (warp == 13) {
         ptx::tmem_alloc(ptx::smem_addr(const_cast<uint32_t*>(tmem_slot)), T::TMEM_COLS);
@@ -505,7 +507,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     if (warp < 8) {
         kv_softmax<D, CAUSAL, BF16>(p, sbase, bar0, tmem, warp / 4, ctl);
     } else if (warp < 12) {
-        kv_epilogue<D, CAUSAL, BF16>(p, bar0, tmem, ctl);
+        kv_epilogue<D, CAUSAL, BF16>(&tmDK, &tmDV, p, sbase, bar0, tmem, ctl);
     } else if (warp == 12) {
         if (lane == 0) kv_producer<D, CAUSAL>(&tmK, &tmV, &tmQ, &tmDO, p, sbase, bar0, ctl);
     } else {
@@ -690,49 +692,42 @@ __device__ void q_softmax(const BwdParams& p, uint32_t bar0, uint32_t tmem, int 
 
 // Thread = TMEM lane = query: dQ (times scale) read out, released, stored.
 template <int D, bool CAUSAL, bool BF16>
-__device__ void q_epilogue(const BwdParams& p, uint32_t bar0, uint32_t tmem, const Ctl& ctl) {
+__device__ void q_epilogue(const CUtensorMap* tmDQ, const BwdParams& p, uint32_t sbase, uint32_t bar0, uint32_t tmem,
+                           const Ctl& ctl) {
     using T = BwdTraits<D>;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     const int quad = (threadIdx.x / 32) % 4;
-    const int row = quad * 32 + threadIdx.x % 32;
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
-    constexpr int CH = D >= 32 ? 32 : 16;
+    const uint32_t stage = sbase + T::Q_OFF_OST + (uint32_t)quad * 32u * T::SW;  // this warp's staging rows
+    // lane 0's stores must have read shared memory before the CTA exits
+    auto drain = [&]() {
+        if (threadIdx.x % 32 == 0) ptx::bulk_wait_all();
+    };
     uint32_t uc = 0;
     for (int pos = blockIdx.x; unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x, ++uc) {
         const DqUnit w = dq_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
-        const int q = w.i * 128 + row;
-        uint8_t* dst = reinterpret_cast<uint8_t*>(p.dq) +
-                       2 * ((int64_t)w.z * p.sdq_z + (int64_t)w.hq * p.sdq_h + (int64_t)q * p.sdq_n);
-        if (!warp_wait_phase(bar(T::QB_DQ_FULL), uc & 1u, ctl, SITE_B_DQ_FULL)) return;
-        ptx::tc_fence_after();
-#pragma unroll
-        for (int cc = 0; cc < D / CH; ++cc) {
-            uint32_t r[CH];
-            if constexpr (CH == 32) ptx::tmem_ld32(tmem + lane_addr + T::TM_DQ + cc * CH, r);
-            else ptx::tmem_ld16(tmem + lane_addr + T::TM_DQ + cc * CH, r);
-            if (cc == D / CH - 1) {
-                ptx::tc_fence_before();
-                ptx::mbar_arrive(bar(T::QB_DQ_FREE));
-            }
-            if (q < p.Nq) {
-                const float m = p.scale;
-#pragma unroll
-                for (int x = 0; x < CH / 8; ++x)
-                    reinterpret_cast<uint4*>(dst + 2 * cc * CH)[x] =
-                        make_uint4(pack2<BF16>(__uint_as_float(r[8 * x]) * m, __uint_as_float(r[8 * x + 1]) * m),
-                                   pack2<BF16>(__uint_as_float(r[8 * x + 2]) * m, __uint_as_float(r[8 * x + 3]) * m),
-                                   pack2<BF16>(__uint_as_float(r[8 * x + 4]) * m, __uint_as_float(r[8 * x + 5]) * m),
-                                   pack2<BF16>(__uint_as_float(r[8 * x + 6]) * m, __uint_as_float(r[8 * x + 7]) * m));
-            }
+        if (!warp_wait_phase(bar(T::QB_DQ_FULL), uc & 1u, ctl, SITE_B_DQ_FULL)) {
+            drain();
+            return;
         }
+        ptx::tc_fence_after();
+        // dQ (x scale) as 32-row boxes of this warp's queries
+        const int q0 = w.i * 128 + 32 * quad;
+        tma_store_rows<D, T::SW, BF16>(tmem + lane_addr + T::TM_DQ, p.scale, stage, tmDQ, q0, w.hq, w.z, q0 < p.Nq,
+                                       [&]() {
+                                           // dQ read: the next unit may accumulate into it
+                                           ptx::tc_fence_before();
+                                           ptx::mbar_arrive(bar(T::QB_DQ_FREE));
+                                       });
     }
+    drain();
 }
 
 template <int D, bool CAUSAL, bool BF16>
 __global__ void __launch_bounds__(BWD_THREADS, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
-                     const BwdParams p) {
+                     const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
     using T = BwdTraits<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = nullptr;
@@ -750,6 +745,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         ptx::prefetch_tmap(&tmV);
         ptx::prefetch_tmap(&tmQ);
         ptx::prefetch_tmap(&tmDO);
+        ptx::prefetch_tmap(&tmDQ);
     }
     if (warp == 13) {
         ptx::tmem_alloc(ptx::smem_addr(const_cast<uint32_t*>(tmem_slot)), T::TMEM_COLS);
@@ -763,7 +759,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     if (warp < 8) {
         q_softmax<D, CAUSAL, BF16>(p, bar0, tmem, warp / 4, ctl);
     } else if (warp < 12) {
-        q_epilogue<D, CAUSAL, BF16>(p, bar0, tmem, ctl);
+        q_epilogue<D, CAUSAL, BF16>(&tmDQ, p, sbase, bar0, tmem, ctl);
     } else if (warp == 12) {
         if (lane == 0) q_producer<D, CAUSAL>(&tmK, &tmV, &tmQ, &tmDO, p, sbase, bar0, ctl);
     } else {

@@ -798,6 +798,53 @@ __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, fl
     }
 }
 
+// One warp's 32 rows of a 128-lane TMEM block out to global memory through
+// shared memory and TMA tensor stores.  The warp reads its TMEM lanes at
+// columns taddr .. taddr + D - 1, multiplies by `mul` and converts to the
+// input type; for each swizzle chunk (SW bytes of a row) it fills its 32-row
+// staging area `stage` (1024-byte aligned, 32 * SW bytes) in the tensor map's
+// swizzled layout -- 16-byte piece c of row `lane` at piece c ^ swz, bank
+// conflict free -- and lane 0 stores the box at (chunk, row0, h, z) unless
+// `store` is false.  Before refilling the area lane 0 waits until the previous
+// box has been read out of it.  `after_read` runs in every lane once the last
+// TMEM load is complete.  The caller's lane 0 must finish with
+// bulk_wait_all() before the CTA exits.
+template <int D, int SW, bool BF16, typename AfterRead>
+__device__ __forceinline__ void tma_store_rows(uint32_t taddr, float mul, uint32_t stage, const CUtensorMap* map,
+                                               int row0, int h, int z, bool store, AfterRead&& after_read) {
+    constexpr int SWE = SW / 2;                 // elements per chunk row
+    constexpr int CH = SWE >= 32 ? 32 : 16;     // columns per TMEM load
+    const int lane = threadIdx.x % 32;
+    const uint32_t swz = ((uint32_t)lane * SW >> 7) & (SW / 16 - 1);
+#pragma unroll 1
+    for (int k = 0; k < D / SWE; ++k) {
+        uint32_t pk[SWE / 2];
+#pragma unroll
+        for (int i = 0; i < SWE / CH; ++i) {
+            uint32_t r[CH];
+            if constexpr (CH == 32) ptx::tmem_ld32(taddr + k * SWE + i * CH, r);
+            else ptx::tmem_ld16(taddr + k * SWE + i * CH, r);
+#pragma unroll
+            for (int x = 0; x < CH / 2; ++x)
+                pk[i * (CH / 2) + x] =
+                    pack2<BF16>(__uint_as_float(r[2 * x]) * mul, __uint_as_float(r[2 * x + 1]) * mul);
+        }
+        if (k == D / SWE - 1) after_read();
+        if (lane == 0) ptx::bulk_wait_read_all();
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < SW / 16; ++c)
+            ptx::st_shared_v4(stage + (uint32_t)lane * SW + ((c ^ swz) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                              pk[4 * c + 3]);
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && store) {
+            ptx::tma_store_4d(map, stage, k * SWE, row0, h, z);
+            ptx::bulk_commit();
+        }
+    }
+}
+
 // ------------------------------------------------------------ epilogue ------
 // O = acc / l in the input type, lse = m + log(l) in natural-log units
 // ("Write Triton Attention Kernel", steps 6-8).  O is read out of TMEM and
@@ -819,10 +866,7 @@ __device__ void run_epilogue(const CUtensorMap* tmO, const FwdParams& p, uint32_
     uint32_t step = 0, ntile = 0;
     constexpr int CH = D >= 32 ? 32 : 16;               // columns per TMEM load
     constexpr int HELD = D / CH < 2 ? D / CH : 2;        // chunks converted before their stores
-    // this warp's staging rows; the 16-byte piece c of row `lane` sits at
-    // piece c ^ swz, the tensor map's swizzle of a 1024-byte aligned buffer
-    const uint32_t stage = sbase + T::OFF_OST + (uint32_t)quad * 32u * T::SW;
-    const uint32_t swz = ((uint32_t)lane * T::SW >> 7) & (T::SW / 16 - 1);
+    const uint32_t stage = sbase + T::OFF_OST + (uint32_t)quad * 32u * T::SW;  // this warp's staging rows
     // lane 0's stores must have read shared memory before the CTA exits
     auto drain = [&]() {
         if (lane == 0) ptx::bulk_wait_all();
@@ -886,38 +930,14 @@ __device__ void run_epilogue(const CUtensorMap* tmO, const FwdParams& p, uint32_
         // run past the end of a packed sequence (the next sequence's rows
         // follow) stores its rows one by one instead.
         if (VAR == 0 || p.cu_q == nullptr || ti.q_start + 32 * quad + 32 <= ti.nq) {
-#pragma unroll 1
-            for (int k = 0; k < T::NCHUNK; ++k) {
-                uint32_t pk[T::SWE / 2];
-#pragma unroll
-                for (int i = 0; i < T::SWE / CH; ++i) {
-                    uint32_t r[CH];
-                    if constexpr (CH == 32) ptx::tmem_ld32(tmem + lane_addr + T::TM_O + k * T::SWE + i * CH, r);
-                    else ptx::tmem_ld16(tmem + lane_addr + T::TM_O + k * T::SWE + i * CH, r);
-#pragma unroll
-                    for (int x = 0; x < CH / 2; ++x)
-                        pk[i * (CH / 2) + x] =
-                            pack2<BF16>(__uint_as_float(r[2 * x]) * inv_l, __uint_as_float(r[2 * x + 1]) * inv_l);
-                }
-                if (k == T::NCHUNK - 1) {
-                    // all of O has been read: the MMA warp may overwrite it with the next tile
-                    ptx::tc_fence_before();
-                    ptx::mbar_arrive(bar(T::B_OFREE));
-                }
-                if (lane == 0) ptx::bulk_wait_read_all();  // the previous box has left the staging rows
-                __syncwarp();
-#pragma unroll
-                for (int c = 0; c < T::SW / 16; ++c)
-                    ptx::st_shared_v4(stage + (uint32_t)lane * T::SW + ((c ^ swz) << 4), pk[4 * c], pk[4 * c + 1],
-                                      pk[4 * c + 2], pk[4 * c + 3]);
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                // (a box that starts past the last row has nothing to store)
-                if (lane == 0 && ti.q_start + 32 * quad < ti.nq) {
-                    ptx::tma_store_4d(tmO, stage, k * T::SWE, ti.qrow0 + ti.q_start + 32 * quad, ti.hq, ti.zc);
-                    ptx::bulk_commit();
-                }
-            }
+            // (a box that starts past the last row has nothing to store)
+            tma_store_rows<D, T::SW, BF16>(tmem + lane_addr + T::TM_O, inv_l, stage, tmO,
+                                           ti.qrow0 + ti.q_start + 32 * quad, ti.hq, ti.zc,
+                                           ti.q_start + 32 * quad < ti.nq, [&]() {
+                                               // all of O has been read: the MMA warp may overwrite it
+                                               ptx::tc_fence_before();
+                                               ptx::mbar_arrive(bar(T::B_OFREE));
+                                           });
             if (store && p.lse != nullptr)
                 p.lse[ti.lse0 + q_row] = (VAR && !(l > 0.f)) ? -INFINITY : (m + log2f(l)) * 0.6931471805599453f;
             continue;

@@ -49,6 +49,9 @@ struct BwdLaunchArgs {
     const CUtensorMap* tmV;
     const CUtensorMap* tmQ;
     const CUtensorMap* tmDO;
+    const CUtensorMap* tmDQ;  // gradients in 32-row boxes, for the epilogues' tensor stores
+    const CUtensorMap* tmDK;
+    const CUtensorMap* tmDV;
     BwdParams params;
     int grid, grid_q, pre_grid;  // dK/dV kernel, dQ kernel, pre kernel
     cudaStream_t stream;
