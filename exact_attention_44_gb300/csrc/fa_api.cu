@@ -26,6 +26,7 @@ struct DeviceInfo {
     std::once_flag once;
     cudaError_t err = cudaSuccess;
     int sms = 0;
+    int l2_bytes = 0;
     uint32_t* status = nullptr;
 };
 DeviceInfo g_devices[kMaxDevices];
@@ -35,6 +36,7 @@ cudaError_t device_info(int dev, DeviceInfo** out) {
     DeviceInfo& d = g_devices[dev];
     std::call_once(d.once, [&] {
         d.err = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (d.err == cudaSuccess) d.err = cudaDeviceGetAttribute(&d.l2_bytes, cudaDevAttrL2CacheSize, dev);
         if (d.err == cudaSuccess) d.err = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_fa_status);
     });
     *out = &d;
@@ -191,11 +193,15 @@ template <bool CAUSAL, int BN>
 int64_t tile_mode_max_blocks_t(const fa::FwdParams& p, int grid) {
     using S = fa::Sched<CAUSAL, BN>;
     if (!CAUSAL) return cdiv(p.ntiles, grid) * p.Tk;
-    const int64_t heads = (int64_t)p.Z * p.Hq;
     int64_t worst = 0;
     for (int c = 0; c < grid; ++c) {
         int64_t sum = 0;
-        for (int64_t t = c; t < p.ntiles; t += grid) sum += S::tile_nkv(p.Tq - 1 - (int)(t / heads), p);
+        for (int64_t t = c; t < p.ntiles; t += grid) {
+            int64_t head;
+            int mb;
+            S::causal_tile(t, p, head, mb);
+            sum += S::tile_nkv(mb, p);
+        }
         worst = std::max(worst, sum);
     }
     return worst;
@@ -203,6 +209,18 @@ int64_t tile_mode_max_blocks_t(const fa::FwdParams& p, int grid) {
 int64_t tile_mode_max_blocks(const fa::FwdParams& p, bool causal, int bn, int grid) {
     if (bn == 64) return causal ? tile_mode_max_blocks_t<true, 64>(p, grid) : tile_mode_max_blocks_t<false, 64>(p, grid);
     return causal ? tile_mode_max_blocks_t<true, 128>(p, grid) : tile_mode_max_blocks_t<false, 128>(p, grid);
+}
+
+// Heads per group of a head-grouped work order: as many as keep the group's
+// data (bytes_per_unit per key/value head, shared by `group` consecutive query
+// heads) within a third of L2, but enough that a group holds at least four
+// rounds of work (units_per_head units per head, `sms` CTAs), so that its
+// heaviest-first order still balances the CTAs.
+int causal_head_group(int heads, int group, int64_t kv_head_bytes, int l2_bytes, int64_t units_per_head, int sms) {
+    const int64_t budget = std::max<int64_t>((int64_t)l2_bytes / 3, 1);
+    const int64_t kv_heads = std::max<int64_t>(1, budget / std::max<int64_t>(kv_head_bytes, 1));
+    const int64_t min_heads = cdiv(4 * (int64_t)sms, std::max<int64_t>(units_per_head, 1));
+    return (int)std::min<int64_t>(std::max(kv_heads * group, min_heads), heads);
 }
 
 // Cutting key ranges costs a partial write per cut tile, a merge launch and
@@ -302,6 +320,7 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* 
     p.Tq = (int)cdiv(Nq, fa::BM);
     p.Tk = (int)cdiv(Nkv, bn);
     p.ntiles = (int)((int64_t)Z * Hq * p.Tq);
+    p.head_group = causal_head_group(Z * Hq, p.group, (int64_t)Nkv * D * 4, info->l2_bytes, p.Tq, info->sms);
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);  // exp(x) = 2^(x log2 e)
     p.status = info->status;
     p.wait_limit_ns = wait_limit_ns();
@@ -390,6 +409,9 @@ fa_status fwd_ex_impl(const void* q, const void* k, const void* v, void* o, floa
     p.Tq = tq;
     p.Tk = (int)cdiv(Nkv, bn);
     p.ntiles = (int)((int64_t)Z * Hq * tq);
+    // a packed sequence's keys: about Nkv / Z of the packed rows
+    p.head_group = causal_head_group(Z * Hq, p.group, (int64_t)(varlen ? std::max(1, Nkv / Z) : Nkv) * D * 4,
+                                     info->l2_bytes, p.Tq, info->sms);
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
     p.status = info->status;
     p.wait_limit_ns = wait_limit_ns();
@@ -548,6 +570,10 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     if (units > INT32_MAX || units_q > INT32_MAX) return FA_ERR_UNSUPPORTED;
     p.nunits = (int)units;
     p.nunits_q = (int)units_q;
+    // a dK/dV group reads the Q and dO rows of its kv heads' query heads; a
+    // causal dQ group the K and V of its query heads (shared within a GQA group)
+    p.kv_head_group = causal_head_group(Z * Hkv, 1, (int64_t)p.group * Nq * D * 4, info->l2_bytes, p.Tk, info->sms);
+    p.q_head_group = causal_head_group(Z * Hq, p.group, (int64_t)Nkv * D * 4, info->l2_bytes, p.Tq, info->sms);
     p.scale = scale;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
     uint8_t* ws = static_cast<uint8_t*>(workspace);

@@ -151,8 +151,11 @@ __device__ __forceinline__ int unit_at(int pos) {
 }
 
 // dK/dV unit u: key block j (ascending: with a causal mask the first key
-// blocks have the most query blocks), then z, kv head.  Its steps run over
-// the group's query heads and, per head, the query blocks from i0 on.
+// blocks have the most query blocks) of kv head (z, hk).  The kv heads go in
+// groups of p.kv_head_group, sized on the host so that the query rows a
+// group reads (Q, dO) fit in a third of L2; within a group key blocks are
+// outermost and heads innermost.  A unit's steps run over the group's query
+// heads and, per head, the query blocks from i0 on.
 struct BwdUnit {
     int z, hk, j, i0, per_head, nsteps;
 };
@@ -160,10 +163,14 @@ struct BwdUnit {
 template <bool CAUSAL>
 __device__ __forceinline__ BwdUnit bwd_unit(int u, const BwdParams& p) {
     BwdUnit w;
-    const int zh = p.Z * p.Hkv;
-    w.j = u / zh;
-    w.z = (u % zh) / p.Hkv;
-    w.hk = (u % zh) % p.Hkv;
+    const int zh = p.Z * p.Hkv, G = p.kv_head_group;
+    const int g0 = u / (G * p.Tk) * G;           // first head of u's group
+    const int gc = zh - g0 < G ? zh - g0 : G;    // heads in the group
+    const int x = u - g0 * p.Tk;                 // u's place in the group
+    w.j = x / gc;
+    const int zhk = g0 + x % gc;
+    w.z = zhk / p.Hkv;
+    w.hk = zhk % p.Hkv;
     // causal (top-left): query row r sees keys <= r, so query blocks before
     // the key block's own index see none of its keys
     w.i0 = CAUSAL ? w.j : 0;
@@ -177,8 +184,11 @@ __device__ __forceinline__ void bwd_step(const BwdUnit& w, int s, const BwdParam
     i = w.i0 + s % w.per_head;
 }
 
-// dQ unit u: query block i of head (z, hq); causal: last query block first
-// (most key blocks), heads innermost.  It sees key blocks 0 .. nkv - 1.
+// dQ unit u: query block i of head (z, hq).  Non-causal: head-major, so the
+// CTAs running together share a head's K/V.  Causal: heads in groups of
+// p.q_head_group (the group's K/V within a third of L2), and within a group
+// the last query block (most key blocks) first, heads innermost.  It sees
+// key blocks 0 .. nkv - 1.
 struct DqUnit {
     int z, hq, hk, i, nkv;
 };
@@ -189,8 +199,12 @@ __device__ __forceinline__ DqUnit dq_unit(int u, const BwdParams& p) {
     const int heads = p.Z * p.Hq;
     int head;
     if (CAUSAL) {
-        w.i = p.Tq - 1 - u / heads;
-        head = u % heads;
+        const int G = p.q_head_group;
+        const int g0 = u / (G * p.Tq) * G;
+        const int gc = heads - g0 < G ? heads - g0 : G;
+        const int x = u - g0 * p.Tq;
+        w.i = p.Tq - 1 - x / gc;
+        head = g0 + x % gc;
     } else {
         head = u / p.Tq;
         w.i = u % p.Tq;

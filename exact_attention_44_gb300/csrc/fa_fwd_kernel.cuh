@@ -185,9 +185,13 @@ __device__ __forceinline__ uint32_t rphase(uint32_t g) { return (g / R) & 1u; }
 // 16 instead of 19 on the busiest CTA at 64 heads x 8 query blocks -- but
 // were measured 9 % slower on GB300, so the order stays round-robin.)
 // Non-causal tiles go head-major, so the CTAs running at the same time share
-// a head's K/V in L2; causal ones go from the last query block (most key
-// blocks) to the first with heads innermost, so the heavy tiles go first and
-// the light ones fill the tail.
+// a head's K/V in L2.  Causal ones go in groups of p.head_group heads, sized
+// on the host so that a group's K/V fits in a third of L2; within a group
+// from the last query block (most key blocks) to the first with the group's
+// heads innermost, so the heavy tiles go first and the light ones fill the
+// tail, and the tiles of a head run close together in time.  (With every
+// head in one group, 1024 heads of N = 1024 re-read each head's K/V from
+// DRAM for each of its query blocks.)
 //
 // Split mode (split != 0): the (tile, key block) pairs of all tiles, tiles
 // head-major and query blocks ascending, are laid end to end and cut into
@@ -217,6 +221,20 @@ struct Sched {
         const int64_t full = p.Tk / r;  // blocks m with r (m + 1) <= Tk
         const int64_t m = mb < full ? mb : full;
         return r * m * (m + 1) / 2 + (mb - m) * (int64_t)p.Tk;
+    }
+    // tile mode, causal: tile t of the order above.  Tile indices fit in 32
+    // bits (the host checks Z * Hq * Tq), and 32-bit divisions keep this
+    // short: every role runs it at the start of every tile.
+    static __host__ __device__ __forceinline__ void causal_tile(int64_t t64, const FwdParams& p, int64_t& head,
+                                                                int& mb) {
+        const uint32_t t = (uint32_t)t64, heads = (uint32_t)(p.Z * p.Hq), G = (uint32_t)p.head_group;
+        const uint32_t tq = (uint32_t)p.Tq;
+        const uint32_t g0 = t / (G * tq) * G;             // first head of t's group
+        const uint32_t gc = heads - g0 < G ? heads - g0 : G;  // heads in the group
+        const uint32_t w = t - g0 * tq;                   // t's place in the group
+        const uint32_t r = w / gc;
+        mb = (int)(tq - 1 - r);
+        head = g0 + (w - r * gc);
     }
     // split mode: first position of tile (head, mb), and the tile holding position x
     static __host__ __device__ __forceinline__ int64_t tile_pos(int64_t head, int mb, const FwdParams& p) {
@@ -277,15 +295,17 @@ struct Sched {
         if (p.split) {
             tile_of(pos, p, head, mb);
         } else if (CAUSAL) {
-            const int heads = p.Z * p.Hq;
-            mb = p.Tq - 1 - (int)(pos / heads);
-            head = pos % heads;
+            causal_tile(pos, p, head, mb);
         } else {
-            head = pos / p.Tq;
-            mb = (int)(pos % p.Tq);
+            const uint32_t t = (uint32_t)pos, h = t / (uint32_t)p.Tq;
+            head = h;
+            mb = (int)(t - h * (uint32_t)p.Tq);
         }
-        s.z = (int)(head / p.Hq);
-        s.hq = (int)(head % p.Hq);
+        {
+            const uint32_t hz = (uint32_t)head / (uint32_t)p.Hq;  // head < Z * Hq < 2^31
+            s.z = (int)hz;
+            s.hq = (int)((uint32_t)head - hz * (uint32_t)p.Hq);
+        }
         s.hk = s.hq / p.group;  // GQA: kv head = q head // (Hq / Hkv)
         s.q_start = mb * BM;
         s.nkv = tile_nkv(mb, p);
@@ -314,17 +334,18 @@ struct Sched {
     // all still finishes them (as O = 0, lse = -inf).
     __device__ __forceinline__ Seg var_seg(int64_t pos, const FwdParams& p) const {
         Seg s;
-        const int heads = p.Z * p.Hq;
         int head, mb;
         if (CAUSAL) {
-            mb = p.Tq - 1 - (int)(pos / heads);
-            head = (int)(pos % heads);
+            int64_t h64;
+            causal_tile(pos, p, h64, mb);
+            head = (int)h64;
         } else {
-            head = (int)(pos / p.Tq);
-            mb = (int)(pos % p.Tq);
+            const uint32_t t = (uint32_t)pos, h = t / (uint32_t)p.Tq;
+            head = (int)h;
+            mb = (int)(t - h * (uint32_t)p.Tq);
         }
         s.z = head / p.Hq;
-        s.hq = head % p.Hq;
+        s.hq = head - s.z * p.Hq;
         s.hk = s.hq / p.group;
         s.q_start = mb * BM;
         if (p.cu_q != nullptr) {

@@ -53,6 +53,7 @@ struct FwdParams {
     int group;               // Hq / Hkv
     int Tq, Tk;              // ceil(Nq / BM), ceil(Nkv / BN)
     int ntiles;              // Z * Hq * Tq
+    int head_group;          // causal tile order: (z, hq) heads per group (>= 1)
     float scale_log2;        // scale * log2(e)
     uint32_t* status;        // device status word (first error wins)
     uint64_t wait_limit_ns;  // bound on every mbarrier wait
@@ -93,6 +94,8 @@ struct BwdParams {
     int Tq, Tk;              // query blocks of 128 rows, key blocks of 128 keys
     int nunits;              // dK/dV units: Z * Hkv * Tk (one key block of one kv head)
     int nunits_q;            // dQ units: Z * Hq * Tq (one query block of one query head)
+    int kv_head_group;       // dK/dV unit order: (z, kv head) heads per group (>= 1)
+    int q_head_group;        // causal dQ unit order: (z, q head) heads per group (>= 1)
     float scale;             // softmax scale (dQ and dK carry it)
     float scale_log2;        // scale * log2(e)
     float* lse2;             // (Z, Hq, Tq * 128) fp32
