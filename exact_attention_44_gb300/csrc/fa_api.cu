@@ -189,26 +189,29 @@ int64_t head_blocks(const fa::FwdParams& p, bool causal, int bn) {
 
 // Key blocks of the busiest CTA when whole tiles are dealt round-robin to
 // `grid` CTAs in the kernel's tile order (causal: last query block first).
-template <bool CAUSAL, int BN>
+template <bool CAUSAL, int BN, bool ALT>
 int64_t tile_mode_max_blocks_t(const fa::FwdParams& p, int grid) {
-    using S = fa::Sched<CAUSAL, BN>;
+    using S = fa::Sched<CAUSAL, BN, false, ALT>;
     if (!CAUSAL) return cdiv(p.ntiles, grid) * p.Tk;
     int64_t worst = 0;
     for (int c = 0; c < grid; ++c) {
         int64_t sum = 0;
-        for (int64_t t = c; t < p.ntiles; t += grid) {
+        for (int64_t pos = c; S::tile_at(pos, grid) < p.ntiles; pos += grid) {
             int64_t head;
             int mb;
-            S::causal_tile(t, p, head, mb);
+            S::causal_tile(S::tile_at(pos, grid), p, head, mb);
             sum += S::tile_nkv(mb, p);
         }
         worst = std::max(worst, sum);
     }
     return worst;
 }
-int64_t tile_mode_max_blocks(const fa::FwdParams& p, bool causal, int bn, int grid) {
-    if (bn == 64) return causal ? tile_mode_max_blocks_t<true, 64>(p, grid) : tile_mode_max_blocks_t<false, 64>(p, grid);
-    return causal ? tile_mode_max_blocks_t<true, 128>(p, grid) : tile_mode_max_blocks_t<false, 128>(p, grid);
+int64_t tile_mode_max_blocks(const fa::FwdParams& p, bool causal, int bn, int grid, bool alt) {
+    if (!causal) return bn == 64 ? tile_mode_max_blocks_t<false, 64, false>(p, grid)
+                                 : tile_mode_max_blocks_t<false, 128, false>(p, grid);
+    if (bn == 64) return alt ? tile_mode_max_blocks_t<true, 64, true>(p, grid)
+                             : tile_mode_max_blocks_t<true, 64, false>(p, grid);
+    return alt ? tile_mode_max_blocks_t<true, 128, true>(p, grid) : tile_mode_max_blocks_t<true, 128, false>(p, grid);
 }
 
 // Heads per group of a head-grouped work order: as many as keep the group's
@@ -223,15 +226,25 @@ int causal_head_group(int heads, int group, int64_t kv_head_bytes, int l2_bytes,
     return (int)std::min<int64_t>(std::max(kv_heads * group, min_heads), heads);
 }
 
+// Whether the causal tile rounds alternate direction.  On paper it always
+// balances the CTAs at least as well, but measured on GB300 it was faster
+// only with long tiles: +11 % at N = 2048 D = 256 (17 key blocks a tile on
+// average), +5 % at N = 8192 D = 128 (32), flat at N = 2048 D = 128 (8.5),
+// and 6-8 % slower at N = 1024 (4.5 blocks: 64 and 1024 heads, D 64 and 128).
+bool causal_alternates(const fa::FwdParams& p, int bn) {
+    const int64_t blocks = head_blocks(p, true, bn);  // key blocks of one head's tiles
+    return blocks >= 16 * (int64_t)p.Tq;
+}
+
 // Cutting key ranges costs a partial write per cut tile, a merge launch and
 // shorter pipelines, measured on GB300 at about the time of 2048 keys of one
 // tile; it pays when whole tiles would leave the busiest CTA that much more
 // work than an even cut.  Many tiles per CTA are balanced already.
 constexpr int64_t kSplitGainKeys = 2048;
-bool split_pays(const fa::FwdParams& p, bool causal, int bn, int sms) {
+bool split_pays(const fa::FwdParams& p, bool causal, int bn, int sms, bool alt) {
     if ((int64_t)p.ntiles >= 16 * (int64_t)sms) return false;
     const int tile_grid = std::min(p.ntiles, sms);
-    const int64_t tile_max = tile_mode_max_blocks(p, causal, bn, tile_grid);
+    const int64_t tile_max = tile_mode_max_blocks(p, causal, bn, tile_grid, alt);
     const int64_t split_max = cdiv(p.total_blocks, std::min<int64_t>(p.total_blocks, sms));
     return (tile_max - split_max) * bn > kSplitGainKeys;
 }
@@ -321,6 +334,8 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* 
     p.Tk = (int)cdiv(Nkv, bn);
     p.ntiles = (int)((int64_t)Z * Hq * p.Tq);
     p.head_group = causal_head_group(Z * Hq, p.group, (int64_t)Nkv * D * 4, info->l2_bytes, p.Tq, info->sms);
+    // the order whole tiles would run in: causal rounds alternate for long tiles
+    const bool alt = causal && causal_alternates(p, bn);
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);  // exp(x) = 2^(x log2 e)
     p.status = info->status;
     p.wait_limit_ns = wait_limit_ns();
@@ -333,7 +348,7 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* 
         p.head_blocks = head_blocks(p, causal != 0, bn);
         p.total_blocks = (int64_t)Z * Hq * p.head_blocks;
         const int force = g_force_split.load();
-        if (force == 1 || (force == 0 && split_pays(p, causal != 0, bn, info->sms))) {
+        if (force == 1 || (force == 0 && split_pays(p, causal != 0, bn, info->sms, alt))) {
             p.split = 1;
             a.grid = (int)std::min<int64_t>(p.total_blocks, info->sms);
             p.slot_floats = split_slot_floats(D);
@@ -352,7 +367,8 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* 
     a.tmO = &mo;
     a.stream = stream;
 
-    const cudaError_t err = launch_for(D, a, causal != 0, dtype == FA_DTYPE_BF16, 0);
+    // kernel variant 4: the plain kernel with alternating causal rounds (tile mode only)
+    const cudaError_t err = launch_for(D, a, causal != 0, dtype == FA_DTYPE_BF16, alt && !p.split ? 4 : 0);
     return err == cudaSuccess ? FA_OK : cuda_fail("forward launch", err);
 }
 

@@ -51,7 +51,8 @@ static cudaError_t launch_one(const LaunchArgs& a) {
     return err;
 }
 
-// variant 0: fa_fwd; 1: window / variable length; 2: the same with ALiBi
+// variant 0: fa_fwd; 1: window / variable length; 2: the same with ALiBi;
+// 4: fa_fwd with alternating causal rounds (tile mode)
 cudaError_t launch_d64(const LaunchArgs& a, bool causal, bool bf16, int variant) {
     if (variant == 2) {
         if (causal) return bf16 ? launch_one<true, true, 2>(a) : launch_one<true, false, 2>(a);
@@ -61,6 +62,7 @@ cudaError_t launch_d64(const LaunchArgs& a, bool causal, bool bf16, int variant)
         if (causal) return bf16 ? launch_one<true, true, 1>(a) : launch_one<true, false, 1>(a);
         return bf16 ? launch_one<false, true, 1>(a) : launch_one<false, false, 1>(a);
     }
+    if (variant == 4 && causal) return bf16 ? launch_one<true, true, 4>(a) : launch_one<true, false, 4>(a);
     if (causal) return bf16 ? launch_one<true, true, 0>(a) : launch_one<true, false, 0>(a);
     return bf16 ? launch_one<false, true, 0>(a) : launch_one<false, false, 0>(a);
 }

@@ -178,20 +178,29 @@ __device__ __forceinline__ uint32_t rslot(uint32_t g) { return g % R; }
 template <int R>
 __device__ __forceinline__ uint32_t rphase(uint32_t g) { return (g / R) & 1u; }
 
+// The kernel's VAR argument: kind 0 plain (fa_fwd), 1 window / variable
+// length, 2 the same with ALiBi; bit 4 set: plain with alternating causal
+// rounds (below).
+__host__ __device__ constexpr int var_kind(int var) { return var & 3; }
+__host__ __device__ constexpr bool var_alt(int var) { return (var & 4) != 0; }
+
 // The static schedule, in one of two modes.
 //
-// Tile mode (split == 0): CTA c takes whole tiles c, c + grid, ...  (Rounds
-// that alternate direction balance the causal blocks better on paper --
-// 16 instead of 19 on the busiest CTA at 64 heads x 8 query blocks -- but
-// were measured 9 % slower on GB300, so the order stays round-robin.)
-// Non-causal tiles go head-major, so the CTAs running at the same time share
-// a head's K/V in L2.  Causal ones go in groups of p.head_group heads, sized
-// on the host so that a group's K/V fits in a third of L2; within a group
+// Tile mode (split == 0): CTA c takes one whole tile per round of `grid`
+// tiles.  Non-causal tiles go head-major, CTA c taking tiles c, c + grid, ...,
+// so the CTAs running at the same time share a head's K/V in L2.  Causal
+// ones go in groups of p.head_group heads, sized on the host so that a
+// group's K/V fits in a third of L2; within a group
 // from the last query block (most key blocks) to the first with the group's
 // heads innermost, so the heavy tiles go first and the light ones fill the
 // tail, and the tiles of a head run close together in time.  (With every
 // head in one group, 1024 heads of N = 1024 re-read each head's K/V from
-// DRAM for each of its query blocks.)
+// DRAM for each of its query blocks.)  With ALT (its own kernel
+// instantiation, so that the plain order compiles as if it did not exist)
+// the causal rounds alternate direction (CTA c takes tile c of round 0, tile
+// grid - 1 - c of round 1, ...), so a CTA that drew a heavier tile in one
+// round draws a lighter one in the next; the host picks it only for long
+// tiles, where it was measured faster (causal_alternates in the host code).
 //
 // Split mode (split != 0): the (tile, key block) pairs of all tiles, tiles
 // head-major and query blocks ascending, are laid end to end and cut into
@@ -203,7 +212,7 @@ __device__ __forceinline__ uint32_t rphase(uint32_t g) { return (g / R) & 1u; }
 // A causal tile stops at the key block holding its last row ("Write Triton
 // Attention Kernel", step 9).  Positions are tiles in tile mode and
 // (tile, key block) pairs in split mode.
-template <bool CAUSAL, int BN, bool VAR = false>
+template <bool CAUSAL, int BN, bool VAR = false, bool ALT = false>
 struct Sched {
     int64_t hi;  // split mode: end of this CTA's range
 
@@ -221,6 +230,12 @@ struct Sched {
         const int64_t full = p.Tk / r;  // blocks m with r (m + 1) <= Tk
         const int64_t m = mb < full ? mb : full;
         return r * m * (m + 1) / 2 + (mb - m) * (int64_t)p.Tk;
+    }
+    // tile mode: the tile at position pos = round * grid + c (CTA c), in 32 bits
+    static __host__ __device__ __forceinline__ int64_t tile_at(int64_t pos, int grid) {
+        if (!CAUSAL || !ALT) return pos;
+        const uint32_t x = (uint32_t)pos, g = (uint32_t)grid, round = x / g;
+        return (round & 1u) ? (int64_t)(2u * round * g + g - 1u - x) : pos;
     }
     // tile mode, causal: tile t of the order above.  Tile indices fit in 32
     // bits (the host checks Z * Hq * Tq), and 32-bit divisions keep this
@@ -268,7 +283,7 @@ struct Sched {
     // the variant schedule skips tiles past the end of their sequence
     __device__ __forceinline__ int64_t skip_empty(int64_t pos, const FwdParams& p) const {
         if constexpr (VAR) {
-            for (; pos < p.ntiles; pos += gridDim.x) {
+            for (; tile_at(pos, gridDim.x) < p.ntiles; pos += gridDim.x) {
                 const Seg t = var_seg(pos, p);
                 if (t.q_start < t.nq) break;
             }
@@ -280,8 +295,8 @@ struct Sched {
         return p.split ? range_lo(blockIdx.x, gridDim.x, p) : (int64_t)blockIdx.x;
     }
     __device__ __forceinline__ bool valid(int64_t pos, const FwdParams& p) const {
-        if constexpr (VAR) return pos < p.ntiles;
-        return p.split ? pos < hi : pos < p.ntiles;
+        if (VAR || !p.split) return tile_at(pos, gridDim.x) < p.ntiles;
+        return pos < hi;
     }
     __device__ __forceinline__ int64_t next(int64_t pos, const Seg& sg, const FwdParams& p) const {
         if constexpr (VAR) return skip_empty(pos + gridDim.x, p);
@@ -295,7 +310,7 @@ struct Sched {
         if (p.split) {
             tile_of(pos, p, head, mb);
         } else if (CAUSAL) {
-            causal_tile(pos, p, head, mb);
+            causal_tile(tile_at(pos, gridDim.x), p, head, mb);
         } else {
             const uint32_t t = (uint32_t)pos, h = t / (uint32_t)p.Tq;
             head = h;
@@ -337,7 +352,7 @@ struct Sched {
         int head, mb;
         if (CAUSAL) {
             int64_t h64;
-            causal_tile(pos, p, h64, mb);
+            causal_tile(tile_at(pos, gridDim.x), p, h64, mb);
             head = (int)h64;
         } else {
             const uint32_t t = (uint32_t)pos, h = t / (uint32_t)p.Tq;
@@ -412,7 +427,7 @@ __device__ void run_producer_qk(const CUtensorMap* tmQ, const CUtensorMap* tmK, 
         ++qi;
         return true;
     };
-    const Sched<CAUSAL, T::BN, (VAR != 0)> sc(p);
+    const Sched<CAUSAL, T::BN, (var_kind(VAR) != 0), var_alt(VAR)> sc(p);
     int64_t pos = sc.first(p);
     if (sc.valid(pos, p)) ok = load_q(sc.seg(pos, p));
     while (ok && sc.valid(pos, p)) {
@@ -463,7 +478,7 @@ __device__ void run_producer_v(const CUtensorMap* tmV, const FwdParams& p, uint3
     const uint64_t pol_kv = ptx::policy_evict_last();
     uint32_t vi = 0;
     bool ok = true;
-    const Sched<CAUSAL, T::BN, (VAR != 0)> sc(p);
+    const Sched<CAUSAL, T::BN, (var_kind(VAR) != 0), var_alt(VAR)> sc(p);
     for (int64_t pos = sc.first(p); ok && sc.valid(pos, p);) {
         const Seg sg = sc.seg(pos, p);
         for (int j = sg.jb; j < sg.je; ++j) {
@@ -505,7 +520,7 @@ __device__ void run_mma_qk(const FwdParams& p, uint32_t sbase, uint32_t bar0, ui
     const uint32_t k_lo0 = ptx::smem_desc_lo(sbase + T::OFF_K, 16);
     uint32_t qi = 0, g = 0;  // Q tiles and S blocks issued
     bool ok = true;
-    const Sched<CAUSAL, T::BN, (VAR != 0)> sc(p);
+    const Sched<CAUSAL, T::BN, (var_kind(VAR) != 0), var_alt(VAR)> sc(p);
     for (int64_t pos = sc.first(p); ok && sc.valid(pos, p);) {
         const Seg sg = sc.seg(pos, p);
         pos = sc.next(pos, sg, p);
@@ -556,7 +571,7 @@ __device__ void run_mma_pv(const FwdParams& p, uint32_t sbase, uint32_t bar0, ui
     const uint32_t v_lo0 = ptx::smem_desc_lo(sbase + T::OFF_V, T::BN * T::SW);  // LBO: next column chunk of V
     uint32_t g = 0, ntile = 0;
     bool ok = true;
-    const Sched<CAUSAL, T::BN, (VAR != 0)> sc(p);
+    const Sched<CAUSAL, T::BN, (var_kind(VAR) != 0), var_alt(VAR)> sc(p);
     for (int64_t pos = sc.first(p); ok && sc.valid(pos, p); ++ntile) {
         const Seg sg = sc.seg(pos, p);
         pos = sc.next(pos, sg, p);
@@ -653,15 +668,15 @@ __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, fl
     const int row = quad * 32 + threadIdx.x % 32;
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
     const float c = p.scale_log2;
-    // with an ALiBi bias (the VAR == 2 instantiation) the scores are scaled
+    // with an ALiBi bias (the kind 2 instantiation) the scores are scaled
     // and biased in place (units of log2), so the maximum and the
     // exponentials take them as they are
-    constexpr bool bias = VAR == 2;
+    constexpr bool bias = var_kind(VAR) == 2;
     const float cm = bias ? 1.f : c;
     const uint64_t c2 = ptx::pack_f32x2(cm, cm);
     uint32_t step = 0, ntile = 0;
 
-    const Sched<CAUSAL, BN, (VAR != 0)> sc(p);
+    const Sched<CAUSAL, BN, (var_kind(VAR) != 0), var_alt(VAR)> sc(p);
     for (int64_t pos = sc.first(p); sc.valid(pos, p); ++ntile) {
         const Seg ti = sc.seg(pos, p);
         pos = sc.next(pos, ti, p);
@@ -688,7 +703,7 @@ __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, fl
             // the mask goes on the scores before the row max (Correctness
             // requirements); only the diagonal block and the key tail need it
             const int k0 = j * BN + h * HC;
-            if constexpr (!VAR) {
+            if constexpr (var_kind(VAR) == 0) {
                 const bool need_mask = (CAUSAL && j * BN + BN - 1 > ti.q_start) || (j * BN + BN > p.Nkv);
                 if (need_mask) {
                     const int kmax = CAUSAL ? min(p.Nkv - 1, q_row) : p.Nkv - 1;  // last kept key for this row
@@ -892,7 +907,7 @@ __device__ void run_epilogue(const CUtensorMap* tmO, const FwdParams& p, uint32_
     auto drain = [&]() {
         if (lane == 0) ptx::bulk_wait_all();
     };
-    const Sched<CAUSAL, T::BN, (VAR != 0)> sc(p);
+    const Sched<CAUSAL, T::BN, (var_kind(VAR) != 0), var_alt(VAR)> sc(p);
     for (int64_t pos = sc.first(p); sc.valid(pos, p); ++ntile) {
         const Seg ti = sc.seg(pos, p);
         pos = sc.next(pos, ti, p);
@@ -946,11 +961,11 @@ __device__ void run_epilogue(const CUtensorMap* tmO, const FwdParams& p, uint32_
         const int q_row = ti.q_start + row;
         const bool store = q_row < ti.nq;
         // a variant row with no kept key (l = 0) is finished as O = 0, lse = -inf
-        const float inv_l = (VAR && !(l > 0.f)) ? 0.f : 1.f / l;
+        const float inv_l = (var_kind(VAR) != 0 && !(l > 0.f)) ? 0.f : 1.f / l;
         // The tensor map clips rows past the tensor's end.  A warp whose rows
         // run past the end of a packed sequence (the next sequence's rows
         // follow) stores its rows one by one instead.
-        if (VAR == 0 || p.cu_q == nullptr || ti.q_start + 32 * quad + 32 <= ti.nq) {
+        if (var_kind(VAR) == 0 || p.cu_q == nullptr || ti.q_start + 32 * quad + 32 <= ti.nq) {
             // (a box that starts past the last row has nothing to store)
             tma_store_rows<D, T::SW, BF16>(tmem + lane_addr + T::TM_O, inv_l, stage, tmO,
                                            ti.qrow0 + ti.q_start + 32 * quad, ti.hq, ti.zc,
@@ -960,7 +975,7 @@ __device__ void run_epilogue(const CUtensorMap* tmO, const FwdParams& p, uint32_
                                                ptx::mbar_arrive(bar(T::B_OFREE));
                                            });
             if (store && p.lse != nullptr)
-                p.lse[ti.lse0 + q_row] = (VAR && !(l > 0.f)) ? -INFINITY : (m + log2f(l)) * 0.6931471805599453f;
+                p.lse[ti.lse0 + q_row] = (var_kind(VAR) != 0 && !(l > 0.f)) ? -INFINITY : (m + log2f(l)) * 0.6931471805599453f;
             continue;
         }
         uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
@@ -993,7 +1008,7 @@ __device__ void run_epilogue(const CUtensorMap* tmO, const FwdParams& p, uint32_
             }
         }
         if (store && p.lse != nullptr)
-            p.lse[ti.lse0 + q_row] = (VAR && !(l > 0.f)) ? -INFINITY : (m + log2f(l)) * 0.6931471805599453f;
+            p.lse[ti.lse0 + q_row] = (var_kind(VAR) != 0 && !(l > 0.f)) ? -INFINITY : (m + log2f(l)) * 0.6931471805599453f;
     }
     drain();
 }

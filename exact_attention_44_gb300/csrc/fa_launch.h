@@ -21,8 +21,9 @@ struct LaunchArgs {
 };
 
 // Launch fa_fwd_kernel<D, causal, bf16, variant> (variant 0: fa_fwd, 1:
-// window / variable length, 2: with ALiBi; and the split merge when the
-// parameters ask for the split schedule); returns the launches' error code.
+// window / variable length, 2: with ALiBi, 4: fa_fwd with alternating causal
+// rounds; and the split merge when the parameters ask for the split
+// schedule); returns the launches' error code.
 cudaError_t launch_d16(const LaunchArgs& a, bool causal, bool bf16, int variant);
 cudaError_t launch_d32(const LaunchArgs& a, bool causal, bool bf16, int variant);
 cudaError_t launch_d64(const LaunchArgs& a, bool causal, bool bf16, int variant);

@@ -122,6 +122,31 @@ def test_long_gqa_causal_sampled_heads():
         assert err <= TOL_GRAD[dtype] * mag, f"{name}: {err:.3e} vs {mag:.3e}"
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_many_heads_sampled(causal):
+    # Z=128 H=8 N=1024 D=64 fp16: 1024 heads, more than one group of the
+    # dK/dV and dQ unit orders (a group's Q/dO or K/V fits in a third of L2);
+    # the oracle differentiates heads spread over the groups, the last included
+    import torch
+    import exact_attention_44_gb300 as fa
+    Z, H, N, D, dtype = 128, 8, 1024, 64, "fp16"
+    scale = 1 / math.sqrt(D)
+    q, k, v = si.qkv(209, Z, H, H, N, N, D, dtype)
+    do = si.normals(1209, 0, q.size, dtype).reshape(q.shape)
+    qt, kt, vt, dot = (to_device(x, dtype) for x in (q, k, v, do))
+    o, lse = fa.fa_fwd(qt, kt, vt, causal=causal)
+    dq, dk, dv = fa.fa_bwd(qt, kt, vt, o, lse, dot, causal=causal)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status()[0] == 0
+    for z, h in [(0, 0), (20, 3), (20, 4), (64, 0), (127, 7)]:
+        one = (slice(z, z + 1), slice(h, h + 1))
+        ref = oracle.attention_bwd(q[one], k[one], v[one], do[one], dtype, scale, causal)
+        for name, got, want in zip(("dq", "dk", "dv"), (dq[one], dk[one], dv[one]), ref):
+            g = got.double().cpu().numpy()
+            err, mag = float(np.max(np.abs(g - want))), float(np.max(np.abs(want)))
+            assert err <= TOL_GRAD[dtype] * mag, f"head ({z}, {h}) {name}: {err:.3e} vs {mag:.3e}"
+
+
 def test_bitwise_repeatable():
     # no atomics: two runs give identical bits for dQ, dK and dV
     import torch
