@@ -159,6 +159,12 @@ __device__ __forceinline__ bool drain_phase(uint32_t bar, uint32_t parity, uint6
     return true;
 }
 
+// The kernel's VAR argument: kind 0 plain (fa_fwd), 1 window / variable
+// length, 2 the same with ALiBi; bit 4 set: plain with alternating causal
+// rounds (see the schedule).
+__host__ __device__ constexpr int var_kind(int var) { return var & 3; }
+__host__ __device__ constexpr bool var_alt(int var) { return (var & 4) != 0; }
+
 // One unit of a CTA's work: key blocks [jb, je) of the query tile
 // (z, hq, q_start), whose whole key range is [0, nkv).
 struct Seg {
@@ -172,17 +178,31 @@ struct Seg {
     int64_t lse0;
 };
 
+// The key block visited at step j (jb <= j < je) of a segment.  With an
+// ALiBi bias (kind 2) the block holding the tile's diagonal goes first: it
+// holds every row's largest bias (0 at the row's own key), so the running
+// maximum it sets is not exceeded by more than the rescale threshold later
+// and the other blocks, in order after it, redo no exponentials and leave O
+// unscaled.  (In plain order a causal tile meets ever larger biases, and
+// with a slope of 1/2 each 128-key block raised the maximum by 64.)  The
+// online softmax gives the same result in any order.  Otherwise block j.
+template <int VAR, int BN>
+__device__ __forceinline__ int key_block(const Seg& sg, int j) {
+    if constexpr (var_kind(VAR) != 2) {
+        return j;
+    } else {
+        int d = (sg.q_start + BM / 2) / BN;  // the block of the tile's middle row's own key
+        d = d < sg.jb ? sg.jb : (d > sg.je - 1 ? sg.je - 1 : d);
+        if (j == sg.jb) return d;
+        return j - 1 >= d ? j : j - 1;  // the others in order, d skipped
+    }
+}
+
 // Barrier slot and phase parity of key block g (global count) in a ring of R.
 template <int R>
 __device__ __forceinline__ uint32_t rslot(uint32_t g) { return g % R; }
 template <int R>
 __device__ __forceinline__ uint32_t rphase(uint32_t g) { return (g / R) & 1u; }
-
-// The kernel's VAR argument: kind 0 plain (fa_fwd), 1 window / variable
-// length, 2 the same with ALiBi; bit 4 set: plain with alternating causal
-// rounds (below).
-__host__ __device__ constexpr int var_kind(int var) { return var & 3; }
-__host__ __device__ constexpr bool var_alt(int var) { return (var & 4) != 0; }
 
 // The static schedule, in one of two modes.
 //
@@ -445,7 +465,7 @@ __device__ void run_producer_qk(const CUtensorMap* tmQ, const CUtensorMap* tmK, 
                 const uint32_t dst = sbase + T::OFF_K + s * T::KV_BYTES;
                 for (int c = 0; c < T::NCHUNK; ++c)
                     ptx::tma_load_4d(dst + c * (T::BN * T::SW), tmK, bar(T::B_KFULL + s), c * T::SWE,
-                                     sg.krow0 + j * T::BN, sg.hk, sg.zc, pol_kv);
+                                     sg.krow0 + key_block<VAR, T::BN>(sg, j) * T::BN, sg.hk, sg.zc, pol_kv);
             }
             ++ki;
             // with two Q slots the next segment's Q can go right after the
@@ -490,7 +510,7 @@ __device__ void run_producer_v(const CUtensorMap* tmV, const FwdParams& p, uint3
             const uint32_t dst = sbase + T::OFF_V + s * T::KV_BYTES;
             for (int c = 0; c < T::NCHUNK; ++c)
                 ptx::tma_load_4d(dst + c * (T::BN * T::SW), tmV, bar(T::B_VFULL + s), c * T::SWE,
-                                 sg.krow0 + j * T::BN, sg.hk, sg.zc, pol_kv);
+                                 sg.krow0 + key_block<VAR, T::BN>(sg, j) * T::BN, sg.hk, sg.zc, pol_kv);
             ++vi;
         }
         pos = sc.next(pos, sg, p);
@@ -702,9 +722,10 @@ __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, fl
             }
             // the mask goes on the scores before the row max (Correctness
             // requirements); only the diagonal block and the key tail need it
-            const int k0 = j * BN + h * HC;
+            const int kj = key_block<VAR, BN>(ti, j);  // the key block of this step
+            const int k0 = kj * BN + h * HC;
             if constexpr (var_kind(VAR) == 0) {
-                const bool need_mask = (CAUSAL && j * BN + BN - 1 > ti.q_start) || (j * BN + BN > p.Nkv);
+                const bool need_mask = (CAUSAL && kj * BN + BN - 1 > ti.q_start) || (kj * BN + BN > p.Nkv);
                 if (need_mask) {
                     const int kmax = CAUSAL ? min(p.Nkv - 1, q_row) : p.Nkv - 1;  // last kept key for this row
 #pragma unroll
@@ -715,11 +736,11 @@ __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, fl
                 // kept keys of this row: kmin .. kmax (sequence end, causal
                 // diagonal, window sides); the mask is applied only when some
                 // row of the tile loses a key of this block
-                const int blast = j * BN + BN - 1;
+                const int blast = kj * BN + BN - 1;
                 bool full = blast < ti.nk;
                 if (CAUSAL) full = full && blast <= ti.q_start;
                 if (p.win_right >= 0) full = full && blast <= ti.q_start + p.win_right;
-                if (p.win_left >= 0) full = full && j * BN >= ti.q_start + BM - 1 - p.win_left;
+                if (p.win_left >= 0) full = full && kj * BN >= ti.q_start + BM - 1 - p.win_left;
                 if (!full) {
                     int kmax = ti.nk - 1;
                     if (CAUSAL) kmax = min(kmax, q_row);
@@ -732,13 +753,23 @@ __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, fl
                 if constexpr (bias) {
                     // scaled score plus -slope |i - j|, in log2 units.  When the
                     // whole block lies on one side of every row of the tile,
-                    // |i - j| is linear in the key: two FMAs per score.
+                    // |i - j| is linear in the key: the bias of a pair of keys
+                    // advances by one packed add and joins the scaled scores in
+                    // one packed FMA.  (The repeated adds round at most ~8 ulp
+                    // of the largest bias of the 32 keys, which matters only
+                    // where that bias is small: a key far from its row's
+                    // maximum has p = 0 either way.)
                     const float d0 = (float)(q_row - k0);  // i - j at x = 0
-                    if (blast <= ti.q_start || j * BN >= ti.q_start + BM - 1) {
+                    if (blast <= ti.q_start || kj * BN >= ti.q_start + BM - 1) {
                         const float sgn = blast <= ti.q_start ? 1.f : -1.f;
                         const float b0 = slope2 * sgn * d0, step = -slope2 * sgn;
+                        const uint64_t cs2 = ptx::pack_f32x2(c, c), inc2 = ptx::pack_f32x2(2.f * step, 2.f * step);
+                        uint64_t b2 = ptx::pack_f32x2(b0, b0 + step);
 #pragma unroll
-                        for (int x = 0; x < HC; ++x) s[x] = fmaf(s[x], c, fmaf((float)x, step, b0));
+                        for (int x = 0; x < HC; x += 2) {
+                            ptx::unpack_f32x2(ptx::ffma2(ptx::pack_f32x2(s[x], s[x + 1]), cs2, b2), s[x], s[x + 1]);
+                            b2 = ptx::fadd2(b2, inc2);
+                        }
                     } else {
 #pragma unroll
                         for (int x = 0; x < HC; ++x) s[x] = fmaf(s[x], c, slope2 * fabsf(d0 - (float)x));
