@@ -391,6 +391,14 @@ fa_status fwd_ex_impl(const void* q, const void* k, const void* v, void* o, floa
         return FA_ERR_ALIGNMENT;
     if (opt->alibi_slopes != nullptr && reinterpret_cast<uintptr_t>(opt->alibi_slopes) % 4 != 0)
         return FA_ERR_ALIGNMENT;
+    // Without a sequence table, a bias or a window side shorter than every
+    // query-key distance, the call is fa_fwd: it takes the plain kernel (the
+    // variant kernel's per-block window and sequence checks cost ~15 %).
+    const int64_t reach_all = (int64_t)Nq + Nkv;
+    const auto open = [&](int w) { return w < 0 || (int64_t)w > reach_all; };
+    if (!varlen && opt->alibi_slopes == nullptr && open(opt->window_left) && open(opt->window_right))
+        return fwd_impl(q, k, v, o, lse, Z, Hq, Hkv, Nq, Nkv, D, sq, sk, sv, so, scale, causal, dtype, stream, false,
+                        nullptr, 0);
     const int tq = (int)cdiv(varlen ? opt->max_seqlen_q : Nq, fa::BM);
     if ((int64_t)Z * Hq * tq > INT32_MAX) return FA_ERR_UNSUPPORTED;
     if ((varlen ? (int64_t)Nq : (int64_t)Z * Hq * Nq) == 0 || (int64_t)Z * Hq * tq == 0) return FA_OK;

@@ -122,8 +122,10 @@ typedef struct {
 } fa_fwd_options;
 
 /*
- * fa_fwd_ex -- fa_fwd with the options above (NULL options: exactly fa_fwd's
- * result, through the variant kernel).  Arguments are those of fa_fwd, except
+ * fa_fwd_ex -- fa_fwd with the options above.  With no sequence table, no
+ * slopes and both window sides open (-1 or longer than Nq + Nkv; NULL options
+ * included) the call is fa_fwd and runs fa_fwd's kernel.  Arguments are those
+ * of fa_fwd, except
  * with cu_seqlens set: Z is the number of sequences, the tensors are packed
  * with a batch extent of one -- q and o (1, Hq, Nq, D), k and v (1, Hkv, Nkv,
  * D), any strides as for fa_fwd (the batch stride is ignored), Nq and Nkv the
