@@ -490,7 +490,7 @@ fa_status fa_fwd_plan(int Z, int Hq, int Hkv, int Nq, int Nkv, int D, int causal
     const int64_t nt = (int64_t)Z * Hq * tq;
     int64_t pairs = 0;
     if (causal) {
-        for (int64_t mb = 0; mb < tq; ++mb) {  // same bound as the kernel's tile_info
+        for (int64_t mb = 0; mb < tq; ++mb) {  // same bound as the kernel's Sched::tile_nkv
             const int64_t last_row = std::min<int64_t>(mb * fa::BM + fa::BM, Nq) - 1;
             pairs += std::min<int64_t>(tk, last_row / bn + 1);
         }
