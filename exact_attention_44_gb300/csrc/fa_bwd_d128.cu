@@ -31,13 +31,29 @@ static cudaError_t launch_one(const BwdLaunchArgs& a) {
     if ((err = set_smem_once(kv, T::KV_SMEM_BYTES, kv_configured)) != cudaSuccess) return err;
     if ((err = set_smem_once(dq, T::Q_SMEM_BYTES, dq_configured)) != cudaSuccess) return err;
     // Δ and lse2 per query row; then dK, dV; then dQ
-    fa_bwd_pre_kernel<128, BF16><<<a.pre_grid, 256, 0, a.stream>>>(a.params);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    kv<<<a.grid, BWD_THREADS, T::KV_SMEM_BYTES, a.stream>>>(*a.tmK, *a.tmV, *a.tmQ, *a.tmDO, *a.tmDK, *a.tmDV,
-                                                            a.params);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    dq<<<a.grid_q, BWD_THREADS, T::Q_SMEM_BYTES, a.stream>>>(*a.tmK, *a.tmV, *a.tmQ, *a.tmDO, *a.tmDQ, a.params);
-    return cudaGetLastError();
+    // each launch is a programmatic dependent of the one before it on the
+    // stream: its set-up overlaps that kernel's tail, and it waits for it
+    // (griddepcontrol.wait) before touching global memory
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = a.stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(a.pre_grid);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    if ((err = cudaLaunchKernelEx(&cfg, fa_bwd_pre_kernel<128, BF16>, a.params)) != cudaSuccess) return err;
+    cfg.gridDim = dim3(a.grid);
+    cfg.blockDim = dim3(BWD_THREADS);
+    cfg.dynamicSmemBytes = T::KV_SMEM_BYTES;
+    if ((err = cudaLaunchKernelEx(&cfg, kv, *a.tmK, *a.tmV, *a.tmQ, *a.tmDO, *a.tmDK, *a.tmDV, a.params)) !=
+        cudaSuccess)
+        return err;
+    cfg.gridDim = dim3(a.grid_q);
+    cfg.dynamicSmemBytes = T::Q_SMEM_BYTES;
+    return cudaLaunchKernelEx(&cfg, dq, *a.tmK, *a.tmV, *a.tmQ, *a.tmDO, *a.tmDQ, a.params);
 }
 
 cudaError_t launch_bwd_d128(const BwdLaunchArgs& a, bool causal, bool bf16) {

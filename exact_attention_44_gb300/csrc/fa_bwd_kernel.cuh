@@ -518,6 +518,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const Ctl ctl{abort_flag, p.status, p.wait_limit_ns};
+    // launched as a programmatic dependent: the set-up above overlaps the
+    // previous kernel's tail; nothing below touches global memory before it
+    // has completed
+    ptx::grid_dependency_wait();
+    ptx::grid_launch_dependents();
     if (warp < 8) {
         kv_softmax<D, CAUSAL, BF16>(p, sbase, bar0, tmem, warp / 4, ctl);
     } else if (warp < 12) {
@@ -770,6 +775,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const Ctl ctl{abort_flag, p.status, p.wait_limit_ns};
+    ptx::grid_dependency_wait();  // as in the dK/dV kernel
+    ptx::grid_launch_dependents();
     if (warp < 8) {
         q_softmax<D, CAUSAL, BF16>(p, bar0, tmem, warp / 4, ctl);
     } else if (warp < 12) {
@@ -793,6 +800,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 // rows and columns get P = 0).  D/8 threads per row, 16 bytes of O and dO each.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
+    ptx::grid_dependency_wait();  // O, dO and lse come from earlier kernels on the stream
+    ptx::grid_launch_dependents();
     constexpr int TPR = D / 8;
     const int64_t rows = (int64_t)p.Z * p.Hq * p.Tq * 128;
     const int sub = threadIdx.x % TPR;

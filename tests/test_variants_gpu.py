@@ -84,13 +84,15 @@ def test_alibi_with_window_and_layouts():
     _run_padded(97, 1, 4, 4, 333, 333, 128, "bf16", True, window=(96, 0), alibi=True, layout="bsnd")
 
 
-def test_no_options_is_fa_fwd_bitwise():
+@pytest.mark.parametrize("window", [(-1, -1), (333 + 444 + 1, -1), (-1, 5000), (10 ** 6, 10 ** 6)])
+def test_no_options_is_fa_fwd_bitwise(window):
+    # no sequence table, no slopes and open window sides: the call is fa_fwd
     import torch
     import exact_attention_44_gb300 as fa
     for causal in (False, True):
         q, k, v = (to_device(x, "bf16") for x in si.qkv(98, 2, 4, 2, 333, 444, 128, "bf16"))
         a = fa.fa_fwd(q, k, v, causal=causal)
-        b = fa.fa_fwd_ex(q, k, v, causal=causal)
+        b = fa.fa_fwd_ex(q, k, v, causal=causal, window=window)
         torch.cuda.synchronize()
         assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
