@@ -47,6 +47,7 @@ _SIGNATURES = {
     "fa_device_status": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)]),
     "fa_fwd_plan": (ctypes.c_int, [ctypes.c_int] * 8 + [ctypes.POINTER(ctypes.c_int64)] * 2 +
                     [ctypes.POINTER(ctypes.c_int)] * 3),
+    "fa_fwd_schedule": (ctypes.c_int, [ctypes.c_int] * 9 + [ctypes.c_int64, ctypes.c_void_p]),
     "fa_debug_set_wait_limit_ms": (None, [ctypes.c_double]),
     "fa_debug_inject_stall": (None, [ctypes.c_int]),
     "fa_debug_force_split": (None, [ctypes.c_int]),
@@ -69,6 +70,12 @@ class fa_strides(ctypes.Structure):
 class fa_fwd_options(ctypes.Structure):
     _fields_ = [("window_left", ctypes.c_int), ("window_right", ctypes.c_int), ("alibi_slopes", ctypes.c_void_p),
                 ("cu_seqlens_q", ctypes.c_void_p), ("cu_seqlens_k", ctypes.c_void_p), ("max_seqlen_q", ctypes.c_int)]
+
+
+class fa_fwd_schedule_info(ctypes.Structure):
+    _fields_ = [("grid", ctypes.c_int), ("split", ctypes.c_int), ("gqa_packed", ctypes.c_int),
+                ("head_group", ctypes.c_int), ("alternate", ctypes.c_int), ("tiles", ctypes.c_int64),
+                ("kv_blocks", ctypes.c_int64), ("busiest_blocks", ctypes.c_int64)]
 
 
 def library_path() -> str:
@@ -419,6 +426,19 @@ def fa_fwd_plan(Z: int, Hq: int, Hkv: int, Nq: int, Nkv: int, D: int, causal: bo
         raise FaError(rc, "fa_fwd_plan")
     return {"tiles": tiles.value, "kv_blocks": pairs.value, "block_n": bn.value, "grid": grid.value,
             "smem_bytes": smem.value}
+
+
+def fa_fwd_schedule(Z: int, Hq: int, Hkv: int, Nq: int, Nkv: int, D: int, causal: bool, *, splitkv: bool = False,
+                    num_sms: int, l2_bytes: int) -> dict:
+    """Host-only (no CUDA call): the schedule fa_fwd (or fa_fwd_splitkv) picks for contiguous BNSD
+    tensors on a device with num_sms SMs and l2_bytes of L2 -- grid, split, gqa_packed, head_group,
+    alternate, tiles, kv_blocks, busiest_blocks (libfa's fa_fwd_schedule)."""
+    info = fa_fwd_schedule_info()
+    rc = load().fa_fwd_schedule(Z, Hq, Hkv, Nq, Nkv, D, int(bool(causal)), int(bool(splitkv)), num_sms, l2_bytes,
+                                ctypes.byref(info))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_schedule")
+    return {name: getattr(info, name) for name, _ in fa_fwd_schedule_info._fields_}
 
 
 def fa_debug_set_wait_limit_ms(ms: float) -> None:

@@ -259,6 +259,33 @@ cudaError_t launch_for(int D, const fa::LaunchArgs& a, bool causal, bool bf16, i
     }
 }
 
+// The schedule of a forward launch whose sizes are in p (Z .. ntiles):
+// causal head groups and alternating rounds for whole tiles, and whether key
+// ranges are cut across CTAs (only where the caller allows it: the cut needs
+// a workspace).  Shared by the launch and the host-only fa_fwd_schedule.
+struct SchedChoice {
+    int grid = 0;
+    bool split = false;
+    bool alt = false;
+};
+SchedChoice choose_schedule(fa::FwdParams& p, int D, bool causal, int bn, int sms, int l2_bytes, bool split_allowed) {
+    SchedChoice c;
+    p.head_group = causal_head_group(p.Z * p.Hq, p.group, (int64_t)p.Nkv * D * 4, l2_bytes, p.Tq, sms);
+    // the order whole tiles would run in: causal rounds alternate for long tiles
+    c.alt = causal && causal_alternates(p, bn);
+    c.grid = std::min(p.ntiles, sms);
+    if (split_allowed) {
+        p.head_blocks = head_blocks(p, causal, bn);
+        p.total_blocks = (int64_t)p.Z * p.Hq * p.head_blocks;
+        const int force = g_force_split.load();
+        if (force == 1 || (force == 0 && split_pays(p, causal, bn, sms, c.alt))) {
+            c.split = true;
+            c.grid = (int)std::min<int64_t>(p.total_blocks, sms);
+        }
+    }
+    return c;
+}
+
 // GQA packing.  Without a causal mask a query row's result does not depend on
 // its position, so the g query heads that share a key/value head can be run
 // as one head of g * Nq rows against that K/V: each key block is then loaded
@@ -333,27 +360,20 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* 
     p.Tq = (int)cdiv(Nq, fa::BM);
     p.Tk = (int)cdiv(Nkv, bn);
     p.ntiles = (int)((int64_t)Z * Hq * p.Tq);
-    p.head_group = causal_head_group(Z * Hq, p.group, (int64_t)Nkv * D * 4, info->l2_bytes, p.Tq, info->sms);
-    // the order whole tiles would run in: causal rounds alternate for long tiles
-    const bool alt = causal && causal_alternates(p, bn);
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);  // exp(x) = 2^(x log2 e)
     p.status = info->status;
     p.wait_limit_ns = wait_limit_ns();
     p.inject_stall = g_inject_stall.load();
-    a.grid = std::min(p.ntiles, info->sms);
-    if (split) {
-        // one equal range of (tile, key block) pairs per SM (every range
-        // non-empty), when that beats whole tiles for this shape
-        if (workspace_bytes < split_workspace_bytes(D, info->sms)) return FA_ERR_WORKSPACE;
-        p.head_blocks = head_blocks(p, causal != 0, bn);
-        p.total_blocks = (int64_t)Z * Hq * p.head_blocks;
-        const int force = g_force_split.load();
-        if (force == 1 || (force == 0 && split_pays(p, causal != 0, bn, info->sms, alt))) {
-            p.split = 1;
-            a.grid = (int)std::min<int64_t>(p.total_blocks, info->sms);
-            p.slot_floats = split_slot_floats(D);
-            p.scratch = static_cast<float*>(workspace);
-        }
+    // split: one equal range of (tile, key block) pairs per SM (every range
+    // non-empty), when that beats whole tiles for this shape
+    if (split && workspace_bytes < split_workspace_bytes(D, info->sms)) return FA_ERR_WORKSPACE;
+    const SchedChoice choice = choose_schedule(p, D, causal != 0, bn, info->sms, info->l2_bytes, split);
+    const bool alt = choice.alt;
+    a.grid = choice.grid;
+    if (choice.split) {
+        p.split = 1;
+        p.slot_floats = split_slot_floats(D);
+        p.scratch = static_cast<float*>(workspace);
     }
 
     CUtensorMap mq, mk, mv, mo;
@@ -503,6 +523,46 @@ fa_status fa_fwd_plan(int Z, int Hq, int Hkv, int Nq, int Nkv, int D, int causal
     if (block_n) *block_n = bn;
     if (grid) *grid = (int)(num_sms > 0 ? std::min<int64_t>(nt, num_sms) : nt);
     if (smem_bytes) *smem_bytes = fa::smem_bytes_for(D);
+    return FA_OK;
+}
+
+fa_status fa_fwd_schedule(int Z, int Hq, int Hkv, int Nq, int Nkv, int D, int causal, int splitkv, int num_sms,
+                          int64_t l2_bytes, fa_fwd_schedule_info* out) {
+    if (out == nullptr || num_sms < 1 || l2_bytes < 1) return FA_ERR_INVALID_ARG;
+    const fa_status st = check_shape(Z, Hq, Hkv, Nq, Nkv, D, causal);
+    if (st != FA_OK) return st;
+    *out = fa_fwd_schedule_info{};
+    // contiguous BNSD tensors, seen as the launch sees them (GQA packing included)
+    const fa_strides sq{(int64_t)Hq * Nq * D, (int64_t)Nq * D, D, 1}, sk{(int64_t)Hkv * Nkv * D, (int64_t)Nkv * D, D, 1};
+    fa_strides pq, pk, pv, po;
+    if ((int64_t)Z * Hq * Nq > 0 && gqa_pack_view(Z, Hq, Hkv, Nq, causal, &sq, &sk, &sk, &sq, &pq, &pk, &pv, &po)) {
+        Nq *= Hq / Hkv;
+        Z *= Hkv;
+        Hq = Hkv = 1;
+        out->gqa_packed = 1;
+    }
+    const int bn = fa::block_n_for(D);
+    fa::FwdParams p{};
+    p.Z = Z;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.Nq = Nq;
+    p.Nkv = Nkv;
+    p.group = Hq / Hkv;
+    p.Tq = (int)cdiv(Nq, fa::BM);
+    p.Tk = (int)cdiv(Nkv, bn);
+    p.ntiles = (int)((int64_t)Z * Hq * p.Tq);
+    if (p.ntiles == 0) return FA_OK;
+    const int l2 = (int)std::min<int64_t>(l2_bytes, INT32_MAX);
+    const SchedChoice c = choose_schedule(p, D, causal != 0, bn, num_sms, l2, splitkv != 0);
+    out->grid = c.grid;
+    out->split = c.split ? 1 : 0;
+    out->head_group = p.head_group;
+    out->alternate = c.alt && !c.split ? 1 : 0;
+    out->tiles = p.ntiles;
+    out->kv_blocks = (int64_t)Z * Hq * head_blocks(p, causal != 0, bn);
+    out->busiest_blocks = c.split ? cdiv(out->kv_blocks, c.grid)
+                                  : tile_mode_max_blocks(p, causal != 0, bn, c.grid, c.alt);
     return FA_OK;
 }
 

@@ -326,6 +326,42 @@ fa_status fa_fwd_plan(int Z, int Hq, int Hkv, int Nq, int Nkv, int D, int causal
                       int64_t* kv_blocks, int* block_n, int* grid, int* smem_bytes);
 
 /*
+ * fa_fwd_schedule -- host-only: the schedule fa_fwd (splitkv = 0) or
+ * fa_fwd_splitkv (splitkv = 1) picks for contiguous BNSD tensors of these
+ * sizes on a device with num_sms SMs and l2_bytes of L2 (what the calls read
+ * from the device); no CUDA call is made.  The page "把 FlashAttention 搬上昇腾..."
+ * (sections 五, 八) schedules heavy causal tiles first over a persistent grid;
+ * the grouping and alternation below are this library's refinements of that.
+ *   grid            CTAs of the forward launch
+ *   split           1: key ranges cut into one equal range per CTA and the
+ *                   cut tiles merged (fa_fwd_splitkv only, where it pays)
+ *   gqa_packed      1: the query heads of each GQA group run as one head of
+ *                   g * Nq rows (non-causal, Nq < 128)
+ *   head_group      causal whole-tile order: heads per group (all heads when
+ *                   their K/V fit in a third of L2)
+ *   alternate       causal whole-tile order: rounds alternate direction
+ *                   (long tiles only)
+ *   tiles           query tiles of the launch (after packing)
+ *   kv_blocks       (tile, key block) pairs of the launch
+ *   busiest_blocks  key blocks of the busiest CTA in the schedule that runs
+ * Errors: those of fa_fwd_plan for bad shapes; FA_ERR_INVALID_ARG for a NULL
+ * out, num_sms < 1 or l2_bytes < 1.  fa_debug_force_split applies here too.
+ */
+typedef struct {
+    int grid;
+    int split;
+    int gqa_packed;
+    int head_group;
+    int alternate;
+    int64_t tiles;
+    int64_t kv_blocks;
+    int64_t busiest_blocks;
+} fa_fwd_schedule_info;
+
+fa_status fa_fwd_schedule(int Z, int Hq, int Hkv, int Nq, int Nkv, int D, int causal, int splitkv, int num_sms,
+                          int64_t l2_bytes, fa_fwd_schedule_info* out);
+
+/*
  * Test hooks for the failure-detection path; not for production use.
  *
  * fa_debug_set_wait_limit_ms -- bound, in milliseconds, on every mbarrier wait

@@ -206,3 +206,120 @@ def test_fwd_ex_option_errors_on_the_host(lib):
     assert call(cq=0x1000, ck=0x2000, maxq=-1) == fa.FA_ERR_INVALID_ARG
     assert call(cq=0x1002, ck=0x2000, maxq=8) == fa.FA_ERR_ALIGNMENT
     assert call(alibi=0x1001) == fa.FA_ERR_ALIGNMENT
+
+
+# ---- fa_fwd_schedule: the forward's schedule, host-only -------------------
+# An independent statement of the documented whole-tile orders: non-causal
+# tiles head-major; causal tiles in groups of head_group heads, each group
+# from the last query block to the first with its heads innermost; tile t of
+# round r = t // grid goes to CTA t - r * grid, or to grid - 1 - (t - r * grid)
+# when the rounds alternate and r is odd.  The busiest CTA's key blocks must
+# equal the planner's.
+
+GB300_SMS, GB300_L2 = 152, 126 * 2 ** 20
+
+
+def _tile_blocks(mb, Nq, Nkv, bn, causal):
+    tk = -(-Nkv // bn)
+    if not causal:
+        return tk
+    last_row = min(mb * 128 + 128, Nq) - 1
+    return min(tk, last_row // bn + 1)
+
+
+def _busiest(Z, Hq, Nq, Nkv, bn, causal, grid, head_group, alternate):
+    heads, tq = Z * Hq, -(-Nq // 128)
+    if causal:
+        order = []
+        for g0 in range(0, heads, head_group):
+            gc = min(head_group, heads - g0)
+            for mb in reversed(range(tq)):
+                order += [_tile_blocks(mb, Nq, Nkv, bn, True)] * gc
+    else:
+        order = [_tile_blocks(0, Nq, Nkv, bn, False)] * (heads * tq)
+    loads = [0] * grid
+    for t, blocks in enumerate(order):
+        r, k = divmod(t, grid)
+        loads[grid - 1 - k if (alternate and r % 2) else k] += blocks
+    return max(loads)
+
+
+@pytest.mark.parametrize("shape", [
+    (4, 16, 16, 1024, 1024, 128, False),   # the bench workload, both masks
+    (4, 16, 16, 1024, 1024, 128, True),
+    (8, 16, 16, 2048, 2048, 256, True),    # long causal tiles (64-key blocks): alternating rounds
+    (128, 8, 8, 1024, 1024, 128, True),    # 1024 heads: several head groups
+    (1, 32, 8, 8192, 8192, 128, True),
+    (1, 32, 8, 32768, 32768, 128, True),   # GQA: groups of 8 query heads
+    (2, 3, 1, 1000, 300, 64, True),        # odd sizes, fewer tiles than SMs
+    (3, 5, 5, 130, 4000, 32, False),
+])
+def test_schedule_matches_the_documented_order(shape):
+    import exact_attention_44_gb300 as fa
+    Z, Hq, Hkv, Nq, Nkv, D, causal = shape
+    s = fa.fa_fwd_schedule(Z, Hq, Hkv, Nq, Nkv, D, causal, num_sms=GB300_SMS, l2_bytes=GB300_L2)
+    bn = 64 if D == 256 else 128
+    heads, tq, tk = Z * Hq, -(-Nq // 128), -(-Nkv // bn)
+    assert s["split"] == 0 and s["gqa_packed"] == 0
+    assert s["tiles"] == heads * tq and s["grid"] == min(heads * tq, GB300_SMS)
+    assert s["kv_blocks"] == Z * Hq * sum(_tile_blocks(mb, Nq, Nkv, bn, causal) for mb in range(tq))
+    if causal:
+        # a group's K/V within a third of L2, at least four rounds of tiles, at most every head
+        kv_heads = max(1, (GB300_L2 // 3) // (Nkv * D * 4))
+        want = min(heads, max(kv_heads * (Hq // Hkv), -(-4 * GB300_SMS // tq)))
+        assert s["head_group"] == want
+        # rounds alternate only for long tiles (>= 16 key blocks a tile on average)
+        assert s["alternate"] == int(s["kv_blocks"] >= 16 * s["tiles"])
+    else:
+        assert s["alternate"] == 0
+    assert s["busiest_blocks"] == _busiest(Z, Hq, Nq, Nkv, bn, causal, s["grid"], s["head_group"], s["alternate"])
+
+
+def test_schedule_known_values():
+    import exact_attention_44_gb300 as fa
+    kw = dict(num_sms=GB300_SMS, l2_bytes=GB300_L2)
+    # the bench workload: 512 tiles on 152 CTAs, 4 tiles of 8 blocks on the busiest;
+    # causal: heaviest first, round-robin, 19 blocks on the busiest (15.2 on average)
+    assert fa.fa_fwd_schedule(4, 16, 16, 1024, 1024, 128, False, **kw)["busiest_blocks"] == 32
+    c = fa.fa_fwd_schedule(4, 16, 16, 1024, 1024, 128, True, **kw)
+    assert (c["head_group"], c["alternate"], c["busiest_blocks"]) == (64, 0, 19)
+    # alternating rounds: 236 blocks on the busiest CTA instead of 284
+    assert fa.fa_fwd_schedule(8, 16, 16, 2048, 2048, 256, True, **kw)["busiest_blocks"] == 236
+
+
+def test_schedule_split_and_gqa_packing():
+    import exact_attention_44_gb300 as fa
+    kw = dict(num_sms=GB300_SMS, l2_bytes=GB300_L2)
+    # a decode row: the 4 query heads of a group run as one head of 4 rows,
+    # and the 8 resulting tiles are cut into one key range per SM
+    d = fa.fa_fwd_schedule(1, 32, 8, 1, 32768, 128, False, splitkv=True, **kw)
+    assert d["gqa_packed"] == 1 and d["tiles"] == 8 and d["split"] == 1 and d["grid"] == GB300_SMS
+    assert d["busiest_blocks"] == -(-8 * 256 // GB300_SMS)
+    # fa_fwd never cuts; through fa_fwd_splitkv the bench workload stays whole
+    # (32 key blocks on the busiest CTA against 27 for an even cut: under the
+    # 2048-key threshold)
+    assert fa.fa_fwd_schedule(1, 32, 8, 1, 32768, 128, False, **kw)["split"] == 0
+    assert fa.fa_fwd_schedule(4, 16, 16, 1024, 1024, 128, False, splitkv=True, **kw)["split"] == 0
+    # and 16 or more tiles per SM are never cut
+    assert fa.fa_fwd_schedule(1, 38, 38, 8192, 8192, 128, False, splitkv=True, **kw)["split"] == 0
+    # causal rows are never packed (a row's keys depend on its position)
+    assert fa.fa_fwd_schedule(1, 32, 8, 64, 4096, 128, True, **kw)["gqa_packed"] == 0
+    # the test hook forces either choice
+    try:
+        fa.fa_debug_force_split(1)
+        assert fa.fa_fwd_schedule(4, 16, 16, 1024, 1024, 128, False, splitkv=True, **kw)["split"] == 1
+        fa.fa_debug_force_split(2)
+        assert fa.fa_fwd_schedule(1, 32, 8, 1, 32768, 128, False, splitkv=True, **kw)["split"] == 0
+    finally:
+        fa.fa_debug_force_split(0)
+
+
+def test_schedule_argument_errors():
+    import exact_attention_44_gb300 as fa
+    for kw in (dict(num_sms=0, l2_bytes=GB300_L2), dict(num_sms=GB300_SMS, l2_bytes=0)):
+        with pytest.raises(fa.FaError) as e:
+            fa.fa_fwd_schedule(1, 1, 1, 128, 128, 64, False, **kw)
+        assert e.value.code == fa.FA_ERR_INVALID_ARG
+    with pytest.raises(fa.FaError) as e:
+        fa.fa_fwd_schedule(1, 3, 2, 128, 128, 64, False, num_sms=GB300_SMS, l2_bytes=GB300_L2)
+    assert e.value.code != fa.FA_OK
