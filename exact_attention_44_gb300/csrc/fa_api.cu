@@ -685,8 +685,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     a.tmDQ = &mdq;
     a.tmDK = &mdk;
     a.tmDV = &mdv;
-    a.grid = (int)std::min<int64_t>(units, info->sms);
-    a.grid_q = (int)std::min<int64_t>(units_q, info->sms);
+    // one CTA per SM (or per unit): dK/dV units from position c, dQ units from grid - 1 - c
+    a.grid = (int)std::min<int64_t>(std::max(units, units_q), info->sms);
     const int64_t pre_threads = (int64_t)Z * Hq * p.Tq * 128 * (D / 8);
     a.pre_grid = (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(pre_threads, 256), (int64_t)info->sms * 16));
     a.stream = stream;

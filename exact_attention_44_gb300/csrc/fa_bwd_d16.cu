@@ -24,16 +24,14 @@ static cudaError_t set_smem_once(K kernel, int smem, std::atomic<uint64_t>& conf
 template <bool CAUSAL, bool BF16>
 static cudaError_t launch_one(const BwdLaunchArgs& a) {
     using T = BwdTraits<16>;
-    auto kv = fa_bwd_kv_kernel<16, CAUSAL, BF16>;
-    auto dq = fa_bwd_dq_kernel<16, CAUSAL, BF16>;
-    static std::atomic<uint64_t> kv_configured{0}, dq_configured{0};
+    auto bwd = fa_bwd_kernel<16, CAUSAL, BF16>;
+    static std::atomic<uint64_t> configured{0};
     cudaError_t err;
-    if ((err = set_smem_once(kv, T::KV_SMEM_BYTES, kv_configured)) != cudaSuccess) return err;
-    if ((err = set_smem_once(dq, T::Q_SMEM_BYTES, dq_configured)) != cudaSuccess) return err;
-    // Δ and lse2 per query row; then dK, dV; then dQ
-    // each launch is a programmatic dependent of the one before it on the
-    // stream: its set-up overlaps that kernel's tail, and it waits for it
-    // (griddepcontrol.wait) before touching global memory
+    if ((err = set_smem_once(bwd, T::FUSED_SMEM_BYTES, configured)) != cudaSuccess) return err;
+    // Δ and lse2 per query row; then dK, dV and dQ in one launch.  Each
+    // launch is a programmatic dependent of the one before it on the stream:
+    // its set-up overlaps that kernel's tail, and it waits for it
+    // (griddepcontrol.wait) before touching global memory.
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -47,13 +45,8 @@ static cudaError_t launch_one(const BwdLaunchArgs& a) {
     if ((err = cudaLaunchKernelEx(&cfg, fa_bwd_pre_kernel<16, BF16>, a.params)) != cudaSuccess) return err;
     cfg.gridDim = dim3(a.grid);
     cfg.blockDim = dim3(BWD_THREADS);
-    cfg.dynamicSmemBytes = T::KV_SMEM_BYTES;
-    if ((err = cudaLaunchKernelEx(&cfg, kv, *a.tmK, *a.tmV, *a.tmQ, *a.tmDO, *a.tmDK, *a.tmDV, a.params)) !=
-        cudaSuccess)
-        return err;
-    cfg.gridDim = dim3(a.grid_q);
-    cfg.dynamicSmemBytes = T::Q_SMEM_BYTES;
-    return cudaLaunchKernelEx(&cfg, dq, *a.tmK, *a.tmV, *a.tmQ, *a.tmDO, *a.tmDQ, a.params);
+    cfg.dynamicSmemBytes = T::FUSED_SMEM_BYTES;
+    return cudaLaunchKernelEx(&cfg, bwd, *a.tmK, *a.tmV, *a.tmQ, *a.tmDO, *a.tmDK, *a.tmDV, *a.tmDQ, a.params);
 }
 
 cudaError_t launch_bwd_d16(const BwdLaunchArgs& a, bool causal, bool bf16) {

@@ -5,28 +5,29 @@
 // Triton Attention Kernel", step 8 and Correctness requirements: the backward
 // needs lse = m + log l).
 //
-// Three kernels on one stream:
-//   fa_bwd_pre_kernel  per query row: Δ = rowsum(dO ∘ O) and the base-2 lse;
-//   fa_bwd_kv_kernel   one unit per (128-key block, kv head): loops over every
+// Two kernels on one stream: fa_bwd_pre_kernel, then fa_bwd_kernel, which
+// runs a dK/dV phase and then a dQ phase in each CTA:
+//   pre kernel         per query row: Δ = rowsum(dO ∘ O) and the base-2 lse;
+//   dK/dV phase        one unit per (128-key block, kv head): loops over every
 //                      query block of every query head of the GQA group (from
 //                      the diagonal on when causal), keys as TMEM lanes:
 //                          Sᵀ  = K Qᵢᵀ,  Pᵀ = 2^(Sᵀ·scale·log2e − lse2ᵢ)
 //                          dPᵀ = V dOᵢᵀ, dSᵀ = Pᵀ ∘ (dPᵀ − Δᵢ)
 //                          dV += Pᵀ dOᵢ,  dK += dSᵀ Qᵢ   (Pᵀ, dSᵀ from TMEM)
 //                      dK (times scale) and dV stay in TMEM and are stored once;
-//   fa_bwd_dq_kernel   one unit per (128-row query block, query head): loops
+//   dQ phase           one unit per (128-row query block, query head): loops
 //                      over the key blocks it sees, queries as TMEM lanes:
 //                          S = Qᵢ Kⱼᵀ, dP = dOᵢ Vⱼᵀ, dS = P ∘ (dP − Δ),
 //                          dQ += dS Kⱼ   (dS from TMEM)
 //                      dQ (times scale) stays in TMEM and is stored once.
 // dQ is summed over key blocks inside one CTA, so no atomics are needed and
 // the result is bitwise reproducible; the price is recomputing S and dP in
-// the dQ kernel (7 tensor-core products per block pair instead of 5).
+// the dQ phase (7 tensor-core products per block pair instead of 5).
 //
-// Warps (both gradient kernels): 0-3 and 4-7 the two column halves of each
+// Warps (both phases): 0-3 and 4-7 the two column halves of each
 // 128x128 block (thread = TMEM lane), 8-11 the epilogue, 12 the TMA producer,
 // 13 the MMA issuer.  Every wait is bounded as in the forward kernel.  Head
-// dims 16 to 128 (the kv kernel's TMEM holds Sᵀ/Pᵀ, dPᵀ/dSᵀ, dV and dK:
+// dims 16 to 128 (the dK/dV phase's TMEM holds Sᵀ/Pᵀ, dPᵀ/dSᵀ, dV and dK:
 // 256 + 2D columns).
 #pragma once
 
@@ -86,7 +87,7 @@ struct BwdTraits {
     static constexpr uint32_t TM_DV = 256;
     static constexpr uint32_t TM_DK = 256 + D;
 
-    // ---- dQ kernel ----
+    // ---- dQ phase ----
     // shared memory: Q, dO of the unit; K, V of two key blocks
     static constexpr int Q_OFF_Q = 0;
     static constexpr int Q_OFF_DO = Q_OFF_Q + TILE;
@@ -109,6 +110,12 @@ struct BwdTraits {
     static constexpr int Q_SMEM_USED = Q_OFF_MISC + 16;
     static constexpr int Q_SMEM_BYTES = Q_SMEM_USED + 1024;
     static_assert(Q_SMEM_BYTES <= 227 * 1024, "shared memory budget");
+    // ---- the fused kernel: dK/dV phase, then dQ phase, in the same shared
+    // memory; the TMEM address and the abort flag sit past both layouts ----
+    static constexpr int FUSED_OFF_MISC = (KV_SMEM_USED > Q_SMEM_USED ? KV_SMEM_USED : Q_SMEM_USED) + 15 & ~15;
+    static constexpr int FUSED_SMEM_USED = FUSED_OFF_MISC + 16;
+    static constexpr int FUSED_SMEM_BYTES = FUSED_SMEM_USED + 1024;
+    static_assert(FUSED_SMEM_BYTES <= 227 * 1024, "shared memory budget");
     static constexpr uint32_t TM_QS = 0;      // [2] S (fp32); dS packed over columns s*128 + 0-31 and 64-95
     static constexpr uint32_t TM_QDP = 256;   // dP (fp32)
     static constexpr uint32_t TM_DQ = 384;
@@ -338,10 +345,9 @@ __device__ void kv_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0, uin
         ptx::tc_commit(bar(T::KB_KV_EMPTY));  // K, V free
         ++uc;
     }
-    if (!ok) {
-        ptx::tc_commit(bar(T::KB_DRAIN));
-        drain_phase(bar(T::KB_DRAIN), 0u, ctl.limit_ns);
-    }
+    // every MMA of this phase completes before the dQ phase reuses shared memory
+    ptx::tc_commit(bar(T::KB_DRAIN));
+    drain_phase(bar(T::KB_DRAIN), 0u, ctl.limit_ns);
 }
 
 // Thread = key (TMEM lane); half h takes queries h*64 .. h*64 + 63 and writes
@@ -483,75 +489,19 @@ __device__ __forceinline__ bool bwd_smem_base(uint8_t* raw, int used, int bytes,
     return true;
 }
 
-template <int D, bool CAUSAL, bool BF16>
-__global__ void __launch_bounds__(BWD_THREADS, 1)
-    fa_bwd_kv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
-                     const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV,
-                     const BwdParams p) {
-    using T = BwdTraits<D>;
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t* smem = nullptr;
-    if (!bwd_smem_base(smem_raw, T::KV_SMEM_USED, T::KV_SMEM_BYTES, p, smem)) return;
-    const uint32_t sbase = ptx::smem_addr(smem);
-    const uint32_t bar0 = sbase + T::KV_OFF_BAR;
-    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + T::KV_OFF_MISC);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + T::KV_OFF_MISC + 4);
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < T::KV_NUM_BARS; ++i) ptx::mbar_init(bar0 + 8u * i, T::kv_bar_count(i));
-        *abort_flag = 0;
-        ptx::fence_mbar_init();
-        ptx::prefetch_tmap(&tmK);
-        ptx::prefetch_tmap(&tmV);
-        ptx::prefetch_tmap(&tmQ);
-        ptx::prefetch_tmap(&tmDO);
-        ptx::prefetch_tmap(&tmDK);
-        ptx::prefetch_tmap(&tmDV);
-    }
-    if (warp == 13) {
-        ptx::tmem_alloc(ptx::smem_addr(const_cast<uint32_t*>(tmem_slot)), T::TMEM_COLS);
-        ptx::tmem_relinquish();
-    }
-    ptx::tc_fence_before();
-    __syncthreads();
-    ptx::tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const Ctl ctl{abort_flag, p.status, p.wait_limit_ns};
-    // launched as a programmatic dependent: the set-up above overlaps the
-    // previous kernel's tail; nothing below touches global memory before it
-    // has completed
-    ptx::grid_dependency_wait();
-    ptx::grid_launch_dependents();
-    if (warp < 8) {
-        kv_softmax<D, CAUSAL, BF16>(p, sbase, bar0, tmem, warp / 4, ctl);
-    } else if (warp < 12) {
-        kv_epilogue<D, CAUSAL, BF16>(&tmDK, &tmDV, p, sbase, bar0, tmem, ctl);
-    } else if (warp == 12) {
-        if (lane == 0) kv_producer<D, CAUSAL>(&tmK, &tmV, &tmQ, &tmDO, p, sbase, bar0, ctl);
-    } else {
-        if (lane == 0) kv_issuer<D, CAUSAL, BF16>(p, sbase, bar0, tmem, ctl);
-    }
-    ptx::tc_fence_before();
-    __syncthreads();
-    if (warp == 13) {
-        ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem, T::TMEM_COLS);
-    }
-}
 
 // ===================================================================== dQ ===
 
 template <int D, bool CAUSAL>
 __device__ void q_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const CUtensorMap* tmQ,
-                           const CUtensorMap* tmDO, const BwdParams& p, uint32_t sbase, uint32_t bar0, const Ctl& ctl) {
+                           const CUtensorMap* tmDO, const BwdParams& p, uint32_t sbase, uint32_t bar0, const Ctl& ctl, int first) {
     using T = BwdTraits<D>;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     const uint64_t pol_q = ptx::policy_evict_first();  // read once per unit
     const uint64_t pol_kv = ptx::policy_evict_last();  // read by every query block of the group
     uint32_t uc = 0, g = 0;
     bool ok = true;
-    for (int pos = blockIdx.x; ok && unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x) {
+    for (int pos = first; ok && unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x) {
         const DqUnit w = dq_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
         if (uc > 0 && !wait_phase(bar(T::QB_QD_EMPTY), (uc - 1) & 1u, ctl, SITE_B_QD_EMPTY)) { ok = false; break; }
         ptx::mbar_arrive_expect_tx(bar(T::QB_QD_FULL), 2 * T::TILE);
@@ -588,7 +538,7 @@ __device__ void q_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const
 // Per key block g: S_{g+1} goes to the other TMEM slot while the softmax
 // warps turn S_g and dP_g into dS_g; then dQ += dS_g K_g and dP_{g+1}.
 template <int D, bool CAUSAL, bool BF16>
-__device__ void q_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0, uint32_t tmem, const Ctl& ctl) {
+__device__ void q_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0, uint32_t tmem, const Ctl& ctl, int first) {
     using T = BwdTraits<D>;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     constexpr uint32_t ID_SQ = ptx::idesc_f16(128, 128, BF16, false, false);  // S = Q Kᵀ, dP = dO Vᵀ
@@ -618,7 +568,7 @@ __device__ void q_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0, uint
     };
     uint32_t uc = 0, g = 0;
     bool ok = true;
-    for (int pos = blockIdx.x; ok && unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x) {
+    for (int pos = first; ok && unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x) {
         const DqUnit w = dq_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
         if (!wait_phase(bar(T::QB_QD_FULL), uc & 1u, ctl, SITE_B_QD_FULL)) { ok = false; break; }
         if (!issue_s(g)) { ok = false; break; }
@@ -654,7 +604,7 @@ __device__ void q_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0, uint
 // Thread = query (TMEM lane); half h takes keys h*64 .. h*64 + 63 of each
 // block.  lse2 and Δ are per row, so they stay in registers for the unit.
 template <int D, bool CAUSAL, bool BF16>
-__device__ void q_softmax(const BwdParams& p, uint32_t bar0, uint32_t tmem, int h, const Ctl& ctl) {
+__device__ void q_softmax(const BwdParams& p, uint32_t bar0, uint32_t tmem, int h, const Ctl& ctl, int first) {
     using T = BwdTraits<D>;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     const int quad = (threadIdx.x / 32) % 4;
@@ -662,7 +612,7 @@ __device__ void q_softmax(const BwdParams& p, uint32_t bar0, uint32_t tmem, int 
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
     const float c = p.scale_log2;
     uint32_t g = 0;
-    for (int pos = blockIdx.x; unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x) {
+    for (int pos = first; unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x) {
         const DqUnit w = dq_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
         const int64_t r = ((int64_t)w.z * p.Hq + w.hq) * p.Tq * 128 + (int64_t)w.i * 128 + row;
         const float l2 = __ldg(p.lse2 + r), dl = __ldg(p.delta + r);
@@ -712,7 +662,7 @@ __device__ void q_softmax(const BwdParams& p, uint32_t bar0, uint32_t tmem, int 
 // Thread = TMEM lane = query: dQ (times scale) read out, released, stored.
 template <int D, bool CAUSAL, bool BF16>
 __device__ void q_epilogue(const CUtensorMap* tmDQ, const BwdParams& p, uint32_t sbase, uint32_t bar0, uint32_t tmem,
-                           const Ctl& ctl) {
+                           const Ctl& ctl, int first) {
     using T = BwdTraits<D>;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     const int quad = (threadIdx.x / 32) % 4;
@@ -723,7 +673,7 @@ __device__ void q_epilogue(const CUtensorMap* tmDQ, const BwdParams& p, uint32_t
         if (threadIdx.x % 32 == 0) ptx::bulk_wait_all();
     };
     uint32_t uc = 0;
-    for (int pos = blockIdx.x; unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x, ++uc) {
+    for (int pos = first; unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x, ++uc) {
         const DqUnit w = dq_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
         if (!warp_wait_phase(bar(T::QB_DQ_FULL), uc & 1u, ctl, SITE_B_DQ_FULL)) {
             drain();
@@ -742,28 +692,48 @@ __device__ void q_epilogue(const CUtensorMap* tmDQ, const BwdParams& p, uint32_t
     drain();
 }
 
+
+// ================================================================ pre pass ==
+// Per query row, padded to whole 128-row blocks: Δ = rowsum(dO ∘ O) in fp32
+// from the input-type values, and the lse in base 2 (+inf past Nq, so those
+// rows and columns get P = 0).  D/8 threads per row, 16 bytes of O and dO each.
+// ================================================================ fused ======
+// One launch runs both gradient kernels' work: each CTA takes its dK/dV units
+// (positions c, c + grid, ...), then, in the same shared memory and TMEM, its
+// dQ units from position grid - 1 - c on, so a CTA that drew one more dK/dV
+// unit than others draws one fewer dQ unit (Z4 H16 N1024: 512 + 512 units on
+// 152 CTAs, at most 7 per CTA instead of 4 + 4).  The phases need nothing
+// from each other (both read the pre kernel's lse2 and Delta), so no CTA
+// waits for another.  The dQ phase's barriers lie in memory the dK/dV phase
+// used for data; they are set up only after every role of that phase has
+// finished: its MMAs drained, its tensor stores read out.
 template <int D, bool CAUSAL, bool BF16>
 __global__ void __launch_bounds__(BWD_THREADS, 1)
-    fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
-                     const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
+    fa_bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
+                  const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV,
+                  const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
     using T = BwdTraits<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = nullptr;
-    if (!bwd_smem_base(smem_raw, T::Q_SMEM_USED, T::Q_SMEM_BYTES, p, smem)) return;
+    if (!bwd_smem_base(smem_raw, T::FUSED_SMEM_USED, T::FUSED_SMEM_BYTES, p, smem)) return;
     const uint32_t sbase = ptx::smem_addr(smem);
-    const uint32_t bar0 = sbase + T::Q_OFF_BAR;
-    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + T::Q_OFF_MISC);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + T::Q_OFF_MISC + 4);
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + T::FUSED_OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + T::FUSED_OFF_MISC + 4);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+    // ---- dK / dV ----
+    const uint32_t kbar0 = sbase + T::KV_OFF_BAR;
     if (threadIdx.x == 0) {
-        for (int i = 0; i < T::Q_NUM_BARS; ++i) ptx::mbar_init(bar0 + 8u * i, T::q_bar_count(i));
+        for (int i = 0; i < T::KV_NUM_BARS; ++i) ptx::mbar_init(kbar0 + 8u * i, T::kv_bar_count(i));
         *abort_flag = 0;
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&tmK);
         ptx::prefetch_tmap(&tmV);
         ptx::prefetch_tmap(&tmQ);
         ptx::prefetch_tmap(&tmDO);
+        ptx::prefetch_tmap(&tmDK);
+        ptx::prefetch_tmap(&tmDV);
         ptx::prefetch_tmap(&tmDQ);
     }
     if (warp == 13) {
@@ -775,29 +745,51 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const Ctl ctl{abort_flag, p.status, p.wait_limit_ns};
-    ptx::grid_dependency_wait();  // as in the dK/dV kernel
+    // launched as a programmatic dependent: the set-up above overlaps the
+    // previous kernel's tail; nothing below touches global memory before it
+    // has completed
+    ptx::grid_dependency_wait();
     ptx::grid_launch_dependents();
     if (warp < 8) {
-        q_softmax<D, CAUSAL, BF16>(p, bar0, tmem, warp / 4, ctl);
+        kv_softmax<D, CAUSAL, BF16>(p, sbase, kbar0, tmem, warp / 4, ctl);
     } else if (warp < 12) {
-        q_epilogue<D, CAUSAL, BF16>(&tmDQ, p, sbase, bar0, tmem, ctl);
+        kv_epilogue<D, CAUSAL, BF16>(&tmDK, &tmDV, p, sbase, kbar0, tmem, ctl);
     } else if (warp == 12) {
-        if (lane == 0) q_producer<D, CAUSAL>(&tmK, &tmV, &tmQ, &tmDO, p, sbase, bar0, ctl);
+        if (lane == 0) kv_producer<D, CAUSAL>(&tmK, &tmV, &tmQ, &tmDO, p, sbase, kbar0, ctl);
     } else {
-        if (lane == 0) q_issuer<D, CAUSAL, BF16>(p, sbase, bar0, tmem, ctl);
+        if (lane == 0) kv_issuer<D, CAUSAL, BF16>(p, sbase, kbar0, tmem, ctl);
     }
     ptx::tc_fence_before();
     __syncthreads();
+
+    // ---- dQ (skipped after an abort: the status word already says why) ----
+    if (*abort_flag == 0) {
+        const uint32_t qbar0 = sbase + T::Q_OFF_BAR;
+        if (threadIdx.x == 0) {
+            for (int i = 0; i < T::Q_NUM_BARS; ++i) ptx::mbar_init(qbar0 + 8u * i, T::q_bar_count(i));
+            ptx::fence_mbar_init();
+        }
+        __syncthreads();
+        ptx::tc_fence_after();
+        const int first = (int)gridDim.x - 1 - (int)blockIdx.x;
+        if (warp < 8) {
+            q_softmax<D, CAUSAL, BF16>(p, qbar0, tmem, warp / 4, ctl, first);
+        } else if (warp < 12) {
+            q_epilogue<D, CAUSAL, BF16>(&tmDQ, p, sbase, qbar0, tmem, ctl, first);
+        } else if (warp == 12) {
+            if (lane == 0) q_producer<D, CAUSAL>(&tmK, &tmV, &tmQ, &tmDO, p, sbase, qbar0, ctl, first);
+        } else {
+            if (lane == 0) q_issuer<D, CAUSAL, BF16>(p, sbase, qbar0, tmem, ctl, first);
+        }
+        ptx::tc_fence_before();
+        __syncthreads();
+    }
     if (warp == 13) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, T::TMEM_COLS);
     }
 }
 
-// ================================================================ pre pass ==
-// Per query row, padded to whole 128-row blocks: Δ = rowsum(dO ∘ O) in fp32
-// from the input-type values, and the lse in base 2 (+inf past Nq, so those
-// rows and columns get P = 0).  D/8 threads per row, 16 bytes of O and dO each.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
     ptx::grid_dependency_wait();  // O, dO and lse come from earlier kernels on the stream

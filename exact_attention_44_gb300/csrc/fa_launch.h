@@ -44,7 +44,7 @@ struct MergeArgs {
 };
 cudaError_t launch_lse_merge(const MergeArgs& a, bool bf16, int grid, cudaStream_t stream);
 
-// Backward: pre kernel, dK/dV kernel, dQ kernel on one stream
+// Backward: the pre kernel, then the fused dK/dV + dQ kernel, on one stream
 struct BwdLaunchArgs {
     const CUtensorMap* tmK;
     const CUtensorMap* tmV;
@@ -54,7 +54,7 @@ struct BwdLaunchArgs {
     const CUtensorMap* tmDK;
     const CUtensorMap* tmDV;
     BwdParams params;
-    int grid, grid_q, pre_grid;  // dK/dV kernel, dQ kernel, pre kernel
+    int grid, pre_grid;  // the fused dK/dV + dQ kernel, the pre kernel
     cudaStream_t stream;
 };
 cudaError_t launch_bwd_d16(const BwdLaunchArgs& a, bool causal, bool bf16);
