@@ -54,7 +54,7 @@ struct BwdTraits {
     static constexpr uint32_t SWIZZLE_CODE = SW == 128 ? 2u : SW == 64 ? 4u : 6u;
     static constexpr int TILE = 128 * D * 2;                  // one 128-row tile of Q, K, V or dO
 
-    // ---- dK / dV kernel ----
+    // ---- dK / dV phase ----
     // shared memory: K, V of the unit; Q, dO, lse2, Δ of two steps
     static constexpr int KV_OFF_K = 0;
     static constexpr int KV_OFF_V = KV_OFF_K + TILE;

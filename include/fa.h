@@ -280,10 +280,11 @@ fa_status fa_lse_merge(int nparts, const void* const* o_parts, const float* cons
  *
  * Requirements: those of fa_fwd, with D in {16, 32, 64, 128} (D = 256 returns
  * FA_ERR_UNSUPPORTED: dK and dV of a 128-key block live in tensor memory)
- * and Nq >= 1 whenever Z*Hkv*Nkv > 0.  Three kernels on `stream`: Delta and
- * lse per row; dK and dV (one CTA per key block and kv head, over every
- * query of the group); dQ (one CTA per query block and head, over its keys,
- * recomputing the scores).  No atomics: results are bitwise reproducible.
+ * and Nq >= 1 whenever Z*Hkv*Nkv > 0.  Two kernels on `stream`: Delta and
+ * lse per row; then one persistent kernel whose CTAs first compute dK and dV
+ * (a unit per key block and kv head, over every query of the group), then
+ * dQ (a unit per query block and head, over its keys, recomputing the
+ * scores).  No atomics: results are bitwise reproducible.
  * Errors: those of fa_fwd, plus FA_ERR_WORKSPACE for a missing, misaligned
  * or small workspace.
  */
