@@ -1117,8 +1117,11 @@ __global__ void __launch_bounds__(Traits<D>::THREADS, 1)
 //     λ = log2 Σ_s 2^λ_s,      O = Σ_s 2^(λ_s − λ) O_s,
 // the same rescaling by the change of maximum that the online softmax applies
 // between key blocks ("Write Triton Attention Kernel", Kernel design rules).
-// Four threads per row, each a quarter of the columns; every part's columns
-// of a thread are loaded together so their latencies overlap.
+// A thread takes a row and 32 of its columns, and loads a part's columns
+// together so their latencies overlap; when the tile has few rows, up to 32
+// lanes share a (row, columns) item and split the parts between them.
+// Measured on GB300 for a decode step (Z1 Hq32 Hkv8 Nq1 Nkv32768 D128: 8
+// tiles of 4 rows, about 19 parts each): one lane per item took 26 us.
 constexpr int MERGE_THREADS = 4 * BM;
 
 template <int D, bool CAUSAL, bool BF16>
@@ -1133,62 +1136,78 @@ __global__ void __launch_bounds__(MERGE_THREADS) fa_split_merge_kernel(const Fwd
     const int64_t t0 = S::tile_pos(head, mb, p);
     if (xb == t0) return;                                     // the cut falls between tiles
     if (b >= 2 && S::range_lo(b - 1, grid, p) > t0) return;  // an earlier cut merges this tile
-    const int r = threadIdx.x % BM, quarter = threadIdx.x / BM;
-    const int q_row = mb * BM + r;
-    if (q_row >= p.Nq) return;                                // no part stored this row
+    const int rows = p.Nq - mb * BM < BM ? p.Nq - mb * BM : BM;  // rows the parts stored
     const int64_t c0 = b - 1;
     const int64_t c1 = S::cta_of(t0 + S::tile_nkv(mb, p) - 1, grid, p);
     auto part = [&](int64_t c) -> const float* {
         return p.scratch + (c == c0 ? 2 * c + 1 : 2 * c) * p.slot_floats;
     };
-    // the parts' log-sum-exps of this row, PB at a time so their loads overlap
-    constexpr int PB = 8;
-    float mx = -INFINITY;
-    for (int64_t c = c0; c <= c1; c += PB) {
-        float x[PB];
-#pragma unroll
-        for (int i = 0; i < PB; ++i) x[i] = c + i <= c1 ? __ldg(part(c + i) + BM * D + r) : -INFINITY;
-#pragma unroll
-        for (int i = 0; i < PB; ++i) mx = fmaxf(mx, x[i]);
-    }
-    float den = 0.f;
-#pragma unroll 4
-    for (int64_t c = c0; c <= c1; ++c) den += exp2f(__ldg(part(c) + BM * D + r) - mx);
-    const float inv = 1.f / den;
+    // A work item is (row, CH float4 column groups).  With few rows (a
+    // decode step stores 4) there are fewer items than threads: then SPL
+    // consecutive lanes share an item, each taking every SPL-th part, so
+    // the parts' loads overlap instead of following one another, and the
+    // lanes combine max, normaliser and O by shuffles.  Every thread runs
+    // the same number of rounds, so the shuffles always see whole warps.
+    constexpr int W = D / 4;                      // float4 column groups of a row
+    constexpr int CH = W < 8 ? W : 8;             // groups per item
+    const int items = rows * (W / CH);
+    int spl = 1;
+    while (spl < 32 && items * spl * 2 <= MERGE_THREADS) spl *= 2;
+    const int lane_s = threadIdx.x % spl;
     const int z = (int)(head / p.Hq), hq = (int)(head % p.Hq);
-    if (quarter == 0 && p.lse != nullptr) p.lse[head * p.Nq + q_row] = (mx + log2f(den)) * 0.6931471805599453f;
-
-    constexpr int G4 = D / 16;                // float4 column groups per thread
-    constexpr int CHUNK = G4 < 8 ? G4 : 8;    // groups loaded together
-    uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
-                    2 * ((int64_t)z * p.so_z + (int64_t)hq * p.so_h + (int64_t)q_row * p.so_n);
+    for (int it0 = 0; it0 < items; it0 += MERGE_THREADS / spl) {
+        const int it = it0 + (int)threadIdx.x / spl;
+        const bool ok = it < items;
+        const int r = ok ? it / (W / CH) : 0, g0 = ok ? (it % (W / CH)) * CH : 0;
+        float mx = -INFINITY;
+        if (ok)
+            for (int64_t c = c0 + lane_s; c <= c1; c += spl) mx = fmaxf(mx, __ldg(part(c) + BM * D + r));
+        for (int m = spl / 2; m > 0; m /= 2) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+        float den = 0.f;
+        float4 acc[CH];
 #pragma unroll
-    for (int g0 = 0; g0 < G4; g0 += CHUNK) {
-        float4 acc[CHUNK];
-#pragma unroll
-        for (int i = 0; i < CHUNK; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = 0; i < CH; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (ok) {
 #pragma unroll 2
-        for (int64_t c = c0; c <= c1; ++c) {
-            const float* pc = part(c);
-            const float w = exp2f(__ldg(pc + BM * D + r) - mx);
-            const float4* col = reinterpret_cast<const float4*>(pc) + r;
-            float4 v[CHUNK];
+            for (int64_t c = c0 + lane_s; c <= c1; c += spl) {
+                const float* pc = part(c);
+                const float w = exp2f(__ldg(pc + BM * D + r) - mx);
+                den += w;
+                const float4* col = reinterpret_cast<const float4*>(pc) + r;
+                float4 v[CH];
 #pragma unroll
-            for (int i = 0; i < CHUNK; ++i) v[i] = __ldg(col + (quarter * G4 + g0 + i) * BM);
+                for (int i = 0; i < CH; ++i) v[i] = __ldg(col + (g0 + i) * BM);
 #pragma unroll
-            for (int i = 0; i < CHUNK; ++i) {
-                acc[i].x += w * v[i].x;
-                acc[i].y += w * v[i].y;
-                acc[i].z += w * v[i].z;
-                acc[i].w += w * v[i].w;
+                for (int i = 0; i < CH; ++i) {
+                    acc[i].x += w * v[i].x;
+                    acc[i].y += w * v[i].y;
+                    acc[i].z += w * v[i].z;
+                    acc[i].w += w * v[i].w;
+                }
             }
         }
+        for (int m = spl / 2; m > 0; m /= 2) {
+            den += __shfl_xor_sync(0xffffffffu, den, m);
 #pragma unroll
-        for (int i = 0; i < CHUNK; ++i) {
+            for (int i = 0; i < CH; ++i) {
+                acc[i].x += __shfl_xor_sync(0xffffffffu, acc[i].x, m);
+                acc[i].y += __shfl_xor_sync(0xffffffffu, acc[i].y, m);
+                acc[i].z += __shfl_xor_sync(0xffffffffu, acc[i].z, m);
+                acc[i].w += __shfl_xor_sync(0xffffffffu, acc[i].w, m);
+            }
+        }
+        if (!ok || lane_s != 0) continue;
+        const int q_row = mb * BM + r;
+        const float inv = 1.f / den;
+        if (g0 == 0 && p.lse != nullptr) p.lse[head * p.Nq + q_row] = (mx + log2f(den)) * 0.6931471805599453f;
+        uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
+                        2 * ((int64_t)z * p.so_z + (int64_t)hq * p.so_h + (int64_t)q_row * p.so_n);
+#pragma unroll
+        for (int i = 0; i < CH; ++i) {
             uint2 out;
             out.x = pack2<BF16>(acc[i].x * inv, acc[i].y * inv);
             out.y = pack2<BF16>(acc[i].z * inv, acc[i].w * inv);
-            reinterpret_cast<uint2*>(orow)[quarter * G4 + g0 + i] = out;
+            reinterpret_cast<uint2*>(orow)[g0 + i] = out;
         }
     }
 }
