@@ -97,11 +97,6 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Atomic add of four consecutive floats in global memory (16-byte aligned).
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
-                 :: "l"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
-}
 
 // Tensor store shared -> global of one box through a 4-D tensor map, in this
 // thread's current bulk-async group; box elements outside the tensor are not
@@ -192,12 +187,7 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool bf16, bool a
 //   bits 0-13 start >> 4, 16-29 leading byte offset >> 4, 32-45 stride byte
 //   offset >> 4, 46-47 version (1), 49-51 base offset (0: atoms 1024-B
 //   aligned), 61-63 swizzle (2 = 128 B, 4 = 64 B, 6 = 32 B).
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t swizzle_code) {
-    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | ((uint64_t)(swizzle_code & 7u) << 61);
-}
-
-// The same descriptor split into its two 32-bit words, so that stepping the
+// It is built as its two 32-bit words, so that stepping the
 // start address is one 32-bit add: the 14-bit start field never carries,
 // since shared-memory addresses stay below 2^18 bytes.
 __device__ __forceinline__ uint32_t smem_desc_lo(uint32_t saddr, uint32_t lbo) {
