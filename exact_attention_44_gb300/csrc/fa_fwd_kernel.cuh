@@ -1158,10 +1158,22 @@ __global__ void __launch_bounds__(MERGE_THREADS) fa_split_merge_kernel(const Fwd
     for (int it0 = 0; it0 < items; it0 += MERGE_THREADS / spl) {
         const int it = it0 + (int)threadIdx.x / spl;
         const bool ok = it < items;
-        const int r = ok ? it / (W / CH) : 0, g0 = ok ? (it % (W / CH)) * CH : 0;
+        // consecutive items are consecutive rows, so that a warp's loads of one
+        // column group ([group][row] in a part) are contiguous
+        const int r = ok ? it % rows : 0, g0 = ok ? (it / rows) * CH : 0;
+        // the parts' log-sum-exps of this row, PB loads at a time so that they overlap
+        constexpr int PB = 8;
         float mx = -INFINITY;
-        if (ok)
-            for (int64_t c = c0 + lane_s; c <= c1; c += spl) mx = fmaxf(mx, __ldg(part(c) + BM * D + r));
+        if (ok) {
+            for (int64_t c = c0 + lane_s; c <= c1; c += PB * spl) {
+                float x[PB];
+#pragma unroll
+                for (int i = 0; i < PB; ++i)
+                    x[i] = c + i * spl <= c1 ? __ldg(part(c + i * spl) + BM * D + r) : -INFINITY;
+#pragma unroll
+                for (int i = 0; i < PB; ++i) mx = fmaxf(mx, x[i]);
+            }
+        }
         for (int m = spl / 2; m > 0; m /= 2) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
         float den = 0.f;
         float4 acc[CH];
