@@ -1110,9 +1110,10 @@ __global__ void __launch_bounds__(Traits<D>::THREADS, 1)
 
 // ------------------------------------------------------------ split merge ---
 // Finishes every tile that the split schedule cut.  Block b - 1 looks at the
-// cut between the ranges of CTAs b - 1 and b; the first cut inside a tile
-// merges that tile, from the part CTA b - 1 ends with (slot 2(b-1) + 1) and
-// the parts CTAs b .. c1 start with (slots 2c).  With λ_s the base-2
+// cut between the ranges of CTAs b - 1 and b; the cuts inside a tile share
+// its rows, each merging a slice from the part CTA c0 (which holds the
+// tile's first block) ends with (slot 2 c0 + 1) and the parts CTAs
+// c0 + 1 .. c1 start with (slots 2c).  With λ_s the base-2
 // log-sum-exp of part s (over its keys) and O_s = its O / l,
 //     λ = log2 Σ_s 2^λ_s,      O = Σ_s 2^(λ_s − λ) O_s,
 // the same rescaling by the change of maximum that the online softmax applies
@@ -1134,11 +1135,18 @@ __global__ void __launch_bounds__(MERGE_THREADS) fa_split_merge_kernel(const Fwd
     int mb;
     S::tile_of(xb, p, head, mb);
     const int64_t t0 = S::tile_pos(head, mb, p);
-    if (xb == t0) return;                                     // the cut falls between tiles
-    if (b >= 2 && S::range_lo(b - 1, grid, p) > t0) return;  // an earlier cut merges this tile
-    const int rows = p.Nq - mb * BM < BM ? p.Nq - mb * BM : BM;  // rows the parts stored
-    const int64_t c0 = b - 1;
+    if (xb == t0) return;  // the cut falls between tiles
+    // The tile's parts come from CTAs c0 (the one holding its first block)
+    // .. c1, so the cuts inside it are c0 + 1 .. c1: each of those blocks
+    // merges one slice of the tile's rows.
+    const int64_t c0 = S::cta_of(t0, grid, p);
     const int64_t c1 = S::cta_of(t0 + S::tile_nkv(mb, p) - 1, grid, p);
+    const int tile_rows = p.Nq - mb * BM < BM ? p.Nq - mb * BM : BM;  // rows the parts stored
+    const int slices = (int)(c1 - c0), slice = (int)(b - 1 - c0);
+    const int per = (tile_rows + slices - 1) / slices;
+    const int row0 = slice * per;
+    const int rows = tile_rows - row0 < per ? tile_rows - row0 : per;  // rows of this block
+    if (rows <= 0) return;
     auto part = [&](int64_t c) -> const float* {
         return p.scratch + (c == c0 ? 2 * c + 1 : 2 * c) * p.slot_floats;
     };
@@ -1160,7 +1168,7 @@ __global__ void __launch_bounds__(MERGE_THREADS) fa_split_merge_kernel(const Fwd
         const bool ok = it < items;
         // consecutive items are consecutive rows, so that a warp's loads of one
         // column group ([group][row] in a part) are contiguous
-        const int r = ok ? it % rows : 0, g0 = ok ? (it / rows) * CH : 0;
+        const int r = ok ? row0 + it % rows : 0, g0 = ok ? (it / rows) * CH : 0;
         // the parts' log-sum-exps of this row, PB loads at a time so that they overlap
         constexpr int PB = 8;
         float mx = -INFINITY;
