@@ -3,12 +3,17 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
 
-One step = one pass of the whole path over one batch of the workload
-"Z=4 Hq=Hkv=16 Nq=Nkv=1024 D=128 bf16, non-causal and causal": two fa_fwd
-launches on the same inputs.  Metric: attention forward TFLOP/s, counting
-4*Nq*Nkv*D per head and half of it for causal.  Inputs are seeded synthetic
-N(0,1) (seeded_inputs); several input sets rotate so that consecutive steps
-never find their operands in L2.  Rank 0 prints one JSON line.
+One step = one pass of the whole path over one batch of the workload, by
+default the largest configuration the path is specified on that fits one GPU:
+"Z=1 Hq=32 Hkv=8 (GQA group 4) Nq=Nkv=32768 D=128 bf16, causal" -- one fa_fwd
+launch.  Metric: attention forward TFLOP/s, counting 4*Nq*Nkv*D per head and
+half of it for causal.  Inputs are seeded synthetic N(0,1) (seeded_inputs);
+input sets rotate so that consecutive steps never find their operands in L2.
+Rank 0 prints one JSON line; besides the headline it times the Z=4 H=16
+N=1024 D=128 workload and the D=128, N>=4096 non-causal shapes the
+throughput target is stated on, each with its own clock record.
+
+--profile runs only eager launches of --workload on one input set (for ncu).
 
 --impl reference times the fp64 CPU oracle on the host cores instead, on a
 bounded sample of the same workload (rows computed one by one).
@@ -51,12 +56,14 @@ WORKLOADS = {
     "z1_hq32_hkv8_nq1_nkv32768_d128_bf16_decode": (1, 32, 8, 1, 32768, 128, "bf16", [False]),
     "z1_h8_nq128_nkv65536_d128_bf16": (1, 8, 8, 128, 65536, 128, "bf16", [False]),
 }
-MAIN = "z4_h16_n1024_d128_bf16"
+MAIN = "z1_hq32_hkv8_n32768_d128_bf16_causal"
 # the shapes the throughput target is stated on (D = 128, N >= 4096, non-causal)
 TARGET_SHAPES = ["z1_hq32_hkv8_n8192_d128_bf16_noncausal", "z1_hq32_hkv8_nq1024_nkv8192_d128_bf16_cross"]
+# timed besides the headline, each as its own line (rotated inputs, own clock record)
+EXTRA_SHAPES = ["z4_h16_n1024_d128_bf16"] + TARGET_SHAPES
 # timed through both entry points: whole tiles (fa_fwd) and cut key ranges where that pays (fa_fwd_splitkv)
-SPLIT_SHAPES = TARGET_SHAPES + ["z1_hq32_hkv8_n32768_d128_bf16_causal", "z1_hq32_hkv8_nq1_nkv32768_d128_bf16_decode",
-                                "z1_h8_nq128_nkv65536_d128_bf16"]
+SPLIT_SHAPES = ["z1_hq32_hkv8_nq1_nkv32768_d128_bf16_decode", "z1_h8_nq128_nkv65536_d128_bf16",
+                "z1_hq32_hkv8_nq1024_nkv8192_d128_bf16_cross"]
 
 
 def flops_of(Z, Hq, Nq, Nkv, D, causal) -> float:
@@ -92,30 +99,34 @@ def load_peaks():
 
 
 # the sources the forward kernel of head dim D is compiled from
-FWD_SOURCES = ["fa_fwd_kernel.cuh", "fa_ptx.cuh", "fa_params.h", "fa_launch.h", "fa_fwd_d{D}.cu"]
+FWD_SOURCES = ["fa_fwd_kernel.cuh", "fa_ptx.cuh", "fa_params.h", "fa_launch.h", "fa_fwd_dim.cu"]
 
 
-def kernel_source_hash(D: int = 128) -> str:
+def kernel_source_hash() -> str:
     """Hash of the forward kernel's own sources (a change anywhere else leaves its counters valid)."""
     h = hashlib.sha256()
     for name in FWD_SOURCES:
-        name = name.format(D=D)
         h.update(name.encode() + b"\0" + open(os.path.join(ROOT, "exact_attention_44_gb300", "csrc", name), "rb").read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str, D: int = 128):
+def recorded_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if taken on the current kernel source."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     try:
-        rec = json.load(open(p)).get(kernel)
+        rec = json.load(open(p)).get(f"{kernel} {workload}")
     except Exception:
         return None
-    if not rec or rec.get("source_hash") != kernel_source_hash(D):
+    if not rec or rec.get("source_hash") != kernel_source_hash():
         return None
     return rec.get("dram_bytes_per_launch")
+
+
+def kernel_name(wl, causal) -> str:
+    Z, Hq, Hkv, Nq, Nkv, D, dtype, _ = wl
+    return f"fa_fwd_kernel<{D},{str(causal).lower()},{'bf16' if dtype == 'bf16' else 'fp16'}>"
 
 
 # ------------------------------------------------------------------ clocks --
@@ -178,27 +189,24 @@ def make_inputs(wl, seed, device):
     return host, [h.to(device) for h in host]
 
 
-def run_native(args, rank, world, device):
+def time_workload(fa, wl, steps, warmup, device, stream, world, eager=False, dev0=None, sample_clocks=True):
+    """Time `steps` steps of a workload (every causal flag of it once per step).
+
+    Input sets rotate so that their total exceeds 3x L2: no step finds its
+    operands in L2 from the step before.  Unless eager, the timed loop replays
+    CUDA graphs: per causal flag, one graph holding that flag's launch on each
+    input set in turn; the K % nsets remaining steps run as eager launches.
+    CUDA events on the launching stream bracket every replay; nvidia-smi
+    samples the clocks meanwhile.  Returns a dict of timings."""
     import torch
 
-    import exact_attention_44_gb300 as fa
-
-    fa.build()
-    fa.load()
-    peaks = load_peaks()
-    wl = WORKLOADS[args.workload]
     Z, Hq, Hkv, Nq, Nkv, D, dtype, flags = wl
     scale = 1.0 / math.sqrt(D)
     tdt = torch.float16 if dtype == "fp16" else torch.bfloat16
-    # a stream of its own (CUDA graphs are not captured on the default stream),
-    # made current so that every copy and launch below is ordered on it
-    stream = torch.cuda.Stream(device)
-    torch.cuda.set_stream(stream)
-
-    # rotating input sets: their total is > 3x L2, so a step never reuses the previous step's operands in L2
     per_set = sum(io_bytes(wl))
     nsets = max(2, min(8, math.ceil(3 * L2_BYTES / per_set)))
-    host, dev0 = make_inputs(wl, 0, device)
+    if dev0 is None:
+        _, dev0 = make_inputs(wl, 0, device)
     sets = [dev0] + [[x.clone() for x in dev0] for _ in range(nsets - 1)]
     outs = [[(torch.empty((Z, Hq, Nq, D), dtype=tdt, device=device),
               torch.empty((Z, Hq, Nq), dtype=torch.float32, device=device)) for _ in flags] for _ in range(nsets)]
@@ -208,18 +216,15 @@ def run_native(args, rank, world, device):
         o, lse = outs[i % nsets][f]
         fa.fa_fwd(q, k, v, o=o, lse=lse, scale=scale, causal=flags[f], stream=stream)
 
-    for i in range(args.warmup):
+    for i in range(warmup):  # untimed warm-up steps
         for f in range(len(flags)):
             launch(i, f)
     torch.cuda.synchronize(device)
     code, word = fa.fa_device_status(stream)
     if code != fa.FA_OK:
         raise RuntimeError(f"device status after warm-up: {word:#x}")
-    # The timed loop replays CUDA graphs: per causal flag, one graph holding that
-    # flag's launch on each of the nsets input sets in turn (nsets steps' worth
-    # of that flag's work).  A replay of every flag's graph is nsets whole steps.
     graphs = []
-    if not args.eager:
+    if not eager:
         with torch.cuda.stream(stream):
             for f in range(len(flags)):
                 g = torch.cuda.CUDAGraph()
@@ -230,12 +235,12 @@ def run_native(args, rank, world, device):
         for g in graphs:
             g.replay()
         torch.cuda.synchronize(device)
-    # exactly K steps: K // nsets replays of every flag's graph, then the
-    # remaining K % nsets steps as eager launches, all inside the timed region
-    reps = args.steps // nsets if graphs else 0
-    tail = args.steps - reps * nsets
+    # exactly `steps` steps: steps // nsets replays of every flag's graph, then
+    # the remaining steps as eager launches, all inside the timed region
+    reps = steps // nsets if graphs else 0
+    tail = steps - reps * nsets
     barrier(world)
-    clocks = ClockSampler(device.index if device.index is not None else 0) if rank == 0 else None
+    clocks = ClockSampler(device.index if device.index is not None else 0) if sample_clocks else None
     time.sleep(0.25 if clocks else 0)
     torch.cuda.synchronize(device)
     nrec = reps + tail
@@ -262,46 +267,76 @@ def run_native(args, rank, world, device):
     code, word = fa.fa_device_status(stream)
     if code != fa.FA_OK:
         raise RuntimeError(f"device status after timing: {word:#x}")
-    max_ms = all_reduce_max(total_ms, world, device)
+    launch_desc = ("eager fa_fwd calls" if not graphs else
+                   f"CUDA graph per causal flag, {nsets} fa_fwd launches (one per input set) per replay")
+    del sets, outs, graphs
+    return {"total_ms": total_ms, "per_kernel_ms": per_kernel_ms, "nsets": nsets, "per_set": per_set,
+            "clock": clock, "launch": launch_desc}
 
+
+def roofline_of(wl, t, peaks, workload):
+    """The dominant launch (largest share of the step) against the bf16 tensor peak."""
+    Z, Hq, Hkv, Nq, Nkv, D, dtype, flags = wl
+    shares = [sum(x) for x in t["per_kernel_ms"]]
+    dom = max(range(len(flags)), key=lambda f: shares[f])
+    dom_ms = statistics.fmean(t["per_kernel_ms"][dom])
+    achieved = flops_of(Z, Hq, Nq, Nkv, D, flags[dom]) / (dom_ms * 1e-3) / 1e12
+    kname = kernel_name(wl, flags[dom])
+    return {"bound": "tensor", "kernel": kname, "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+            "peak_source": f"{peaks['source']} bf16 burst (cuBLAS)",
+            "frac_of_sustained": (round(achieved / peaks["bf16_tflops_sustained"], 4)
+                                  if peaks.get("bf16_tflops_sustained") else None),
+            "traffic": recorded_traffic(kname, workload),
+            "algorithmic_bytes": algorithmic_bytes(wl), "ms_per_launch": round(dom_ms, 5)}
+
+
+def run_native(args, rank, world, device):
+    import torch
+
+    import exact_attention_44_gb300 as fa
+
+    fa.build()
+    fa.load()
+    peaks = load_peaks()
+    wl = WORKLOADS[args.workload]
+    Z, Hq, Hkv, Nq, Nkv, D, dtype, flags = wl
+    scale = 1.0 / math.sqrt(D)
+    # a stream of its own (CUDA graphs are not captured on the default stream),
+    # made current so that every copy and launch below is ordered on it
+    stream = torch.cuda.Stream(device)
+    torch.cuda.set_stream(stream)
+
+    host, dev0 = make_inputs(wl, 0, device)
+    t = time_workload(fa, wl, args.steps, args.warmup, device, stream, world, eager=args.eager, dev0=dev0,
+                      sample_clocks=rank == 0)
+    max_ms = all_reduce_max(t["total_ms"], world, device)
     flops = step_flops(wl)
     value = world * flops * args.steps / (max_ms * 1e-3) / 1e12
-
-    # dominant kernel: the launch kind with the largest share of the step
-    shares = [sum(x) for x in per_kernel_ms]
-    dom = max(range(len(flags)), key=lambda f: shares[f])
-    dom_ms = statistics.fmean(per_kernel_ms[dom])
-    dom_flops = flops_of(Z, Hq, Nq, Nkv, D, flags[dom])
-    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
-    kname = f"fa_fwd_kernel<{D},{str(flags[dom]).lower()},{'bf16' if dtype == 'bf16' else 'fp16'}>"
-    roofline = {"bound": "tensor", "kernel": kname, "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
-                "peak_source": f"{peaks['source']} bf16 burst (cuBLAS)",
-                "frac_of_sustained": (round(achieved / peaks["bf16_tflops_sustained"], 4)
-                                      if peaks.get("bf16_tflops_sustained") else None),
-                "traffic": recorded_traffic(kname, D),
-                "algorithmic_bytes": algorithmic_bytes(wl), "ms_per_launch": round(dom_ms, 5)}
-
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": "synthetic (seeded N(0,1))",
         "config": {"workload": args.workload, "Z": Z, "Hq": Hq, "Hkv": Hkv, "Nq": Nq, "Nkv": Nkv, "D": D,
                    "causal_per_step": flags, "scale": scale, "layout": "BNSD contiguous",
-                   "l2": f"{nsets} rotating input sets ({nsets * per_set / 2**20:.0f} MiB > 3x L2)",
-                   "launch": ("eager fa_fwd calls" if not graphs else
-                              f"CUDA graph per causal flag, {nsets} fa_fwd launches (one per input set) per replay"),
-                   "parallelism": "replicas only" if world > 1 else "single GPU"},
+                   "l2": f"{t['nsets']} rotating input sets ({t['nsets'] * t['per_set'] / 2**20:.0f} MiB > 3x L2)",
+                   "launch": t["launch"], "parallelism": "replicas only" if world > 1 else "single GPU"},
         "frac_of_peak": round(value / world / peaks["bf16_tflops"], 4),
-        "per_launch_ms": {f"causal={c}": round(statistics.fmean(per_kernel_ms[f]), 5) for f, c in enumerate(flags)},
-        "roofline": roofline,
+        "per_launch_ms": {f"causal={c}": round(statistics.fmean(t["per_kernel_ms"][f]), 5)
+                          for f, c in enumerate(flags)},
+        "roofline": roofline_of(wl, t, peaks, args.workload),
         "gpu_launches": len(flags) * args.steps,
-        "clocks": clock,
+        "clocks": t["clock"],
     }
     if not args.no_e2e:
         result["e2e"] = run_e2e(args, wl, host, flags, scale, device, stream, world)
+        if rank == 0:
+            result["e2e"]["host_link"] = measure_host_link(wl, host, device, stream)
+    del host, dev0
+    torch.cuda.empty_cache()
     if args.shapes and rank == 0:
-        result["target_shapes"] = [measure_shape(name, device, stream, peaks) for name in TARGET_SHAPES]
+        result["extra_shapes"] = [measure_extra(fa, name, device, stream, peaks, world) for name in EXTRA_SHAPES
+                                  if name != args.workload]
         result["split_kv_shapes"] = [measure_shape(name, device, stream, peaks, impl=impl)
                                      for name in SPLIT_SHAPES for impl in ("fwd", "splitkv")]
         result["variant_shapes"] = [measure_variant(name, device, stream, peaks) for name in VARIANT_SHAPES]
@@ -309,9 +344,28 @@ def run_native(args, rank, world, device):
     return result
 
 
+def measure_extra(fa, name, device, stream, peaks, world):
+    """One more workload timed like the headline (graph replays, rotated inputs, own clock record)."""
+    import torch
+
+    wl = WORKLOADS[name]
+    # about a quarter of a second of timed work
+    steps = max(20, min(2000, int(0.25 / max(step_flops(wl) / 1.2e15, 1e-6))))
+    t = time_workload(fa, wl, steps, 5, device, stream, world)
+    value = step_flops(wl) * steps / (t["total_ms"] * 1e-3) / 1e12
+    flags = wl[7]
+    torch.cuda.empty_cache()
+    return {"workload": name, "tflops": round(value, 2), "frac_of_peak": round(value / peaks["bf16_tflops"], 4),
+            "ms_per_step": round(t["total_ms"] / steps, 5), "steps": steps,
+            "per_launch_ms": {f"causal={c}": round(statistics.fmean(t["per_kernel_ms"][f]), 5)
+                              for f, c in enumerate(flags)},
+            "roofline": roofline_of(wl, t, peaks, name),
+            "l2": f"{t['nsets']} rotating input sets", "launch": t["launch"], "clocks": t["clock"]}
+
+
 def run_e2e(args, wl, host, flags, scale, device, stream, world):
     """Same metric through the public API with host buffers: H2D of Q/K/V from pinned memory,
-    both launches, D2H of O and lse, every step, all inside the timed region.
+    every launch of the step, D2H of O and lse, every step, all inside the timed region.
 
     Steps alternate between two streams, each with its own device and pinned host buffers,
     so that one step's device-to-host copies overlap the next step's host-to-device copies
@@ -360,13 +414,86 @@ def run_e2e(args, wl, host, flags, scale, device, stream, world):
     torch.cuda.synchronize(device)
     ms = all_reduce_max(a.elapsed_time(b), world, device)
     h2d, d2h = io_bytes(wl)
+    del lanes
     return {"value": round(world * step_flops(wl) * steps / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": round(ms / steps, 4), "streams": 2}
 
 
+def measure_host_link(wl, host, device, stream, reps=10):
+    """Plain pinned-memory copy bandwidth with the e2e step's byte counts: the host link's ceiling
+    for e2e.  H2D of Q, K, V alone; D2H of O and lse alone; and both at once on two streams."""
+    import torch
+
+    Z, Hq, Hkv, Nq, Nkv, D, dtype, flags = wl
+    dev_in = [torch.empty_like(h, device=device) for h in host]
+    dev_out = [torch.empty((Z, Hq, Nq, D), dtype=host[0].dtype, device=device),
+               torch.empty((Z, Hq, Nq), dtype=torch.float32, device=device)]
+    host_out = [torch.empty_like(d, device="cpu").pin_memory() for d in dev_out]
+    s2 = torch.cuda.Stream(device=device)
+    h2d, d2h = io_bytes(wl)
+    d2h = d2h // max(1, len(flags))  # one launch's outputs
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize(device)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        s2.wait_event(a)
+        for _ in range(reps):
+            fn()
+        done = torch.cuda.Event()
+        done.record(s2)
+        stream.wait_event(done)
+        b.record(stream)
+        torch.cuda.synchronize(device)
+        return a.elapsed_time(b) / reps
+
+    def up():
+        with torch.cuda.stream(stream):
+            for d, h in zip(dev_in, host):
+                d.copy_(h, non_blocking=True)
+
+    def down(s=None):
+        with torch.cuda.stream(s or stream):
+            for d, h in zip(dev_out, host_out):
+                h.copy_(d, non_blocking=True)
+
+    ms_up = timed(up)
+    ms_down = timed(down)
+    ms_both = timed(lambda: (up(), down(s2)))
+    del dev_in, dev_out, host_out
+    return {"h2d_gbs": round(h2d / (ms_up * 1e-3) / 1e9, 1), "d2h_gbs": round(d2h / (ms_down * 1e-3) / 1e9, 1),
+            "both_ms": round(ms_both, 4), "h2d_ms": round(ms_up, 4), "d2h_ms": round(ms_down, 4),
+            "what": "plain pinned cudaMemcpyAsync of one step's inputs (H2D) and one launch's outputs (D2H), "
+                    "alone and at once on two streams"}
+
+
+def run_profile(args, device):
+    """Eager launches of one workload on one input set, nothing else (a small, predictable ncu target)."""
+    import torch
+
+    import exact_attention_44_gb300 as fa
+    fa.build()
+    fa.load()
+    wl = WORKLOADS[args.workload]
+    Z, Hq, Hkv, Nq, Nkv, D, dtype, flags = wl
+    _, (q, k, v) = make_inputs(wl, 0, device)
+    stream = torch.cuda.current_stream(device)
+    o = torch.empty((Z, Hq, Nq, D), dtype=q.dtype, device=device)
+    lse = torch.empty((Z, Hq, Nq), dtype=torch.float32, device=device)
+    for _ in range(args.warmup + args.steps):
+        for c in flags:
+            fa.fa_fwd(q, k, v, o=o, lse=lse, causal=c, stream=stream)
+    torch.cuda.synchronize(device)
+    code, word = fa.fa_device_status(stream)
+    if code != fa.FA_OK:
+        raise RuntimeError(f"device status: {word:#x}")
+    print(json.dumps({"profile": args.workload, "launches": (args.warmup + args.steps) * len(flags)}), flush=True)
+
+
 def measure_shape(name, device, stream, peaks, steps=10, impl="fwd"):
-    """TFLOP/s of one extra workload (same timing method, 10 steps, inputs > L2 or rotated).
+    """TFLOP/s of one extra workload (eager launches, 10 steps, inputs > L2 or rotated).
 
     impl "fwd" calls fa_fwd; "splitkv" calls fa_fwd_splitkv, which cuts the key
     ranges across SMs when that beats whole tiles."""
@@ -649,18 +776,21 @@ def all_reduce_max(x: float, world: int, device) -> float:
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=12000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=MAIN)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--eager", action="store_true", help="time eager fa_fwd calls instead of CUDA-graph replays")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--shapes", dest="shapes", action="store_true", default=True,
-                    help="also time the D=128, N>=4096 non-causal target shapes (default)")
+                    help="also time the Z=4 H=16 N=1024 workload, the D=128 N>=4096 non-causal target shapes, "
+                         "split-KV, variant and backward workloads (default)")
     ap.add_argument("--no-shapes", dest="shapes", action="store_false")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for cpu_baseline (and the cap per step of --impl reference)")
+    ap.add_argument("--profile", action="store_true",
+                    help="only W + K eager launches of --workload on one input set, no timing (an ncu target)")
     ap.add_argument("--bwd-only", action="store_true",
                     help="time only fa_bwd on --workload (one JSON line per causal flag; for profiling)")
     ap.add_argument("--all", action="store_true",
@@ -683,6 +813,9 @@ def main(argv=None):
         raise SystemExit("bench.py: no CUDA device (the native path has no CPU fallback)")
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
+    if args.profile:
+        run_profile(args, device)
+        return 0
     if args.bwd_only:
         import exact_attention_44_gb300 as fa
         fa.build()

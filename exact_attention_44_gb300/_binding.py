@@ -33,6 +33,8 @@ _SIGNATURES = {
                        [ctypes.c_void_p] * 4 + [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                                  ctypes.c_size_t, ctypes.c_void_p]),
     "fa_fwd_splitkv_workspace_size": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]),
+    "fa_fwd_splitkv_workspace_size_for": (ctypes.c_int, [ctypes.c_int, ctypes.c_int,
+                                                         ctypes.POINTER(ctypes.c_size_t)]),
     "fa_bwd": (ctypes.c_int, [ctypes.c_void_p] * 9 + [ctypes.c_int] * 6 + [ctypes.c_void_p] * 8 +
                [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "fa_bwd_workspace_size": (ctypes.c_int, [ctypes.c_int] * 4 + [ctypes.POINTER(ctypes.c_size_t)]),
@@ -293,6 +295,15 @@ def fa_fwd_splitkv_workspace_size(D: int, device=None) -> int:
         rc = load().fa_fwd_splitkv_workspace_size(int(D), ctypes.byref(n))
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd_splitkv_workspace_size")
+    return n.value
+
+
+def fa_fwd_splitkv_workspace_size_for(D: int, num_sms: int) -> int:
+    """Workspace bytes fa_fwd_splitkv needs for head dim D on a device of num_sms SMs (host only)."""
+    n = ctypes.c_size_t(0)
+    rc = load().fa_fwd_splitkv_workspace_size_for(int(D), int(num_sms), ctypes.byref(n))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_splitkv_workspace_size_for")
     return n.value
 
 

@@ -23,8 +23,13 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libfa.so")
 
-SOURCES = (["fa_api.cu", "fa_lse_merge.cu", "fa_noalloc.cu"] + [f"fa_fwd_d{d}.cu" for d in (16, 32, 64, 128, 256)] +
-           [f"fa_bwd_d{d}.cu" for d in (16, 32, 64, 128)])
+# (source, object, extra flags): the per-head-dim launchers are one source
+# each, compiled once per supported head dim
+FWD_DIMS = (16, 32, 64, 128, 256)
+BWD_DIMS = (16, 32, 64, 128)
+UNITS = ([(src, src.replace(".cu", ".o"), []) for src in ("fa_api.cu", "fa_lse_merge.cu", "fa_noalloc.cu")] +
+         [("fa_fwd_dim.cu", f"fa_fwd_d{d}.o", [f"-DFA_HEAD_DIM={d}"]) for d in FWD_DIMS] +
+         [("fa_bwd_dim.cu", f"fa_bwd_d{d}.o", [f"-DFA_HEAD_DIM={d}"]) for d in BWD_DIMS])
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
                 "--expt-relaxed-constexpr", f"-I{INCLUDE}", f"-I{CSRC}"]
@@ -58,9 +63,9 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
         return LIB
     cc = nvcc()
     jobs = []
-    for src in SOURCES:
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
-        cmd = [cc, *FLAGS, *extra_flags, "-c", os.path.join(CSRC, src), "-o", obj]
+    for src, obj_name, unit_flags in UNITS:
+        obj = os.path.join(BUILD, obj_name)
+        cmd = [cc, *FLAGS, *unit_flags, *extra_flags, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         jobs.append((src, obj, cmd))
@@ -68,7 +73,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
     def run(job):
         src, obj, cmd = job
         r = subprocess.run(cmd, capture_output=True, text=True)
-        return src, r
+        return os.path.basename(obj), r
 
     with cf.ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 4)) as ex:
         results = list(ex.map(run, jobs))

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cfloat>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -22,25 +23,51 @@ __device__ uint32_t g_fa_status;  // first device-side error of any launch on th
 
 constexpr int kMaxDevices = 64;
 
+// What a launch needs to know about device `dev` (the current device): its
+// SM count and L2 size (fixed for the device), and the device address of the
+// status word, which belongs to the current CUDA context: it is looked up
+// again when the context changes (after cudaDeviceReset the module is loaded
+// anew and the word may move).  Failures are not remembered.
 struct DeviceInfo {
-    std::once_flag once;
-    cudaError_t err = cudaSuccess;
+    std::mutex mu;
+    bool have_attrs = false;
     int sms = 0;
     int l2_bytes = 0;
+    uint64_t ctx = 0;  // context the status address was looked up in (0: none yet)
     uint32_t* status = nullptr;
 };
 DeviceInfo g_devices[kMaxDevices];
 
-cudaError_t device_info(int dev, DeviceInfo** out) {
+struct LaunchInfo {
+    int sms;
+    int l2_bytes;
+    uint32_t* status;
+};
+
+cudaError_t device_info(int dev, LaunchInfo* out) {
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     DeviceInfo& d = g_devices[dev];
-    std::call_once(d.once, [&] {
-        d.err = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
-        if (d.err == cudaSuccess) d.err = cudaDeviceGetAttribute(&d.l2_bytes, cudaDevAttrL2CacheSize, dev);
-        if (d.err == cudaSuccess) d.err = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_fa_status);
-    });
-    *out = &d;
-    return d.err;
+    std::lock_guard<std::mutex> lock(d.mu);
+    cudaError_t err;
+    if (!d.have_attrs) {
+        int sms = 0, l2 = 0;
+        if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
+        if ((err = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev)) != cudaSuccess) return err;
+        d.sms = sms;
+        d.l2_bytes = l2;
+        d.have_attrs = true;
+    }
+    // the status word's address in the current context, looked up on the
+    // first call in a context (which should come before any stream capture)
+    const uint64_t ctx = fa::current_context_id();
+    if (ctx == 0 || ctx != d.ctx || d.status == nullptr) {
+        void* status = nullptr;
+        if ((err = cudaGetSymbolAddress(&status, g_fa_status)) != cudaSuccess) return err;
+        d.status = static_cast<uint32_t*>(status);
+        d.ctx = fa::current_context_id();  // the lookup may have created the context
+    }
+    *out = LaunchInfo{d.sms, d.l2_bytes, d.status};
+    return cudaSuccess;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -55,6 +82,28 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
             fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
     });
     return fn;
+}
+
+// cuCtxGetCurrent and cuCtxGetId through the runtime's driver entry points
+// (no link against libcuda): the ID of the calling thread's current context.
+struct CtxFns {
+    PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    PFN_cuCtxGetId_v12000 get_id = nullptr;
+};
+const CtxFns& ctx_fns() {
+    static const CtxFns fns = [] {
+        CtxFns f;
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            f.get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            f.get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+        return f;
+    }();
+    return fns;
 }
 
 std::atomic<uint64_t> g_wait_limit_ns{0};
@@ -87,6 +136,31 @@ fa_status cuda_fail(const char* what, CUresult r) { return cuda_fail(what, (int)
 bool supported_head_dim(int D) { return D == 16 || D == 32 || D == 64 || D == 128 || D == 256; }
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// The forward kernels take the softmax scale as c = |scale|·log2(e) > 0 and
+// its sign separately.  They reference the probabilities of a row to the
+// maximum of the raw scores times c and mask keys by setting raw scores to
+// -inf, both of which need c > 0:
+//   * scale < 0: the S = Q Kᵀ products negate Q (the tensor core's negate-A
+//     bit, exact in fp16/bf16), so raw score times c is scale·s·log2(e);
+//   * scale = 0 (every kept key weighs the same): c is the smallest normal
+//     fp32 value 2^-126.  For a score |s| < 2^100, s·c has magnitude below
+//     2^-25, where 2^x rounds to 1 in fp32, so every kept key gets p = 1 as
+//     with scale 0, and masked keys (-inf) still get p = 0;
+//   * a scale whose c overflows fp32 (|scale| > FLT_MAX / log2(e), about
+//     2.4e38) is rejected: no scaled score would be representable.
+// Returns false for a scale the kernels cannot take (non-finite, or c
+// overflows).
+bool fwd_scale(float scale, float* c, int* negate) {
+    if (!std::isfinite(scale)) return false;
+    const double x = std::fabs((double)scale) * 1.4426950408889634;  // exp(y) = 2^(y log2 e)
+    if (!(x <= (double)FLT_MAX)) return false;
+    float cf = (float)x;
+    if (!(cf >= FLT_MIN)) cf = FLT_MIN;  // zero, or below the normal range
+    *c = cf;
+    *negate = scale < 0.f ? 1 : 0;
+    return true;
+}
 
 fa_status check_shape(int Z, int Hq, int Hkv, int Nq, int Nkv, int D, int causal) {
     if (Z < 0 || Hq < 0 || Hkv < 1 || Nq < 0 || Nkv < 0) return FA_ERR_INVALID_ARG;
@@ -140,6 +214,16 @@ CUresult make_map(CUtensorMap* map, const void* ptr, fa_dtype dt, int D, int N, 
 }  // namespace
 
 namespace fa {
+uint64_t current_context_id() {
+    const CtxFns& f = ctx_fns();
+    if (f.get_current == nullptr || f.get_id == nullptr) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (f.get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+    if (f.get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return (uint64_t)id;
+}
+
 template <int D>
 static void facts(int* bn, int* smem, int* swe) {
     *bn = Traits<D>::BN;
@@ -327,7 +411,9 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* 
                         dtype, stream, split, workspace, workspace_bytes);
     }
     if (dtype != FA_DTYPE_F16 && dtype != FA_DTYPE_BF16) return FA_ERR_UNSUPPORTED;
-    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;  // a softmax temperature is positive
+    float c = 0.f;
+    int negate = 0;
+    if (!fwd_scale(scale, &c, &negate)) return FA_ERR_INVALID_ARG;
     if ((int64_t)Z * Hq * Nq == 0) return FA_OK;
     if ((st = check_tensor(q, sq, Z, Hq, Nq)) != FA_OK) return st;
     if ((st = check_tensor(k, sk, Z, Hkv, Nkv)) != FA_OK) return st;
@@ -339,8 +425,9 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* 
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
-    DeviceInfo* info = nullptr;
-    if (device_info(dev, &info) != cudaSuccess) return FA_ERR_CUDA;
+    LaunchInfo li;
+    if (device_info(dev, &li) != cudaSuccess) return FA_ERR_CUDA;
+    const LaunchInfo* info = &li;
 
     const int bn = fa::block_n_for(D);
     fa::LaunchArgs a;
@@ -360,7 +447,8 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* 
     p.Tq = (int)cdiv(Nq, fa::BM);
     p.Tk = (int)cdiv(Nkv, bn);
     p.ntiles = (int)((int64_t)Z * Hq * p.Tq);
-    p.scale_log2 = (float)((double)scale * 1.4426950408889634);  // exp(x) = 2^(x log2 e)
+    p.scale_log2 = c;
+    p.negate_s = negate;
     p.status = info->status;
     p.wait_limit_ns = wait_limit_ns();
     p.inject_stall = g_inject_stall.load();
@@ -401,7 +489,9 @@ fa_status fwd_ex_impl(const void* q, const void* k, const void* v, void* o, floa
     fa_status st = check_shape(Z, Hq, Hkv, Nq, Nkv, D, causal);
     if (st != FA_OK) return st;
     if (dtype != FA_DTYPE_F16 && dtype != FA_DTYPE_BF16) return FA_ERR_UNSUPPORTED;
-    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+    float c = 0.f;
+    int negate = 0;
+    if (!fwd_scale(scale, &c, &negate)) return FA_ERR_INVALID_ARG;
     if (opt->window_left < -1 || opt->window_right < -1) return FA_ERR_INVALID_ARG;
     const bool varlen = opt->cu_seqlens_q != nullptr || opt->cu_seqlens_k != nullptr;
     if (varlen && (opt->cu_seqlens_q == nullptr || opt->cu_seqlens_k == nullptr || opt->max_seqlen_q < 0))
@@ -432,8 +522,9 @@ fa_status fwd_ex_impl(const void* q, const void* k, const void* v, void* o, floa
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
-    DeviceInfo* info = nullptr;
-    if (device_info(dev, &info) != cudaSuccess) return FA_ERR_CUDA;
+    LaunchInfo li;
+    if (device_info(dev, &li) != cudaSuccess) return FA_ERR_CUDA;
+    const LaunchInfo* info = &li;
 
     const int bn = fa::block_n_for(D);
     fa::LaunchArgs a;
@@ -456,7 +547,8 @@ fa_status fwd_ex_impl(const void* q, const void* k, const void* v, void* o, floa
     // a packed sequence's keys: about Nkv / Z of the packed rows
     p.head_group = causal_head_group(Z * Hq, p.group, (int64_t)(varlen ? std::max(1, Nkv / Z) : Nkv) * D * 4,
                                      info->l2_bytes, p.Tq, info->sms);
-    p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    p.scale_log2 = c;
+    p.negate_s = negate;
     p.status = info->status;
     p.wait_limit_ns = wait_limit_ns();
     p.inject_stall = g_inject_stall.load();
@@ -606,7 +698,11 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     if (st != FA_OK) return st;
     if (!(D == 16 || D == 32 || D == 64 || D == 128)) return FA_ERR_UNSUPPORTED;
     if (dtype != FA_DTYPE_F16 && dtype != FA_DTYPE_BF16) return FA_ERR_UNSUPPORTED;
-    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+    // any finite scale whose log2 factor is finite in fp32: the backward
+    // builds P = 2^(s·scale·log2e − lse·log2e) from the saved lse (no row
+    // maximum) and masks after scaling, so the sign and zero need no care
+    if (!std::isfinite(scale) || !(std::fabs((double)scale) * 1.4426950408889634 <= (double)FLT_MAX))
+        return FA_ERR_INVALID_ARG;
     if ((int64_t)Z * Hkv * Nkv == 0) return FA_OK;
     if (Nq == 0) return FA_ERR_INVALID_ARG;  // gradients of an empty query set: nothing to differentiate
     if ((st = check_tensor(q, sq, Z, Hq, Nq)) != FA_OK) return st;
@@ -625,8 +721,9 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
-    DeviceInfo* info = nullptr;
-    if (device_info(dev, &info) != cudaSuccess) return FA_ERR_CUDA;
+    LaunchInfo li;
+    if (device_info(dev, &li) != cudaSuccess) return FA_ERR_CUDA;
+    const LaunchInfo* info = &li;
 
     fa::BwdLaunchArgs a;
     fa::BwdParams& p = a.params;
@@ -701,13 +798,21 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     return err == cudaSuccess ? FA_OK : cuda_fail("backward launch", err);
 }
 
+fa_status fa_fwd_splitkv_workspace_size_for(int D, int num_sms, size_t* bytes) {
+    if (bytes == nullptr || num_sms < 1) return FA_ERR_INVALID_ARG;
+    if (!supported_head_dim(D)) return FA_ERR_UNSUPPORTED;
+    *bytes = split_workspace_bytes(D, num_sms);
+    return FA_OK;
+}
+
 fa_status fa_fwd_splitkv_workspace_size(int D, size_t* bytes) {
     if (bytes == nullptr) return FA_ERR_INVALID_ARG;
     if (!supported_head_dim(D)) return FA_ERR_UNSUPPORTED;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
-    DeviceInfo* info = nullptr;
-    if (device_info(dev, &info) != cudaSuccess) return FA_ERR_CUDA;
+    LaunchInfo li;
+    if (device_info(dev, &li) != cudaSuccess) return FA_ERR_CUDA;
+    const LaunchInfo* info = &li;
     *bytes = split_workspace_bytes(D, info->sms);
     return FA_OK;
 }
@@ -734,8 +839,9 @@ fa_status fa_lse_merge(int nparts, const void* const* o_parts, const float* cons
     if (lse != nullptr && reinterpret_cast<uintptr_t>(lse) % 4 != 0) return FA_ERR_ALIGNMENT;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
-    DeviceInfo* info = nullptr;
-    if (device_info(dev, &info) != cudaSuccess) return FA_ERR_CUDA;
+    LaunchInfo li;
+    if (device_info(dev, &li) != cudaSuccess) return FA_ERR_CUDA;
+    const LaunchInfo* info = &li;
     a.nparts = nparts;
     a.H = H;
     a.N = N;

@@ -1,5 +1,8 @@
-// Specialisations of the attention backward for head dim 128.
-#include <atomic>
+// Specialisations of the attention backward for one head dim, D =
+// FA_HEAD_DIM (compiled once per supported D, in parallel).
+#ifndef FA_HEAD_DIM
+#error "compile with -DFA_HEAD_DIM=<16|32|64|128>"
+#endif
 #include <cstdint>
 
 #include "fa_bwd_kernel.cuh"
@@ -7,27 +10,14 @@
 
 namespace fa {
 
-template <typename K>
-static cudaError_t set_smem_once(K kernel, int smem, std::atomic<uint64_t>& configured) {
-    int dev = 0;
-    cudaError_t err = cudaGetDevice(&dev);
-    if (err != cudaSuccess) return err;
-    const uint64_t bit = 1ull << (dev & 63);
-    if (!(configured.load() & bit)) {
-        err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (err != cudaSuccess) return err;
-        configured.fetch_or(bit);
-    }
-    return cudaSuccess;
-}
-
 template <bool CAUSAL, bool BF16>
 static cudaError_t launch_one(const BwdLaunchArgs& a) {
-    using T = BwdTraits<128>;
-    auto bwd = fa_bwd_kernel<128, CAUSAL, BF16>;
-    static std::atomic<uint64_t> configured{0};
+    constexpr int D = FA_HEAD_DIM;
+    using T = BwdTraits<D>;
+    auto bwd = fa_bwd_kernel<D, CAUSAL, BF16>;
+    static std::atomic<uint64_t> configured{0};  // context the opt-in shared memory size was set in
     cudaError_t err;
-    if ((err = set_smem_once(bwd, T::FUSED_SMEM_BYTES, configured)) != cudaSuccess) return err;
+    if ((err = set_smem_for_context(bwd, T::FUSED_SMEM_BYTES, configured)) != cudaSuccess) return err;
     // Δ and lse2 per query row; then dK, dV and dQ in one launch.  Each
     // launch is a programmatic dependent of the one before it on the stream:
     // its set-up overlaps that kernel's tail, and it waits for it
@@ -42,14 +32,16 @@ static cudaError_t launch_one(const BwdLaunchArgs& a) {
     cfg.gridDim = dim3(a.pre_grid);
     cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = 0;
-    if ((err = cudaLaunchKernelEx(&cfg, fa_bwd_pre_kernel<128, BF16>, a.params)) != cudaSuccess) return err;
+    if ((err = cudaLaunchKernelEx(&cfg, fa_bwd_pre_kernel<D, BF16>, a.params)) != cudaSuccess) return err;
     cfg.gridDim = dim3(a.grid);
     cfg.blockDim = dim3(BWD_THREADS);
     cfg.dynamicSmemBytes = T::FUSED_SMEM_BYTES;
     return cudaLaunchKernelEx(&cfg, bwd, *a.tmK, *a.tmV, *a.tmQ, *a.tmDO, *a.tmDK, *a.tmDV, *a.tmDQ, a.params);
 }
 
-cudaError_t launch_bwd_d128(const BwdLaunchArgs& a, bool causal, bool bf16) {
+#define FA_CAT2(a, b) a##b
+#define FA_CAT(a, b) FA_CAT2(a, b)
+cudaError_t FA_CAT(launch_bwd_d, FA_HEAD_DIM)(const BwdLaunchArgs& a, bool causal, bool bf16) {
     if (causal) return bf16 ? launch_one<true, true>(a) : launch_one<true, false>(a);
     return bf16 ? launch_one<false, true>(a) : launch_one<false, false>(a);
 }

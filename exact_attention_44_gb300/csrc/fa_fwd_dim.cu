@@ -1,5 +1,10 @@
-// Specialisations of the attention forward kernel for head dim 16.
-#include <atomic>
+// Specialisations of the attention forward kernel for one head dim, D =
+// FA_HEAD_DIM (the build compiles this file once per supported D, in parallel:
+// "把 FlashAttention 搬上昇腾：Triton-Ascend CV Pipeline 优化实战", section 七,
+// specialises the kernel per head dim the same way).
+#ifndef FA_HEAD_DIM
+#error "compile with -DFA_HEAD_DIM=<16|32|64|128|256>"
+#endif
 #include <cstdint>
 
 #include "fa_fwd_kernel.cuh"
@@ -9,19 +14,12 @@ namespace fa {
 
 template <bool CAUSAL, bool BF16, int VAR>
 static cudaError_t launch_one(const LaunchArgs& a) {
-    auto kernel = fa_fwd_kernel<16, CAUSAL, BF16, VAR>;
-    constexpr int smem = Traits<16>::SMEM_BYTES;
-    // the opt-in shared memory size is set once per device
-    static std::atomic<uint64_t> configured{0};
-    int dev = 0;
-    cudaError_t err = cudaGetDevice(&dev);
+    constexpr int D = FA_HEAD_DIM;
+    auto kernel = fa_fwd_kernel<D, CAUSAL, BF16, VAR>;
+    constexpr int smem = Traits<D>::SMEM_BYTES;
+    static std::atomic<uint64_t> configured{0};  // context the opt-in shared memory size was set in
+    cudaError_t err = set_smem_for_context(kernel, smem, configured);
     if (err != cudaSuccess) return err;
-    const uint64_t bit = 1ull << (dev & 63);
-    if (!(configured.load() & bit)) {
-        err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (err != cudaSuccess) return err;
-        configured.fetch_or(bit);
-    }
     // programmatic dependent launch: the kernel's set-up may overlap the tail
     // of the previous kernel on the stream (it waits for it before any
     // global memory access)
@@ -30,7 +28,7 @@ static cudaError_t launch_one(const LaunchArgs& a) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.grid);
-    cfg.blockDim = dim3(Traits<16>::THREADS);
+    cfg.blockDim = dim3(Traits<D>::THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = a.stream;
     cfg.attrs = attr;
@@ -45,7 +43,7 @@ static cudaError_t launch_one(const LaunchArgs& a) {
             mcfg.stream = a.stream;
             mcfg.attrs = attr;
             mcfg.numAttrs = 1;
-            err = cudaLaunchKernelEx(&mcfg, fa_split_merge_kernel<16, CAUSAL, BF16>, a.params, a.grid);
+            err = cudaLaunchKernelEx(&mcfg, fa_split_merge_kernel<D, CAUSAL, BF16>, a.params, a.grid);
         }
     }
     return err;
@@ -53,7 +51,9 @@ static cudaError_t launch_one(const LaunchArgs& a) {
 
 // variant 0: fa_fwd; 1: window / variable length; 2: the same with ALiBi;
 // 4: fa_fwd with alternating causal rounds (tile mode)
-cudaError_t launch_d16(const LaunchArgs& a, bool causal, bool bf16, int variant) {
+#define FA_CAT2(a, b) a##b
+#define FA_CAT(a, b) FA_CAT2(a, b)
+cudaError_t FA_CAT(launch_d, FA_HEAD_DIM)(const LaunchArgs& a, bool causal, bool bf16, int variant) {
     if (variant == 2) {
         if (causal) return bf16 ? launch_one<true, true, 2>(a) : launch_one<true, false, 2>(a);
         return bf16 ? launch_one<false, true, 2>(a) : launch_one<false, false, 2>(a);

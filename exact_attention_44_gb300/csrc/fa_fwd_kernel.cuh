@@ -534,7 +534,8 @@ template <int D, bool CAUSAL, bool BF16, int VAR>
 __device__ void run_mma_qk(const FwdParams& p, uint32_t sbase, uint32_t bar0, uint32_t tmem, const Ctl& ctl) {
     using T = Traits<D>;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
-    constexpr uint32_t IDESC = ptx::idesc_f16(BM, T::BN, BF16, false, false);  // Q, K both K-major
+    // Q, K both K-major; with a negative scale Q is negated (the kernel's c is |scale|·log2e)
+    const uint32_t IDESC = ptx::idesc_f16(BM, T::BN, BF16, false, false) | (p.negate_s ? ptx::IDESC_NEGATE_A : 0u);
     constexpr uint32_t HI = ptx::smem_desc_hi(8 * T::SW, T::SWIZZLE_CODE);     // 8-row swizzle atoms
     const uint32_t q_lo0 = ptx::smem_desc_lo(sbase + T::OFF_Q, 16);
     const uint32_t k_lo0 = ptx::smem_desc_lo(sbase + T::OFF_K, 16);
@@ -794,7 +795,7 @@ __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, fl
                 float mm = pmax;
 #pragma unroll
                 for (int g2 = 0; g2 < NG; ++g2) mm = fmaxf(mm, red[(b * NG + g2) * BM + row]);
-                return mm * cm;  // scale > 0
+                return mm * cm;  // cm > 0 (a negative scale negates S instead)
             };
             if (j == ti.jb) {
                 // the first block sets the reference maximum m

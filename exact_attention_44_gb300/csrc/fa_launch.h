@@ -1,14 +1,36 @@
-// Per-head-dim launchers, one translation unit each (compiled in parallel).
+// Per-head-dim launchers: fa_fwd_dim.cu and fa_bwd_dim.cu, each compiled once
+// per head dim (-DFA_HEAD_DIM=D), in parallel.
 #pragma once
 
 #include <cuda.h>
 #include <cuda_runtime_api.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "fa_params.h"
 
 namespace fa {
+
+// ID of the calling thread's current CUDA context (cuCtxGetId), or 0 when
+// there is none or the driver cannot say.  Per-context state of this library
+// (a kernel's shared-memory attribute, the device address of a __device__
+// variable) is remembered under this ID: a context destroyed by
+// cudaDeviceReset and created again gets a new ID, so that state is set up
+// anew instead of reused.
+uint64_t current_context_id();
+
+// Set `kernel`'s opt-in dynamic shared memory size, once per CUDA context:
+// `ctx` holds the ID of the context it was last set in.  A failed call is not
+// remembered (the next launch tries again).
+template <typename K>
+inline cudaError_t set_smem_for_context(K kernel, int smem, std::atomic<uint64_t>& ctx) {
+    const uint64_t id = current_context_id();
+    if (id != 0 && ctx.load() == id) return cudaSuccess;
+    const cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err == cudaSuccess && id != 0) ctx.store(id);
+    return err;
+}
 
 struct LaunchArgs {
     const CUtensorMap* tmQ;

@@ -3,12 +3,17 @@
 // must not allocate device memory during a call.
 //
 // The array is a file-scope __device__ variable of this translation unit, so
-// the device image of this file (and with it the array) is loaded on a GPU
-// the first time this entry point runs there, and stays until the process
-// exits.  Host code cannot use the name of a __device__ variable as a device
-// address (on the host it names a stand-in object), so the address is asked
-// of the runtime once per device, with that device current, and passed to
-// the kernels as an ordinary pointer.
+// it is part of the library's device image: it takes device memory in every
+// CUDA context that loads that image (under lazy module loading, the default,
+// the first time this entry point runs in the context; with
+// CUDA_MODULE_LOADING=EAGER, when the context is created) and keeps it until
+// the context is destroyed.  Host code cannot use the name of a __device__
+// variable as a device address (on the host it names a stand-in object), so
+// the address is asked of the runtime with the device current, on the first
+// call in each CUDA context, and passed to the kernels as an ordinary
+// pointer.  A context that cudaDeviceReset destroyed and the runtime created
+// again has a new ID and gets a fresh lookup; a failed lookup is not
+// remembered.
 #include <cuda_runtime.h>
 
 #include <cstddef>
@@ -16,6 +21,7 @@
 #include <mutex>
 
 #include "fa.h"
+#include "fa_launch.h"
 
 namespace {
 
@@ -24,24 +30,28 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[FA_NOALLOC_SCRA
 constexpr int kMaxDevices = 64;
 
 struct ScratchSlot {
-    std::once_flag once;
-    cudaError_t err = cudaSuccess;
+    std::mutex mu;
+    uint64_t ctx = 0;    // context the address was looked up in
     void* ptr = nullptr;
 };
 ScratchSlot g_slots[kMaxDevices];
 
-// Device address of the array on device `dev`, looked up on the first call
-// for that device (the caller has made `dev` current).
+// Device address of the array in the current context of device `dev` (the
+// caller has made `dev` current).
 cudaError_t scratch_address(int dev, void** out) {
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     ScratchSlot& s = g_slots[dev];
-    std::call_once(s.once, [&] {
+    std::lock_guard<std::mutex> lock(s.mu);
+    const uint64_t ctx = fa::current_context_id();
+    if (ctx == 0 || ctx != s.ctx || s.ptr == nullptr) {
         void* p = nullptr;
-        s.err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (s.err == cudaSuccess) s.ptr = p;
-    });
+        const cudaError_t err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (err != cudaSuccess) return err;  // not remembered: the next call tries again
+        s.ptr = p;
+        s.ctx = fa::current_context_id();    // the lookup may have created the context
+    }
     *out = s.ptr;
-    return s.err;
+    return cudaSuccess;
 }
 
 }  // namespace

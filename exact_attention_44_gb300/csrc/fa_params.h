@@ -54,7 +54,11 @@ struct FwdParams {
     int Tq, Tk;              // ceil(Nq / BM), ceil(Nkv / BN)
     int ntiles;              // Z * Hq * Tq
     int head_group;          // causal tile order: (z, hq) heads per group (>= 1)
-    float scale_log2;        // scale * log2(e)
+    // |scale| * log2(e), > 0 (see fwd_scale in the host code); with
+    // negate_s the S = Q Kᵀ products negate Q, so that the kernel's scores
+    // times scale_log2 are the scaled scores of a negative scale
+    float scale_log2;
+    int negate_s;
     uint32_t* status;        // device status word (first error wins)
     uint64_t wait_limit_ns;  // bound on every mbarrier wait
     int inject_stall;        // test hook: 1 = withhold the first K tile of CTA 0 (waits must time out)

@@ -176,12 +176,15 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
 
 // Instruction descriptor for kind::f16 with an fp32 accumulator.
 //   bits 4-5 D format (1 = f32), 7-9 A format, 10-12 B format (0 = f16,
-//   1 = bf16), 15 A major, 16 B major (0 = K-major, 1 = MN-major),
+//   1 = bf16), 13 negate A, 14 negate B, 15 A major, 16 B major (0 = K-major, 1 = MN-major),
 //   17-22 N >> 3, 24-28 M >> 4.
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool bf16, bool a_mn_major, bool b_mn_major) {
     return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((a_mn_major ? 1u : 0u) << 15) |
            ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+
+// Instruction descriptor bit 13: negate the A operand (exact for f16/bf16).
+constexpr uint32_t IDESC_NEGATE_A = 1u << 13;
 
 // Shared-memory matrix descriptor:
 //   bits 0-13 start >> 4, 16-29 leading byte offset >> 4, 32-45 stride byte

@@ -36,7 +36,7 @@ extern "C" {
 /* Status codes.  Host-side errors are returned before anything is enqueued. */
 typedef enum {
     FA_OK = 0,
-    FA_ERR_INVALID_ARG = 1,     /* null pointer, negative size, Hq % Hkv != 0, Nkv == 0 with work, bad scale */
+    FA_ERR_INVALID_ARG = 1,     /* null pointer, negative size, Hq % Hkv != 0, Nkv == 0 with work, non-finite scale */
     FA_ERR_UNSUPPORTED = 2,     /* D not in {16, 32, 64, 128, 256}, dtype not fp16/bf16 */
     FA_ERR_ALIGNMENT = 3,       /* d-stride != 1, a base or stride not 16-byte aligned, negative stride */
     FA_ERR_CUDA = 4,            /* a CUDA runtime/driver call failed (launch, tensor map, device query) */
@@ -63,7 +63,11 @@ typedef struct {
  *   v    (Z, Hkv, Nkv, D)  dtype, strides *sv
  *   o    (Z, Hq,  Nq,  D)  dtype, strides *so   (written)
  *   lse  (Z, Hq,  Nq)      fp32, contiguous      (written; may be NULL to skip)
- *   scale   softmax scale, finite and > 0 (commonly 1/sqrt(D))
+ *   scale   softmax scale (commonly 1/sqrt(D)): any finite value, zero and
+ *           negative included ("Write Triton Attention Kernel", Inputs 4:
+ *           1/sqrt(D) or a custom value), as long as |scale|·log2(e) is
+ *           finite in fp32 (|scale| <= ~2.4e38).  Scale 0 weighs every kept
+ *           key equally (O = mean of their V, lse = log of their count).
  *   causal  0 or 1
  *   dtype   FA_DTYPE_F16 or FA_DTYPE_BF16 for Q, K, V and O
  *   stream  CUDA stream (0 = legacy default stream)
@@ -188,6 +192,14 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
  */
 fa_status fa_fwd_splitkv_workspace_size(int D, size_t* bytes);
 
+/*
+ * fa_fwd_splitkv_workspace_size_for -- host only, no CUDA call: the same size
+ * for a device with num_sms SMs (two slots per SM, each 128 x D + 128 fp32
+ * values padded to 256 bytes).  FA_ERR_INVALID_ARG for a NULL bytes or
+ * num_sms < 1, FA_ERR_UNSUPPORTED for an unsupported D.
+ */
+fa_status fa_fwd_splitkv_workspace_size_for(int D, int num_sms, size_t* bytes);
+
 /* Size in bytes of the device array fa_fwd_splitkv_noalloc works in (40 MiB). */
 #define FA_NOALLOC_SCRATCH_BYTES (40u * 1024u * 1024u)
 
@@ -204,12 +216,21 @@ fa_status fa_fwd_splitkv_workspace_size(int D, size_t* bytes);
  * device's memory.  Arguments, results and the other errors are those of
  * fa_fwd_splitkv; this call makes no cudaMalloc or cudaFree.
  *
- * The array: every GPU on which this entry point runs holds it from that
- * first call until the process exits.  The first call on each device also
- * looks up the array's device address (once per device, with that device
- * current); make that first call before any stream capture.  40 MiB covers
- * two partial slots per SM at D = 256 on GPUs of up to 159 SMs; a device that
- * needs more is rejected with FA_ERR_WORKSPACE before anything is enqueued.
+ * The array is part of this library's device image, so it takes 40 MiB of
+ * device memory in each CUDA context that loads the image, until that
+ * context is destroyed.  Under lazy module loading (the CUDA default) that
+ * happens on the first call of this entry point in the context, and the
+ * call fails with FA_ERR_CUDA if 40 MiB of device memory are not free then;
+ * with CUDA_MODULE_LOADING=EAGER every context the process creates reserves
+ * the 40 MiB when it is created, whether or not it ever calls this entry
+ * point.  The first call in each context also looks up the array's device
+ * address (with the device current); make that first call before any stream
+ * capture.  A context destroyed by cudaDeviceReset and created again gets a
+ * new lookup on its next first call; a failed lookup is retried by the next
+ * call.  40 MiB covers two partial slots per SM at D = 256 on GPUs of up to
+ * 159 SMs (fa_fwd_splitkv_workspace_size_for gives the need for a given SM
+ * count); a device that needs more is rejected with FA_ERR_WORKSPACE before
+ * anything is enqueued.
  * Nothing in the array has to start at zero: each call writes every slot it
  * later reads.  All calls on a device share the one array, so two calls whose
  * work may overlap on the GPU (different streams without ordering between

@@ -128,3 +128,93 @@ def check_sampled(seed, Z, Hq, Hkv, Nq, Nkv, D, dtype, causal, n_groups=2, rows_
         d = compare(og, lg, o_ref, lse_ref, dtype, f"z={z} hk={hk} {(Z, Hq, Hkv, Nq, Nkv, D, dtype, causal)}")
         worst = (max(worst[0], d[0]), max(worst[1], d[1]))
     return worst
+
+
+def _gpu_tensors(q, k, v, dtype, scale, causal, impl="fwd"):
+    """Full-size GPU run on seeded bits; (O, lse) stay on the device."""
+    import torch
+    from exact_attention_44_gb300 import fa_device_status, fa_fwd, fa_fwd_splitkv
+
+    qt, kt, vt = (to_device(x, dtype) for x in (q, k, v))
+    if impl == "splitkv":
+        o, lse = fa_fwd_splitkv(qt, kt, vt, scale=scale, causal=causal)
+    else:
+        o, lse = fa_fwd(qt, kt, vt, scale=scale, causal=causal)
+    torch.cuda.synchronize()
+    code, word = fa_device_status()
+    assert code == 0, f"device status {word:#x}: a bounded wait ran out"
+    del qt, kt, vt
+    return o, lse
+
+
+def check_full_chunked(seed, Z, Hq, Hkv, Nq, Nkv, D, dtype, causal, scale=None, impl="fwd",
+                       max_rows=1 << 18):
+    """Every output row of a full-size run against the oracle.
+
+    The GPU computes the whole problem at once (the launch the benchmark
+    times); the oracle then takes it in chunks of whole GQA groups, at most
+    about `max_rows` query rows per chunk, so host memory stays bounded.
+    Returns the worst (max|dO|, max|dlse|) over all rows."""
+    scale = 1 / math.sqrt(D) if scale is None else scale
+    q, k, v = si.qkv(seed, Z, Hq, Hkv, Nq, Nkv, D, dtype)
+    o_dev, lse_dev = _gpu_tensors(q, k, v, dtype, scale, causal, impl)
+    g = Hq // Hkv
+    group_rows = g * Nq
+    groups_per_chunk = max(1, max_rows // max(group_rows, 1))
+    worst = (0.0, 0.0)
+    # chunks of (z, kv head) groups in memory order: z outer, kv head inner
+    for first in range(0, Z * Hkv, groups_per_chunk):
+        last = min(Z * Hkv, first + groups_per_chunk)
+        for z in range(first // Hkv, (last - 1) // Hkv + 1):
+            h0 = max(first - z * Hkv, 0)
+            h1 = min(last - z * Hkv, Hkv)
+            qs = q[z:z + 1, h0 * g:h1 * g]
+            ks, vs = k[z:z + 1, h0:h1], v[z:z + 1, h0:h1]
+            o_ref, lse_ref = oracle.attention_fwd(qs, ks, vs, dtype, scale, causal)
+            og = o_dev[z:z + 1, h0 * g:h1 * g].double().cpu().numpy()
+            lg = lse_dev[z:z + 1, h0 * g:h1 * g].double().cpu().numpy()
+            d = compare(og, lg, o_ref, lse_ref, dtype,
+                        f"z={z} kv heads {h0}..{h1 - 1} {(Z, Hq, Hkv, Nq, Nkv, D, dtype, causal)}")
+            worst = (max(worst[0], d[0]), max(worst[1], d[1]))
+    return worst
+
+
+def check_heads_full_rest_sampled(seed, Z, Hq, Hkv, Nq, Nkv, D, dtype, causal, full_heads, rows_per_head=512,
+                                  scale=None, impl="fwd"):
+    """Full-size run; every row of the (z = 0) query heads in `full_heads`, and in
+    every other head of z = 0 a seeded sample: rows 0, 127, 128 and Nq - 1, the
+    first row of every 128-row tile, and `rows_per_head` random rows.
+
+    For problems whose full comparison would take the oracle far longer
+    than a test may (the causal N = 32768 workload is ~8.8 TFLOP in fp64)."""
+    scale = 1 / math.sqrt(D) if scale is None else scale
+    q, k, v = si.qkv(seed, Z, Hq, Hkv, Nq, Nkv, D, dtype)
+    o_dev, lse_dev = _gpu_tensors(q, k, v, dtype, scale, causal, impl)
+    g = Hq // Hkv
+    rng = np.random.default_rng(seed + 7)
+    fixed = {0, 127, 128, Nq - 1} | set(range(0, Nq, 128))
+    worst = (0.0, 0.0)
+    for hk in range(Hkv):
+        rows, flat = [], []
+        for h in range(hk * g, (hk + 1) * g):
+            if h in full_heads:
+                # shuffled: the oracle gives each thread a contiguous slice of
+                # the rows, and causal rows cost in proportion to their index
+                r = rng.permutation(Nq).astype(np.int64)
+            else:
+                r = np.array(sorted(x for x in fixed | set(rng.integers(0, Nq, size=rows_per_head).tolist())
+                                    if 0 <= x < Nq), dtype=np.int64)
+            rows.append((h, r))
+            flat.append((h - hk * g) * Nq + r)
+        o_ref, lse_ref = oracle.attention_fwd(q[0:1, hk * g:(hk + 1) * g], k[0:1, hk:hk + 1], v[0:1, hk:hk + 1],
+                                              dtype, scale, causal, rows=np.concatenate(flat))
+        og = np.concatenate([o_dev[0, h][torch_index(r)].double().cpu().numpy() for h, r in rows])
+        lg = np.concatenate([lse_dev[0, h][torch_index(r)].double().cpu().numpy() for h, r in rows])
+        d = compare(og, lg, o_ref, lse_ref, dtype, f"kv head {hk} {(Z, Hq, Hkv, Nq, Nkv, D, dtype, causal)}")
+        worst = (max(worst[0], d[0]), max(worst[1], d[1]))
+    return worst
+
+
+def torch_index(rows):
+    import torch
+    return torch.from_numpy(np.asarray(rows, dtype=np.int64)).cuda()

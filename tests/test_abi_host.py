@@ -100,8 +100,8 @@ def _call(Z=1, Hq=2, Hkv=1, Nq=64, Nkv=64, D=64, scale=0.125, causal=0, dtype=0,
     (dict(causal=2), fa.FA_ERR_INVALID_ARG),
     (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
     (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
-    (dict(scale=0.0), fa.FA_ERR_INVALID_ARG),
-    (dict(scale=-0.1), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=3.0e38), fa.FA_ERR_INVALID_ARG),   # scale * log2(e) overflows fp32
+    (dict(scale=-3.0e38), fa.FA_ERR_INVALID_ARG),
     (dict(D=48), fa.FA_ERR_UNSUPPORTED),
     (dict(D=512), fa.FA_ERR_UNSUPPORTED),
     (dict(dtype=2), fa.FA_ERR_UNSUPPORTED),
@@ -111,6 +111,15 @@ def _call(Z=1, Hq=2, Hkv=1, Nq=64, Nkv=64, D=64, scale=0.125, causal=0, dtype=0,
 ])
 def test_argument_errors(lib, kw, code):
     assert _call(**kw) == code
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.0, -0.1, -8.0, 1e-40, -1e-40, 2.0e38, -2.0e38])
+def test_every_finite_scale_passes_validation(lib, scale):
+    # "1/sqrt(D) or a custom value" ("Write Triton Attention Kernel", Inputs 4):
+    # zero, negative and subnormal scales are valid.  An empty problem (Z = 0)
+    # returns FA_OK right after validation, before any device call.
+    assert _call(Z=0, scale=scale) == fa.FA_OK
+    assert _call(Z=0, scale=float("nan")) == fa.FA_ERR_INVALID_ARG
 
 
 def test_stride_errors(lib):
@@ -323,3 +332,31 @@ def test_schedule_argument_errors():
     with pytest.raises(fa.FaError) as e:
         fa.fa_fwd_schedule(1, 3, 2, 128, 128, 64, False, num_sms=GB300_SMS, l2_bytes=GB300_L2)
     assert e.value.code != fa.FA_OK
+
+
+def _noalloc_scratch_bytes():
+    # the size the header gives the no-allocation entry point's fixed array
+    import re
+    text = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "fa.h")).read()
+    m = re.search(r"#define FA_NOALLOC_SCRATCH_BYTES \((\d+)u \* (\d+)u \* (\d+)u\)", text)
+    assert m, "FA_NOALLOC_SCRATCH_BYTES not found in include/fa.h"
+    return int(m.group(1)) * int(m.group(2)) * int(m.group(3))
+
+
+def test_noalloc_array_covers_the_documented_sm_count(lib):
+    # the header promises two D = 256 partial slots per SM on GPUs of up to
+    # 159 SMs (152 on GB300), and that a device needing more is rejected:
+    # the array must hold 159 SMs' worth and not 160
+    size = _noalloc_scratch_bytes()
+    assert fa.fa_fwd_splitkv_workspace_size_for(256, 159) <= size < fa.fa_fwd_splitkv_workspace_size_for(256, 160)
+    # smaller head dims need less per slot, so 152 SMs fit at every D
+    for D in (16, 32, 64, 128, 256):
+        assert fa.fa_fwd_splitkv_workspace_size_for(D, 152) <= size
+    # the slot layout: 128 x D fp32 values and 128 log-sum-exps, padded to 256 bytes
+    for D in (16, 64, 256):
+        slot = ((128 * D + 128) * 4 + 255) // 256 * 256
+        assert fa.fa_fwd_splitkv_workspace_size_for(D, 7) == 2 * 7 * slot
+    with pytest.raises(fa.FaError):
+        fa.fa_fwd_splitkv_workspace_size_for(48, 152)
+    with pytest.raises(fa.FaError):
+        fa.fa_fwd_splitkv_workspace_size_for(128, 0)

@@ -146,3 +146,40 @@ def test_output_matches_torch_sdpa_as_a_second_opinion():
     s = (qt @ kt.transpose(-1, -2)) * 0.125
     s = s.masked_fill(torch.ones(333, 333, dtype=torch.bool).triu(1), float("-inf"))
     assert np.max(np.abs(lse - torch.logsumexp(s, -1).double().numpy())) < 1e-3
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("causal", [False, True])
+def test_scale_zero_gives_mean_of_kept_values(D, causal):
+    # scale 0 ("1/sqrt(D) or a custom value", "Write Triton Attention Kernel",
+    # Inputs 4): every kept key weighs the same, O = mean of their V and
+    # lse = log of their count -- the closed form the oracle is pinned to
+    import oracle
+    q, k, v = si.qkv(13, 1, 2, 2, 300, 300, D, "bf16")
+    o, lse = run_gpu(q, k, v, "bf16", 0.0, causal)
+    check_full(13, 1, 2, 2, 300, 300, D, "bf16", causal, scale=0.0)
+    vd = oracle.decode(v, "bf16")
+    n = np.arange(1, 301) if causal else np.full(300, 300)
+    mean = (np.cumsum(vd[0, 0], axis=0) / n[:, None]) if causal else np.broadcast_to(vd[0, 0].mean(0), (300, D))
+    assert np.max(np.abs(o[0, 0] - mean)) <= 2e-2
+    assert np.max(np.abs(lse[0, 0] - np.log(n))) <= 1e-5
+
+
+@pytest.mark.parametrize("D", [32, 128, 256])
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_negative_scale(D, dtype, causal):
+    # a negative scale turns the softmax toward the lowest scores: the row
+    # extreme that references the exponentials is then the row minimum
+    check_full(14, 1, 2, 1, 260, 390, D, dtype, causal, scale=-1 / math.sqrt(D))
+    check_full(15, 1, 2, 1, 200, 200, D, dtype, causal, scale=-1.0)
+
+
+def test_negative_and_zero_scale_through_the_split_schedule_and_variants():
+    import exact_attention_44_gb300 as fa
+    fa.fa_debug_force_split(1)
+    try:
+        check_full(16, 1, 4, 2, 150, 1500, 128, "bf16", False, scale=-0.2, impl="splitkv")
+        check_full(16, 1, 4, 2, 150, 1500, 128, "bf16", True, scale=0.0, impl="splitkv")
+    finally:
+        fa.fa_debug_force_split(0)
