@@ -99,7 +99,8 @@ def load_peaks():
 
 
 # the sources the forward kernel of head dim D is compiled from
-FWD_SOURCES = ["fa_fwd_kernel.cuh", "fa_ptx.cuh", "fa_params.h", "fa_launch.h", "fa_fwd_dim.cu"]
+FWD_SOURCES = ["fa_fwd_kernel.cuh", "fa_fwd_chain_kernel.cuh", "fa_ptx.cuh", "fa_params.h", "fa_launch.h",
+               "fa_fwd_dim.cu"]
 
 
 def kernel_source_hash() -> str:
@@ -478,6 +479,7 @@ def run_profile(args, device):
     fa.load()
     wl = WORKLOADS[args.workload]
     Z, Hq, Hkv, Nq, Nkv, D, dtype, flags = wl
+    fa.fa_debug_force_chains(args.force_chains)
     _, (q, k, v) = make_inputs(wl, 0, device)
     stream = torch.cuda.current_stream(device)
     o = torch.empty((Z, Hq, Nq, D), dtype=q.dtype, device=device)
@@ -791,6 +793,8 @@ def main(argv=None):
                     help="seconds of oracle work for cpu_baseline (and the cap per step of --impl reference)")
     ap.add_argument("--profile", action="store_true",
                     help="only W + K eager launches of --workload on one input set, no timing (an ncu target)")
+    ap.add_argument("--force-chains", type=int, choices=[0, 1, 2], default=0,
+                    help="with --profile: 0 the library's choice, 1 two softmax chains, 2 one")
     ap.add_argument("--bwd-only", action="store_true",
                     help="time only fa_bwd on --workload (one JSON line per causal flag; for profiling)")
     ap.add_argument("--all", action="store_true",

@@ -53,6 +53,7 @@ _SIGNATURES = {
     "fa_debug_set_wait_limit_ms": (None, [ctypes.c_double]),
     "fa_debug_inject_stall": (None, [ctypes.c_int]),
     "fa_debug_force_split": (None, [ctypes.c_int]),
+    "fa_debug_force_chains": (None, [ctypes.c_int]),
 }
 
 _lock = threading.Lock()
@@ -77,7 +78,7 @@ class fa_fwd_options(ctypes.Structure):
 class fa_fwd_schedule_info(ctypes.Structure):
     _fields_ = [("grid", ctypes.c_int), ("split", ctypes.c_int), ("gqa_packed", ctypes.c_int),
                 ("head_group", ctypes.c_int), ("alternate", ctypes.c_int), ("tiles", ctypes.c_int64),
-                ("kv_blocks", ctypes.c_int64), ("busiest_blocks", ctypes.c_int64)]
+                ("kv_blocks", ctypes.c_int64), ("busiest_blocks", ctypes.c_int64), ("softmax_chains", ctypes.c_int)]
 
 
 def library_path() -> str:
@@ -458,6 +459,11 @@ def fa_debug_set_wait_limit_ms(ms: float) -> None:
 
 def fa_debug_inject_stall(enable: bool) -> None:
     load().fa_debug_inject_stall(int(bool(enable)))
+
+
+def fa_debug_force_chains(mode: int) -> None:
+    """Which kernel runs whole tiles of D <= 128: 0 by shape (default), 1 two softmax chains, 2 one."""
+    load().fa_debug_force_chains(int(mode))
 
 
 def fa_debug_force_split(mode: int) -> None:

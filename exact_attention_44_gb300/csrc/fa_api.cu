@@ -11,6 +11,8 @@
 #include <cstdio>
 #include <cstdlib>
 #include <mutex>
+#include <vector>
+#include <algorithm>
 
 #include "fa.h"
 #include "fa_bwd_kernel.cuh"
@@ -109,6 +111,7 @@ const CtxFns& ctx_fns() {
 std::atomic<uint64_t> g_wait_limit_ns{0};
 std::atomic<int> g_inject_stall{0};
 std::atomic<int> g_force_split{0};  // 0: decide by shape, 1: always cut key ranges, 2: never
+std::atomic<int> g_force_chains{0};  // 0: decide by shape, 1: two softmax chains wherever they apply, 2: never
 
 uint64_t wait_limit_ns() {
     uint64_t v = g_wait_limit_ns.load();
@@ -343,6 +346,34 @@ cudaError_t launch_for(int D, const fa::LaunchArgs& a, bool causal, bool bf16, i
     }
 }
 
+cudaError_t launch_chain_for(int D, const fa::LaunchArgs& a, bool causal, bool bf16, bool alt) {
+    switch (D) {
+        case 16: return fa::launch_chain_d16(a, causal, bf16, alt);
+        case 32: return fa::launch_chain_d32(a, causal, bf16, alt);
+        case 64: return fa::launch_chain_d64(a, causal, bf16, alt);
+        default: return fa::launch_chain_d128(a, causal, bf16, alt);
+    }
+}
+
+// Whole-tile launches may run the two-softmax-chain kernel
+// (fa_fwd_chain_kernel: two warpgroups take the key blocks in turn, each with
+// a whole row of scores per thread) for head dims up to 128; D = 256 (256
+// score columns would not fit a thread's registers) and the split schedule
+// run the one-chain kernel.  Measured on GB300 (same tiles, same order):
+// where the softmax sets the pace -- head dims up to 64 -- with long tiles
+// (at least 16 key blocks a tile on average) two chains were 9-17 % faster
+// (Z8 H16 N2048 non-causal, D 16/32/64); with short tiles (N = 1024, or
+// causal at N = 2048: 4.5-8.5 blocks) 1-25 % slower, since the blocks of a
+// tile then pass through a chain of one warpgroup instead of four; and at
+// D = 128, where the tensor core and its shared-memory operand traffic set
+// the pace, 3-25 % slower.  fa_debug_force_chains overrides the choice.
+bool chain_kernel_applies(const fa::FwdParams& p, int D, bool causal, bool split) {
+    if (split || D > 128) return false;
+    const int force = g_force_chains.load();
+    if (force != 0) return force == 1;
+    return D <= 64 && head_blocks(p, causal, 128) >= 16 * (int64_t)p.Tq;
+}
+
 // The schedule of a forward launch whose sizes are in p (Z .. ntiles):
 // causal head groups and alternating rounds for whole tiles, and whether key
 // ranges are cut across CTAs (only where the caller allows it: the cut needs
@@ -351,6 +382,7 @@ struct SchedChoice {
     int grid = 0;
     bool split = false;
     bool alt = false;
+    bool chains = false;  // the two-softmax-chain kernel (same tiles and order as the one-chain kernel)
 };
 SchedChoice choose_schedule(fa::FwdParams& p, int D, bool causal, int bn, int sms, int l2_bytes, bool split_allowed) {
     SchedChoice c;
@@ -367,6 +399,7 @@ SchedChoice choose_schedule(fa::FwdParams& p, int D, bool causal, int bn, int sm
             c.grid = (int)std::min<int64_t>(p.total_blocks, sms);
         }
     }
+    c.chains = chain_kernel_applies(p, D, causal, c.split);
     return c;
 }
 
@@ -475,6 +508,10 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* 
     a.tmO = &mo;
     a.stream = stream;
 
+    if (choice.chains) {
+        const cudaError_t err = launch_chain_for(D, a, causal != 0, dtype == FA_DTYPE_BF16, alt);
+        return err == cudaSuccess ? FA_OK : cuda_fail("forward launch", err);
+    }
     // kernel variant 4: the plain kernel with alternating causal rounds (tile mode only)
     const cudaError_t err = launch_for(D, a, causal != 0, dtype == FA_DTYPE_BF16, alt && !p.split ? 4 : 0);
     return err == cudaSuccess ? FA_OK : cuda_fail("forward launch", err);
@@ -653,6 +690,7 @@ fa_status fa_fwd_schedule(int Z, int Hq, int Hkv, int Nq, int Nkv, int D, int ca
     out->alternate = c.alt && !c.split ? 1 : 0;
     out->tiles = p.ntiles;
     out->kv_blocks = (int64_t)Z * Hq * head_blocks(p, causal != 0, bn);
+    out->softmax_chains = c.chains ? 2 : 1;
     out->busiest_blocks = c.split ? cdiv(out->kv_blocks, c.grid)
                                   : tile_mode_max_blocks(p, causal != 0, bn, c.grid, c.alt);
     return FA_OK;
@@ -879,5 +917,6 @@ void fa_debug_set_wait_limit_ms(double ms) {
 }
 void fa_debug_inject_stall(int enable) { g_inject_stall.store(enable ? 1 : 0); }
 void fa_debug_force_split(int mode) { g_force_split.store(mode == 1 || mode == 2 ? mode : 0); }
+void fa_debug_force_chains(int mode) { g_force_chains.store(mode == 1 || mode == 2 ? mode : 0); }
 
 }  // extern "C"

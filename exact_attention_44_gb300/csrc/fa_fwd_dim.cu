@@ -8,6 +8,7 @@
 #include <cstdint>
 
 #include "fa_fwd_kernel.cuh"
+#include "fa_fwd_chain_kernel.cuh"
 #include "fa_launch.h"
 
 namespace fa {
@@ -66,5 +67,38 @@ cudaError_t FA_CAT(launch_d, FA_HEAD_DIM)(const LaunchArgs& a, bool causal, bool
     if (causal) return bf16 ? launch_one<true, true, 0>(a) : launch_one<true, false, 0>(a);
     return bf16 ? launch_one<false, true, 0>(a) : launch_one<false, false, 0>(a);
 }
+
+
+#if FA_HEAD_DIM <= 128
+// The two-softmax-chain kernel (fa_fwd, whole tiles, head dims up to 128).
+template <bool CAUSAL, bool BF16, bool ALT>
+static cudaError_t launch_chain_one(const LaunchArgs& a) {
+    constexpr int D = FA_HEAD_DIM;
+    auto kernel = fa_fwd_chain_kernel<D, CAUSAL, BF16, ALT>;
+    constexpr int smem = Traits<D>::SMEM_BYTES;
+    static std::atomic<uint64_t> configured{0};  // context the opt-in shared memory size was set in
+    cudaError_t err = set_smem_for_context(kernel, smem, configured);
+    if (err != cudaSuccess) return err;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.grid);
+    cfg.blockDim = dim3(CHAIN_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = a.stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, *a.tmQ, *a.tmK, *a.tmV, *a.tmO, a.params);
+}
+
+cudaError_t FA_CAT(launch_chain_d, FA_HEAD_DIM)(const LaunchArgs& a, bool causal, bool bf16, bool alt) {
+    if (causal) {
+        if (alt) return bf16 ? launch_chain_one<true, true, true>(a) : launch_chain_one<true, false, true>(a);
+        return bf16 ? launch_chain_one<true, true, false>(a) : launch_chain_one<true, false, false>(a);
+    }
+    return bf16 ? launch_chain_one<false, true, false>(a) : launch_chain_one<false, false, false>(a);
+}
+#endif
 
 }  // namespace fa

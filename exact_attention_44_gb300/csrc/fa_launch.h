@@ -52,6 +52,14 @@ cudaError_t launch_d64(const LaunchArgs& a, bool causal, bool bf16, int variant)
 cudaError_t launch_d128(const LaunchArgs& a, bool causal, bool bf16, int variant);
 cudaError_t launch_d256(const LaunchArgs& a, bool causal, bool bf16, int variant);
 
+// Launch fa_fwd_chain_kernel<D, causal, bf16, alt>: whole tiles (fa_fwd,
+// D <= 128) with two softmax chains taking the key blocks in turn; the same
+// grid and tile order as the one-tile kernel's tile mode.
+cudaError_t launch_chain_d16(const LaunchArgs& a, bool causal, bool bf16, bool alt);
+cudaError_t launch_chain_d32(const LaunchArgs& a, bool causal, bool bf16, bool alt);
+cudaError_t launch_chain_d64(const LaunchArgs& a, bool causal, bool bf16, bool alt);
+cudaError_t launch_chain_d128(const LaunchArgs& a, bool causal, bool bf16, bool alt);
+
 // fa_lse_merge: parts share one layout; rows = Z * H * N
 constexpr int MERGE_MAX_PARTS = 16;
 struct MergeArgs {

@@ -366,6 +366,9 @@ fa_status fa_fwd_plan(int Z, int Hq, int Hkv, int Nq, int Nkv, int D, int causal
  *   tiles           query tiles of the launch (after packing)
  *   kv_blocks       (tile, key block) pairs of the launch
  *   busiest_blocks  key blocks of the busiest CTA in the schedule that runs
+ *   softmax_chains  2: whole tiles of head dims up to 128 run the kernel
+ *                   whose softmax is two warpgroups taking the key blocks in
+ *                   turn (the same tiles and order); 1: one chain
  * Errors: those of fa_fwd_plan for bad shapes; FA_ERR_INVALID_ARG for a NULL
  * out, num_sms < 1 or l2_bytes < 1.  fa_debug_force_split applies here too.
  */
@@ -378,6 +381,7 @@ typedef struct {
     int64_t tiles;
     int64_t kv_blocks;
     int64_t busiest_blocks;
+    int softmax_chains;
 } fa_fwd_schedule_info;
 
 fa_status fa_fwd_schedule(int Z, int Hq, int Hkv, int Nq, int Nkv, int D, int causal, int splitkv, int num_sms,
@@ -392,6 +396,9 @@ fa_status fa_fwd_schedule(int Z, int Hq, int Hkv, int Nq, int Nkv, int D, int ca
  *   microseconds; the bound only matters when something is wrong.
  * fa_debug_force_split -- how fa_fwd_splitkv chooses between cutting key
  *   ranges and whole tiles: 0 by the shape (default), 1 always cut, 2 never.
+ * fa_debug_force_chains -- which kernel runs whole tiles of head dims up to
+ *   128: 0 by the shape (default: two softmax chains), 1 two chains, 2 one
+ *   chain.  Both compute the same result (up to the order of rounding).
  * fa_debug_inject_stall -- when enabled, CTA 0 of later launches never issues
  *   the copy of its first K tile, so the wait for it runs out: the kernel
  *   records FA_ERR_DEVICE_TIMEOUT (read with fa_device_status), every role of
@@ -402,6 +409,7 @@ fa_status fa_fwd_schedule(int Z, int Hq, int Hkv, int Nq, int Nkv, int D, int ca
 void fa_debug_set_wait_limit_ms(double ms);
 void fa_debug_inject_stall(int enable);
 void fa_debug_force_split(int mode);
+void fa_debug_force_chains(int mode);
 
 #ifdef __cplusplus
 }

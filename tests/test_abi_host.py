@@ -270,6 +270,9 @@ def test_schedule_matches_the_documented_order(shape):
     bn = 64 if D == 256 else 128
     heads, tq, tk = Z * Hq, -(-Nq // 128), -(-Nkv // bn)
     assert s["split"] == 0 and s["gqa_packed"] == 0
+    # head dims up to 64 with long tiles (>= 16 key blocks a tile on average) run
+    # two softmax chains, the rest one
+    assert s["softmax_chains"] == (2 if D <= 64 and s["kv_blocks"] >= 16 * s["tiles"] else 1)
     assert s["tiles"] == heads * tq and s["grid"] == min(heads * tq, GB300_SMS)
     assert s["kv_blocks"] == Z * Hq * sum(_tile_blocks(mb, Nq, Nkv, bn, causal) for mb in range(tq))
     if causal:
@@ -287,11 +290,22 @@ def test_schedule_matches_the_documented_order(shape):
 def test_schedule_known_values():
     import exact_attention_44_gb300 as fa
     kw = dict(num_sms=GB300_SMS, l2_bytes=GB300_L2)
-    # the bench workload: 512 tiles on 152 CTAs, 4 tiles of 8 blocks on the busiest;
+    # the Z4 H16 N1024 workload: 512 tiles on 152 CTAs, 4 tiles of 8 blocks on the busiest;
     # causal: heaviest first, round-robin, 19 blocks on the busiest (15.2 on average)
     assert fa.fa_fwd_schedule(4, 16, 16, 1024, 1024, 128, False, **kw)["busiest_blocks"] == 32
     c = fa.fa_fwd_schedule(4, 16, 16, 1024, 1024, 128, True, **kw)
-    assert (c["head_group"], c["alternate"], c["busiest_blocks"]) == (64, 0, 19)
+    assert (c["head_group"], c["alternate"], c["busiest_blocks"], c["softmax_chains"]) == (64, 0, 19, 1)
+    # the two-chain kernel runs the same schedule
+    try:
+        fa.fa_debug_force_chains(1)
+        c = fa.fa_fwd_schedule(4, 16, 16, 1024, 1024, 128, True, **kw)
+        assert (c["head_group"], c["alternate"], c["busiest_blocks"], c["softmax_chains"]) == (64, 0, 19, 2)
+    finally:
+        fa.fa_debug_force_chains(0)
+    # head dims up to 64 with long tiles take two chains
+    assert fa.fa_fwd_schedule(8, 16, 16, 2048, 2048, 64, False, **kw)["softmax_chains"] == 2
+    assert fa.fa_fwd_schedule(8, 16, 16, 2048, 2048, 64, True, **kw)["softmax_chains"] == 1
+    assert fa.fa_fwd_schedule(1, 32, 8, 8192, 8192, 128, False, **kw)["softmax_chains"] == 1
     # alternating rounds: 236 blocks on the busiest CTA instead of 284
     assert fa.fa_fwd_schedule(8, 16, 16, 2048, 2048, 256, True, **kw)["busiest_blocks"] == 236
 

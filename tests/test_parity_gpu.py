@@ -183,3 +183,56 @@ def test_negative_and_zero_scale_through_the_split_schedule_and_variants():
         check_full(16, 1, 4, 2, 150, 1500, 128, "bf16", True, scale=0.0, impl="splitkv")
     finally:
         fa.fa_debug_force_split(0)
+
+
+@pytest.fixture(params=[1, 2], ids=["two_chains", "one_chain"])
+def softmax_kernel(request):
+    # whole tiles of D <= 128 run one of two kernels (one or two softmax
+    # chains); the library picks by shape, these tests force each in turn
+    import exact_attention_44_gb300 as fa
+    fa.fa_debug_force_chains(request.param)
+    yield request.param
+    fa.fa_debug_force_chains(0)
+
+
+@pytest.mark.parametrize("D", [16, 32, 64, 128])
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_both_softmax_kernels_head_dims(softmax_kernel, D, dtype, causal):
+    check_full(31, 1, 2, 2, 300, 300, D, dtype, causal)
+
+
+@pytest.mark.parametrize("Nq,Nkv", [(1, 1), (1, 300), (129, 129), (200, 77), (77, 200), (1000, 1000), (256, 1024)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_both_softmax_kernels_ragged(softmax_kernel, Nq, Nkv, causal):
+    # odd block counts: the two chains' hand-off crosses tile boundaries
+    check_full(32, 2, 2, 1, Nq, Nkv, 64, "fp16", causal)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 1), (32, 8)])
+def test_both_softmax_kernels_gqa(softmax_kernel, Hq, Hkv):
+    check_full(33, 2, Hq, Hkv, 130, 900, 128, "bf16", True)
+
+
+def test_both_softmax_kernels_rescale_and_scales(softmax_kernel):
+    # block maxima that keep growing: the maximum moves in both chains, O and
+    # each chain's row sum are rescaled; and the zero and negative scales
+    def grow(q, k, v):
+        kd = (k.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        ramp = np.linspace(0.2, 3.0, k.shape[2])[None, None, :, None]
+        return q, si.round_bits(kd * ramp, "bf16"), v
+    check_full(34, 1, 2, 2, 256, 2048, 64, "bf16", False, transform=grow)
+    check_full(34, 1, 2, 2, 256, 2048, 128, "bf16", True, transform=grow)
+    check_full(35, 1, 2, 1, 300, 700, 64, "fp16", True, scale=0.0)
+    check_full(35, 1, 2, 1, 300, 700, 128, "bf16", False, scale=-0.3)
+
+
+def test_both_softmax_kernels_bitwise_repeatable(softmax_kernel):
+    import torch
+    from exact_attention_44_gb300 import fa_fwd
+    q, k, v = si.qkv(36, 2, 8, 2, 1000, 1000, 64, "fp16")
+    qt, kt, vt = (si.as_torch(x, "fp16").cuda() for x in (q, k, v))
+    outs = [fa_fwd(qt, kt, vt, causal=c) for c in (True, True, False, False)]
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    assert torch.equal(outs[2][0], outs[3][0]) and torch.equal(outs[2][1], outs[3][1])

@@ -10,11 +10,13 @@ from parity_util import check_full
 pytestmark = pytest.mark.gpu
 
 
-def test_withheld_copy_times_out_and_the_context_recovers():
+@pytest.mark.parametrize("chains", [1, 2], ids=["two_chains", "one_chain"])
+def test_withheld_copy_times_out_and_the_context_recovers(chains):
     import torch
 
     import exact_attention_44_gb300 as fa
     fa.build()
+    fa.fa_debug_force_chains(chains)
     q, k, v = si.qkv(21, 1, 4, 2, 1024, 1024, 64, "bf16")
     qt, kt, vt = (si.as_torch(x, "bf16").cuda() for x in (q, k, v))
     assert fa.fa_device_status()[0] == fa.FA_OK
@@ -26,6 +28,7 @@ def test_withheld_copy_times_out_and_the_context_recovers():
     finally:
         fa.fa_debug_inject_stall(False)
         fa.fa_debug_set_wait_limit_ms(0)
+        fa.fa_debug_force_chains(0)
     assert code == fa.FA_ERR_DEVICE_TIMEOUT, hex(word)
     assert word & 0xFF == fa.FA_ERR_DEVICE_TIMEOUT
     assert (word >> 16) == 0          # CTA 0 gave up first
