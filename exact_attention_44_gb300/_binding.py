@@ -54,6 +54,7 @@ _SIGNATURES = {
     "fa_debug_inject_stall": (None, [ctypes.c_int]),
     "fa_debug_force_split": (None, [ctypes.c_int]),
     "fa_debug_force_chains": (None, [ctypes.c_int]),
+    "fa_debug_exp2": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]),
 }
 
 _lock = threading.Lock()
@@ -459,6 +460,21 @@ def fa_debug_set_wait_limit_ms(ms: float) -> None:
 
 def fa_debug_inject_stall(enable: bool) -> None:
     load().fa_debug_inject_stall(int(bool(enable)))
+
+
+def fa_debug_exp2(x, y=None, stream=None):
+    """The softmax kernels' polynomial exponential on a CUDA float32 tensor (a test hook); returns y."""
+    import torch
+
+    if x.dtype != torch.float32 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous float32 CUDA tensor")
+    y = torch.empty_like(x) if y is None else y
+    stream = torch.cuda.current_stream(x.device) if stream is None else stream
+    with torch.cuda.device(x.device):
+        rc = load().fa_debug_exp2(x.data_ptr(), y.data_ptr(), x.numel(), ctypes.c_void_p(stream.cuda_stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_debug_exp2")
+    return y
 
 
 def fa_debug_force_chains(mode: int) -> None:

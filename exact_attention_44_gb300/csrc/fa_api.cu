@@ -910,6 +910,30 @@ fa_status fa_device_status(cudaStream_t stream, uint32_t* detail) {
     return word == 0 ? FA_OK : (fa_status)(word & 0xFFu);
 }
 
+// Test hook (declared in fa.h): the softmax kernels' polynomial exponential
+// applied to an array, so that it can be checked against CUDA's exp2f.
+namespace {
+__global__ void exp2_poly_kernel(const float* __restrict__ x, float* __restrict__ y, int64_t n) {
+    const int64_t i = 2 * ((int64_t)blockIdx.x * blockDim.x + threadIdx.x);
+    if (i >= n) return;
+    const float x1 = i + 1 < n ? x[i + 1] : 0.f;
+    float y0, y1;
+    fa::ptx::unpack_f32x2(fa::ptx::exp2_poly2(fa::ptx::pack_f32x2(x[i], x1)), y0, y1);
+    y[i] = y0;
+    if (i + 1 < n) y[i + 1] = y1;
+}
+}  // namespace
+
+fa_status fa_debug_exp2(const float* x, float* y, int64_t n, cudaStream_t stream) {
+    if (n < 0 || (n > 0 && (x == nullptr || y == nullptr))) return FA_ERR_INVALID_ARG;
+    if (n == 0) return FA_OK;
+    const int64_t pairs = (n + 1) / 2, blocks = (pairs + 255) / 256;
+    if (blocks > INT32_MAX) return FA_ERR_UNSUPPORTED;
+    exp2_poly_kernel<<<(unsigned)blocks, 256, 0, stream>>>(x, y, n);
+    const cudaError_t err = cudaGetLastError();
+    return err == cudaSuccess ? FA_OK : cuda_fail("exp2 test launch", err);
+}
+
 // Test hooks (declared in fa.h): the bound on every device-side wait, and a
 // switch that makes CTA 0 withhold one K tile so that its waits run out.
 void fa_debug_set_wait_limit_ms(double ms) {

@@ -38,6 +38,8 @@
 // copies and MMAs land and frees TMEM.
 #pragma once
 
+#include <type_traits>
+
 #include "fa_fwd_kernel.cuh"
 
 namespace fa {
@@ -50,6 +52,16 @@ constexpr uint32_t CHAIN_REG_SOFTMAX = 176;  // warpgroups 1, 2: the softmax cha
 constexpr uint32_t CHAIN_REG_EPI = 88;       // warpgroup 3: epilogue
 static_assert(128 * (CHAIN_REG_CTRL + 2 * CHAIN_REG_SOFTMAX + CHAIN_REG_EPI) == CHAIN_THREADS * 128,
               "register budgets of the warpgroups");
+
+// Key pairs (of every 16) whose exponentials the chain softmax computes on the
+// FMA pipe (ptx::exp2_poly2) instead of the MUFU unit, in blocks without a
+// masked key.  None: measured on GB300 (Z8 H16 N2048, D 16/32/64, fp16, both
+// masks), giving 2, 4, 6 or 8 pairs of every 16 to the polynomial made every
+// shape slower, by 10-15 % at 2 and 30-40 % at 8 -- a packed FMA pair costs two
+// pipe cycles and the polynomial needs ~8 of them plus integer work, against
+// 8 XU cycles for two MUFU ex2, so it only trades one busy pipe for another
+// and adds issue slots; the softmax here is bound by its latency chain.
+constexpr int chain_emu_pairs(int D) { return D < 0 ? 1 : 0; }
 
 // The one-tile kernel's shared memory, TMEM and barrier layout (so that its
 // producers and MMA issuers run unchanged), with the softmax regions and
@@ -126,7 +138,8 @@ __device__ void chain_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, 
             // the mask goes on the scores before the row max (Correctness
             // requirements); only the diagonal block and the key tail need it
             const int k0 = j * BN;
-            if ((CAUSAL && k0 + BN - 1 > ti.q_start) || (k0 + BN > p.Nkv)) {
+            const bool masked = (CAUSAL && k0 + BN - 1 > ti.q_start) || (k0 + BN > p.Nkv);
+            if (masked) {
                 const int kmax = (CAUSAL ? min(p.Nkv - 1, q_row) : p.Nkv - 1) - k0;  // last kept key of this row
 #pragma unroll
                 for (int x = 0; x < BN; ++x)
@@ -185,25 +198,41 @@ __device__ void chain_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, 
             mx[(g & 1u) * BM + row] = m;
             ptx::mbar_arrive(bar(T::B_RED + (g & 1u)));
             // p = 2^(s·c − m): l sums the fp32 p, the P·V product takes p cast
-            // to the input type, over the first BN/2 columns of the slot
+            // to the input type, over the first BN/2 columns of the slot.  In
+            // a block with no masked key, EMU of every 16 key pairs take the
+            // polynomial exponential on the FMA pipe and the others the MUFU
+            // unit's ex2, whose throughput otherwise bounds this loop.
             const uint64_t negm2 = ptx::pack_f32x2(-m, -m);
             uint64_t sum_a = ptx::pack_f32x2(0.f, 0.f), sum_b = sum_a;
+            auto exps = [&](auto emu) {
+                constexpr int EMU = decltype(emu)::value;
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
-                uint32_t pk[16];
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    uint32_t pk[16];
 #pragma unroll
-                for (int x = 0; x < 16; ++x) {
-                    const int k = c4 * 32 + 2 * x;
-                    float a0, a1;
-                    ptx::unpack_f32x2(ptx::ffma2(ptx::pack_f32x2(s[k], s[k + 1]), c2, negm2), a0, a1);
-                    const float p0 = ptx::ex2(a0), p1 = ptx::ex2(a1);
-                    if (x & 1) sum_b = ptx::fadd2(sum_b, ptx::pack_f32x2(p0, p1));
-                    else sum_a = ptx::fadd2(sum_a, ptx::pack_f32x2(p0, p1));
-                    pk[x] = pack2<BF16>(p0, p1);
+                    for (int x = 0; x < 16; ++x) {
+                        const int k = c4 * 32 + 2 * x;
+                        const uint64_t a2 = ptx::ffma2(ptx::pack_f32x2(s[k], s[k + 1]), c2, negm2);
+                        float p0, p1;
+                        if (x < EMU) {
+                            ptx::unpack_f32x2(ptx::exp2_poly2(a2), p0, p1);
+                        } else {
+                            float a0, a1;
+                            ptx::unpack_f32x2(a2, a0, a1);
+                            p0 = ptx::ex2(a0);
+                            p1 = ptx::ex2(a1);
+                        }
+                        if (x & 1) sum_b = ptx::fadd2(sum_b, ptx::pack_f32x2(p0, p1));
+                        else sum_a = ptx::fadd2(sum_a, ptx::pack_f32x2(p0, p1));
+                        pk[x] = pack2<BF16>(p0, p1);
+                    }
+                    // keys 32·c4 .. at packed columns 16·c4 ..: scores this thread has read
+                    ptx::tmem_st16(s_addr + 16 * c4, pk);
                 }
-                // keys 32·c4 .. at packed columns 16·c4 ..: scores this thread has read
-                ptx::tmem_st16(s_addr + 16 * c4, pk);
-            }
+            };
+            constexpr int EMU = chain_emu_pairs(D);
+            if (EMU > 0 && !masked) exps(std::integral_constant<int, EMU>{});
+            else exps(std::integral_constant<int, 0>{});
             if (rescale) {
                 // O holds every block up to g - 1 once that block's P·V is complete
                 if (!warp_wait_phase(bar(T::B_PVDONE + rslot<T::SR>(g - 1u)), rphase<T::SR>(g - 1u), ctl,

@@ -360,6 +360,36 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return d;
 }
 
+// 2^x for the two values of a packed pair on the FMA and integer pipes, for
+// softmax arguments x <= 8 (values below -126 are taken as -126, giving
+// ~1.2e-38 instead of a smaller positive number).  Cody-Waite range
+// reduction in base 2 -- n = round(x), f = x - n in [-1/2, 1/2], exact in
+// fp32 -- then a degree-4 minimax polynomial of 2^f in Horner form (max
+// relative error 2.6e-6; coefficients from a Remez exchange, generated and
+// checked by exact_attention_44_gb300/exp2_poly.py), then n added to the
+// exponent field.  The rounding to an integer adds 1.5 * 2^23 (the sum's
+// low mantissa bits hold n, and shifted left by 23 they are n << 23).
+constexpr float EXP2_C0 = 0x1.ffffe8p-1f, EXP2_C1 = 0x1.62e0dcp-1f, EXP2_C2 = 0x1.ec06dap-3f,
+                EXP2_C3 = 0x1.ca1440p-5f, EXP2_C4 = 0x1.3997d6p-7f;
+__device__ __forceinline__ uint64_t exp2_poly2(uint64_t x2) {
+    float x0, x1;
+    unpack_f32x2(x2, x0, x1);
+    const uint64_t xc = pack_f32x2(fmaxf(x0, -126.f), fmaxf(x1, -126.f));
+    const uint64_t t2 = fadd2(xc, pack_f32x2(12582912.f, 12582912.f));     // x + 1.5 * 2^23
+    const uint64_t n2 = fadd2(t2, pack_f32x2(-12582912.f, -12582912.f));   // round(x)
+    const uint64_t f2 = ffma2(n2, pack_f32x2(-1.f, -1.f), xc);              // x - round(x)
+    uint64_t p2 = pack_f32x2(EXP2_C4, EXP2_C4);
+    p2 = ffma2(p2, f2, pack_f32x2(EXP2_C3, EXP2_C3));
+    p2 = ffma2(p2, f2, pack_f32x2(EXP2_C2, EXP2_C2));
+    p2 = ffma2(p2, f2, pack_f32x2(EXP2_C1, EXP2_C1));
+    p2 = ffma2(p2, f2, pack_f32x2(EXP2_C0, EXP2_C0));
+    float p0, p1, t0, t1;
+    unpack_f32x2(p2, p0, p1);
+    unpack_f32x2(t2, t0, t1);
+    return pack_f32x2(__uint_as_float(__float_as_uint(p0) + (__float_as_uint(t0) << 23)),
+                      __uint_as_float(__float_as_uint(p1) + (__float_as_uint(t1) << 23)));
+}
+
 // Hardware base-2 exponential (MUFU); ex2(-inf) = +0.
 __device__ __forceinline__ float ex2(float x) {
     float y;

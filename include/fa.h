@@ -407,6 +407,18 @@ fa_status fa_fwd_schedule(int Z, int Hq, int Hkv, int Nq, int Nkv, int D, int ca
  *   launch are incomplete.  No GPU fault, trap or hang is involved.
  */
 void fa_debug_set_wait_limit_ms(double ms);
+
+/*
+ * fa_debug_exp2 -- test hook: y[i] = 2^x[i] computed by the polynomial
+ *   exponential the softmax kernels use for part of their exponentials (the
+ *   pages compute p = exp2(s·scale·log2e − m): "把 FlashAttention 搬上昇腾...",
+ *   section 一): Cody-Waite reduction in base 2, a degree-4 minimax polynomial
+ *   of 2^f on [-1/2, 1/2] (max relative error 2.6e-6), the integer part added
+ *   to the exponent field.  Meant for arguments <= 8 (the softmax never
+ *   exceeds its rescale threshold); x <= -126 gives ~1.2e-38.  x and y are
+ *   device arrays of n floats; asynchronous on `stream`.
+ */
+fa_status fa_debug_exp2(const float* x, float* y, int64_t n, cudaStream_t stream);
 void fa_debug_inject_stall(int enable);
 void fa_debug_force_split(int mode);
 void fa_debug_force_chains(int mode);
