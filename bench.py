@@ -484,9 +484,13 @@ def run_profile(args, device):
     stream = torch.cuda.current_stream(device)
     o = torch.empty((Z, Hq, Nq, D), dtype=q.dtype, device=device)
     lse = torch.empty((Z, Hq, Nq), dtype=torch.float32, device=device)
+    ws = fa.workspace_for(D, device) if args.profile_impl == "splitkv" else None
     for _ in range(args.warmup + args.steps):
         for c in flags:
-            fa.fa_fwd(q, k, v, o=o, lse=lse, causal=c, stream=stream)
+            if ws is not None:
+                fa.fa_fwd_splitkv(q, k, v, o=o, lse=lse, causal=c, workspace=ws, stream=stream)
+            else:
+                fa.fa_fwd(q, k, v, o=o, lse=lse, causal=c, stream=stream)
     torch.cuda.synchronize(device)
     code, word = fa.fa_device_status(stream)
     if code != fa.FA_OK:
@@ -793,6 +797,8 @@ def main(argv=None):
                     help="seconds of oracle work for cpu_baseline (and the cap per step of --impl reference)")
     ap.add_argument("--profile", action="store_true",
                     help="only W + K eager launches of --workload on one input set, no timing (an ncu target)")
+    ap.add_argument("--profile-impl", choices=["fwd", "splitkv"], default="fwd",
+                    help="with --profile: the entry point launched (fa_fwd or fa_fwd_splitkv)")
     ap.add_argument("--force-chains", type=int, choices=[0, 1, 2], default=0,
                     help="with --profile: 0 the library's choice, 1 two softmax chains, 2 one")
     ap.add_argument("--bwd-only", action="store_true",

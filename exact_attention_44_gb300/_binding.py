@@ -21,6 +21,7 @@ FA_ERR_ALIGNMENT = 3
 FA_ERR_CUDA = 4
 FA_ERR_DEVICE_TIMEOUT = 5
 FA_ERR_WORKSPACE = 6
+FA_ERR_DEVICE_CHECK = 7
 FA_MERGE_MAX_PARTS = 16
 FA_DTYPE_F16 = 0
 FA_DTYPE_BF16 = 1
@@ -59,6 +60,7 @@ _SIGNATURES = {
 
 _lock = threading.Lock()
 _lib = None
+_path = None  # another build of libfa to load instead of the default one (use_library)
 
 
 class FaError(RuntimeError):
@@ -86,12 +88,23 @@ def library_path() -> str:
     return _build.LIB
 
 
+def use_library(path: str | None) -> str | None:
+    """Make later calls go to the libfa.so at `path` (None: the default build), e.g. the
+    debug-check build; returns the path used before.  Not for concurrent use."""
+    global _lib, _path
+    with _lock:
+        before = _path
+        _path = path
+        _lib = None
+    return before
+
+
 def load() -> ctypes.CDLL:
     """Load libfa.so (built by exact_attention_44_gb300.build); raises if it is missing."""
     global _lib
     with _lock:
         if _lib is None:
-            path = library_path()
+            path = _path or library_path()
             if not os.path.exists(path):
                 raise ImportError(f"libfa.so is not built ({path}); run `python -m exact_attention_44_gb300.build`")
             lib = ctypes.CDLL(path)

@@ -1,10 +1,12 @@
 """Build libfa.so in-tree with nvcc for sm_103a (one -gencode, parallel TUs).
 
-    python -m exact_attention_44_gb300.build [--force] [--verbose]
+    python -m exact_attention_44_gb300.build [--force] [--verbose] [--debug-checks]
 
 Objects and the shared library go to exact_attention_44_gb300/_build/ (git
 ignored).  A content hash of the sources, headers and flags is stored next to
-the library; an unchanged tree is not rebuilt.
+the library; an unchanged tree is not rebuilt.  --debug-checks builds a
+second library, _build/checks/libfa.so, whose forward kernels check every
+unit they decode against the launch's sizes (FA_DEBUG_CHECKS=1).
 """
 from __future__ import annotations
 
@@ -53,18 +55,26 @@ def _tree_hash(extra_flags: list[str]) -> str:
     return h.hexdigest()
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
-    """Compile every translation unit (in parallel) and link libfa.so; returns its path."""
+def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None,
+          debug_checks: bool = False) -> str:
+    """Compile every translation unit (in parallel) and link libfa.so; returns its path.
+
+    debug_checks: build the index-checking variant into _build/checks/ instead."""
     extra_flags = list(extra_flags or [])
-    os.makedirs(BUILD, exist_ok=True)
+    build_dir, lib_path = BUILD, LIB
+    if debug_checks:
+        extra_flags.append("-DFA_DEBUG_CHECKS=1")
+        build_dir = os.path.join(BUILD, "checks")
+        lib_path = os.path.join(build_dir, "libfa.so")
+    os.makedirs(build_dir, exist_ok=True)
     digest = _tree_hash(extra_flags)
-    stamp = LIB + ".hash"
-    if not force and os.path.exists(LIB) and os.path.exists(stamp) and open(stamp).read() == digest:
-        return LIB
+    stamp = lib_path + ".hash"
+    if not force and os.path.exists(lib_path) and os.path.exists(stamp) and open(stamp).read() == digest:
+        return lib_path
     cc = nvcc()
     jobs = []
     for src, obj_name, unit_flags in UNITS:
-        obj = os.path.join(BUILD, obj_name)
+        obj = os.path.join(build_dir, obj_name)
         cmd = [cc, *FLAGS, *unit_flags, *extra_flags, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
@@ -86,23 +96,25 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
             sys.stderr.write(f"--- {src}\n{r.stdout}{r.stderr}\n")
     if failed:
         raise RuntimeError("libfa build failed")
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     link = [cc, *ARCH, "-shared", "-o", tmp, *[obj for _, obj, _ in jobs]]
     r = subprocess.run(link, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"libfa link failed:\n{r.stdout}{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib_path)
     with open(stamp, "w") as f:
         f.write(digest)
-    return LIB
+    return lib_path
 
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--verbose", action="store_true", help="print ptxas register/spill/smem usage")
+    ap.add_argument("--debug-checks", action="store_true",
+                    help="build the variant whose kernels check every unit against the launch's sizes")
     a = ap.parse_args(argv)
-    print(build(force=a.force, verbose=a.verbose))
+    print(build(force=a.force, verbose=a.verbose, debug_checks=a.debug_checks))
 
 
 if __name__ == "__main__":

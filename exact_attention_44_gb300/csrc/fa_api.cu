@@ -626,6 +626,7 @@ const char* fa_status_string(fa_status s) {
         case FA_ERR_CUDA: return "FA_ERR_CUDA";
         case FA_ERR_DEVICE_TIMEOUT: return "FA_ERR_DEVICE_TIMEOUT";
         case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE";
+        case FA_ERR_DEVICE_CHECK: return "FA_ERR_DEVICE_CHECK";
     }
     return "FA_ERR_UNKNOWN";
 }

@@ -105,6 +105,7 @@ __device__ void chain_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, 
     const Sched<CAUSAL, BN, false, ALT> sc(p);
     for (int64_t pos = sc.first(p); sc.valid(pos, p); ++ntile) {
         const Seg ti = sc.seg(pos, p);
+        if (!seg_checked<ALT ? 4 : 0, BN>(ti, p, ctl, SITE_CHECK_SOFTMAX)) return;
         pos = sc.next(pos, ti, p);
         const int q_row = ti.q_start + row;
         float m = -INFINITY, l = 0.f;  // this chain's view of the running max, its part of the row sum
@@ -281,6 +282,10 @@ __device__ void chain_epilogue(const CUtensorMap* tmO, const FwdParams& p, uint3
     const Sched<CAUSAL, T::BN, false, ALT> sc(p);
     for (int64_t pos = sc.first(p); sc.valid(pos, p); ++ntile) {
         const Seg ti = sc.seg(pos, p);
+        if (!seg_checked<ALT ? 4 : 0, T::BN>(ti, p, ctl, SITE_CHECK_EPILOGUE)) {
+            drain();
+            return;
+        }
         pos = sc.next(pos, ti, p);
         step += ti.je - ti.jb;
         const uint32_t slot = ntile & 1u;

@@ -198,6 +198,45 @@ __device__ __forceinline__ int key_block(const Seg& sg, int j) {
     }
 }
 
+// Debug builds (compiled with FA_DEBUG_CHECKS=1; `python -m
+// exact_attention_44_gb300.build --debug-checks`) check every unit a role
+// decodes against the launch's sizes before the role touches memory for it:
+// batch, query head, key/value head (and its GQA relation), first query row,
+// key-block range and partial-result slot.  A unit outside them records
+// STATUS_DEVICE_CHECK with the role's site in the status word and raises the
+// CTA's abort flag, so every role stops at its next wait and the kernel ends
+// as after a timed-out wait (copies and products land, TMEM is freed).  No
+// trap or device assert is used.  Release builds compile the checks away.
+#ifndef FA_DEBUG_CHECKS
+#define FA_DEBUG_CHECKS 0
+#endif
+
+template <int VAR, int BN>
+__device__ __forceinline__ bool seg_checked(const Seg& s, const FwdParams& p, const Ctl& c, uint32_t site) {
+    if constexpr (!FA_DEBUG_CHECKS) {
+        return true;
+    } else {
+        const bool packed = var_kind(VAR) != 0 && p.cu_q != nullptr;
+        const int nb = packed ? 1 : p.Z;  // batch extent of the tensor maps
+        const int tk = (s.nk + BN - 1) / BN;
+        bool ok = s.z >= 0 && s.z < p.Z && s.zc >= 0 && s.zc < nb && s.hq >= 0 && s.hq < p.Hq && s.hk >= 0 &&
+                  s.hk < p.Hkv && s.hk == s.hq / p.group && s.q_start >= 0 && s.q_start % BM == 0 &&
+                  s.qrow0 >= 0 && s.krow0 >= 0 && s.nq >= 0 && s.nk >= 0 && s.qrow0 + s.nq <= p.Nq &&
+                  s.krow0 + s.nk <= p.Nkv && s.jb >= 0 && s.jb < s.je && s.je <= s.nkv && s.lse0 >= 0 &&
+                  s.lse0 + (packed ? 0 : s.nq) <= (int64_t)p.Z * p.Hq * p.Nq &&
+                  s.slot >= -1 && s.slot < 2 * (int)gridDim.x;
+        // a key block past the keys: allowed only as a variant tile's single
+        // block whose rows keep no key (it is masked whole)
+        if (var_kind(VAR) == 0) ok = ok && s.je <= tk && s.q_start < s.nq;
+        else ok = ok && (s.je <= tk || s.je == s.jb + 1);
+        if (!ok) {
+            *c.abort_flag = 1;
+            atomicCAS(c.status, 0u, STATUS_DEVICE_CHECK | (site << 8) | ((blockIdx.x & 0xFFFFu) << 16));
+        }
+        return ok;
+    }
+}
+
 // Barrier slot and phase parity of key block g (global count) in a ring of R.
 template <int R>
 __device__ __forceinline__ uint32_t rslot(uint32_t g) { return g % R; }
@@ -437,6 +476,7 @@ __device__ void run_producer_qk(const CUtensorMap* tmQ, const CUtensorMap* tmK, 
     bool ok = true;
     bool withheld = false;
     auto load_q = [&](const Seg& sg) -> bool {
+        if (!seg_checked<VAR, T::BN>(sg, p, ctl, SITE_CHECK_LOAD_QK)) return false;
         const uint32_t s = qi % T::Q_STAGES, ph = (qi / T::Q_STAGES) & 1u;
         if (!wait_phase(bar(T::B_QEMPTY + s), ph ^ 1u, ctl, SITE_Q_EMPTY)) return false;
         ptx::mbar_arrive_expect_tx(bar(T::B_QFULL + s), T::Q_BYTES);
@@ -452,6 +492,7 @@ __device__ void run_producer_qk(const CUtensorMap* tmQ, const CUtensorMap* tmK, 
     if (sc.valid(pos, p)) ok = load_q(sc.seg(pos, p));
     while (ok && sc.valid(pos, p)) {
         const Seg sg = sc.seg(pos, p);
+        if (!seg_checked<VAR, T::BN>(sg, p, ctl, SITE_CHECK_LOAD_QK)) { ok = false; break; }
         const int64_t nxt = sc.next(pos, sg, p);
         for (int j = sg.jb; j < sg.je; ++j) {
             // slot ki & 1 held block ki - 2, free once S of that block is complete
@@ -501,6 +542,7 @@ __device__ void run_producer_v(const CUtensorMap* tmV, const FwdParams& p, uint3
     const Sched<CAUSAL, T::BN, (var_kind(VAR) != 0), var_alt(VAR)> sc(p);
     for (int64_t pos = sc.first(p); ok && sc.valid(pos, p);) {
         const Seg sg = sc.seg(pos, p);
+        if (!seg_checked<VAR, T::BN>(sg, p, ctl, SITE_CHECK_LOAD_V)) { ok = false; break; }
         for (int j = sg.jb; j < sg.je; ++j) {
             // slot vi & 1 held block vi - 2, free once its P·V is complete
             const uint32_t s = vi & 1u;
@@ -544,6 +586,7 @@ __device__ void run_mma_qk(const FwdParams& p, uint32_t sbase, uint32_t bar0, ui
     const Sched<CAUSAL, T::BN, (var_kind(VAR) != 0), var_alt(VAR)> sc(p);
     for (int64_t pos = sc.first(p); ok && sc.valid(pos, p);) {
         const Seg sg = sc.seg(pos, p);
+        if (!seg_checked<VAR, T::BN>(sg, p, ctl, SITE_CHECK_MMA_S)) { ok = false; break; }
         pos = sc.next(pos, sg, p);
         const uint32_t qs = qi % T::Q_STAGES;
         if (!wait_phase(bar(T::B_QFULL + qs), (qi / T::Q_STAGES) & 1u, ctl, SITE_Q_FULL)) { ok = false; break; }
@@ -595,6 +638,7 @@ __device__ void run_mma_pv(const FwdParams& p, uint32_t sbase, uint32_t bar0, ui
     const Sched<CAUSAL, T::BN, (var_kind(VAR) != 0), var_alt(VAR)> sc(p);
     for (int64_t pos = sc.first(p); ok && sc.valid(pos, p); ++ntile) {
         const Seg sg = sc.seg(pos, p);
+        if (!seg_checked<VAR, T::BN>(sg, p, ctl, SITE_CHECK_MMA_PV)) { ok = false; break; }
         pos = sc.next(pos, sg, p);
         for (int j = sg.jb; j < sg.je; ++j, ++g) {
             const uint32_t vb = g & 1u, r = rslot<T::SR>(g);
@@ -700,6 +744,7 @@ __device__ void run_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, fl
     const Sched<CAUSAL, BN, (var_kind(VAR) != 0), var_alt(VAR)> sc(p);
     for (int64_t pos = sc.first(p); sc.valid(pos, p); ++ntile) {
         const Seg ti = sc.seg(pos, p);
+        if (!seg_checked<VAR, BN>(ti, p, ctl, SITE_CHECK_SOFTMAX)) return;
         pos = sc.next(pos, ti, p);
         const int q_row = ti.q_start + row;
         float slope2 = 0.f;
@@ -942,6 +987,10 @@ __device__ void run_epilogue(const CUtensorMap* tmO, const FwdParams& p, uint32_
     const Sched<CAUSAL, T::BN, (var_kind(VAR) != 0), var_alt(VAR)> sc(p);
     for (int64_t pos = sc.first(p); sc.valid(pos, p); ++ntile) {
         const Seg ti = sc.seg(pos, p);
+        if (!seg_checked<VAR, T::BN>(ti, p, ctl, SITE_CHECK_EPILOGUE)) {
+            drain();
+            return;
+        }
         pos = sc.next(pos, ti, p);
         step += ti.je - ti.jb;
         const uint32_t slot = ntile & 1u;

@@ -43,7 +43,18 @@ enum WaitSite : uint32_t {
     SITE_B_DQ_FREE = 30,
     SITE_B_ACC_FULL = 31,
     SITE_B_ACC_FREE = 32,
+    // debug index checks (builds with FA_DEBUG_CHECKS=1): the role that found
+    // a unit outside the launch's sizes
+    SITE_CHECK_LOAD_QK = 40,
+    SITE_CHECK_LOAD_V = 41,
+    SITE_CHECK_MMA_S = 42,
+    SITE_CHECK_MMA_PV = 43,
+    SITE_CHECK_SOFTMAX = 44,
+    SITE_CHECK_EPILOGUE = 45,
 };
+
+// Status code of a failed debug index check (FA_ERR_DEVICE_CHECK in fa.h).
+constexpr uint32_t STATUS_DEVICE_CHECK = 7;
 
 struct FwdParams {
     void* o;                 // output, dtype of the inputs, d-stride 1

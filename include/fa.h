@@ -41,7 +41,9 @@ typedef enum {
     FA_ERR_ALIGNMENT = 3,       /* d-stride != 1, a base or stride not 16-byte aligned, negative stride */
     FA_ERR_CUDA = 4,            /* a CUDA runtime/driver call failed (launch, tensor map, device query) */
     FA_ERR_DEVICE_TIMEOUT = 5,  /* a bounded device-side wait ran out (see fa_device_status) */
-    FA_ERR_WORKSPACE = 6        /* workspace missing, not 256-byte aligned, or smaller than required */
+    FA_ERR_WORKSPACE = 6,       /* workspace missing, not 256-byte aligned, or smaller than required */
+    FA_ERR_DEVICE_CHECK = 7     /* debug-check builds only: a kernel role decoded a unit outside the
+                                   launch's sizes (see fa_device_status) and stopped */
 } fa_status;
 
 typedef enum { FA_DTYPE_F16 = 0, FA_DTYPE_BF16 = 1 } fa_dtype;
@@ -324,8 +326,12 @@ const char* fa_status_string(fa_status status);
 /*
  * fa_device_status -- synchronise `stream`, then read and clear the current
  * device's status word.  Returns FA_OK, FA_ERR_DEVICE_TIMEOUT (a bounded
- * mbarrier wait inside a kernel gave up and the kernel exited cleanly), or
- * FA_ERR_CUDA if the synchronisation itself failed.  When `detail` is not
+ * mbarrier wait inside a kernel gave up and the kernel exited cleanly),
+ * FA_ERR_DEVICE_CHECK (only in a library built with debug index checks,
+ * `python -m exact_attention_44_gb300.build --debug-checks`: a role of the
+ * forward kernel found a unit outside the launch's sizes, recorded it and
+ * stopped; the wait site field then names the role), or FA_ERR_CUDA if the
+ * synchronisation itself failed.  When `detail` is not
  * NULL it receives the raw word: bits 0-7 the code, 8-15 the wait site,
  * 16-31 the CTA index that gave up first.
  */
