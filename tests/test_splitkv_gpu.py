@@ -148,3 +148,31 @@ def test_gqa_packed_short_queries(Z, Hq, Hkv, Nq, Nkv, impl):
 def test_gqa_pack_skipped_for_other_layouts_and_causal():
     check_full(43, 2, 8, 2, 7, 800, 64, "fp16", False, layout="bsnd", impl="splitkv")
     check_full(44, 2, 8, 2, 7, 800, 64, "fp16", True, impl="splitkv")
+
+
+@pytest.mark.parametrize("D", [16, 32, 64, 128])
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_few_row_tiles(D, dtype):
+    # cut launches of tiles with few query rows: decode rows (GQA-packed: 4
+    # query heads x 2 rows = 8 rows a tile) against thousands of keys, and 64
+    # plain rows, at every head dim up to 128
+    check_full(46, 2, 8, 2, 2, 3000, D, dtype, False, impl="splitkv")
+    check_full(47, 1, 2, 2, 64, 2500, D, dtype, False, impl="splitkv")
+
+
+def test_few_row_stall_times_out_and_recovers():
+    import torch
+    import exact_attention_44_gb300 as fa
+    q, k, v = (si.as_torch(x, "bf16").cuda() for x in si.qkv(48, 1, 8, 2, 1, 4096, 128, "bf16"))
+    fa.fa_debug_set_wait_limit_ms(100)
+    fa.fa_debug_inject_stall(True)
+    try:
+        fa.fa_fwd_splitkv(q, k, v)
+        code, word = fa.fa_device_status()
+    finally:
+        fa.fa_debug_inject_stall(False)
+        fa.fa_debug_set_wait_limit_ms(0)
+    assert code == fa.FA_ERR_DEVICE_TIMEOUT and (word >> 16) == 0
+    check_full(48, 1, 8, 2, 1, 4096, 128, "bf16", False, impl="splitkv")
+    torch.cuda.synchronize()
+    assert fa.fa_device_status()[0] == 0
