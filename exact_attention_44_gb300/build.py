@@ -28,7 +28,7 @@ LIB = os.path.join(BUILD, "libfa.so")
 # (source, object, extra flags): the per-head-dim launchers are one source
 # each, compiled once per supported head dim
 FWD_DIMS = (16, 32, 64, 128, 256)
-BWD_DIMS = (16, 32, 64, 128)
+BWD_DIMS = (16, 32, 64, 128, 256)
 UNITS = ([(src, src.replace(".cu", ".o"), []) for src in ("fa_api.cu", "fa_lse_merge.cu", "fa_noalloc.cu")] +
          [("fa_fwd_dim.cu", f"fa_fwd_d{d}.o", [f"-DFA_HEAD_DIM={d}"]) for d in FWD_DIMS] +
          [("fa_bwd_dim.cu", f"fa_bwd_d{d}.o", [f"-DFA_HEAD_DIM={d}"]) for d in BWD_DIMS])

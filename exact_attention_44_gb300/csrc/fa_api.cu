@@ -723,7 +723,7 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float*
 
 fa_status fa_bwd_workspace_size(int Z, int Hq, int Nq, int D, size_t* bytes) {
     if (bytes == nullptr || Z < 0 || Hq < 0 || Nq < 0) return FA_ERR_INVALID_ARG;
-    if (!(D == 16 || D == 32 || D == 64 || D == 128)) return FA_ERR_UNSUPPORTED;
+    if (!supported_head_dim(D)) return FA_ERR_UNSUPPORTED;
     *bytes = bwd_workspace_bytes(Z, Hq, Nq, D);
     return FA_OK;
 }
@@ -735,7 +735,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  fa_dtype dtype, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
     fa_status st = check_shape(Z, Hq, Hkv, Nq, Nkv, D, causal);
     if (st != FA_OK) return st;
-    if (!(D == 16 || D == 32 || D == 64 || D == 128)) return FA_ERR_UNSUPPORTED;
+    if (!supported_head_dim(D)) return FA_ERR_UNSUPPORTED;
     if (dtype != FA_DTYPE_F16 && dtype != FA_DTYPE_BF16) return FA_ERR_UNSUPPORTED;
     // any finite scale whose log2 factor is finite in fp32: the backward
     // builds P = 2^(s·scale·log2e − lse·log2e) from the saved lse (no row
@@ -803,12 +803,15 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     p.status = info->status;
     p.wait_limit_ns = wait_limit_ns();
 
+    // operand loads: 128-row boxes; at D = 256 the kernel moves 64-row steps
+    // (and its resident 128-row tiles as two boxes)
     CUtensorMap mk, mv, mq, mdo;
     CUresult cr;
-    if ((cr = make_map(&mk, k, dtype, D, Nkv, Hkv, Z, sk, 128)) != CUDA_SUCCESS) return cuda_fail("K tensor map", cr);
-    if ((cr = make_map(&mv, v, dtype, D, Nkv, Hkv, Z, sv, 128)) != CUDA_SUCCESS) return cuda_fail("V tensor map", cr);
-    if ((cr = make_map(&mq, q, dtype, D, Nq, Hq, Z, sq, 128)) != CUDA_SUCCESS) return cuda_fail("Q tensor map", cr);
-    if ((cr = make_map(&mdo, dO, dtype, D, Nq, Hq, Z, sdo, 128)) != CUDA_SUCCESS)
+    const int box = D == 256 ? 64 : 128;
+    if ((cr = make_map(&mk, k, dtype, D, Nkv, Hkv, Z, sk, box)) != CUDA_SUCCESS) return cuda_fail("K tensor map", cr);
+    if ((cr = make_map(&mv, v, dtype, D, Nkv, Hkv, Z, sv, box)) != CUDA_SUCCESS) return cuda_fail("V tensor map", cr);
+    if ((cr = make_map(&mq, q, dtype, D, Nq, Hq, Z, sq, box)) != CUDA_SUCCESS) return cuda_fail("Q tensor map", cr);
+    if ((cr = make_map(&mdo, dO, dtype, D, Nq, Hq, Z, sdo, box)) != CUDA_SUCCESS)
         return cuda_fail("dO tensor map", cr);
     CUtensorMap mdq, mdk, mdv;
     if ((cr = make_map(&mdq, dq, dtype, D, Nq, Hq, Z, sdq, 32)) != CUDA_SUCCESS) return cuda_fail("dQ tensor map", cr);
@@ -832,7 +835,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
         case 16: err = fa::launch_bwd_d16(a, causal != 0, bf16); break;
         case 32: err = fa::launch_bwd_d32(a, causal != 0, bf16); break;
         case 64: err = fa::launch_bwd_d64(a, causal != 0, bf16); break;
-        default: err = fa::launch_bwd_d128(a, causal != 0, bf16); break;
+        case 128: err = fa::launch_bwd_d128(a, causal != 0, bf16); break;
+        default: err = fa::launch_bwd_d256(a, causal != 0, bf16); break;
     }
     return err == cudaSuccess ? FA_OK : cuda_fail("backward launch", err);
 }

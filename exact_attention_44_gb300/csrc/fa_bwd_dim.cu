@@ -1,11 +1,15 @@
 // Specialisations of the attention backward for one head dim, D =
 // FA_HEAD_DIM (compiled once per supported D, in parallel).
 #ifndef FA_HEAD_DIM
-#error "compile with -DFA_HEAD_DIM=<16|32|64|128>"
+#error "compile with -DFA_HEAD_DIM=<16|32|64|128|256>"
 #endif
 #include <cstdint>
 
+#if FA_HEAD_DIM == 256
+#include "fa_bwd_wide_kernel.cuh"
+#else
 #include "fa_bwd_kernel.cuh"
+#endif
 #include "fa_launch.h"
 
 namespace fa {
@@ -13,11 +17,16 @@ namespace fa {
 template <bool CAUSAL, bool BF16>
 static cudaError_t launch_one(const BwdLaunchArgs& a) {
     constexpr int D = FA_HEAD_DIM;
-    using T = BwdTraits<D>;
+#if FA_HEAD_DIM == 256
+    auto bwd = fa_bwd_wide_kernel<CAUSAL, BF16>;
+    constexpr int SMEM = WideTraits::SMEM_BYTES, THREADS = WIDE_THREADS;
+#else
     auto bwd = fa_bwd_kernel<D, CAUSAL, BF16>;
+    constexpr int SMEM = BwdTraits<D>::FUSED_SMEM_BYTES, THREADS = BWD_THREADS;
+#endif
     static std::atomic<uint64_t> configured{0};  // context the opt-in shared memory size was set in
     cudaError_t err;
-    if ((err = set_smem_for_context(bwd, T::FUSED_SMEM_BYTES, configured)) != cudaSuccess) return err;
+    if ((err = set_smem_for_context(bwd, SMEM, configured)) != cudaSuccess) return err;
     // Δ and lse2 per query row; then dK, dV and dQ in one launch.  Each
     // launch is a programmatic dependent of the one before it on the stream:
     // its set-up overlaps that kernel's tail, and it waits for it
@@ -34,8 +43,8 @@ static cudaError_t launch_one(const BwdLaunchArgs& a) {
     cfg.dynamicSmemBytes = 0;
     if ((err = cudaLaunchKernelEx(&cfg, fa_bwd_pre_kernel<D, BF16>, a.params)) != cudaSuccess) return err;
     cfg.gridDim = dim3(a.grid);
-    cfg.blockDim = dim3(BWD_THREADS);
-    cfg.dynamicSmemBytes = T::FUSED_SMEM_BYTES;
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM;
     return cudaLaunchKernelEx(&cfg, bwd, *a.tmK, *a.tmV, *a.tmQ, *a.tmDO, *a.tmDK, *a.tmDV, *a.tmDQ, a.params);
 }
 

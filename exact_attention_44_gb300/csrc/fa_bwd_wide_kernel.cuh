@@ -1,0 +1,628 @@
+// Attention backward for head dim 256 on sm_103a: gradients dQ, dK, dV of
+// the fused forward from the saved log-sum-exp (blog "把 FlashAttention 搬上昇腾：
+// Triton-Ascend CV Pipeline 优化实战", section 二: recompute P from the lse,
+// then dP, dS and the three gradients; section 七 treats D = 256 in pieces
+// of D = 128 for the same reason this kernel does: one pass does not fit).
+//
+// At D = 256 the layout of the smaller head dims (fa_bwd_kernel.cuh) fits
+// neither budget: its dK/dV phase would need Sᵀ, dPᵀ, dV and dK in tensor
+// memory (128 + 128 + 256 + 256 of 512 columns) and 64 KB tiles of K, V, Q and
+// dO in shared memory (256 of 227 KB).  So:
+//   dK/dV phase   per unit (128-key block, kv head), K and V resident, query
+//                 steps of 64 rows (Q, dO: 32 KB each), and two passes over
+//                 the steps, each with one 256-column accumulator in TMEM:
+//                   dV pass   Sᵀ = K Qᵢᵀ, Pᵀ = 2^(Sᵀ·scale·log2e − lse2ᵢ),
+//                             dV += Pᵀ dOᵢ
+//                   dK pass   Sᵀ, Pᵀ as above, dPᵀ = V dOᵢᵀ,
+//                             dSᵀ = Pᵀ ∘ (dPᵀ − Δᵢ), dK += dSᵀ Qᵢ
+//                 (five products a step instead of four: Sᵀ is computed twice);
+//   dQ phase      per unit (128-row query block, query head), Q and dO
+//                 resident, key steps of 64 keys:
+//                   S = Qᵢ Kⱼᵀ, dP = dOᵢ Vⱼᵀ, dS = P ∘ (dP − Δ), dQ += dS Kⱼ.
+// Operands are single-buffered and the steps run one after another.  dK, dV
+// and dQ are each summed inside one CTA: no atomics, bitwise reproducible.
+// The pre kernel (Δ, base-2 lse), the unit orders and the tile stores are the
+// smaller head dims' (fa_bwd_kernel.cuh).
+//
+// Warps: 0-3 softmax (thread = TMEM lane: a key in the dK/dV phase, a query
+// in the dQ phase), 4-7 epilogue, 8 TMA producer, 9 MMA issuer.  Every wait is
+// bounded as in the forward kernel.
+#pragma once
+
+#include "fa_bwd_kernel.cuh"
+
+namespace fa {
+
+constexpr int WIDE_THREADS = 10 * 32;
+
+struct WideTraits {
+    static constexpr int D = 256;
+    static constexpr int SW = 128;                 // bytes per swizzled row chunk
+    static constexpr int SWE = 64;                 // elements per row chunk
+    static constexpr int NCHUNK = D / SWE;         // 4
+    static constexpr uint32_t SWIZZLE_CODE = 2u;   // 128-byte swizzle
+    static constexpr int STEP = 64;                // query rows (dK/dV) or keys (dQ) per step
+    static constexpr int TILE128 = 128 * D * 2;    // 64 KB: a resident 128-row tile
+    static constexpr int TILE64 = STEP * D * 2;    // 32 KB: a step's 64-row tile
+    // ---- dK / dV phase ----
+    static constexpr int KV_OFF_K = 0;
+    static constexpr int KV_OFF_V = KV_OFF_K + TILE128;
+    static constexpr int KV_OFF_Q = KV_OFF_V + TILE128;
+    static constexpr int KV_OFF_DO = KV_OFF_Q + TILE64;
+    static constexpr int KV_OFF_LSE = KV_OFF_DO + TILE64;     // 64 floats
+    static constexpr int KV_OFF_DELTA = KV_OFF_LSE + 256;     // 64 floats
+    static constexpr int KV_OFF_OST = (KV_OFF_DELTA + 256 + 1023) / 1024 * 1024;  // epilogue staging
+    static constexpr int KV_OFF_BAR = KV_OFF_OST + 128 * SW;
+    static constexpr int KB_KV_FULL = 0;      // K, V of a unit landed (TMA)
+    static constexpr int KB_KV_EMPTY = 1;     // the unit's products are done (commit)
+    static constexpr int KB_QD_FULL = 2;      // Q, dO, lse2, Δ of a step landed
+    static constexpr int KB_QD_EMPTY = 3;     // that step's products are done (commit)
+    static constexpr int KB_S_FULL = 4;       // Sᵀ (and dPᵀ in the dK pass) in TMEM (commit)
+    static constexpr int KB_P_FULL = 5;       // Pᵀ (dV pass) or dSᵀ (dK pass) written (128)
+    static constexpr int KB_ACC_FULL = 6;     // dV or dK of a unit complete (commit)
+    static constexpr int KB_ACC_FREE = 7;     // that accumulator read out (128)
+    static constexpr int KB_DRAIN = 8;
+    static constexpr int KV_NUM_BARS = 9;
+    static constexpr int KV_SMEM_USED = KV_OFF_BAR + KV_NUM_BARS * 8;
+    // ---- dQ phase ----
+    static constexpr int Q_OFF_Q = 0;
+    static constexpr int Q_OFF_DO = Q_OFF_Q + TILE128;
+    static constexpr int Q_OFF_K = Q_OFF_DO + TILE128;
+    static constexpr int Q_OFF_V = Q_OFF_K + TILE64;
+    static constexpr int Q_OFF_OST = Q_OFF_V + TILE64;
+    static constexpr int Q_OFF_BAR = Q_OFF_OST + 128 * SW;
+    static constexpr int QB_QD_FULL = 0;      // Q, dO of a unit landed
+    static constexpr int QB_QD_EMPTY = 1;     // the unit's products are done (commit)
+    static constexpr int QB_KV_FULL = 2;      // K, V of a step landed
+    static constexpr int QB_KV_EMPTY = 3;     // that step's products are done (commit)
+    static constexpr int QB_S_FULL = 4;       // S and dP in TMEM (commit)
+    static constexpr int QB_DS_FULL = 5;      // dS written (128)
+    static constexpr int QB_DQ_FULL = 6;      // dQ of a unit complete (commit)
+    static constexpr int QB_DQ_FREE = 7;      // dQ read out (128)
+    static constexpr int QB_DRAIN = 8;
+    static constexpr int Q_NUM_BARS = 9;
+    static constexpr int Q_SMEM_USED = Q_OFF_BAR + Q_NUM_BARS * 8;
+    static constexpr int OFF_MISC = ((KV_SMEM_USED > Q_SMEM_USED ? KV_SMEM_USED : Q_SMEM_USED) + 15) & ~15;
+    static constexpr int SMEM_USED = OFF_MISC + 16;
+    static constexpr int SMEM_BYTES = SMEM_USED + 1024;
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+    // tensor memory: two 64-column fp32 blocks (S / Sᵀ, dP / dPᵀ; P, dS packed
+    // over their first 32 columns) and one 256-column accumulator
+    static constexpr uint32_t TM_S = 0;
+    static constexpr uint32_t TM_DP = 64;
+    static constexpr uint32_t TM_ACC = 256;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static_assert(TM_ACC + D <= TMEM_COLS, "tensor memory budget");
+
+    static __device__ __forceinline__ uint32_t kv_bar_count(int i) {
+        return (i == KB_P_FULL || i == KB_ACC_FREE) ? 128 : 1;
+    }
+    static __device__ __forceinline__ uint32_t q_bar_count(int i) {
+        return (i == QB_DS_FULL || i == QB_DQ_FREE) ? 128 : 1;
+    }
+};
+
+// K-major operand of `rows` rows in 64-element (128-byte) swizzled chunks:
+// descriptor start offset (16-byte units) of the 16-element K step kk
+__device__ __forceinline__ uint32_t wide_kmaj(int kk, int rows) {
+    return (uint32_t)(((kk / 4) * (rows * 128) + (kk % 4) * 32) >> 4);
+}
+
+// A 64-row step tile (rows r0 .. r0 + 63 of the 256-wide tensor) into shared
+// memory: four 64-element column chunks of one 64-row box each.
+__device__ __forceinline__ void wide_load64(uint32_t dst, const CUtensorMap* map, uint32_t bar, int r0, int h, int z,
+                                            uint64_t pol) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) ptx::tma_load_4d(dst + c * (64 * 128), map, bar, c * 64, r0, h, z, pol);
+}
+// A resident 128-row tile: four column chunks of two 64-row boxes each.
+__device__ __forceinline__ void wide_load128(uint32_t dst, const CUtensorMap* map, uint32_t bar, int r0, int h, int z,
+                                             uint64_t pol) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        ptx::tma_load_4d(dst + c * (128 * 128), map, bar, c * 64, r0, h, z, pol);
+        ptx::tma_load_4d(dst + c * (128 * 128) + 64 * 128, map, bar, c * 64, r0 + 64, h, z, pol);
+    }
+}
+
+// ================================================================ dK / dV ===
+// A unit's steps: per query head of the group, the 64-row halves of the
+// query blocks from i0 on (causal: block j's keys are seen from block j on).
+__device__ __forceinline__ void wide_step(const BwdUnit& w, int s, const BwdParams& p, int& hq, int& r0) {
+    const int per_head = 2 * w.per_head;
+    hq = w.hk * p.group + s / per_head;
+    r0 = (w.i0 + (s % per_head) / 2) * 128 + (s % 2) * 64;
+}
+
+template <bool CAUSAL>
+__device__ void wide_kv_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const CUtensorMap* tmQ,
+                                 const CUtensorMap* tmDO, const BwdParams& p, uint32_t sbase, uint32_t bar0,
+                                 const Ctl& ctl) {
+    using T = WideTraits;
+    auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+    const uint64_t pol_kv = ptx::policy_evict_first();
+    const uint64_t pol_q = ptx::policy_evict_last();
+    uint32_t uc = 0, t = 0;
+    bool ok = true;
+    for (int pos = blockIdx.x; ok && unit_at<CAUSAL>(pos) < p.nunits; pos += gridDim.x) {
+        const BwdUnit w = bwd_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        if (w.nsteps == 0) continue;
+        if (uc > 0 && !wait_phase(bar(T::KB_KV_EMPTY), (uc - 1) & 1u, ctl, SITE_B_KV_EMPTY)) { ok = false; break; }
+        ptx::mbar_arrive_expect_tx(bar(T::KB_KV_FULL), 2 * T::TILE128);
+        wide_load128(sbase + T::KV_OFF_K, tmK, bar(T::KB_KV_FULL), w.j * 128, w.hk, w.z, pol_kv);
+        wide_load128(sbase + T::KV_OFF_V, tmV, bar(T::KB_KV_FULL), w.j * 128, w.hk, w.z, pol_kv);
+        ++uc;
+        // the dV pass, then the dK pass: every step's Q, dO, lse2, Δ twice
+        const int steps = 2 * w.nsteps;
+        for (int pass = 0; ok && pass < 2; ++pass) {
+            for (int s = 0; s < steps; ++s, ++t) {
+                if (t >= 1 && !wait_phase(bar(T::KB_QD_EMPTY), (t - 1) & 1u, ctl, SITE_B_QD_EMPTY)) {
+                    ok = false;
+                    break;
+                }
+                int hq, r0;
+                wide_step(w, s, p, hq, r0);
+                const uint32_t full = bar(T::KB_QD_FULL);
+                ptx::mbar_arrive_expect_tx(full, 2 * T::TILE64 + 512);
+                wide_load64(sbase + T::KV_OFF_Q, tmQ, full, r0, hq, w.z, pol_q);
+                wide_load64(sbase + T::KV_OFF_DO, tmDO, full, r0, hq, w.z, pol_q);
+                const int64_t row0 = ((int64_t)w.z * p.Hq + hq) * p.Tq * 128 + r0;
+                ptx::bulk_load(sbase + T::KV_OFF_LSE, p.lse2 + row0, 256, full);
+                ptx::bulk_load(sbase + T::KV_OFF_DELTA, p.delta + row0, 256, full);
+            }
+        }
+    }
+    if (!ok) {
+        if (uc > 0) drain_phase(bar(T::KB_KV_FULL), (uc - 1) & 1u, ctl.limit_ns);
+        if (t > 0) drain_phase(bar(T::KB_QD_FULL), (t - 1) & 1u, ctl.limit_ns);
+    }
+}
+
+template <bool CAUSAL, bool BF16>
+__device__ void wide_kv_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0, uint32_t tmem, const Ctl& ctl) {
+    using T = WideTraits;
+    auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+    constexpr uint32_t ID_S = ptx::idesc_f16(128, 64, BF16, false, false);   // Sᵀ = K Qᵀ, dPᵀ = V dOᵀ (N = 64)
+    constexpr uint32_t ID_ACC = ptx::idesc_f16(128, 256, BF16, false, true); // dV, dK: B MN-major (N = 256)
+    constexpr uint32_t HI = ptx::smem_desc_hi(8 * T::SW, T::SWIZZLE_CODE);
+    const uint32_t k_lo = ptx::smem_desc_lo(sbase + T::KV_OFF_K, 16);
+    const uint32_t v_lo = ptx::smem_desc_lo(sbase + T::KV_OFF_V, 16);
+    const uint32_t q_lo = ptx::smem_desc_lo(sbase + T::KV_OFF_Q, 16);
+    const uint32_t do_lo = ptx::smem_desc_lo(sbase + T::KV_OFF_DO, 16);
+    const uint32_t qmn_lo = ptx::smem_desc_lo(sbase + T::KV_OFF_Q, 64 * T::SW);    // LBO: next 64-column chunk
+    const uint32_t domn_lo = ptx::smem_desc_lo(sbase + T::KV_OFF_DO, 64 * T::SW);
+    uint32_t uc = 0, t = 0, acc = 0;
+    bool ok = true;
+    for (int pos = blockIdx.x; ok && unit_at<CAUSAL>(pos) < p.nunits; pos += gridDim.x) {
+        const BwdUnit w = bwd_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        if (w.nsteps == 0) continue;
+        if (!wait_phase(bar(T::KB_KV_FULL), uc & 1u, ctl, SITE_B_KV_FULL)) { ok = false; break; }
+        const int steps = 2 * w.nsteps;
+        for (int pass = 0; ok && pass < 2; ++pass) {
+            for (int s = 0; s < steps; ++s, ++t) {
+                if (!wait_phase(bar(T::KB_QD_FULL), t & 1u, ctl, SITE_B_QD_FULL)) { ok = false; break; }
+                ptx::tc_fence_after();
+                // Sᵀ = K Qᵢᵀ (and dPᵀ = V dOᵢᵀ in the dK pass), K = 256 in 16 steps
+#pragma unroll
+                for (int kk = 0; kk < 16; ++kk)
+                    ptx::mma_ss(tmem + T::TM_S, ptx::desc64(k_lo + wide_kmaj(kk, 128), HI),
+                                ptx::desc64(q_lo + wide_kmaj(kk, 64), HI), ID_S, kk > 0 ? 1u : 0u);
+                if (pass == 1) {
+#pragma unroll
+                    for (int kk = 0; kk < 16; ++kk)
+                        ptx::mma_ss(tmem + T::TM_DP, ptx::desc64(v_lo + wide_kmaj(kk, 128), HI),
+                                    ptx::desc64(do_lo + wide_kmaj(kk, 64), HI), ID_S, kk > 0 ? 1u : 0u);
+                }
+                ptx::tc_commit(bar(T::KB_S_FULL));
+                if (!wait_phase(bar(T::KB_P_FULL), t & 1u, ctl, SITE_B_P_FULL)) { ok = false; break; }
+                // the accumulator of this pass: free once the epilogue has read the previous one
+                if (s == 0 && acc > 0 && !wait_phase(bar(T::KB_ACC_FREE), (acc - 1) & 1u, ctl, SITE_B_ACC_FREE)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                // dV += Pᵀ dOᵢ (pass 0) or dK += dSᵀ Qᵢ (pass 1): 64 queries in 4 K steps
+                const uint32_t a_tmem = tmem + (pass == 0 ? T::TM_S : T::TM_DP);
+                const uint32_t b_lo = pass == 0 ? domn_lo : qmn_lo;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    ptx::mma_ts(tmem + T::TM_ACC, a_tmem + kk * 8, ptx::desc64(b_lo + ((kk * 16 * T::SW) >> 4), HI),
+                                ID_ACC, (s > 0 || kk > 0) ? 1u : 0u);
+                ptx::tc_commit(bar(T::KB_QD_EMPTY));  // the step's Q, dO and TMEM blocks free
+            }
+            if (!ok) break;
+            ptx::tc_commit(bar(T::KB_ACC_FULL));  // dV (pass 0) or dK (pass 1) of the unit complete
+            ++acc;
+        }
+        if (!ok) break;
+        ptx::tc_commit(bar(T::KB_KV_EMPTY));
+        ++uc;
+    }
+    // every MMA of this phase completes before the dQ phase reuses shared memory
+    ptx::tc_commit(bar(T::KB_DRAIN));
+    drain_phase(bar(T::KB_DRAIN), 0u, ctl.limit_ns);
+}
+
+// Thread = key (TMEM lane).  dV pass: Pᵀ over the first 32 columns of Sᵀ;
+// dK pass: Pᵀ in registers, dSᵀ = Pᵀ ∘ (dPᵀ − Δ) over the first 32 columns
+// of dPᵀ.  P and dS are rounded to the input type (the products' operands).
+template <bool CAUSAL, bool BF16>
+__device__ void wide_kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar0, uint32_t tmem, const Ctl& ctl) {
+    using T = WideTraits;
+    auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+    const int quad = (threadIdx.x / 32) % 4;
+    const int row = quad * 32 + threadIdx.x % 32;  // key within the block
+    const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
+    const float c = p.scale_log2;
+    const uint32_t lse_a = sbase + T::KV_OFF_LSE, del_a = sbase + T::KV_OFF_DELTA;
+    uint32_t t = 0;
+    for (int pos = blockIdx.x; unit_at<CAUSAL>(pos) < p.nunits; pos += gridDim.x) {
+        const BwdUnit w = bwd_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        const int key = w.j * 128 + row;
+        const int steps = 2 * w.nsteps;
+        for (int pass = 0; pass < 2; ++pass) {
+            for (int s = 0; s < steps; ++s, ++t) {
+                int hq, r0;
+                wide_step(w, s, p, hq, r0);
+                // lse2 and Δ of the step's queries arrive with Qᵢ (TMA); the
+                // slot is refilled only after this step's P_FULL
+                if (!warp_wait_phase(bar(T::KB_QD_FULL), t & 1u, ctl, SITE_B_QD_FULL)) return;
+                if (!warp_wait_phase(bar(T::KB_S_FULL), t & 1u, ctl, SITE_B_S_FULL)) return;
+                ptx::tc_fence_after();
+                // causal: only the diagonal block has keys after queries (key > query -> P = 0)
+                const bool diag = CAUSAL && r0 / 128 == w.j;
+                float pf[64];
+                {
+                    uint32_t a[32], b[32];
+                    ptx::tmem_ld32_issue(tmem + lane_addr + T::TM_S, a);
+                    ptx::tmem_ld32_issue(tmem + lane_addr + T::TM_S + 32, b);
+                    ptx::tmem_wait_ld();
+                    ptx::reg_fence32(a);
+                    ptx::reg_fence32(b);
+#pragma unroll
+                    for (int x = 0; x < 64; x += 2) {
+                        float l0, l1;
+                        asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(l0), "=f"(l1) : "r"(lse_a + 4u * x));
+                        const uint32_t u0 = x < 32 ? a[x] : b[x - 32], u1 = x < 32 ? a[x + 1] : b[x - 31];
+                        float e0 = fmaf(__uint_as_float(u0), c, -l0);
+                        float e1 = fmaf(__uint_as_float(u1), c, -l1);
+                        if (diag && key > r0 + x) e0 = -INFINITY;
+                        if (diag && key > r0 + x + 1) e1 = -INFINITY;
+                        pf[x] = ptx::ex2(e0);
+                        pf[x + 1] = ptx::ex2(e1);
+                    }
+                }
+                uint32_t pk[32];
+#pragma unroll
+                for (int x = 0; x < 32; ++x) pk[x] = pack2<BF16>(pf[2 * x], pf[2 * x + 1]);
+                if (pass == 0) {
+                    ptx::tmem_st32(tmem + lane_addr + T::TM_S, pk);
+                } else {
+                    uint32_t a[32], b[32];
+                    ptx::tmem_ld32_issue(tmem + lane_addr + T::TM_DP, a);
+                    ptx::tmem_ld32_issue(tmem + lane_addr + T::TM_DP + 32, b);
+                    ptx::tmem_wait_ld();
+                    ptx::reg_fence32(a);
+                    ptx::reg_fence32(b);
+                    uint32_t ds[32];
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) {
+                        float d0, d1;
+                        asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(d0), "=f"(d1) : "r"(del_a + 8u * x));
+                        const float2 pp = unpack2<BF16>(pk[x]);  // dS uses the rounded P
+                        const uint32_t u0 = 2 * x < 32 ? a[2 * x] : b[2 * x - 32];
+                        const uint32_t u1 = 2 * x < 32 ? a[2 * x + 1] : b[2 * x - 31];
+                        ds[x] = pack2<BF16>(pp.x * (__uint_as_float(u0) - d0), pp.y * (__uint_as_float(u1) - d1));
+                    }
+                    ptx::tmem_st32(tmem + lane_addr + T::TM_DP, ds);
+                }
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(bar(T::KB_P_FULL));
+            }
+        }
+    }
+}
+
+// Thread = key: dV, then dK (times scale), read out, released, stored; a
+// unit no query sees gets zeros.
+template <bool CAUSAL, bool BF16>
+__device__ void wide_kv_epilogue(const CUtensorMap* tmDK, const CUtensorMap* tmDV, const BwdParams& p, uint32_t sbase,
+                                 uint32_t bar0, uint32_t tmem, const Ctl& ctl) {
+    using T = WideTraits;
+    auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+    const int quad = (threadIdx.x / 32) % 4;
+    const int row = quad * 32 + threadIdx.x % 32;
+    const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
+    const uint32_t stage = sbase + T::KV_OFF_OST + (uint32_t)quad * 32u * T::SW;
+    auto drain = [&]() {
+        if (threadIdx.x % 32 == 0) ptx::bulk_wait_all();
+    };
+    uint32_t acc = 0;
+    for (int pos = blockIdx.x; unit_at<CAUSAL>(pos) < p.nunits; pos += gridDim.x) {
+        const BwdUnit w = bwd_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        const int key = w.j * 128 + row;
+        if (w.nsteps == 0) {
+            if (key < p.Nkv) {
+                uint8_t* dk_row = reinterpret_cast<uint8_t*>(p.dk) +
+                                  2 * ((int64_t)w.z * p.sdk_z + (int64_t)w.hk * p.sdk_h + (int64_t)key * p.sdk_n);
+                uint8_t* dv_row = reinterpret_cast<uint8_t*>(p.dv) +
+                                  2 * ((int64_t)w.z * p.sdv_z + (int64_t)w.hk * p.sdv_h + (int64_t)key * p.sdv_n);
+#pragma unroll
+                for (int x = 0; x < 256 / 8; ++x) {
+                    reinterpret_cast<uint4*>(dk_row)[x] = make_uint4(0, 0, 0, 0);
+                    reinterpret_cast<uint4*>(dv_row)[x] = make_uint4(0, 0, 0, 0);
+                }
+            }
+            continue;
+        }
+        const int key0 = w.j * 128 + 32 * quad;
+        for (int pass = 0; pass < 2; ++pass, ++acc) {
+            if (!warp_wait_phase(bar(T::KB_ACC_FULL), acc & 1u, ctl, SITE_B_ACC_FULL)) {
+                drain();
+                return;
+            }
+            ptx::tc_fence_after();
+            tma_store_rows<256, T::SW, BF16>(tmem + lane_addr + T::TM_ACC, pass == 0 ? 1.f : p.scale, stage,
+                                             pass == 0 ? tmDV : tmDK, key0, w.hk, w.z, key0 < p.Nkv, [&]() {
+                                                 ptx::tc_fence_before();
+                                                 ptx::mbar_arrive(bar(T::KB_ACC_FREE));
+                                             });
+        }
+    }
+    drain();
+}
+
+// ===================================================================== dQ ===
+template <bool CAUSAL>
+__device__ void wide_q_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const CUtensorMap* tmQ,
+                                const CUtensorMap* tmDO, const BwdParams& p, uint32_t sbase, uint32_t bar0,
+                                const Ctl& ctl, int first) {
+    using T = WideTraits;
+    auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+    const uint64_t pol_q = ptx::policy_evict_first();
+    const uint64_t pol_kv = ptx::policy_evict_last();
+    uint32_t uc = 0, g = 0;
+    bool ok = true;
+    for (int pos = first; ok && unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x) {
+        const DqUnit w = dq_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        if (uc > 0 && !wait_phase(bar(T::QB_QD_EMPTY), (uc - 1) & 1u, ctl, SITE_B_QD_EMPTY)) { ok = false; break; }
+        ptx::mbar_arrive_expect_tx(bar(T::QB_QD_FULL), 2 * T::TILE128);
+        wide_load128(sbase + T::Q_OFF_Q, tmQ, bar(T::QB_QD_FULL), w.i * 128, w.hq, w.z, pol_q);
+        wide_load128(sbase + T::Q_OFF_DO, tmDO, bar(T::QB_QD_FULL), w.i * 128, w.hq, w.z, pol_q);
+        ++uc;
+        const int steps = 2 * w.nkv;  // 64-key steps
+        for (int s = 0; s < steps; ++s, ++g) {
+            if (g >= 1 && !wait_phase(bar(T::QB_KV_EMPTY), (g - 1) & 1u, ctl, SITE_B_KV_EMPTY)) { ok = false; break; }
+            const uint32_t full = bar(T::QB_KV_FULL);
+            ptx::mbar_arrive_expect_tx(full, 2 * T::TILE64);
+            wide_load64(sbase + T::Q_OFF_K, tmK, full, s * 64, w.hk, w.z, pol_kv);
+            wide_load64(sbase + T::Q_OFF_V, tmV, full, s * 64, w.hk, w.z, pol_kv);
+        }
+    }
+    if (!ok) {
+        if (uc > 0) drain_phase(bar(T::QB_QD_FULL), (uc - 1) & 1u, ctl.limit_ns);
+        if (g > 0) drain_phase(bar(T::QB_KV_FULL), (g - 1) & 1u, ctl.limit_ns);
+    }
+}
+
+template <bool CAUSAL, bool BF16>
+__device__ void wide_q_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0, uint32_t tmem, const Ctl& ctl,
+                              int first) {
+    using T = WideTraits;
+    auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+    constexpr uint32_t ID_S = ptx::idesc_f16(128, 64, BF16, false, false);    // S = Q Kᵀ, dP = dO Vᵀ (N = 64)
+    constexpr uint32_t ID_DQ = ptx::idesc_f16(128, 256, BF16, false, true);   // dQ += dS K (K MN-major)
+    constexpr uint32_t HI = ptx::smem_desc_hi(8 * T::SW, T::SWIZZLE_CODE);
+    const uint32_t q_lo = ptx::smem_desc_lo(sbase + T::Q_OFF_Q, 16);
+    const uint32_t do_lo = ptx::smem_desc_lo(sbase + T::Q_OFF_DO, 16);
+    const uint32_t k_lo = ptx::smem_desc_lo(sbase + T::Q_OFF_K, 16);
+    const uint32_t v_lo = ptx::smem_desc_lo(sbase + T::Q_OFF_V, 16);
+    const uint32_t kmn_lo = ptx::smem_desc_lo(sbase + T::Q_OFF_K, 64 * T::SW);
+    uint32_t uc = 0, g = 0;
+    bool ok = true;
+    for (int pos = first; ok && unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x) {
+        const DqUnit w = dq_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        if (!wait_phase(bar(T::QB_QD_FULL), uc & 1u, ctl, SITE_B_QD_FULL)) { ok = false; break; }
+        const int steps = 2 * w.nkv;
+        for (int s = 0; s < steps; ++s, ++g) {
+            if (!wait_phase(bar(T::QB_KV_FULL), g & 1u, ctl, SITE_B_KV_FULL)) { ok = false; break; }
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk)
+                ptx::mma_ss(tmem + T::TM_S, ptx::desc64(q_lo + wide_kmaj(kk, 128), HI),
+                            ptx::desc64(k_lo + wide_kmaj(kk, 64), HI), ID_S, kk > 0 ? 1u : 0u);
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk)
+                ptx::mma_ss(tmem + T::TM_DP, ptx::desc64(do_lo + wide_kmaj(kk, 128), HI),
+                            ptx::desc64(v_lo + wide_kmaj(kk, 64), HI), ID_S, kk > 0 ? 1u : 0u);
+            ptx::tc_commit(bar(T::QB_S_FULL));
+            if (!wait_phase(bar(T::QB_DS_FULL), g & 1u, ctl, SITE_B_DS_FULL)) { ok = false; break; }
+            if (s == 0 && uc > 0 && !wait_phase(bar(T::QB_DQ_FREE), (uc - 1) & 1u, ctl, SITE_B_DQ_FREE)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                ptx::mma_ts(tmem + T::TM_ACC, tmem + T::TM_S + kk * 8, ptx::desc64(kmn_lo + ((kk * 16 * T::SW) >> 4), HI),
+                            ID_DQ, (s > 0 || kk > 0) ? 1u : 0u);
+            ptx::tc_commit(bar(T::QB_KV_EMPTY));  // K, V of the step and the TMEM blocks free
+        }
+        if (!ok) break;
+        ptx::tc_commit(bar(T::QB_DQ_FULL));
+        ptx::tc_commit(bar(T::QB_QD_EMPTY));
+        ++uc;
+    }
+    if (!ok) {
+        ptx::tc_commit(bar(T::QB_DRAIN));
+        drain_phase(bar(T::QB_DRAIN), 0u, ctl.limit_ns);
+    }
+}
+
+// Thread = query (TMEM lane): P = 2^(S·c − lse2), dS = P ∘ (dP − Δ) over the
+// first 32 columns of S.
+template <bool CAUSAL, bool BF16>
+__device__ void wide_q_softmax(const BwdParams& p, uint32_t bar0, uint32_t tmem, const Ctl& ctl, int first) {
+    using T = WideTraits;
+    auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+    const int quad = (threadIdx.x / 32) % 4;
+    const int row = quad * 32 + threadIdx.x % 32;
+    const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
+    const float c = p.scale_log2;
+    uint32_t g = 0;
+    for (int pos = first; unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x) {
+        const DqUnit w = dq_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        const int64_t r = ((int64_t)w.z * p.Hq + w.hq) * p.Tq * 128 + (int64_t)w.i * 128 + row;
+        const float l2 = __ldg(p.lse2 + r), dl = __ldg(p.delta + r);
+        const int q = w.i * 128 + row;
+        const int steps = 2 * w.nkv;
+        for (int s = 0; s < steps; ++s, ++g) {
+            if (!warp_wait_phase(bar(T::QB_S_FULL), g & 1u, ctl, SITE_B_S_FULL)) return;
+            ptx::tc_fence_after();
+            const bool diag = CAUSAL && s / 2 == w.i;  // keys after the query only on the diagonal block
+            const int k0 = s * 64;
+            uint32_t sa[32], sb[32], da[32], db[32];
+            ptx::tmem_ld32_issue(tmem + lane_addr + T::TM_S, sa);
+            ptx::tmem_ld32_issue(tmem + lane_addr + T::TM_S + 32, sb);
+            ptx::tmem_ld32_issue(tmem + lane_addr + T::TM_DP, da);
+            ptx::tmem_ld32_issue(tmem + lane_addr + T::TM_DP + 32, db);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence32(sa);
+            ptx::reg_fence32(sb);
+            ptx::reg_fence32(da);
+            ptx::reg_fence32(db);
+            uint32_t ds[32];
+#pragma unroll
+            for (int x = 0; x < 32; ++x) {
+                const int k = 2 * x;
+                const uint32_t s0 = k < 32 ? sa[k] : sb[k - 32], s1 = k < 32 ? sa[k + 1] : sb[k - 31];
+                const uint32_t d0 = k < 32 ? da[k] : db[k - 32], d1 = k < 32 ? da[k + 1] : db[k - 31];
+                float e0 = fmaf(__uint_as_float(s0), c, -l2);
+                float e1 = fmaf(__uint_as_float(s1), c, -l2);
+                if (diag && k0 + k > q) e0 = -INFINITY;
+                if (diag && k0 + k + 1 > q) e1 = -INFINITY;
+                const float2 pp = unpack2<BF16>(pack2<BF16>(ptx::ex2(e0), ptx::ex2(e1)));  // P rounded as in dV
+                ds[x] = pack2<BF16>(pp.x * (__uint_as_float(d0) - dl), pp.y * (__uint_as_float(d1) - dl));
+            }
+            ptx::tmem_st32(tmem + lane_addr + T::TM_S, ds);
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(T::QB_DS_FULL));
+        }
+    }
+}
+
+// Thread = query: dQ (times scale) read out, released, stored.
+template <bool CAUSAL, bool BF16>
+__device__ void wide_q_epilogue(const CUtensorMap* tmDQ, const BwdParams& p, uint32_t sbase, uint32_t bar0,
+                                uint32_t tmem, const Ctl& ctl, int first) {
+    using T = WideTraits;
+    auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+    const int quad = (threadIdx.x / 32) % 4;
+    const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
+    const uint32_t stage = sbase + T::Q_OFF_OST + (uint32_t)quad * 32u * T::SW;
+    auto drain = [&]() {
+        if (threadIdx.x % 32 == 0) ptx::bulk_wait_all();
+    };
+    uint32_t uc = 0;
+    for (int pos = first; unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x, ++uc) {
+        const DqUnit w = dq_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        if (!warp_wait_phase(bar(T::QB_DQ_FULL), uc & 1u, ctl, SITE_B_DQ_FULL)) {
+            drain();
+            return;
+        }
+        ptx::tc_fence_after();
+        const int q0 = w.i * 128 + 32 * quad;
+        tma_store_rows<256, T::SW, BF16>(tmem + lane_addr + T::TM_ACC, p.scale, stage, tmDQ, q0, w.hq, w.z, q0 < p.Nq,
+                                         [&]() {
+                                             ptx::tc_fence_before();
+                                             ptx::mbar_arrive(bar(T::QB_DQ_FREE));
+                                         });
+    }
+    drain();
+}
+
+// ================================================================ fused ======
+// dK/dV units (positions c, c + grid, ...) then dQ units from position
+// grid - 1 - c on, in the same shared memory and TMEM, as for the smaller
+// head dims.
+template <bool CAUSAL, bool BF16>
+__global__ void __launch_bounds__(WIDE_THREADS, 1)
+    fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                       const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
+                       const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV,
+                       const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
+    using T = WideTraits;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = nullptr;
+    if (!bwd_smem_base(smem_raw, T::SMEM_USED, T::SMEM_BYTES, p, smem)) return;
+    const uint32_t sbase = ptx::smem_addr(smem);
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + T::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + T::OFF_MISC + 4);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+    const uint32_t kbar0 = sbase + T::KV_OFF_BAR;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < T::KV_NUM_BARS; ++i) ptx::mbar_init(kbar0 + 8u * i, T::kv_bar_count(i));
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+        ptx::prefetch_tmap(&tmK);
+        ptx::prefetch_tmap(&tmV);
+        ptx::prefetch_tmap(&tmQ);
+        ptx::prefetch_tmap(&tmDO);
+        ptx::prefetch_tmap(&tmDK);
+        ptx::prefetch_tmap(&tmDV);
+        ptx::prefetch_tmap(&tmDQ);
+    }
+    if (warp == 9) {
+        ptx::tmem_alloc(ptx::smem_addr(const_cast<uint32_t*>(tmem_slot)), T::TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const Ctl ctl{abort_flag, p.status, p.wait_limit_ns};
+    ptx::grid_dependency_wait();
+    ptx::grid_launch_dependents();
+    if (warp < 4) {
+        wide_kv_softmax<CAUSAL, BF16>(p, sbase, kbar0, tmem, ctl);
+    } else if (warp < 8) {
+        wide_kv_epilogue<CAUSAL, BF16>(&tmDK, &tmDV, p, sbase, kbar0, tmem, ctl);
+    } else if (warp == 8) {
+        if (lane == 0) wide_kv_producer<CAUSAL>(&tmK, &tmV, &tmQ, &tmDO, p, sbase, kbar0, ctl);
+    } else {
+        if (lane == 0) wide_kv_issuer<CAUSAL, BF16>(p, sbase, kbar0, tmem, ctl);
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+
+    if (*abort_flag == 0) {
+        const uint32_t qbar0 = sbase + T::Q_OFF_BAR;
+        if (threadIdx.x == 0) {
+            for (int i = 0; i < T::Q_NUM_BARS; ++i) ptx::mbar_init(qbar0 + 8u * i, T::q_bar_count(i));
+            ptx::fence_mbar_init();
+        }
+        __syncthreads();
+        ptx::tc_fence_after();
+        const int first = (int)gridDim.x - 1 - (int)blockIdx.x;
+        if (warp < 4) {
+            wide_q_softmax<CAUSAL, BF16>(p, qbar0, tmem, ctl, first);
+        } else if (warp < 8) {
+            wide_q_epilogue<CAUSAL, BF16>(&tmDQ, p, sbase, qbar0, tmem, ctl, first);
+        } else if (warp == 8) {
+            if (lane == 0) wide_q_producer<CAUSAL>(&tmK, &tmV, &tmQ, &tmDO, p, sbase, qbar0, ctl, first);
+        } else {
+            if (lane == 0) wide_q_issuer<CAUSAL, BF16>(p, sbase, qbar0, tmem, ctl, first);
+        }
+        ptx::tc_fence_before();
+        __syncthreads();
+    }
+    if (warp == 9) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, T::TMEM_COLS);
+    }
+}
+
+}  // namespace fa

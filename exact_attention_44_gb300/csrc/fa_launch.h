@@ -91,6 +91,7 @@ cudaError_t launch_bwd_d16(const BwdLaunchArgs& a, bool causal, bool bf16);
 cudaError_t launch_bwd_d32(const BwdLaunchArgs& a, bool causal, bool bf16);
 cudaError_t launch_bwd_d64(const BwdLaunchArgs& a, bool causal, bool bf16);
 cudaError_t launch_bwd_d128(const BwdLaunchArgs& a, bool causal, bool bf16);
+cudaError_t launch_bwd_d256(const BwdLaunchArgs& a, bool causal, bool bf16);
 
 // Host-side shape facts of each specialisation.
 int block_n_for(int D);      // keys per block

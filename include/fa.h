@@ -301,13 +301,14 @@ fa_status fa_lse_merge(int nparts, const void* const* o_parts, const float* cons
  *                and lse); no initialisation needed, overwritten; not shared
  *                by calls that may overlap
  *
- * Requirements: those of fa_fwd, with D in {16, 32, 64, 128} (D = 256 returns
- * FA_ERR_UNSUPPORTED: dK and dV of a 128-key block live in tensor memory)
- * and Nq >= 1 whenever Z*Hkv*Nkv > 0.  Two kernels on `stream`: Delta and
- * lse per row; then one persistent kernel whose CTAs first compute dK and dV
- * (a unit per key block and kv head, over every query of the group), then
- * dQ (a unit per query block and head, over its keys, recomputing the
- * scores).  No atomics: results are bitwise reproducible.
+ * Requirements: those of fa_fwd (D in {16, 32, 64, 128, 256}) and Nq >= 1
+ * whenever Z*Hkv*Nkv > 0.  Two kernels on `stream`: Delta and lse per row;
+ * then one persistent kernel whose CTAs first compute dK and dV (a unit per
+ * key block and kv head, over every query of the group), then dQ (a unit per
+ * query block and head, over its keys, recomputing the scores).  At D = 256
+ * the dK/dV units take dV and dK in two passes over the queries (one
+ * 256-column accumulator in tensor memory at a time) and both phases step
+ * 64 rows at a time.  No atomics: results are bitwise reproducible.
  * Errors: those of fa_fwd, plus FA_ERR_WORKSPACE for a missing, misaligned
  * or small workspace.
  */
@@ -317,7 +318,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  const fa_strides* sdq, const fa_strides* sdk, const fa_strides* sdv, float scale, int causal,
                  fa_dtype dtype, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
-/* Bytes of workspace fa_bwd needs (host only; FA_ERR_UNSUPPORTED for D = 256). */
+/* Bytes of workspace fa_bwd needs (host only; FA_ERR_UNSUPPORTED for an unsupported D). */
 fa_status fa_bwd_workspace_size(int Z, int Hq, int Nq, int D, size_t* bytes);
 
 /* Human-readable name of a status code (static storage, never NULL). */

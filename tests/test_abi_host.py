@@ -374,3 +374,14 @@ def test_noalloc_array_covers_the_documented_sm_count(lib):
         fa.fa_fwd_splitkv_workspace_size_for(48, 152)
     with pytest.raises(fa.FaError):
         fa.fa_fwd_splitkv_workspace_size_for(128, 0)
+
+
+@pytest.mark.parametrize("D", [16, 32, 64, 128, 256])
+def test_bwd_workspace_every_head_dim(lib, D):
+    # lse2 and Delta per query row, padded to whole 128-row blocks and 256 bytes
+    Z, Hq, Nq = 2, 3, 300
+    rows = Z * Hq * -(-Nq // 128) * 128 * 4
+    assert fa.fa_bwd_workspace_size(Z, Hq, Nq, D) == 2 * (-(-rows // 256) * 256)
+    with pytest.raises(fa.FaError) as e:
+        fa.fa_bwd_workspace_size(Z, Hq, Nq, 96)
+    assert e.value.code == fa.FA_ERR_UNSUPPORTED

@@ -61,11 +61,44 @@ def check_bwd(seed, Z, Hq, Hkv, Nq, Nkv, D, dtype, causal, scale=None, layout="b
     return worst
 
 
-@pytest.mark.parametrize("D", [16, 32, 64, 128])
+@pytest.mark.parametrize("D", [16, 32, 64, 128, 256])
 @pytest.mark.parametrize("dtype", ["fp16", "bf16"])
 @pytest.mark.parametrize("causal", [False, True])
 def test_head_dims(D, dtype, causal):
     print(check_bwd(201, 1, 2, 2, 300, 300, D, dtype, causal))
+
+
+# D = 256 runs its own kernel (two passes for dV and dK, 64-row steps): the
+# ragged tails of both sequence lengths, a query block that ends inside a
+# step, GQA groups, and more units than CTAs so that CTAs take several units
+# of both phases.
+@pytest.mark.parametrize("Nq,Nkv", [(1, 1), (1, 200), (63, 65), (65, 63), (129, 129), (200, 77), (77, 200),
+                                    (256, 640), (640, 256)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_d256_ragged(Nq, Nkv, causal):
+    print(check_bwd(211, 2, 2, 1, Nq, Nkv, 256, "bf16", causal))
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 1), (8, 2)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_d256_gqa(Hq, Hkv, causal):
+    print(check_bwd(212, 1, Hq, Hkv, 330, 330, 256, "fp16", causal))
+
+
+def test_d256_layouts():
+    print(check_bwd(213, 2, 4, 2, 200, 300, 256, "bf16", True, layout="bsnd"))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_d256_many_units_per_cta(causal):
+    # 2 x 8 heads x 10 key blocks = 160 dK/dV units and 160 dQ units on
+    # at most 152 CTAs
+    print(check_bwd(214, 2, 8, 8, 1280, 1280, 256, "bf16", causal))
+
+
+@pytest.mark.parametrize("scale", [0.0, -1.0])
+def test_d256_zero_and_negative_scale(scale):
+    print(check_bwd(215, 1, 2, 1, 260, 300, 256, "bf16", True, scale=scale))
 
 
 @pytest.mark.parametrize("Nq,Nkv", [(1, 1), (1, 200), (129, 129), (200, 77), (77, 200), (256, 640), (640, 256)])
@@ -103,9 +136,9 @@ def test_workspace_and_argument_errors():
     with pytest.raises(fa.FaError) as e:
         fa.fa_bwd(q, q, q, q, lse, q, workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
     assert e.value.code == fa.FA_ERR_WORKSPACE
-    q256 = torch.zeros(1, 1, 64, 256, dtype=torch.float16, device="cuda")
+    q96 = torch.zeros(1, 1, 64, 96, dtype=torch.float16, device="cuda")
     with pytest.raises(fa.FaError) as e:
-        fa.fa_bwd(q256, q256, q256, q256, lse, q256, workspace=torch.empty(1 << 20, dtype=torch.uint8, device="cuda"))
+        fa.fa_bwd(q96, q96, q96, q96, lse, q96, workspace=torch.empty(1 << 20, dtype=torch.uint8, device="cuda"))
     assert e.value.code == fa.FA_ERR_UNSUPPORTED
 
 
