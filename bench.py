@@ -99,8 +99,8 @@ def load_peaks():
 
 
 # the sources the forward kernel of head dim D is compiled from
-FWD_SOURCES = ["fa_fwd_kernel.cuh", "fa_fwd_chain_kernel.cuh", "fa_ptx.cuh", "fa_params.h", "fa_launch.h",
-               "fa_fwd_dim.cu"]
+FWD_SOURCES = ["fa_fwd_kernel.cuh", "fa_fwd_chain_kernel.cuh", "fa_fwd_pair_kernel.cuh", "fa_ptx.cuh", "fa_params.h",
+               "fa_launch.h", "fa_fwd_dim.cu"]
 
 
 def kernel_source_hash() -> str:

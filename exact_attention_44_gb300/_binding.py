@@ -55,6 +55,7 @@ _SIGNATURES = {
     "fa_debug_inject_stall": (None, [ctypes.c_int]),
     "fa_debug_force_split": (None, [ctypes.c_int]),
     "fa_debug_force_chains": (None, [ctypes.c_int]),
+    "fa_debug_force_pair": (None, [ctypes.c_int]),
     "fa_debug_exp2": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]),
 }
 
@@ -81,7 +82,8 @@ class fa_fwd_options(ctypes.Structure):
 class fa_fwd_schedule_info(ctypes.Structure):
     _fields_ = [("grid", ctypes.c_int), ("split", ctypes.c_int), ("gqa_packed", ctypes.c_int),
                 ("head_group", ctypes.c_int), ("alternate", ctypes.c_int), ("tiles", ctypes.c_int64),
-                ("kv_blocks", ctypes.c_int64), ("busiest_blocks", ctypes.c_int64), ("softmax_chains", ctypes.c_int)]
+                ("kv_blocks", ctypes.c_int64), ("busiest_blocks", ctypes.c_int64), ("softmax_chains", ctypes.c_int),
+                ("cta_pairs", ctypes.c_int)]
 
 
 def library_path() -> str:
@@ -458,7 +460,7 @@ def fa_fwd_schedule(Z: int, Hq: int, Hkv: int, Nq: int, Nkv: int, D: int, causal
                     num_sms: int, l2_bytes: int) -> dict:
     """Host-only (no CUDA call): the schedule fa_fwd (or fa_fwd_splitkv) picks for contiguous BNSD
     tensors on a device with num_sms SMs and l2_bytes of L2 -- grid, split, gqa_packed, head_group,
-    alternate, tiles, kv_blocks, busiest_blocks (libfa's fa_fwd_schedule)."""
+    alternate, tiles, kv_blocks, busiest_blocks, softmax_chains, cta_pairs (libfa's fa_fwd_schedule)."""
     info = fa_fwd_schedule_info()
     rc = load().fa_fwd_schedule(Z, Hq, Hkv, Nq, Nkv, D, int(bool(causal)), int(bool(splitkv)), num_sms, l2_bytes,
                                 ctypes.byref(info))
@@ -493,6 +495,11 @@ def fa_debug_exp2(x, y=None, stream=None):
 def fa_debug_force_chains(mode: int) -> None:
     """Which kernel runs whole tiles of D <= 128: 0 by shape (default), 1 two softmax chains, 2 one."""
     load().fa_debug_force_chains(int(mode))
+
+
+def fa_debug_force_pair(mode: int) -> None:
+    """Whether whole tiles of D = 128 run on CTA pairs: 0 default (no), 1 wherever they apply, 2 never."""
+    load().fa_debug_force_pair(int(mode))
 
 
 def fa_debug_force_split(mode: int) -> None:

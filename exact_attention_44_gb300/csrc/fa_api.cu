@@ -112,6 +112,7 @@ std::atomic<uint64_t> g_wait_limit_ns{0};
 std::atomic<int> g_inject_stall{0};
 std::atomic<int> g_force_split{0};  // 0: decide by shape, 1: always cut key ranges, 2: never
 std::atomic<int> g_force_chains{0};  // 0: decide by shape, 1: two softmax chains wherever they apply, 2: never
+std::atomic<int> g_force_pair{0};    // 0: decide by shape, 1: CTA pairs wherever they apply, 2: never
 
 uint64_t wait_limit_ns() {
     uint64_t v = g_wait_limit_ns.load();
@@ -374,6 +375,70 @@ bool chain_kernel_applies(const fa::FwdParams& p, int D, bool causal, bool split
     return D <= 64 && head_blocks(p, causal, 128) >= 16 * (int64_t)p.Tq;
 }
 
+// Whole-tile launches at D = 128 can run the CTA-pair kernel
+// (fa_fwd_pair_kernel: a cluster of two CTAs takes two query tiles that see
+// the same key blocks and multiplies each key block once for both, M = 256,
+// each SM holding half of every K and V block), with the two softmax chains
+// of fa_fwd_chain_kernel on each SM.  It cuts the shared-memory traffic of a
+// key block per SM from ~160 KB to ~96 KB, which bounds the one-SM kernels
+// at D = 128; measured on GB300 the bound then moves to the two chains'
+// softmax (~1.36 us per chain and block), and the pair kernel runs level
+// with the one-SM kernel on long tiles (the 32K causal GQA workload 1495 vs
+// 1495 TFLOP/s, N = 8192 0.99x) and slower on short ones (Z8 H16 N2048
+// causal 0.78x).  So it runs only when fa_debug_force_pair asks for it.
+bool pair_kernel_applies(const fa::FwdParams& p, int D, bool causal, bool split) {
+    (void)p;
+    (void)causal;
+    if (split || D != 128) return false;
+    return g_force_pair.load() == 1;
+}
+
+// The pair kernel's units (fa::FwdParams::pair*): head pairs when the GQA
+// group is even (both heads see the same K/V and key blocks), else pairs of
+// adjacent query blocks of one head.
+void set_pair_units(fa::FwdParams& p, int D, bool causal, int l2_bytes, int clusters) {
+    p.pair = p.group % 2 == 0 ? 1 : 2;
+    p.pair_heads = p.pair == 1 ? p.Z * p.Hq / 2 : p.Z * p.Hq;
+    p.pair_tq = p.pair == 1 ? p.Tq : (p.Tq + 1) / 2;
+    p.pair_units = (int)((int64_t)p.pair_heads * p.pair_tq);
+    const int per_kv = p.pair == 1 ? p.group / 2 : p.group;  // virtual heads sharing a K/V head
+    p.pair_head_group = causal ? causal_head_group(p.pair_heads, per_kv, (int64_t)p.Nkv * D * 4, l2_bytes,
+                                                   p.pair_tq, std::max(clusters, 1))
+                               : 1;
+}
+
+// Key blocks of the busiest cluster of the pair kernel with `clusters`
+// clusters (host mirror of PairSched: unit order, alternating rounds, each
+// unit's key blocks).
+template <bool CAUSAL>
+int64_t pair_max_blocks_t(const fa::FwdParams& p, bool alt, int clusters) {
+    using S = fa::Sched<CAUSAL, 128>;
+    int64_t worst = 0;
+    for (int c = 0; c < clusters; ++c) {
+        int64_t sum = 0;
+        for (int64_t pos = c;; pos += clusters) {
+            int64_t t = pos;
+            if (CAUSAL && alt) {
+                const int64_t round = pos / clusters;
+                if (round & 1) t = 2 * round * clusters + clusters - 1 - pos;
+            }
+            if (t >= p.pair_units) break;
+            int vmb;
+            if (CAUSAL) {
+                const int64_t G = p.pair_head_group, tq = p.pair_tq;
+                const int64_t g0 = t / (G * tq) * G;
+                const int64_t gc = std::min<int64_t>(G, p.pair_heads - g0);
+                vmb = (int)(tq - 1 - (t - g0 * tq) / gc);
+            } else {
+                vmb = (int)(t % p.pair_tq);
+            }
+            sum += p.pair == 1 ? S::tile_nkv(vmb, p) : S::tile_nkv(std::min(2 * vmb + 1, p.Tq - 1), p);
+        }
+        worst = std::max(worst, sum);
+    }
+    return worst;
+}
+
 // The schedule of a forward launch whose sizes are in p (Z .. ntiles):
 // causal head groups and alternating rounds for whole tiles, and whether key
 // ranges are cut across CTAs (only where the caller allows it: the cut needs
@@ -383,6 +448,7 @@ struct SchedChoice {
     bool split = false;
     bool alt = false;
     bool chains = false;  // the two-softmax-chain kernel (same tiles and order as the one-chain kernel)
+    bool pair = false;    // the CTA-pair kernel (grid and order set by set_pair_units at launch)
 };
 SchedChoice choose_schedule(fa::FwdParams& p, int D, bool causal, int bn, int sms, int l2_bytes, bool split_allowed) {
     SchedChoice c;
@@ -400,6 +466,7 @@ SchedChoice choose_schedule(fa::FwdParams& p, int D, bool causal, int bn, int sm
         }
     }
     c.chains = chain_kernel_applies(p, D, causal, c.split);
+    c.pair = pair_kernel_applies(p, D, causal, c.split);
     return c;
 }
 
@@ -508,6 +575,21 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* 
     a.tmO = &mo;
     a.stream = stream;
 
+    if (choice.pair) {
+        // clusters of two CTAs, as many as can be resident (pairs of SMs in
+        // one GPC), each CTA loading half of every key block
+        const int limit = fa::pair_cluster_limit_d128();
+        if (limit > 0) {
+            set_pair_units(p, D, causal != 0, info->l2_bytes, limit);
+            a.grid = 2 * std::min(p.pair_units, limit);
+            CUtensorMap mk_half;
+            if (make_map(&mk_half, k, dtype, D, Nkv, Hkv, Z, sk, bn / 2) != CUDA_SUCCESS) return FA_ERR_CUDA;
+            a.tmK = &mk_half;
+            const cudaError_t err = fa::launch_pair_d128(a, causal != 0, dtype == FA_DTYPE_BF16, alt);
+            return err == cudaSuccess ? FA_OK : cuda_fail("forward launch", err);
+        }
+        p.pair = 0;  // no cluster of two fits this device: the one-SM kernels
+    }
     if (choice.chains) {
         const cudaError_t err = launch_chain_for(D, a, causal != 0, dtype == FA_DTYPE_BF16, alt);
         return err == cudaSuccess ? FA_OK : cuda_fail("forward launch", err);
@@ -691,9 +773,19 @@ fa_status fa_fwd_schedule(int Z, int Hq, int Hkv, int Nq, int Nkv, int D, int ca
     out->alternate = c.alt && !c.split ? 1 : 0;
     out->tiles = p.ntiles;
     out->kv_blocks = (int64_t)Z * Hq * head_blocks(p, causal != 0, bn);
-    out->softmax_chains = c.chains ? 2 : 1;
+    out->softmax_chains = c.chains || c.pair ? 2 : 1;
     out->busiest_blocks = c.split ? cdiv(out->kv_blocks, c.grid)
                                   : tile_mode_max_blocks(p, causal != 0, bn, c.grid, c.alt);
+    out->cta_pairs = c.pair ? 1 : 0;
+    if (c.pair) {
+        // clusters of two: as many as the SMs hold (at launch: as the device can hold at once)
+        const int clusters = std::max(1, num_sms / 2);
+        set_pair_units(p, D, causal != 0, l2, clusters);
+        const int used = std::min(p.pair_units, clusters);
+        out->grid = 2 * used;
+        out->head_group = causal ? p.pair_head_group : p.head_group;
+        out->busiest_blocks = causal ? pair_max_blocks_t<true>(p, c.alt, used) : pair_max_blocks_t<false>(p, false, used);
+    }
     return FA_OK;
 }
 
@@ -947,5 +1039,6 @@ void fa_debug_set_wait_limit_ms(double ms) {
 void fa_debug_inject_stall(int enable) { g_inject_stall.store(enable ? 1 : 0); }
 void fa_debug_force_split(int mode) { g_force_split.store(mode == 1 || mode == 2 ? mode : 0); }
 void fa_debug_force_chains(int mode) { g_force_chains.store(mode == 1 || mode == 2 ? mode : 0); }
+void fa_debug_force_pair(int mode) { g_force_pair.store(mode == 1 || mode == 2 ? mode : 0); }
 
 }  // extern "C"

@@ -76,24 +76,48 @@ struct ChainTraits : Traits<D> {
     static_assert(D <= 128 && T::BN == 128, "two-chain kernel: head dims up to 128");
     static_assert(4 * BM * 4 * 2 <= 2 * T::HAND_ROWS * BM * 4, "epilogue hand-over fits");
     static_assert(2 * BM * 4 <= 2 * T::NG * BM * 4, "m hand-off fits");
+    // arrivals are one per warp (ptx::mbar_arrive_warp)
     static __device__ __forceinline__ uint32_t bar_count(int i) {
-        if (i >= T::B_PFULL && i < T::B_PFULL + T::SR) return 128;      // one chain writes P_g
-        if (i >= T::B_EPIFULL && i < T::B_EPIFULL + 2) return 256;      // both chains hand over
-        if (i >= T::B_EPIEMPTY && i < T::B_OFREE + 1) return 128;       // epilogue
-        if (i >= T::B_RED && i < T::B_RED + 2) return 128;              // one chain publishes m
+        if (i >= T::B_PFULL && i < T::B_PFULL + T::SR) return 4;        // one chain writes P_g
+        if (i >= T::B_EPIFULL && i < T::B_EPIFULL + 2) return 8;        // both chains hand over
+        if (i >= T::B_EPIEMPTY && i < T::B_OFREE + 1) return 4;         // epilogue
+        if (i >= T::B_RED && i < T::B_RED + 2) return 4;                // one chain publishes m
         return 1;
     }
+};
+
+// What the softmax chains and the epilogue need from their kernel: the
+// TMEM and barrier layout (L), the tile schedule (S), the scope of their
+// waits, and how "P_g written" and "O read" reach the P·V issuer.  One CTA:
+// every thread arrives on the CTA's own barrier.
+// kSplitP: P_g goes to a ring of its own (L::PR slots of BN / 2 columns at
+// L::TM_P) instead of over the first columns of S_g, so that the score slot
+// is released (arrive_sfree) as soon as the scores are loaded, and the P slot
+// once O += P V of the block that used it last is complete.
+template <int D, bool CAUSAL, bool ALT>
+struct ChainSolo {
+    using L = Traits<D>;
+    using S = Sched<CAUSAL, L::BN, false, ALT>;
+    static constexpr bool kCluster = false;
+    static constexpr bool kSplitP = false;
+    static constexpr int kCheckVar = ALT ? 4 : 0;  // the schedule seg_checked validates
+    uint32_t bar0;
+    __device__ __forceinline__ void arrive_p(uint32_t r) const { ptx::mbar_arrive_warp(bar0 + 8u * (L::B_PFULL + r)); }
+    __device__ __forceinline__ void arrive_sfree(uint32_t) const {}
+    __device__ __forceinline__ void arrive_ofree() const { ptx::mbar_arrive_warp(bar0 + 8u * L::B_OFREE); }
 };
 
 // ------------------------------------------------------------ softmax chain -
 // Chain `ch` (0 or 1) of the online softmax: the key blocks g with g % 2 ==
 // ch, counting every block of every tile this CTA runs.  Thread = query row
 // = TMEM lane; the block's 128 scores sit in the thread's registers.
-template <int D, bool CAUSAL, bool BF16, bool ALT>
-__device__ void chain_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, float* hand, float* mx, int ch,
+template <int D, bool CAUSAL, bool BF16, class C>
+__device__ void chain_softmax(const FwdParams& p, const C& cp, uint32_t tmem, float* hand, float* mx, int ch,
                               const Ctl& ctl) {
-    using T = Traits<D>;
+    using T = typename C::L;
     constexpr int BN = T::BN;
+    constexpr bool CL = C::kCluster;
+    const uint32_t bar0 = cp.bar0;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     const int quad = (threadIdx.x / 32) % 4;  // TMEM lane quadrant this warp may access
     const int row = quad * 32 + threadIdx.x % 32;
@@ -102,10 +126,10 @@ __device__ void chain_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, 
     const float c = p.scale_log2;  // > 0: a negative scale negates S instead
     const uint64_t c2 = ptx::pack_f32x2(c, c);
     uint32_t g = 0, ntile = 0;
-    const Sched<CAUSAL, BN, false, ALT> sc(p);
+    const typename C::S sc(p);
     for (int64_t pos = sc.first(p); sc.valid(pos, p); ++ntile) {
         const Seg ti = sc.seg(pos, p);
-        if (!seg_checked<ALT ? 4 : 0, BN>(ti, p, ctl, SITE_CHECK_SOFTMAX)) return;
+        if (!seg_checked<C::kCheckVar, BN>(ti, p, ctl, SITE_CHECK_SOFTMAX)) return;
         pos = sc.next(pos, ti, p);
         const int q_row = ti.q_start + row;
         float m = -INFINITY, l = 0.f;  // this chain's view of the running max, its part of the row sum
@@ -113,9 +137,12 @@ __device__ void chain_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, 
         for (int j = ti.jb; j < ti.je; ++j, ++g) {
             if ((g & 1u) != (uint32_t)ch) continue;
             const uint32_t r = rslot<T::SR>(g);
-            if (!warp_wait_phase(bar(T::B_SFULL + r), rphase<T::SR>(g), ctl, SITE_S_FULL)) return;
+            if (!warp_wait_phase<CL>(bar(T::B_SFULL + r), rphase<T::SR>(g), ctl, SITE_S_FULL)) return;
             ptx::tc_fence_after();
             const uint32_t s_addr = tmem + lane_addr + T::TM_S + r * BN;
+            const uint32_t pr = rslot<T::PR>(g);
+            uint32_t p_addr = s_addr;  // P over the first BN / 2 columns of the score slot
+            if constexpr (C::kSplitP) p_addr = tmem + lane_addr + T::TM_P + pr * (BN / 2);
             float s[BN];
             {
                 uint32_t r0[32], r1[32], r2[32], r3[32];
@@ -124,6 +151,11 @@ __device__ void chain_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, 
                 ptx::tmem_ld32_issue(s_addr + 64, r2);
                 ptx::tmem_ld32_issue(s_addr + 96, r3);
                 ptx::tmem_wait_ld();
+                if constexpr (C::kSplitP) {
+                    // the scores are in registers: S_{g + SR} may overwrite the slot
+                    ptx::tc_fence_before();
+                    cp.arrive_sfree(r);
+                }
                 ptx::reg_fence32(r0);
                 ptx::reg_fence32(r1);
                 ptx::reg_fence32(r2);
@@ -166,7 +198,7 @@ __device__ void chain_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, 
             float m_prev = -INFINITY;
             if (g > 0) {
                 const uint32_t h = (g - 1u) & 1u;
-                if (!warp_wait_phase(bar(T::B_RED + h), ((g - 1u) >> 1) & 1u, ctl, SITE_MAX_XCHG)) return;
+                if (!warp_wait_phase<CL>(bar(T::B_RED + h), ((g - 1u) >> 1) & 1u, ctl, SITE_MAX_XCHG)) return;
                 m_prev = mx[h * BM + row];
             }
             float alpha = 1.f;
@@ -197,12 +229,19 @@ __device__ void chain_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, 
             have = true;
             // publish the maximum blocks 0..g settled on for the chain of block g + 1
             mx[(g & 1u) * BM + row] = m;
-            ptx::mbar_arrive(bar(T::B_RED + (g & 1u)));
+            ptx::mbar_arrive_warp(bar(T::B_RED + (g & 1u)));
             // p = 2^(s·c − m): l sums the fp32 p, the P·V product takes p cast
             // to the input type, over the first BN/2 columns of the slot.  In
             // a block with no masked key, EMU of every 16 key pairs take the
             // polynomial exponential on the FMA pipe and the others the MUFU
             // unit's ex2, whose throughput otherwise bounds this loop.
+            if constexpr (C::kSplitP) {
+                // the P slot held P_{g - PR}: free once that block's P·V is complete
+                if (g >= (uint32_t)T::PR &&
+                    !warp_wait_phase<CL>(bar(T::B_PVDONE + pr), rphase<T::PR>(g - T::PR), ctl, SITE_P_FREE))
+                    return;
+                ptx::tc_fence_after();
+            }
             const uint64_t negm2 = ptx::pack_f32x2(-m, -m);
             uint64_t sum_a = ptx::pack_f32x2(0.f, 0.f), sum_b = sum_a;
             auto exps = [&](auto emu) {
@@ -227,8 +266,9 @@ __device__ void chain_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, 
                         else sum_a = ptx::fadd2(sum_a, ptx::pack_f32x2(p0, p1));
                         pk[x] = pack2<BF16>(p0, p1);
                     }
-                    // keys 32·c4 .. at packed columns 16·c4 ..: scores this thread has read
-                    ptx::tmem_st16(s_addr + 16 * c4, pk);
+                    // keys 32·c4 .. at packed columns 16·c4 .. (of the score slot:
+                    // scores this thread has read)
+                    ptx::tmem_st16(p_addr + 16 * c4, pk);
                 }
             };
             constexpr int EMU = chain_emu_pairs(D);
@@ -236,15 +276,15 @@ __device__ void chain_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, 
             else exps(std::integral_constant<int, 0>{});
             if (rescale) {
                 // O holds every block up to g - 1 once that block's P·V is complete
-                if (!warp_wait_phase(bar(T::B_PVDONE + rslot<T::SR>(g - 1u)), rphase<T::SR>(g - 1u), ctl,
-                                     SITE_PV_DONE))
+                if (!warp_wait_phase<CL>(bar(T::B_PVDONE + rslot<T::PR>(g - 1u)), rphase<T::PR>(g - 1u), ctl,
+                                         SITE_PV_DONE))
                     return;
                 ptx::tc_fence_after();
                 rescale_o<D>(o_addr, alpha);
             }
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(bar(T::B_PFULL + r));
+            cp.arrive_p(pr);
             float sa, sb, sc2, sd;
             ptx::unpack_f32x2(sum_a, sa, sb);
             ptx::unpack_f32x2(sum_b, sc2, sd);
@@ -253,10 +293,10 @@ __device__ void chain_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, 
         // hand this chain's (m, l) of the tile to the epilogue (-inf, 0 if
         // no block of the tile went through this chain)
         const uint32_t slot = ntile & 1u;
-        if (!warp_wait_phase(bar(T::B_EPIEMPTY + slot), ((ntile >> 1) & 1u) ^ 1u, ctl, SITE_EPI_EMPTY)) return;
+        if (!warp_wait_phase<CL>(bar(T::B_EPIEMPTY + slot), ((ntile >> 1) & 1u) ^ 1u, ctl, SITE_EPI_EMPTY)) return;
         hand[(slot * 4 + 2 * ch) * BM + row] = have ? m : -INFINITY;
         hand[(slot * 4 + 2 * ch + 1) * BM + row] = l;
-        ptx::mbar_arrive(bar(T::B_EPIFULL + slot));
+        ptx::mbar_arrive_warp(bar(T::B_EPIFULL + slot));
     }
 }
 
@@ -265,10 +305,12 @@ __device__ void chain_softmax(const FwdParams& p, uint32_t bar0, uint32_t tmem, 
 // (one 32-row box per warp and swizzle chunk), lse = (m + log2 l)·ln 2
 // ("Write Triton Attention Kernel", steps 6-8), with m and l combined from
 // the two chains; O is released to the P·V issuer as soon as it is read.
-template <int D, bool CAUSAL, bool BF16, bool ALT>
-__device__ void chain_epilogue(const CUtensorMap* tmO, const FwdParams& p, uint32_t sbase, uint32_t bar0,
+template <int D, bool CAUSAL, bool BF16, class C>
+__device__ void chain_epilogue(const CUtensorMap* tmO, const FwdParams& p, const C& cp, uint32_t sbase,
                                uint32_t tmem, const float* hand, const Ctl& ctl) {
-    using T = Traits<D>;
+    using T = typename C::L;
+    constexpr bool CL = C::kCluster;
+    const uint32_t bar0 = cp.bar0;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     const int quad = (threadIdx.x / 32) % 4;
     const int row = quad * 32 + threadIdx.x % 32;
@@ -279,29 +321,29 @@ __device__ void chain_epilogue(const CUtensorMap* tmO, const FwdParams& p, uint3
     auto drain = [&]() {
         if (lane == 0) ptx::bulk_wait_all();
     };
-    const Sched<CAUSAL, T::BN, false, ALT> sc(p);
+    const typename C::S sc(p);
     for (int64_t pos = sc.first(p); sc.valid(pos, p); ++ntile) {
         const Seg ti = sc.seg(pos, p);
-        if (!seg_checked<ALT ? 4 : 0, T::BN>(ti, p, ctl, SITE_CHECK_EPILOGUE)) {
+        if (!seg_checked<C::kCheckVar, T::BN>(ti, p, ctl, SITE_CHECK_EPILOGUE)) {
             drain();
             return;
         }
         pos = sc.next(pos, ti, p);
         step += ti.je - ti.jb;
         const uint32_t slot = ntile & 1u;
-        if (!warp_wait_phase(bar(T::B_EPIFULL + slot), (ntile >> 1) & 1u, ctl, SITE_EPI_FULL)) {
+        if (!warp_wait_phase<CL>(bar(T::B_EPIFULL + slot), (ntile >> 1) & 1u, ctl, SITE_EPI_FULL)) {
             drain();
             return;
         }
         const float m0 = hand[(slot * 4 + 0) * BM + row], l0 = hand[(slot * 4 + 1) * BM + row];
         const float m1 = hand[(slot * 4 + 2) * BM + row], l1 = hand[(slot * 4 + 3) * BM + row];
-        ptx::mbar_arrive(bar(T::B_EPIEMPTY + slot));
+        ptx::mbar_arrive_warp(bar(T::B_EPIEMPTY + slot));
         // O is referenced to the larger maximum (m only grows from block to
         // block); a chain without a block of the tile has m = -inf, l = 0
         const float m = fmaxf(m0, m1);
         const float l = l0 * ptx::ex2(m0 - m) + l1 * ptx::ex2(m1 - m);
         const uint32_t g = step - 1;  // the tile's last P·V
-        if (!warp_wait_phase(bar(T::B_PVDONE + rslot<T::SR>(g)), rphase<T::SR>(g), ctl, SITE_PV_DONE)) {
+        if (!warp_wait_phase<CL>(bar(T::B_PVDONE + rslot<T::PR>(g)), rphase<T::PR>(g), ctl, SITE_PV_DONE)) {
             drain();
             return;
         }
@@ -311,7 +353,7 @@ __device__ void chain_epilogue(const CUtensorMap* tmO, const FwdParams& p, uint3
                                        ti.hq, ti.z, ti.q_start + 32 * quad < p.Nq, [&]() {
                                            // all of O has been read: the next tile's P·V may overwrite it
                                            ptx::tc_fence_before();
-                                           ptx::mbar_arrive(bar(T::B_OFREE));
+                                           cp.arrive_ofree();
                                        });
         if (q_row < p.Nq && p.lse != nullptr) p.lse[ti.lse0 + q_row] = (m + log2f(l)) * 0.6931471805599453f;
     }
@@ -372,10 +414,10 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         }
     } else if (wg < 3) {
         ptx::setmaxnreg_inc<CHAIN_REG_SOFTMAX>();
-        chain_softmax<D, CAUSAL, BF16, ALT>(p, bar0, tmem, hand, mx, wg - 1, ctl);
+        chain_softmax<D, CAUSAL, BF16>(p, ChainSolo<D, CAUSAL, ALT>{bar0}, tmem, hand, mx, wg - 1, ctl);
     } else {
         ptx::setmaxnreg_dec<CHAIN_REG_EPI>();
-        chain_epilogue<D, CAUSAL, BF16, ALT>(&tmO, p, sbase, bar0, tmem, hand, ctl);
+        chain_epilogue<D, CAUSAL, BF16>(&tmO, p, ChainSolo<D, CAUSAL, ALT>{bar0}, sbase, tmem, hand, ctl);
     }
 
     ptx::tc_fence_before();

@@ -9,6 +9,9 @@
 
 #include "fa_fwd_kernel.cuh"
 #include "fa_fwd_chain_kernel.cuh"
+#if FA_HEAD_DIM == 128
+#include "fa_fwd_pair_kernel.cuh"
+#endif
 #include "fa_launch.h"
 
 namespace fa {
@@ -98,6 +101,61 @@ cudaError_t FA_CAT(launch_chain_d, FA_HEAD_DIM)(const LaunchArgs& a, bool causal
         return bf16 ? launch_chain_one<true, true, false>(a) : launch_chain_one<true, false, false>(a);
     }
     return bf16 ? launch_chain_one<false, true, false>(a) : launch_chain_one<false, false, false>(a);
+}
+#endif
+
+#if FA_HEAD_DIM == 128
+// The CTA-pair kernel (fa_fwd, whole tiles, D = 128): clusters of two CTAs,
+// a.grid = 2 x clusters.
+template <bool CAUSAL, bool BF16, bool ALT>
+static cudaError_t launch_pair_one(const LaunchArgs& a) {
+    constexpr int D = FA_HEAD_DIM;
+    auto kernel = fa_fwd_pair_kernel<D, CAUSAL, BF16, ALT>;
+    constexpr int smem = PairTraits<D>::SMEM_BYTES;
+    static std::atomic<uint64_t> configured{0};
+    cudaError_t err = set_smem_for_context(kernel, smem, configured);
+    if (err != cudaSuccess) return err;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.grid);
+    cfg.blockDim = dim3(CHAIN_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = a.stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, *a.tmQ, *a.tmK, *a.tmV, *a.tmO, a.params);
+}
+
+cudaError_t launch_pair_d128(const LaunchArgs& a, bool causal, bool bf16, bool alt) {
+    if (causal) {
+        if (alt) return bf16 ? launch_pair_one<true, true, true>(a) : launch_pair_one<true, false, true>(a);
+        return bf16 ? launch_pair_one<true, true, false>(a) : launch_pair_one<true, false, false>(a);
+    }
+    return bf16 ? launch_pair_one<false, true, false>(a) : launch_pair_one<false, false, false>(a);
+}
+
+// Clusters of the pair kernel that can be resident at once on the current
+// device (pairs of SMs in one GPC); every instantiation has the same
+// resources.  Asked once per context; 0 when the query fails.
+int pair_cluster_limit_d128() {
+    static std::atomic<uint64_t> ctx{0};
+    static std::atomic<int> limit{0};
+    const uint64_t id = current_context_id();
+    if (id != 0 && ctx.load() == id) return limit.load();
+    auto kernel = fa_fwd_pair_kernel<FA_HEAD_DIM, false, true, false>;
+    constexpr int smem = PairTraits<FA_HEAD_DIM>::SMEM_BYTES;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(CHAIN_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) return 0;
+    limit.store(n);
+    if (id != 0) ctx.store(id);
+    return n;
 }
 #endif
 

@@ -68,6 +68,7 @@ struct Traits {
     // each holding S_g (BN fp32 columns) and then, in its first BN/2
     // columns, P_g (two 16-bit values per column); then O (D fp32 columns)
     static constexpr int SR = 3;
+    static constexpr int PR = SR;                              // P_g lives in its score slot
     static constexpr uint32_t TM_S = 0;                        // S/P ring slot r at TM_S + r * BN
     static constexpr uint32_t TM_O = SR * BN;                  // O
     static constexpr uint32_t TMEM_COLS = 512;
@@ -131,12 +132,20 @@ __device__ __forceinline__ void record_timeout(const Ctl& c, uint32_t site) {
 }
 
 // Wait for the phase of `bar` with parity `parity`.  Gives up (false) when
-// another role has aborted or after limit_ns, recording the site.
+// another role has aborted or after limit_ns, recording the site.  CLUSTER:
+// the phase may complete through arrivals from the other CTA of a pair, whose
+// writes the wait then acquires (cluster scope).
+template <bool CLUSTER = false>
+__device__ __forceinline__ bool try_phase(uint32_t bar, uint32_t parity) {
+    if constexpr (CLUSTER) return ptx::mbar_try_wait_cluster(bar, parity);
+    else return ptx::mbar_try_wait(bar, parity);
+}
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Ctl& c, uint32_t site) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (try_phase<CLUSTER>(bar, parity)) return true;
     const uint64_t t0 = ptx::globaltimer_ns();
     for (;;) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (try_phase<CLUSTER>(bar, parity)) return true;
         if (*c.abort_flag) return false;
         if (ptx::globaltimer_ns() - t0 > c.limit_ns) {
             record_timeout(c, site);
@@ -147,14 +156,16 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
 
 // The same wait taken by a whole warp: every lane leaves with the same answer,
 // so no lane can run ahead into a warp-collective tcgen05 access alone.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool warp_wait_phase(uint32_t bar, uint32_t parity, const Ctl& c, uint32_t site) {
-    return __all_sync(0xffffffffu, wait_phase(bar, parity, c, site));
+    return __all_sync(0xffffffffu, wait_phase<CLUSTER>(bar, parity, c, site));
 }
 
 // Teardown wait after an abort: ignores the abort flag, bounded by limit_ns.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool drain_phase(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
     const uint64_t t0 = ptx::globaltimer_ns();
-    while (!ptx::mbar_try_wait(bar, parity))
+    while (!try_phase<CLUSTER>(bar, parity))
         if (ptx::globaltimer_ns() - t0 > limit_ns) return false;
     return true;
 }
@@ -227,7 +238,8 @@ __device__ __forceinline__ bool seg_checked(const Seg& s, const FwdParams& p, co
                   s.slot >= -1 && s.slot < 2 * (int)gridDim.x;
         // a key block past the keys: allowed only as a variant tile's single
         // block whose rows keep no key (it is masked whole)
-        if (var_kind(VAR) == 0) ok = ok && s.je <= tk && s.q_start < s.nq;
+        // (a CTA pair of query blocks 2m, 2m + 1 may hold a tile past the rows)
+        if (var_kind(VAR) == 0) ok = ok && s.je <= tk && (s.q_start < s.nq || p.pair == 2);
         else ok = ok && (s.je <= tk || s.je == s.jb + 1);
         if (!ok) {
             *c.abort_flag = 1;

@@ -60,6 +60,13 @@ cudaError_t launch_chain_d32(const LaunchArgs& a, bool causal, bool bf16, bool a
 cudaError_t launch_chain_d64(const LaunchArgs& a, bool causal, bool bf16, bool alt);
 cudaError_t launch_chain_d128(const LaunchArgs& a, bool causal, bool bf16, bool alt);
 
+// Launch fa_fwd_pair_kernel<128, causal, bf16, alt>: whole tiles (fa_fwd,
+// D = 128) in units of two tiles per cluster of two CTAs (params.pair*);
+// a.grid = 2 x clusters, at most 2 x pair_cluster_limit_d128(), and tmK in
+// 64-row boxes (each CTA loads half of every key block).
+cudaError_t launch_pair_d128(const LaunchArgs& a, bool causal, bool bf16, bool alt);
+int pair_cluster_limit_d128();
+
 // fa_lse_merge: parts share one layout; rows = Z * H * N
 constexpr int MERGE_MAX_PARTS = 16;
 struct MergeArgs {

@@ -29,6 +29,10 @@ enum WaitSite : uint32_t {
     SITE_MAX_XCHG = 13,
     SITE_P_FREE = 14,
     SITE_S_FREE = 15,
+    SITE_PEER_Q = 16,       // CTA pair: the other CTA's Q tile, K or V half landed
+    SITE_PEER_K = 17,
+    SITE_PEER_V = 18,
+    SITE_DRAIN = 19,
     // backward
     SITE_B_KV_FULL = 20,
     SITE_B_KV_EMPTY = 21,
@@ -87,6 +91,17 @@ struct FwdParams {
     const float* alibi;      // (Hq) slopes, or nullptr
     const int* cu_q;         // (Z + 1) offsets into the packed query rows, or nullptr
     const int* cu_k;         // (Z + 1) offsets into the packed key rows
+    // CTA-pair kernel (pair != 0): a cluster of two CTAs takes a unit of two
+    // query tiles that see the same key blocks -- pair 1: query heads 2k and
+    // 2k + 1 (one GQA group) at query block mb; pair 2: query blocks 2m and
+    // 2m + 1 of one head -- one tile per CTA.  Units are tiles of "virtual
+    // heads" of pair_tq virtual query blocks, ordered like whole tiles
+    // (causal: groups of pair_head_group virtual heads, heaviest first).
+    int pair;
+    int pair_heads;          // Z * Hq / 2 (pair 1) or Z * Hq (pair 2)
+    int pair_tq;             // Tq (pair 1) or ceil(Tq / 2) (pair 2)
+    int pair_units;          // pair_heads * pair_tq
+    int pair_head_group;
 };
 
 // Backward kernel parameters (fa_bwd).  Tensor strides are in elements; the

@@ -376,6 +376,15 @@ fa_status fa_fwd_plan(int Z, int Hq, int Hkv, int Nq, int Nkv, int D, int causal
  *   softmax_chains  2: whole tiles of head dims up to 128 run the kernel
  *                   whose softmax is two warpgroups taking the key blocks in
  *                   turn (the same tiles and order); 1: one chain
+ *   cta_pairs       1: whole tiles at D = 128 run on clusters of two CTAs,
+ *                   each cluster taking two query tiles that see the same key
+ *                   blocks (two query heads of a GQA group, else query blocks
+ *                   2m and 2m + 1 of one head) and multiplying each key block
+ *                   once for both (M = 256 over two SMs, each holding half of
+ *                   every K and V block), with two softmax chains per SM;
+ *                   grid is then 2 x min(units, num_sms / 2) (at launch: the
+ *                   clusters the device can hold at once) and busiest_blocks
+ *                   the key blocks of the busiest cluster
  * Errors: those of fa_fwd_plan for bad shapes; FA_ERR_INVALID_ARG for a NULL
  * out, num_sms < 1 or l2_bytes < 1.  fa_debug_force_split applies here too.
  */
@@ -389,6 +398,7 @@ typedef struct {
     int64_t kv_blocks;
     int64_t busiest_blocks;
     int softmax_chains;
+    int cta_pairs;
 } fa_fwd_schedule_info;
 
 fa_status fa_fwd_schedule(int Z, int Hq, int Hkv, int Nq, int Nkv, int D, int causal, int splitkv, int num_sms,
@@ -406,6 +416,11 @@ fa_status fa_fwd_schedule(int Z, int Hq, int Hkv, int Nq, int Nkv, int D, int ca
  * fa_debug_force_chains -- which kernel runs whole tiles of head dims up to
  *   128: 0 by the shape (default: two softmax chains), 1 two chains, 2 one
  *   chain.  Both compute the same result (up to the order of rounding).
+ * fa_debug_force_pair -- whether whole tiles at D = 128 run on CTA pairs
+ *   (see fa_fwd_schedule's cta_pairs): 0 default (one-SM kernels: the pair
+ *   kernel measured level with them on long tiles and slower on short ones),
+ *   1 wherever the kernel applies, 2 never.  It takes precedence over
+ *   fa_debug_force_chains.  The same result up to the order of rounding.
  * fa_debug_inject_stall -- when enabled, CTA 0 of later launches never issues
  *   the copy of its first K tile, so the wait for it runs out: the kernel
  *   records FA_ERR_DEVICE_TIMEOUT (read with fa_device_status), every role of
@@ -429,6 +444,7 @@ fa_status fa_debug_exp2(const float* x, float* y, int64_t n, cudaStream_t stream
 void fa_debug_inject_stall(int enable);
 void fa_debug_force_split(int mode);
 void fa_debug_force_chains(int mode);
+void fa_debug_force_pair(int mode);
 
 #ifdef __cplusplus
 }

@@ -253,6 +253,38 @@ def _busiest(Z, Hq, Nq, Nkv, bn, causal, grid, head_group, alternate):
     return max(loads)
 
 
+def _pair_units(Z, Hq, Hkv, Nq):
+    """CTA-pair kernel: (mode, virtual heads, virtual query blocks); mode 1 pairs the query
+    heads 2k, 2k + 1 of a GQA group, mode 2 the query blocks 2m, 2m + 1 of one head."""
+    tq = -(-Nq // 128)
+    if (Hq // Hkv) % 2 == 0:
+        return 1, Z * Hq // 2, tq
+    return 2, Z * Hq, -(-tq // 2)
+
+
+def _pair_busiest(Z, Hq, Hkv, Nq, Nkv, causal, clusters, head_group, alternate):
+    mode, vheads, vtq = _pair_units(Z, Hq, Hkv, Nq)
+    tq = -(-Nq // 128)
+
+    def blocks(vmb):  # both tiles of a unit visit the key blocks of the later one
+        mb = vmb if mode == 1 else min(2 * vmb + 1, tq - 1)
+        return _tile_blocks(mb, Nq, Nkv, 128, causal)
+
+    if causal:
+        order = []
+        for g0 in range(0, vheads, head_group):
+            gc = min(head_group, vheads - g0)
+            for vmb in reversed(range(vtq)):
+                order += [blocks(vmb)] * gc
+    else:
+        order = [blocks(vmb) for _ in range(vheads) for vmb in range(vtq)]
+    loads = [0] * clusters
+    for t, b in enumerate(order):
+        r, k = divmod(t, clusters)
+        loads[clusters - 1 - k if (alternate and r % 2) else k] += b
+    return max(loads)
+
+
 @pytest.mark.parametrize("shape", [
     (4, 16, 16, 1024, 1024, 128, False),   # the bench workload, both masks
     (4, 16, 16, 1024, 1024, 128, True),
@@ -260,20 +292,46 @@ def _busiest(Z, Hq, Nq, Nkv, bn, causal, grid, head_group, alternate):
     (128, 8, 8, 1024, 1024, 128, True),    # 1024 heads: several head groups
     (1, 32, 8, 8192, 8192, 128, True),
     (1, 32, 8, 32768, 32768, 128, True),   # GQA: groups of 8 query heads
+    (1, 32, 8, 8192, 8192, 128, False),
+    (2, 3, 1, 4000, 4000, 128, True),      # CTA pairs of query blocks, odd block count
     (2, 3, 1, 1000, 300, 64, True),        # odd sizes, fewer tiles than SMs
     (3, 5, 5, 130, 4000, 32, False),
 ])
-def test_schedule_matches_the_documented_order(shape):
+@pytest.mark.parametrize("pairs", [False, True], ids=["one_sm", "cta_pairs"])
+def test_schedule_matches_the_documented_order(shape, pairs):
     import exact_attention_44_gb300 as fa
     Z, Hq, Hkv, Nq, Nkv, D, causal = shape
-    s = fa.fa_fwd_schedule(Z, Hq, Hkv, Nq, Nkv, D, causal, num_sms=GB300_SMS, l2_bytes=GB300_L2)
+    fa.fa_debug_force_pair(1 if pairs else 0)
+    try:
+        s = fa.fa_fwd_schedule(Z, Hq, Hkv, Nq, Nkv, D, causal, num_sms=GB300_SMS, l2_bytes=GB300_L2)
+    finally:
+        fa.fa_debug_force_pair(0)
     bn = 64 if D == 256 else 128
     heads, tq, tk = Z * Hq, -(-Nq // 128), -(-Nkv // bn)
     assert s["split"] == 0 and s["gqa_packed"] == 0
-    # head dims up to 64 with long tiles (>= 16 key blocks a tile on average) run
-    # two softmax chains, the rest one
-    assert s["softmax_chains"] == (2 if D <= 64 and s["kv_blocks"] >= 16 * s["tiles"] else 1)
-    assert s["tiles"] == heads * tq and s["grid"] == min(heads * tq, GB300_SMS)
+    long_tiles = s["kv_blocks"] >= 16 * s["tiles"]
+    # head dims up to 64 with long tiles (>= 16 key blocks a tile on average)
+    # run two softmax chains, the rest one; CTA pairs (D = 128) only when asked
+    assert s["cta_pairs"] == int(pairs and D == 128)
+    assert s["softmax_chains"] == (2 if (D <= 64 and long_tiles) or s["cta_pairs"] else 1)
+    assert s["tiles"] == heads * tq
+    if s["cta_pairs"]:
+        mode, vheads, vtq = _pair_units(Z, Hq, Hkv, Nq)
+        clusters = min(vheads * vtq, GB300_SMS // 2)
+        assert s["grid"] == 2 * clusters
+        assert s["kv_blocks"] == Z * Hq * sum(_tile_blocks(mb, Nq, Nkv, bn, causal) for mb in range(tq))
+        alternate = int(causal and long_tiles)
+        assert s["alternate"] == alternate
+        assert s["kv_blocks"] == Z * Hq * sum(_tile_blocks(mb, Nq, Nkv, bn, causal) for mb in range(tq))
+        if causal:
+            per_kv = (Hq // Hkv) // 2 if mode == 1 else Hq // Hkv
+            kv_heads = max(1, (GB300_L2 // 3) // (Nkv * D * 4))
+            want = min(vheads, max(kv_heads * per_kv, -(-4 * clusters // vtq)))
+            assert s["head_group"] == want
+        assert s["busiest_blocks"] == _pair_busiest(Z, Hq, Hkv, Nq, Nkv, causal, clusters, s["head_group"],
+                                                    alternate)
+        return
+    assert s["grid"] == min(heads * tq, GB300_SMS)
     assert s["kv_blocks"] == Z * Hq * sum(_tile_blocks(mb, Nq, Nkv, bn, causal) for mb in range(tq))
     if causal:
         # a group's K/V within a third of L2, at least four rounds of tiles, at most every head
@@ -305,7 +363,18 @@ def test_schedule_known_values():
     # head dims up to 64 with long tiles take two chains
     assert fa.fa_fwd_schedule(8, 16, 16, 2048, 2048, 64, False, **kw)["softmax_chains"] == 2
     assert fa.fa_fwd_schedule(8, 16, 16, 2048, 2048, 64, True, **kw)["softmax_chains"] == 1
-    assert fa.fa_fwd_schedule(1, 32, 8, 8192, 8192, 128, False, **kw)["softmax_chains"] == 1
+    # D = 128: one SM per tile unless CTA pairs are asked for; then 1024 units
+    # of two tiles on 76 clusters, 14 units of 64 key blocks on the busiest
+    c = fa.fa_fwd_schedule(1, 32, 8, 8192, 8192, 128, False, **kw)
+    assert (c["cta_pairs"], c["softmax_chains"], c["grid"]) == (0, 1, 152)
+    try:
+        fa.fa_debug_force_pair(1)
+        c = fa.fa_fwd_schedule(1, 32, 8, 8192, 8192, 128, False, **kw)
+        assert (c["cta_pairs"], c["softmax_chains"], c["grid"], c["busiest_blocks"]) == (1, 2, 152, 14 * 64)
+        # never at other head dims or with cut key ranges
+        assert fa.fa_fwd_schedule(1, 32, 8, 8192, 8192, 64, False, **kw)["cta_pairs"] == 0
+    finally:
+        fa.fa_debug_force_pair(0)
     # alternating rounds: 236 blocks on the busiest CTA instead of 284
     assert fa.fa_fwd_schedule(8, 16, 16, 2048, 2048, 256, True, **kw)["busiest_blocks"] == 236
 

@@ -38,3 +38,36 @@ def test_withheld_copy_times_out_and_the_context_recovers(chains):
     check_full(22, 1, 4, 2, 300, 300, 64, "bf16", True)
     assert fa.fa_device_status() == (fa.FA_OK, 0)
     torch.cuda.synchronize()
+
+
+def test_withheld_copy_times_out_on_cta_pairs():
+    # the CTA-pair kernel (D = 128, long tiles): CTA 0 withholds its first K
+    # half; a CTA of cluster 0 records the timeout (the even CTA waiting for
+    # that half, or the odd one waiting for the scores that never come), both
+    # leave through the cluster barrier, the context stays usable
+    import torch
+
+    import exact_attention_44_gb300 as fa
+    fa.build()
+    fa.fa_debug_force_pair(1)
+    q, k, v = si.qkv(23, 1, 4, 2, 1024, 2048, 128, "bf16")
+    qt, kt, vt = (si.as_torch(x, "bf16").cuda() for x in (q, k, v))
+    assert fa.fa_device_status()[0] == fa.FA_OK
+    fa.fa_debug_set_wait_limit_ms(100)
+    fa.fa_debug_inject_stall(True)
+    try:
+        fa.fa_fwd(qt, kt, vt, causal=False)
+        code, word = fa.fa_device_status()
+    finally:
+        fa.fa_debug_inject_stall(False)
+        fa.fa_debug_set_wait_limit_ms(0)
+    try:
+        assert code == fa.FA_ERR_DEVICE_TIMEOUT, hex(word)
+        assert (word >> 16) in (0, 1)          # a CTA of cluster 0
+        assert 1 <= (word >> 8) & 0xFF <= 19   # a known wait site
+        assert fa.fa_device_status() == (fa.FA_OK, 0)
+        check_full(24, 1, 4, 2, 300, 2100, 128, "bf16", True)
+        assert fa.fa_device_status() == (fa.FA_OK, 0)
+    finally:
+        fa.fa_debug_force_pair(0)
+    torch.cuda.synchronize()
