@@ -370,7 +370,10 @@ def run_e2e(args, wl, host, flags, scale, device, stream, world):
 
     Steps alternate between two streams, each with its own device and pinned host buffers,
     so that one step's device-to-host copies overlap the next step's host-to-device copies
-    (opposite directions, separate copy engines); every step still moves all of its bytes."""
+    (opposite directions, separate copy engines); every step still moves all of its bytes.
+    Events around each step's launches give the kernels' own time inside the loop (a step's
+    launches start once its copies are in and the previous step's launches are done), and
+    nvidia-smi samples the clocks over the loop."""
     import torch
 
     import exact_attention_44_gb300 as fa
@@ -387,14 +390,19 @@ def run_e2e(args, wl, host, flags, scale, device, stream, world):
         lanes.append((dev_in, outs, host_out))
     steps = max(3, min(args.steps, 50))
 
-    def step(i):
+    def step(i, spans=None):
         s = streams[i % 2]
         dev_in, outs, host_out = lanes[i % 2]
         with torch.cuda.stream(s):
             for d, h in zip(dev_in, host):
                 d.copy_(h, non_blocking=True)
+            if spans is not None:
+                spans.append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
+                spans[-1][0].record(s)
             for (o, lse), causal in zip(outs, flags):
                 fa.fa_fwd(*dev_in, o=o, lse=lse, scale=scale, causal=causal, stream=s)
+            if spans is not None:
+                spans[-1][1].record(s)
             for (o, lse), (ho, hl) in zip(outs, host_out):
                 ho.copy_(o, non_blocking=True)
                 hl.copy_(lse, non_blocking=True)
@@ -403,22 +411,34 @@ def run_e2e(args, wl, host, flags, scale, device, stream, world):
         step(i)
     torch.cuda.synchronize(device)
     barrier(world)
+    clocks = ClockSampler(device.index if device.index is not None else 0) if int(os.environ.get("RANK", "0")) == 0 else None
+    spans = []
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
     streams[1].wait_event(a)
     for i in range(steps):
-        step(i)
+        step(i, spans)
     done = torch.cuda.Event()
     done.record(streams[1])
     stream.wait_event(done)
     b.record(stream)
     torch.cuda.synchronize(device)
+    clock = clocks.stop() if clocks is not None else None
     ms = all_reduce_max(a.elapsed_time(b), world, device)
+    # a step's launches run from when its copies are in and the previous step's are done
+    ends = [a.elapsed_time(e1) for _, e1 in spans]
+    kernel_ms = [ends[i] - max(a.elapsed_time(e0), ends[i - 1] if i else 0.0) for i, (e0, _) in enumerate(spans)]
     h2d, d2h = io_bytes(wl)
     del lanes
-    return {"value": round(world * step_flops(wl) * steps / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
-            "ms_per_step": round(ms / steps, 4), "streams": 2}
+    out = {"value": round(world * step_flops(wl) * steps / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+           "ms_per_step": round(ms / steps, 4), "streams": 2,
+           "kernel_ms_per_step": {"mean": round(statistics.fmean(kernel_ms), 4),
+                                  "first": round(kernel_ms[0], 4), "last": round(kernel_ms[-1], 4)},
+           "kernel_share": round(sum(kernel_ms) / ms, 4)}
+    if clock is not None:
+        out["clocks"] = clock
+    return out
 
 
 def measure_host_link(wl, host, device, stream, reps=10):
