@@ -19,8 +19,14 @@
 //   dQ phase      per unit (128-row query block, query head), Q and dO
 //                 resident, key steps of 64 keys:
 //                   S = Qᵢ Kⱼᵀ, dP = dOᵢ Vⱼᵀ, dS = P ∘ (dP − Δ), dQ += dS Kⱼ.
-// Operands are single-buffered and the steps run one after another.  dK, dV
-// and dQ are each summed inside one CTA: no atomics, bitwise reproducible.
+// The dV pass does not need V: its 64 KB hold a second slot of Q, dO (and a
+// second Sᵀ block in TMEM), so that pass issues step t + 1's Sᵀ before step
+// t's accumulation while step t + 2's copies are in flight, and V loads once
+// the pass is done.  The dK pass and the dQ phase are single-buffered (no
+// room for a second slot; measured on GB300 at Z8 H16 N2048 with one slot
+// everywhere: ~2.2 us a step in the dV pass against ~0.7 us of tensor work).
+// dK, dV and dQ are each summed inside one CTA: no atomics, bitwise
+// reproducible.
 // The pre kernel (Δ, base-2 lse), the unit orders and the tile stores are the
 // smaller head dims' (fa_bwd_kernel.cuh).
 //
@@ -46,23 +52,27 @@ struct WideTraits {
     static constexpr int TILE64 = STEP * D * 2;    // 32 KB: a step's 64-row tile
     // ---- dK / dV phase ----
     static constexpr int KV_OFF_K = 0;
-    static constexpr int KV_OFF_V = KV_OFF_K + TILE128;
-    static constexpr int KV_OFF_Q = KV_OFF_V + TILE128;
-    static constexpr int KV_OFF_DO = KV_OFF_Q + TILE64;
-    static constexpr int KV_OFF_LSE = KV_OFF_DO + TILE64;     // 64 floats
-    static constexpr int KV_OFF_DELTA = KV_OFF_LSE + 256;     // 64 floats
-    static constexpr int KV_OFF_OST = (KV_OFF_DELTA + 256 + 1023) / 1024 * 1024;  // epilogue staging
+    static constexpr int KV_OFF_V = KV_OFF_K + TILE128;       // V (dK pass), or slot 1's Q and dO (dV pass)
+    static constexpr int KV_OFF_Q = KV_OFF_V + TILE128;       // slot 0's Q
+    static constexpr int KV_OFF_DO = KV_OFF_Q + TILE64;       // slot 0's dO
+    static constexpr int KV_OFF_LSE = KV_OFF_DO + TILE64;     // [2] x 64 floats
+    static constexpr int KV_OFF_DELTA = KV_OFF_LSE + 512;     // [2] x 64 floats
+    static constexpr int KV_OFF_OST = (KV_OFF_DELTA + 512 + 1023) / 1024 * 1024;  // epilogue staging
     static constexpr int KV_OFF_BAR = KV_OFF_OST + 128 * SW;
-    static constexpr int KB_KV_FULL = 0;      // K, V of a unit landed (TMA)
+    static constexpr int KB_K_FULL = 0;       // K of a unit landed (TMA)
     static constexpr int KB_KV_EMPTY = 1;     // the unit's products are done (commit)
-    static constexpr int KB_QD_FULL = 2;      // Q, dO, lse2, Δ of a step landed
-    static constexpr int KB_QD_EMPTY = 3;     // that step's products are done (commit)
-    static constexpr int KB_S_FULL = 4;       // Sᵀ (and dPᵀ in the dK pass) in TMEM (commit)
-    static constexpr int KB_P_FULL = 5;       // Pᵀ (dV pass) or dSᵀ (dK pass) written (128)
-    static constexpr int KB_ACC_FULL = 6;     // dV or dK of a unit complete (commit)
-    static constexpr int KB_ACC_FREE = 7;     // that accumulator read out (128)
-    static constexpr int KB_DRAIN = 8;
-    static constexpr int KV_NUM_BARS = 9;
+    static constexpr int KB_QD_FULL = 2;      // [2] Q, dO, lse2, Δ of a step landed in slot b
+    static constexpr int KB_QD_EMPTY = 4;     // [2] that step's products are done (commit)
+    static constexpr int KB_S_FULL = 6;       // [2] Sᵀ (and dPᵀ in the dK pass) in TMEM (commit)
+    static constexpr int KB_P_FULL = 8;       // [2] Pᵀ (dV pass) or dSᵀ (dK pass) written (128)
+    static constexpr int KB_ACC_FULL = 10;    // dV or dK of a unit complete (commit)
+    static constexpr int KB_ACC_FREE = 11;    // that accumulator read out (128)
+    static constexpr int KB_DRAIN = 12;
+    static constexpr int KB_V_FULL = 13;      // V of a unit landed, after the dV pass (TMA)
+    static constexpr int KV_NUM_BARS = 14;
+    // a step slot's Q and dO tiles (slot 1 lives where V goes)
+    static __host__ __device__ constexpr uint32_t kv_q(uint32_t b) { return b ? KV_OFF_V : KV_OFF_Q; }
+    static __host__ __device__ constexpr uint32_t kv_do(uint32_t b) { return b ? KV_OFF_V + TILE64 : KV_OFF_DO; }
     static constexpr int KV_SMEM_USED = KV_OFF_BAR + KV_NUM_BARS * 8;
     // ---- dQ phase ----
     static constexpr int Q_OFF_Q = 0;
@@ -90,12 +100,14 @@ struct WideTraits {
     // over their first 32 columns) and one 256-column accumulator
     static constexpr uint32_t TM_S = 0;
     static constexpr uint32_t TM_DP = 64;
+    // dV pass: Sᵀ of slot b (slot 1 takes the dPᵀ block, unused in that pass)
+    static __host__ __device__ constexpr uint32_t tm_slot(uint32_t b) { return b ? TM_DP : TM_S; }
     static constexpr uint32_t TM_ACC = 256;
     static constexpr uint32_t TMEM_COLS = 512;
     static_assert(TM_ACC + D <= TMEM_COLS, "tensor memory budget");
 
     static __device__ __forceinline__ uint32_t kv_bar_count(int i) {
-        return (i == KB_P_FULL || i == KB_ACC_FREE) ? 128 : 1;
+        return ((i >= KB_P_FULL && i < KB_P_FULL + 2) || i == KB_ACC_FREE) ? 128 : 1;
     }
     static __device__ __forceinline__ uint32_t q_bar_count(int i) {
         return (i == QB_DS_FULL || i == QB_DQ_FREE) ? 128 : 1;
@@ -134,6 +146,9 @@ __device__ __forceinline__ void wide_step(const BwdUnit& w, int s, const BwdPara
     r0 = (w.i0 + (s % per_head) / 2) * 128 + (s % 2) * 64;
 }
 
+// Step slots: the dV pass alternates slots 0 and 1 (step s in slot s & 1),
+// the dK pass uses slot 0.  Every role counts the fills of each slot;
+// fill n of a slot completes phase n & 1 of its barriers.
 template <bool CAUSAL>
 __device__ void wide_kv_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const CUtensorMap* tmQ,
                                  const CUtensorMap* tmDO, const BwdParams& p, uint32_t sbase, uint32_t bar0,
@@ -142,39 +157,48 @@ __device__ void wide_kv_producer(const CUtensorMap* tmK, const CUtensorMap* tmV,
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     const uint64_t pol_kv = ptx::policy_evict_first();
     const uint64_t pol_q = ptx::policy_evict_last();
-    uint32_t uc = 0, t = 0;
+    uint32_t uc = 0, vc = 0, n0 = 0, n1 = 0;  // fills of slots 0 and 1
     bool ok = true;
+    // Q, dO, lse2, Δ of step s into slot b, once that slot's previous step is done
+    auto fill = [&](const BwdUnit& w, int s, uint32_t b) -> bool {
+        const uint32_t nb = b ? n1 : n0;
+        if (nb >= 1 && !wait_phase(bar(T::KB_QD_EMPTY + b), (nb - 1) & 1u, ctl, SITE_B_QD_EMPTY)) return false;
+        int hq, r0;
+        wide_step(w, s, p, hq, r0);
+        const uint32_t full = bar(T::KB_QD_FULL + b);
+        ptx::mbar_arrive_expect_tx(full, 2 * T::TILE64 + 512);
+        wide_load64(sbase + T::kv_q(b), tmQ, full, r0, hq, w.z, pol_q);
+        wide_load64(sbase + T::kv_do(b), tmDO, full, r0, hq, w.z, pol_q);
+        const int64_t row0 = ((int64_t)w.z * p.Hq + hq) * p.Tq * 128 + r0;
+        ptx::bulk_load(sbase + T::KV_OFF_LSE + b * 256u, p.lse2 + row0, 256, full);
+        ptx::bulk_load(sbase + T::KV_OFF_DELTA + b * 256u, p.delta + row0, 256, full);
+        if (b) ++n1;
+        else ++n0;
+        return true;
+    };
     for (int pos = blockIdx.x; ok && unit_at<CAUSAL>(pos) < p.nunits; pos += gridDim.x) {
         const BwdUnit w = bwd_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
         if (w.nsteps == 0) continue;
+        // K and the V region (slot 1, then V) are free once the previous unit is done
         if (uc > 0 && !wait_phase(bar(T::KB_KV_EMPTY), (uc - 1) & 1u, ctl, SITE_B_KV_EMPTY)) { ok = false; break; }
-        ptx::mbar_arrive_expect_tx(bar(T::KB_KV_FULL), 2 * T::TILE128);
-        wide_load128(sbase + T::KV_OFF_K, tmK, bar(T::KB_KV_FULL), w.j * 128, w.hk, w.z, pol_kv);
-        wide_load128(sbase + T::KV_OFF_V, tmV, bar(T::KB_KV_FULL), w.j * 128, w.hk, w.z, pol_kv);
+        ptx::mbar_arrive_expect_tx(bar(T::KB_K_FULL), T::TILE128);
+        wide_load128(sbase + T::KV_OFF_K, tmK, bar(T::KB_K_FULL), w.j * 128, w.hk, w.z, pol_kv);
         ++uc;
-        // the dV pass, then the dK pass: every step's Q, dO, lse2, Δ twice
-        const int steps = 2 * w.nsteps;
-        for (int pass = 0; ok && pass < 2; ++pass) {
-            for (int s = 0; s < steps; ++s, ++t) {
-                if (t >= 1 && !wait_phase(bar(T::KB_QD_EMPTY), (t - 1) & 1u, ctl, SITE_B_QD_EMPTY)) {
-                    ok = false;
-                    break;
-                }
-                int hq, r0;
-                wide_step(w, s, p, hq, r0);
-                const uint32_t full = bar(T::KB_QD_FULL);
-                ptx::mbar_arrive_expect_tx(full, 2 * T::TILE64 + 512);
-                wide_load64(sbase + T::KV_OFF_Q, tmQ, full, r0, hq, w.z, pol_q);
-                wide_load64(sbase + T::KV_OFF_DO, tmDO, full, r0, hq, w.z, pol_q);
-                const int64_t row0 = ((int64_t)w.z * p.Hq + hq) * p.Tq * 128 + r0;
-                ptx::bulk_load(sbase + T::KV_OFF_LSE, p.lse2 + row0, 256, full);
-                ptx::bulk_load(sbase + T::KV_OFF_DELTA, p.delta + row0, 256, full);
-            }
-        }
+        const int steps = 2 * w.nsteps;  // >= 2: slot 1 is filled at least once
+        for (int s = 0; ok && s < steps; ++s) ok = fill(w, s, (uint32_t)s & 1u);
+        if (!ok) break;
+        // V over slot 1, once its last dV step is done
+        if (!wait_phase(bar(T::KB_QD_EMPTY + 1), (n1 - 1) & 1u, ctl, SITE_B_QD_EMPTY)) { ok = false; break; }
+        ptx::mbar_arrive_expect_tx(bar(T::KB_V_FULL), T::TILE128);
+        wide_load128(sbase + T::KV_OFF_V, tmV, bar(T::KB_V_FULL), w.j * 128, w.hk, w.z, pol_kv);
+        ++vc;
+        for (int s = 0; ok && s < steps; ++s) ok = fill(w, s, 0u);
     }
     if (!ok) {
-        if (uc > 0) drain_phase(bar(T::KB_KV_FULL), (uc - 1) & 1u, ctl.limit_ns);
-        if (t > 0) drain_phase(bar(T::KB_QD_FULL), (t - 1) & 1u, ctl.limit_ns);
+        if (uc > 0) drain_phase(bar(T::KB_K_FULL), (uc - 1) & 1u, ctl.limit_ns);
+        if (vc > 0) drain_phase(bar(T::KB_V_FULL), (vc - 1) & 1u, ctl.limit_ns);
+        if (n0 > 0) drain_phase(bar(T::KB_QD_FULL), (n0 - 1) & 1u, ctl.limit_ns);
+        if (n1 > 0) drain_phase(bar(T::KB_QD_FULL + 1), (n1 - 1) & 1u, ctl.limit_ns);
     }
 }
 
@@ -187,52 +211,84 @@ __device__ void wide_kv_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0
     constexpr uint32_t HI = ptx::smem_desc_hi(8 * T::SW, T::SWIZZLE_CODE);
     const uint32_t k_lo = ptx::smem_desc_lo(sbase + T::KV_OFF_K, 16);
     const uint32_t v_lo = ptx::smem_desc_lo(sbase + T::KV_OFF_V, 16);
-    const uint32_t q_lo = ptx::smem_desc_lo(sbase + T::KV_OFF_Q, 16);
-    const uint32_t do_lo = ptx::smem_desc_lo(sbase + T::KV_OFF_DO, 16);
-    const uint32_t qmn_lo = ptx::smem_desc_lo(sbase + T::KV_OFF_Q, 64 * T::SW);    // LBO: next 64-column chunk
-    const uint32_t domn_lo = ptx::smem_desc_lo(sbase + T::KV_OFF_DO, 64 * T::SW);
-    uint32_t uc = 0, t = 0, acc = 0;
+    auto q_lo = [&](uint32_t b) { return ptx::smem_desc_lo(sbase + T::kv_q(b), 16); };
+    auto do_lo = [&](uint32_t b) { return ptx::smem_desc_lo(sbase + T::kv_do(b), 16); };
+    // MN-major views (LBO: the next 64-column chunk, 64 rows on)
+    auto qmn_lo = [&](uint32_t b) { return ptx::smem_desc_lo(sbase + T::kv_q(b), 64 * T::SW); };
+    auto domn_lo = [&](uint32_t b) { return ptx::smem_desc_lo(sbase + T::kv_do(b), 64 * T::SW); };
+    uint32_t uc = 0, acc = 0, n0 = 0, n1 = 0;  // fills of slots 0 and 1 consumed
     bool ok = true;
+    // Sᵀ = K Qᵀ of the step in slot b into TMEM block tm, K = 256 in 16 steps
+    auto issue_s = [&](uint32_t b, uint32_t tm) {
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk)
+            ptx::mma_ss(tmem + tm, ptx::desc64(k_lo + wide_kmaj(kk, 128), HI),
+                        ptx::desc64(q_lo(b) + wide_kmaj(kk, 64), HI), ID_S, kk > 0 ? 1u : 0u);
+    };
+    // acc += (Pᵀ or dSᵀ in TMEM block a) times (dO or Q of slot b); its
+    // commit frees the slot and the block.  s: the step's place in its pass.
+    auto accumulate = [&](uint32_t a, uint32_t b_lo, uint32_t b, int s, int steps) -> bool {
+        if (s == 0 && acc > 0 && !wait_phase(bar(T::KB_ACC_FREE), (acc - 1) & 1u, ctl, SITE_B_ACC_FREE)) return false;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            ptx::mma_ts(tmem + T::TM_ACC, tmem + a + kk * 8, ptx::desc64(b_lo + ((kk * 16 * T::SW) >> 4), HI), ID_ACC,
+                        (s > 0 || kk > 0) ? 1u : 0u);
+        ptx::tc_commit(bar(T::KB_QD_EMPTY + b));  // the step's Q, dO and TMEM block free
+        if (s == steps - 1) {
+            ptx::tc_commit(bar(T::KB_ACC_FULL));  // dV (dV pass) or dK (dK pass) of the unit complete
+            ++acc;
+        }
+        return true;
+    };
     for (int pos = blockIdx.x; ok && unit_at<CAUSAL>(pos) < p.nunits; pos += gridDim.x) {
         const BwdUnit w = bwd_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
         if (w.nsteps == 0) continue;
-        if (!wait_phase(bar(T::KB_KV_FULL), uc & 1u, ctl, SITE_B_KV_FULL)) { ok = false; break; }
+        if (!wait_phase(bar(T::KB_K_FULL), uc & 1u, ctl, SITE_B_KV_FULL)) { ok = false; break; }
         const int steps = 2 * w.nsteps;
-        for (int pass = 0; ok && pass < 2; ++pass) {
-            for (int s = 0; s < steps; ++s, ++t) {
-                if (!wait_phase(bar(T::KB_QD_FULL), t & 1u, ctl, SITE_B_QD_FULL)) { ok = false; break; }
+        // dV pass: step s + 1's Sᵀ goes to the tensor core before step s's
+        // accumulation (which waits for the softmax).  Its slot and TMEM
+        // block were freed by step s - 1's accumulation, which the copies of
+        // step s + 1 (QD_FULL) already waited for.
+        int pend = -1;          // the step whose accumulation is still to issue
+        uint32_t pend_n = 0;    // its fill count
+        for (int s = 0; s <= steps && ok; ++s) {
+            if (s < steps) {
+                const uint32_t b = (uint32_t)s & 1u, nb = b ? n1++ : n0++;
+                if (!wait_phase(bar(T::KB_QD_FULL + b), nb & 1u, ctl, SITE_B_QD_FULL)) { ok = false; break; }
                 ptx::tc_fence_after();
-                // Sᵀ = K Qᵢᵀ (and dPᵀ = V dOᵢᵀ in the dK pass), K = 256 in 16 steps
-#pragma unroll
-                for (int kk = 0; kk < 16; ++kk)
-                    ptx::mma_ss(tmem + T::TM_S, ptx::desc64(k_lo + wide_kmaj(kk, 128), HI),
-                                ptx::desc64(q_lo + wide_kmaj(kk, 64), HI), ID_S, kk > 0 ? 1u : 0u);
-                if (pass == 1) {
-#pragma unroll
-                    for (int kk = 0; kk < 16; ++kk)
-                        ptx::mma_ss(tmem + T::TM_DP, ptx::desc64(v_lo + wide_kmaj(kk, 128), HI),
-                                    ptx::desc64(do_lo + wide_kmaj(kk, 64), HI), ID_S, kk > 0 ? 1u : 0u);
-                }
-                ptx::tc_commit(bar(T::KB_S_FULL));
-                if (!wait_phase(bar(T::KB_P_FULL), t & 1u, ctl, SITE_B_P_FULL)) { ok = false; break; }
-                // the accumulator of this pass: free once the epilogue has read the previous one
-                if (s == 0 && acc > 0 && !wait_phase(bar(T::KB_ACC_FREE), (acc - 1) & 1u, ctl, SITE_B_ACC_FREE)) {
+                issue_s(b, T::tm_slot(b));
+                ptx::tc_commit(bar(T::KB_S_FULL + b));
+            }
+            if (pend >= 0) {
+                const uint32_t b = (uint32_t)pend & 1u;
+                if (!wait_phase(bar(T::KB_P_FULL + b), pend_n & 1u, ctl, SITE_B_P_FULL) ||
+                    !accumulate(T::tm_slot(b), domn_lo(b), b, pend, steps)) {
                     ok = false;
                     break;
                 }
-                ptx::tc_fence_after();
-                // dV += Pᵀ dOᵢ (pass 0) or dK += dSᵀ Qᵢ (pass 1): 64 queries in 4 K steps
-                const uint32_t a_tmem = tmem + (pass == 0 ? T::TM_S : T::TM_DP);
-                const uint32_t b_lo = pass == 0 ? domn_lo : qmn_lo;
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    ptx::mma_ts(tmem + T::TM_ACC, a_tmem + kk * 8, ptx::desc64(b_lo + ((kk * 16 * T::SW) >> 4), HI),
-                                ID_ACC, (s > 0 || kk > 0) ? 1u : 0u);
-                ptx::tc_commit(bar(T::KB_QD_EMPTY));  // the step's Q, dO and TMEM blocks free
             }
-            if (!ok) break;
-            ptx::tc_commit(bar(T::KB_ACC_FULL));  // dV (pass 0) or dK (pass 1) of the unit complete
-            ++acc;
+            pend = s;
+            pend_n = s < steps ? (((uint32_t)s & 1u) ? n1 : n0) - 1 : 0;
+        }
+        if (!ok) break;
+        // dK pass in slot 0: needs V, loaded over slot 1 after the dV pass
+        if (!wait_phase(bar(T::KB_V_FULL), uc & 1u, ctl, SITE_B_KV_FULL)) { ok = false; break; }
+        for (int s = 0; s < steps; ++s) {
+            const uint32_t nb = n0++;
+            if (!wait_phase(bar(T::KB_QD_FULL), nb & 1u, ctl, SITE_B_QD_FULL)) { ok = false; break; }
+            ptx::tc_fence_after();
+            issue_s(0, T::TM_S);
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk)
+                ptx::mma_ss(tmem + T::TM_DP, ptx::desc64(v_lo + wide_kmaj(kk, 128), HI),
+                            ptx::desc64(do_lo(0) + wide_kmaj(kk, 64), HI), ID_S, kk > 0 ? 1u : 0u);
+            ptx::tc_commit(bar(T::KB_S_FULL));
+            if (!wait_phase(bar(T::KB_P_FULL), nb & 1u, ctl, SITE_B_P_FULL) ||
+                !accumulate(T::TM_DP, qmn_lo(0), 0, s, steps)) {
+                ok = false;
+                break;
+            }
         }
         if (!ok) break;
         ptx::tc_commit(bar(T::KB_KV_EMPTY));
@@ -243,9 +299,10 @@ __device__ void wide_kv_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0
     drain_phase(bar(T::KB_DRAIN), 0u, ctl.limit_ns);
 }
 
-// Thread = key (TMEM lane).  dV pass: Pᵀ over the first 32 columns of Sᵀ;
-// dK pass: Pᵀ in registers, dSᵀ = Pᵀ ∘ (dPᵀ − Δ) over the first 32 columns
-// of dPᵀ.  P and dS are rounded to the input type (the products' operands).
+// Thread = key (TMEM lane).  dV pass: Pᵀ over the first 32 columns of the
+// step's Sᵀ block; dK pass: Pᵀ in registers, dSᵀ = Pᵀ ∘ (dPᵀ − Δ) over the
+// first 32 columns of dPᵀ.  P and dS are rounded to the input type (the
+// products' operands).
 template <bool CAUSAL, bool BF16>
 __device__ void wide_kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar0, uint32_t tmem, const Ctl& ctl) {
     using T = WideTraits;
@@ -254,36 +311,38 @@ __device__ void wide_kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar
     const int row = quad * 32 + threadIdx.x % 32;  // key within the block
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
     const float c = p.scale_log2;
-    const uint32_t lse_a = sbase + T::KV_OFF_LSE, del_a = sbase + T::KV_OFF_DELTA;
-    uint32_t t = 0;
+    uint32_t n0 = 0, n1 = 0;  // fills of slots 0 and 1 consumed
     for (int pos = blockIdx.x; unit_at<CAUSAL>(pos) < p.nunits; pos += gridDim.x) {
         const BwdUnit w = bwd_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
         const int key = w.j * 128 + row;
         const int steps = 2 * w.nsteps;
         for (int pass = 0; pass < 2; ++pass) {
-            for (int s = 0; s < steps; ++s, ++t) {
+            for (int s = 0; s < steps; ++s) {
+                const uint32_t b = pass == 0 ? (uint32_t)s & 1u : 0u, ph = (b ? n1++ : n0++) & 1u;
                 int hq, r0;
                 wide_step(w, s, p, hq, r0);
                 // lse2 and Δ of the step's queries arrive with Qᵢ (TMA); the
                 // slot is refilled only after this step's P_FULL
-                if (!warp_wait_phase(bar(T::KB_QD_FULL), t & 1u, ctl, SITE_B_QD_FULL)) return;
-                if (!warp_wait_phase(bar(T::KB_S_FULL), t & 1u, ctl, SITE_B_S_FULL)) return;
+                if (!warp_wait_phase(bar(T::KB_QD_FULL + b), ph, ctl, SITE_B_QD_FULL)) return;
+                if (!warp_wait_phase(bar(T::KB_S_FULL + b), ph, ctl, SITE_B_S_FULL)) return;
                 ptx::tc_fence_after();
+                const uint32_t lse_a = sbase + T::KV_OFF_LSE + b * 256u, del_a = sbase + T::KV_OFF_DELTA + b * 256u;
+                const uint32_t tm_s = pass == 0 ? T::tm_slot(b) : T::TM_S;
                 // causal: only the diagonal block has keys after queries (key > query -> P = 0)
                 const bool diag = CAUSAL && r0 / 128 == w.j;
                 float pf[64];
                 {
-                    uint32_t a[32], b[32];
-                    ptx::tmem_ld32_issue(tmem + lane_addr + T::TM_S, a);
-                    ptx::tmem_ld32_issue(tmem + lane_addr + T::TM_S + 32, b);
+                    uint32_t a[32], bb[32];
+                    ptx::tmem_ld32_issue(tmem + lane_addr + tm_s, a);
+                    ptx::tmem_ld32_issue(tmem + lane_addr + tm_s + 32, bb);
                     ptx::tmem_wait_ld();
                     ptx::reg_fence32(a);
-                    ptx::reg_fence32(b);
+                    ptx::reg_fence32(bb);
 #pragma unroll
                     for (int x = 0; x < 64; x += 2) {
                         float l0, l1;
                         asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(l0), "=f"(l1) : "r"(lse_a + 4u * x));
-                        const uint32_t u0 = x < 32 ? a[x] : b[x - 32], u1 = x < 32 ? a[x + 1] : b[x - 31];
+                        const uint32_t u0 = x < 32 ? a[x] : bb[x - 32], u1 = x < 32 ? a[x + 1] : bb[x - 31];
                         float e0 = fmaf(__uint_as_float(u0), c, -l0);
                         float e1 = fmaf(__uint_as_float(u1), c, -l1);
                         if (diag && key > r0 + x) e0 = -INFINITY;
@@ -296,29 +355,29 @@ __device__ void wide_kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar
 #pragma unroll
                 for (int x = 0; x < 32; ++x) pk[x] = pack2<BF16>(pf[2 * x], pf[2 * x + 1]);
                 if (pass == 0) {
-                    ptx::tmem_st32(tmem + lane_addr + T::TM_S, pk);
+                    ptx::tmem_st32(tmem + lane_addr + tm_s, pk);
                 } else {
-                    uint32_t a[32], b[32];
+                    uint32_t a[32], bb[32];
                     ptx::tmem_ld32_issue(tmem + lane_addr + T::TM_DP, a);
-                    ptx::tmem_ld32_issue(tmem + lane_addr + T::TM_DP + 32, b);
+                    ptx::tmem_ld32_issue(tmem + lane_addr + T::TM_DP + 32, bb);
                     ptx::tmem_wait_ld();
                     ptx::reg_fence32(a);
-                    ptx::reg_fence32(b);
+                    ptx::reg_fence32(bb);
                     uint32_t ds[32];
 #pragma unroll
                     for (int x = 0; x < 32; ++x) {
                         float d0, d1;
                         asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(d0), "=f"(d1) : "r"(del_a + 8u * x));
                         const float2 pp = unpack2<BF16>(pk[x]);  // dS uses the rounded P
-                        const uint32_t u0 = 2 * x < 32 ? a[2 * x] : b[2 * x - 32];
-                        const uint32_t u1 = 2 * x < 32 ? a[2 * x + 1] : b[2 * x - 31];
+                        const uint32_t u0 = 2 * x < 32 ? a[2 * x] : bb[2 * x - 32];
+                        const uint32_t u1 = 2 * x < 32 ? a[2 * x + 1] : bb[2 * x - 31];
                         ds[x] = pack2<BF16>(pp.x * (__uint_as_float(u0) - d0), pp.y * (__uint_as_float(u1) - d1));
                     }
                     ptx::tmem_st32(tmem + lane_addr + T::TM_DP, ds);
                 }
                 ptx::tmem_wait_st();
                 ptx::tc_fence_before();
-                ptx::mbar_arrive(bar(T::KB_P_FULL));
+                ptx::mbar_arrive(bar(T::KB_P_FULL + b));
             }
         }
     }
