@@ -894,6 +894,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     p.delta = reinterpret_cast<float*>(ws + row_bytes);
     p.status = info->status;
     p.wait_limit_ns = wait_limit_ns();
+    p.inject_stall = g_inject_stall.load();
 
     // operand loads: 128-row boxes; at D = 256 the kernel moves 64-row steps
     // (and its resident 128-row tiles as two boxes)

@@ -235,16 +235,21 @@ __device__ void kv_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, cons
     const uint64_t pol_q = ptx::policy_evict_last();    // read by every key block
     uint32_t uc = 0, t = 0;
     bool ok = true;
+    bool withheld = false;
     for (int pos = blockIdx.x; ok && unit_at<CAUSAL>(pos) < p.nunits; pos += gridDim.x) {
         const BwdUnit w = bwd_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
         if (w.nsteps == 0) continue;
         if (uc > 0 && !wait_phase(bar(T::KB_KV_EMPTY), (uc - 1) & 1u, ctl, SITE_B_KV_EMPTY)) { ok = false; break; }
-        ptx::mbar_arrive_expect_tx(bar(T::KB_KV_FULL), 2 * T::TILE);
-        for (int c = 0; c < T::NCHUNK; ++c) {
-            ptx::tma_load_4d(sbase + T::KV_OFF_K + c * (128 * T::SW), tmK, bar(T::KB_KV_FULL), c * T::SWE, w.j * 128,
-                             w.hk, w.z, pol_kv);
-            ptx::tma_load_4d(sbase + T::KV_OFF_V + c * (128 * T::SW), tmV, bar(T::KB_KV_FULL), c * T::SWE, w.j * 128,
-                             w.hk, w.z, pol_kv);
+        if (p.inject_stall && blockIdx.x == 0 && uc == 0) {
+            withheld = true;  // never issued: the issuer's wait for K, V must time out
+        } else {
+            ptx::mbar_arrive_expect_tx(bar(T::KB_KV_FULL), 2 * T::TILE);
+            for (int c = 0; c < T::NCHUNK; ++c) {
+                ptx::tma_load_4d(sbase + T::KV_OFF_K + c * (128 * T::SW), tmK, bar(T::KB_KV_FULL), c * T::SWE,
+                                 w.j * 128, w.hk, w.z, pol_kv);
+                ptx::tma_load_4d(sbase + T::KV_OFF_V + c * (128 * T::SW), tmV, bar(T::KB_KV_FULL), c * T::SWE,
+                                 w.j * 128, w.hk, w.z, pol_kv);
+            }
         }
         ++uc;
         for (int s = 0; s < w.nsteps; ++s, ++t) {
@@ -269,8 +274,9 @@ __device__ void kv_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, cons
         }
     }
     if (!ok) {
-        // let the copies in flight land before shared memory goes away
-        if (uc > 0) drain_phase(bar(T::KB_KV_FULL), (uc - 1) & 1u, ctl.limit_ns);
+        // let the copies in flight land before shared memory goes away (the
+        // withheld copy never completes; its wait simply runs out)
+        if (uc > 0) drain_phase(bar(T::KB_KV_FULL), (uc - 1) & 1u, withheld && uc == 1 ? ctl.limit_ns / 64 : ctl.limit_ns);
         for (uint32_t x = t > 2u ? t - 2u : 0u; x < t; ++x)
             drain_phase(bar(T::KB_QD_FULL + (x & 1u)), (x >> 1) & 1u, ctl.limit_ns);
     }

@@ -159,6 +159,7 @@ __device__ void wide_kv_producer(const CUtensorMap* tmK, const CUtensorMap* tmV,
     const uint64_t pol_q = ptx::policy_evict_last();
     uint32_t uc = 0, vc = 0, n0 = 0, n1 = 0;  // fills of slots 0 and 1
     bool ok = true;
+    bool withheld = false;
     // Q, dO, lse2, Δ of step s into slot b, once that slot's previous step is done
     auto fill = [&](const BwdUnit& w, int s, uint32_t b) -> bool {
         const uint32_t nb = b ? n1 : n0;
@@ -181,8 +182,12 @@ __device__ void wide_kv_producer(const CUtensorMap* tmK, const CUtensorMap* tmV,
         if (w.nsteps == 0) continue;
         // K and the V region (slot 1, then V) are free once the previous unit is done
         if (uc > 0 && !wait_phase(bar(T::KB_KV_EMPTY), (uc - 1) & 1u, ctl, SITE_B_KV_EMPTY)) { ok = false; break; }
-        ptx::mbar_arrive_expect_tx(bar(T::KB_K_FULL), T::TILE128);
-        wide_load128(sbase + T::KV_OFF_K, tmK, bar(T::KB_K_FULL), w.j * 128, w.hk, w.z, pol_kv);
+        if (p.inject_stall && blockIdx.x == 0 && uc == 0) {
+            withheld = true;  // never issued: the issuer's wait for K must time out
+        } else {
+            ptx::mbar_arrive_expect_tx(bar(T::KB_K_FULL), T::TILE128);
+            wide_load128(sbase + T::KV_OFF_K, tmK, bar(T::KB_K_FULL), w.j * 128, w.hk, w.z, pol_kv);
+        }
         ++uc;
         const int steps = 2 * w.nsteps;  // >= 2: slot 1 is filled at least once
         for (int s = 0; ok && s < steps; ++s) ok = fill(w, s, (uint32_t)s & 1u);
@@ -195,7 +200,8 @@ __device__ void wide_kv_producer(const CUtensorMap* tmK, const CUtensorMap* tmV,
         for (int s = 0; ok && s < steps; ++s) ok = fill(w, s, 0u);
     }
     if (!ok) {
-        if (uc > 0) drain_phase(bar(T::KB_K_FULL), (uc - 1) & 1u, ctl.limit_ns);
+        // (the withheld copy never completes; its wait simply runs out)
+        if (uc > 0) drain_phase(bar(T::KB_K_FULL), (uc - 1) & 1u, withheld && uc == 1 ? ctl.limit_ns / 64 : ctl.limit_ns);
         if (vc > 0) drain_phase(bar(T::KB_V_FULL), (vc - 1) & 1u, ctl.limit_ns);
         if (n0 > 0) drain_phase(bar(T::KB_QD_FULL), (n0 - 1) & 1u, ctl.limit_ns);
         if (n1 > 0) drain_phase(bar(T::KB_QD_FULL + 1), (n1 - 1) & 1u, ctl.limit_ns);

@@ -132,6 +132,7 @@ struct BwdParams {
     float* delta;            // (Z, Hq, Tq * 128) fp32
     uint32_t* status;
     uint64_t wait_limit_ns;
+    int inject_stall;        // test hook: 1 = withhold CTA 0's first K/V copy of the dK/dV phase
 };
 
 }  // namespace fa

@@ -422,7 +422,8 @@ fa_status fa_fwd_schedule(int Z, int Hq, int Hkv, int Nq, int Nkv, int D, int ca
  *   1 wherever the kernel applies, 2 never.  It takes precedence over
  *   fa_debug_force_chains.  The same result up to the order of rounding.
  * fa_debug_inject_stall -- when enabled, CTA 0 of later launches never issues
- *   the copy of its first K tile, so the wait for it runs out: the kernel
+ *   the copy of its first K tile (forward kernels) or of its first unit's K
+ *   and V (fa_bwd's dK/dV phase), so the wait for it runs out: the kernel
  *   records FA_ERR_DEVICE_TIMEOUT (read with fa_device_status), every role of
  *   that CTA stops, in-flight copies and MMAs land, TMEM is freed and the
  *   kernel returns.  The other CTAs finish their tiles.  Outputs of such a

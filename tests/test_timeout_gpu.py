@@ -71,3 +71,37 @@ def test_withheld_copy_times_out_on_cta_pairs():
     finally:
         fa.fa_debug_force_pair(0)
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("D", [128, 256])
+def test_withheld_copy_times_out_in_the_backward(D):
+    # fa_bwd's dK/dV phase (the D <= 128 kernel and the D = 256 kernel): CTA 0
+    # withholds its first unit's K (and V); the MMA issuer's wait runs out,
+    # every role of that CTA stops (the dQ phase is skipped), in-flight copies
+    # land, TMEM is freed, and the next backward is correct
+    import torch
+
+    import exact_attention_44_gb300 as fa
+    from test_bwd_gpu import check_bwd
+    fa.build()
+    q, k, v = (si.as_torch(x, "bf16").cuda() for x in si.qkv(25, 1, 4, 4, 512, 512, D, "bf16"))
+    do = si.as_torch(si.normals(26, 0, q.numel(), "bf16").reshape(tuple(q.shape)), "bf16").cuda()
+    o, lse = fa.fa_fwd(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status()[0] == fa.FA_OK
+    fa.fa_debug_set_wait_limit_ms(100)
+    fa.fa_debug_inject_stall(True)
+    try:
+        fa.fa_bwd(q, k, v, o, lse, do, causal=True)
+        code, word = fa.fa_device_status()
+    finally:
+        fa.fa_debug_inject_stall(False)
+        fa.fa_debug_set_wait_limit_ms(0)
+    assert code == fa.FA_ERR_DEVICE_TIMEOUT, hex(word)
+    assert word & 0xFF == fa.FA_ERR_DEVICE_TIMEOUT
+    assert (word >> 16) == 0           # CTA 0 gave up first
+    assert 20 <= (word >> 8) & 0xFF <= 32  # a backward wait site
+    assert fa.fa_device_status() == (fa.FA_OK, 0)
+    check_bwd(24, 1, 2, 1, 300, 300, D, "bf16", True)
+    assert fa.fa_device_status() == (fa.FA_OK, 0)
+    torch.cuda.synchronize()
