@@ -223,6 +223,37 @@ __device__ __forceinline__ DqUnit dq_unit(int u, const BwdParams& p) {
     return w;
 }
 
+// Debug builds (FA_DEBUG_CHECKS=1): every role checks each unit it decodes
+// against the launch's sizes before touching memory for it, as the forward's
+// roles do; a unit outside them records FA_ERR_DEVICE_CHECK with the role's
+// site and raises the CTA's abort flag, so the kernel ends through the same
+// path as a timed-out wait.  Other builds compile the checks away.
+__device__ __forceinline__ bool bwd_check_failed(const Ctl& c, uint32_t site) {
+    *c.abort_flag = 1;
+    atomicCAS(c.status, 0u, STATUS_DEVICE_CHECK | (site << 8) | ((blockIdx.x & 0xFFFFu) << 16));
+    return false;
+}
+__device__ __forceinline__ bool unit_checked(const BwdUnit& w, const BwdParams& p, const Ctl& c, uint32_t site) {
+    if constexpr (!FA_DEBUG_CHECKS) {
+        return true;
+    } else {
+        // the unit's query blocks are i0 .. Tq - 1 of each query head of the group
+        const bool ok = w.z >= 0 && w.z < p.Z && w.hk >= 0 && w.hk < p.Hkv && w.j >= 0 && w.j < p.Tk &&
+                        w.i0 >= 0 && w.per_head >= 0 && (w.per_head == 0 || w.i0 + w.per_head == p.Tq) &&
+                        w.nsteps == w.per_head * p.group;
+        return ok || bwd_check_failed(c, site);
+    }
+}
+__device__ __forceinline__ bool unit_checked(const DqUnit& w, const BwdParams& p, const Ctl& c, uint32_t site) {
+    if constexpr (!FA_DEBUG_CHECKS) {
+        return true;
+    } else {
+        const bool ok = w.z >= 0 && w.z < p.Z && w.hq >= 0 && w.hq < p.Hq && w.hk == w.hq / p.group &&
+                        w.hk < p.Hkv && w.i >= 0 && w.i < p.Tq && w.nkv >= 1 && w.nkv <= p.Tk;
+        return ok || bwd_check_failed(c, site);
+    }
+}
+
 // ================================================================ dK / dV ===
 
 template <int D, bool CAUSAL>
@@ -238,6 +269,7 @@ __device__ void kv_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, cons
     bool withheld = false;
     for (int pos = blockIdx.x; ok && unit_at<CAUSAL>(pos) < p.nunits; pos += gridDim.x) {
         const BwdUnit w = bwd_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_LOAD)) { ok = false; break; }
         if (w.nsteps == 0) continue;
         if (uc > 0 && !wait_phase(bar(T::KB_KV_EMPTY), (uc - 1) & 1u, ctl, SITE_B_KV_EMPTY)) { ok = false; break; }
         if (p.inject_stall && blockIdx.x == 0 && uc == 0) {
@@ -311,6 +343,7 @@ __device__ void kv_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0, uin
     bool ok = true;
     for (int pos = blockIdx.x; ok && unit_at<CAUSAL>(pos) < p.nunits; pos += gridDim.x) {
         const BwdUnit w = bwd_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_MMA)) { ok = false; break; }
         if (w.nsteps == 0) continue;
         if (!wait_phase(bar(T::KB_KV_FULL), uc & 1u, ctl, SITE_B_KV_FULL)) { ok = false; break; }
         if (!issue_s(t)) { ok = false; break; }
@@ -370,6 +403,7 @@ __device__ void kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar0, ui
     uint32_t t = 0;
     for (int pos = blockIdx.x; unit_at<CAUSAL>(pos) < p.nunits; pos += gridDim.x) {
         const BwdUnit w = bwd_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_SOFTMAX)) return;
         for (int s = 0; s < w.nsteps; ++s, ++t) {
             const uint32_t st = t & 1u;
             int hq, i;
@@ -446,6 +480,10 @@ __device__ void kv_epilogue(const CUtensorMap* tmDK, const CUtensorMap* tmDV, co
     uint32_t uc = 0;
     for (int pos = blockIdx.x; unit_at<CAUSAL>(pos) < p.nunits; pos += gridDim.x) {
         const BwdUnit w = bwd_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_EPILOGUE)) {
+            drain();
+            return;
+        }
         const int key = w.j * 128 + row;
         uint8_t* dk_row = reinterpret_cast<uint8_t*>(p.dk) +
                           2 * ((int64_t)w.z * p.sdk_z + (int64_t)w.hk * p.sdk_h + (int64_t)key * p.sdk_n);
@@ -509,6 +547,7 @@ __device__ void q_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const
     bool ok = true;
     for (int pos = first; ok && unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x) {
         const DqUnit w = dq_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_LOAD)) { ok = false; break; }
         if (uc > 0 && !wait_phase(bar(T::QB_QD_EMPTY), (uc - 1) & 1u, ctl, SITE_B_QD_EMPTY)) { ok = false; break; }
         ptx::mbar_arrive_expect_tx(bar(T::QB_QD_FULL), 2 * T::TILE);
         for (int c = 0; c < T::NCHUNK; ++c) {
@@ -576,6 +615,7 @@ __device__ void q_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0, uint
     bool ok = true;
     for (int pos = first; ok && unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x) {
         const DqUnit w = dq_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_MMA)) { ok = false; break; }
         if (!wait_phase(bar(T::QB_QD_FULL), uc & 1u, ctl, SITE_B_QD_FULL)) { ok = false; break; }
         if (!issue_s(g)) { ok = false; break; }
         issue_dp(g);
@@ -620,6 +660,7 @@ __device__ void q_softmax(const BwdParams& p, uint32_t bar0, uint32_t tmem, int 
     uint32_t g = 0;
     for (int pos = first; unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x) {
         const DqUnit w = dq_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_SOFTMAX)) return;
         const int64_t r = ((int64_t)w.z * p.Hq + w.hq) * p.Tq * 128 + (int64_t)w.i * 128 + row;
         const float l2 = __ldg(p.lse2 + r), dl = __ldg(p.delta + r);
         for (int j = 0; j < w.nkv; ++j, ++g) {
@@ -681,6 +722,10 @@ __device__ void q_epilogue(const CUtensorMap* tmDQ, const BwdParams& p, uint32_t
     uint32_t uc = 0;
     for (int pos = first; unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x, ++uc) {
         const DqUnit w = dq_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_EPILOGUE)) {
+            drain();
+            return;
+        }
         if (!warp_wait_phase(bar(T::QB_DQ_FULL), uc & 1u, ctl, SITE_B_DQ_FULL)) {
             drain();
             return;

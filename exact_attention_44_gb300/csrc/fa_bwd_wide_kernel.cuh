@@ -179,6 +179,7 @@ __device__ void wide_kv_producer(const CUtensorMap* tmK, const CUtensorMap* tmV,
     };
     for (int pos = blockIdx.x; ok && unit_at<CAUSAL>(pos) < p.nunits; pos += gridDim.x) {
         const BwdUnit w = bwd_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_LOAD)) { ok = false; break; }
         if (w.nsteps == 0) continue;
         // K and the V region (slot 1, then V) are free once the previous unit is done
         if (uc > 0 && !wait_phase(bar(T::KB_KV_EMPTY), (uc - 1) & 1u, ctl, SITE_B_KV_EMPTY)) { ok = false; break; }
@@ -249,6 +250,7 @@ __device__ void wide_kv_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0
     };
     for (int pos = blockIdx.x; ok && unit_at<CAUSAL>(pos) < p.nunits; pos += gridDim.x) {
         const BwdUnit w = bwd_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_MMA)) { ok = false; break; }
         if (w.nsteps == 0) continue;
         if (!wait_phase(bar(T::KB_K_FULL), uc & 1u, ctl, SITE_B_KV_FULL)) { ok = false; break; }
         const int steps = 2 * w.nsteps;
@@ -320,6 +322,7 @@ __device__ void wide_kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar
     uint32_t n0 = 0, n1 = 0;  // fills of slots 0 and 1 consumed
     for (int pos = blockIdx.x; unit_at<CAUSAL>(pos) < p.nunits; pos += gridDim.x) {
         const BwdUnit w = bwd_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_SOFTMAX)) return;
         const int key = w.j * 128 + row;
         const int steps = 2 * w.nsteps;
         for (int pass = 0; pass < 2; ++pass) {
@@ -406,6 +409,10 @@ __device__ void wide_kv_epilogue(const CUtensorMap* tmDK, const CUtensorMap* tmD
     uint32_t acc = 0;
     for (int pos = blockIdx.x; unit_at<CAUSAL>(pos) < p.nunits; pos += gridDim.x) {
         const BwdUnit w = bwd_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_EPILOGUE)) {
+            drain();
+            return;
+        }
         const int key = w.j * 128 + row;
         if (w.nsteps == 0) {
             if (key < p.Nkv) {
@@ -451,6 +458,7 @@ __device__ void wide_q_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, 
     bool ok = true;
     for (int pos = first; ok && unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x) {
         const DqUnit w = dq_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_LOAD)) { ok = false; break; }
         if (uc > 0 && !wait_phase(bar(T::QB_QD_EMPTY), (uc - 1) & 1u, ctl, SITE_B_QD_EMPTY)) { ok = false; break; }
         ptx::mbar_arrive_expect_tx(bar(T::QB_QD_FULL), 2 * T::TILE128);
         wide_load128(sbase + T::Q_OFF_Q, tmQ, bar(T::QB_QD_FULL), w.i * 128, w.hq, w.z, pol_q);
@@ -488,6 +496,7 @@ __device__ void wide_q_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0,
     bool ok = true;
     for (int pos = first; ok && unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x) {
         const DqUnit w = dq_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_MMA)) { ok = false; break; }
         if (!wait_phase(bar(T::QB_QD_FULL), uc & 1u, ctl, SITE_B_QD_FULL)) { ok = false; break; }
         const int steps = 2 * w.nkv;
         for (int s = 0; s < steps; ++s, ++g) {
@@ -538,6 +547,7 @@ __device__ void wide_q_softmax(const BwdParams& p, uint32_t bar0, uint32_t tmem,
     uint32_t g = 0;
     for (int pos = first; unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x) {
         const DqUnit w = dq_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_SOFTMAX)) return;
         const int64_t r = ((int64_t)w.z * p.Hq + w.hq) * p.Tq * 128 + (int64_t)w.i * 128 + row;
         const float l2 = __ldg(p.lse2 + r), dl = __ldg(p.delta + r);
         const int q = w.i * 128 + row;
@@ -593,6 +603,10 @@ __device__ void wide_q_epilogue(const CUtensorMap* tmDQ, const BwdParams& p, uin
     uint32_t uc = 0;
     for (int pos = first; unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x, ++uc) {
         const DqUnit w = dq_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_EPILOGUE)) {
+            drain();
+            return;
+        }
         if (!warp_wait_phase(bar(T::QB_DQ_FULL), uc & 1u, ctl, SITE_B_DQ_FULL)) {
             drain();
             return;

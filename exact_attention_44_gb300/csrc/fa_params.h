@@ -55,6 +55,10 @@ enum WaitSite : uint32_t {
     SITE_CHECK_MMA_PV = 43,
     SITE_CHECK_SOFTMAX = 44,
     SITE_CHECK_EPILOGUE = 45,
+    SITE_CHECK_BWD_LOAD = 46,       // backward roles: TMA producer, MMA issuer, softmax, epilogue
+    SITE_CHECK_BWD_MMA = 47,
+    SITE_CHECK_BWD_SOFTMAX = 48,
+    SITE_CHECK_BWD_EPILOGUE = 49,
 };
 
 // Status code of a failed debug index check (FA_ERR_DEVICE_CHECK in fa.h).

@@ -1,12 +1,13 @@
 """The debug-check build of libfa (FA_DEBUG_CHECKS=1): every role of the
-forward kernels checks each unit it decodes against the launch's sizes
-before touching memory for it, records FA_ERR_DEVICE_CHECK and stops if one
-is outside them (no trap, no device assert).
+forward and backward kernels checks each unit it decodes against the
+launch's sizes before touching memory for it, records FA_ERR_DEVICE_CHECK
+and stops if one is outside them (no trap, no device assert).
 
 CPU: the variant builds and exports the same C ABI.  GPU: every launch mode
 of the forward (whole tiles with one and two softmax chains, causal and not,
 the split schedule and its merge, window / ALiBi / packed variable-length
-variants, GQA packing) runs through the checking kernels with a clean status
+variants, GQA packing) and the backward (the D <= 128 and D = 256 kernels,
+causal and not, GQA) runs through the checking kernels with a clean status
 and the same results as the oracle -- the checks never fire on valid work.
 No test plants a bad index on the GPU: an unchecked bad index is the kind of
 fault these GPUs are shared too widely to risk."""
@@ -51,6 +52,12 @@ def test_checking_kernels_run_clean_on_every_launch_mode():
             check_full(41, 1, 2, 2, 700, 900, 128, "bf16", False)
         fa.fa_debug_force_chains(0)
         check_full(42, 1, 2, 1, 260, 260, 256, "bf16", True)
+        # the backward's roles check their dK/dV and dQ units (D <= 128 and D = 256 kernels)
+        from test_bwd_gpu import check_bwd
+        check_bwd(46, 2, 4, 2, 300, 300, 64, "fp16", True)
+        check_bwd(46, 1, 4, 1, 200, 400, 128, "bf16", False)
+        check_bwd(46, 1, 2, 2, 260, 260, 256, "bf16", True)
+        assert fa.fa_device_status() == (fa.FA_OK, 0)
         check_full(43, 1, 8, 2, 3, 2000, 128, "bf16", False)  # GQA packing
         fa.fa_debug_force_split(1)
         try:
