@@ -79,6 +79,12 @@ def load(source: str | None = None, tag: str = "") -> ctypes.CDLL:
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_double, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+            lib.oracle_attention_bwd_ex.restype = ctypes.c_int
+            lib.oracle_attention_bwd_ex.argtypes = [
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_double, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
             lib.oracle_lse_merge.restype = ctypes.c_int
             lib.oracle_lse_merge.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
                                              ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
@@ -236,4 +242,35 @@ def attention_bwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, do: np.ndarray, d
         raise ValueError("oracle_attention_bwd: invalid arguments")
     if rc != 0:
         raise MemoryError("oracle_attention_bwd: out of memory")
+    return dq, dk, dv
+
+
+def attention_bwd_ex(q: np.ndarray, k: np.ndarray, v: np.ndarray, do: np.ndarray, dtype: str, scale: float,
+                     causal: bool, window=(-1, -1), alibi=None, nthreads: int | None = None,
+                     lib: ctypes.CDLL | None = None):
+    """Gradients (dq, dk, dv) of attention_fwd_ex's window / ALiBi forward (dense tensors), float64.
+
+    window: (left, right), -1 for an open side; alibi: Hq slopes or None.
+    q, do: (Z, Hq, Nq, D); k, v: (Z, Hkv, Nkv, D) uint16 bit arrays of dtype.
+    """
+    lib = lib or load()
+    q, k, v, do = (np.ascontiguousarray(x, dtype=np.uint16) for x in (q, k, v, do))
+    Z, Hq, Nq, D = q.shape
+    Zk, Hkv, Nkv, Dk = k.shape
+    if v.shape != k.shape or do.shape != q.shape or Zk != Z or Dk != D:
+        raise ValueError("shape mismatch")
+    slopes = None if alibi is None else np.ascontiguousarray(alibi, dtype=np.float64)
+    if slopes is not None and slopes.shape != (Hq,):
+        raise ValueError("alibi takes one slope per query head")
+    dq = np.zeros(q.shape, dtype=np.float64)
+    dk = np.zeros(k.shape, dtype=np.float64)
+    dv = np.zeros(k.shape, dtype=np.float64)
+    rc = lib.oracle_attention_bwd_ex(q.ctypes.data, k.ctypes.data, v.ctypes.data, do.ctypes.data, DTYPES[dtype], Z,
+                                     Hq, Hkv, Nq, Nkv, D, float(scale), int(bool(causal)), int(window[0]),
+                                     int(window[1]), None if slopes is None else slopes.ctypes.data, dq.ctypes.data,
+                                     dk.ctypes.data, dv.ctypes.data, nthreads or host_threads())
+    if rc == -1:
+        raise ValueError("oracle_attention_bwd_ex: invalid arguments")
+    if rc != 0:
+        raise MemoryError("oracle_attention_bwd_ex: out of memory")
     return dq, dk, dv

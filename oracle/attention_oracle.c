@@ -523,3 +523,134 @@ int oracle_attention_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v
     free(jobs); free(tid); free(created); free(table); free(buf);
     return status;
 }
+
+
+/*
+ * Backward of the attention forward with the window and ALiBi variants
+ * (oracle_attention_fwd_ex's readings, dense (Z, H, N, D) tensors): the same
+ * steps as oracle_attention_bwd, over each row's kept keys [lo, hi) and with
+ * the scaled score s_ij = scale q_i . k_j - slope[hq] |i - j|.  The bias is
+ * constant in q, k and v, so the softmax Jacobian and the gradient formulas
+ * are those of the plain backward; a row with no kept key contributes
+ * nothing (its O is 0).
+ */
+typedef struct {
+    const double *q, *k, *v, *dO;
+    int Z, Hq, Hkv, Nq, Nkv, D;
+    double scale;
+    int causal, window_left, window_right;
+    const double* alibi;             /* (Hq) slopes or NULL */
+    double *dq, *dk, *dv;
+    int64_t begin, end;
+    int status;
+} oracle_bwd_ex_job;
+
+static void* oracle_bwd_ex_worker(void* arg) {
+    oracle_bwd_ex_job* J = (oracle_bwd_ex_job*)arg;
+    const int D = J->D, g = J->Hq / J->Hkv;
+    double* se = (double*)malloc(sizeof(double) * (size_t)J->Nkv);
+    double* dpe = (double*)malloc(sizeof(double) * (size_t)J->Nkv);
+    if (!se || !dpe) { J->status = -2; free(se); free(dpe); return NULL; }
+    for (int64_t grp = J->begin; grp < J->end; ++grp) {
+        const int z = (int)(grp / J->Hkv), hk = (int)(grp % J->Hkv);
+        const int64_t kvoff = ((int64_t)z * J->Hkv + hk) * J->Nkv * D;
+        const double* kb = J->k + kvoff;
+        const double* vb = J->v + kvoff;
+        double* dkb = J->dk + kvoff;
+        double* dvb = J->dv + kvoff;
+        for (int64_t x = 0; x < (int64_t)J->Nkv * D; ++x) { dkb[x] = 0.0; dvb[x] = 0.0; }
+        for (int hq = hk * g; hq < hk * g + g; ++hq) {
+            const int64_t qoff = ((int64_t)z * J->Hq + hq) * J->Nq * D;
+            const double slope = J->alibi ? J->alibi[hq] : 0.0;
+            for (int64_t i = 0; i < J->Nq; ++i) {
+                const double* qr = J->q + qoff + i * D;
+                const double* gr = J->dO + qoff + i * D;
+                double* dqr = J->dq + qoff + i * D;
+                for (int d = 0; d < D; ++d) dqr[d] = 0.0;
+                int64_t klo = 0, khi = J->Nkv;  /* kept keys [klo, khi) */
+                if (J->causal && i + 1 < khi) khi = i + 1;
+                if (J->window_right >= 0 && i + J->window_right + 1 < khi) khi = i + J->window_right + 1;
+                if (J->window_left >= 0 && i - J->window_left > klo) klo = i - J->window_left;
+                if (klo >= khi) continue;
+                double Mr = -INFINITY;
+                for (int64_t j = klo; j < khi; ++j) {
+                    double dotk = 0.0;
+                    for (int d = 0; d < D; ++d) dotk += qr[d] * kb[j * D + d];
+                    const double gap = (double)(i > j ? i - j : j - i);
+                    se[j] = J->scale * dotk - slope * gap;
+                    Mr = se[j] > Mr ? se[j] : Mr;
+                }
+                double Lr = 0.0;
+                for (int64_t j = klo; j < khi; ++j) Lr += exp(se[j] - Mr);
+                double rsum = 0.0;  /* sum_k P_ik dP_ik */
+                for (int64_t j = klo; j < khi; ++j) {
+                    const double pe = exp(se[j] - Mr) / Lr;
+                    double dov = 0.0;
+                    for (int d = 0; d < D; ++d) dov += gr[d] * vb[j * D + d];
+                    dpe[j] = dov;
+                    rsum += pe * dov;
+                    for (int d = 0; d < D; ++d) dvb[j * D + d] += pe * gr[d];
+                }
+                for (int64_t j = klo; j < khi; ++j) {
+                    const double pe = exp(se[j] - Mr) / Lr;
+                    const double dse = pe * (dpe[j] - rsum);
+                    for (int d = 0; d < D; ++d) {
+                        dqr[d] += J->scale * dse * kb[j * D + d];
+                        dkb[j * D + d] += J->scale * dse * qr[d];
+                    }
+                }
+            }
+        }
+    }
+    free(se);
+    free(dpe);
+    return NULL;
+}
+
+/*
+ * The backward with window_left/window_right (-1: an open side) and ALiBi
+ * slopes (Hq values, or NULL), tensors as for oracle_attention_bwd.
+ * Returns 0, -1 for invalid arguments, -2 when memory runs out.
+ */
+int oracle_attention_bwd_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* dO, int dtype,
+                            int Z, int Hq, int Hkv, int Nq, int Nkv, int D, double scale, int causal,
+                            int window_left, int window_right, const double* alibi, double* dq, double* dk,
+                            double* dv, int nthreads) {
+    if (dtype < 0 || dtype > 1 || Z < 0 || Hq < 1 || Hkv < 1 || Nq < 0 || Nkv < 1 || D < 1) return -1;
+    if (Hq % Hkv != 0 || !isfinite(scale) || window_left < -1 || window_right < -1) return -1;
+    const int64_t nq = (int64_t)Z * Hq * Nq * D, nk = (int64_t)Z * Hkv * Nkv * D;
+    if (nk == 0) return 0;
+    double* table = (double*)malloc(sizeof(double) * 65536);
+    double* buf = (double*)malloc(sizeof(double) * (size_t)(2 * nq + 2 * nk + 1));
+    if (!table || !buf) { free(table); free(buf); return -2; }
+    for (int b = 0; b < 65536; ++b) table[b] = oracle_decode((uint16_t)b, dtype);
+    double *qd = buf, *gd = buf + nq, *kd = buf + 2 * nq, *vd = buf + 2 * nq + nk;
+    for (int64_t x = 0; x < nq; ++x) { qd[x] = table[q[x]]; gd[x] = table[dO[x]]; }
+    for (int64_t x = 0; x < nk; ++x) { kd[x] = table[k[x]]; vd[x] = table[v[x]]; }
+
+    const int64_t groups = (int64_t)Z * Hkv;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 512) nthreads = 512;
+    if (nthreads > groups) nthreads = (int)groups;
+    oracle_bwd_ex_job* jobs = (oracle_bwd_ex_job*)calloc((size_t)nthreads, sizeof(oracle_bwd_ex_job));
+    pthread_t* tid = (pthread_t*)calloc((size_t)nthreads, sizeof(pthread_t));
+    int* created = (int*)calloc((size_t)nthreads, sizeof(int));
+    if (!jobs || !tid || !created) { free(jobs); free(tid); free(created); free(table); free(buf); return -2; }
+    const int64_t chunk = (groups + nthreads - 1) / nthreads;
+    for (int t = 0; t < nthreads; ++t) {
+        oracle_bwd_ex_job* J = &jobs[t];
+        *J = (oracle_bwd_ex_job){qd, kd, vd, gd, Z, Hq, Hkv, Nq, Nkv, D, scale, causal, window_left, window_right,
+                                 alibi, dq, dk, dv, (int64_t)t * chunk,
+                                 (int64_t)t * chunk + chunk < groups ? (int64_t)t * chunk + chunk : groups, 0};
+        if (J->begin >= J->end) continue;
+        if (nthreads > 1 && pthread_create(&tid[t], NULL, oracle_bwd_ex_worker, J) == 0) created[t] = 1;
+        else oracle_bwd_ex_worker(J);
+    }
+    int status = 0;
+    for (int t = 0; t < nthreads; ++t) {
+        if (created[t]) pthread_join(tid[t], NULL);
+        if (jobs[t].status) status = jobs[t].status;
+    }
+    free(jobs); free(tid); free(created); free(table); free(buf);
+    return status;
+}

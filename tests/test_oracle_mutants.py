@@ -59,6 +59,16 @@ MUTANTS = {
     "bwd score scale dropped": ("sc[j] = J->scale * qk;", "sc[j] = qk;"),
     "bwd dp uses q": ("for (int d = 0; d < D; ++d) acc += gi[d] * vh[j * D + d];",
                       "for (int d = 0; d < D; ++d) acc += qi[d] * vh[j * D + d];"),
+    "bwd ex alibi sign": ("se[j] = J->scale * dotk - slope * gap;", "se[j] = J->scale * dotk + slope * gap;"),
+    "bwd ex window left off by one": ("if (J->window_left >= 0 && i - J->window_left > klo) klo = i - J->window_left;",
+                                      "if (J->window_left >= 0 && i - J->window_left + 1 > klo) klo = i - J->window_left + 1;"),
+    "bwd ex window right dropped": ("if (J->window_right >= 0 && i + J->window_right + 1 < khi) khi = i + J->window_right + 1;",
+                                    "if (0 && i + J->window_right + 1 < khi) khi = i + J->window_right + 1;"),
+    "bwd ex causal dropped": ("if (J->causal && i + 1 < khi) khi = i + 1;", "if (0 && i + 1 < khi) khi = i + 1;"),
+    "bwd ex softmax jacobian": ("const double dse = pe * (dpe[j] - rsum);", "const double dse = pe * dpe[j];"),
+    "bwd ex dk uses k": ("dkb[j * D + d] += J->scale * dse * qr[d];", "dkb[j * D + d] += J->scale * dse * kb[j * D + d];"),
+    "bwd ex slope head": ("const double slope = J->alibi ? J->alibi[hq] : 0.0;\n            for (int64_t i = 0; i < J->Nq; ++i) {\n                const double* qr",
+                          "const double slope = J->alibi ? J->alibi[hk] : 0.0;\n            for (int64_t i = 0; i < J->Nq; ++i) {\n                const double* qr"),
     "variant causal dropped": ("if (J->causal && i + 1 < hi) hi = i + 1;", "if (0 && i + 1 < hi) hi = i + 1;"),
 }
 
@@ -87,6 +97,11 @@ PIN_CALLS = [
     ("bwd fd", lambda: pins.test_bwd_matches_finite_differences("bf16", True, (2, 4, 2, 9, 6, 4))),
     ("bwd single key", pins.test_bwd_single_key_closed_form),
     ("bwd scale zero", pins.test_bwd_scale_zero_closed_form),
+    ("bwd ex fd", lambda: pins.test_bwd_ex_matches_finite_differences("bf16", True, (3, -1), [0.5, 0.125],
+                                                                      (1, 2, 2, 8, 10, 4))),
+    ("bwd ex fd window", lambda: pins.test_bwd_ex_matches_finite_differences("fp16", False, (-1, 2),
+                                                                             [0.25, 1.0, 0.0, 0.75], (2, 4, 2, 7, 6, 8))),
+    ("bwd ex diagonal", pins.test_bwd_ex_diagonal_window_closed_form),
 ]
 
 

@@ -509,3 +509,93 @@ def test_bwd_causal_first_row_has_no_query_gradient():
     do = si.normals(120, 0, q.size, "fp16").reshape(q.shape)
     dq, _, _ = oracle.attention_bwd(q, k, v, do, "fp16", 0.7, True)
     assert np.all(dq[:, :, 0] == 0) and np.any(dq[:, :, 1] != 0)
+
+
+# ------------------------------------------------------- backward, variants ----
+# The window / ALiBi backward (attention_bwd_ex): without a variant it is the
+# plain backward bit for bit; it matches central finite differences of an
+# independent float64 forward with the same readings (numpy + scipy: kept keys
+# i - left <= j <= i + right, causal j <= i, bias -slope |i - j|, a row with no
+# kept key O = 0); and a window of the diagonal alone is a closed form.
+
+def _np_forward_ex(Q, K, V, scale, causal, window, alibi):
+    from scipy.special import softmax
+    Z, Hq, Nq, D = Q.shape
+    g = Hq // K.shape[1]
+    Nkv = K.shape[2]
+    i = np.arange(Nq)[:, None]
+    j = np.arange(Nkv)[None, :]
+    keep = np.ones((Nq, Nkv), dtype=bool)
+    if causal:
+        keep &= j <= i
+    if window[0] >= 0:
+        keep &= j >= i - window[0]
+    if window[1] >= 0:
+        keep &= j <= i + window[1]
+    O = np.zeros_like(Q)
+    for z in range(Z):
+        for h in range(Hq):
+            S = scale * Q[z, h] @ K[z, h // g].T
+            if alibi is not None:
+                S = S - alibi[h] * np.abs(i - j)
+            S = np.where(keep, S, -np.inf)
+            rows = keep.any(axis=1)
+            P = np.zeros_like(S)
+            P[rows] = softmax(S[rows], axis=1)
+            O[z, h] = P @ V[z, h // g]
+    return O
+
+
+@pytest.mark.parametrize("dtype,causal", [("fp16", False), ("bf16", True)])
+def test_bwd_ex_without_variants_is_the_plain_backward(dtype, causal):
+    q, k, v = si.qkv(121, 2, 4, 2, 13, 11, 16, dtype)
+    do = si.normals(122, 0, q.size, dtype).reshape(q.shape)
+    plain = oracle.attention_bwd(q, k, v, do, dtype, 0.5, causal)
+    ex = oracle.attention_bwd_ex(q, k, v, do, dtype, 0.5, causal, window=(-1, -1), alibi=None)
+    for a, b in zip(plain, ex):
+        assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("dtype,causal,window,alibi,shape", [
+    ("fp16", False, (2, 1), None, (1, 2, 1, 9, 9, 8)),
+    ("bf16", True, (3, -1), [0.5, 0.125], (1, 2, 2, 8, 10, 4)),
+    ("fp16", False, (-1, 2), [0.25, 1.0, 0.0, 0.75], (2, 4, 2, 7, 6, 8)),
+    ("fp16", True, (1, -1), None, (1, 2, 1, 12, 5, 4)),      # rows past the keys keep none
+])
+def test_bwd_ex_matches_finite_differences(dtype, causal, window, alibi, shape):
+    Z, Hq, Hkv, Nq, Nkv, D = shape
+    scale = 0.6
+    slopes = None if alibi is None else np.asarray(alibi, dtype=np.float64)
+    q, k, v = si.qkv(123, Z, Hq, Hkv, Nq, Nkv, D, dtype)
+    do = si.normals(124, 0, q.size, dtype).reshape(q.shape)
+    dq, dk, dv = oracle.attention_bwd_ex(q, k, v, do, dtype, scale, causal, window=window, alibi=slopes)
+    Q, K, V, G = (_np_decode(x, dtype) for x in (q, k, v, do))
+
+    def loss(Qx, Kx, Vx):
+        return float(np.sum(G * _np_forward_ex(Qx, Kx, Vx, scale, causal, window, slopes)))
+
+    rng = np.random.default_rng(8)
+    h = 1e-5
+    for name, X, grad in (("q", Q, dq), ("k", K, dk), ("v", V, dv)):
+        for _ in range(12):
+            idx = tuple(int(rng.integers(n)) for n in X.shape)
+            Xp, Xm = X.copy(), X.copy()
+            Xp[idx] += h
+            Xm[idx] -= h
+            args_p = {"q": (Xp, K, V), "k": (Q, Xp, V), "v": (Q, K, Xp)}[name]
+            args_m = {"q": (Xm, K, V), "k": (Q, Xm, V), "v": (Q, K, Xm)}[name]
+            fd = (loss(*args_p) - loss(*args_m)) / (2 * h)
+            assert abs(fd - grad[idx]) <= 1e-7 * max(1.0, abs(fd)), (name, idx, fd, grad[idx])
+
+
+def test_bwd_ex_diagonal_window_closed_form():
+    # window (0, 0): each query keeps only key i, so O_i = v_i, P = 1 there:
+    # dV_i = dO_i (summed over the group's query heads), dS = 0, so dQ = dK = 0;
+    # queries past the keys keep nothing
+    q, k, v = si.qkv(125, 1, 4, 2, 9, 7, 8, "bf16")
+    do = si.normals(126, 0, q.size, "bf16").reshape(q.shape)
+    dq, dk, dv = oracle.attention_bwd_ex(q, k, v, do, "bf16", 0.8, False, window=(0, 0), alibi=[0.3, 0.1, 0.0, 2.0])
+    G = _np_decode(do, "bf16")
+    assert np.all(dq == 0.0) and np.all(dk == 0.0)
+    want = np.stack([G[0, 0:2, :7].sum(axis=0), G[0, 2:4, :7].sum(axis=0)])[None]
+    np.testing.assert_allclose(dv, want, rtol=0, atol=1e-12)
