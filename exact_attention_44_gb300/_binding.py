@@ -39,6 +39,9 @@ _SIGNATURES = {
     "fa_bwd": (ctypes.c_int, [ctypes.c_void_p] * 9 + [ctypes.c_int] * 6 + [ctypes.c_void_p] * 8 +
                [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "fa_bwd_workspace_size": (ctypes.c_int, [ctypes.c_int] * 4 + [ctypes.POINTER(ctypes.c_size_t)]),
+    "fa_bwd_ex": (ctypes.c_int, [ctypes.c_void_p] * 9 + [ctypes.c_int] * 6 + [ctypes.c_void_p] * 8 +
+                  [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                   ctypes.c_void_p]),
     "fa_fwd_ex": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_void_p] + [ctypes.c_int] * 6 +
                   [ctypes.c_void_p] * 4 + [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                             ctypes.c_void_p]),
@@ -271,6 +274,27 @@ def fa_bwd(q, k, v, o, lse, do, dq=None, dk=None, dv=None, *, scale: float | Non
     do: upstream gradient shaped like o.  Outputs are allocated when omitted;
     workspace (CUDA uint8, >= fa_bwd_workspace_size bytes) likewise.
     """
+    return _bwd(q, k, v, o, lse, do, dq, dk, dv, scale, causal, workspace, stream, None)
+
+
+def fa_bwd_ex(q, k, v, o, lse, do, dq=None, dk=None, dv=None, *, scale: float | None = None, causal: bool = False,
+              window=(-1, -1), alibi_slopes=None, workspace=None, stream=None):
+    """Gradients of fa_fwd_ex's window / ALiBi forward (libfa's fa_bwd_ex; dense tensors, D <= 128).
+
+    Arguments as for fa_bwd, plus window (left, right), -1 for an open side, and
+    alibi_slopes (CUDA fp32 (Hq,) or None), the options the forward took.
+    """
+    import torch
+
+    Hq = q.shape[1]
+    if alibi_slopes is not None and (alibi_slopes.dtype != torch.float32 or alibi_slopes.numel() != Hq):
+        raise ValueError("alibi_slopes must be float32 with Hq entries")
+    opt = fa_fwd_options(int(window[0]), int(window[1]),
+                         alibi_slopes.data_ptr() if alibi_slopes is not None else None, None, None, 0)
+    return _bwd(q, k, v, o, lse, do, dq, dk, dv, scale, causal, workspace, stream, opt)
+
+
+def _bwd(q, k, v, o, lse, do, dq, dk, dv, scale, causal, workspace, stream, opt):
     import torch
 
     Z, Hq, Nq, D = q.shape
@@ -294,12 +318,17 @@ def fa_bwd(q, k, v, o, lse, do, dq=None, dk=None, dv=None, *, scale: float | Non
         stream = torch.cuda.current_stream(q.device)
     st = [_strides(x) for x in (q, k, v, o, do, dq, dk, dv)]
     with torch.cuda.device(q.device):
-        rc = load().fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(),
-                           dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), Z, Hq, Hkv, Nq, Nkv, D,
-                           *[ctypes.byref(x) for x in st], float(scale), int(bool(causal)), dt, workspace.data_ptr(),
-                           workspace.numel() * workspace.element_size(), ctypes.c_void_p(stream.cuda_stream))
+        lib = load()
+        args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(), dq.data_ptr(),
+                dk.data_ptr(), dv.data_ptr(), Z, Hq, Hkv, Nq, Nkv, D, *[ctypes.byref(x) for x in st], float(scale),
+                int(bool(causal)), dt)
+        ws = (workspace.data_ptr(), workspace.numel() * workspace.element_size(), ctypes.c_void_p(stream.cuda_stream))
+        if opt is None:
+            rc, name = lib.fa_bwd(*args, *ws), "fa_bwd"
+        else:
+            rc, name = lib.fa_bwd_ex(*args, ctypes.byref(opt), *ws), "fa_bwd_ex"
     if rc != FA_OK:
-        raise FaError(rc, "fa_bwd")
+        raise FaError(rc, name)
     return dq, dk, dv
 
 

@@ -820,11 +820,15 @@ fa_status fa_bwd_workspace_size(int Z, int Hq, int Nq, int D, size_t* bytes) {
     return FA_OK;
 }
 
-fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
-                 void* dq, void* dk, void* dv, int Z, int Hq, int Hkv, int Nq, int Nkv, int D, const fa_strides* sq,
-                 const fa_strides* sk, const fa_strides* sv, const fa_strides* so, const fa_strides* sdo,
-                 const fa_strides* sdq, const fa_strides* sdk, const fa_strides* sdv, float scale, int causal,
-                 fa_dtype dtype, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+// The backward, plain (variant 0) or with the window / ALiBi options of
+// fa_bwd_ex (variant 1: window; 2: window and ALiBi; head dims up to 128).
+static fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                          const void* dO, void* dq, void* dk, void* dv, int Z, int Hq, int Hkv, int Nq, int Nkv, int D,
+                          const fa_strides* sq, const fa_strides* sk, const fa_strides* sv, const fa_strides* so,
+                          const fa_strides* sdo, const fa_strides* sdq, const fa_strides* sdk,
+                          const fa_strides* sdv, float scale, int causal, fa_dtype dtype, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream, int variant, int win_left, int win_right,
+                          const float* alibi) {
     fa_status st = check_shape(Z, Hq, Hkv, Nq, Nkv, D, causal);
     if (st != FA_OK) return st;
     if (!supported_head_dim(D)) return FA_ERR_UNSUPPORTED;
@@ -895,6 +899,9 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     p.status = info->status;
     p.wait_limit_ns = wait_limit_ns();
     p.inject_stall = g_inject_stall.load();
+    p.win_left = win_left;
+    p.win_right = win_right;
+    p.alibi = alibi;
 
     // operand loads: 128-row boxes; at D = 256 the kernel moves 64-row steps
     // (and its resident 128-row tiles as two boxes)
@@ -925,13 +932,45 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     const bool bf16 = dtype == FA_DTYPE_BF16;
     cudaError_t err;
     switch (D) {
-        case 16: err = fa::launch_bwd_d16(a, causal != 0, bf16); break;
-        case 32: err = fa::launch_bwd_d32(a, causal != 0, bf16); break;
-        case 64: err = fa::launch_bwd_d64(a, causal != 0, bf16); break;
-        case 128: err = fa::launch_bwd_d128(a, causal != 0, bf16); break;
-        default: err = fa::launch_bwd_d256(a, causal != 0, bf16); break;
+        case 16: err = fa::launch_bwd_d16(a, causal != 0, bf16, variant); break;
+        case 32: err = fa::launch_bwd_d32(a, causal != 0, bf16, variant); break;
+        case 64: err = fa::launch_bwd_d64(a, causal != 0, bf16, variant); break;
+        case 128: err = fa::launch_bwd_d128(a, causal != 0, bf16, variant); break;
+        default: err = fa::launch_bwd_d256(a, causal != 0, bf16, variant); break;
     }
     return err == cudaSuccess ? FA_OK : cuda_fail("backward launch", err);
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                 void* dq, void* dk, void* dv, int Z, int Hq, int Hkv, int Nq, int Nkv, int D, const fa_strides* sq,
+                 const fa_strides* sk, const fa_strides* sv, const fa_strides* so, const fa_strides* sdo,
+                 const fa_strides* sdq, const fa_strides* sdk, const fa_strides* sdv, float scale, int causal,
+                 fa_dtype dtype, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, Z, Hq, Hkv, Nq, Nkv, D, sq, sk, sv, so, sdo, sdq, sdk, sdv, scale,
+                    causal, dtype, workspace, workspace_bytes, stream, 0, -1, -1, nullptr);
+}
+
+fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                    void* dq, void* dk, void* dv, int Z, int Hq, int Hkv, int Nq, int Nkv, int D,
+                    const fa_strides* sq, const fa_strides* sk, const fa_strides* sv, const fa_strides* so,
+                    const fa_strides* sdo, const fa_strides* sdq, const fa_strides* sdk, const fa_strides* sdv,
+                    float scale, int causal, fa_dtype dtype, const fa_fwd_options* options, void* workspace,
+                    size_t workspace_bytes, cudaStream_t stream) {
+    const fa_fwd_options none = {-1, -1, nullptr, nullptr, nullptr, 0};
+    const fa_fwd_options* opt = options != nullptr ? options : &none;
+    if (opt->window_left < -1 || opt->window_right < -1) return FA_ERR_INVALID_ARG;
+    if (opt->cu_seqlens_q != nullptr || opt->cu_seqlens_k != nullptr) return FA_ERR_UNSUPPORTED;
+    if (opt->alibi_slopes != nullptr && reinterpret_cast<uintptr_t>(opt->alibi_slopes) % 4 != 0)
+        return FA_ERR_ALIGNMENT;
+    // a window side longer than every query-key distance is open
+    const int64_t reach_all = (int64_t)Nq + Nkv;
+    const auto open = [&](int w) { return w < 0 || (int64_t)w > reach_all; };
+    const int wl = open(opt->window_left) ? -1 : opt->window_left;
+    const int wr = open(opt->window_right) ? -1 : opt->window_right;
+    const int variant = opt->alibi_slopes != nullptr ? 2 : (wl >= 0 || wr >= 0) ? 1 : 0;
+    if (variant != 0 && D > 128) return FA_ERR_UNSUPPORTED;
+    return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, Z, Hq, Hkv, Nq, Nkv, D, sq, sk, sv, so, sdo, sdq, sdk, sdv, scale,
+                    causal, dtype, workspace, workspace_bytes, stream, variant, wl, wr, opt->alibi_slopes);
 }
 
 fa_status fa_fwd_splitkv_workspace_size_for(int D, int num_sms, size_t* bytes) {

@@ -14,14 +14,15 @@
 
 namespace fa {
 
-template <bool CAUSAL, bool BF16>
+template <bool CAUSAL, bool BF16, int VAR>
 static cudaError_t launch_one(const BwdLaunchArgs& a) {
     constexpr int D = FA_HEAD_DIM;
 #if FA_HEAD_DIM == 256
+    static_assert(VAR == 0, "no backward variants at head dim 256");
     auto bwd = fa_bwd_wide_kernel<CAUSAL, BF16>;
     constexpr int SMEM = WideTraits::SMEM_BYTES, THREADS = WIDE_THREADS;
 #else
-    auto bwd = fa_bwd_kernel<D, CAUSAL, BF16>;
+    auto bwd = fa_bwd_kernel<D, CAUSAL, BF16, VAR>;
     constexpr int SMEM = BwdTraits<D>::FUSED_SMEM_BYTES, THREADS = BWD_THREADS;
 #endif
     static std::atomic<uint64_t> configured{0};  // context the opt-in shared memory size was set in
@@ -50,9 +51,23 @@ static cudaError_t launch_one(const BwdLaunchArgs& a) {
 
 #define FA_CAT2(a, b) a##b
 #define FA_CAT(a, b) FA_CAT2(a, b)
-cudaError_t FA_CAT(launch_bwd_d, FA_HEAD_DIM)(const BwdLaunchArgs& a, bool causal, bool bf16) {
-    if (causal) return bf16 ? launch_one<true, true>(a) : launch_one<true, false>(a);
-    return bf16 ? launch_one<false, true>(a) : launch_one<false, false>(a);
+// variant 0: fa_bwd; 1: window (fa_bwd_ex); 2: window and ALiBi (head dims
+// up to 128)
+cudaError_t FA_CAT(launch_bwd_d, FA_HEAD_DIM)(const BwdLaunchArgs& a, bool causal, bool bf16, int variant) {
+#if FA_HEAD_DIM != 256
+    if (variant == 2) {
+        if (causal) return bf16 ? launch_one<true, true, 2>(a) : launch_one<true, false, 2>(a);
+        return bf16 ? launch_one<false, true, 2>(a) : launch_one<false, false, 2>(a);
+    }
+    if (variant == 1) {
+        if (causal) return bf16 ? launch_one<true, true, 1>(a) : launch_one<true, false, 1>(a);
+        return bf16 ? launch_one<false, true, 1>(a) : launch_one<false, false, 1>(a);
+    }
+#else
+    if (variant != 0) return cudaErrorNotSupported;
+#endif
+    if (causal) return bf16 ? launch_one<true, true, 0>(a) : launch_one<true, false, 0>(a);
+    return bf16 ? launch_one<false, true, 0>(a) : launch_one<false, false, 0>(a);
 }
 
 }  // namespace fa

@@ -167,7 +167,10 @@ struct BwdUnit {
     int z, hk, j, i0, per_head, nsteps;
 };
 
-template <bool CAUSAL>
+// Variant kernels (VAR = 1: window, 2: window and ALiBi) visit only the query
+// blocks holding a row that keeps a key of block j: rows j·128 − win_right ..
+// j·128 + 127 + win_left.
+template <bool CAUSAL, int VAR = 0>
 __device__ __forceinline__ BwdUnit bwd_unit(int u, const BwdParams& p) {
     BwdUnit w;
     const int zh = p.Z * p.Hkv, G = p.kv_head_group;
@@ -181,7 +184,18 @@ __device__ __forceinline__ BwdUnit bwd_unit(int u, const BwdParams& p) {
     // causal (top-left): query row r sees keys <= r, so query blocks before
     // the key block's own index see none of its keys
     w.i0 = CAUSAL ? w.j : 0;
-    w.per_head = p.Tq > w.i0 ? p.Tq - w.i0 : 0;
+    int i_end = p.Tq;
+    if constexpr (VAR != 0) {
+        if (p.win_right >= 0) {
+            const int lo_row = w.j * 128 - p.win_right;
+            if (lo_row > 0 && lo_row / 128 > w.i0) w.i0 = lo_row / 128;
+        }
+        if (p.win_left >= 0) {
+            const int64_t hi_block = ((int64_t)w.j * 128 + 127 + p.win_left) / 128 + 1;
+            if (hi_block < i_end) i_end = (int)hi_block;
+        }
+    }
+    w.per_head = i_end > w.i0 ? i_end - w.i0 : 0;
     w.nsteps = w.per_head * p.group;
     return w;
 }
@@ -195,12 +209,15 @@ __device__ __forceinline__ void bwd_step(const BwdUnit& w, int s, const BwdParam
 // CTAs running together share a head's K/V.  Causal: heads in groups of
 // p.q_head_group (the group's K/V within a third of L2), and within a group
 // the last query block (most key blocks) first, heads innermost.  It sees
-// key blocks 0 .. nkv - 1.
+// key blocks j0 .. j0 + nkv - 1 (j0 = 0 but in the variant kernels, whose
+// window bounds the blocks: keys i·128 − win_left .. i·128 + 127 +
+// win_right; a block whose rows keep no key at all still takes one key
+// block, every pair of it masked, and ends with dQ = 0).
 struct DqUnit {
-    int z, hq, hk, i, nkv;
+    int z, hq, hk, i, j0, nkv;
 };
 
-template <bool CAUSAL>
+template <bool CAUSAL, int VAR = 0>
 __device__ __forceinline__ DqUnit dq_unit(int u, const BwdParams& p) {
     DqUnit w;
     const int heads = p.Z * p.Hq;
@@ -219,8 +236,42 @@ __device__ __forceinline__ DqUnit dq_unit(int u, const BwdParams& p) {
     w.z = head / p.Hq;
     w.hq = head % p.Hq;
     w.hk = w.hq / p.group;
+    w.j0 = 0;
     w.nkv = CAUSAL ? (w.i + 1 < p.Tk ? w.i + 1 : p.Tk) : p.Tk;
+    if constexpr (VAR != 0) {
+        int jlo = 0, jhi = w.nkv;
+        if (p.win_left >= 0) {
+            const int lo_key = w.i * 128 - p.win_left;
+            jlo = lo_key > 0 ? lo_key / 128 : 0;
+        }
+        if (p.win_right >= 0) {
+            const int64_t hi_block = ((int64_t)w.i * 128 + 127 + p.win_right) / 128 + 1;
+            if (hi_block < jhi) jhi = (int)hi_block;
+        }
+        if (jlo >= jhi) {
+            jlo = jlo < p.Tk - 1 ? jlo : p.Tk - 1;
+            jhi = jlo + 1;
+        }
+        w.j0 = jlo;
+        w.nkv = jhi - jlo;
+    }
     return w;
+}
+
+// Variant kernels: whether query q drops key k, for d = q − k (the top-left
+// causal rule and the window sides of fa_fwd_ex; a key past the keys is
+// dropped too: with a window a row may keep none of the real keys, and its
+// lse is then −inf), and whether a whole 128 × 128 block of differences
+// d_min .. d_max with keys below k_end is kept.
+template <bool CAUSAL>
+__device__ __forceinline__ bool var_dropped(int d, int k, const BwdParams& p) {
+    return k >= p.Nkv || (CAUSAL && d < 0) || (p.win_left >= 0 && d > p.win_left) ||
+           (p.win_right >= 0 && -d > p.win_right);
+}
+template <bool CAUSAL>
+__device__ __forceinline__ bool var_block_kept(int d_min, int d_max, int k_end, const BwdParams& p) {
+    return k_end <= p.Nkv && (!CAUSAL || d_min >= 0) && (p.win_left < 0 || d_max <= p.win_left) &&
+           (p.win_right < 0 || -d_min <= p.win_right);
 }
 
 // Debug builds (FA_DEBUG_CHECKS=1): every role checks each unit it decodes
@@ -239,7 +290,7 @@ __device__ __forceinline__ bool unit_checked(const BwdUnit& w, const BwdParams& 
     } else {
         // the unit's query blocks are i0 .. Tq - 1 of each query head of the group
         const bool ok = w.z >= 0 && w.z < p.Z && w.hk >= 0 && w.hk < p.Hkv && w.j >= 0 && w.j < p.Tk &&
-                        w.i0 >= 0 && w.per_head >= 0 && (w.per_head == 0 || w.i0 + w.per_head == p.Tq) &&
+                        w.i0 >= 0 && w.per_head >= 0 && (w.per_head == 0 || w.i0 + w.per_head <= p.Tq) &&
                         w.nsteps == w.per_head * p.group;
         return ok || bwd_check_failed(c, site);
     }
@@ -249,14 +300,14 @@ __device__ __forceinline__ bool unit_checked(const DqUnit& w, const BwdParams& p
         return true;
     } else {
         const bool ok = w.z >= 0 && w.z < p.Z && w.hq >= 0 && w.hq < p.Hq && w.hk == w.hq / p.group &&
-                        w.hk < p.Hkv && w.i >= 0 && w.i < p.Tq && w.nkv >= 1 && w.nkv <= p.Tk;
+                        w.hk < p.Hkv && w.i >= 0 && w.i < p.Tq && w.j0 >= 0 && w.nkv >= 1 && w.j0 + w.nkv <= p.Tk;
         return ok || bwd_check_failed(c, site);
     }
 }
 
 // ================================================================ dK / dV ===
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, int VAR>
 __device__ void kv_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const CUtensorMap* tmQ,
                             const CUtensorMap* tmDO, const BwdParams& p, uint32_t sbase, uint32_t bar0,
                             const Ctl& ctl) {
@@ -268,7 +319,7 @@ __device__ void kv_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, cons
     bool ok = true;
     bool withheld = false;
     for (int pos = blockIdx.x; ok && unit_at<CAUSAL>(pos) < p.nunits; pos += gridDim.x) {
-        const BwdUnit w = bwd_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        const BwdUnit w = bwd_unit<CAUSAL, VAR>(unit_at<CAUSAL>(pos), p);
         if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_LOAD)) { ok = false; break; }
         if (w.nsteps == 0) continue;
         if (uc > 0 && !wait_phase(bar(T::KB_KV_EMPTY), (uc - 1) & 1u, ctl, SITE_B_KV_EMPTY)) { ok = false; break; }
@@ -318,7 +369,7 @@ __device__ void kv_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, cons
 // issued before it), then dK_t -- so the softmax warps build Pᵀ_{t+1} while
 // the tensor core runs dK_t and dPᵀ_{t+1}.  Products issued by one thread
 // run in order, so a product never overwrites TMEM an earlier one still reads.
-template <int D, bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16, int VAR>
 __device__ void kv_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0, uint32_t tmem, const Ctl& ctl) {
     using T = BwdTraits<D>;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
@@ -342,7 +393,7 @@ __device__ void kv_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0, uin
     uint32_t uc = 0, t = 0;
     bool ok = true;
     for (int pos = blockIdx.x; ok && unit_at<CAUSAL>(pos) < p.nunits; pos += gridDim.x) {
-        const BwdUnit w = bwd_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        const BwdUnit w = bwd_unit<CAUSAL, VAR>(unit_at<CAUSAL>(pos), p);
         if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_MMA)) { ok = false; break; }
         if (w.nsteps == 0) continue;
         if (!wait_phase(bar(T::KB_KV_FULL), uc & 1u, ctl, SITE_B_KV_FULL)) { ok = false; break; }
@@ -392,7 +443,7 @@ __device__ void kv_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0, uin
 // Thread = key (TMEM lane); half h takes queries h*64 .. h*64 + 63 and writes
 // its Pᵀ and dSᵀ (input type, two per column) over its own fp32 columns, so
 // no half overwrites values the other has not read.
-template <int D, bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16, int VAR>
 __device__ void kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar0, uint32_t tmem, int h, const Ctl& ctl) {
     using T = BwdTraits<D>;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
@@ -402,7 +453,7 @@ __device__ void kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar0, ui
     const float c = p.scale_log2;
     uint32_t t = 0;
     for (int pos = blockIdx.x; unit_at<CAUSAL>(pos) < p.nunits; pos += gridDim.x) {
-        const BwdUnit w = bwd_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        const BwdUnit w = bwd_unit<CAUSAL, VAR>(unit_at<CAUSAL>(pos), p);
         if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_SOFTMAX)) return;
         for (int s = 0; s < w.nsteps; ++s, ++t) {
             const uint32_t st = t & 1u;
@@ -416,6 +467,14 @@ __device__ void kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar0, ui
             ptx::tc_fence_after();
             // causal: only the diagonal block has keys after queries (key > query -> 0)
             const bool diag = CAUSAL && i == w.j;
+            // variants: d = query − key = dbase + col; the window and causal
+            // rule drop pairs unless the whole block is kept; ALiBi adds
+            // slope2·|d| (log2 units)
+            const int dbase = (i - w.j) * 128 - row;
+            const bool full =
+                VAR == 0 || var_block_kept<CAUSAL>((i - w.j) * 128 - 127, (i - w.j) * 128 + 127, w.j * 128 + 128, p);
+            const int key = w.j * 128 + row;
+            const float slope2 = VAR == 2 ? -__ldg(p.alibi + hq) * 1.4426950408889634f : 0.f;
             uint32_t pk[32];  // Pᵀ in the input type: the dV operand, and what dS uses
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
@@ -428,8 +487,20 @@ __device__ void kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar0, ui
                     asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(l0), "=f"(l1) : "r"(lse_a + 4u * (32 * cc + 2 * x)));
                     float e0 = fmaf(__uint_as_float(r[2 * x]), c, -l0);
                     float e1 = fmaf(__uint_as_float(r[2 * x + 1]), c, -l1);
-                    if (diag && row > col) e0 = -INFINITY;
-                    if (diag && row > col + 1) e1 = -INFINITY;
+                    if constexpr (VAR == 0) {
+                        if (diag && row > col) e0 = -INFINITY;
+                        if (diag && row > col + 1) e1 = -INFINITY;
+                    } else {
+                        const int d0 = dbase + col;
+                        if constexpr (VAR == 2) {
+                            e0 = fmaf(slope2, fabsf((float)d0), e0);
+                            e1 = fmaf(slope2, fabsf((float)(d0 + 1)), e1);
+                        }
+                        if (!full) {
+                            if (var_dropped<CAUSAL>(d0, key, p)) e0 = -INFINITY;
+                            if (var_dropped<CAUSAL>(d0 + 1, key, p)) e1 = -INFINITY;
+                        }
+                    }
                     pk[16 * cc + x] = pack2<BF16>(ptx::ex2(e0), ptx::ex2(e1));
                 }
             }
@@ -464,7 +535,7 @@ __device__ void kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar0, ui
 
 // Thread = TMEM lane = key: per unit, dK (times scale) and dV are read out,
 // released and stored in the input type; a unit no query sees gets zeros.
-template <int D, bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16, int VAR>
 __device__ void kv_epilogue(const CUtensorMap* tmDK, const CUtensorMap* tmDV, const BwdParams& p, uint32_t sbase,
                             uint32_t bar0, uint32_t tmem, const Ctl& ctl) {
     using T = BwdTraits<D>;
@@ -479,7 +550,7 @@ __device__ void kv_epilogue(const CUtensorMap* tmDK, const CUtensorMap* tmDV, co
     };
     uint32_t uc = 0;
     for (int pos = blockIdx.x; unit_at<CAUSAL>(pos) < p.nunits; pos += gridDim.x) {
-        const BwdUnit w = bwd_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        const BwdUnit w = bwd_unit<CAUSAL, VAR>(unit_at<CAUSAL>(pos), p);
         if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_EPILOGUE)) {
             drain();
             return;
@@ -536,7 +607,7 @@ __device__ __forceinline__ bool bwd_smem_base(uint8_t* raw, int used, int bytes,
 
 // ===================================================================== dQ ===
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, int VAR>
 __device__ void q_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const CUtensorMap* tmQ,
                            const CUtensorMap* tmDO, const BwdParams& p, uint32_t sbase, uint32_t bar0, const Ctl& ctl, int first) {
     using T = BwdTraits<D>;
@@ -546,7 +617,7 @@ __device__ void q_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const
     uint32_t uc = 0, g = 0;
     bool ok = true;
     for (int pos = first; ok && unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x) {
-        const DqUnit w = dq_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        const DqUnit w = dq_unit<CAUSAL, VAR>(unit_at<CAUSAL>(pos), p);
         if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_LOAD)) { ok = false; break; }
         if (uc > 0 && !wait_phase(bar(T::QB_QD_EMPTY), (uc - 1) & 1u, ctl, SITE_B_QD_EMPTY)) { ok = false; break; }
         ptx::mbar_arrive_expect_tx(bar(T::QB_QD_FULL), 2 * T::TILE);
@@ -567,9 +638,9 @@ __device__ void q_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const
             ptx::mbar_arrive_expect_tx(full, 2 * T::TILE);
             for (int c = 0; c < T::NCHUNK; ++c) {
                 ptx::tma_load_4d(sbase + T::Q_OFF_K + st * T::TILE + c * (128 * T::SW), tmK, full, c * T::SWE,
-                                 j * 128, w.hk, w.z, pol_kv);
+                                 (w.j0 + j) * 128, w.hk, w.z, pol_kv);
                 ptx::tma_load_4d(sbase + T::Q_OFF_V + st * T::TILE + c * (128 * T::SW), tmV, full, c * T::SWE,
-                                 j * 128, w.hk, w.z, pol_kv);
+                                 (w.j0 + j) * 128, w.hk, w.z, pol_kv);
             }
         }
     }
@@ -582,7 +653,7 @@ __device__ void q_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const
 
 // Per key block g: S_{g+1} goes to the other TMEM slot while the softmax
 // warps turn S_g and dP_g into dS_g; then dQ += dS_g K_g and dP_{g+1}.
-template <int D, bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16, int VAR>
 __device__ void q_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0, uint32_t tmem, const Ctl& ctl, int first) {
     using T = BwdTraits<D>;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
@@ -614,7 +685,7 @@ __device__ void q_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0, uint
     uint32_t uc = 0, g = 0;
     bool ok = true;
     for (int pos = first; ok && unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x) {
-        const DqUnit w = dq_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        const DqUnit w = dq_unit<CAUSAL, VAR>(unit_at<CAUSAL>(pos), p);
         if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_MMA)) { ok = false; break; }
         if (!wait_phase(bar(T::QB_QD_FULL), uc & 1u, ctl, SITE_B_QD_FULL)) { ok = false; break; }
         if (!issue_s(g)) { ok = false; break; }
@@ -649,7 +720,7 @@ __device__ void q_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0, uint
 
 // Thread = query (TMEM lane); half h takes keys h*64 .. h*64 + 63 of each
 // block.  lse2 and Δ are per row, so they stay in registers for the unit.
-template <int D, bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16, int VAR>
 __device__ void q_softmax(const BwdParams& p, uint32_t bar0, uint32_t tmem, int h, const Ctl& ctl, int first) {
     using T = BwdTraits<D>;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
@@ -659,16 +730,22 @@ __device__ void q_softmax(const BwdParams& p, uint32_t bar0, uint32_t tmem, int 
     const float c = p.scale_log2;
     uint32_t g = 0;
     for (int pos = first; unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x) {
-        const DqUnit w = dq_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        const DqUnit w = dq_unit<CAUSAL, VAR>(unit_at<CAUSAL>(pos), p);
         if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_SOFTMAX)) return;
         const int64_t r = ((int64_t)w.z * p.Hq + w.hq) * p.Tq * 128 + (int64_t)w.i * 128 + row;
         const float l2 = __ldg(p.lse2 + r), dl = __ldg(p.delta + r);
+        const float slope2 = VAR == 2 ? -__ldg(p.alibi + w.hq) * 1.4426950408889634f : 0.f;
         for (int j = 0; j < w.nkv; ++j, ++g) {
             const uint32_t st = g & 1u;
             const uint32_t slot = tmem + lane_addr + T::TM_QS + st * 128;
             if (!warp_wait_phase(bar(T::QB_S_FULL + st), (g >> 1) & 1u, ctl, SITE_B_S_FULL)) return;
             ptx::tc_fence_after();
-            const bool diag = CAUSAL && j == w.i;  // key > query only on the diagonal block
+            const int jj = w.j0 + j;                // the key block
+            const bool diag = CAUSAL && jj == w.i;  // key > query only on the diagonal block
+            // variants: d = query − key = dbase − col (as in the dK/dV phase)
+            const int dbase = (w.i - jj) * 128 + row;
+            const bool full =
+                VAR == 0 || var_block_kept<CAUSAL>((w.i - jj) * 128 - 127, (w.i - jj) * 128 + 127, jj * 128 + 128, p);
             uint32_t pk[32];
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
@@ -679,8 +756,20 @@ __device__ void q_softmax(const BwdParams& p, uint32_t bar0, uint32_t tmem, int 
                     const int col = h * 64 + 32 * cc + 2 * x;
                     float e0 = fmaf(__uint_as_float(rr[2 * x]), c, -l2);
                     float e1 = fmaf(__uint_as_float(rr[2 * x + 1]), c, -l2);
-                    if (diag && col > row) e0 = -INFINITY;
-                    if (diag && col + 1 > row) e1 = -INFINITY;
+                    if constexpr (VAR == 0) {
+                        if (diag && col > row) e0 = -INFINITY;
+                        if (diag && col + 1 > row) e1 = -INFINITY;
+                    } else {
+                        const int d0 = dbase - col;
+                        if constexpr (VAR == 2) {
+                            e0 = fmaf(slope2, fabsf((float)d0), e0);
+                            e1 = fmaf(slope2, fabsf((float)(d0 - 1)), e1);
+                        }
+                        if (!full) {
+                            if (var_dropped<CAUSAL>(d0, jj * 128 + col, p)) e0 = -INFINITY;
+                            if (var_dropped<CAUSAL>(d0 - 1, jj * 128 + col + 1, p)) e1 = -INFINITY;
+                        }
+                    }
                     pk[16 * cc + x] = pack2<BF16>(ptx::ex2(e0), ptx::ex2(e1));
                 }
             }
@@ -707,7 +796,7 @@ __device__ void q_softmax(const BwdParams& p, uint32_t bar0, uint32_t tmem, int 
 }
 
 // Thread = TMEM lane = query: dQ (times scale) read out, released, stored.
-template <int D, bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16, int VAR>
 __device__ void q_epilogue(const CUtensorMap* tmDQ, const BwdParams& p, uint32_t sbase, uint32_t bar0, uint32_t tmem,
                            const Ctl& ctl, int first) {
     using T = BwdTraits<D>;
@@ -721,7 +810,7 @@ __device__ void q_epilogue(const CUtensorMap* tmDQ, const BwdParams& p, uint32_t
     };
     uint32_t uc = 0;
     for (int pos = first; unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x, ++uc) {
-        const DqUnit w = dq_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        const DqUnit w = dq_unit<CAUSAL, VAR>(unit_at<CAUSAL>(pos), p);
         if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_EPILOGUE)) {
             drain();
             return;
@@ -758,7 +847,7 @@ __device__ void q_epilogue(const CUtensorMap* tmDQ, const BwdParams& p, uint32_t
 // waits for another.  The dQ phase's barriers lie in memory the dK/dV phase
 // used for data; they are set up only after every role of that phase has
 // finished: its MMAs drained, its tensor stores read out.
-template <int D, bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16, int VAR>
 __global__ void __launch_bounds__(BWD_THREADS, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
@@ -802,13 +891,13 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     ptx::grid_dependency_wait();
     ptx::grid_launch_dependents();
     if (warp < 8) {
-        kv_softmax<D, CAUSAL, BF16>(p, sbase, kbar0, tmem, warp / 4, ctl);
+        kv_softmax<D, CAUSAL, BF16, VAR>(p, sbase, kbar0, tmem, warp / 4, ctl);
     } else if (warp < 12) {
-        kv_epilogue<D, CAUSAL, BF16>(&tmDK, &tmDV, p, sbase, kbar0, tmem, ctl);
+        kv_epilogue<D, CAUSAL, BF16, VAR>(&tmDK, &tmDV, p, sbase, kbar0, tmem, ctl);
     } else if (warp == 12) {
-        if (lane == 0) kv_producer<D, CAUSAL>(&tmK, &tmV, &tmQ, &tmDO, p, sbase, kbar0, ctl);
+        if (lane == 0) kv_producer<D, CAUSAL, VAR>(&tmK, &tmV, &tmQ, &tmDO, p, sbase, kbar0, ctl);
     } else {
-        if (lane == 0) kv_issuer<D, CAUSAL, BF16>(p, sbase, kbar0, tmem, ctl);
+        if (lane == 0) kv_issuer<D, CAUSAL, BF16, VAR>(p, sbase, kbar0, tmem, ctl);
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -824,13 +913,13 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         ptx::tc_fence_after();
         const int first = (int)gridDim.x - 1 - (int)blockIdx.x;
         if (warp < 8) {
-            q_softmax<D, CAUSAL, BF16>(p, qbar0, tmem, warp / 4, ctl, first);
+            q_softmax<D, CAUSAL, BF16, VAR>(p, qbar0, tmem, warp / 4, ctl, first);
         } else if (warp < 12) {
-            q_epilogue<D, CAUSAL, BF16>(&tmDQ, p, sbase, qbar0, tmem, ctl, first);
+            q_epilogue<D, CAUSAL, BF16, VAR>(&tmDQ, p, sbase, qbar0, tmem, ctl, first);
         } else if (warp == 12) {
-            if (lane == 0) q_producer<D, CAUSAL>(&tmK, &tmV, &tmQ, &tmDO, p, sbase, qbar0, ctl, first);
+            if (lane == 0) q_producer<D, CAUSAL, VAR>(&tmK, &tmV, &tmQ, &tmDO, p, sbase, qbar0, ctl, first);
         } else {
-            if (lane == 0) q_issuer<D, CAUSAL, BF16>(p, sbase, qbar0, tmem, ctl, first);
+            if (lane == 0) q_issuer<D, CAUSAL, BF16, VAR>(p, sbase, qbar0, tmem, ctl, first);
         }
         ptx::tc_fence_before();
         __syncthreads();

@@ -94,11 +94,11 @@ struct BwdLaunchArgs {
     int grid, pre_grid;  // the fused dK/dV + dQ kernel, the pre kernel
     cudaStream_t stream;
 };
-cudaError_t launch_bwd_d16(const BwdLaunchArgs& a, bool causal, bool bf16);
-cudaError_t launch_bwd_d32(const BwdLaunchArgs& a, bool causal, bool bf16);
-cudaError_t launch_bwd_d64(const BwdLaunchArgs& a, bool causal, bool bf16);
-cudaError_t launch_bwd_d128(const BwdLaunchArgs& a, bool causal, bool bf16);
-cudaError_t launch_bwd_d256(const BwdLaunchArgs& a, bool causal, bool bf16);
+cudaError_t launch_bwd_d16(const BwdLaunchArgs& a, bool causal, bool bf16, int variant);
+cudaError_t launch_bwd_d32(const BwdLaunchArgs& a, bool causal, bool bf16, int variant);
+cudaError_t launch_bwd_d64(const BwdLaunchArgs& a, bool causal, bool bf16, int variant);
+cudaError_t launch_bwd_d128(const BwdLaunchArgs& a, bool causal, bool bf16, int variant);
+cudaError_t launch_bwd_d256(const BwdLaunchArgs& a, bool causal, bool bf16, int variant);
 
 // Host-side shape facts of each specialisation.
 int block_n_for(int D);      // keys per block

@@ -137,6 +137,11 @@ struct BwdParams {
     uint32_t* status;
     uint64_t wait_limit_ns;
     int inject_stall;        // test hook: 1 = withhold CTA 0's first K/V copy of the dK/dV phase
+    // variants (the kernel instantiated with VAR, D <= 128): key j is kept
+    // for query i iff i - win_left <= j <= i + win_right (-1: open side);
+    // ALiBi adds -alibi[hq] * |i - j| to the scaled score
+    int win_left, win_right;
+    const float* alibi;      // (Hq) slopes, or nullptr
 };
 
 }  // namespace fa

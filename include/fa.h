@@ -318,7 +318,31 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  const fa_strides* sdq, const fa_strides* sdk, const fa_strides* sdv, float scale, int causal,
                  fa_dtype dtype, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
-/* Bytes of workspace fa_bwd needs (host only; FA_ERR_UNSUPPORTED for an unsupported D). */
+/*
+ * fa_bwd_ex -- fa_bwd for fa_fwd_ex's window and ALiBi options (fa_fwd_options
+ * above; the variants of "Write Triton Attention Kernel", Inputs): the same
+ * formulas with s_ij = scale q_i . k_j - alibi_slopes[hq] |i - j| over the
+ * kept keys of the window (and the causal rule).  Arguments are those of
+ * fa_bwd plus `options` (NULL: none); q, k, v, o and lse come from fa_fwd_ex
+ * (or fa_fwd) with the same options.  With both window sides open (-1 or
+ * longer than Nq + Nkv) and no slopes the call is fa_bwd.  A dK/dV unit visits
+ * only the query blocks that keep a key of its block, a dQ unit only the key
+ * blocks its rows keep; a query row with no kept key gets dQ = 0, a key no row
+ * keeps dK = dV = 0.
+ *
+ * Errors: those of fa_bwd, plus FA_ERR_INVALID_ARG for a window side below
+ * -1, FA_ERR_ALIGNMENT for slopes not 4-byte aligned, and FA_ERR_UNSUPPORTED
+ * for cu_seqlens (packed variable-length gradients are not built) or for a
+ * window or slopes at D = 256.
+ */
+fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                    void* dq, void* dk, void* dv, int Z, int Hq, int Hkv, int Nq, int Nkv, int D,
+                    const fa_strides* sq, const fa_strides* sk, const fa_strides* sv, const fa_strides* so,
+                    const fa_strides* sdo, const fa_strides* sdq, const fa_strides* sdk, const fa_strides* sdv,
+                    float scale, int causal, fa_dtype dtype, const fa_fwd_options* options, void* workspace,
+                    size_t workspace_bytes, cudaStream_t stream);
+
+/* Bytes of workspace fa_bwd (and fa_bwd_ex) needs (host only; FA_ERR_UNSUPPORTED for an unsupported D). */
 fa_status fa_bwd_workspace_size(int Z, int Hq, int Nq, int D, size_t* bytes);
 
 /* Human-readable name of a status code (static storage, never NULL). */
