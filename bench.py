@@ -341,6 +341,8 @@ def run_native(args, rank, world, device):
         result["split_kv_shapes"] = [measure_shape(name, device, stream, peaks, impl=impl)
                                      for name in SPLIT_SHAPES for impl in ("fwd", "splitkv")]
         result["variant_shapes"] = [measure_variant(name, device, stream, peaks) for name in VARIANT_SHAPES]
+        result["variant_shapes"] += [measure_variant(name, device, stream, peaks, bwd=True) for name in VARIANT_SHAPES
+                                     if VARIANT_SHAPES[name][9] is None]
         result["bwd_shapes"] = [r for name in BWD_SHAPES for r in measure_bwd(name, device, stream, peaks)]
     return result
 
@@ -596,8 +598,9 @@ def variant_flops(Z, Hq, N, D, causal, window, lens):
     return 4.0 * Z * Hq * pairs * D
 
 
-def measure_variant(name, device, stream, peaks, steps=10):
-    """TFLOP/s of fa_fwd_ex on a window / ALiBi / variable-length workload (kept pairs only)."""
+def measure_variant(name, device, stream, peaks, steps=10, bwd=False):
+    """TFLOP/s of fa_fwd_ex on a window / ALiBi / variable-length workload (kept pairs only); with bwd,
+    of fa_bwd_ex on a dense one (5 products of the kept pairs)."""
     import numpy as np
     import torch
 
@@ -627,6 +630,17 @@ def measure_variant(name, device, stream, peaks, steps=10):
     def call():
         fa.fa_fwd_ex(q, k, v, o=o, causal=causal, window=window, stream=stream, **kw)
 
+    if bwd:
+        o, lse = fa.fa_fwd_ex(q, k, v, causal=causal, window=window, stream=stream, **kw)
+        do = si.as_torch(si.normals(1, 0, nq, dtype).reshape(shape_q), dtype).to(device)
+        ws = torch.empty(fa.fa_bwd_workspace_size(Z, Hq, N, D), dtype=torch.uint8, device=device)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        slopes = kw.get("alibi_slopes")
+
+        def call():  # noqa: F811 (the timed call of this mode)
+            fa.fa_bwd_ex(q, k, v, o, lse, do, dq, dk, dv, causal=causal, window=window, alibi_slopes=slopes,
+                         workspace=ws, stream=stream)
+
     for _ in range(3):
         call()
     torch.cuda.synchronize(device)
@@ -640,9 +654,10 @@ def measure_variant(name, device, stream, peaks, steps=10):
     code, word = fa.fa_device_status(stream)
     if code != fa.FA_OK:
         raise RuntimeError(f"device status after {name}: {word:#x}")
-    tf = variant_flops(Z, Hq, N, D, causal, window, lens) / (ms * 1e-3) / 1e12
-    return {"workload": name, "impl": "fwd_ex", "tflops": round(tf, 2), "frac_of_peak": round(tf / peaks["bf16_tflops"], 4),
-            "ms_per_step": round(ms, 4), "steps": steps, "flops": "kept (query, key) pairs x 4 D"}
+    tf = (2.5 if bwd else 1.0) * variant_flops(Z, Hq, N, D, causal, window, lens) / (ms * 1e-3) / 1e12
+    return {"workload": name, "impl": "bwd_ex" if bwd else "fwd_ex", "tflops": round(tf, 2),
+            "frac_of_peak": round(tf / peaks["bf16_tflops"], 4), "ms_per_step": round(ms, 4), "steps": steps,
+            "flops": "kept (query, key) pairs x 10 D (5 products)" if bwd else "kept (query, key) pairs x 4 D"}
 
 
 # fa_bwd workloads (gradients of the forward; 5 products of 2 N^2 D per head, half for causal)

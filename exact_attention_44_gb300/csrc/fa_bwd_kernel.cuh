@@ -475,6 +475,7 @@ __device__ void kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar0, ui
                 VAR == 0 || var_block_kept<CAUSAL>((i - w.j) * 128 - 127, (i - w.j) * 128 + 127, w.j * 128 + 128, p);
             const int key = w.j * 128 + row;
             const float slope2 = VAR == 2 ? -__ldg(p.alibi + hq) * 1.4426950408889634f : 0.f;
+            const float dbf = (float)(dbase + h * 64);  // d of this half's first column (exact: |d| < 2^24)
             uint32_t pk[32];  // Pᵀ in the input type: the dV operand, and what dS uses
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
@@ -493,8 +494,9 @@ __device__ void kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar0, ui
                     } else {
                         const int d0 = dbase + col;
                         if constexpr (VAR == 2) {
-                            e0 = fmaf(slope2, fabsf((float)d0), e0);
-                            e1 = fmaf(slope2, fabsf((float)(d0 + 1)), e1);
+                            const float df = dbf + (float)(32 * cc + 2 * x);
+                            e0 = fmaf(slope2, fabsf(df), e0);
+                            e1 = fmaf(slope2, fabsf(df + 1.f), e1);
                         }
                         if (!full) {
                             if (var_dropped<CAUSAL>(d0, key, p)) e0 = -INFINITY;
@@ -744,6 +746,7 @@ __device__ void q_softmax(const BwdParams& p, uint32_t bar0, uint32_t tmem, int 
             const bool diag = CAUSAL && jj == w.i;  // key > query only on the diagonal block
             // variants: d = query − key = dbase − col (as in the dK/dV phase)
             const int dbase = (w.i - jj) * 128 + row;
+            const float dbf = (float)(dbase - h * 64);  // d of this half's first column (exact: |d| < 2^24)
             const bool full =
                 VAR == 0 || var_block_kept<CAUSAL>((w.i - jj) * 128 - 127, (w.i - jj) * 128 + 127, jj * 128 + 128, p);
             uint32_t pk[32];
@@ -762,8 +765,9 @@ __device__ void q_softmax(const BwdParams& p, uint32_t bar0, uint32_t tmem, int 
                     } else {
                         const int d0 = dbase - col;
                         if constexpr (VAR == 2) {
-                            e0 = fmaf(slope2, fabsf((float)d0), e0);
-                            e1 = fmaf(slope2, fabsf((float)(d0 - 1)), e1);
+                            const float df = dbf - (float)(32 * cc + 2 * x);
+                            e0 = fmaf(slope2, fabsf(df), e0);
+                            e1 = fmaf(slope2, fabsf(df - 1.f), e1);
                         }
                         if (!full) {
                             if (var_dropped<CAUSAL>(d0, jj * 128 + col, p)) e0 = -INFINITY;
