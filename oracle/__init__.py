@@ -246,14 +246,34 @@ def attention_bwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, do: np.ndarray, d
 
 
 def attention_bwd_ex(q: np.ndarray, k: np.ndarray, v: np.ndarray, do: np.ndarray, dtype: str, scale: float,
-                     causal: bool, window=(-1, -1), alibi=None, nthreads: int | None = None,
+                     causal: bool, window=(-1, -1), alibi=None, cu_q=None, cu_k=None, nthreads: int | None = None,
                      lib: ctypes.CDLL | None = None):
-    """Gradients (dq, dk, dv) of attention_fwd_ex's window / ALiBi forward (dense tensors), float64.
+    """Gradients (dq, dk, dv) of attention_fwd_ex's forward, float64.
 
     window: (left, right), -1 for an open side; alibi: Hq slopes or None.
-    q, do: (Z, Hq, Nq, D); k, v: (Z, Hkv, Nkv, D) uint16 bit arrays of dtype.
+    Without cu_q/cu_k: q, do (Z, Hq, Nq, D); k, v (Z, Hkv, Nkv, D) uint16 bit
+    arrays of dtype.  With them (int arrays of Z + 1 offsets, as for
+    attention_fwd_ex): q, do (1, Hq, total_q, D), k, v (1, Hkv, total_k, D);
+    a sequence attends only to its own keys, so its gradients are those of
+    the dense backward on its own rows (a sequence without keys: dq = 0), and
+    rows outside every sequence get 0.
     """
     lib = lib or load()
+    if cu_q is not None or cu_k is not None:
+        if cu_q is None or cu_k is None or q.shape[0] != 1:
+            raise ValueError("varlen takes (1, H, total, D) tensors and both offset arrays")
+        cq, ck = np.asarray(cu_q, dtype=np.int64), np.asarray(cu_k, dtype=np.int64)
+        dq = np.zeros(q.shape, dtype=np.float64)
+        dk = np.zeros(k.shape, dtype=np.float64)
+        dv = np.zeros(k.shape, dtype=np.float64)
+        for z in range(len(cq) - 1):
+            a, b, c, e = int(cq[z]), int(cq[z + 1]), int(ck[z]), int(ck[z + 1])
+            if b == a or e == c:
+                continue
+            g = attention_bwd_ex(q[:, :, a:b], k[:, :, c:e], v[:, :, c:e], do[:, :, a:b], dtype, scale, causal,
+                                 window=window, alibi=alibi, nthreads=nthreads, lib=lib)
+            dq[:, :, a:b], dk[:, :, c:e], dv[:, :, c:e] = g
+        return dq, dk, dv
     q, k, v, do = (np.ascontiguousarray(x, dtype=np.uint16) for x in (q, k, v, do))
     Z, Hq, Nq, D = q.shape
     Zk, Hkv, Nkv, Dk = k.shape

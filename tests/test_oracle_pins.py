@@ -599,3 +599,46 @@ def test_bwd_ex_diagonal_window_closed_form():
     assert np.all(dq == 0.0) and np.all(dk == 0.0)
     want = np.stack([G[0, 0:2, :7].sum(axis=0), G[0, 2:4, :7].sum(axis=0)])[None]
     np.testing.assert_allclose(dv, want, rtol=0, atol=1e-12)
+
+
+def test_bwd_ex_varlen_matches_finite_differences():
+    # packed sequences (one without keys, one of a single row): central
+    # differences of the independent numpy forward run sequence by sequence
+    lens_q, lens_k = [5, 0, 1, 7], [6, 3, 0, 4]
+    cq = np.concatenate([[0], np.cumsum(lens_q)]).astype(np.int32)
+    ck = np.concatenate([[0], np.cumsum(lens_k)]).astype(np.int32)
+    Hq, Hkv, D, dtype, scale, causal, window = 4, 2, 8, "fp16", 0.7, True, (4, -1)
+    slopes = np.array([0.5, 0.0, 0.25, 1.0])
+    tq, tk = int(cq[-1]), int(ck[-1])
+    q = si.normals(131, 0, Hq * tq * D, dtype).reshape(1, Hq, tq, D)
+    k = si.normals(131, q.size, Hkv * tk * D, dtype).reshape(1, Hkv, tk, D)
+    v = si.normals(131, q.size + k.size, Hkv * tk * D, dtype).reshape(1, Hkv, tk, D)
+    do = si.normals(132, 0, q.size, dtype).reshape(q.shape)
+    dq, dk, dv = oracle.attention_bwd_ex(q, k, v, do, dtype, scale, causal, window=window, alibi=slopes,
+                                         cu_q=cq, cu_k=ck)
+    Q, K, V, G = (_np_decode(x, dtype) for x in (q, k, v, do))
+
+    def loss(Qx, Kx, Vx):
+        total = 0.0
+        for z in range(len(lens_q)):
+            a, b, c, e = cq[z], cq[z + 1], ck[z], ck[z + 1]
+            if b == a or e == c:
+                continue
+            O = _np_forward_ex(Qx[:, :, a:b], Kx[:, :, c:e], Vx[:, :, c:e], scale, causal, window, slopes)
+            total += float(np.sum(G[:, :, a:b] * O))
+        return total
+
+    rng = np.random.default_rng(9)
+    h = 1e-5
+    for name, X, grad in (("q", Q, dq), ("k", K, dk), ("v", V, dv)):
+        for _ in range(16):
+            idx = tuple(int(rng.integers(n)) for n in X.shape)
+            Xp, Xm = X.copy(), X.copy()
+            Xp[idx] += h
+            Xm[idx] -= h
+            args_p = {"q": (Xp, K, V), "k": (Q, Xp, V), "v": (Q, K, Xp)}[name]
+            args_m = {"q": (Xm, K, V), "k": (Q, Xm, V), "v": (Q, K, Xm)}[name]
+            fd = (loss(*args_p) - loss(*args_m)) / (2 * h)
+            assert abs(fd - grad[idx]) <= 1e-7 * max(1.0, abs(fd)), (name, idx, fd, grad[idx])
+    # the sequence without keys has no query gradient
+    assert np.all(dq[:, :, cq[1]:cq[2]] == 0.0) and np.all(dq[:, :, cq[2]:cq[3]] == 0.0)
