@@ -79,7 +79,8 @@ class fa_strides(ctypes.Structure):
 
 class fa_fwd_options(ctypes.Structure):
     _fields_ = [("window_left", ctypes.c_int), ("window_right", ctypes.c_int), ("alibi_slopes", ctypes.c_void_p),
-                ("cu_seqlens_q", ctypes.c_void_p), ("cu_seqlens_k", ctypes.c_void_p), ("max_seqlen_q", ctypes.c_int)]
+                ("cu_seqlens_q", ctypes.c_void_p), ("cu_seqlens_k", ctypes.c_void_p), ("max_seqlen_q", ctypes.c_int),
+                ("max_seqlen_k", ctypes.c_int)]
 
 
 class fa_fwd_schedule_info(ctypes.Structure):
@@ -278,23 +279,59 @@ def fa_bwd(q, k, v, o, lse, do, dq=None, dk=None, dv=None, *, scale: float | Non
 
 
 def fa_bwd_ex(q, k, v, o, lse, do, dq=None, dk=None, dv=None, *, scale: float | None = None, causal: bool = False,
-              window=(-1, -1), alibi_slopes=None, workspace=None, stream=None):
-    """Gradients of fa_fwd_ex's window / ALiBi forward (libfa's fa_bwd_ex; dense tensors, D <= 128).
+              window=(-1, -1), alibi_slopes=None, cu_seqlens_q=None, cu_seqlens_k=None,
+              max_seqlen_q: int | None = None, max_seqlen_k: int | None = None, workspace=None, stream=None):
+    """Gradients of fa_fwd_ex's forward (libfa's fa_bwd_ex; D <= 128 with any option).
 
-    Arguments as for fa_bwd, plus window (left, right), -1 for an open side, and
-    alibi_slopes (CUDA fp32 (Hq,) or None), the options the forward took.
+    Arguments as for fa_bwd, plus the options the forward took: window (left,
+    right), -1 for an open side; alibi_slopes (CUDA fp32 (Hq,) or None); and
+    cu_seqlens_q / cu_seqlens_k (CUDA int32, Z + 1 offsets) for packed
+    sequences: q, k, v, o, do (and dq, dk, dv) then hold packed rows, either
+    (total, H, D) or (1, H, total, D), the gradients come back in q's / k's
+    form, lse is the forward's (Hq, total_q), and max_seqlen_q / max_seqlen_k
+    default to the longest sequences (read back from the device once).
     """
     import torch
 
-    Hq = q.shape[1]
+    varlen = cu_seqlens_q is not None or cu_seqlens_k is not None
+    Hq = q.shape[1] if q.dim() == 4 else q.shape[-2]
     if alibi_slopes is not None and (alibi_slopes.dtype != torch.float32 or alibi_slopes.numel() != Hq):
         raise ValueError("alibi_slopes must be float32 with Hq entries")
+    if not varlen:
+        opt = fa_fwd_options(int(window[0]), int(window[1]),
+                             alibi_slopes.data_ptr() if alibi_slopes is not None else None, None, None, 0, 0)
+        return _bwd(q, k, v, o, lse, do, dq, dk, dv, scale, causal, workspace, stream, opt)
+    if cu_seqlens_q is None or cu_seqlens_k is None:
+        raise ValueError("pass both cu_seqlens_q and cu_seqlens_k")
+    if cu_seqlens_q.dtype != torch.int32 or cu_seqlens_k.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    if cu_seqlens_q.numel() != cu_seqlens_k.numel() or cu_seqlens_q.numel() < 1:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must hold the same Z + 1 offsets")
+
+    def longest(cu):
+        c = cu.cpu()
+        return int((c[1:] - c[:-1]).max().item()) if c.numel() > 1 else 0
+
+    if max_seqlen_q is None:
+        max_seqlen_q = longest(cu_seqlens_q)
+    if max_seqlen_k is None:
+        max_seqlen_k = longest(cu_seqlens_k)
+    grads = []
+    for g, like in ((dq, q), (dk, k), (dv, v)):
+        grads.append(torch.empty_like(like, memory_format=torch.contiguous_format) if g is None else g)
+    dq_user, dk_user, dv_user = grads
     opt = fa_fwd_options(int(window[0]), int(window[1]),
-                         alibi_slopes.data_ptr() if alibi_slopes is not None else None, None, None, 0)
-    return _bwd(q, k, v, o, lse, do, dq, dk, dv, scale, causal, workspace, stream, opt)
+                         alibi_slopes.data_ptr() if alibi_slopes is not None else None, cu_seqlens_q.data_ptr(),
+                         cu_seqlens_k.data_ptr(), int(max_seqlen_q), int(max_seqlen_k))
+    _bwd(_packed(q), _packed(k), _packed(v), _packed(o), lse, _packed(do), _packed(dq_user), _packed(dk_user),
+         _packed(dv_user), scale, causal, workspace, stream, opt,
+         seqs=(cu_seqlens_q.numel() - 1, int(max_seqlen_q)))
+    return dq_user, dk_user, dv_user
 
 
-def _bwd(q, k, v, o, lse, do, dq, dk, dv, scale, causal, workspace, stream, opt):
+def _bwd(q, k, v, o, lse, do, dq, dk, dv, scale, causal, workspace, stream, opt, seqs=None):
+    """Marshal one fa_bwd / fa_bwd_ex call.  seqs = (number of sequences,
+    longest query sequence) for packed tensors (batch extent one, lse (Hq, total))."""
     import torch
 
     Z, Hq, Nq, D = q.shape
@@ -305,13 +342,19 @@ def _bwd(q, k, v, o, lse, do, dq, dk, dv, scale, causal, workspace, stream, opt)
             raise TypeError(f"{name} must have q's dtype")
     if tuple(o.shape) != tuple(q.shape) or tuple(do.shape) != tuple(q.shape) or tuple(v.shape) != tuple(k.shape):
         raise ValueError("shape mismatch")
-    if lse.dtype != torch.float32 or tuple(lse.shape) != (Z, Hq, Nq) or not lse.is_contiguous():
-        raise ValueError("lse must be the forward's contiguous float32 (Z, Hq, Nq) tensor")
+    lse_shape, ws_rows = (Z, Hq, Nq), Nq
+    if seqs is not None:
+        if Z != 1:
+            raise ValueError("packed sequences take (1, H, total, D) or (total, H, D) tensors")
+        Z, ws_rows = seqs
+        lse_shape = (Hq, Nq)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != lse_shape or not lse.is_contiguous():
+        raise ValueError(f"lse must be the forward's contiguous float32 {lse_shape} tensor")
     dq = torch.empty_like(q, memory_format=torch.contiguous_format) if dq is None else dq
     dk = torch.empty_like(k, memory_format=torch.contiguous_format) if dk is None else dk
     dv = torch.empty_like(v, memory_format=torch.contiguous_format) if dv is None else dv
     if workspace is None:
-        workspace = torch.empty(fa_bwd_workspace_size(Z, Hq, Nq, D), dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(max(1, fa_bwd_workspace_size(Z, Hq, ws_rows, D)), dtype=torch.uint8, device=q.device)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if stream is None:

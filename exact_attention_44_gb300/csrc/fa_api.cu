@@ -808,7 +808,7 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float*
                     int Nkv, int D, const fa_strides* sq, const fa_strides* sk, const fa_strides* sv,
                     const fa_strides* so, float scale, int causal, fa_dtype dtype, const fa_fwd_options* options,
                     cudaStream_t stream) {
-    static const fa_fwd_options none = {-1, -1, nullptr, nullptr, nullptr, 0};
+    static const fa_fwd_options none = {-1, -1, nullptr, nullptr, nullptr, 0, 0};
     return fwd_ex_impl(q, k, v, o, lse, Z, Hq, Hkv, Nq, Nkv, D, sq, sk, sv, so, scale, causal, dtype,
                        options ? options : &none, stream);
 }
@@ -820,15 +820,19 @@ fa_status fa_bwd_workspace_size(int Z, int Hq, int Nq, int D, size_t* bytes) {
     return FA_OK;
 }
 
-// The backward, plain (variant 0) or with the window / ALiBi options of
-// fa_bwd_ex (variant 1: window; 2: window and ALiBi; head dims up to 128).
+// The backward, plain (variant 0) or with the options of fa_bwd_ex (variant
+// 1: window; 2: window and ALiBi; 3: packed variable-length sequences, with or
+// without them; head dims up to 128).  With a sequence table (cu_q, cu_k) Z
+// counts sequences, the tensors have one batch entry, Nq / Nkv are the packed
+// row totals, max_q / max_k bound the sequences' lengths and lse is (Hq, Nq).
 static fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
                           const void* dO, void* dq, void* dk, void* dv, int Z, int Hq, int Hkv, int Nq, int Nkv, int D,
                           const fa_strides* sq, const fa_strides* sk, const fa_strides* sv, const fa_strides* so,
                           const fa_strides* sdo, const fa_strides* sdq, const fa_strides* sdk,
                           const fa_strides* sdv, float scale, int causal, fa_dtype dtype, void* workspace,
                           size_t workspace_bytes, cudaStream_t stream, int variant, int win_left, int win_right,
-                          const float* alibi) {
+                          const float* alibi, const int32_t* cu_q = nullptr, const int32_t* cu_k = nullptr,
+                          int max_q = 0, int max_k = 0) {
     fa_status st = check_shape(Z, Hq, Hkv, Nq, Nkv, D, causal);
     if (st != FA_OK) return st;
     if (!supported_head_dim(D)) return FA_ERR_UNSUPPORTED;
@@ -840,18 +844,23 @@ static fa_status bwd_impl(const void* q, const void* k, const void* v, const voi
         return FA_ERR_INVALID_ARG;
     if ((int64_t)Z * Hkv * Nkv == 0) return FA_OK;
     if (Nq == 0) return FA_ERR_INVALID_ARG;  // gradients of an empty query set: nothing to differentiate
-    if ((st = check_tensor(q, sq, Z, Hq, Nq)) != FA_OK) return st;
-    if ((st = check_tensor(k, sk, Z, Hkv, Nkv)) != FA_OK) return st;
-    if ((st = check_tensor(v, sv, Z, Hkv, Nkv)) != FA_OK) return st;
-    if ((st = check_tensor(o, so, Z, Hq, Nq)) != FA_OK) return st;
-    if ((st = check_tensor(dO, sdo, Z, Hq, Nq)) != FA_OK) return st;
-    if ((st = check_tensor(dq, sdq, Z, Hq, Nq)) != FA_OK) return st;
-    if ((st = check_tensor(dk, sdk, Z, Hkv, Nkv)) != FA_OK) return st;
-    if ((st = check_tensor(dv, sdv, Z, Hkv, Nkv)) != FA_OK) return st;
+    // packed tensors of a variable-length batch have one batch entry
+    const bool varlen = cu_q != nullptr;
+    const int nb = varlen ? 1 : Z;
+    const int rows_q = varlen ? max_q : Nq;                    // query rows per (sequence, head) computed
+    const int rows_k = varlen ? (max_k > 0 ? max_k : Nkv) : Nkv;  // key rows per (sequence, head)
+    if ((st = check_tensor(q, sq, nb, Hq, Nq)) != FA_OK) return st;
+    if ((st = check_tensor(k, sk, nb, Hkv, Nkv)) != FA_OK) return st;
+    if ((st = check_tensor(v, sv, nb, Hkv, Nkv)) != FA_OK) return st;
+    if ((st = check_tensor(o, so, nb, Hq, Nq)) != FA_OK) return st;
+    if ((st = check_tensor(dO, sdo, nb, Hq, Nq)) != FA_OK) return st;
+    if ((st = check_tensor(dq, sdq, nb, Hq, Nq)) != FA_OK) return st;
+    if ((st = check_tensor(dk, sdk, nb, Hkv, Nkv)) != FA_OK) return st;
+    if ((st = check_tensor(dv, sdv, nb, Hkv, Nkv)) != FA_OK) return st;
     if (lse == nullptr) return FA_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(lse) % 4 != 0) return FA_ERR_ALIGNMENT;
     if (workspace == nullptr || reinterpret_cast<uintptr_t>(workspace) % 256 != 0 ||
-        workspace_bytes < bwd_workspace_bytes(Z, Hq, Nq, D))
+        workspace_bytes < bwd_workspace_bytes(Z, Hq, rows_q, D))
         return FA_ERR_WORKSPACE;
 
     int dev = 0;
@@ -880,16 +889,19 @@ static fa_status bwd_impl(const void* q, const void* k, const void* v, const voi
     p.Nq = Nq;
     p.Nkv = Nkv;
     p.group = Hq / Hkv;
-    p.Tq = (int)cdiv(Nq, 128);
-    p.Tk = (int)cdiv(Nkv, 128);
+    p.Tq = (int)cdiv(rows_q, 128);
+    p.Tk = (int)cdiv(rows_k, 128);
     const int64_t units = (int64_t)Z * Hkv * p.Tk, units_q = (int64_t)Z * Hq * p.Tq;
     if (units > INT32_MAX || units_q > INT32_MAX) return FA_ERR_UNSUPPORTED;
     p.nunits = (int)units;
     p.nunits_q = (int)units_q;
     // a dK/dV group reads the Q and dO rows of its kv heads' query heads; a
-    // causal dQ group the K and V of its query heads (shared within a GQA group)
-    p.kv_head_group = causal_head_group(Z * Hkv, 1, (int64_t)p.group * Nq * D * 4, info->l2_bytes, p.Tk, info->sms);
-    p.q_head_group = causal_head_group(Z * Hq, p.group, (int64_t)Nkv * D * 4, info->l2_bytes, p.Tq, info->sms);
+    // causal dQ group the K and V of its query heads (shared within a GQA
+    // group); a packed sequence holds about a Z-th of the packed rows
+    const int64_t seq_q = varlen ? std::max(1, Nq / std::max(1, Z)) : Nq;
+    const int64_t seq_k = varlen ? std::max(1, Nkv / std::max(1, Z)) : Nkv;
+    p.kv_head_group = causal_head_group(Z * Hkv, 1, (int64_t)p.group * seq_q * D * 4, info->l2_bytes, p.Tk, info->sms);
+    p.q_head_group = causal_head_group(Z * Hq, p.group, seq_k * D * 4, info->l2_bytes, p.Tq, info->sms);
     p.scale = scale;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -902,21 +914,23 @@ static fa_status bwd_impl(const void* q, const void* k, const void* v, const voi
     p.win_left = win_left;
     p.win_right = win_right;
     p.alibi = alibi;
+    p.cu_q = cu_q;
+    p.cu_k = varlen ? cu_k : nullptr;
 
     // operand loads: 128-row boxes; at D = 256 the kernel moves 64-row steps
     // (and its resident 128-row tiles as two boxes)
     CUtensorMap mk, mv, mq, mdo;
     CUresult cr;
     const int box = D == 256 ? 64 : 128;
-    if ((cr = make_map(&mk, k, dtype, D, Nkv, Hkv, Z, sk, box)) != CUDA_SUCCESS) return cuda_fail("K tensor map", cr);
-    if ((cr = make_map(&mv, v, dtype, D, Nkv, Hkv, Z, sv, box)) != CUDA_SUCCESS) return cuda_fail("V tensor map", cr);
-    if ((cr = make_map(&mq, q, dtype, D, Nq, Hq, Z, sq, box)) != CUDA_SUCCESS) return cuda_fail("Q tensor map", cr);
-    if ((cr = make_map(&mdo, dO, dtype, D, Nq, Hq, Z, sdo, box)) != CUDA_SUCCESS)
+    if ((cr = make_map(&mk, k, dtype, D, Nkv, Hkv, nb, sk, box)) != CUDA_SUCCESS) return cuda_fail("K tensor map", cr);
+    if ((cr = make_map(&mv, v, dtype, D, Nkv, Hkv, nb, sv, box)) != CUDA_SUCCESS) return cuda_fail("V tensor map", cr);
+    if ((cr = make_map(&mq, q, dtype, D, Nq, Hq, nb, sq, box)) != CUDA_SUCCESS) return cuda_fail("Q tensor map", cr);
+    if ((cr = make_map(&mdo, dO, dtype, D, Nq, Hq, nb, sdo, box)) != CUDA_SUCCESS)
         return cuda_fail("dO tensor map", cr);
     CUtensorMap mdq, mdk, mdv;
-    if ((cr = make_map(&mdq, dq, dtype, D, Nq, Hq, Z, sdq, 32)) != CUDA_SUCCESS) return cuda_fail("dQ tensor map", cr);
-    if ((cr = make_map(&mdk, dk, dtype, D, Nkv, Hkv, Z, sdk, 32)) != CUDA_SUCCESS) return cuda_fail("dK tensor map", cr);
-    if ((cr = make_map(&mdv, dv, dtype, D, Nkv, Hkv, Z, sdv, 32)) != CUDA_SUCCESS) return cuda_fail("dV tensor map", cr);
+    if ((cr = make_map(&mdq, dq, dtype, D, Nq, Hq, nb, sdq, 32)) != CUDA_SUCCESS) return cuda_fail("dQ tensor map", cr);
+    if ((cr = make_map(&mdk, dk, dtype, D, Nkv, Hkv, nb, sdk, 32)) != CUDA_SUCCESS) return cuda_fail("dK tensor map", cr);
+    if ((cr = make_map(&mdv, dv, dtype, D, Nkv, Hkv, nb, sdv, 32)) != CUDA_SUCCESS) return cuda_fail("dV tensor map", cr);
     a.tmK = &mk;
     a.tmV = &mv;
     a.tmQ = &mq;
@@ -956,10 +970,16 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
                     const fa_strides* sdo, const fa_strides* sdq, const fa_strides* sdk, const fa_strides* sdv,
                     float scale, int causal, fa_dtype dtype, const fa_fwd_options* options, void* workspace,
                     size_t workspace_bytes, cudaStream_t stream) {
-    const fa_fwd_options none = {-1, -1, nullptr, nullptr, nullptr, 0};
+    const fa_fwd_options none = {-1, -1, nullptr, nullptr, nullptr, 0, 0};
     const fa_fwd_options* opt = options != nullptr ? options : &none;
     if (opt->window_left < -1 || opt->window_right < -1) return FA_ERR_INVALID_ARG;
-    if (opt->cu_seqlens_q != nullptr || opt->cu_seqlens_k != nullptr) return FA_ERR_UNSUPPORTED;
+    const bool varlen = opt->cu_seqlens_q != nullptr || opt->cu_seqlens_k != nullptr;
+    if (varlen && (opt->cu_seqlens_q == nullptr || opt->cu_seqlens_k == nullptr || opt->max_seqlen_q < 0 ||
+                   opt->max_seqlen_k < 0))
+        return FA_ERR_INVALID_ARG;
+    if (varlen && (reinterpret_cast<uintptr_t>(opt->cu_seqlens_q) % 4 != 0 ||
+                   reinterpret_cast<uintptr_t>(opt->cu_seqlens_k) % 4 != 0))
+        return FA_ERR_ALIGNMENT;
     if (opt->alibi_slopes != nullptr && reinterpret_cast<uintptr_t>(opt->alibi_slopes) % 4 != 0)
         return FA_ERR_ALIGNMENT;
     // a window side longer than every query-key distance is open
@@ -967,10 +987,12 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
     const auto open = [&](int w) { return w < 0 || (int64_t)w > reach_all; };
     const int wl = open(opt->window_left) ? -1 : opt->window_left;
     const int wr = open(opt->window_right) ? -1 : opt->window_right;
-    const int variant = opt->alibi_slopes != nullptr ? 2 : (wl >= 0 || wr >= 0) ? 1 : 0;
+    const int variant = varlen ? 3 : opt->alibi_slopes != nullptr ? 2 : (wl >= 0 || wr >= 0) ? 1 : 0;
     if (variant != 0 && D > 128) return FA_ERR_UNSUPPORTED;
     return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, Z, Hq, Hkv, Nq, Nkv, D, sq, sk, sv, so, sdo, sdq, sdk, sdv, scale,
-                    causal, dtype, workspace, workspace_bytes, stream, variant, wl, wr, opt->alibi_slopes);
+                    causal, dtype, workspace, workspace_bytes, stream, variant, wl, wr, opt->alibi_slopes,
+                    varlen ? opt->cu_seqlens_q : nullptr, varlen ? opt->cu_seqlens_k : nullptr, opt->max_seqlen_q,
+                    opt->max_seqlen_k);
 }
 
 fa_status fa_fwd_splitkv_workspace_size_for(int D, int num_sms, size_t* bytes) {

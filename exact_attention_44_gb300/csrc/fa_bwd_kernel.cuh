@@ -163,13 +163,41 @@ __device__ __forceinline__ int unit_at(int pos) {
 // group reads (Q, dO) fit in a third of L2; within a group key blocks are
 // outermost and heads innermost.  A unit's steps run over the group's query
 // heads and, per head, the query blocks from i0 on.
+// zc, qrow0, krow0: the batch coordinate and first query / key row of the
+// unit's sequence in the tensor maps; nq, nk: its query and key counts (the
+// whole tensors but for packed variable-length batches).
 struct BwdUnit {
     int z, hk, j, i0, per_head, nsteps;
+    int zc, qrow0, krow0, nq, nk;
 };
 
-// Variant kernels (VAR = 1: window, 2: window and ALiBi) visit only the query
-// blocks holding a row that keeps a key of block j: rows j·128 − win_right ..
-// j·128 + 127 + win_left.
+// Sequence z's rows and counts (VAR = 3 with a sequence table), else the
+// dense batch z's.  Offsets are clamped to the packed extents.
+template <int VAR, typename U>
+__device__ __forceinline__ void unit_sequence(U& w, const BwdParams& p) {
+    w.zc = w.z;
+    w.qrow0 = 0;
+    w.krow0 = 0;
+    w.nq = p.Nq;
+    w.nk = p.Nkv;
+    if constexpr (VAR == 3) {
+        if (p.cu_q != nullptr) {
+            auto clampi = [](int x, int hi) { return x < 0 ? 0 : (x > hi ? hi : x); };
+            const int q0 = clampi(__ldg(p.cu_q + w.z), p.Nq), q1 = clampi(__ldg(p.cu_q + w.z + 1), p.Nq);
+            const int k0 = clampi(__ldg(p.cu_k + w.z), p.Nkv), k1 = clampi(__ldg(p.cu_k + w.z + 1), p.Nkv);
+            w.zc = 0;
+            w.qrow0 = q0;
+            w.krow0 = k0;
+            w.nq = q1 > q0 ? q1 - q0 : 0;
+            w.nk = k1 > k0 ? k1 - k0 : 0;
+        }
+    }
+}
+
+// Variant kernels (VAR = 1: window, 2: window and ALiBi, 3: the same on
+// packed sequences) visit only the query blocks holding a row that keeps a
+// key of block j: rows j·128 − win_right .. j·128 + 127 + win_left (of the
+// unit's sequence).
 template <bool CAUSAL, int VAR = 0>
 __device__ __forceinline__ BwdUnit bwd_unit(int u, const BwdParams& p) {
     BwdUnit w;
@@ -181,10 +209,16 @@ __device__ __forceinline__ BwdUnit bwd_unit(int u, const BwdParams& p) {
     const int zhk = g0 + x % gc;
     w.z = zhk / p.Hkv;
     w.hk = zhk % p.Hkv;
+    unit_sequence<VAR>(w, p);
     // causal (top-left): query row r sees keys <= r, so query blocks before
     // the key block's own index see none of its keys
     w.i0 = CAUSAL ? w.j : 0;
     int i_end = p.Tq;
+    if constexpr (VAR == 3) {
+        // the sequence's query blocks; a key block past its keys has none
+        i_end = (w.nq + 127) / 128 < p.Tq ? (w.nq + 127) / 128 : p.Tq;
+        if (w.j * 128 >= w.nk) i_end = 0;
+    }
     if constexpr (VAR != 0) {
         if (p.win_right >= 0) {
             const int lo_row = w.j * 128 - p.win_right;
@@ -215,6 +249,8 @@ __device__ __forceinline__ void bwd_step(const BwdUnit& w, int s, const BwdParam
 // block, every pair of it masked, and ends with dQ = 0).
 struct DqUnit {
     int z, hq, hk, i, j0, nkv;
+    int zc, qrow0, krow0, nq, nk;
+    bool skip;  // packed sequences: a query block past the sequence's rows (no work, nothing stored)
 };
 
 template <bool CAUSAL, int VAR = 0>
@@ -236,8 +272,16 @@ __device__ __forceinline__ DqUnit dq_unit(int u, const BwdParams& p) {
     w.z = head / p.Hq;
     w.hq = head % p.Hq;
     w.hk = w.hq / p.group;
+    unit_sequence<VAR>(w, p);
+    w.skip = VAR == 3 && w.i * 128 >= w.nq;
+    int tk = p.Tk;
+    if constexpr (VAR == 3) {
+        // the sequence's key blocks (a sequence without keys: one, masked)
+        tk = (w.nk + 127) / 128 < p.Tk ? (w.nk + 127) / 128 : p.Tk;
+        tk = tk > 0 ? tk : 1;
+    }
     w.j0 = 0;
-    w.nkv = CAUSAL ? (w.i + 1 < p.Tk ? w.i + 1 : p.Tk) : p.Tk;
+    w.nkv = CAUSAL ? (w.i + 1 < tk ? w.i + 1 : tk) : tk;
     if constexpr (VAR != 0) {
         int jlo = 0, jhi = w.nkv;
         if (p.win_left >= 0) {
@@ -249,7 +293,7 @@ __device__ __forceinline__ DqUnit dq_unit(int u, const BwdParams& p) {
             if (hi_block < jhi) jhi = (int)hi_block;
         }
         if (jlo >= jhi) {
-            jlo = jlo < p.Tk - 1 ? jlo : p.Tk - 1;
+            jlo = jlo < tk - 1 ? jlo : tk - 1;
             jhi = jlo + 1;
         }
         w.j0 = jlo;
@@ -264,13 +308,13 @@ __device__ __forceinline__ DqUnit dq_unit(int u, const BwdParams& p) {
 // lse is then −inf), and whether a whole 128 × 128 block of differences
 // d_min .. d_max with keys below k_end is kept.
 template <bool CAUSAL>
-__device__ __forceinline__ bool var_dropped(int d, int k, const BwdParams& p) {
-    return k >= p.Nkv || (CAUSAL && d < 0) || (p.win_left >= 0 && d > p.win_left) ||
+__device__ __forceinline__ bool var_dropped(int d, int k, int nk, const BwdParams& p) {
+    return k >= nk || (CAUSAL && d < 0) || (p.win_left >= 0 && d > p.win_left) ||
            (p.win_right >= 0 && -d > p.win_right);
 }
 template <bool CAUSAL>
-__device__ __forceinline__ bool var_block_kept(int d_min, int d_max, int k_end, const BwdParams& p) {
-    return k_end <= p.Nkv && (!CAUSAL || d_min >= 0) && (p.win_left < 0 || d_max <= p.win_left) &&
+__device__ __forceinline__ bool var_block_kept(int d_min, int d_max, int k_end, int nk, const BwdParams& p) {
+    return k_end <= nk && (!CAUSAL || d_min >= 0) && (p.win_left < 0 || d_max <= p.win_left) &&
            (p.win_right < 0 || -d_min <= p.win_right);
 }
 
@@ -329,9 +373,9 @@ __device__ void kv_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, cons
             ptx::mbar_arrive_expect_tx(bar(T::KB_KV_FULL), 2 * T::TILE);
             for (int c = 0; c < T::NCHUNK; ++c) {
                 ptx::tma_load_4d(sbase + T::KV_OFF_K + c * (128 * T::SW), tmK, bar(T::KB_KV_FULL), c * T::SWE,
-                                 w.j * 128, w.hk, w.z, pol_kv);
+                                 w.krow0 + w.j * 128, w.hk, w.zc, pol_kv);
                 ptx::tma_load_4d(sbase + T::KV_OFF_V + c * (128 * T::SW), tmV, bar(T::KB_KV_FULL), c * T::SWE,
-                                 w.j * 128, w.hk, w.z, pol_kv);
+                                 w.krow0 + w.j * 128, w.hk, w.zc, pol_kv);
             }
         }
         ++uc;
@@ -347,9 +391,9 @@ __device__ void kv_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, cons
             ptx::mbar_arrive_expect_tx(full, 2 * T::TILE + 1024);
             for (int c = 0; c < T::NCHUNK; ++c) {
                 ptx::tma_load_4d(sbase + T::KV_OFF_Q + st * T::TILE + c * (128 * T::SW), tmQ, full, c * T::SWE,
-                                 i * 128, hq, w.z, pol_q);
+                                 w.qrow0 + i * 128, hq, w.zc, pol_q);
                 ptx::tma_load_4d(sbase + T::KV_OFF_DO + st * T::TILE + c * (128 * T::SW), tmDO, full, c * T::SWE,
-                                 i * 128, hq, w.z, pol_q);
+                                 w.qrow0 + i * 128, hq, w.zc, pol_q);
             }
             const int64_t row0 = ((int64_t)w.z * p.Hq + hq) * p.Tq * 128 + (int64_t)i * 128;
             ptx::bulk_load(sbase + T::KV_OFF_LSE + st * 512, p.lse2 + row0, 512, full);
@@ -472,9 +516,10 @@ __device__ void kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar0, ui
             // slope2·|d| (log2 units)
             const int dbase = (i - w.j) * 128 - row;
             const bool full =
-                VAR == 0 || var_block_kept<CAUSAL>((i - w.j) * 128 - 127, (i - w.j) * 128 + 127, w.j * 128 + 128, p);
+                VAR == 0 || var_block_kept<CAUSAL>((i - w.j) * 128 - 127, (i - w.j) * 128 + 127, w.j * 128 + 128, w.nk, p);
             const int key = w.j * 128 + row;
-            const float slope2 = VAR == 2 ? -__ldg(p.alibi + hq) * 1.4426950408889634f : 0.f;
+            const float slope2 =
+                (VAR == 2 || (VAR == 3 && p.alibi != nullptr)) ? -__ldg(p.alibi + hq) * 1.4426950408889634f : 0.f;
             const float dbf = (float)(dbase + h * 64);  // d of this half's first column (exact: |d| < 2^24)
             uint32_t pk[32];  // Pᵀ in the input type: the dV operand, and what dS uses
 #pragma unroll
@@ -493,14 +538,14 @@ __device__ void kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar0, ui
                         if (diag && row > col + 1) e1 = -INFINITY;
                     } else {
                         const int d0 = dbase + col;
-                        if constexpr (VAR == 2) {
+                        if constexpr (VAR >= 2) {
                             const float df = dbf + (float)(32 * cc + 2 * x);
                             e0 = fmaf(slope2, fabsf(df), e0);
                             e1 = fmaf(slope2, fabsf(df + 1.f), e1);
                         }
                         if (!full) {
-                            if (var_dropped<CAUSAL>(d0, key, p)) e0 = -INFINITY;
-                            if (var_dropped<CAUSAL>(d0 + 1, key, p)) e1 = -INFINITY;
+                            if (var_dropped<CAUSAL>(d0, key, w.nk, p)) e0 = -INFINITY;
+                            if (var_dropped<CAUSAL>(d0 + 1, key, w.nk, p)) e1 = -INFINITY;
                         }
                     }
                     pk[16 * cc + x] = pack2<BF16>(ptx::ex2(e0), ptx::ex2(e1));
@@ -535,6 +580,33 @@ __device__ void kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar0, ui
     }
 }
 
+// One row per thread, straight to global memory, for a 32-row box that runs
+// past the end of a packed sequence: the next sequence's rows follow, so the
+// tensor store's clipping at the tensor's end does not guard them.  Every lane
+// takes part in the TMEM loads; only lanes with `store` write.  `after_read`
+// runs once the last TMEM load is complete.
+template <int D, bool BF16, typename AfterRead>
+__device__ __forceinline__ void direct_store_row(uint32_t taddr, float mul, uint8_t* dst_row, bool store,
+                                                 AfterRead&& after_read) {
+    constexpr int CH = D >= 32 ? 32 : 16;  // columns per TMEM load
+#pragma unroll 1
+    for (int k = 0; k < D / CH; ++k) {
+        uint32_t r[CH];
+        if constexpr (CH == 32) ptx::tmem_ld32(taddr + k * CH, r);
+        else ptx::tmem_ld16(taddr + k * CH, r);
+        uint32_t pk[CH / 2];
+#pragma unroll
+        for (int x = 0; x < CH / 2; ++x)
+            pk[x] = pack2<BF16>(__uint_as_float(r[2 * x]) * mul, __uint_as_float(r[2 * x + 1]) * mul);
+        if (k == D / CH - 1) after_read();
+        if (store) {
+            uint4* dst = reinterpret_cast<uint4*>(dst_row + 2 * k * CH);
+#pragma unroll
+            for (int x = 0; x < CH / 8; ++x) dst[x] = make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
+        }
+    }
+}
+
 // Thread = TMEM lane = key: per unit, dK (times scale) and dV are read out,
 // released and stored in the input type; a unit no query sees gets zeros.
 template <int D, bool CAUSAL, bool BF16, int VAR>
@@ -557,13 +629,13 @@ __device__ void kv_epilogue(const CUtensorMap* tmDK, const CUtensorMap* tmDV, co
             drain();
             return;
         }
-        const int key = w.j * 128 + row;
+        const int key = w.j * 128 + row;  // within the unit's sequence
         uint8_t* dk_row = reinterpret_cast<uint8_t*>(p.dk) +
-                          2 * ((int64_t)w.z * p.sdk_z + (int64_t)w.hk * p.sdk_h + (int64_t)key * p.sdk_n);
+                          2 * ((int64_t)w.zc * p.sdk_z + (int64_t)w.hk * p.sdk_h + (int64_t)(w.krow0 + key) * p.sdk_n);
         uint8_t* dv_row = reinterpret_cast<uint8_t*>(p.dv) +
-                          2 * ((int64_t)w.z * p.sdv_z + (int64_t)w.hk * p.sdv_h + (int64_t)key * p.sdv_n);
+                          2 * ((int64_t)w.zc * p.sdv_z + (int64_t)w.hk * p.sdv_h + (int64_t)(w.krow0 + key) * p.sdv_n);
         if (w.nsteps == 0) {
-            if (key < p.Nkv) {
+            if (key < w.nk) {
 #pragma unroll
                 for (int x = 0; x < D / 8; ++x) {
                     reinterpret_cast<uint4*>(dk_row)[x] = make_uint4(0, 0, 0, 0);
@@ -580,14 +652,20 @@ __device__ void kv_epilogue(const CUtensorMap* tmDK, const CUtensorMap* tmDV, co
         // dV, then dK (x scale), as 32-row boxes of this warp's keys; a box
         // that starts past the last key has nothing to store
         const int key0 = w.j * 128 + 32 * quad;
-        tma_store_rows<D, T::SW, BF16>(tmem + lane_addr + T::TM_DV, 1.f, stage, tmDV, key0, w.hk, w.z, key0 < p.Nkv,
-                                       []() {});
-        tma_store_rows<D, T::SW, BF16>(tmem + lane_addr + T::TM_DK, p.scale, stage, tmDK, key0, w.hk, w.z,
-                                       key0 < p.Nkv, [&]() {
-                                           // dK and dV read: the next unit may accumulate into them
-                                           ptx::tc_fence_before();
-                                           ptx::mbar_arrive(bar(T::KB_ACC_FREE));
-                                       });
+        const auto release = [&]() {
+            // dK and dV read: the next unit may accumulate into them
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(T::KB_ACC_FREE));
+        };
+        if (VAR != 3 || p.cu_k == nullptr || key0 + 32 <= w.nk) {
+            tma_store_rows<D, T::SW, BF16>(tmem + lane_addr + T::TM_DV, 1.f, stage, tmDV, w.krow0 + key0, w.hk, w.zc,
+                                           key0 < w.nk, []() {});
+            tma_store_rows<D, T::SW, BF16>(tmem + lane_addr + T::TM_DK, p.scale, stage, tmDK, w.krow0 + key0, w.hk,
+                                           w.zc, key0 < w.nk, release);
+        } else {
+            direct_store_row<D, BF16>(tmem + lane_addr + T::TM_DV, 1.f, dv_row, key < w.nk, []() {});
+            direct_store_row<D, BF16>(tmem + lane_addr + T::TM_DK, p.scale, dk_row, key < w.nk, release);
+        }
         ++uc;
     }
     drain();
@@ -621,13 +699,14 @@ __device__ void q_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const
     for (int pos = first; ok && unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x) {
         const DqUnit w = dq_unit<CAUSAL, VAR>(unit_at<CAUSAL>(pos), p);
         if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_LOAD)) { ok = false; break; }
+        if (w.skip) continue;
         if (uc > 0 && !wait_phase(bar(T::QB_QD_EMPTY), (uc - 1) & 1u, ctl, SITE_B_QD_EMPTY)) { ok = false; break; }
         ptx::mbar_arrive_expect_tx(bar(T::QB_QD_FULL), 2 * T::TILE);
         for (int c = 0; c < T::NCHUNK; ++c) {
-            ptx::tma_load_4d(sbase + T::Q_OFF_Q + c * (128 * T::SW), tmQ, bar(T::QB_QD_FULL), c * T::SWE, w.i * 128,
-                             w.hq, w.z, pol_q);
+            ptx::tma_load_4d(sbase + T::Q_OFF_Q + c * (128 * T::SW), tmQ, bar(T::QB_QD_FULL), c * T::SWE,
+                             w.qrow0 + w.i * 128, w.hq, w.zc, pol_q);
             ptx::tma_load_4d(sbase + T::Q_OFF_DO + c * (128 * T::SW), tmDO, bar(T::QB_QD_FULL), c * T::SWE,
-                             w.i * 128, w.hq, w.z, pol_q);
+                             w.qrow0 + w.i * 128, w.hq, w.zc, pol_q);
         }
         ++uc;
         for (int j = 0; j < w.nkv; ++j, ++g) {
@@ -640,9 +719,9 @@ __device__ void q_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const
             ptx::mbar_arrive_expect_tx(full, 2 * T::TILE);
             for (int c = 0; c < T::NCHUNK; ++c) {
                 ptx::tma_load_4d(sbase + T::Q_OFF_K + st * T::TILE + c * (128 * T::SW), tmK, full, c * T::SWE,
-                                 (w.j0 + j) * 128, w.hk, w.z, pol_kv);
+                                 w.krow0 + (w.j0 + j) * 128, w.hk, w.zc, pol_kv);
                 ptx::tma_load_4d(sbase + T::Q_OFF_V + st * T::TILE + c * (128 * T::SW), tmV, full, c * T::SWE,
-                                 (w.j0 + j) * 128, w.hk, w.z, pol_kv);
+                                 w.krow0 + (w.j0 + j) * 128, w.hk, w.zc, pol_kv);
             }
         }
     }
@@ -689,6 +768,7 @@ __device__ void q_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0, uint
     for (int pos = first; ok && unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x) {
         const DqUnit w = dq_unit<CAUSAL, VAR>(unit_at<CAUSAL>(pos), p);
         if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_MMA)) { ok = false; break; }
+        if (w.skip) continue;
         if (!wait_phase(bar(T::QB_QD_FULL), uc & 1u, ctl, SITE_B_QD_FULL)) { ok = false; break; }
         if (!issue_s(g)) { ok = false; break; }
         issue_dp(g);
@@ -734,9 +814,11 @@ __device__ void q_softmax(const BwdParams& p, uint32_t bar0, uint32_t tmem, int 
     for (int pos = first; unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x) {
         const DqUnit w = dq_unit<CAUSAL, VAR>(unit_at<CAUSAL>(pos), p);
         if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_SOFTMAX)) return;
+        if (w.skip) continue;
         const int64_t r = ((int64_t)w.z * p.Hq + w.hq) * p.Tq * 128 + (int64_t)w.i * 128 + row;
         const float l2 = __ldg(p.lse2 + r), dl = __ldg(p.delta + r);
-        const float slope2 = VAR == 2 ? -__ldg(p.alibi + w.hq) * 1.4426950408889634f : 0.f;
+        const float slope2 =
+            (VAR == 2 || (VAR == 3 && p.alibi != nullptr)) ? -__ldg(p.alibi + w.hq) * 1.4426950408889634f : 0.f;
         for (int j = 0; j < w.nkv; ++j, ++g) {
             const uint32_t st = g & 1u;
             const uint32_t slot = tmem + lane_addr + T::TM_QS + st * 128;
@@ -748,7 +830,7 @@ __device__ void q_softmax(const BwdParams& p, uint32_t bar0, uint32_t tmem, int 
             const int dbase = (w.i - jj) * 128 + row;
             const float dbf = (float)(dbase - h * 64);  // d of this half's first column (exact: |d| < 2^24)
             const bool full =
-                VAR == 0 || var_block_kept<CAUSAL>((w.i - jj) * 128 - 127, (w.i - jj) * 128 + 127, jj * 128 + 128, p);
+                VAR == 0 || var_block_kept<CAUSAL>((w.i - jj) * 128 - 127, (w.i - jj) * 128 + 127, jj * 128 + 128, w.nk, p);
             uint32_t pk[32];
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
@@ -764,14 +846,14 @@ __device__ void q_softmax(const BwdParams& p, uint32_t bar0, uint32_t tmem, int 
                         if (diag && col + 1 > row) e1 = -INFINITY;
                     } else {
                         const int d0 = dbase - col;
-                        if constexpr (VAR == 2) {
+                        if constexpr (VAR >= 2) {
                             const float df = dbf - (float)(32 * cc + 2 * x);
                             e0 = fmaf(slope2, fabsf(df), e0);
                             e1 = fmaf(slope2, fabsf(df - 1.f), e1);
                         }
                         if (!full) {
-                            if (var_dropped<CAUSAL>(d0, jj * 128 + col, p)) e0 = -INFINITY;
-                            if (var_dropped<CAUSAL>(d0 - 1, jj * 128 + col + 1, p)) e1 = -INFINITY;
+                            if (var_dropped<CAUSAL>(d0, jj * 128 + col, w.nk, p)) e0 = -INFINITY;
+                            if (var_dropped<CAUSAL>(d0 - 1, jj * 128 + col + 1, w.nk, p)) e1 = -INFINITY;
                         }
                     }
                     pk[16 * cc + x] = pack2<BF16>(ptx::ex2(e0), ptx::ex2(e1));
@@ -806,6 +888,7 @@ __device__ void q_epilogue(const CUtensorMap* tmDQ, const BwdParams& p, uint32_t
     using T = BwdTraits<D>;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     const int quad = (threadIdx.x / 32) % 4;
+    const int row = quad * 32 + threadIdx.x % 32;  // query within the block
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
     const uint32_t stage = sbase + T::Q_OFF_OST + (uint32_t)quad * 32u * T::SW;  // this warp's staging rows
     // lane 0's stores must have read shared memory before the CTA exits
@@ -813,12 +896,13 @@ __device__ void q_epilogue(const CUtensorMap* tmDQ, const BwdParams& p, uint32_t
         if (threadIdx.x % 32 == 0) ptx::bulk_wait_all();
     };
     uint32_t uc = 0;
-    for (int pos = first; unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x, ++uc) {
+    for (int pos = first; unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x) {
         const DqUnit w = dq_unit<CAUSAL, VAR>(unit_at<CAUSAL>(pos), p);
         if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_EPILOGUE)) {
             drain();
             return;
         }
+        if (w.skip) continue;
         if (!warp_wait_phase(bar(T::QB_DQ_FULL), uc & 1u, ctl, SITE_B_DQ_FULL)) {
             drain();
             return;
@@ -826,12 +910,21 @@ __device__ void q_epilogue(const CUtensorMap* tmDQ, const BwdParams& p, uint32_t
         ptx::tc_fence_after();
         // dQ (x scale) as 32-row boxes of this warp's queries
         const int q0 = w.i * 128 + 32 * quad;
-        tma_store_rows<D, T::SW, BF16>(tmem + lane_addr + T::TM_DQ, p.scale, stage, tmDQ, q0, w.hq, w.z, q0 < p.Nq,
-                                       [&]() {
-                                           // dQ read: the next unit may accumulate into it
-                                           ptx::tc_fence_before();
-                                           ptx::mbar_arrive(bar(T::QB_DQ_FREE));
-                                       });
+        const auto release = [&]() {
+            // dQ read: the next unit may accumulate into it
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(T::QB_DQ_FREE));
+        };
+        if (VAR != 3 || p.cu_q == nullptr || q0 + 32 <= w.nq) {
+            tma_store_rows<D, T::SW, BF16>(tmem + lane_addr + T::TM_DQ, p.scale, stage, tmDQ, w.qrow0 + q0, w.hq, w.zc,
+                                           q0 < w.nq, release);
+        } else {
+            const int qr = w.i * 128 + row;
+            uint8_t* dq_row = reinterpret_cast<uint8_t*>(p.dq) +
+                              2 * ((int64_t)w.zc * p.sdq_z + (int64_t)w.hq * p.sdq_h + (int64_t)(w.qrow0 + qr) * p.sdq_n);
+            direct_store_row<D, BF16>(tmem + lane_addr + T::TM_DQ, p.scale, dq_row, qr < w.nq, release);
+        }
+        ++uc;
     }
     drain();
 }
@@ -839,8 +932,9 @@ __device__ void q_epilogue(const CUtensorMap* tmDQ, const BwdParams& p, uint32_t
 
 // ================================================================ pre pass ==
 // Per query row, padded to whole 128-row blocks: Δ = rowsum(dO ∘ O) in fp32
-// from the input-type values, and the lse in base 2 (+inf past Nq, so those
-// rows and columns get P = 0).  D/8 threads per row, 16 bytes of O and dO each.
+// from the input-type values, and the lse in base 2 (+inf past Nq, or past a
+// packed sequence's length, so those rows and columns get P = 0: the rows of
+// the next sequence that a block crossing the end reads contribute nothing).  D/8 threads per row, 16 bytes of O and dO each.
 // ================================================================ fused ======
 // One launch runs both gradient kernels' work: each CTA takes its dK/dV units
 // (positions c, c + grid, ...), then, in the same shared memory and TMEM, its
@@ -948,12 +1042,24 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
         const int64_t head = r / ((int64_t)p.Tq * 128);
         const int i = (int)(r - head * p.Tq * 128);
         const int z = (int)(head / p.Hq), hq = (int)(head % p.Hq);
+        // the row's batch entry, packed row and lse index; packed sequences:
+        // row i of sequence z, kept while i is below its length
+        int zc = z, n = p.Nq;
+        int64_t qr = i, li = head * p.Nq + i;
+        if (p.cu_q != nullptr) {
+            const int q0 = min(max(__ldg(p.cu_q + z), 0), p.Nq), q1 = min(max(__ldg(p.cu_q + z + 1), 0), p.Nq);
+            zc = 0;
+            n = q1 > q0 ? q1 - q0 : 0;
+            qr = (int64_t)q0 + i;
+            li = (int64_t)hq * p.Nq + q0 + i;
+        }
+        const bool kept = i < n;
         float delta = 0.f;
-        if (i < p.Nq) {
-            const uint4 a = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.o) + (int64_t)z * p.so_z +
-                                                           (int64_t)hq * p.so_h + (int64_t)i * p.so_n)[sub];
-            const uint4 b = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.dO) + (int64_t)z * p.sdo_z +
-                                                           (int64_t)hq * p.sdo_h + (int64_t)i * p.sdo_n)[sub];
+        if (kept) {
+            const uint4 a = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.o) + (int64_t)zc * p.so_z +
+                                                           (int64_t)hq * p.so_h + qr * p.so_n)[sub];
+            const uint4 b = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.dO) + (int64_t)zc * p.sdo_z +
+                                                           (int64_t)hq * p.sdo_h + qr * p.sdo_n)[sub];
             const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
             for (int y = 0; y < 4; ++y) {
@@ -966,7 +1072,7 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
         for (int m = TPR / 2; m > 0; m /= 2) delta += __shfl_xor_sync(0xffffffffu, delta, m);
         if (sub == 0) {
             p.delta[r] = delta;
-            p.lse2[r] = i < p.Nq ? p.lse[head * p.Nq + i] * 1.4426950408889634f : INFINITY;
+            p.lse2[r] = kept ? p.lse[li] * 1.4426950408889634f : INFINITY;
         }
     }
 }

@@ -115,6 +115,9 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
  *                               keys; both start at 0 and never decrease
  *   max_seqlen_q                with cu_seqlens: at least the longest query
  *                               sequence (rows past it are not computed)
+ *   max_seqlen_k                with cu_seqlens, read by fa_bwd_ex only: at
+ *                               least the longest key sequence (keys past it
+ *                               get no gradient), or 0 for the packed total
  *
  * A query row with no kept key gets O = 0 and lse = -inf.
  */
@@ -125,6 +128,7 @@ typedef struct {
     const int32_t* cu_seqlens_q;
     const int32_t* cu_seqlens_k;
     int max_seqlen_q;
+    int max_seqlen_k;
 } fa_fwd_options;
 
 /*
@@ -319,21 +323,30 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  fa_dtype dtype, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
- * fa_bwd_ex -- fa_bwd for fa_fwd_ex's window and ALiBi options (fa_fwd_options
- * above; the variants of "Write Triton Attention Kernel", Inputs): the same
- * formulas with s_ij = scale q_i . k_j - alibi_slopes[hq] |i - j| over the
- * kept keys of the window (and the causal rule).  Arguments are those of
- * fa_bwd plus `options` (NULL: none); q, k, v, o and lse come from fa_fwd_ex
- * (or fa_fwd) with the same options.  With both window sides open (-1 or
- * longer than Nq + Nkv) and no slopes the call is fa_bwd.  A dK/dV unit visits
- * only the query blocks that keep a key of its block, a dQ unit only the key
- * blocks its rows keep; a query row with no kept key gets dQ = 0, a key no row
- * keeps dK = dV = 0.
+ * fa_bwd_ex -- fa_bwd for fa_fwd_ex's options (fa_fwd_options above; the
+ * variants of "Write Triton Attention Kernel", Inputs): the same formulas with
+ * s_ij = scale q_i . k_j - alibi_slopes[hq] |i - j| over the kept keys of the
+ * window (and the causal rule), within each packed sequence when cu_seqlens
+ * are set.  Arguments are those of fa_bwd plus `options` (NULL: none); q, k,
+ * v, o and lse come from fa_fwd_ex (or fa_fwd) with the same options.  With no
+ * sequence table, both window sides open (-1 or longer than Nq + Nkv) and no
+ * slopes the call is fa_bwd.  A dK/dV unit visits only the query blocks that
+ * keep a key of its block, a dQ unit only the key blocks its rows keep; a
+ * query row with no kept key gets dQ = 0, a key no row keeps dK = dV = 0.
+ *
+ * With cu_seqlens set, as for fa_fwd_ex: Z is the number of sequences, all
+ * nine tensors are packed with a batch extent of one (q, o, dO, dq (1, Hq, Nq,
+ * D); k, v, dk, dv (1, Hkv, Nkv, D); Nq and Nkv the packed row totals), lse is
+ * (Hq, Nq) fp32 contiguous, and the workspace is fa_bwd_workspace_size(Z, Hq,
+ * max_seqlen_q, D) bytes.  Rows of the packed tensors outside every sequence
+ * are not written.
  *
  * Errors: those of fa_bwd, plus FA_ERR_INVALID_ARG for a window side below
- * -1, FA_ERR_ALIGNMENT for slopes not 4-byte aligned, and FA_ERR_UNSUPPORTED
- * for cu_seqlens (packed variable-length gradients are not built) or for a
- * window or slopes at D = 256.
+ * -1, only one of the cu_seqlens arrays, or a negative max_seqlen_q or
+ * max_seqlen_k, FA_ERR_ALIGNMENT for an option array not 4-byte aligned, and
+ * FA_ERR_UNSUPPORTED for any option at D = 256.  The offsets are not
+ * validated on the host; those outside the packed extents are clamped to them
+ * on the device.
  */
 fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
                     void* dq, void* dk, void* dv, int Z, int Hq, int Hkv, int Nq, int Nkv, int D,

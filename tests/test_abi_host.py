@@ -217,6 +217,29 @@ def test_fwd_ex_option_errors_on_the_host(lib):
     assert call(alibi=0x1001) == fa.FA_ERR_ALIGNMENT
 
 
+def test_bwd_ex_option_errors_on_the_host(lib):
+    s = fa.fa_strides(2 * 64 * 64, 64 * 64, 64, 1)
+    kv = fa.fa_strides(64 * 64, 64 * 64, 64, 1)
+
+    def call(D=64, **kw):
+        opt = fa.fa_fwd_options(kw.get("wl", -1), kw.get("wr", -1), kw.get("alibi"), kw.get("cq"), kw.get("ck"),
+                                kw.get("maxq", 0), kw.get("maxk", 0))
+        t = 0x10000
+        return lib.fa_bwd_ex(t, t, t, t, t, t, t, t, t, 1, 2, 1, 64, 64, D, *[ctypes.byref(x) for x in (s, kv, kv, s, s, s, kv, kv)],
+                             0.125, 0, 0, ctypes.byref(opt), t, 1 << 20, None)
+    assert call(wl=-2) == fa.FA_ERR_INVALID_ARG
+    assert call(cq=0x1000) == fa.FA_ERR_INVALID_ARG          # only one offset array
+    assert call(ck=0x1000) == fa.FA_ERR_INVALID_ARG
+    assert call(cq=0x1000, ck=0x2000, maxq=-1) == fa.FA_ERR_INVALID_ARG
+    assert call(cq=0x1000, ck=0x2000, maxk=-1) == fa.FA_ERR_INVALID_ARG
+    assert call(cq=0x1002, ck=0x2000, maxq=8) == fa.FA_ERR_ALIGNMENT
+    assert call(cq=0x1000, ck=0x2001, maxq=8) == fa.FA_ERR_ALIGNMENT
+    assert call(alibi=0x1001) == fa.FA_ERR_ALIGNMENT
+    # every option needs a head dim up to 128
+    assert call(D=256, cq=0x1000, ck=0x2000, maxq=64) == fa.FA_ERR_UNSUPPORTED
+    assert call(D=256, wl=8) == fa.FA_ERR_UNSUPPORTED
+
+
 # ---- fa_fwd_schedule: the forward's schedule, host-only -------------------
 # An independent statement of the documented whole-tile orders: non-causal
 # tiles head-major; causal tiles in groups of head_group heads, each group

@@ -1,5 +1,6 @@
-"""GPU parity of fa_bwd_ex (gradients of the window / ALiBi forward) against
-the fp64 oracle's attention_bwd_ex, on dense (Z, H, N, D) tensors.
+"""GPU parity of fa_bwd_ex (gradients of the window / ALiBi forward, on dense
+(Z, H, N, D) tensors and on packed variable-length sequences) against the fp64
+oracle's attention_bwd_ex.
 
 The forward's O and lse come from fa_fwd_ex with the same options (the GPU's
 own chain, as for fa_bwd); the oracle differentiates the definition from Q, K,
@@ -121,3 +122,109 @@ def test_head_dim_256_variants_are_unsupported():
     with pytest.raises(fa.FaError) as e:
         fa.fa_bwd_ex(qt, kt, vt, o, lse, torch.zeros_like(qt), window=(8, 8))
     assert e.value.code == fa.FA_ERR_UNSUPPORTED
+    cu = torch.tensor([0, 64], dtype=torch.int32, device="cuda")
+    with pytest.raises(fa.FaError) as e:
+        fa.fa_bwd_ex(qt, kt, vt, o, lse[0], torch.zeros_like(qt), cu_seqlens_q=cu, cu_seqlens_k=cu)
+    assert e.value.code == fa.FA_ERR_UNSUPPORTED
+
+
+# ---- packed variable-length sequences -------------------------------------
+# Sequence z owns query rows cu_q[z] .. cu_q[z+1]-1 and key rows cu_k[z] ..
+# cu_k[z+1]-1 and attends only to its own keys; the oracle composes the
+# dense backward sequence by sequence.  The gradient buffers start filled
+# with a sentinel: packed rows outside every sequence must keep it.
+
+SENTINEL = 7.0
+
+
+def _varlen_inputs(seed, lens_q, lens_k, Hq, Hkv, D, dtype, extra_q=0, extra_k=0):
+    cu_q = np.concatenate([[0], np.cumsum(lens_q)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(lens_k)]).astype(np.int32)
+    tq, tk = int(cu_q[-1]) + extra_q, int(cu_k[-1]) + extra_k
+    q = si.normals(seed, 0, Hq * tq * D, dtype).reshape(1, Hq, tq, D)
+    k = si.normals(seed, q.size, Hkv * tk * D, dtype).reshape(1, Hkv, tk, D)
+    v = si.normals(seed, q.size + k.size, Hkv * tk * D, dtype).reshape(1, Hkv, tk, D)
+    do = si.normals(seed + 1000, 0, q.size, dtype).reshape(q.shape)
+    return cu_q, cu_k, q, k, v, do
+
+
+def check_bwd_varlen(seed, lens_q, lens_k, Hq, Hkv, D, dtype, causal, window=(-1, -1), alibi=None, thd=False,
+                     extra_q=0, extra_k=0, max_seqlen_k=None):
+    import torch
+    import exact_attention_44_gb300 as fa
+    cu_q, cu_k, q, k, v, do = _varlen_inputs(seed, lens_q, lens_k, Hq, Hkv, D, dtype, extra_q, extra_k)
+    scale = 1 / math.sqrt(D)
+    qt, kt, vt, dot = (to_device(x, dtype) for x in (q, k, v, do))
+    if thd:  # (total, H, D) storage
+        qt, kt, vt, dot = (x[0].permute(1, 0, 2).contiguous() for x in (qt, kt, vt, dot))
+    slopes = None if alibi is None else torch.tensor(alibi, dtype=torch.float32, device="cuda")
+    cq, ck = torch.from_numpy(cu_q).cuda(), torch.from_numpy(cu_k).cuda()
+    o, lse = fa.fa_fwd_ex(qt, kt, vt, o=torch.zeros_like(qt), scale=scale, causal=causal, window=window,
+                          alibi_slopes=slopes, cu_seqlens_q=cq, cu_seqlens_k=ck)
+    dq, dk, dv = (torch.full_like(x, SENTINEL) for x in (qt, kt, vt))
+    fa.fa_bwd_ex(qt, kt, vt, o, lse, dot, dq, dk, dv, scale=scale, causal=causal, window=window, alibi_slopes=slopes,
+                 cu_seqlens_q=cq, cu_seqlens_k=ck, max_seqlen_k=max_seqlen_k)
+    torch.cuda.synchronize()
+    code, word = fa.fa_device_status()
+    assert code == 0, f"device status {word:#x}"
+    ref = oracle.attention_bwd_ex(q, k, v, do, dtype, scale, causal, window=window,
+                                  alibi=None if alibi is None else np.asarray(alibi, dtype=np.float64),
+                                  cu_q=cu_q, cu_k=cu_k)
+    nq, nk = int(cu_q[-1]), int(cu_k[-1])
+    got = []
+    for name, g, want, n in zip(("dq", "dk", "dv"), (dq, dk, dv), ref, (nq, nk, nk)):
+        g = (g.permute(1, 0, 2).unsqueeze(0) if thd else g).double().cpu().numpy()
+        assert np.all(g[:, :, n:] == SENTINEL), f"{name}: a packed row outside every sequence was written"
+        g = g[:, :, :n]
+        assert np.all(np.isfinite(g)), f"{name}: non-finite"
+        err = float(np.max(np.abs(g - want[:, :, :n]))) if g.size else 0.0
+        mag = float(np.max(np.abs(want[:, :, :n]))) if g.size else 0.0
+        assert err <= TOL_GRAD[dtype] * max(mag, 1e-3), f"{name}: max|d| = {err:.3e}, max|ref| = {mag:.3e}"
+        got.append(g)
+    return cu_q, cu_k, got
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("thd", [False, True])
+def test_varlen(causal, thd):
+    # a sequence without queries (its keys: dK = dV = 0), one without keys
+    # (its rows: dQ = 0), single rows, whole and ragged 128-row blocks, and
+    # packed rows past the last sequence
+    lens_q = [5, 0, 135, 60, 1, 300, 128, 129]
+    lens_k = [7, 23, 0, 300, 1, 290, 128, 500]
+    cu_q, cu_k, (dq, dk, dv) = check_bwd_varlen(400, lens_q, lens_k, 4, 2, 128, "bf16", causal, thd=thd,
+                                                extra_q=10, extra_k=6)
+    assert np.all(dk[:, :, cu_k[1]:cu_k[2]] == 0) and np.all(dv[:, :, cu_k[1]:cu_k[2]] == 0)
+    assert np.all(dq[:, :, cu_q[2]:cu_q[3]] == 0)
+
+
+def test_varlen_with_window_alibi_gqa():
+    check_bwd_varlen(401, [200, 17, 260], [200, 300, 260], 8, 2, 64, "fp16", True, window=(50, -1),
+                     alibi=[2.0 ** (-(i + 1)) for i in range(8)])
+
+
+@pytest.mark.parametrize("D", [16, 32, 64])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_varlen_head_dims(D, dtype):
+    check_bwd_varlen(402 + D, [33, 129, 256, 70], [40, 100, 300, 1], 2, 1, D, dtype, False, window=(-1, 40))
+
+
+def test_varlen_window_both_sides_causal_alibi():
+    check_bwd_varlen(420, [500, 64, 1, 383], [500, 64, 3, 383], 4, 4, 128, "bf16", True, window=(100, 30),
+                     alibi=[0.5, 0.25, 0.125, 0.0625])
+
+
+def test_varlen_key_bound_defaults_to_the_packed_total():
+    # max_seqlen_k = 0: the kernel bounds each sequence's key blocks by the
+    # packed total instead of the longest sequence; the gradients are the same
+    import torch
+    a = check_bwd_varlen(421, [100, 300], [260, 140], 2, 2, 64, "bf16", True)[2]
+    b = check_bwd_varlen(421, [100, 300], [260, 140], 2, 2, 64, "bf16", True, max_seqlen_k=0)[2]
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+
+
+def test_varlen_longer_sequences():
+    # a packed batch of 5.4K rows: sequences from 1 to 2000 rows, GQA 4:1
+    check_bwd_varlen(422, [2000, 1, 1500, 129, 1800], [2000, 5, 1500, 700, 1800], 4, 1, 128, "bf16", True,
+                     extra_q=3)
