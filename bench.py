@@ -341,8 +341,7 @@ def run_native(args, rank, world, device):
         result["split_kv_shapes"] = [measure_shape(name, device, stream, peaks, impl=impl)
                                      for name in SPLIT_SHAPES for impl in ("fwd", "splitkv")]
         result["variant_shapes"] = [measure_variant(name, device, stream, peaks) for name in VARIANT_SHAPES]
-        result["variant_shapes"] += [measure_variant(name, device, stream, peaks, bwd=True) for name in VARIANT_SHAPES
-                                     if VARIANT_SHAPES[name][9] is None]
+        result["variant_shapes"] += [measure_variant(name, device, stream, peaks, bwd=True) for name in VARIANT_SHAPES]
         result["bwd_shapes"] = [r for name in BWD_SHAPES for r in measure_bwd(name, device, stream, peaks)]
     return result
 
@@ -600,7 +599,7 @@ def variant_flops(Z, Hq, N, D, causal, window, lens):
 
 def measure_variant(name, device, stream, peaks, steps=10, bwd=False):
     """TFLOP/s of fa_fwd_ex on a window / ALiBi / variable-length workload (kept pairs only); with bwd,
-    of fa_bwd_ex on a dense one (5 products of the kept pairs)."""
+    of fa_bwd_ex on it (5 products of the kept pairs)."""
     import numpy as np
     import torch
 
@@ -616,8 +615,10 @@ def measure_variant(name, device, stream, peaks, steps=10, bwd=False):
         shape_q, shape_k = (1, Hq, total, D), (1, Hkv, total, D)
         cu_t = torch.from_numpy(cu).to(device)
         kw.update(cu_seqlens_q=cu_t, cu_seqlens_k=cu_t, max_seqlen_q=int(lens.max()))
+        bwd_kw = dict(cu_seqlens_q=cu_t, cu_seqlens_k=cu_t, max_seqlen_q=int(lens.max()), max_seqlen_k=int(lens.max()))
     else:
         shape_q, shape_k = (Z, Hq, N, D), (Z, Hkv, N, D)
+        bwd_kw = {}
     nq, nk = int(np.prod(shape_q)), int(np.prod(shape_k))
     q = si.as_torch(si.normals(0, 0, nq, dtype).reshape(shape_q), dtype).to(device)
     k = si.as_torch(si.normals(0, nq, nk, dtype).reshape(shape_k), dtype).to(device)
@@ -633,13 +634,14 @@ def measure_variant(name, device, stream, peaks, steps=10, bwd=False):
     if bwd:
         o, lse = fa.fa_fwd_ex(q, k, v, causal=causal, window=window, stream=stream, **kw)
         do = si.as_torch(si.normals(1, 0, nq, dtype).reshape(shape_q), dtype).to(device)
-        ws = torch.empty(fa.fa_bwd_workspace_size(Z, Hq, N, D), dtype=torch.uint8, device=device)
+        rows = int(lens.max()) if lens is not None else N  # packed: rows of the longest sequence
+        ws = torch.empty(fa.fa_bwd_workspace_size(Z, Hq, rows, D), dtype=torch.uint8, device=device)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         slopes = kw.get("alibi_slopes")
 
         def call():  # noqa: F811 (the timed call of this mode)
             fa.fa_bwd_ex(q, k, v, o, lse, do, dq, dk, dv, causal=causal, window=window, alibi_slopes=slopes,
-                         workspace=ws, stream=stream)
+                         workspace=ws, stream=stream, **bwd_kw)
 
     for _ in range(3):
         call()

@@ -52,10 +52,14 @@ static cudaError_t launch_one(const BwdLaunchArgs& a) {
 #define FA_CAT2(a, b) a##b
 #define FA_CAT(a, b) FA_CAT2(a, b)
 // variant 0: fa_bwd; 1: window (fa_bwd_ex); 2: window and ALiBi; 3: packed
-// variable-length sequences, with or without a window and slopes (head dims
-// up to 128)
+// variable-length sequences with a window and ALiBi; 4: packed sequences with
+// a window (head dims up to 128)
 cudaError_t FA_CAT(launch_bwd_d, FA_HEAD_DIM)(const BwdLaunchArgs& a, bool causal, bool bf16, int variant) {
 #if FA_HEAD_DIM != 256
+    if (variant == 4) {
+        if (causal) return bf16 ? launch_one<true, true, 4>(a) : launch_one<true, false, 4>(a);
+        return bf16 ? launch_one<false, true, 4>(a) : launch_one<false, false, 4>(a);
+    }
     if (variant == 3) {
         if (causal) return bf16 ? launch_one<true, true, 3>(a) : launch_one<true, false, 3>(a);
         return bf16 ? launch_one<false, true, 3>(a) : launch_one<false, false, 3>(a);

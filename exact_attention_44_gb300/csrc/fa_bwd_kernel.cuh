@@ -163,6 +163,11 @@ __device__ __forceinline__ int unit_at(int pos) {
 // group reads (Q, dO) fit in a third of L2; within a group key blocks are
 // outermost and heads innermost.  A unit's steps run over the group's query
 // heads and, per head, the query blocks from i0 on.
+// Variant kernels: VAR 0 plain; 1 window; 2 window and ALiBi; 3 packed
+// sequences with a window and ALiBi; 4 packed sequences with a window.
+constexpr bool bwd_alibi(int VAR) { return VAR == 2 || VAR == 3; }
+constexpr bool bwd_varlen(int VAR) { return VAR >= 3; }
+
 // zc, qrow0, krow0: the batch coordinate and first query / key row of the
 // unit's sequence in the tensor maps; nq, nk: its query and key counts (the
 // whole tensors but for packed variable-length batches).
@@ -171,8 +176,8 @@ struct BwdUnit {
     int zc, qrow0, krow0, nq, nk;
 };
 
-// Sequence z's rows and counts (VAR = 3 with a sequence table), else the
-// dense batch z's.  Offsets are clamped to the packed extents.
+// Sequence z's rows and counts (packed variants with a sequence table), else
+// the dense batch z's.  Offsets are clamped to the packed extents.
 template <int VAR, typename U>
 __device__ __forceinline__ void unit_sequence(U& w, const BwdParams& p) {
     w.zc = w.z;
@@ -180,7 +185,7 @@ __device__ __forceinline__ void unit_sequence(U& w, const BwdParams& p) {
     w.krow0 = 0;
     w.nq = p.Nq;
     w.nk = p.Nkv;
-    if constexpr (VAR == 3) {
+    if constexpr (bwd_varlen(VAR)) {
         if (p.cu_q != nullptr) {
             auto clampi = [](int x, int hi) { return x < 0 ? 0 : (x > hi ? hi : x); };
             const int q0 = clampi(__ldg(p.cu_q + w.z), p.Nq), q1 = clampi(__ldg(p.cu_q + w.z + 1), p.Nq);
@@ -194,8 +199,7 @@ __device__ __forceinline__ void unit_sequence(U& w, const BwdParams& p) {
     }
 }
 
-// Variant kernels (VAR = 1: window, 2: window and ALiBi, 3: the same on
-// packed sequences) visit only the query blocks holding a row that keeps a
+// Variant kernels (window, ALiBi, packed sequences) visit only the query blocks holding a row that keeps a
 // key of block j: rows j·128 − win_right .. j·128 + 127 + win_left (of the
 // unit's sequence).
 template <bool CAUSAL, int VAR = 0>
@@ -214,7 +218,7 @@ __device__ __forceinline__ BwdUnit bwd_unit(int u, const BwdParams& p) {
     // the key block's own index see none of its keys
     w.i0 = CAUSAL ? w.j : 0;
     int i_end = p.Tq;
-    if constexpr (VAR == 3) {
+    if constexpr (bwd_varlen(VAR)) {
         // the sequence's query blocks; a key block past its keys has none
         i_end = (w.nq + 127) / 128 < p.Tq ? (w.nq + 127) / 128 : p.Tq;
         if (w.j * 128 >= w.nk) i_end = 0;
@@ -273,9 +277,9 @@ __device__ __forceinline__ DqUnit dq_unit(int u, const BwdParams& p) {
     w.hq = head % p.Hq;
     w.hk = w.hq / p.group;
     unit_sequence<VAR>(w, p);
-    w.skip = VAR == 3 && w.i * 128 >= w.nq;
+    w.skip = bwd_varlen(VAR) && w.i * 128 >= w.nq;
     int tk = p.Tk;
-    if constexpr (VAR == 3) {
+    if constexpr (bwd_varlen(VAR)) {
         // the sequence's key blocks (a sequence without keys: one, masked)
         tk = (w.nk + 127) / 128 < p.Tk ? (w.nk + 127) / 128 : p.Tk;
         tk = tk > 0 ? tk : 1;
@@ -519,7 +523,7 @@ __device__ void kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar0, ui
                 VAR == 0 || var_block_kept<CAUSAL>((i - w.j) * 128 - 127, (i - w.j) * 128 + 127, w.j * 128 + 128, w.nk, p);
             const int key = w.j * 128 + row;
             const float slope2 =
-                (VAR == 2 || (VAR == 3 && p.alibi != nullptr)) ? -__ldg(p.alibi + hq) * 1.4426950408889634f : 0.f;
+                bwd_alibi(VAR) ? -__ldg(p.alibi + hq) * 1.4426950408889634f : 0.f;
             const float dbf = (float)(dbase + h * 64);  // d of this half's first column (exact: |d| < 2^24)
             uint32_t pk[32];  // Pᵀ in the input type: the dV operand, and what dS uses
 #pragma unroll
@@ -538,7 +542,7 @@ __device__ void kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar0, ui
                         if (diag && row > col + 1) e1 = -INFINITY;
                     } else {
                         const int d0 = dbase + col;
-                        if constexpr (VAR >= 2) {
+                        if constexpr (bwd_alibi(VAR)) {
                             const float df = dbf + (float)(32 * cc + 2 * x);
                             e0 = fmaf(slope2, fabsf(df), e0);
                             e1 = fmaf(slope2, fabsf(df + 1.f), e1);
@@ -657,7 +661,7 @@ __device__ void kv_epilogue(const CUtensorMap* tmDK, const CUtensorMap* tmDV, co
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(T::KB_ACC_FREE));
         };
-        if (VAR != 3 || p.cu_k == nullptr || key0 + 32 <= w.nk) {
+        if (!bwd_varlen(VAR) || p.cu_k == nullptr || key0 + 32 <= w.nk) {
             tma_store_rows<D, T::SW, BF16>(tmem + lane_addr + T::TM_DV, 1.f, stage, tmDV, w.krow0 + key0, w.hk, w.zc,
                                            key0 < w.nk, []() {});
             tma_store_rows<D, T::SW, BF16>(tmem + lane_addr + T::TM_DK, p.scale, stage, tmDK, w.krow0 + key0, w.hk,
@@ -818,7 +822,7 @@ __device__ void q_softmax(const BwdParams& p, uint32_t bar0, uint32_t tmem, int 
         const int64_t r = ((int64_t)w.z * p.Hq + w.hq) * p.Tq * 128 + (int64_t)w.i * 128 + row;
         const float l2 = __ldg(p.lse2 + r), dl = __ldg(p.delta + r);
         const float slope2 =
-            (VAR == 2 || (VAR == 3 && p.alibi != nullptr)) ? -__ldg(p.alibi + w.hq) * 1.4426950408889634f : 0.f;
+            bwd_alibi(VAR) ? -__ldg(p.alibi + w.hq) * 1.4426950408889634f : 0.f;
         for (int j = 0; j < w.nkv; ++j, ++g) {
             const uint32_t st = g & 1u;
             const uint32_t slot = tmem + lane_addr + T::TM_QS + st * 128;
@@ -846,7 +850,7 @@ __device__ void q_softmax(const BwdParams& p, uint32_t bar0, uint32_t tmem, int 
                         if (diag && col + 1 > row) e1 = -INFINITY;
                     } else {
                         const int d0 = dbase - col;
-                        if constexpr (VAR >= 2) {
+                        if constexpr (bwd_alibi(VAR)) {
                             const float df = dbf - (float)(32 * cc + 2 * x);
                             e0 = fmaf(slope2, fabsf(df), e0);
                             e1 = fmaf(slope2, fabsf(df - 1.f), e1);
@@ -915,7 +919,7 @@ __device__ void q_epilogue(const CUtensorMap* tmDQ, const BwdParams& p, uint32_t
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(T::QB_DQ_FREE));
         };
-        if (VAR != 3 || p.cu_q == nullptr || q0 + 32 <= w.nq) {
+        if (!bwd_varlen(VAR) || p.cu_q == nullptr || q0 + 32 <= w.nq) {
             tma_store_rows<D, T::SW, BF16>(tmem + lane_addr + T::TM_DQ, p.scale, stage, tmDQ, w.qrow0 + q0, w.hq, w.zc,
                                            q0 < w.nq, release);
         } else {

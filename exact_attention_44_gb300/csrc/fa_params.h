@@ -142,7 +142,7 @@ struct BwdParams {
     // ALiBi adds -alibi[hq] * |i - j| to the scaled score
     int win_left, win_right;
     const float* alibi;      // (Hq) slopes, or nullptr
-    // packed variable-length batches (VAR = 3): Z counts sequences, sequence
+    // packed variable-length batches (VAR 3, 4): Z counts sequences, sequence
     // z owns query rows cu_q[z] .. cu_q[z+1]-1 and key rows cu_k[z] ..
     // cu_k[z+1]-1 of (1, H, total, D) tensors (Nq, Nkv: the totals; Tq, Tk:
     // blocks of the longest sequence); lse is (Hq, Nq)
