@@ -67,7 +67,7 @@ struct BwdTraits {
     static constexpr int KV_OFF_OST = (KV_OFF_DELTA + 2 * 512 + 1023) / 1024 * 1024;
     static constexpr int KV_OFF_BAR = KV_OFF_OST + 128 * SW;
     static constexpr int KB_KV_FULL = 0;      // K, V of a unit landed (TMA)
-    static constexpr int KB_KV_EMPTY = 1;     // the unit's products are done (commit)
+    static constexpr int KB_KV_EMPTY = 1;     // the unit's last Sᵀ and dPᵀ are done (commit)
     static constexpr int KB_QD_FULL = 2;      // [2] Q, dO, lse2, Δ of a step landed (TMA)
     static constexpr int KB_QD_EMPTY = 4;     // [2] that step's products are done (commit)
     static constexpr int KB_S_FULL = 6;       // Sᵀ in TMEM (commit)
@@ -96,7 +96,7 @@ struct BwdTraits {
     static constexpr int Q_OFF_OST = Q_OFF_V + 2 * TILE;       // dQ staging (as KV_OFF_OST)
     static constexpr int Q_OFF_BAR = Q_OFF_OST + 128 * SW;
     static constexpr int QB_QD_FULL = 0;      // Q, dO of a unit landed (TMA)
-    static constexpr int QB_QD_EMPTY = 1;     // the unit's products are done (commit)
+    static constexpr int QB_QD_EMPTY = 1;     // the unit's last S and dP are done (commit)
     static constexpr int QB_KV_FULL = 2;      // [2] K, V of a key block landed (TMA)
     static constexpr int QB_KV_EMPTY = 4;     // [2] that block's products are done (commit)
     static constexpr int QB_S_FULL = 6;       // [2] S in its TMEM slot (commit)
@@ -165,8 +165,8 @@ __device__ __forceinline__ int unit_at(int pos) {
 // heads and, per head, the query blocks from i0 on.
 // Variant kernels: VAR 0 plain; 1 window; 2 window and ALiBi; 3 packed
 // sequences with a window and ALiBi; 4 packed sequences with a window.
-constexpr bool bwd_alibi(int VAR) { return VAR == 2 || VAR == 3; }
-constexpr bool bwd_varlen(int VAR) { return VAR >= 3; }
+__host__ __device__ constexpr bool bwd_alibi(int VAR) { return VAR == 2 || VAR == 3; }
+__host__ __device__ constexpr bool bwd_varlen(int VAR) { return VAR >= 3; }
 
 // zc, qrow0, krow0: the batch coordinate and first query / key row of the
 // unit's sequence in the tensor maps; nq, nk: its query and key counts (the
@@ -457,6 +457,9 @@ __device__ void kv_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0, uin
                 ptx::mma_ss(tmem + T::TM_DP, ptx::desc64(v_lo + kmaj_off(kk, T::SWE, T::SW), HI),
                             ptx::desc64(do_lo + kmaj_off(kk, T::SWE, T::SW), HI), ID_SQ, kk > 0 ? 1u : 0u);
             ptx::tc_commit(bar(T::KB_DP_FULL));
+            // the unit's last Sᵀ and dPᵀ were its last reads of K and V: the
+            // next unit's K, V may land while its last dV, dK run
+            if (s + 1 == w.nsteps) ptx::tc_commit(bar(T::KB_KV_EMPTY));
             // dV += Pᵀ dOᵢ; a unit's first step waits for the last unit's dK, dV to be read
             if (!wait_phase(bar(T::KB_P_FULL), t & 1u, ctl, SITE_B_P_FULL)) { ok = false; break; }
             if (s == 0 && uc > 0 && !wait_phase(bar(T::KB_ACC_FREE), (uc - 1) & 1u, ctl, SITE_B_ACC_FREE)) {
@@ -480,7 +483,6 @@ __device__ void kv_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0, uin
         }
         if (!ok) break;
         ptx::tc_commit(bar(T::KB_ACC_FULL));  // dK, dV of the unit complete
-        ptx::tc_commit(bar(T::KB_KV_EMPTY));  // K, V free
         ++uc;
     }
     // every MMA of this phase completes before the dQ phase reuses shared memory
@@ -656,8 +658,10 @@ __device__ void kv_epilogue(const CUtensorMap* tmDK, const CUtensorMap* tmDV, co
         // dV, then dK (x scale), as 32-row boxes of this warp's keys; a box
         // that starts past the last key has nothing to store
         const int key0 = w.j * 128 + 32 * quad;
+        // dK and dV read: the next unit may accumulate into them (a separate
+        // signal for dV, letting the next unit's first dV start before dK is
+        // read, measured 2 % slower at N = 8192 on GB300)
         const auto release = [&]() {
-            // dK and dV read: the next unit may accumulate into them
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(T::KB_ACC_FREE));
         };
@@ -776,6 +780,9 @@ __device__ void q_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0, uint
         if (!wait_phase(bar(T::QB_QD_FULL), uc & 1u, ctl, SITE_B_QD_FULL)) { ok = false; break; }
         if (!issue_s(g)) { ok = false; break; }
         issue_dp(g);
+        // the unit's last S and dP are its last reads of Q and dO: the next
+        // unit's Q, dO may land while its last dQ products run
+        if (w.nkv == 1) ptx::tc_commit(bar(T::QB_QD_EMPTY));
         for (int j = 0; j < w.nkv; ++j, ++g) {
             const uint32_t st = g & 1u;
             if (j + 1 < w.nkv && !issue_s(g + 1)) { ok = false; break; }
@@ -791,11 +798,13 @@ __device__ void q_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0, uint
                 ptx::mma_ts(tmem + T::TM_DQ, tmem + T::TM_QS + st * 128 + packed_col(kk),
                             ptx::desc64(kmn_lo + ((kk * 16 * T::SW) >> 4), HI), ID_DQ, (j > 0 || kk > 0) ? 1u : 0u);
             ptx::tc_commit(bar(T::QB_KV_EMPTY + st));  // K_g, V_g free
-            if (j + 1 < w.nkv) issue_dp(g + 1);
+            if (j + 1 < w.nkv) {
+                issue_dp(g + 1);
+                if (j + 2 == w.nkv) ptx::tc_commit(bar(T::QB_QD_EMPTY));  // Q, dO free
+            }
         }
         if (!ok) break;
         ptx::tc_commit(bar(T::QB_DQ_FULL));   // dQ of the unit complete
-        ptx::tc_commit(bar(T::QB_QD_EMPTY));  // Q, dO free
         ++uc;
     }
     if (!ok) {
