@@ -60,7 +60,7 @@ struct WideTraits {
     static constexpr int KV_OFF_OST = (KV_OFF_DELTA + 512 + 1023) / 1024 * 1024;  // epilogue staging
     static constexpr int KV_OFF_BAR = KV_OFF_OST + 128 * SW;
     static constexpr int KB_K_FULL = 0;       // K of a unit landed (TMA)
-    static constexpr int KB_KV_EMPTY = 1;     // the unit's products are done (commit)
+    static constexpr int KB_KV_EMPTY = 1;     // the unit's last Sᵀ and dPᵀ are done (commit)
     static constexpr int KB_QD_FULL = 2;      // [2] Q, dO, lse2, Δ of a step landed in slot b
     static constexpr int KB_QD_EMPTY = 4;     // [2] that step's products are done (commit)
     static constexpr int KB_S_FULL = 6;       // [2] Sᵀ (and dPᵀ in the dK pass) in TMEM (commit)
@@ -82,7 +82,7 @@ struct WideTraits {
     static constexpr int Q_OFF_OST = Q_OFF_V + TILE64;
     static constexpr int Q_OFF_BAR = Q_OFF_OST + 128 * SW;
     static constexpr int QB_QD_FULL = 0;      // Q, dO of a unit landed
-    static constexpr int QB_QD_EMPTY = 1;     // the unit's products are done (commit)
+    static constexpr int QB_QD_EMPTY = 1;     // the unit's last S and dP are done (commit)
     static constexpr int QB_KV_FULL = 2;      // K, V of a step landed
     static constexpr int QB_KV_EMPTY = 3;     // that step's products are done (commit)
     static constexpr int QB_S_FULL = 4;       // S and dP in TMEM (commit)
@@ -181,7 +181,8 @@ __device__ void wide_kv_producer(const CUtensorMap* tmK, const CUtensorMap* tmV,
         const BwdUnit w = bwd_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
         if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_LOAD)) { ok = false; break; }
         if (w.nsteps == 0) continue;
-        // K and the V region (slot 1, then V) are free once the previous unit is done
+        // K and the V region (slot 1, then V) are free once the previous
+        // unit's last Sᵀ and dPᵀ are done
         if (uc > 0 && !wait_phase(bar(T::KB_KV_EMPTY), (uc - 1) & 1u, ctl, SITE_B_KV_EMPTY)) { ok = false; break; }
         if (p.inject_stall && blockIdx.x == 0 && uc == 0) {
             withheld = true;  // never issued: the issuer's wait for K must time out
@@ -292,6 +293,9 @@ __device__ void wide_kv_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0
                 ptx::mma_ss(tmem + T::TM_DP, ptx::desc64(v_lo + wide_kmaj(kk, 128), HI),
                             ptx::desc64(do_lo(0) + wide_kmaj(kk, 64), HI), ID_S, kk > 0 ? 1u : 0u);
             ptx::tc_commit(bar(T::KB_S_FULL));
+            // the unit's last Sᵀ and dPᵀ were its last reads of K and V: the
+            // next unit's K (and slot 1, over V) may land during the last dK step
+            if (s + 1 == steps) ptx::tc_commit(bar(T::KB_KV_EMPTY));
             if (!wait_phase(bar(T::KB_P_FULL), nb & 1u, ctl, SITE_B_P_FULL) ||
                 !accumulate(T::TM_DP, qmn_lo(0), 0, s, steps)) {
                 ok = false;
@@ -299,7 +303,6 @@ __device__ void wide_kv_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0
             }
         }
         if (!ok) break;
-        ptx::tc_commit(bar(T::KB_KV_EMPTY));
         ++uc;
     }
     // every MMA of this phase completes before the dQ phase reuses shared memory
@@ -511,6 +514,8 @@ __device__ void wide_q_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0,
                 ptx::mma_ss(tmem + T::TM_DP, ptx::desc64(do_lo + wide_kmaj(kk, 128), HI),
                             ptx::desc64(v_lo + wide_kmaj(kk, 64), HI), ID_S, kk > 0 ? 1u : 0u);
             ptx::tc_commit(bar(T::QB_S_FULL));
+            // the unit's last S and dP were its last reads of Q and dO
+            if (s + 1 == steps) ptx::tc_commit(bar(T::QB_QD_EMPTY));
             if (!wait_phase(bar(T::QB_DS_FULL), g & 1u, ctl, SITE_B_DS_FULL)) { ok = false; break; }
             if (s == 0 && uc > 0 && !wait_phase(bar(T::QB_DQ_FREE), (uc - 1) & 1u, ctl, SITE_B_DQ_FREE)) {
                 ok = false;
@@ -525,7 +530,6 @@ __device__ void wide_q_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0,
         }
         if (!ok) break;
         ptx::tc_commit(bar(T::QB_DQ_FULL));
-        ptx::tc_commit(bar(T::QB_QD_EMPTY));
         ++uc;
     }
     if (!ok) {
