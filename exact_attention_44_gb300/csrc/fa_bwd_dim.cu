@@ -23,7 +23,7 @@ static cudaError_t launch_one(const BwdLaunchArgs& a) {
     constexpr int SMEM = WideTraits::SMEM_BYTES, THREADS = WIDE_THREADS;
 #else
     auto bwd = fa_bwd_kernel<D, CAUSAL, BF16, VAR>;
-    constexpr int SMEM = BwdTraits<D>::FUSED_SMEM_BYTES, THREADS = BWD_THREADS;
+    constexpr int SMEM = BwdTraits<D>::FUSED_SMEM_BYTES, THREADS = BwdWarps<D>::THREADS;
 #endif
     static std::atomic<uint64_t> configured{0};  // context the opt-in shared memory size was set in
     cudaError_t err;

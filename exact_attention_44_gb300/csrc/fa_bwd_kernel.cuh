@@ -24,9 +24,9 @@
 // the result is bitwise reproducible; the price is recomputing S and dP in
 // the dQ phase (7 tensor-core products per block pair instead of 5).
 //
-// Warps (both phases): 0-3 and 4-7 the two column halves of each
-// 128x128 block (thread = TMEM lane), 8-11 the epilogue, 12 the TMA producer,
-// 13 the MMA issuer.  Every wait is bounded as in the forward kernel.  Head
+// Warps (both phases): column groups of each 128x128 block (thread = TMEM
+// lane; four groups of 32 columns, warps 0-15, at D = 128, else two of 64,
+// warps 0-7), then the 4 epilogue warps, the TMA producer and the MMA issuer.  Every wait is bounded as in the forward kernel.  Head
 // dims 16 to 128 (the dK/dV phase's TMEM holds Sᵀ/Pᵀ, dPᵀ/dSᵀ, dV and dK:
 // 256 + 2D columns).
 #pragma once
@@ -35,7 +35,34 @@
 
 namespace fa {
 
-constexpr int BWD_THREADS = 14 * 32;
+// The softmax warps of both phases split the 128 columns of a block into NG
+// groups of CW (4 warps each, one per TMEM lane quarter); then 4 epilogue
+// warps, the TMA producer and the MMA issuer.  Four groups at D = 128, two
+// below (measured on GB300: four groups +4 % at Z1 Hq32 Hkv8 N8192 D128,
+// level at N1024; at D = 64 3-4 % slower than two).
+template <int D>
+struct BwdWarps {
+    static constexpr int NG = D == 128 ? 4 : 2;
+    static constexpr int CW = 128 / NG;
+    static constexpr int CH = CW == 32 ? 16 : 32;  // columns per softmax TMEM load
+    static constexpr int SOFTMAX_WARPS = 4 * NG;
+    static constexpr int THREADS = (SOFTMAX_WARPS + 6) * 32;
+};
+
+// TMEM loads and stores of a width fixed at compile time
+template <int N>
+__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, uint32_t (&r)[N]) {
+    static_assert(N == 16 || N == 32, "16 or 32 columns");
+    if constexpr (N == 32) ptx::tmem_ld32(taddr, r);
+    else ptx::tmem_ld16(taddr, r);
+}
+template <int N>
+__device__ __forceinline__ void tmem_st_n(uint32_t taddr, const uint32_t (&r)[N]) {
+    static_assert(N == 8 || N == 16 || N == 32, "8, 16 or 32 columns");
+    if constexpr (N == 32) ptx::tmem_st32(taddr, r);
+    else if constexpr (N == 16) ptx::tmem_st16(taddr, r);
+    else ptx::tmem_st8(taddr, r);
+}
 
 // two fp16 / bf16 values -> float2 (exact)
 template <bool BF16>
@@ -72,8 +99,8 @@ struct BwdTraits {
     static constexpr int KB_QD_EMPTY = 4;     // [2] that step's products are done (commit)
     static constexpr int KB_S_FULL = 6;       // Sᵀ in TMEM (commit)
     static constexpr int KB_DP_FULL = 7;      // dPᵀ in TMEM (commit)
-    static constexpr int KB_P_FULL = 8;       // Pᵀ written over Sᵀ (256)
-    static constexpr int KB_DS_FULL = 9;      // dSᵀ written over dPᵀ (256)
+    static constexpr int KB_P_FULL = 8;       // Pᵀ written over Sᵀ (every softmax thread)
+    static constexpr int KB_DS_FULL = 9;      // dSᵀ written over dPᵀ (every softmax thread)
     static constexpr int KB_ACC_FULL = 10;    // dK, dV of a unit complete (commit)
     static constexpr int KB_ACC_FREE = 11;    // dK, dV read out of TMEM (128)
     static constexpr int KB_DRAIN = 12;
@@ -101,7 +128,7 @@ struct BwdTraits {
     static constexpr int QB_KV_EMPTY = 4;     // [2] that block's products are done (commit)
     static constexpr int QB_S_FULL = 6;       // [2] S in its TMEM slot (commit)
     static constexpr int QB_DP_FULL = 8;      // dP in TMEM (commit)
-    static constexpr int QB_DS_FULL = 9;      // [2] dS written over S in its slot (256)
+    static constexpr int QB_DS_FULL = 9;      // [2] dS written over S in its slot (every softmax thread)
     static constexpr int QB_DQ_FULL = 11;     // dQ of a unit complete (commit)
     static constexpr int QB_DQ_FREE = 12;     // dQ read out of TMEM (128)
     static constexpr int QB_DRAIN = 13;
@@ -124,12 +151,12 @@ struct BwdTraits {
     static_assert(256 + 2 * D <= 512 && 384 + D <= 512, "tensor memory budget");
 
     static __device__ __forceinline__ uint32_t kv_bar_count(int i) {
-        if (i == KB_P_FULL || i == KB_DS_FULL) return 256;
+        if (i == KB_P_FULL || i == KB_DS_FULL) return 32 * BwdWarps<D_>::SOFTMAX_WARPS;
         if (i == KB_ACC_FREE) return 128;
         return 1;
     }
     static __device__ __forceinline__ uint32_t q_bar_count(int i) {
-        if (i == QB_DS_FULL || i == QB_DS_FULL + 1) return 256;
+        if (i == QB_DS_FULL || i == QB_DS_FULL + 1) return 32 * BwdWarps<D_>::SOFTMAX_WARPS;
         if (i == QB_DQ_FREE) return 128;
         return 1;
     }
@@ -141,9 +168,12 @@ __host__ __device__ constexpr uint32_t kmaj_off(int kk, int swe, int sw) {
     return (uint32_t)((((kk * 16) / swe) * (128 * sw) + ((kk * 16) % swe) * 2) >> 4);
 }
 
-// Packed 16-bit columns of a 128-wide block written by two halves over their
-// own fp32 columns: K step kk (16 elements) of the block
-__device__ __forceinline__ uint32_t packed_col(int kk) { return kk < 4 ? kk * 8 : 64 + (kk - 4) * 8; }
+// Packed 16-bit columns of a 128-wide block written by column groups of CW
+// over the first halves of their own fp32 columns: K step kk (16 elements)
+template <int CW>
+__device__ __forceinline__ uint32_t packed_col(int kk) {
+    return (uint32_t)((16 * kk / CW) * CW + (16 * kk % CW) / 2);
+}
 
 // ---------------------------------------------------------------- schedules --
 // CTA c takes one unit per round of `grid` units.  Causal units are ordered
@@ -469,7 +499,7 @@ __device__ void kv_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0, uin
             ptx::tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 128 / 16; ++kk)
-                ptx::mma_ts(tmem + T::TM_DV, tmem + T::TM_S + packed_col(kk),
+                ptx::mma_ts(tmem + T::TM_DV, tmem + T::TM_S + packed_col<BwdWarps<D>::CW>(kk),
                             ptx::desc64(domn_lo + ((kk * 16 * T::SW) >> 4), HI), ID_ND, (s > 0 || kk > 0) ? 1u : 0u);
             if (s + 1 < w.nsteps && !issue_s(t + 1)) { ok = false; break; }
             // dK += dSᵀ Qᵢ
@@ -477,7 +507,7 @@ __device__ void kv_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0, uin
             ptx::tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 128 / 16; ++kk)
-                ptx::mma_ts(tmem + T::TM_DK, tmem + T::TM_DP + packed_col(kk),
+                ptx::mma_ts(tmem + T::TM_DK, tmem + T::TM_DP + packed_col<BwdWarps<D>::CW>(kk),
                             ptx::desc64(qmn_lo + ((kk * 16 * T::SW) >> 4), HI), ID_ND, (s > 0 || kk > 0) ? 1u : 0u);
             ptx::tc_commit(bar(T::KB_QD_EMPTY + st));  // Qᵢ, dOᵢ slot free
         }
@@ -490,9 +520,9 @@ __device__ void kv_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0, uin
     drain_phase(bar(T::KB_DRAIN), 0u, ctl.limit_ns);
 }
 
-// Thread = key (TMEM lane); half h takes queries h*64 .. h*64 + 63 and writes
-// its Pᵀ and dSᵀ (input type, two per column) over its own fp32 columns, so
-// no half overwrites values the other has not read.
+// Thread = key (TMEM lane); column group h takes queries h*CW .. h*CW + CW - 1
+// and writes its Pᵀ and dSᵀ (input type, two per column) over its own fp32
+// columns, so no group overwrites values another has not read.
 template <int D, bool CAUSAL, bool BF16, int VAR>
 __device__ void kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar0, uint32_t tmem, int h, const Ctl& ctl) {
     using T = BwdTraits<D>;
@@ -501,6 +531,7 @@ __device__ void kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar0, ui
     const int row = quad * 32 + threadIdx.x % 32;  // key within the block
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
     const float c = p.scale_log2;
+    constexpr int CW = BwdWarps<D>::CW, CH = BwdWarps<D>::CH;
     uint32_t t = 0;
     for (int pos = blockIdx.x; unit_at<CAUSAL>(pos) < p.nunits; pos += gridDim.x) {
         const BwdUnit w = bwd_unit<CAUSAL, VAR>(unit_at<CAUSAL>(pos), p);
@@ -511,8 +542,8 @@ __device__ void kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar0, ui
             bwd_step(w, s, p, hq, i);
             // lse2 and Δ of the step's queries arrive with Qᵢ (TMA)
             if (!warp_wait_phase(bar(T::KB_QD_FULL + st), (t >> 1) & 1u, ctl, SITE_B_QD_FULL)) return;
-            const uint32_t lse_a = sbase + T::KV_OFF_LSE + st * 512 + h * 256;
-            const uint32_t del_a = sbase + T::KV_OFF_DELTA + st * 512 + h * 256;
+            const uint32_t lse_a = sbase + T::KV_OFF_LSE + st * 512 + h * CW * 4;
+            const uint32_t del_a = sbase + T::KV_OFF_DELTA + st * 512 + h * CW * 4;
             if (!warp_wait_phase(bar(T::KB_S_FULL), t & 1u, ctl, SITE_B_S_FULL)) return;
             ptx::tc_fence_after();
             // causal: only the diagonal block has keys after queries (key > query -> 0)
@@ -526,17 +557,17 @@ __device__ void kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar0, ui
             const int key = w.j * 128 + row;
             const float slope2 =
                 bwd_alibi(VAR) ? -__ldg(p.alibi + hq) * 1.4426950408889634f : 0.f;
-            const float dbf = (float)(dbase + h * 64);  // d of this half's first column (exact: |d| < 2^24)
-            uint32_t pk[32];  // Pᵀ in the input type: the dV operand, and what dS uses
+            const float dbf = (float)(dbase + h * CW);  // d of this group's first column (exact: |d| < 2^24)
+            uint32_t pk[CW / 2];  // Pᵀ in the input type: the dV operand, and what dS uses
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                uint32_t r[32];
-                ptx::tmem_ld32(tmem + lane_addr + T::TM_S + h * 64 + 32 * cc, r);
+            for (int cc = 0; cc < CW / CH; ++cc) {
+                uint32_t r[CH];
+                tmem_ld_n<CH>(tmem + lane_addr + T::TM_S + h * CW + CH * cc, r);
 #pragma unroll
-                for (int x = 0; x < 16; ++x) {
-                    const int col = h * 64 + 32 * cc + 2 * x;
+                for (int x = 0; x < CH / 2; ++x) {
+                    const int col = h * CW + CH * cc + 2 * x;
                     float l0, l1;
-                    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(l0), "=f"(l1) : "r"(lse_a + 4u * (32 * cc + 2 * x)));
+                    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(l0), "=f"(l1) : "r"(lse_a + 4u * (CH * cc + 2 * x)));
                     float e0 = fmaf(__uint_as_float(r[2 * x]), c, -l0);
                     float e1 = fmaf(__uint_as_float(r[2 * x + 1]), c, -l1);
                     if constexpr (VAR == 0) {
@@ -545,7 +576,7 @@ __device__ void kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar0, ui
                     } else {
                         const int d0 = dbase + col;
                         if constexpr (bwd_alibi(VAR)) {
-                            const float df = dbf + (float)(32 * cc + 2 * x);
+                            const float df = dbf + (float)(CH * cc + 2 * x);
                             e0 = fmaf(slope2, fabsf(df), e0);
                             e1 = fmaf(slope2, fabsf(df + 1.f), e1);
                         }
@@ -554,10 +585,10 @@ __device__ void kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar0, ui
                             if (var_dropped<CAUSAL>(d0 + 1, key, w.nk, p)) e1 = -INFINITY;
                         }
                     }
-                    pk[16 * cc + x] = pack2<BF16>(ptx::ex2(e0), ptx::ex2(e1));
+                    pk[(CH / 2) * cc + x] = pack2<BF16>(ptx::ex2(e0), ptx::ex2(e1));
                 }
             }
-            ptx::tmem_st32(tmem + lane_addr + T::TM_S + h * 64, pk);
+            tmem_st_n<CW / 2>(tmem + lane_addr + T::TM_S + h * CW, pk);
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(T::KB_P_FULL));
@@ -565,19 +596,19 @@ __device__ void kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar0, ui
             if (!warp_wait_phase(bar(T::KB_DP_FULL), t & 1u, ctl, SITE_B_DP_FULL)) return;
             ptx::tc_fence_after();
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                uint32_t r[32];
-                ptx::tmem_ld32(tmem + lane_addr + T::TM_DP + h * 64 + 32 * cc, r);
-                uint32_t ds[16];
+            for (int cc = 0; cc < CW / CH; ++cc) {
+                uint32_t r[CH];
+                tmem_ld_n<CH>(tmem + lane_addr + T::TM_DP + h * CW + CH * cc, r);
+                uint32_t ds[CH / 2];
 #pragma unroll
-                for (int x = 0; x < 16; ++x) {
+                for (int x = 0; x < CH / 2; ++x) {
                     float d0, d1;
-                    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(d0), "=f"(d1) : "r"(del_a + 4u * (32 * cc + 2 * x)));
-                    const float2 pp = unpack2<BF16>(pk[16 * cc + x]);
+                    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(d0), "=f"(d1) : "r"(del_a + 4u * (CH * cc + 2 * x)));
+                    const float2 pp = unpack2<BF16>(pk[(CH / 2) * cc + x]);
                     ds[x] = pack2<BF16>(pp.x * (__uint_as_float(r[2 * x]) - d0), pp.y * (__uint_as_float(r[2 * x + 1]) - d1));
                 }
-                // packed columns h*64 + 16cc .. : fp32 columns this thread has already read
-                ptx::tmem_st16(tmem + lane_addr + T::TM_DP + h * 64 + 16 * cc, ds);
+                // packed columns h*CW + (CH/2)cc .. : fp32 columns this thread has already read
+                tmem_st_n<CH / 2>(tmem + lane_addr + T::TM_DP + h * CW + (CH / 2) * cc, ds);
             }
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
@@ -795,7 +826,7 @@ __device__ void q_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0, uint
             const uint32_t kmn_lo = ptx::smem_desc_lo(sbase + T::Q_OFF_K + st * T::TILE, 128 * T::SW);
 #pragma unroll
             for (int kk = 0; kk < 128 / 16; ++kk)
-                ptx::mma_ts(tmem + T::TM_DQ, tmem + T::TM_QS + st * 128 + packed_col(kk),
+                ptx::mma_ts(tmem + T::TM_DQ, tmem + T::TM_QS + st * 128 + packed_col<BwdWarps<D>::CW>(kk),
                             ptx::desc64(kmn_lo + ((kk * 16 * T::SW) >> 4), HI), ID_DQ, (j > 0 || kk > 0) ? 1u : 0u);
             ptx::tc_commit(bar(T::QB_KV_EMPTY + st));  // K_g, V_g free
             if (j + 1 < w.nkv) {
@@ -813,7 +844,7 @@ __device__ void q_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0, uint
     }
 }
 
-// Thread = query (TMEM lane); half h takes keys h*64 .. h*64 + 63 of each
+// Thread = query (TMEM lane); column group h takes keys h*CW .. h*CW + CW - 1 of each
 // block.  lse2 and Δ are per row, so they stay in registers for the unit.
 template <int D, bool CAUSAL, bool BF16, int VAR>
 __device__ void q_softmax(const BwdParams& p, uint32_t bar0, uint32_t tmem, int h, const Ctl& ctl, int first) {
@@ -823,6 +854,7 @@ __device__ void q_softmax(const BwdParams& p, uint32_t bar0, uint32_t tmem, int 
     const int row = quad * 32 + threadIdx.x % 32;  // query within the block
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
     const float c = p.scale_log2;
+    constexpr int CW = BwdWarps<D>::CW, CH = BwdWarps<D>::CH;
     uint32_t g = 0;
     for (int pos = first; unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x) {
         const DqUnit w = dq_unit<CAUSAL, VAR>(unit_at<CAUSAL>(pos), p);
@@ -841,17 +873,17 @@ __device__ void q_softmax(const BwdParams& p, uint32_t bar0, uint32_t tmem, int 
             const bool diag = CAUSAL && jj == w.i;  // key > query only on the diagonal block
             // variants: d = query − key = dbase − col (as in the dK/dV phase)
             const int dbase = (w.i - jj) * 128 + row;
-            const float dbf = (float)(dbase - h * 64);  // d of this half's first column (exact: |d| < 2^24)
+            const float dbf = (float)(dbase - h * CW);  // d of this group's first column (exact: |d| < 2^24)
             const bool full =
                 VAR == 0 || var_block_kept<CAUSAL>((w.i - jj) * 128 - 127, (w.i - jj) * 128 + 127, jj * 128 + 128, w.nk, p);
-            uint32_t pk[32];
+            uint32_t pk[CW / 2];
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                uint32_t rr[32];
-                ptx::tmem_ld32(slot + h * 64 + 32 * cc, rr);
+            for (int cc = 0; cc < CW / CH; ++cc) {
+                uint32_t rr[CH];
+                tmem_ld_n<CH>(slot + h * CW + CH * cc, rr);
 #pragma unroll
-                for (int x = 0; x < 16; ++x) {
-                    const int col = h * 64 + 32 * cc + 2 * x;
+                for (int x = 0; x < CH / 2; ++x) {
+                    const int col = h * CW + CH * cc + 2 * x;
                     float e0 = fmaf(__uint_as_float(rr[2 * x]), c, -l2);
                     float e1 = fmaf(__uint_as_float(rr[2 * x + 1]), c, -l2);
                     if constexpr (VAR == 0) {
@@ -860,7 +892,7 @@ __device__ void q_softmax(const BwdParams& p, uint32_t bar0, uint32_t tmem, int 
                     } else {
                         const int d0 = dbase - col;
                         if constexpr (bwd_alibi(VAR)) {
-                            const float df = dbf - (float)(32 * cc + 2 * x);
+                            const float df = dbf - (float)(CH * cc + 2 * x);
                             e0 = fmaf(slope2, fabsf(df), e0);
                             e1 = fmaf(slope2, fabsf(df - 1.f), e1);
                         }
@@ -869,23 +901,23 @@ __device__ void q_softmax(const BwdParams& p, uint32_t bar0, uint32_t tmem, int 
                             if (var_dropped<CAUSAL>(d0 - 1, jj * 128 + col + 1, w.nk, p)) e1 = -INFINITY;
                         }
                     }
-                    pk[16 * cc + x] = pack2<BF16>(ptx::ex2(e0), ptx::ex2(e1));
+                    pk[(CH / 2) * cc + x] = pack2<BF16>(ptx::ex2(e0), ptx::ex2(e1));
                 }
             }
             if (!warp_wait_phase(bar(T::QB_DP_FULL), g & 1u, ctl, SITE_B_DP_FULL)) return;
             ptx::tc_fence_after();
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                uint32_t rr[32];
-                ptx::tmem_ld32(tmem + lane_addr + T::TM_QDP + h * 64 + 32 * cc, rr);
-                uint32_t ds[16];
+            for (int cc = 0; cc < CW / CH; ++cc) {
+                uint32_t rr[CH];
+                tmem_ld_n<CH>(tmem + lane_addr + T::TM_QDP + h * CW + CH * cc, rr);
+                uint32_t ds[CH / 2];
 #pragma unroll
-                for (int x = 0; x < 16; ++x) {
-                    const float2 pp = unpack2<BF16>(pk[16 * cc + x]);
+                for (int x = 0; x < CH / 2; ++x) {
+                    const float2 pp = unpack2<BF16>(pk[(CH / 2) * cc + x]);
                     ds[x] = pack2<BF16>(pp.x * (__uint_as_float(rr[2 * x]) - dl), pp.y * (__uint_as_float(rr[2 * x + 1]) - dl));
                 }
                 // dS over the slot's packed columns h*64 + 16cc .. (S already read)
-                ptx::tmem_st16(slot + h * 64 + 16 * cc, ds);
+                tmem_st_n<CH / 2>(slot + h * CW + (CH / 2) * cc, ds);
             }
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
@@ -959,7 +991,7 @@ __device__ void q_epilogue(const CUtensorMap* tmDQ, const BwdParams& p, uint32_t
 // used for data; they are set up only after every role of that phase has
 // finished: its MMAs drained, its tensor stores read out.
 template <int D, bool CAUSAL, bool BF16, int VAR>
-__global__ void __launch_bounds__(BWD_THREADS, 1)
+__global__ void __launch_bounds__(BwdWarps<D>::THREADS, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
                   const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV,
@@ -987,7 +1019,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         ptx::prefetch_tmap(&tmDV);
         ptx::prefetch_tmap(&tmDQ);
     }
-    if (warp == 13) {
+    constexpr int W_EPI = BwdWarps<D>::SOFTMAX_WARPS, W_PRODUCER = W_EPI + 4, W_ISSUER = W_EPI + 5;
+    if (warp == W_ISSUER) {
         ptx::tmem_alloc(ptx::smem_addr(const_cast<uint32_t*>(tmem_slot)), T::TMEM_COLS);
         ptx::tmem_relinquish();
     }
@@ -1001,11 +1034,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     // has completed
     ptx::grid_dependency_wait();
     ptx::grid_launch_dependents();
-    if (warp < 8) {
+    if (warp < W_EPI) {
         kv_softmax<D, CAUSAL, BF16, VAR>(p, sbase, kbar0, tmem, warp / 4, ctl);
-    } else if (warp < 12) {
+    } else if (warp < W_PRODUCER) {
         kv_epilogue<D, CAUSAL, BF16, VAR>(&tmDK, &tmDV, p, sbase, kbar0, tmem, ctl);
-    } else if (warp == 12) {
+    } else if (warp == W_PRODUCER) {
         if (lane == 0) kv_producer<D, CAUSAL, VAR>(&tmK, &tmV, &tmQ, &tmDO, p, sbase, kbar0, ctl);
     } else {
         if (lane == 0) kv_issuer<D, CAUSAL, BF16, VAR>(p, sbase, kbar0, tmem, ctl);
@@ -1023,11 +1056,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         __syncthreads();
         ptx::tc_fence_after();
         const int first = (int)gridDim.x - 1 - (int)blockIdx.x;
-        if (warp < 8) {
+        if (warp < W_EPI) {
             q_softmax<D, CAUSAL, BF16, VAR>(p, qbar0, tmem, warp / 4, ctl, first);
-        } else if (warp < 12) {
+        } else if (warp < W_PRODUCER) {
             q_epilogue<D, CAUSAL, BF16, VAR>(&tmDQ, p, sbase, qbar0, tmem, ctl, first);
-        } else if (warp == 12) {
+        } else if (warp == W_PRODUCER) {
             if (lane == 0) q_producer<D, CAUSAL, VAR>(&tmK, &tmV, &tmQ, &tmDO, p, sbase, qbar0, ctl, first);
         } else {
             if (lane == 0) q_issuer<D, CAUSAL, BF16, VAR>(p, sbase, qbar0, tmem, ctl, first);
@@ -1035,7 +1068,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         ptx::tc_fence_before();
         __syncthreads();
     }
-    if (warp == 13) {
+    if (warp == W_ISSUER) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, T::TMEM_COLS);
     }
