@@ -28,6 +28,18 @@ static cudaError_t launch_one(const BwdLaunchArgs& a) {
     static std::atomic<uint64_t> configured{0};  // context the opt-in shared memory size was set in
     cudaError_t err;
     if ((err = set_smem_for_context(bwd, SMEM, configured)) != cudaSuccess) return err;
+#if FA_HEAD_DIM != 256
+    if constexpr (BwdWarps<D>::SPLIT_REGS) {
+        // the warpgroups' setmaxnreg budgets add up only at this launch size
+        static std::atomic<int> regs{0};
+        if (regs.load() == 0) {
+            cudaFuncAttributes attr;
+            if ((err = cudaFuncGetAttributes(&attr, bwd)) != cudaSuccess) return err;
+            regs.store(attr.numRegs);
+        }
+        if (regs.load() != (int)BwdWarps<D>::REG_LAUNCH) return cudaErrorInvalidConfiguration;
+    }
+#endif
     // Δ and lse2 per query row; then dK, dV and dQ in one launch.  Each
     // launch is a programmatic dependent of the one before it on the stream:
     // its set-up overlaps that kernel's tail, and it waits for it

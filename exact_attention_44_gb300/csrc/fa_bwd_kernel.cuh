@@ -26,7 +26,8 @@
 //
 // Warps (both phases): column groups of each 128x128 block (thread = TMEM
 // lane; four groups of 32 columns, warps 0-15, at D = 128, else two of 64,
-// warps 0-7), then the 4 epilogue warps, the TMA producer and the MMA issuer.  Every wait is bounded as in the forward kernel.  Head
+// warps 0-7), then the 4 epilogue warps, the TMA producer and the MMA issuer
+// (at D = 128 two idle warps complete the last warpgroup).  Every wait is bounded as in the forward kernel.  Head
 // dims 16 to 128 (the dK/dV phase's TMEM holds Sᵀ/Pᵀ, dPᵀ/dSᵀ, dV and dK:
 // 256 + 2D columns).
 #pragma once
@@ -46,7 +47,18 @@ struct BwdWarps {
     static constexpr int CW = 128 / NG;
     static constexpr int CH = CW == 32 ? 16 : 32;  // columns per softmax TMEM load
     static constexpr int SOFTMAX_WARPS = 4 * NG;
-    static constexpr int THREADS = (SOFTMAX_WARPS + 6) * 32;
+    // D = 128: whole warpgroups (the last one: producer, issuer and two idle
+    // warps), launched at 80 registers a thread; setmaxnreg then moves 32 a
+    // thread from the last warpgroup to the softmax warpgroups (80 -> 88).
+    // The host launches this kernel only after checking that it was built
+    // with exactly REG_LAUNCH registers, so the budgets always add up.
+    static constexpr bool SPLIT_REGS = D == 128;
+    static constexpr int WARPS = SPLIT_REGS ? (SOFTMAX_WARPS + 6 + 3) / 4 * 4 : SOFTMAX_WARPS + 6;
+    static constexpr int THREADS = WARPS * 32;
+    static constexpr uint32_t REG_LAUNCH = 65536 / THREADS / 8 * 8;
+    static constexpr uint32_t REG_SOFTMAX = 88, REG_EPI = 72, REG_CTRL = 56;
+    static_assert(!SPLIT_REGS || 128 * (NG * REG_SOFTMAX + REG_EPI + REG_CTRL) == THREADS * REG_LAUNCH,
+                  "register budgets of the warpgroups");
 };
 
 // TMEM loads and stores of a width fixed at compile time
@@ -1034,13 +1046,18 @@ __global__ void __launch_bounds__(BwdWarps<D>::THREADS, 1)
     // has completed
     ptx::grid_dependency_wait();
     ptx::grid_launch_dependents();
+    if constexpr (BwdWarps<D>::SPLIT_REGS) {
+        if (warp < W_EPI) ptx::setmaxnreg_inc<BwdWarps<D>::REG_SOFTMAX>();
+        else if (warp < W_PRODUCER) ptx::setmaxnreg_dec<BwdWarps<D>::REG_EPI>();
+        else ptx::setmaxnreg_dec<BwdWarps<D>::REG_CTRL>();
+    }
     if (warp < W_EPI) {
         kv_softmax<D, CAUSAL, BF16, VAR>(p, sbase, kbar0, tmem, warp / 4, ctl);
     } else if (warp < W_PRODUCER) {
         kv_epilogue<D, CAUSAL, BF16, VAR>(&tmDK, &tmDV, p, sbase, kbar0, tmem, ctl);
     } else if (warp == W_PRODUCER) {
         if (lane == 0) kv_producer<D, CAUSAL, VAR>(&tmK, &tmV, &tmQ, &tmDO, p, sbase, kbar0, ctl);
-    } else {
+    } else if (warp == W_ISSUER) {
         if (lane == 0) kv_issuer<D, CAUSAL, BF16, VAR>(p, sbase, kbar0, tmem, ctl);
     }
     ptx::tc_fence_before();
@@ -1062,7 +1079,7 @@ __global__ void __launch_bounds__(BwdWarps<D>::THREADS, 1)
             q_epilogue<D, CAUSAL, BF16, VAR>(&tmDQ, p, sbase, qbar0, tmem, ctl, first);
         } else if (warp == W_PRODUCER) {
             if (lane == 0) q_producer<D, CAUSAL, VAR>(&tmK, &tmV, &tmQ, &tmDO, p, sbase, qbar0, ctl, first);
-        } else {
+        } else if (warp == W_ISSUER) {
             if (lane == 0) q_issuer<D, CAUSAL, BF16, VAR>(p, sbase, qbar0, tmem, ctl, first);
         }
         ptx::tc_fence_before();
