@@ -30,16 +30,24 @@
 // The pre kernel (Δ, base-2 lse), the unit orders and the tile stores are the
 // smaller head dims' (fa_bwd_kernel.cuh).
 //
-// Warps: 0-3 softmax (thread = TMEM lane: a key in the dK/dV phase, a query
-// in the dQ phase), 4-7 epilogue, 8 TMA producer, 9 MMA issuer.  Every wait is
-// bounded as in the forward kernel.
+// Warps: 0-7 softmax, two column groups of 32 of each 64-column step (thread
+// = TMEM lane: a key in the dK/dV phase, a query in the dQ phase), 8-11
+// epilogue, 12 TMA producer, 13 MMA issuer.  Every wait is bounded as in the
+// forward kernel.
 #pragma once
 
 #include "fa_bwd_kernel.cuh"
 
 namespace fa {
 
-constexpr int WIDE_THREADS = 10 * 32;
+// Softmax column groups of a 64-column step (4 warps each).  Measured on
+// GB300 at Z8 H16 N2048: two groups of 32 columns +1.1 % non-causal, +3.3 %
+// causal against one group of 64 (the steps are bound by their serial
+// load -> Sᵀ -> softmax -> accumulation chain more than by the softmax).
+constexpr int WIDE_NG = 2;
+constexpr int WIDE_CW = 64 / WIDE_NG;
+constexpr int WIDE_SOFTMAX_WARPS = 4 * WIDE_NG;
+constexpr int WIDE_THREADS = (WIDE_SOFTMAX_WARPS + 6) * 32;
 
 struct WideTraits {
     static constexpr int D = 256;
@@ -64,7 +72,7 @@ struct WideTraits {
     static constexpr int KB_QD_FULL = 2;      // [2] Q, dO, lse2, Δ of a step landed in slot b
     static constexpr int KB_QD_EMPTY = 4;     // [2] that step's products are done (commit)
     static constexpr int KB_S_FULL = 6;       // [2] Sᵀ (and dPᵀ in the dK pass) in TMEM (commit)
-    static constexpr int KB_P_FULL = 8;       // [2] Pᵀ (dV pass) or dSᵀ (dK pass) written (128)
+    static constexpr int KB_P_FULL = 8;       // [2] Pᵀ (dV pass) or dSᵀ (dK pass) written (every softmax thread)
     static constexpr int KB_ACC_FULL = 10;    // dV or dK of a unit complete (commit)
     static constexpr int KB_ACC_FREE = 11;    // that accumulator read out (128)
     static constexpr int KB_DRAIN = 12;
@@ -86,7 +94,7 @@ struct WideTraits {
     static constexpr int QB_KV_FULL = 2;      // K, V of a step landed
     static constexpr int QB_KV_EMPTY = 3;     // that step's products are done (commit)
     static constexpr int QB_S_FULL = 4;       // S and dP in TMEM (commit)
-    static constexpr int QB_DS_FULL = 5;      // dS written (128)
+    static constexpr int QB_DS_FULL = 5;      // dS written (every softmax thread)
     static constexpr int QB_DQ_FULL = 6;      // dQ of a unit complete (commit)
     static constexpr int QB_DQ_FREE = 7;      // dQ read out (128)
     static constexpr int QB_DRAIN = 8;
@@ -97,7 +105,8 @@ struct WideTraits {
     static constexpr int SMEM_BYTES = SMEM_USED + 1024;
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
     // tensor memory: two 64-column fp32 blocks (S / Sᵀ, dP / dPᵀ; P, dS packed
-    // over their first 32 columns) and one 256-column accumulator
+    // by each column group over the first half of its own columns) and one
+    // 256-column accumulator
     static constexpr uint32_t TM_S = 0;
     static constexpr uint32_t TM_DP = 64;
     // dV pass: Sᵀ of slot b (slot 1 takes the dPᵀ block, unused in that pass)
@@ -107,10 +116,12 @@ struct WideTraits {
     static_assert(TM_ACC + D <= TMEM_COLS, "tensor memory budget");
 
     static __device__ __forceinline__ uint32_t kv_bar_count(int i) {
-        return ((i >= KB_P_FULL && i < KB_P_FULL + 2) || i == KB_ACC_FREE) ? 128 : 1;
+        if (i >= KB_P_FULL && i < KB_P_FULL + 2) return 32 * WIDE_SOFTMAX_WARPS;
+        return i == KB_ACC_FREE ? 128 : 1;
     }
     static __device__ __forceinline__ uint32_t q_bar_count(int i) {
-        return (i == QB_DS_FULL || i == QB_DQ_FREE) ? 128 : 1;
+        if (i == QB_DS_FULL) return 32 * WIDE_SOFTMAX_WARPS;
+        return i == QB_DQ_FREE ? 128 : 1;
     }
 };
 
@@ -240,7 +251,7 @@ __device__ void wide_kv_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0
         ptx::tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-            ptx::mma_ts(tmem + T::TM_ACC, tmem + a + kk * 8, ptx::desc64(b_lo + ((kk * 16 * T::SW) >> 4), HI), ID_ACC,
+            ptx::mma_ts(tmem + T::TM_ACC, tmem + a + packed_col<WIDE_CW>(kk), ptx::desc64(b_lo + ((kk * 16 * T::SW) >> 4), HI), ID_ACC,
                         (s > 0 || kk > 0) ? 1u : 0u);
         ptx::tc_commit(bar(T::KB_QD_EMPTY + b));  // the step's Q, dO and TMEM block free
         if (s == steps - 1) {
@@ -310,12 +321,15 @@ __device__ void wide_kv_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0
     drain_phase(bar(T::KB_DRAIN), 0u, ctl.limit_ns);
 }
 
-// Thread = key (TMEM lane).  dV pass: Pᵀ over the first 32 columns of the
-// step's Sᵀ block; dK pass: Pᵀ in registers, dSᵀ = Pᵀ ∘ (dPᵀ − Δ) over the
-// first 32 columns of dPᵀ.  P and dS are rounded to the input type (the
-// products' operands).
+// Thread = key (TMEM lane); column group h takes the step's queries h*CW ..
+// h*CW + CW - 1.  dV pass: Pᵀ over the first half of the group's columns of
+// the step's Sᵀ block; dK pass: Pᵀ in registers, dSᵀ = Pᵀ ∘ (dPᵀ − Δ) over the
+// first half of the group's columns of dPᵀ.  P and dS are rounded to the
+// input type (the products' operands).
 template <bool CAUSAL, bool BF16>
-__device__ void wide_kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar0, uint32_t tmem, const Ctl& ctl) {
+__device__ void wide_kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar0, uint32_t tmem, int h,
+                                const Ctl& ctl) {
+    static_assert(WIDE_CW == 32, "one 32-column TMEM load per group");
     using T = WideTraits;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     const int quad = (threadIdx.x / 32) % 4;
@@ -338,54 +352,43 @@ __device__ void wide_kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar
                 if (!warp_wait_phase(bar(T::KB_QD_FULL + b), ph, ctl, SITE_B_QD_FULL)) return;
                 if (!warp_wait_phase(bar(T::KB_S_FULL + b), ph, ctl, SITE_B_S_FULL)) return;
                 ptx::tc_fence_after();
-                const uint32_t lse_a = sbase + T::KV_OFF_LSE + b * 256u, del_a = sbase + T::KV_OFF_DELTA + b * 256u;
-                const uint32_t tm_s = pass == 0 ? T::tm_slot(b) : T::TM_S;
+                const uint32_t lse_a = sbase + T::KV_OFF_LSE + b * 256u + 4u * (h * WIDE_CW);
+                const uint32_t del_a = sbase + T::KV_OFF_DELTA + b * 256u + 4u * (h * WIDE_CW);
+                const uint32_t tm_s = (pass == 0 ? T::tm_slot(b) : T::TM_S) + h * WIDE_CW;
                 // causal: only the diagonal block has keys after queries (key > query -> P = 0)
                 const bool diag = CAUSAL && r0 / 128 == w.j;
-                float pf[64];
+                const int q0 = r0 + h * WIDE_CW;  // the group's first query
+                uint32_t pk[WIDE_CW / 2];
                 {
-                    uint32_t a[32], bb[32];
-                    ptx::tmem_ld32_issue(tmem + lane_addr + tm_s, a);
-                    ptx::tmem_ld32_issue(tmem + lane_addr + tm_s + 32, bb);
-                    ptx::tmem_wait_ld();
-                    ptx::reg_fence32(a);
-                    ptx::reg_fence32(bb);
+                    uint32_t a[32];
+                    ptx::tmem_ld32(tmem + lane_addr + tm_s, a);
 #pragma unroll
-                    for (int x = 0; x < 64; x += 2) {
+                    for (int x = 0; x < 32; x += 2) {
                         float l0, l1;
                         asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(l0), "=f"(l1) : "r"(lse_a + 4u * x));
-                        const uint32_t u0 = x < 32 ? a[x] : bb[x - 32], u1 = x < 32 ? a[x + 1] : bb[x - 31];
-                        float e0 = fmaf(__uint_as_float(u0), c, -l0);
-                        float e1 = fmaf(__uint_as_float(u1), c, -l1);
-                        if (diag && key > r0 + x) e0 = -INFINITY;
-                        if (diag && key > r0 + x + 1) e1 = -INFINITY;
-                        pf[x] = ptx::ex2(e0);
-                        pf[x + 1] = ptx::ex2(e1);
+                        float e0 = fmaf(__uint_as_float(a[x]), c, -l0);
+                        float e1 = fmaf(__uint_as_float(a[x + 1]), c, -l1);
+                        if (diag && key > q0 + x) e0 = -INFINITY;
+                        if (diag && key > q0 + x + 1) e1 = -INFINITY;
+                        pk[x / 2] = pack2<BF16>(ptx::ex2(e0), ptx::ex2(e1));
                     }
                 }
-                uint32_t pk[32];
-#pragma unroll
-                for (int x = 0; x < 32; ++x) pk[x] = pack2<BF16>(pf[2 * x], pf[2 * x + 1]);
                 if (pass == 0) {
-                    ptx::tmem_st32(tmem + lane_addr + tm_s, pk);
+                    ptx::tmem_st16(tmem + lane_addr + tm_s, pk);
                 } else {
-                    uint32_t a[32], bb[32];
-                    ptx::tmem_ld32_issue(tmem + lane_addr + T::TM_DP, a);
-                    ptx::tmem_ld32_issue(tmem + lane_addr + T::TM_DP + 32, bb);
-                    ptx::tmem_wait_ld();
-                    ptx::reg_fence32(a);
-                    ptx::reg_fence32(bb);
-                    uint32_t ds[32];
+                    const uint32_t tm_dp = T::TM_DP + h * WIDE_CW;
+                    uint32_t a[32];
+                    ptx::tmem_ld32(tmem + lane_addr + tm_dp, a);
+                    uint32_t ds[16];
 #pragma unroll
-                    for (int x = 0; x < 32; ++x) {
+                    for (int x = 0; x < 16; ++x) {
                         float d0, d1;
                         asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(d0), "=f"(d1) : "r"(del_a + 8u * x));
                         const float2 pp = unpack2<BF16>(pk[x]);  // dS uses the rounded P
-                        const uint32_t u0 = 2 * x < 32 ? a[2 * x] : bb[2 * x - 32];
-                        const uint32_t u1 = 2 * x < 32 ? a[2 * x + 1] : bb[2 * x - 31];
-                        ds[x] = pack2<BF16>(pp.x * (__uint_as_float(u0) - d0), pp.y * (__uint_as_float(u1) - d1));
+                        ds[x] = pack2<BF16>(pp.x * (__uint_as_float(a[2 * x]) - d0),
+                                            pp.y * (__uint_as_float(a[2 * x + 1]) - d1));
                     }
-                    ptx::tmem_st32(tmem + lane_addr + T::TM_DP, ds);
+                    ptx::tmem_st16(tmem + lane_addr + tm_dp, ds);
                 }
                 ptx::tmem_wait_st();
                 ptx::tc_fence_before();
@@ -524,7 +527,7 @@ __device__ void wide_q_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0,
             ptx::tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-                ptx::mma_ts(tmem + T::TM_ACC, tmem + T::TM_S + kk * 8, ptx::desc64(kmn_lo + ((kk * 16 * T::SW) >> 4), HI),
+                ptx::mma_ts(tmem + T::TM_ACC, tmem + T::TM_S + packed_col<WIDE_CW>(kk), ptx::desc64(kmn_lo + ((kk * 16 * T::SW) >> 4), HI),
                             ID_DQ, (s > 0 || kk > 0) ? 1u : 0u);
             ptx::tc_commit(bar(T::QB_KV_EMPTY));  // K, V of the step and the TMEM blocks free
         }
@@ -538,10 +541,11 @@ __device__ void wide_q_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0,
     }
 }
 
-// Thread = query (TMEM lane): P = 2^(S·c − lse2), dS = P ∘ (dP − Δ) over the
-// first 32 columns of S.
+// Thread = query (TMEM lane); column group h takes the step's keys h*CW ..
+// h*CW + CW - 1: P = 2^(S·c − lse2), dS = P ∘ (dP − Δ) over the first half of
+// the group's columns of S.
 template <bool CAUSAL, bool BF16>
-__device__ void wide_q_softmax(const BwdParams& p, uint32_t bar0, uint32_t tmem, const Ctl& ctl, int first) {
+__device__ void wide_q_softmax(const BwdParams& p, uint32_t bar0, uint32_t tmem, int h, const Ctl& ctl, int first) {
     using T = WideTraits;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     const int quad = (threadIdx.x / 32) % 4;
@@ -560,31 +564,25 @@ __device__ void wide_q_softmax(const BwdParams& p, uint32_t bar0, uint32_t tmem,
             if (!warp_wait_phase(bar(T::QB_S_FULL), g & 1u, ctl, SITE_B_S_FULL)) return;
             ptx::tc_fence_after();
             const bool diag = CAUSAL && s / 2 == w.i;  // keys after the query only on the diagonal block
-            const int k0 = s * 64;
-            uint32_t sa[32], sb[32], da[32], db[32];
-            ptx::tmem_ld32_issue(tmem + lane_addr + T::TM_S, sa);
-            ptx::tmem_ld32_issue(tmem + lane_addr + T::TM_S + 32, sb);
-            ptx::tmem_ld32_issue(tmem + lane_addr + T::TM_DP, da);
-            ptx::tmem_ld32_issue(tmem + lane_addr + T::TM_DP + 32, db);
+            const int k0 = s * 64 + h * WIDE_CW;       // the group's first key
+            uint32_t sa[32], da[32];
+            ptx::tmem_ld32_issue(tmem + lane_addr + T::TM_S + h * WIDE_CW, sa);
+            ptx::tmem_ld32_issue(tmem + lane_addr + T::TM_DP + h * WIDE_CW, da);
             ptx::tmem_wait_ld();
             ptx::reg_fence32(sa);
-            ptx::reg_fence32(sb);
             ptx::reg_fence32(da);
-            ptx::reg_fence32(db);
-            uint32_t ds[32];
+            uint32_t ds[16];
 #pragma unroll
-            for (int x = 0; x < 32; ++x) {
+            for (int x = 0; x < 16; ++x) {
                 const int k = 2 * x;
-                const uint32_t s0 = k < 32 ? sa[k] : sb[k - 32], s1 = k < 32 ? sa[k + 1] : sb[k - 31];
-                const uint32_t d0 = k < 32 ? da[k] : db[k - 32], d1 = k < 32 ? da[k + 1] : db[k - 31];
-                float e0 = fmaf(__uint_as_float(s0), c, -l2);
-                float e1 = fmaf(__uint_as_float(s1), c, -l2);
+                float e0 = fmaf(__uint_as_float(sa[k]), c, -l2);
+                float e1 = fmaf(__uint_as_float(sa[k + 1]), c, -l2);
                 if (diag && k0 + k > q) e0 = -INFINITY;
                 if (diag && k0 + k + 1 > q) e1 = -INFINITY;
                 const float2 pp = unpack2<BF16>(pack2<BF16>(ptx::ex2(e0), ptx::ex2(e1)));  // P rounded as in dV
-                ds[x] = pack2<BF16>(pp.x * (__uint_as_float(d0) - dl), pp.y * (__uint_as_float(d1) - dl));
+                ds[x] = pack2<BF16>(pp.x * (__uint_as_float(da[k]) - dl), pp.y * (__uint_as_float(da[k + 1]) - dl));
             }
-            ptx::tmem_st32(tmem + lane_addr + T::TM_S, ds);
+            ptx::tmem_st16(tmem + lane_addr + T::TM_S + h * WIDE_CW, ds);
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(T::QB_DS_FULL));
@@ -658,7 +656,8 @@ __global__ void __launch_bounds__(WIDE_THREADS, 1)
         ptx::prefetch_tmap(&tmDV);
         ptx::prefetch_tmap(&tmDQ);
     }
-    if (warp == 9) {
+    constexpr int W_EPI = WIDE_SOFTMAX_WARPS, W_PRODUCER = W_EPI + 4, W_ISSUER = W_EPI + 5;
+    if (warp == W_ISSUER) {
         ptx::tmem_alloc(ptx::smem_addr(const_cast<uint32_t*>(tmem_slot)), T::TMEM_COLS);
         ptx::tmem_relinquish();
     }
@@ -669,11 +668,11 @@ __global__ void __launch_bounds__(WIDE_THREADS, 1)
     const Ctl ctl{abort_flag, p.status, p.wait_limit_ns};
     ptx::grid_dependency_wait();
     ptx::grid_launch_dependents();
-    if (warp < 4) {
-        wide_kv_softmax<CAUSAL, BF16>(p, sbase, kbar0, tmem, ctl);
-    } else if (warp < 8) {
+    if (warp < W_EPI) {
+        wide_kv_softmax<CAUSAL, BF16>(p, sbase, kbar0, tmem, warp / 4, ctl);
+    } else if (warp < W_PRODUCER) {
         wide_kv_epilogue<CAUSAL, BF16>(&tmDK, &tmDV, p, sbase, kbar0, tmem, ctl);
-    } else if (warp == 8) {
+    } else if (warp == W_PRODUCER) {
         if (lane == 0) wide_kv_producer<CAUSAL>(&tmK, &tmV, &tmQ, &tmDO, p, sbase, kbar0, ctl);
     } else {
         if (lane == 0) wide_kv_issuer<CAUSAL, BF16>(p, sbase, kbar0, tmem, ctl);
@@ -690,11 +689,11 @@ __global__ void __launch_bounds__(WIDE_THREADS, 1)
         __syncthreads();
         ptx::tc_fence_after();
         const int first = (int)gridDim.x - 1 - (int)blockIdx.x;
-        if (warp < 4) {
-            wide_q_softmax<CAUSAL, BF16>(p, qbar0, tmem, ctl, first);
-        } else if (warp < 8) {
+        if (warp < W_EPI) {
+            wide_q_softmax<CAUSAL, BF16>(p, qbar0, tmem, warp / 4, ctl, first);
+        } else if (warp < W_PRODUCER) {
             wide_q_epilogue<CAUSAL, BF16>(&tmDQ, p, sbase, qbar0, tmem, ctl, first);
-        } else if (warp == 8) {
+        } else if (warp == W_PRODUCER) {
             if (lane == 0) wide_q_producer<CAUSAL>(&tmK, &tmV, &tmQ, &tmDO, p, sbase, qbar0, ctl, first);
         } else {
             if (lane == 0) wide_q_issuer<CAUSAL, BF16>(p, sbase, qbar0, tmem, ctl, first);
@@ -702,7 +701,7 @@ __global__ void __launch_bounds__(WIDE_THREADS, 1)
         ptx::tc_fence_before();
         __syncthreads();
     }
-    if (warp == 9) {
+    if (warp == W_ISSUER) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, T::TMEM_COLS);
     }
