@@ -9,7 +9,9 @@ of the input type relative to the largest reference gradient.  Cases: each
 window side alone and both, with and without the causal rule, ALiBi alone and
 with a window, GQA, query and key lengths that differ (rows that keep no key:
 dQ = 0), windows so narrow most blocks are skipped, the open window routed to
-fa_bwd's kernel, and the head dim the variants do not cover."""
+fa_bwd's kernel, and the head dim the variants do not cover; packed
+sequences; and the bench's three variant workloads at full size, whole heads
+(or sequences) against the oracle."""
 import math
 
 import numpy as np
@@ -228,3 +230,67 @@ def test_varlen_longer_sequences():
     # a packed batch of 5.4K rows: sequences from 1 to 2000 rows, GQA 4:1
     check_bwd_varlen(422, [2000, 1, 1500, 129, 1800], [2000, 5, 1500, 700, 1800], 4, 1, 128, "bf16", True,
                      extra_q=3)
+
+
+# ---- the bench's variant workloads at full size, whole heads ----------------
+# A head's gradients depend on that head's Q, K, V, dO only (and a packed
+# sequence's on its own rows), so the oracle differentiates whole heads (or
+# sequences) of the full-size launch one at a time.
+
+def _check_heads(q, k, v, do, got, dtype, scale, causal, heads, **opt):
+    for z, h in heads:
+        one_q = (slice(z, z + 1), slice(h, h + 1))
+        ref = oracle.attention_bwd_ex(q[one_q], k[one_q], v[one_q], do[one_q], dtype, scale, causal, **opt)
+        for name, g, want in zip(("dq", "dk", "dv"), got, ref):
+            g = g[one_q].double().cpu().numpy()
+            err, mag = float(np.max(np.abs(g - want))), float(np.max(np.abs(want)))
+            assert err <= TOL_GRAD[dtype] * max(mag, 1e-3), f"head ({z}, {h}) {name}: {err:.3e} vs {mag:.3e}"
+
+
+def test_full_size_window_whole_heads():
+    # Z4 H16 N4096 D128 bf16, causal with a 512-key window
+    Z, H, N, D, dtype, window = 4, 16, 4096, 128, "bf16", (512, 0)
+    (q, k, v, do, scale), got = run_bwd_ex(430, Z, H, H, N, N, D, dtype, True, window, None)
+    _check_heads(q, k, v, do, got, dtype, scale, True, [(0, 0), (1, 7), (3, 15)], window=window)
+
+
+def test_full_size_alibi_whole_heads():
+    # Z4 H16 N2048 D128 bf16, causal with ALiBi slopes 2^(-8(h+1)/H)
+    Z, H, N, D, dtype = 4, 16, 2048, 128, "bf16"
+    slopes = [2.0 ** (-8.0 * (h + 1) / H) for h in range(H)]
+    (q, k, v, do, scale), got = run_bwd_ex(431, Z, H, H, N, N, D, dtype, True, (-1, -1), slopes)
+    for z, h in [(0, 0), (2, 9), (3, 15)]:
+        _check_heads(q, k, v, do, got, dtype, scale, True, [(z, h)],
+                     alibi=np.full(1, slopes[h], dtype=np.float64))
+
+
+def test_full_size_varlen_whole_sequences():
+    # 16 packed causal sequences of 256-4096 rows (seeded), H16 D128 bf16: the
+    # oracle differentiates the shortest and the longest sequence, two heads each
+    import torch
+    import exact_attention_44_gb300 as fa
+    H, D, dtype = 16, 128, "bf16"
+    lens = np.random.default_rng(0).integers(256, 4097, size=16)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    total = int(cu[-1])
+    q = si.normals(432, 0, H * total * D, dtype).reshape(1, H, total, D)
+    k = si.normals(432, q.size, H * total * D, dtype).reshape(1, H, total, D)
+    v = si.normals(432, 2 * q.size, H * total * D, dtype).reshape(1, H, total, D)
+    do = si.normals(1432, 0, q.size, dtype).reshape(q.shape)
+    scale = 1 / math.sqrt(D)
+    qt, kt, vt, dot = (to_device(x, dtype) for x in (q, k, v, do))
+    cu_t = torch.from_numpy(cu).cuda()
+    o, lse = fa.fa_fwd_ex(qt, kt, vt, scale=scale, causal=True, cu_seqlens_q=cu_t, cu_seqlens_k=cu_t)
+    dq, dk, dv = fa.fa_bwd_ex(qt, kt, vt, o, lse, dot, scale=scale, causal=True, cu_seqlens_q=cu_t,
+                              cu_seqlens_k=cu_t)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status()[0] == 0
+    for z in (int(np.argmin(lens)), int(np.argmax(lens))):
+        rows = slice(int(cu[z]), int(cu[z + 1]))
+        for h in (0, H - 1):
+            one = (slice(0, 1), slice(h, h + 1), rows)
+            ref = oracle.attention_bwd_ex(q[one], k[one], v[one], do[one], dtype, scale, True)
+            for name, g, want in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+                g = g[one].double().cpu().numpy()
+                err, mag = float(np.max(np.abs(g - want))), float(np.max(np.abs(want)))
+                assert err <= TOL_GRAD[dtype] * max(mag, 1e-3), f"sequence {z} head {h} {name}: {err:.3e} vs {mag:.3e}"
