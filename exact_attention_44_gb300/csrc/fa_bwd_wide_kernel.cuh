@@ -24,7 +24,9 @@
 // t's accumulation while step t + 2's copies are in flight, and V loads once
 // the pass is done.  The dK pass and the dQ phase are single-buffered (no
 // room for a second slot; measured on GB300 at Z8 H16 N2048 with one slot
-// everywhere: ~2.2 us a step in the dV pass against ~0.7 us of tensor work).
+// everywhere: ~2.2 us a step in the dV pass against ~0.7 us of tensor work);
+// in the dK pass a step's dO, read only by its dPᵀ, is loaded as soon as the
+// previous step's dPᵀ is done, so only Q waits for the accumulation.
 // dK, dV and dQ are each summed inside one CTA: no atomics, bitwise
 // reproducible.
 // The pre kernel (Δ, base-2 lse), the unit orders and the tile stores are the
@@ -77,7 +79,9 @@ struct WideTraits {
     static constexpr int KB_ACC_FREE = 11;    // that accumulator read out (128)
     static constexpr int KB_DRAIN = 12;
     static constexpr int KB_V_FULL = 13;      // V of a unit landed, after the dV pass (TMA)
-    static constexpr int KV_NUM_BARS = 14;
+    static constexpr int KB_DO_FULL = 14;     // dK pass: a step's dO landed (TMA)
+    static constexpr int KB_DO_EMPTY = 15;    // dK pass: that step's dPᵀ is done (commit)
+    static constexpr int KV_NUM_BARS = 16;
     // a step slot's Q and dO tiles (slot 1 lives where V goes)
     static __host__ __device__ constexpr uint32_t kv_q(uint32_t b) { return b ? KV_OFF_V : KV_OFF_Q; }
     static __host__ __device__ constexpr uint32_t kv_do(uint32_t b) { return b ? KV_OFF_V + TILE64 : KV_OFF_DO; }
@@ -169,6 +173,7 @@ __device__ void wide_kv_producer(const CUtensorMap* tmK, const CUtensorMap* tmV,
     const uint64_t pol_kv = ptx::policy_evict_first();
     const uint64_t pol_q = ptx::policy_evict_last();
     uint32_t uc = 0, vc = 0, n0 = 0, n1 = 0;  // fills of slots 0 and 1
+    uint32_t nd = 0;                          // dO fills of the dK passes
     bool ok = true;
     bool withheld = false;
     // Q, dO, lse2, Δ of step s into slot b, once that slot's previous step is done
@@ -186,6 +191,31 @@ __device__ void wide_kv_producer(const CUtensorMap* tmK, const CUtensorMap* tmV,
         ptx::bulk_load(sbase + T::KV_OFF_DELTA + b * 256u, p.delta + row0, 256, full);
         if (b) ++n1;
         else ++n0;
+        return true;
+    };
+    // dK pass step s in slot 0: dO (read only by the step's dPᵀ) as soon as
+    // the previous step's dPᵀ is done, then Q, lse2, Δ once the previous
+    // step's accumulation is (it reads Q); the first step's dO waits for the
+    // dV pass's last slot-0 accumulation, which read the dO buffer
+    auto fill_dk = [&](const BwdUnit& w, int s) -> bool {
+        int hq, r0;
+        wide_step(w, s, p, hq, r0);
+        if (s == 0) {
+            if (n0 >= 1 && !wait_phase(bar(T::KB_QD_EMPTY), (n0 - 1) & 1u, ctl, SITE_B_QD_EMPTY)) return false;
+        } else if (!wait_phase(bar(T::KB_DO_EMPTY), (nd - 1) & 1u, ctl, SITE_B_QD_EMPTY)) {
+            return false;
+        }
+        ptx::mbar_arrive_expect_tx(bar(T::KB_DO_FULL), T::TILE64);
+        wide_load64(sbase + T::kv_do(0), tmDO, bar(T::KB_DO_FULL), r0, hq, w.z, pol_q);
+        ++nd;
+        if (n0 >= 1 && !wait_phase(bar(T::KB_QD_EMPTY), (n0 - 1) & 1u, ctl, SITE_B_QD_EMPTY)) return false;
+        const uint32_t full = bar(T::KB_QD_FULL);
+        ptx::mbar_arrive_expect_tx(full, T::TILE64 + 512);
+        wide_load64(sbase + T::kv_q(0), tmQ, full, r0, hq, w.z, pol_q);
+        const int64_t row0 = ((int64_t)w.z * p.Hq + hq) * p.Tq * 128 + r0;
+        ptx::bulk_load(sbase + T::KV_OFF_LSE, p.lse2 + row0, 256, full);
+        ptx::bulk_load(sbase + T::KV_OFF_DELTA, p.delta + row0, 256, full);
+        ++n0;
         return true;
     };
     for (int pos = blockIdx.x; ok && unit_at<CAUSAL>(pos) < p.nunits; pos += gridDim.x) {
@@ -210,13 +240,14 @@ __device__ void wide_kv_producer(const CUtensorMap* tmK, const CUtensorMap* tmV,
         ptx::mbar_arrive_expect_tx(bar(T::KB_V_FULL), T::TILE128);
         wide_load128(sbase + T::KV_OFF_V, tmV, bar(T::KB_V_FULL), w.j * 128, w.hk, w.z, pol_kv);
         ++vc;
-        for (int s = 0; ok && s < steps; ++s) ok = fill(w, s, 0u);
+        for (int s = 0; ok && s < steps; ++s) ok = fill_dk(w, s);
     }
     if (!ok) {
         // (the withheld copy never completes; its wait simply runs out)
         if (uc > 0) drain_phase(bar(T::KB_K_FULL), (uc - 1) & 1u, withheld && uc == 1 ? ctl.limit_ns / 64 : ctl.limit_ns);
         if (vc > 0) drain_phase(bar(T::KB_V_FULL), (vc - 1) & 1u, ctl.limit_ns);
         if (n0 > 0) drain_phase(bar(T::KB_QD_FULL), (n0 - 1) & 1u, ctl.limit_ns);
+        if (nd > 0) drain_phase(bar(T::KB_DO_FULL), (nd - 1) & 1u, ctl.limit_ns);
         if (n1 > 0) drain_phase(bar(T::KB_QD_FULL + 1), (n1 - 1) & 1u, ctl.limit_ns);
     }
 }
@@ -236,6 +267,7 @@ __device__ void wide_kv_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0
     auto qmn_lo = [&](uint32_t b) { return ptx::smem_desc_lo(sbase + T::kv_q(b), 64 * T::SW); };
     auto domn_lo = [&](uint32_t b) { return ptx::smem_desc_lo(sbase + T::kv_do(b), 64 * T::SW); };
     uint32_t uc = 0, acc = 0, n0 = 0, n1 = 0;  // fills of slots 0 and 1 consumed
+    uint32_t nd = 0;                           // dO fills of the dK passes consumed
     bool ok = true;
     // Sᵀ = K Qᵀ of the step in slot b into TMEM block tm, K = 256 in 16 steps
     auto issue_s = [&](uint32_t b, uint32_t tm) {
@@ -299,11 +331,15 @@ __device__ void wide_kv_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0
             if (!wait_phase(bar(T::KB_QD_FULL), nb & 1u, ctl, SITE_B_QD_FULL)) { ok = false; break; }
             ptx::tc_fence_after();
             issue_s(0, T::TM_S);
+            if (!wait_phase(bar(T::KB_DO_FULL), nd & 1u, ctl, SITE_B_QD_FULL)) { ok = false; break; }
+            ++nd;
+            ptx::tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 16; ++kk)
                 ptx::mma_ss(tmem + T::TM_DP, ptx::desc64(v_lo + wide_kmaj(kk, 128), HI),
                             ptx::desc64(do_lo(0) + wide_kmaj(kk, 64), HI), ID_S, kk > 0 ? 1u : 0u);
             ptx::tc_commit(bar(T::KB_S_FULL));
+            ptx::tc_commit(bar(T::KB_DO_EMPTY));  // the step's dO is free once its dPᵀ is done
             // the unit's last Sᵀ and dPᵀ were its last reads of K and V: the
             // next unit's K (and slot 1, over V) may land during the last dK step
             if (s + 1 == steps) ptx::tc_commit(bar(T::KB_KV_EMPTY));
