@@ -95,14 +95,16 @@ struct WideTraits {
     static constexpr int Q_OFF_BAR = Q_OFF_OST + 128 * SW;
     static constexpr int QB_QD_FULL = 0;      // Q, dO of a unit landed
     static constexpr int QB_QD_EMPTY = 1;     // the unit's last S and dP are done (commit)
-    static constexpr int QB_KV_FULL = 2;      // K, V of a step landed
+    static constexpr int QB_KV_FULL = 2;      // K of a step landed
     static constexpr int QB_KV_EMPTY = 3;     // that step's products are done (commit)
     static constexpr int QB_S_FULL = 4;       // S and dP in TMEM (commit)
     static constexpr int QB_DS_FULL = 5;      // dS written (every softmax thread)
     static constexpr int QB_DQ_FULL = 6;      // dQ of a unit complete (commit)
     static constexpr int QB_DQ_FREE = 7;      // dQ read out (128)
     static constexpr int QB_DRAIN = 8;
-    static constexpr int Q_NUM_BARS = 9;
+    static constexpr int QB_V_FULL = 9;       // V of a step landed
+    static constexpr int QB_V_EMPTY = 10;     // that step's dP is done (commit)
+    static constexpr int Q_NUM_BARS = 11;
     static constexpr int Q_SMEM_USED = Q_OFF_BAR + Q_NUM_BARS * 8;
     static constexpr int OFF_MISC = ((KV_SMEM_USED > Q_SMEM_USED ? KV_SMEM_USED : Q_SMEM_USED) + 15) & ~15;
     static constexpr int SMEM_USED = OFF_MISC + 16;
@@ -496,7 +498,7 @@ __device__ void wide_q_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, 
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     const uint64_t pol_q = ptx::policy_evict_first();
     const uint64_t pol_kv = ptx::policy_evict_last();
-    uint32_t uc = 0, g = 0;
+    uint32_t uc = 0, g = 0, gv = 0;  // fills of Q/dO, K and V
     bool ok = true;
     for (int pos = first; ok && unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x) {
         const DqUnit w = dq_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
@@ -508,16 +510,21 @@ __device__ void wide_q_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, 
         ++uc;
         const int steps = 2 * w.nkv;  // 64-key steps
         for (int s = 0; s < steps; ++s, ++g) {
+            // V (read only by the step's dP) once the previous step's dP is
+            // done, then K once the previous step's dQ product (it reads K) is
+            if (gv >= 1 && !wait_phase(bar(T::QB_V_EMPTY), (gv - 1) & 1u, ctl, SITE_B_KV_EMPTY)) { ok = false; break; }
+            ptx::mbar_arrive_expect_tx(bar(T::QB_V_FULL), T::TILE64);
+            wide_load64(sbase + T::Q_OFF_V, tmV, bar(T::QB_V_FULL), s * 64, w.hk, w.z, pol_kv);
+            ++gv;
             if (g >= 1 && !wait_phase(bar(T::QB_KV_EMPTY), (g - 1) & 1u, ctl, SITE_B_KV_EMPTY)) { ok = false; break; }
-            const uint32_t full = bar(T::QB_KV_FULL);
-            ptx::mbar_arrive_expect_tx(full, 2 * T::TILE64);
-            wide_load64(sbase + T::Q_OFF_K, tmK, full, s * 64, w.hk, w.z, pol_kv);
-            wide_load64(sbase + T::Q_OFF_V, tmV, full, s * 64, w.hk, w.z, pol_kv);
+            ptx::mbar_arrive_expect_tx(bar(T::QB_KV_FULL), T::TILE64);
+            wide_load64(sbase + T::Q_OFF_K, tmK, bar(T::QB_KV_FULL), s * 64, w.hk, w.z, pol_kv);
         }
     }
     if (!ok) {
         if (uc > 0) drain_phase(bar(T::QB_QD_FULL), (uc - 1) & 1u, ctl.limit_ns);
         if (g > 0) drain_phase(bar(T::QB_KV_FULL), (g - 1) & 1u, ctl.limit_ns);
+        if (gv > 0) drain_phase(bar(T::QB_V_FULL), (gv - 1) & 1u, ctl.limit_ns);
     }
 }
 
@@ -548,11 +555,14 @@ __device__ void wide_q_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0,
             for (int kk = 0; kk < 16; ++kk)
                 ptx::mma_ss(tmem + T::TM_S, ptx::desc64(q_lo + wide_kmaj(kk, 128), HI),
                             ptx::desc64(k_lo + wide_kmaj(kk, 64), HI), ID_S, kk > 0 ? 1u : 0u);
+            if (!wait_phase(bar(T::QB_V_FULL), g & 1u, ctl, SITE_B_KV_FULL)) { ok = false; break; }
+            ptx::tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 16; ++kk)
                 ptx::mma_ss(tmem + T::TM_DP, ptx::desc64(do_lo + wide_kmaj(kk, 128), HI),
                             ptx::desc64(v_lo + wide_kmaj(kk, 64), HI), ID_S, kk > 0 ? 1u : 0u);
             ptx::tc_commit(bar(T::QB_S_FULL));
+            ptx::tc_commit(bar(T::QB_V_EMPTY));  // the step's V is free once its dP is done
             // the unit's last S and dP were its last reads of Q and dO
             if (s + 1 == steps) ptx::tc_commit(bar(T::QB_QD_EMPTY));
             if (!wait_phase(bar(T::QB_DS_FULL), g & 1u, ctl, SITE_B_DS_FULL)) { ok = false; break; }
@@ -565,7 +575,7 @@ __device__ void wide_q_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0,
             for (int kk = 0; kk < 4; ++kk)
                 ptx::mma_ts(tmem + T::TM_ACC, tmem + T::TM_S + packed_col<WIDE_CW>(kk), ptx::desc64(kmn_lo + ((kk * 16 * T::SW) >> 4), HI),
                             ID_DQ, (s > 0 || kk > 0) ? 1u : 0u);
-            ptx::tc_commit(bar(T::QB_KV_EMPTY));  // K, V of the step and the TMEM blocks free
+            ptx::tc_commit(bar(T::QB_KV_EMPTY));  // K of the step free
         }
         if (!ok) break;
         ptx::tc_commit(bar(T::QB_DQ_FULL));
