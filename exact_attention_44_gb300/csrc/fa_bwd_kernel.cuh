@@ -48,16 +48,27 @@ struct BwdWarps {
     static constexpr int CH = CW == 32 ? 16 : 32;  // columns per softmax TMEM load
     static constexpr int SOFTMAX_WARPS = 4 * NG;
     // D = 128: whole warpgroups (the last one: producer, issuer and two idle
-    // warps), launched at 80 registers a thread; setmaxnreg then moves 32 a
-    // thread from the last warpgroup to the softmax warpgroups (80 -> 88).
+    // warps), launched at 80 registers a thread; setmaxnreg then gives the
+    // softmax warpgroups 88 and splits the rest between the epilogue and the
+    // last warpgroup.
     // The host launches this kernel only after checking that it was built
     // with exactly REG_LAUNCH registers, so the budgets always add up.
     static constexpr bool SPLIT_REGS = D == 128;
     static constexpr int WARPS = SPLIT_REGS ? (SOFTMAX_WARPS + 6 + 3) / 4 * 4 : SOFTMAX_WARPS + 6;
     static constexpr int THREADS = WARPS * 32;
     static constexpr uint32_t REG_LAUNCH = 65536 / THREADS / 8 * 8;
-    static constexpr uint32_t REG_SOFTMAX = 88, REG_EPI = 72, REG_CTRL = 56;
-    static_assert(!SPLIT_REGS || 128 * (NG * REG_SOFTMAX + REG_EPI + REG_CTRL) == THREADS * REG_LAUNCH,
+    // Causal (short units, the epilogue's read-out often on the critical
+    // path): epilogue 72, producer/issuer 56.  Non-causal: epilogue 56 with
+    // the leaner store (bwd_store_rows), producer/issuer 72, whose MMA issue
+    // then spills less (measured on GB300: +3.0 % at Z1 Hq32 Hkv8 N8192,
+    // +1.2 % at Z4 H16 N1024 non-causal, -1.4 % if used when causal).
+    static constexpr uint32_t REG_SOFTMAX = 88;
+    static constexpr uint32_t reg_epi(bool causal) { return causal ? 72 : 56; }
+    static constexpr uint32_t reg_ctrl(bool causal) { return causal ? 56 : 72; }
+    static constexpr bool lean_store(bool causal) { return SPLIT_REGS && !causal; }
+    static_assert(!SPLIT_REGS || 128 * (NG * REG_SOFTMAX + reg_epi(true) + reg_ctrl(true)) == THREADS * REG_LAUNCH,
+                  "register budgets of the warpgroups");
+    static_assert(!SPLIT_REGS || 128 * (NG * REG_SOFTMAX + reg_epi(false) + reg_ctrl(false)) == THREADS * REG_LAUNCH,
                   "register budgets of the warpgroups");
 };
 
@@ -629,6 +640,59 @@ __device__ void kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar0, ui
     }
 }
 
+// The forward's tma_store_rows (one warp's 32 rows of a TMEM block out
+// through its staging area and TMA tensor stores) with fewer registers: each
+// swizzle chunk is converted and staged 32 columns at a time instead of
+// whole, so the epilogue warpgroup fits in its setmaxnreg budget.
+template <int D, int SW, bool BF16, typename AfterRead>
+__device__ __forceinline__ void bwd_store_rows(uint32_t taddr, float mul, uint32_t stage, const CUtensorMap* map,
+                                               int row0, int h, int z, bool store, AfterRead&& after_read) {
+    constexpr int SWE = SW / 2;              // elements per chunk row
+    constexpr int CH = SWE >= 32 ? 32 : 16;  // columns per TMEM load
+    constexpr int UPC = CH / 8;              // 16-byte units a piece fills
+    const int lane = threadIdx.x % 32;
+    const uint32_t swz = ((uint32_t)lane * SW >> 7) & (SW / 16 - 1);
+#pragma unroll 1
+    for (int k = 0; k < D / SWE; ++k) {
+#pragma unroll
+        for (int i = 0; i < SWE / CH; ++i) {
+            uint32_t r[CH];
+            if constexpr (CH == 32) ptx::tmem_ld32(taddr + k * SWE + i * CH, r);
+            else ptx::tmem_ld16(taddr + k * SWE + i * CH, r);
+            uint32_t pk[CH / 2];
+#pragma unroll
+            for (int x = 0; x < CH / 2; ++x)
+                pk[x] = pack2<BF16>(__uint_as_float(r[2 * x]) * mul, __uint_as_float(r[2 * x + 1]) * mul);
+            if (k == D / SWE - 1 && i == SWE / CH - 1) after_read();
+            if (i == 0) {
+                // the previous box must have been read out of the staging
+                // area (waited for after this chunk's first TMEM load)
+                if (lane == 0) ptx::bulk_wait_read_all();
+                __syncwarp();
+            }
+#pragma unroll
+            for (int c = 0; c < UPC; ++c)
+                ptx::st_shared_v4(stage + (uint32_t)lane * SW + ((((uint32_t)(i * UPC + c)) ^ swz) << 4), pk[4 * c],
+                                  pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && store) {
+            ptx::tma_store_4d(map, stage, k * SWE, row0, h, z);
+            ptx::bulk_commit();
+        }
+    }
+}
+
+// The store the epilogue warps use (bwd_store_rows where their register
+// budget is the smaller one, else the forward's tma_store_rows)
+template <int D, int SW, bool BF16, bool LEAN, typename AfterRead>
+__device__ __forceinline__ void epi_store_rows(uint32_t taddr, float mul, uint32_t stage, const CUtensorMap* map,
+                                               int row0, int h, int z, bool store, AfterRead&& after_read) {
+    if constexpr (LEAN) bwd_store_rows<D, SW, BF16>(taddr, mul, stage, map, row0, h, z, store, after_read);
+    else tma_store_rows<D, SW, BF16>(taddr, mul, stage, map, row0, h, z, store, after_read);
+}
+
 // One row per thread, straight to global memory, for a 32-row box that runs
 // past the end of a packed sequence: the next sequence's rows follow, so the
 // tensor store's clipping at the tensor's end does not guard them.  Every lane
@@ -709,9 +773,9 @@ __device__ void kv_epilogue(const CUtensorMap* tmDK, const CUtensorMap* tmDV, co
             ptx::mbar_arrive(bar(T::KB_ACC_FREE));
         };
         if (!bwd_varlen(VAR) || p.cu_k == nullptr || key0 + 32 <= w.nk) {
-            tma_store_rows<D, T::SW, BF16>(tmem + lane_addr + T::TM_DV, 1.f, stage, tmDV, w.krow0 + key0, w.hk, w.zc,
+            epi_store_rows<D, T::SW, BF16, BwdWarps<D>::lean_store(CAUSAL)>(tmem + lane_addr + T::TM_DV, 1.f, stage, tmDV, w.krow0 + key0, w.hk, w.zc,
                                            key0 < w.nk, []() {});
-            tma_store_rows<D, T::SW, BF16>(tmem + lane_addr + T::TM_DK, p.scale, stage, tmDK, w.krow0 + key0, w.hk,
+            epi_store_rows<D, T::SW, BF16, BwdWarps<D>::lean_store(CAUSAL)>(tmem + lane_addr + T::TM_DK, p.scale, stage, tmDK, w.krow0 + key0, w.hk,
                                            w.zc, key0 < w.nk, release);
         } else {
             direct_store_row<D, BF16>(tmem + lane_addr + T::TM_DV, 1.f, dv_row, key < w.nk, []() {});
@@ -973,7 +1037,7 @@ __device__ void q_epilogue(const CUtensorMap* tmDQ, const BwdParams& p, uint32_t
             ptx::mbar_arrive(bar(T::QB_DQ_FREE));
         };
         if (!bwd_varlen(VAR) || p.cu_q == nullptr || q0 + 32 <= w.nq) {
-            tma_store_rows<D, T::SW, BF16>(tmem + lane_addr + T::TM_DQ, p.scale, stage, tmDQ, w.qrow0 + q0, w.hq, w.zc,
+            epi_store_rows<D, T::SW, BF16, BwdWarps<D>::lean_store(CAUSAL)>(tmem + lane_addr + T::TM_DQ, p.scale, stage, tmDQ, w.qrow0 + q0, w.hq, w.zc,
                                            q0 < w.nq, release);
         } else {
             const int qr = w.i * 128 + row;
@@ -1048,8 +1112,8 @@ __global__ void __launch_bounds__(BwdWarps<D>::THREADS, 1)
     ptx::grid_launch_dependents();
     if constexpr (BwdWarps<D>::SPLIT_REGS) {
         if (warp < W_EPI) ptx::setmaxnreg_inc<BwdWarps<D>::REG_SOFTMAX>();
-        else if (warp < W_PRODUCER) ptx::setmaxnreg_dec<BwdWarps<D>::REG_EPI>();
-        else ptx::setmaxnreg_dec<BwdWarps<D>::REG_CTRL>();
+        else if (warp < W_PRODUCER) ptx::setmaxnreg_dec<BwdWarps<D>::reg_epi(CAUSAL)>();
+        else ptx::setmaxnreg_dec<BwdWarps<D>::reg_ctrl(CAUSAL)>();
     }
     if (warp < W_EPI) {
         kv_softmax<D, CAUSAL, BF16, VAR>(p, sbase, kbar0, tmem, warp / 4, ctl);
