@@ -477,3 +477,12 @@ def test_bwd_workspace_every_head_dim(lib, D):
     with pytest.raises(fa.FaError) as e:
         fa.fa_bwd_workspace_size(Z, Hq, Nq, 96)
     assert e.value.code == fa.FA_ERR_UNSUPPORTED
+
+
+def test_autograd_layer_imports_without_a_gpu():
+    # the autograd functions are defined (torch imported) without any CUDA call
+    import exact_attention_44_gb300 as fa
+    from exact_attention_44_gb300 import autograd
+    assert callable(fa.attention) and callable(fa.attention_varlen)
+    assert issubclass(autograd._Attention, __import__("torch").autograd.Function)
+    assert autograd._plain((-1, -1), None) and not autograd._plain((8, -1), None)
