@@ -40,7 +40,8 @@ namespace fa {
 // groups of CW (4 warps each, one per TMEM lane quarter); then 4 epilogue
 // warps, the TMA producer and the MMA issuer.  Four groups at D = 128, two
 // below (measured on GB300: four groups +4 % at Z1 Hq32 Hkv8 N8192 D128,
-// level at N1024; at D = 64 3-4 % slower than two).
+// level at N1024; at D = 64 3-4 % slower than two, and still 1-2 % slower
+// with the register split below).
 template <int D>
 struct BwdWarps {
     static constexpr int NG = D == 128 ? 4 : 2;
