@@ -822,7 +822,7 @@ fa_status fa_bwd_workspace_size(int Z, int Hq, int Nq, int D, size_t* bytes) {
 
 // The backward, plain (variant 0) or with the options of fa_bwd_ex (variant
 // 1: window; 2: window and ALiBi; 3: packed variable-length sequences with a
-// window and ALiBi; 4: packed sequences with a window; head dims up to 128).  With a sequence table (cu_q, cu_k) Z
+// window and ALiBi; 4: packed sequences with a window).  With a sequence table (cu_q, cu_k) Z
 // counts sequences, the tensors have one batch entry, Nq / Nkv are the packed
 // row totals, max_q / max_k bound the sequences' lengths and lse is (Hq, Nq).
 static fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -989,7 +989,6 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
     const int wr = open(opt->window_right) ? -1 : opt->window_right;
     const bool alibi = opt->alibi_slopes != nullptr;
     const int variant = varlen ? (alibi ? 3 : 4) : alibi ? 2 : (wl >= 0 || wr >= 0) ? 1 : 0;
-    if (variant != 0 && D > 128) return FA_ERR_UNSUPPORTED;
     return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, Z, Hq, Hkv, Nq, Nkv, D, sq, sk, sv, so, sdo, sdq, sdk, sdv, scale,
                     causal, dtype, workspace, workspace_bytes, stream, variant, wl, wr, opt->alibi_slopes,
                     varlen ? opt->cu_seqlens_q : nullptr, varlen ? opt->cu_seqlens_k : nullptr, opt->max_seqlen_q,

@@ -18,8 +18,7 @@ template <bool CAUSAL, bool BF16, int VAR>
 static cudaError_t launch_one(const BwdLaunchArgs& a) {
     constexpr int D = FA_HEAD_DIM;
 #if FA_HEAD_DIM == 256
-    static_assert(VAR == 0, "no backward variants at head dim 256");
-    auto bwd = fa_bwd_wide_kernel<CAUSAL, BF16>;
+    auto bwd = fa_bwd_wide_kernel<CAUSAL, BF16, VAR>;
     constexpr int SMEM = WideTraits::SMEM_BYTES, THREADS = WIDE_THREADS;
 #else
     auto bwd = fa_bwd_kernel<D, CAUSAL, BF16, VAR>;
@@ -65,9 +64,8 @@ static cudaError_t launch_one(const BwdLaunchArgs& a) {
 #define FA_CAT(a, b) FA_CAT2(a, b)
 // variant 0: fa_bwd; 1: window (fa_bwd_ex); 2: window and ALiBi; 3: packed
 // variable-length sequences with a window and ALiBi; 4: packed sequences with
-// a window (head dims up to 128)
+// a window
 cudaError_t FA_CAT(launch_bwd_d, FA_HEAD_DIM)(const BwdLaunchArgs& a, bool causal, bool bf16, int variant) {
-#if FA_HEAD_DIM != 256
     if (variant == 4) {
         if (causal) return bf16 ? launch_one<true, true, 4>(a) : launch_one<true, false, 4>(a);
         return bf16 ? launch_one<false, true, 4>(a) : launch_one<false, false, 4>(a);
@@ -84,9 +82,6 @@ cudaError_t FA_CAT(launch_bwd_d, FA_HEAD_DIM)(const BwdLaunchArgs& a, bool causa
         if (causal) return bf16 ? launch_one<true, true, 1>(a) : launch_one<true, false, 1>(a);
         return bf16 ? launch_one<false, true, 1>(a) : launch_one<false, false, 1>(a);
     }
-#else
-    if (variant != 0) return cudaErrorNotSupported;
-#endif
     if (causal) return bf16 ? launch_one<true, true, 0>(a) : launch_one<true, false, 0>(a);
     return bf16 ? launch_one<false, true, 0>(a) : launch_one<false, false, 0>(a);
 }

@@ -166,7 +166,7 @@ __device__ __forceinline__ void wide_step(const BwdUnit& w, int s, const BwdPara
 // Step slots: the dV pass alternates slots 0 and 1 (step s in slot s & 1),
 // the dK pass uses slot 0.  Every role counts the fills of each slot;
 // fill n of a slot completes phase n & 1 of its barriers.
-template <bool CAUSAL>
+template <bool CAUSAL, int VAR>
 __device__ void wide_kv_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const CUtensorMap* tmQ,
                                  const CUtensorMap* tmDO, const BwdParams& p, uint32_t sbase, uint32_t bar0,
                                  const Ctl& ctl) {
@@ -186,8 +186,8 @@ __device__ void wide_kv_producer(const CUtensorMap* tmK, const CUtensorMap* tmV,
         wide_step(w, s, p, hq, r0);
         const uint32_t full = bar(T::KB_QD_FULL + b);
         ptx::mbar_arrive_expect_tx(full, 2 * T::TILE64 + 512);
-        wide_load64(sbase + T::kv_q(b), tmQ, full, r0, hq, w.z, pol_q);
-        wide_load64(sbase + T::kv_do(b), tmDO, full, r0, hq, w.z, pol_q);
+        wide_load64(sbase + T::kv_q(b), tmQ, full, w.qrow0 + r0, hq, w.zc, pol_q);
+        wide_load64(sbase + T::kv_do(b), tmDO, full, w.qrow0 + r0, hq, w.zc, pol_q);
         const int64_t row0 = ((int64_t)w.z * p.Hq + hq) * p.Tq * 128 + r0;
         ptx::bulk_load(sbase + T::KV_OFF_LSE + b * 256u, p.lse2 + row0, 256, full);
         ptx::bulk_load(sbase + T::KV_OFF_DELTA + b * 256u, p.delta + row0, 256, full);
@@ -208,12 +208,12 @@ __device__ void wide_kv_producer(const CUtensorMap* tmK, const CUtensorMap* tmV,
             return false;
         }
         ptx::mbar_arrive_expect_tx(bar(T::KB_DO_FULL), T::TILE64);
-        wide_load64(sbase + T::kv_do(0), tmDO, bar(T::KB_DO_FULL), r0, hq, w.z, pol_q);
+        wide_load64(sbase + T::kv_do(0), tmDO, bar(T::KB_DO_FULL), w.qrow0 + r0, hq, w.zc, pol_q);
         ++nd;
         if (n0 >= 1 && !wait_phase(bar(T::KB_QD_EMPTY), (n0 - 1) & 1u, ctl, SITE_B_QD_EMPTY)) return false;
         const uint32_t full = bar(T::KB_QD_FULL);
         ptx::mbar_arrive_expect_tx(full, T::TILE64 + 512);
-        wide_load64(sbase + T::kv_q(0), tmQ, full, r0, hq, w.z, pol_q);
+        wide_load64(sbase + T::kv_q(0), tmQ, full, w.qrow0 + r0, hq, w.zc, pol_q);
         const int64_t row0 = ((int64_t)w.z * p.Hq + hq) * p.Tq * 128 + r0;
         ptx::bulk_load(sbase + T::KV_OFF_LSE, p.lse2 + row0, 256, full);
         ptx::bulk_load(sbase + T::KV_OFF_DELTA, p.delta + row0, 256, full);
@@ -221,7 +221,7 @@ __device__ void wide_kv_producer(const CUtensorMap* tmK, const CUtensorMap* tmV,
         return true;
     };
     for (int pos = blockIdx.x; ok && unit_at<CAUSAL>(pos) < p.nunits; pos += gridDim.x) {
-        const BwdUnit w = bwd_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        const BwdUnit w = bwd_unit<CAUSAL, VAR>(unit_at<CAUSAL>(pos), p);
         if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_LOAD)) { ok = false; break; }
         if (w.nsteps == 0) continue;
         // K and the V region (slot 1, then V) are free once the previous
@@ -231,7 +231,7 @@ __device__ void wide_kv_producer(const CUtensorMap* tmK, const CUtensorMap* tmV,
             withheld = true;  // never issued: the issuer's wait for K must time out
         } else {
             ptx::mbar_arrive_expect_tx(bar(T::KB_K_FULL), T::TILE128);
-            wide_load128(sbase + T::KV_OFF_K, tmK, bar(T::KB_K_FULL), w.j * 128, w.hk, w.z, pol_kv);
+            wide_load128(sbase + T::KV_OFF_K, tmK, bar(T::KB_K_FULL), w.krow0 + w.j * 128, w.hk, w.zc, pol_kv);
         }
         ++uc;
         const int steps = 2 * w.nsteps;  // >= 2: slot 1 is filled at least once
@@ -240,7 +240,7 @@ __device__ void wide_kv_producer(const CUtensorMap* tmK, const CUtensorMap* tmV,
         // V over slot 1, once its last dV step is done
         if (!wait_phase(bar(T::KB_QD_EMPTY + 1), (n1 - 1) & 1u, ctl, SITE_B_QD_EMPTY)) { ok = false; break; }
         ptx::mbar_arrive_expect_tx(bar(T::KB_V_FULL), T::TILE128);
-        wide_load128(sbase + T::KV_OFF_V, tmV, bar(T::KB_V_FULL), w.j * 128, w.hk, w.z, pol_kv);
+        wide_load128(sbase + T::KV_OFF_V, tmV, bar(T::KB_V_FULL), w.krow0 + w.j * 128, w.hk, w.zc, pol_kv);
         ++vc;
         for (int s = 0; ok && s < steps; ++s) ok = fill_dk(w, s);
     }
@@ -254,7 +254,7 @@ __device__ void wide_kv_producer(const CUtensorMap* tmK, const CUtensorMap* tmV,
     }
 }
 
-template <bool CAUSAL, bool BF16>
+template <bool CAUSAL, bool BF16, int VAR>
 __device__ void wide_kv_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0, uint32_t tmem, const Ctl& ctl) {
     using T = WideTraits;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
@@ -295,7 +295,7 @@ __device__ void wide_kv_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0
         return true;
     };
     for (int pos = blockIdx.x; ok && unit_at<CAUSAL>(pos) < p.nunits; pos += gridDim.x) {
-        const BwdUnit w = bwd_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        const BwdUnit w = bwd_unit<CAUSAL, VAR>(unit_at<CAUSAL>(pos), p);
         if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_MMA)) { ok = false; break; }
         if (w.nsteps == 0) continue;
         if (!wait_phase(bar(T::KB_K_FULL), uc & 1u, ctl, SITE_B_KV_FULL)) { ok = false; break; }
@@ -364,7 +364,7 @@ __device__ void wide_kv_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0
 // the step's Sᵀ block; dK pass: Pᵀ in registers, dSᵀ = Pᵀ ∘ (dPᵀ − Δ) over the
 // first half of the group's columns of dPᵀ.  P and dS are rounded to the
 // input type (the products' operands).
-template <bool CAUSAL, bool BF16>
+template <bool CAUSAL, bool BF16, int VAR>
 __device__ void wide_kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar0, uint32_t tmem, int h,
                                 const Ctl& ctl) {
     static_assert(WIDE_CW == 32, "one 32-column TMEM load per group");
@@ -376,7 +376,7 @@ __device__ void wide_kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar
     const float c = p.scale_log2;
     uint32_t n0 = 0, n1 = 0;  // fills of slots 0 and 1 consumed
     for (int pos = blockIdx.x; unit_at<CAUSAL>(pos) < p.nunits; pos += gridDim.x) {
-        const BwdUnit w = bwd_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        const BwdUnit w = bwd_unit<CAUSAL, VAR>(unit_at<CAUSAL>(pos), p);
         if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_SOFTMAX)) return;
         const int key = w.j * 128 + row;
         const int steps = 2 * w.nsteps;
@@ -396,6 +396,12 @@ __device__ void wide_kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar
                 // causal: only the diagonal block has keys after queries (key > query -> P = 0)
                 const bool diag = CAUSAL && r0 / 128 == w.j;
                 const int q0 = r0 + h * WIDE_CW;  // the group's first query
+                // variants: d = query − key, masked per pair only in a step not
+                // wholly kept (window sides, causal rule, keys past the
+                // sequence's); ALiBi adds slope2·|d| (log2 units)
+                const bool full = VAR == 0 || var_block_kept<CAUSAL>(r0 - (w.j * 128 + 127), r0 + 63 - w.j * 128,
+                                                                     w.j * 128 + 128, w.nk, p);
+                const float slope2 = bwd_alibi(VAR) ? -__ldg(p.alibi + hq) * 1.4426950408889634f : 0.f;
                 uint32_t pk[WIDE_CW / 2];
                 {
                     uint32_t a[32];
@@ -406,8 +412,20 @@ __device__ void wide_kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar
                         asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(l0), "=f"(l1) : "r"(lse_a + 4u * x));
                         float e0 = fmaf(__uint_as_float(a[x]), c, -l0);
                         float e1 = fmaf(__uint_as_float(a[x + 1]), c, -l1);
-                        if (diag && key > q0 + x) e0 = -INFINITY;
-                        if (diag && key > q0 + x + 1) e1 = -INFINITY;
+                        if constexpr (VAR == 0) {
+                            if (diag && key > q0 + x) e0 = -INFINITY;
+                            if (diag && key > q0 + x + 1) e1 = -INFINITY;
+                        } else {
+                            const int d0 = q0 + x - key;
+                            if constexpr (bwd_alibi(VAR)) {
+                                e0 = fmaf(slope2, fabsf((float)d0), e0);
+                                e1 = fmaf(slope2, fabsf((float)(d0 + 1)), e1);
+                            }
+                            if (!full) {
+                                if (var_dropped<CAUSAL>(d0, key, w.nk, p)) e0 = -INFINITY;
+                                if (var_dropped<CAUSAL>(d0 + 1, key, w.nk, p)) e1 = -INFINITY;
+                            }
+                        }
                         pk[x / 2] = pack2<BF16>(ptx::ex2(e0), ptx::ex2(e1));
                     }
                 }
@@ -438,7 +456,7 @@ __device__ void wide_kv_softmax(const BwdParams& p, uint32_t sbase, uint32_t bar
 
 // Thread = key: dV, then dK (times scale), read out, released, stored; a
 // unit no query sees gets zeros.
-template <bool CAUSAL, bool BF16>
+template <bool CAUSAL, bool BF16, int VAR>
 __device__ void wide_kv_epilogue(const CUtensorMap* tmDK, const CUtensorMap* tmDV, const BwdParams& p, uint32_t sbase,
                                  uint32_t bar0, uint32_t tmem, const Ctl& ctl) {
     using T = WideTraits;
@@ -452,18 +470,18 @@ __device__ void wide_kv_epilogue(const CUtensorMap* tmDK, const CUtensorMap* tmD
     };
     uint32_t acc = 0;
     for (int pos = blockIdx.x; unit_at<CAUSAL>(pos) < p.nunits; pos += gridDim.x) {
-        const BwdUnit w = bwd_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        const BwdUnit w = bwd_unit<CAUSAL, VAR>(unit_at<CAUSAL>(pos), p);
         if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_EPILOGUE)) {
             drain();
             return;
         }
-        const int key = w.j * 128 + row;
+        const int key = w.j * 128 + row;  // within the unit's sequence
+        uint8_t* dk_row = reinterpret_cast<uint8_t*>(p.dk) +
+                          2 * ((int64_t)w.zc * p.sdk_z + (int64_t)w.hk * p.sdk_h + (int64_t)(w.krow0 + key) * p.sdk_n);
+        uint8_t* dv_row = reinterpret_cast<uint8_t*>(p.dv) +
+                          2 * ((int64_t)w.zc * p.sdv_z + (int64_t)w.hk * p.sdv_h + (int64_t)(w.krow0 + key) * p.sdv_n);
         if (w.nsteps == 0) {
-            if (key < p.Nkv) {
-                uint8_t* dk_row = reinterpret_cast<uint8_t*>(p.dk) +
-                                  2 * ((int64_t)w.z * p.sdk_z + (int64_t)w.hk * p.sdk_h + (int64_t)key * p.sdk_n);
-                uint8_t* dv_row = reinterpret_cast<uint8_t*>(p.dv) +
-                                  2 * ((int64_t)w.z * p.sdv_z + (int64_t)w.hk * p.sdv_h + (int64_t)key * p.sdv_n);
+            if (key < w.nk) {
 #pragma unroll
                 for (int x = 0; x < 256 / 8; ++x) {
                     reinterpret_cast<uint4*>(dk_row)[x] = make_uint4(0, 0, 0, 0);
@@ -479,18 +497,26 @@ __device__ void wide_kv_epilogue(const CUtensorMap* tmDK, const CUtensorMap* tmD
                 return;
             }
             ptx::tc_fence_after();
-            tma_store_rows<256, T::SW, BF16>(tmem + lane_addr + T::TM_ACC, pass == 0 ? 1.f : p.scale, stage,
-                                             pass == 0 ? tmDV : tmDK, key0, w.hk, w.z, key0 < p.Nkv, [&]() {
-                                                 ptx::tc_fence_before();
-                                                 ptx::mbar_arrive(bar(T::KB_ACC_FREE));
-                                             });
+            const auto release = [&]() {
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(bar(T::KB_ACC_FREE));
+            };
+            // a 32-row box past the end of a packed sequence goes row by row
+            if (!bwd_varlen(VAR) || p.cu_k == nullptr || key0 + 32 <= w.nk) {
+                tma_store_rows<256, T::SW, BF16>(tmem + lane_addr + T::TM_ACC, pass == 0 ? 1.f : p.scale, stage,
+                                                 pass == 0 ? tmDV : tmDK, w.krow0 + key0, w.hk, w.zc, key0 < w.nk,
+                                                 release);
+            } else {
+                direct_store_row<256, BF16>(tmem + lane_addr + T::TM_ACC, pass == 0 ? 1.f : p.scale,
+                                            pass == 0 ? dv_row : dk_row, key < w.nk, release);
+            }
         }
     }
     drain();
 }
 
 // ===================================================================== dQ ===
-template <bool CAUSAL>
+template <bool CAUSAL, int VAR>
 __device__ void wide_q_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const CUtensorMap* tmQ,
                                 const CUtensorMap* tmDO, const BwdParams& p, uint32_t sbase, uint32_t bar0,
                                 const Ctl& ctl, int first) {
@@ -501,12 +527,13 @@ __device__ void wide_q_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, 
     uint32_t uc = 0, g = 0, gv = 0;  // fills of Q/dO, K and V
     bool ok = true;
     for (int pos = first; ok && unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x) {
-        const DqUnit w = dq_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        const DqUnit w = dq_unit<CAUSAL, VAR>(unit_at<CAUSAL>(pos), p);
         if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_LOAD)) { ok = false; break; }
+        if (w.skip) continue;
         if (uc > 0 && !wait_phase(bar(T::QB_QD_EMPTY), (uc - 1) & 1u, ctl, SITE_B_QD_EMPTY)) { ok = false; break; }
         ptx::mbar_arrive_expect_tx(bar(T::QB_QD_FULL), 2 * T::TILE128);
-        wide_load128(sbase + T::Q_OFF_Q, tmQ, bar(T::QB_QD_FULL), w.i * 128, w.hq, w.z, pol_q);
-        wide_load128(sbase + T::Q_OFF_DO, tmDO, bar(T::QB_QD_FULL), w.i * 128, w.hq, w.z, pol_q);
+        wide_load128(sbase + T::Q_OFF_Q, tmQ, bar(T::QB_QD_FULL), w.qrow0 + w.i * 128, w.hq, w.zc, pol_q);
+        wide_load128(sbase + T::Q_OFF_DO, tmDO, bar(T::QB_QD_FULL), w.qrow0 + w.i * 128, w.hq, w.zc, pol_q);
         ++uc;
         const int steps = 2 * w.nkv;  // 64-key steps
         for (int s = 0; s < steps; ++s, ++g) {
@@ -514,11 +541,11 @@ __device__ void wide_q_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, 
             // done, then K once the previous step's dQ product (it reads K) is
             if (gv >= 1 && !wait_phase(bar(T::QB_V_EMPTY), (gv - 1) & 1u, ctl, SITE_B_KV_EMPTY)) { ok = false; break; }
             ptx::mbar_arrive_expect_tx(bar(T::QB_V_FULL), T::TILE64);
-            wide_load64(sbase + T::Q_OFF_V, tmV, bar(T::QB_V_FULL), s * 64, w.hk, w.z, pol_kv);
+            wide_load64(sbase + T::Q_OFF_V, tmV, bar(T::QB_V_FULL), w.krow0 + w.j0 * 128 + s * 64, w.hk, w.zc, pol_kv);
             ++gv;
             if (g >= 1 && !wait_phase(bar(T::QB_KV_EMPTY), (g - 1) & 1u, ctl, SITE_B_KV_EMPTY)) { ok = false; break; }
             ptx::mbar_arrive_expect_tx(bar(T::QB_KV_FULL), T::TILE64);
-            wide_load64(sbase + T::Q_OFF_K, tmK, bar(T::QB_KV_FULL), s * 64, w.hk, w.z, pol_kv);
+            wide_load64(sbase + T::Q_OFF_K, tmK, bar(T::QB_KV_FULL), w.krow0 + w.j0 * 128 + s * 64, w.hk, w.zc, pol_kv);
         }
     }
     if (!ok) {
@@ -528,7 +555,7 @@ __device__ void wide_q_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, 
     }
 }
 
-template <bool CAUSAL, bool BF16>
+template <bool CAUSAL, bool BF16, int VAR>
 __device__ void wide_q_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0, uint32_t tmem, const Ctl& ctl,
                               int first) {
     using T = WideTraits;
@@ -544,8 +571,9 @@ __device__ void wide_q_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0,
     uint32_t uc = 0, g = 0;
     bool ok = true;
     for (int pos = first; ok && unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x) {
-        const DqUnit w = dq_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        const DqUnit w = dq_unit<CAUSAL, VAR>(unit_at<CAUSAL>(pos), p);
         if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_MMA)) { ok = false; break; }
+        if (w.skip) continue;
         if (!wait_phase(bar(T::QB_QD_FULL), uc & 1u, ctl, SITE_B_QD_FULL)) { ok = false; break; }
         const int steps = 2 * w.nkv;
         for (int s = 0; s < steps; ++s, ++g) {
@@ -590,7 +618,7 @@ __device__ void wide_q_issuer(const BwdParams& p, uint32_t sbase, uint32_t bar0,
 // Thread = query (TMEM lane); column group h takes the step's keys h*CW ..
 // h*CW + CW - 1: P = 2^(S·c − lse2), dS = P ∘ (dP − Δ) over the first half of
 // the group's columns of S.
-template <bool CAUSAL, bool BF16>
+template <bool CAUSAL, bool BF16, int VAR>
 __device__ void wide_q_softmax(const BwdParams& p, uint32_t bar0, uint32_t tmem, int h, const Ctl& ctl, int first) {
     using T = WideTraits;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
@@ -600,17 +628,23 @@ __device__ void wide_q_softmax(const BwdParams& p, uint32_t bar0, uint32_t tmem,
     const float c = p.scale_log2;
     uint32_t g = 0;
     for (int pos = first; unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x) {
-        const DqUnit w = dq_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+        const DqUnit w = dq_unit<CAUSAL, VAR>(unit_at<CAUSAL>(pos), p);
         if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_SOFTMAX)) return;
+        if (w.skip) continue;
         const int64_t r = ((int64_t)w.z * p.Hq + w.hq) * p.Tq * 128 + (int64_t)w.i * 128 + row;
         const float l2 = __ldg(p.lse2 + r), dl = __ldg(p.delta + r);
+        const float slope2 = bwd_alibi(VAR) ? -__ldg(p.alibi + w.hq) * 1.4426950408889634f : 0.f;
         const int q = w.i * 128 + row;
         const int steps = 2 * w.nkv;
         for (int s = 0; s < steps; ++s, ++g) {
             if (!warp_wait_phase(bar(T::QB_S_FULL), g & 1u, ctl, SITE_B_S_FULL)) return;
             ptx::tc_fence_after();
-            const bool diag = CAUSAL && s / 2 == w.i;  // keys after the query only on the diagonal block
-            const int k0 = s * 64 + h * WIDE_CW;       // the group's first key
+            const int kb = w.j0 * 128 + s * 64;         // the step's first key
+            const bool diag = CAUSAL && kb / 128 == w.i;  // keys after the query only on the diagonal block
+            const int k0 = kb + h * WIDE_CW;              // the group's first key
+            // variants: d = query − key, masked per pair only in a step not wholly kept
+            const bool full = VAR == 0 || var_block_kept<CAUSAL>(w.i * 128 - (kb + 63), w.i * 128 + 127 - kb, kb + 64,
+                                                                 w.nk, p);
             uint32_t sa[32], da[32];
             ptx::tmem_ld32_issue(tmem + lane_addr + T::TM_S + h * WIDE_CW, sa);
             ptx::tmem_ld32_issue(tmem + lane_addr + T::TM_DP + h * WIDE_CW, da);
@@ -623,8 +657,20 @@ __device__ void wide_q_softmax(const BwdParams& p, uint32_t bar0, uint32_t tmem,
                 const int k = 2 * x;
                 float e0 = fmaf(__uint_as_float(sa[k]), c, -l2);
                 float e1 = fmaf(__uint_as_float(sa[k + 1]), c, -l2);
-                if (diag && k0 + k > q) e0 = -INFINITY;
-                if (diag && k0 + k + 1 > q) e1 = -INFINITY;
+                if constexpr (VAR == 0) {
+                    if (diag && k0 + k > q) e0 = -INFINITY;
+                    if (diag && k0 + k + 1 > q) e1 = -INFINITY;
+                } else {
+                    const int d0 = q - (k0 + k);
+                    if constexpr (bwd_alibi(VAR)) {
+                        e0 = fmaf(slope2, fabsf((float)d0), e0);
+                        e1 = fmaf(slope2, fabsf((float)(d0 - 1)), e1);
+                    }
+                    if (!full) {
+                        if (var_dropped<CAUSAL>(d0, k0 + k, w.nk, p)) e0 = -INFINITY;
+                        if (var_dropped<CAUSAL>(d0 - 1, k0 + k + 1, w.nk, p)) e1 = -INFINITY;
+                    }
+                }
                 const float2 pp = unpack2<BF16>(pack2<BF16>(ptx::ex2(e0), ptx::ex2(e1)));  // P rounded as in dV
                 ds[x] = pack2<BF16>(pp.x * (__uint_as_float(da[k]) - dl), pp.y * (__uint_as_float(da[k + 1]) - dl));
             }
@@ -637,35 +683,46 @@ __device__ void wide_q_softmax(const BwdParams& p, uint32_t bar0, uint32_t tmem,
 }
 
 // Thread = query: dQ (times scale) read out, released, stored.
-template <bool CAUSAL, bool BF16>
+template <bool CAUSAL, bool BF16, int VAR>
 __device__ void wide_q_epilogue(const CUtensorMap* tmDQ, const BwdParams& p, uint32_t sbase, uint32_t bar0,
                                 uint32_t tmem, const Ctl& ctl, int first) {
     using T = WideTraits;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     const int quad = (threadIdx.x / 32) % 4;
+    const int row = quad * 32 + threadIdx.x % 32;  // query within the block
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
     const uint32_t stage = sbase + T::Q_OFF_OST + (uint32_t)quad * 32u * T::SW;
     auto drain = [&]() {
         if (threadIdx.x % 32 == 0) ptx::bulk_wait_all();
     };
     uint32_t uc = 0;
-    for (int pos = first; unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x, ++uc) {
-        const DqUnit w = dq_unit<CAUSAL>(unit_at<CAUSAL>(pos), p);
+    for (int pos = first; unit_at<CAUSAL>(pos) < p.nunits_q; pos += gridDim.x) {
+        const DqUnit w = dq_unit<CAUSAL, VAR>(unit_at<CAUSAL>(pos), p);
         if (!unit_checked(w, p, ctl, SITE_CHECK_BWD_EPILOGUE)) {
             drain();
             return;
         }
+        if (w.skip) continue;
         if (!warp_wait_phase(bar(T::QB_DQ_FULL), uc & 1u, ctl, SITE_B_DQ_FULL)) {
             drain();
             return;
         }
         ptx::tc_fence_after();
         const int q0 = w.i * 128 + 32 * quad;
-        tma_store_rows<256, T::SW, BF16>(tmem + lane_addr + T::TM_ACC, p.scale, stage, tmDQ, q0, w.hq, w.z, q0 < p.Nq,
-                                         [&]() {
-                                             ptx::tc_fence_before();
-                                             ptx::mbar_arrive(bar(T::QB_DQ_FREE));
-                                         });
+        const auto release = [&]() {
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(T::QB_DQ_FREE));
+        };
+        if (!bwd_varlen(VAR) || p.cu_q == nullptr || q0 + 32 <= w.nq) {
+            tma_store_rows<256, T::SW, BF16>(tmem + lane_addr + T::TM_ACC, p.scale, stage, tmDQ, w.qrow0 + q0, w.hq,
+                                             w.zc, q0 < w.nq, release);
+        } else {
+            const int qr = w.i * 128 + row;
+            uint8_t* dq_row = reinterpret_cast<uint8_t*>(p.dq) +
+                              2 * ((int64_t)w.zc * p.sdq_z + (int64_t)w.hq * p.sdq_h + (int64_t)(w.qrow0 + qr) * p.sdq_n);
+            direct_store_row<256, BF16>(tmem + lane_addr + T::TM_ACC, p.scale, dq_row, qr < w.nq, release);
+        }
+        ++uc;
     }
     drain();
 }
@@ -674,7 +731,7 @@ __device__ void wide_q_epilogue(const CUtensorMap* tmDQ, const BwdParams& p, uin
 // dK/dV units (positions c, c + grid, ...) then dQ units from position
 // grid - 1 - c on, in the same shared memory and TMEM, as for the smaller
 // head dims.
-template <bool CAUSAL, bool BF16>
+template <bool CAUSAL, bool BF16, int VAR = 0>
 __global__ void __launch_bounds__(WIDE_THREADS, 1)
     fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                        const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
@@ -715,13 +772,13 @@ __global__ void __launch_bounds__(WIDE_THREADS, 1)
     ptx::grid_dependency_wait();
     ptx::grid_launch_dependents();
     if (warp < W_EPI) {
-        wide_kv_softmax<CAUSAL, BF16>(p, sbase, kbar0, tmem, warp / 4, ctl);
+        wide_kv_softmax<CAUSAL, BF16, VAR>(p, sbase, kbar0, tmem, warp / 4, ctl);
     } else if (warp < W_PRODUCER) {
-        wide_kv_epilogue<CAUSAL, BF16>(&tmDK, &tmDV, p, sbase, kbar0, tmem, ctl);
+        wide_kv_epilogue<CAUSAL, BF16, VAR>(&tmDK, &tmDV, p, sbase, kbar0, tmem, ctl);
     } else if (warp == W_PRODUCER) {
-        if (lane == 0) wide_kv_producer<CAUSAL>(&tmK, &tmV, &tmQ, &tmDO, p, sbase, kbar0, ctl);
+        if (lane == 0) wide_kv_producer<CAUSAL, VAR>(&tmK, &tmV, &tmQ, &tmDO, p, sbase, kbar0, ctl);
     } else {
-        if (lane == 0) wide_kv_issuer<CAUSAL, BF16>(p, sbase, kbar0, tmem, ctl);
+        if (lane == 0) wide_kv_issuer<CAUSAL, BF16, VAR>(p, sbase, kbar0, tmem, ctl);
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -736,13 +793,13 @@ __global__ void __launch_bounds__(WIDE_THREADS, 1)
         ptx::tc_fence_after();
         const int first = (int)gridDim.x - 1 - (int)blockIdx.x;
         if (warp < W_EPI) {
-            wide_q_softmax<CAUSAL, BF16>(p, qbar0, tmem, warp / 4, ctl, first);
+            wide_q_softmax<CAUSAL, BF16, VAR>(p, qbar0, tmem, warp / 4, ctl, first);
         } else if (warp < W_PRODUCER) {
-            wide_q_epilogue<CAUSAL, BF16>(&tmDQ, p, sbase, qbar0, tmem, ctl, first);
+            wide_q_epilogue<CAUSAL, BF16, VAR>(&tmDQ, p, sbase, qbar0, tmem, ctl, first);
         } else if (warp == W_PRODUCER) {
-            if (lane == 0) wide_q_producer<CAUSAL>(&tmK, &tmV, &tmQ, &tmDO, p, sbase, qbar0, ctl, first);
+            if (lane == 0) wide_q_producer<CAUSAL, VAR>(&tmK, &tmV, &tmQ, &tmDO, p, sbase, qbar0, ctl, first);
         } else {
-            if (lane == 0) wide_q_issuer<CAUSAL, BF16>(p, sbase, qbar0, tmem, ctl, first);
+            if (lane == 0) wide_q_issuer<CAUSAL, BF16, VAR>(p, sbase, qbar0, tmem, ctl, first);
         }
         ptx::tc_fence_before();
         __syncthreads();

@@ -343,10 +343,10 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
  *
  * Errors: those of fa_bwd, plus FA_ERR_INVALID_ARG for a window side below
  * -1, only one of the cu_seqlens arrays, or a negative max_seqlen_q or
- * max_seqlen_k, FA_ERR_ALIGNMENT for an option array not 4-byte aligned, and
- * FA_ERR_UNSUPPORTED for any option at D = 256.  The offsets are not
- * validated on the host; those outside the packed extents are clamped to them
- * on the device.
+ * max_seqlen_k, and FA_ERR_ALIGNMENT for an option array not 4-byte aligned.
+ * Every head dim of fa_bwd takes every option.  The offsets are not validated
+ * on the host; those outside the packed extents are clamped to them on the
+ * device.
  */
 fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
                     void* dq, void* dk, void* dv, int Z, int Hq, int Hkv, int Nq, int Nkv, int D,

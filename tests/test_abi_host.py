@@ -235,9 +235,6 @@ def test_bwd_ex_option_errors_on_the_host(lib):
     assert call(cq=0x1002, ck=0x2000, maxq=8) == fa.FA_ERR_ALIGNMENT
     assert call(cq=0x1000, ck=0x2001, maxq=8) == fa.FA_ERR_ALIGNMENT
     assert call(alibi=0x1001) == fa.FA_ERR_ALIGNMENT
-    # every option needs a head dim up to 128
-    assert call(D=256, cq=0x1000, ck=0x2000, maxq=64) == fa.FA_ERR_UNSUPPORTED
-    assert call(D=256, wl=8) == fa.FA_ERR_UNSUPPORTED
 
 
 # ---- fa_fwd_schedule: the forward's schedule, host-only -------------------

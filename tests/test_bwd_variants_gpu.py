@@ -115,19 +115,28 @@ def test_open_window_is_the_plain_backward_bit_for_bit():
         assert torch.equal(a, b)
 
 
-def test_head_dim_256_variants_are_unsupported():
-    import torch
-    import exact_attention_44_gb300 as fa
-    q, k, v = si.qkv(309, 1, 2, 2, 64, 64, 256, "bf16")
-    qt, kt, vt = (to_device(x, "bf16") for x in (q, k, v))
-    o, lse = fa.fa_fwd(qt, kt, vt, causal=False)
-    with pytest.raises(fa.FaError) as e:
-        fa.fa_bwd_ex(qt, kt, vt, o, lse, torch.zeros_like(qt), window=(8, 8))
-    assert e.value.code == fa.FA_ERR_UNSUPPORTED
-    cu = torch.tensor([0, 64], dtype=torch.int32, device="cuda")
-    with pytest.raises(fa.FaError) as e:
-        fa.fa_bwd_ex(qt, kt, vt, o, lse[0], torch.zeros_like(qt), cu_seqlens_q=cu, cu_seqlens_k=cu)
-    assert e.value.code == fa.FA_ERR_UNSUPPORTED
+@pytest.mark.parametrize("causal", [False, True])
+def test_head_dim_256_window(causal):
+    # the two-pass D = 256 kernel with window-bounded units, ragged lengths
+    check_bwd_ex(440, 1, 4, 2, 300, 333, 256, "bf16", causal, window=(100, 40))
+
+
+def test_head_dim_256_alibi_with_window():
+    check_bwd_ex(441, 2, 4, 4, 257, 257, 256, "fp16", True, window=(150, -1), alibi=[0.5, 0.25, 0.125, 0.0625])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_head_dim_256_varlen(causal):
+    # packed sequences at D = 256: a sequence without queries, one without
+    # keys, single rows, crossing and ragged blocks, rows past the last
+    lens_q = [5, 0, 135, 60, 1, 129]
+    lens_k = [7, 23, 0, 300, 1, 200]
+    check_bwd_varlen(442, lens_q, lens_k, 4, 2, 256, "bf16", causal, extra_q=9, extra_k=4)
+
+
+def test_head_dim_256_varlen_window_alibi():
+    check_bwd_varlen(443, [200, 17, 260], [200, 300, 260], 4, 2, 256, "fp16", True, window=(50, -1),
+                     alibi=[0.5, 0.25, 0.125, 0.0625])
 
 
 # ---- packed variable-length sequences -------------------------------------
