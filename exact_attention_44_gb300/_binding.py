@@ -281,7 +281,7 @@ def fa_bwd(q, k, v, o, lse, do, dq=None, dk=None, dv=None, *, scale: float | Non
 def fa_bwd_ex(q, k, v, o, lse, do, dq=None, dk=None, dv=None, *, scale: float | None = None, causal: bool = False,
               window=(-1, -1), alibi_slopes=None, cu_seqlens_q=None, cu_seqlens_k=None,
               max_seqlen_q: int | None = None, max_seqlen_k: int | None = None, workspace=None, stream=None):
-    """Gradients of fa_fwd_ex's forward (libfa's fa_bwd_ex; D <= 128 with any option).
+    """Gradients of fa_fwd_ex's forward (libfa's fa_bwd_ex; every head dim, any option).
 
     Arguments as for fa_bwd, plus the options the forward took: window (left,
     right), -1 for an open side; alibi_slopes (CUDA fp32 (Hq,) or None); and

@@ -76,8 +76,6 @@ def attention(q, k, v, *, scale: float | None = None, causal: bool = False, wind
     1/sqrt(D).  window = (left, right) keeps keys j with i - left <= j <= i +
     right (-1: open side); alibi_slopes: CUDA fp32 (Hq,) or None.  Returns O
     shaped like q (and the (Z, Hq, Nq) natural-log lse with return_lse).
-    Gradients need D <= 128 with a window or slopes (any supported D
-    without).
     """
     o, lse = _Attention.apply(q, k, v, scale, bool(causal), tuple(window), alibi_slopes)
     return (o, lse) if return_lse else o
@@ -92,7 +90,7 @@ def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int | No
     cu_seqlens_q / cu_seqlens_k: CUDA int32 (Z + 1) offsets (sequence z owns
     rows cu[z] .. cu[z+1]-1 and attends only to its own keys).  max_seqlen_q /
     max_seqlen_k default to the longest sequences (read back from the device
-    once per call).  Returns O in q's form (and lse (Hq, total_q)).  D <= 128.
+    once per call).  Returns O in q's form (and lse (Hq, total_q)).
     """
     def longest(cu):
         c = cu.cpu()
