@@ -571,6 +571,7 @@ VARIANT_SHAPES = {
     "z4_h16_n4096_d128_bf16_causal_window512": (4, 16, 16, 4096, 128, "bf16", True, (512, 0), False, None),
     "z4_h16_n2048_d128_bf16_causal_alibi": (4, 16, 16, 2048, 128, "bf16", True, (-1, -1), True, None),
     "varlen_16seq_256to4096_h16_d128_bf16_causal": (16, 16, 16, 0, 128, "bf16", True, (-1, -1), False, "seeded"),
+    "z2_h16_n4096_d256_bf16_causal_window512": (2, 16, 16, 4096, 256, "bf16", True, (512, 0), False, None),
 }
 
 
