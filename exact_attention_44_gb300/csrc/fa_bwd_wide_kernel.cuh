@@ -33,7 +33,7 @@
 // forward's options, "Write Triton Attention Kernel", Inputs) take the
 // shared unit decoders' window ranges and sequence tables: loads start at the
 // sequence's rows and the window's first key block, pairs are masked only in
-// steps not wholly kept, ALiBi adds slope·log2e·|i − j| in both phases, and a
+// steps not wholly kept, ALiBi subtracts slope·log2e·|i − j| in both phases, and a
 // 32-row box that crosses a sequence end is stored row by row.
 // The pre kernel (Δ, base-2 lse), the unit orders and the tile stores are the
 // smaller head dims' (fa_bwd_kernel.cuh).
