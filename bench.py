@@ -665,7 +665,7 @@ def measure_variant(name, device, stream, peaks, steps=10, bwd=False):
 
 # fa_bwd workloads (gradients of the forward; 5 products of 2 N^2 D per head, half for causal)
 BWD_SHAPES = ["z4_h16_n1024_d128_bf16", "z1_hq32_hkv8_n8192_d128_bf16_noncausal", "z8_h16_n2048_d64_fp16",
-              "z8_h16_n2048_d256_bf16"]
+              "z8_h16_n2048_d256_bf16", "z1_hq32_hkv8_n32768_d128_bf16_causal"]
 
 
 def measure_bwd(name, device, stream, peaks, steps=10):

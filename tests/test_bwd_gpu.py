@@ -207,3 +207,34 @@ def test_bitwise_repeatable():
         b = fa.fa_bwd(q, k, v, o, lse, do, causal=causal)
         torch.cuda.synchronize()
         assert all(torch.equal(x, y) for x, y in zip(a, b))
+
+
+def test_headline_size_gradient_invariants():
+    # Z1 Hq32 Hkv8 N32768 D128 bf16 causal (the forward's headline workload):
+    # too large for the oracle, so two properties that hold at any size are
+    # checked per kv head over its GQA group.  Rows of P sum to one, so the
+    # keys' dV sum to the queries' dO sum; rows of dS sum to zero (Δ is the
+    # row sum of P ∘ dP), so the keys' dK sum to zero.  With these inputs the
+    # early key blocks hold most of every causal row's mass: one of them left
+    # out or given to the wrong head moves the dV sum far past the tolerance
+    # (the last few blocks hold too little mass for this check to see).
+    import torch
+    import exact_attention_44_gb300 as fa
+    Z, Hq, Hkv, N, D = 1, 32, 8, 32768, 128
+    g = torch.Generator(device="cuda").manual_seed(2024)
+    q, do = (torch.randn(Z, Hq, N, D, generator=g, device="cuda").to(torch.bfloat16) for _ in range(2))
+    k, v = (torch.randn(Z, Hkv, N, D, generator=g, device="cuda").to(torch.bfloat16) for _ in range(2))
+    o, lse = fa.fa_fwd(q, k, v, causal=True)
+    dq, dk, dv = fa.fa_bwd(q, k, v, o, lse, do, causal=True)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status()[0] == 0
+    grp = Hq // Hkv
+    for hk in range(Hkv):
+        want = do[0, hk * grp:(hk + 1) * grp].double().sum(dim=(0, 1))
+        got = dv[0, hk].double().sum(dim=0)
+        assert torch.isfinite(dq).all() and torch.isfinite(dk).all() and torch.isfinite(dv).all()
+        err = float((got - want).abs().max())
+        assert err <= 1e-2 * float(want.abs().max()), f"kv head {hk}: sum dV off by {err:.3e}"
+        ksum = dk[0, hk].double().sum(dim=0).abs()
+        kabs = dk[0, hk].double().abs().sum(dim=0)
+        assert float((ksum / kabs).max()) <= 1e-2, f"kv head {hk}: sum dK not ~0"
