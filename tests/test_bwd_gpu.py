@@ -218,6 +218,7 @@ def test_headline_size_gradient_invariants():
     # early key blocks hold most of every causal row's mass: one of them left
     # out or given to the wrong head moves the dV sum far past the tolerance
     # (the last few blocks hold too little mass for this check to see).
+    # Sampled rows of dQ are held against the oracle.
     import torch
     import exact_attention_44_gb300 as fa
     Z, Hq, Hkv, N, D = 1, 32, 8, 32768, 128
@@ -238,3 +239,19 @@ def test_headline_size_gradient_invariants():
         ksum = dk[0, hk].double().sum(dim=0).abs()
         kabs = dk[0, hk].double().abs().sum(dim=0)
         assert float((ksum / kabs).max()) <= 1e-2, f"kv head {hk}: sum dK not ~0"
+    # sampled dQ rows against the oracle: causal row i's dQ is the non-causal
+    # dQ of a one-row sequence whose keys are 0 .. i (the oracle's packed
+    # sequences), which it differentiates in O(i D)
+    def bits(t):
+        return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    scale = 1 / math.sqrt(D)
+    for hq, i in [(0, 0), (5, 127), (9, 12345), (31, N - 1)]:
+        hk = hq // grp
+        one = lambda t, rows: bits(t[0, hq if t.shape[1] == Hq else hk, rows].reshape(1, 1, -1, D))
+        ref = oracle.attention_bwd_ex(one(q, slice(i, i + 1)), one(k, slice(0, i + 1)), one(v, slice(0, i + 1)),
+                                      one(do, slice(i, i + 1)), "bf16", scale, False,
+                                      cu_q=np.array([0, 1], dtype=np.int32), cu_k=np.array([0, i + 1], dtype=np.int32))[0]
+        got = dq[0, hq, i].double().cpu().numpy()
+        want = ref[0, 0, 0]
+        err, mag = float(np.max(np.abs(got - want))), float(np.max(np.abs(want)))
+        assert err <= TOL_GRAD["bf16"] * max(mag, 1e-3), f"dQ row ({hq}, {i}): {err:.3e} vs {mag:.3e}"
