@@ -901,6 +901,13 @@ static fa_status bwd_impl(const void* q, const void* k, const void* v, const voi
     const int64_t seq_q = varlen ? std::max(1, Nq / std::max(1, Z)) : Nq;
     const int64_t seq_k = varlen ? std::max(1, Nkv / std::max(1, Z)) : Nkv;
     p.kv_head_group = causal_head_group(Z * Hkv, 1, (int64_t)p.group * seq_q * D * 4, info->l2_bytes, p.Tk, info->sms);
+    // D = 256, non-causal: groups of about one round of CTAs, so every key
+    // block of a head runs at once and its Q and dO (re-read by both passes
+    // of every step) stay in L2.  Measured on GB300 (Z8 H16 N2048): +6.0 %;
+    // causal -10 % (its heaviest-first order needs the larger groups), D = 64
+    // -2 %, D = 128 level.
+    if (!causal && D == 256)
+        p.kv_head_group = (int)std::min<int64_t>(Z * Hkv, std::max<int64_t>(1, cdiv(info->sms, p.Tk)));
     p.q_head_group = causal_head_group(Z * Hq, p.group, seq_k * D * 4, info->l2_bytes, p.Tq, info->sms);
     p.scale = scale;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
